@@ -1,0 +1,127 @@
+"""ctypes front end of the float64 CPU oracle (``oracle.c``).
+
+TEST INFRASTRUCTURE ONLY: the tests, the smoke check and the benchmark's
+CPU-baseline / reference leg use this package to check and to time the CUDA
+library.  The library never imports it, and it imports nothing from the
+library.  ``build()`` compiles ``oracle.c`` with gcc (plain -O2, no fast-math,
+no FP contraction, OpenMP only across independent channels).
+
+Every function here takes and returns float64 numpy arrays in the layouts that
+``oracle.c`` documents; callers widen bf16/fp32 inputs exactly before calling.
+Every oracle function is pinned by ``tests/test_oracle_pins.py`` (brute-force
+sums, the time-invariant convolution closed form, a log-depth associative
+scan, limiting cases and invariances); none is "parity unpinned".
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+from typing import Optional
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+SRC = os.path.join(_HERE, "oracle.c")
+LIB = os.path.join(_HERE, "liboracle.so")
+CFLAGS = ["-O2", "-fPIC", "-shared", "-std=c11", "-fopenmp", "-ffp-contract=off",
+          "-fno-fast-math"]
+
+_lib = None
+
+
+def build(src: str = SRC, out: str = LIB, extra: Optional[list] = None) -> str:
+    """Compile the oracle into a shared library and return its path."""
+    cmd = ["gcc", *CFLAGS, *(extra or []), "-o", out, src, "-lm"]
+    subprocess.run(cmd, check=True)
+    return out
+
+
+def load(path: Optional[str] = None):
+    """Load (building first if needed) the oracle library."""
+    global _lib
+    if path is None and _lib is not None:
+        return _lib
+    p = path or LIB
+    if path is None and (not os.path.exists(p) or os.path.getmtime(p) < os.path.getmtime(SRC)):
+        build()
+    lib = ctypes.CDLL(p)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.oracle_scan.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp] + [ctypes.c_int] * 4
+    lib.oracle_scan.restype = ctypes.c_int
+    lib.oracle_step.argtypes = [dp] * 9 + [ctypes.c_int, dp] + [ctypes.c_int] * 3
+    lib.oracle_step.restype = ctypes.c_int
+    lib.oracle_softplus.argtypes = [ctypes.c_double]
+    lib.oracle_softplus.restype = ctypes.c_double
+    lib.oracle_silu.argtypes = [ctypes.c_double]
+    lib.oracle_silu.restype = ctypes.c_double
+    lib.oracle_set_threads.argtypes = [ctypes.c_int]
+    lib.oracle_max_threads.restype = ctypes.c_int
+    if path is None:
+        _lib = lib
+    return lib
+
+
+def _p(a):
+    if a is None:
+        return None
+    assert a.dtype == np.float64 and a.flags["C_CONTIGUOUS"], "oracle takes C-contiguous float64"
+    return a.ctypes.data_as(ctypes.POINTER(ctypes.c_double))
+
+
+def _f64(a):
+    return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
+
+
+def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
+         want_last_state=True, lib=None):
+    """Full-sequence selective scan.
+
+    u, delta, z: (batch, L, dim); B, C: (batch, N, L); A: (dim, N);
+    D, delta_bias: (dim,).  Returns (out (batch, L, dim), last_state
+    (batch, dim, N) or None), float64.
+    """
+    lib = lib or load()
+    u, delta, A, B, C, D, z, delta_bias = map(_f64, (u, delta, A, B, C, D, z, delta_bias))
+    bt, L, dim = u.shape
+    N = A.shape[1]
+    assert delta.shape == u.shape and A.shape == (dim, N)
+    assert B.shape == (bt, N, L) and C.shape == (bt, N, L)
+    out = np.empty_like(u)
+    last = np.empty((bt, dim, N)) if want_last_state else None
+    rc = lib.oracle_scan(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                         int(bool(softplus)), _p(out), _p(last), bt, dim, L, N)
+    if rc != 0:
+        raise ValueError(f"oracle_scan rejected its arguments (code {rc})")
+    return out, last
+
+
+def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, lib=None):
+    """One recurrent update.  ``state`` (batch, dim, N) float64 is updated in
+    place; x, dt, z: (batch, dim); B, C: (batch, N).  Returns out (batch, dim)."""
+    lib = lib or load()
+    assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
+    x, dt, A, B, C, D, z, dt_bias = map(_f64, (x, dt, A, B, C, D, z, dt_bias))
+    bt, dim, N = state.shape
+    out = np.empty((bt, dim))
+    rc = lib.oracle_step(_p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z),
+                         _p(dt_bias), int(bool(dt_softplus)), _p(out), bt, dim, N)
+    if rc != 0:
+        raise ValueError(f"oracle_step rejected its arguments (code {rc})")
+    return out
+
+
+def softplus(x: float, lib=None) -> float:
+    return (lib or load()).oracle_softplus(float(x))
+
+
+def silu(x: float, lib=None) -> float:
+    return (lib or load()).oracle_silu(float(x))
+
+
+def set_threads(n: int, lib=None) -> None:
+    (lib or load()).oracle_set_threads(int(n))
+
+
+def max_threads(lib=None) -> int:
+    return (lib or load()).oracle_max_threads()

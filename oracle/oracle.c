@@ -1,0 +1,169 @@
+/*
+ * oracle.c -- plain, slow, sequential float64 reference of the Mamba selective
+ * scan and of its single-token recurrent update.
+ *
+ * TEST INFRASTRUCTURE ONLY.  This file is the checker the CUDA library is
+ * measured against.  Only the test suite, the smoke check and the benchmark's
+ * CPU-baseline leg may load it; the library itself never does.  It shares no
+ * code, header, table or helper with the CUDA path.
+ *
+ * What it computes, and where that comes from:
+ *
+ *  - "Mamba: Selective State Space Models" (eeshsaxena/mamba-ssm-implementation
+ *    README), section "Mathematical Foundation / State Space Model": the
+ *    continuous model h'(t) = A h(t) + B x(t), y(t) = C h(t) + D x(t).
+ *  - same page, "Selective Mechanism": B, C and the timestep Delta depend on the
+ *    input; Delta = tau_Delta(Parameter + Linear_Delta(x)).  Here the already
+ *    projected Delta_raw is an input, "Parameter" is delta_bias, and tau_Delta
+ *    is softplus (applied when softplus_flag is set).
+ *  - same page, "Architecture": Delta drives a discretisation step; the page
+ *    does not print the formula.  The reading adopted here is zero-order hold
+ *    for A and the Euler rule for B:  dA = exp(Delta*A),  dB*u = Delta*B*u.
+ *  - same page, "Efficient Scan", item 2 (sequential scan for inference): the
+ *    recurrence h_t = dA_t * h_{t-1} + dB_t * u_t run one step at a time with a
+ *    constant-size state, starting from h = 0.
+ *  - readout y_t = C_t . h_t + D * u_t (the y equation above, with h_t taken
+ *    after the step-t update), then the Mamba block's gate
+ *    ("Features": "Mamba block with gated residuals"): y_t *= silu(z_t).
+ *
+ * Everything is float64; every input arrives already widened exactly from its
+ * stored type.  No exp2, no log2(e) prescale, no chunking, no reordering: loop
+ * order is batch -> channel -> time -> state, exactly the definition.
+ *
+ * Layouts (row-major):
+ *   u, delta, z, out : [batch][seqlen][dim]
+ *   B, C             : [batch][dstate][seqlen]
+ *   A                : [dim][dstate]
+ *   D, delta_bias    : [dim]
+ *   last_state       : [batch][dim][dstate]
+ * Decode step:
+ *   state            : [batch][dim][dstate]  (updated in place)
+ *   x, dt, z, out    : [batch][dim]
+ *   B, C             : [batch][dstate]
+ */
+#include <math.h>
+#include <stddef.h>
+#include <stdint.h>
+#include <stdlib.h>
+
+#ifdef _OPENMP
+#include <omp.h>
+#endif
+
+#define ORACLE_MAX_DSTATE 256
+
+/* softplus(x) = log(1 + e^x), written in the overflow-free form
+ * max(x, 0) + log1p(exp(-|x|)). */
+static double softplus(double x) {
+    return (x > 0.0 ? x : 0.0) + log1p(exp(-fabs(x)));
+}
+
+/* silu(z) = z * sigmoid(z) = z / (1 + e^-z). */
+static double silu(double zv) {
+    return zv / (1.0 + exp(-zv));
+}
+
+/* Delta for one (time, channel): optional bias add, optional softplus. */
+static double timestep(double delta_raw, const double* delta_bias, int d,
+                       int softplus_flag) {
+    double x = delta_raw + (delta_bias ? delta_bias[d] : 0.0);
+    return softplus_flag ? softplus(x) : x;
+}
+
+/* One recurrence step for one (batch, channel): updates h[0..N) in place and
+ * returns the gated output.  Bv / Cv give B and C of this step, read with a
+ * stride so the same step serves the scan layout ([N][L]) and the decode
+ * layout ([N]). */
+static double one_step(double* h, const double* Arow, int N,
+                       const double* Bv, const double* Cv, ptrdiff_t bc_stride,
+                       double uv, double dlt, double Dd, const double* zp) {
+    double y = 0.0;
+    for (int n = 0; n < N; ++n) {
+        double dA = exp(dlt * Arow[n]);                 /* zero-order hold */
+        double dBu = (dlt * Bv[n * bc_stride]) * uv;    /* Euler:  (Delta B) u */
+        h[n] = dA * h[n] + dBu;
+        y += Cv[n * bc_stride] * h[n];
+    }
+    y += Dd * uv;
+    if (zp) y *= silu(*zp);
+    return y;
+}
+
+static int check_dims(int batch, int dim, int seqlen, int dstate) {
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return 1;
+    if (dstate > ORACLE_MAX_DSTATE) return 1;
+    return 0;
+}
+
+/* Full-sequence scan of every (batch, channel), independently.  The OpenMP
+ * loop only distributes whole independent channels across threads; each
+ * channel's arithmetic is the sequential definition above. */
+int oracle_scan(const double* u, const double* delta, const double* A,
+                const double* B, const double* C, const double* D,
+                const double* z, const double* delta_bias, int softplus_flag,
+                double* out, double* last_state,
+                int batch, int dim, int seqlen, int dstate) {
+    if (!u || !delta || !A || !B || !C || !out) return 1;
+    if (check_dims(batch, dim, seqlen, dstate)) return 2;
+    const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
+    const long long total = (long long)batch * dim;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long bd = 0; bd < total; ++bd) {
+        const ptrdiff_t b = bd / Dm, d = bd % Dm;
+        double h[ORACLE_MAX_DSTATE];
+        for (ptrdiff_t n = 0; n < N; ++n) h[n] = 0.0;
+        const double* Bb = B + b * N * L;
+        const double* Cb = C + b * N * L;
+        const double Dd = D ? D[d] : 0.0;
+        for (ptrdiff_t t = 0; t < L; ++t) {
+            const ptrdiff_t i = (b * L + t) * Dm + d;
+            const double dlt = timestep(delta[i], delta_bias, (int)d, softplus_flag);
+            out[i] = one_step(h, A + d * N, (int)N, Bb + t, Cb + t, L,
+                              u[i], dlt, Dd, z ? z + i : NULL);
+        }
+        if (last_state)
+            for (ptrdiff_t n = 0; n < N; ++n) last_state[(b * Dm + d) * N + n] = h[n];
+    }
+    return 0;
+}
+
+/* Single-token recurrent update ("Efficient Scan", item 2): the same step as
+ * the scan's body, applied once to a caller-held state. */
+int oracle_step(double* state, const double* x, const double* dt,
+                const double* A, const double* B, const double* C,
+                const double* D, const double* z, const double* dt_bias,
+                int dt_softplus, double* out, int batch, int dim, int dstate) {
+    if (!state || !x || !dt || !A || !B || !C || !out) return 1;
+    if (check_dims(batch, dim, 1, dstate)) return 2;
+    const ptrdiff_t Dm = dim, N = dstate;
+    const long long total = (long long)batch * dim;
+#pragma omp parallel for schedule(static)
+    for (long long bd = 0; bd < total; ++bd) {
+        const ptrdiff_t b = bd / Dm, d = bd % Dm;
+        const ptrdiff_t i = b * Dm + d;
+        const double dlt = timestep(dt[i], dt_bias, (int)d, dt_softplus);
+        out[i] = one_step(state + i * N, A + d * N, (int)N, B + b * N, C + b * N, 1,
+                          x[i], dlt, D ? D[d] : 0.0, z ? z + i : NULL);
+    }
+    return 0;
+}
+
+/* Scalar helpers exposed so the pins can test them against closed forms. */
+double oracle_softplus(double x) { return softplus(x); }
+double oracle_silu(double x) { return silu(x); }
+
+void oracle_set_threads(int n) {
+#ifdef _OPENMP
+    if (n > 0) omp_set_num_threads(n);
+#else
+    (void)n;
+#endif
+}
+
+int oracle_max_threads(void) {
+#ifdef _OPENMP
+    return omp_get_max_threads();
+#else
+    return 1;
+#endif
+}

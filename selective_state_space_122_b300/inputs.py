@@ -1,0 +1,181 @@
+"""Seeded synthetic inputs for the selective scan and the decode step.
+
+This module is shared by the CUDA path's tests/bench and by the CPU oracle's
+callers. It draws random numbers and lays them out; it performs none of the
+scan's arithmetic.
+
+Recipe (one numpy ``Generator(PCG64(seed))`` per workload):
+
+* draw order: u, delta_raw, z, B, C, dt (-> delta_bias); for the decode
+  workload additionally state0, then per-step tokens x, dt, z, B, C;
+* every activation is drawn in float32 from N(0, 1) and, for bf16 workloads,
+  rounded to bfloat16 with round-to-nearest-even on the host, so the GPU and
+  the oracle see bit-identical values;
+* A[d, n] = -(n + 1) for every channel (the S4D-real initialisation the Mamba
+  block uses; a random negative A is available for robustness cases);
+* D = 1 for every channel;
+* delta_bias = softplus^-1(dt) with dt log-uniform in [1e-3, 0.1] per
+  channel: the "targeted range" initialisation of the Delta projection bias
+  named in the state-spaces/mamba docs ("Troubleshoot initialization issues");
+* decode state0 ~ N(0, 0.1) (standard deviation 0.1), fp32.
+
+Layouts follow the (batch, length, dim) convention of the Mamba block:
+u, delta, z, out are (batch, L, D) channel-contiguous; B and C are
+(batch, N, L) time-contiguous; A is (D, N); D and delta_bias are (D,);
+states are (batch, D, N).
+"""
+from __future__ import annotations
+
+import dataclasses
+from typing import Optional
+
+import numpy as np
+
+F32 = "f32"
+BF16 = "bf16"
+
+
+@dataclasses.dataclass(frozen=True)
+class ScanShape:
+    name: str
+    batch: int
+    dim: int
+    seqlen: int
+    dstate: int
+    dtype: str
+    want_last_state: bool = True
+
+
+# The five workloads: a tiny fp32 case, a Mamba-130M-shaped layer
+# (d_model 768, expand 2), a mid-size prefill, a 128K-token long sequence at
+# d_model 2560, and a batched decode step.
+TINY_F32 = ScanShape("tiny-f32 1x16x64 N4", 1, 16, 64, 4, F32)
+LAYER_130M = ScanShape("mamba130m-layer 4x1536x1024 N16", 4, 1536, 1024, 16, BF16)
+PREFILL_MID = ScanShape("prefill 8x2048x2048 N16", 8, 2048, 2048, 16, BF16)
+LONG_SEQ = ScanShape("long-seq 1x5120x131072 N16", 1, 5120, 131072, 16, BF16)
+
+
+@dataclasses.dataclass(frozen=True)
+class DecodeShape:
+    name: str
+    batch: int
+    dim: int
+    dstate: int
+    dtype: str
+
+
+DECODE_256 = DecodeShape("decode 256x5120 N16", 256, 5120, 16, BF16)
+
+SCAN_WORKLOADS = {0: TINY_F32, 1: LAYER_130M, 2: PREFILL_MID, 3: LONG_SEQ}
+
+
+def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    x = np.ascontiguousarray(x, dtype=np.float32)
+    w = x.view(np.uint32).astype(np.uint64)
+    bias = ((w >> 16) & 1) + 0x7FFF
+    return ((w + bias) >> 16).astype(np.uint16)
+
+
+def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
+    """Exact widening of bfloat16 bit patterns to float64."""
+    w = b.astype(np.uint32) << 16
+    return w.view(np.float32).astype(np.float64)
+
+
+def _normal(rng: np.random.Generator, shape, sigma: float = 1.0) -> np.ndarray:
+    out = rng.standard_normal(size=shape, dtype=np.float32)
+    if sigma != 1.0:
+        out *= np.float32(sigma)
+    return out
+
+
+def _activation(rng, shape, dtype):
+    a = _normal(rng, shape)
+    return round_to_bf16_bits(a) if dtype == BF16 else a
+
+
+def _delta_bias(rng, dim, dt_min=1e-3, dt_max=0.1):
+    lo, hi = np.log(dt_min), np.log(dt_max)
+    dt = np.exp(rng.uniform(lo, hi, size=dim))            # float64
+    # softplus^-1(dt) = log(exp(dt) - 1) = dt + log(-expm1(-dt)), in float64
+    inv = dt + np.log(-np.expm1(-dt))
+    return inv.astype(np.float32)
+
+
+def a_s4d_real(dim: int, dstate: int) -> np.ndarray:
+    """A[d, n] = -(n + 1), float32, shape (dim, dstate)."""
+    return np.tile(-np.arange(1, dstate + 1, dtype=np.float32), (dim, 1))
+
+
+def a_random(rng: np.random.Generator, dim: int, dstate: int) -> np.ndarray:
+    """A = -exp(N(0, 1)): unstructured negative real A (robustness cases)."""
+    return (-np.exp(rng.standard_normal((dim, dstate)))).astype(np.float32)
+
+
+@dataclasses.dataclass
+class ScanInputs:
+    shape: ScanShape
+    u: np.ndarray          # (batch, L, D)   f32 or bf16 bits (uint16)
+    delta: np.ndarray      # (batch, L, D)
+    z: Optional[np.ndarray]
+    B: np.ndarray          # (batch, N, L)
+    C: np.ndarray          # (batch, N, L)
+    A: np.ndarray          # (D, N) f32
+    D: Optional[np.ndarray]
+    delta_bias: Optional[np.ndarray]
+    softplus: bool = True
+
+    def as_f64(self) -> dict:
+        """Exact float64 copies of every input (for the oracle)."""
+        w = bf16_bits_to_f64 if self.shape.dtype == BF16 else (lambda a: a.astype(np.float64))
+        f = lambda a: None if a is None else a.astype(np.float64)
+        return dict(u=w(self.u), delta=w(self.delta), z=None if self.z is None else w(self.z),
+                    B=w(self.B), C=w(self.C), A=f(self.A), D=f(self.D),
+                    delta_bias=f(self.delta_bias), softplus=self.softplus)
+
+
+def make_scan_inputs(shape: ScanShape, seed: int, *, random_a: bool = False,
+                     with_z: bool = True, with_d: bool = True,
+                     with_bias: bool = True, softplus: bool = True) -> ScanInputs:
+    """Seeded inputs for a full-sequence scan of ``shape``."""
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bt, L, D, N, dt = shape.batch, shape.seqlen, shape.dim, shape.dstate, shape.dtype
+    u = _activation(rng, (bt, L, D), dt)
+    delta = _activation(rng, (bt, L, D), dt)
+    z = _activation(rng, (bt, L, D), dt)
+    B = _activation(rng, (bt, N, L), dt)
+    C = _activation(rng, (bt, N, L), dt)
+    bias = _delta_bias(rng, D)
+    A = a_random(rng, D, N) if random_a else a_s4d_real(D, N)
+    return ScanInputs(shape, u, delta, z if with_z else None, B, C, A,
+                      np.ones(D, np.float32) if with_d else None,
+                      bias if with_bias else None, softplus)
+
+
+@dataclasses.dataclass
+class DecodeInputs:
+    shape: DecodeShape
+    state0: np.ndarray     # (batch, D, N) f32
+    A: np.ndarray
+    D: np.ndarray
+    dt_bias: np.ndarray
+    rng: np.random.Generator
+
+    def token(self):
+        """Next token: x, dt, z (batch, D) and B, C (batch, N) in the workload dtype."""
+        s = self.shape
+        x = _activation(self.rng, (s.batch, s.dim), s.dtype)
+        dt = _activation(self.rng, (s.batch, s.dim), s.dtype)
+        z = _activation(self.rng, (s.batch, s.dim), s.dtype)
+        B = _activation(self.rng, (s.batch, s.dstate), s.dtype)
+        C = _activation(self.rng, (s.batch, s.dstate), s.dtype)
+        return x, dt, z, B, C
+
+
+def make_decode_inputs(shape: DecodeShape, seed: int) -> DecodeInputs:
+    rng = np.random.Generator(np.random.PCG64(seed))
+    bias = _delta_bias(rng, shape.dim)
+    state0 = _normal(rng, (shape.batch, shape.dim, shape.dstate), sigma=0.1)
+    return DecodeInputs(shape, state0, a_s4d_real(shape.dim, shape.dstate),
+                        np.ones(shape.dim, np.float32), bias, rng)
