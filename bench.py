@@ -1,0 +1,476 @@
+"""Benchmark of the selective-scan hot path on one (or N replica) B300s.
+
+One step = one full-sequence selective scan over the long-sequence workload
+(batch 1, d_inner 5120, L 131072, d_state 16, bf16 activations) followed by
+one recurrent decode step over the batched decode workload (batch 256,
+d_inner 5120, d_state 16, fp32 state updated in place).  Both run through the
+library's C ABI on inputs resident in HBM; the scan's 5.4 GB of traffic per
+step is far larger than the 126 MB L2, so no explicit flush is needed between
+steps and the decode state (84 MB) is evicted by the scan that precedes it.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
+
+Prints ONE JSON line (rank 0).  Under torchrun every rank runs an independent
+replica (the path has no data exchange); time is the max over ranks.
+
+``--impl reference`` times the float64 CPU oracle on the host cores on a
+bounded sample of the same workload (rank 0 only).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+from selective_state_space_122_b300 import inputs  # noqa: E402
+
+METRIC = "selective-scan elements (B·D·L·N)/s and achieved HBM GB/s vs roofline, 1 B300"
+SCAN = inputs.LONG_SEQ
+DECODE = inputs.DECODE_256
+# Special-function unit rates of a B300 SM, per clock (measured with a
+# dependent-chain microbenchmark: ex2 ~30/clk/SM, lg2/rcp/tanh ~15/clk/SM):
+EX2_PER_SM_PER_CLK = 32
+HALF_RATE_SFU_COST = 2            # lg2 and rcp occupy the unit twice as long as ex2
+# Transcendental work of the method per (b, t, d), in ex2-equivalents:
+#   N exps for exp(Delta A), softplus = exp + log, silu = exp + reciprocal.
+def sfu_ex2_equiv_per_td(n):
+    return (n + 2) + 2 * HALF_RATE_SFU_COST
+FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "sm_max_mhz": 2032.0, "source": "fallback"}
+
+
+# ---------------------------------------------------------------- accounting
+
+def scan_elements(s=SCAN):
+    return s.batch * s.dim * s.seqlen * s.dstate
+
+
+def scan_bytes(s=SCAN, es=2):
+    """Algorithmic HBM bytes of one scan: u, delta, z read and out written once
+    per (b, t, d); B and C once; A, D, delta_bias once; final state written."""
+    btd = s.batch * s.seqlen * s.dim
+    return (4 * btd * es + 2 * s.batch * s.dstate * s.seqlen * es
+            + s.dim * s.dstate * 4 + 2 * s.dim * 4 + s.batch * s.dim * s.dstate * 4)
+
+
+def scan_sfu_ops(s=SCAN):
+    """SFU work of one scan in ex2-equivalents (half-rate ops count twice)."""
+    return s.batch * s.seqlen * s.dim * sfu_ex2_equiv_per_td(s.dstate)
+
+
+def decode_elements(s=DECODE):
+    return s.batch * s.dim * s.dstate
+
+
+def decode_bytes(s=DECODE, es=2):
+    """State read + written (fp32), x, dt, z read and out written, B, C, A, D, bias."""
+    return (2 * s.batch * s.dim * s.dstate * 4 + 4 * s.batch * s.dim * es
+            + 2 * s.batch * s.dstate * es + s.dim * s.dstate * 4 + 2 * s.dim * 4)
+
+
+def load_peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "sm_max_mhz": float(d.get("sm_max_mhz", 2032.0)),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS)
+
+
+# ---------------------------------------------------------------- distributed
+
+def dist_env():
+    return (int(os.environ.get("RANK", "0")), int(os.environ.get("WORLD_SIZE", "1")),
+            int(os.environ.get("LOCAL_RANK", "0")))
+
+
+def dist_init(world, backend):
+    import torch.distributed as dist
+    if world > 1 and not dist.is_initialized():
+        dist.init_process_group(backend=backend)
+    return dist
+
+
+def max_over_ranks(value, world, device=None):
+    """Max of a float over all ranks (identity when world == 1)."""
+    if world <= 1:
+        return float(value)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(value)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+# ---------------------------------------------------------------- clocks
+
+class ClockSampler:
+    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+             "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+             "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index):
+        self.gpu = gpu_index
+        self.proc = None
+        self.path = None
+
+    def __enter__(self):
+        out_dir = os.path.join(ROOT, "gpurun_out")
+        os.makedirs(out_dir, exist_ok=True)
+        self.path = os.path.join(out_dir, f"clocks_rank{self.gpu}.csv")
+        try:
+            self.f = open(self.path, "w")
+            self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
+                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                         stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except OSError:
+            self.proc = None
+        return self
+
+    def __exit__(self, *exc):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+            self.f.close()
+
+    def summary(self):
+        if self.proc is None or not self.path or not os.path.exists(self.path):
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        sm, smax, reasons, power = [], [], set(), []
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in open(self.path):
+            f = [x.strip() for x in line.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+                power.append(float(f[3]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
+                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+
+
+# ---------------------------------------------------------------- our arm
+
+def make_workload(device):
+    """Seeded inputs generated on the host and made resident on the device."""
+    import torch
+
+    def up(a):
+        if a.dtype == np.uint16:
+            return torch.from_numpy(a.view(np.int16)).view(torch.bfloat16).to(device)
+        return torch.from_numpy(a).to(device)
+
+    si = inputs.make_scan_inputs(SCAN, 3)
+    di = inputs.make_decode_inputs(DECODE, 4)
+    x, dt, z, B, C = di.token()
+    w = {
+        "scan_host": si,
+        "scan": {k: up(getattr(si, k)) for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias")},
+        "dec": {"state": up(di.state0), "x": up(x), "dt": up(dt), "z": up(z), "B": up(B), "C": up(C),
+                "A": up(di.A), "D": up(di.D), "dt_bias": up(di.dt_bias)},
+        "dec_host": (di, x, dt, z, B, C),
+    }
+    s = w["scan"]
+    w["scan_out"] = torch.empty_like(s["u"])
+    w["scan_last"] = torch.empty((SCAN.batch, SCAN.dim, SCAN.dstate), dtype=torch.float32, device=device)
+    w["dec_out"] = torch.empty_like(w["dec"]["x"])
+    return w
+
+
+def run_step(w, ev=None):
+    """One step of the hot path: the long-sequence scan, then one decode step."""
+    from selective_state_space_122_b300 import ssm_scan_fwd, ssm_state_update
+    s, d = w["scan"], w["dec"]
+    if ev is not None:
+        ev[0].record()
+    ssm_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"], s["delta_bias"], True,
+                 out=w["scan_out"], last_state=w["scan_last"])
+    if ev is not None:
+        ev[1].record()
+    ssm_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
+                     True, out=w["dec_out"])
+    if ev is not None:
+        ev[2].record()
+
+
+def run_e2e(w, steps, device):
+    """The same step through the public API from pinned HOST buffers: copy
+    every input of the step host->device, run, copy both outputs back."""
+    import torch
+    from selective_state_space_122_b300 import ssm_scan_fwd, ssm_state_update
+    s, d = w["scan"], w["dec"]
+    hs = {k: v.cpu().pin_memory() for k, v in s.items()}
+    hd = {k: v.cpu().pin_memory() for k, v in d.items()}
+    out_h = torch.empty(w["scan_out"].shape, dtype=w["scan_out"].dtype).pin_memory()
+    last_h = torch.empty(w["scan_last"].shape, dtype=torch.float32).pin_memory()
+    dec_out_h = torch.empty(w["dec_out"].shape, dtype=w["dec_out"].dtype).pin_memory()
+    dec_state_h = torch.empty(d["state"].shape, dtype=torch.float32).pin_memory()
+    ds = {k: torch.empty_like(v) for k, v in s.items()}
+    dd = {k: torch.empty_like(v) for k, v in d.items()}
+    h2d = sum(v.numel() * v.element_size() for v in hs.values()) + \
+        sum(v.numel() * v.element_size() for v in hd.values())
+    d2h = (out_h.numel() * out_h.element_size() + last_h.numel() * 4
+           + dec_out_h.numel() * dec_out_h.element_size() + dec_state_h.numel() * 4)
+
+    def one():
+        for k in ds:
+            ds[k].copy_(hs[k], non_blocking=True)
+        for k in dd:
+            dd[k].copy_(hd[k], non_blocking=True)
+        o, last = ssm_scan_fwd(ds["u"], ds["delta"], ds["A"], ds["B"], ds["C"], ds["D"], ds["z"],
+                               ds["delta_bias"], True, out=w["scan_out"], last_state=w["scan_last"])
+        y = ssm_state_update(dd["state"], dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
+                             dd["dt_bias"], True, out=w["dec_out"])
+        out_h.copy_(o, non_blocking=True)
+        last_h.copy_(last, non_blocking=True)
+        dec_out_h.copy_(y, non_blocking=True)
+        dec_state_h.copy_(dd["state"], non_blocking=True)
+
+    one()
+    torch.cuda.synchronize()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    e0.record()
+    for _ in range(steps):
+        one()
+    e1.record()
+    torch.cuda.synchronize()
+    ms = e0.elapsed_time(e1) / steps
+    return ms, h2d, d2h
+
+
+def cpu_baseline_sample(si, target_s=12.0, max_channels=None):
+    """Time the float64 oracle (as it stands) on a bounded channel sample of the
+    long-sequence scan ``si``, all host cores.  Returns a dict for the JSON line."""
+    import oracle
+    threads = oracle.max_threads()
+
+    def run(ch):
+        g = si.channels(np.arange(ch)).as_f64()
+        t0 = time.perf_counter()
+        oracle.scan(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"], True)
+        return time.perf_counter() - t0
+
+    ch = max(threads, 8)
+    dt = run(ch)
+    want = int(ch * target_s / max(dt, 1e-3))
+    want = max(ch, min(want, max_channels or SCAN.dim, SCAN.dim))
+    want = max(threads, (want // threads) * threads) if want >= threads else want
+    dt = run(want)
+    elems = want * SCAN.seqlen * SCAN.dstate
+    return {"value": elems / dt, "unit": "elements/s", "cores": threads, "kind": "oracle",
+            "sample": f"{want} of 5120 channels x {SCAN.seqlen} steps x {SCAN.dstate} states "
+                      f"(long-sequence scan), float64, {dt:.1f} s wall"}
+
+
+def bench_ours(args):
+    import torch
+    rank, world, local = dist_env()
+    torch.cuda.set_device(local)
+    device = torch.device("cuda", local)
+    dist_init(world, "nccl")
+    from selective_state_space_122_b300 import load_library
+    load_library()
+    w = make_workload(device)
+    torch.cuda.synchronize()
+
+    for _ in range(args.warmup):
+        run_step(w)
+    torch.cuda.synchronize()
+    barrier(world)
+
+    stream = torch.cuda.current_stream(device)
+    evs = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(args.steps)]
+    e_start, e_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    with ClockSampler(local) as clk:
+        barrier(world)
+        torch.cuda.synchronize()
+        e_start.record(stream)
+        for k in range(args.steps):
+            run_step(w, evs[k])
+        e_end.record(stream)
+        torch.cuda.synchronize()
+        barrier(world)
+    total_ms = e_start.elapsed_time(e_end)
+    scan_ms = [e[0].elapsed_time(e[1]) for e in evs]
+    dec_ms = [e[1].elapsed_time(e[2]) for e in evs]
+    total_ms = max_over_ranks(total_ms, world, device)
+    clocks = clk.summary()
+
+    e2e = None
+    if not args.no_e2e:
+        e2e_ms, h2d, d2h = run_e2e(w, args.e2e_steps, device)
+        e2e_ms = max_over_ranks(e2e_ms, world, device)
+        e2e = (e2e_ms, h2d, d2h)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        cpu = cpu_baseline_sample(w["scan_host"], args.cpu_seconds)
+
+    if rank != 0:
+        barrier(world)
+        return None
+
+    peaks = load_peaks()
+    sms = torch.cuda.get_device_properties(device).multi_processor_count
+    ms_step = total_ms / args.steps
+    elems = (scan_elements() + decode_elements()) * world
+    scan_avg = statistics.mean(scan_ms)
+    dec_avg = statistics.mean(dec_ms)
+    sfu_peak = sms * EX2_PER_SM_PER_CLK * peaks["sm_max_mhz"] * 1e6      # ex2-equivalents/s
+    sfu_ach = scan_sfu_ops() / (scan_avg * 1e-3)
+    hbm_ach = scan_bytes() / (scan_avg * 1e-3) / 1e9
+    t_roof_ms = max(scan_bytes() / (peaks["hbm_gbs"] * 1e9), scan_sfu_ops() / sfu_peak) * 1e3
+    line = {
+        "metric": METRIC,
+        "value": elems / (ms_step * 1e-3),
+        "unit": "elements/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "f32",
+        "data": "synthetic",
+        "config": {
+            "workload": ("long-sequence scan 1x5120x131072 d_state 16 (bf16 u/delta/z/B/C, f32 A/D/bias, "
+                         "final state) + one decode step 256x5120 d_state 16 (f32 state in place)"),
+            "io_dtype": "bf16",
+            "l2": "no flush: each step streams 5.4 GB (> 126 MB L2) before the decode step",
+            "parallelism": f"replicas x{world}",
+            "sms": sms,
+        },
+        "scan_ms": scan_avg,
+        "decode_us": dec_avg * 1e3,
+        "roofline": {
+            "bound": "alu",
+            "unit": "G ex2-equiv/s",
+            "achieved": sfu_ach / 1e9,
+            "peak": sfu_peak / 1e9,
+            "frac": sfu_ach / sfu_peak,
+            "traffic": None,
+            "kernel": "scan_fwd_kernel (long-sequence scan)",
+            "peak_source": (f"derived: {sms} SMs x {EX2_PER_SM_PER_CLK} ex2/clk x "
+                            f"{peaks['sm_max_mhz']:.0f} MHz max SM clock; work counted in ex2-equivalents "
+                            f"({sfu_ex2_equiv_per_td(SCAN.dstate)} per (b,t,d): N+2 ex2, log and "
+                            f"reciprocal at half rate)"),
+            "sfu_ex2_equiv_per_launch": scan_sfu_ops(),
+            "hbm": {"achieved_gbs": hbm_ach, "peak_gbs": peaks["hbm_gbs"],
+                    "frac": hbm_ach / peaks["hbm_gbs"], "bytes_per_launch": scan_bytes(),
+                    "peak_source": peaks["source"]},
+            "t_roof_ms": t_roof_ms,
+            "frac_of_roofline_time": t_roof_ms / scan_avg,
+        },
+        "decode": {
+            "us_per_step": dec_avg * 1e3,
+            "bytes_per_step": decode_bytes(),
+            "achieved_gbs": decode_bytes() / (dec_avg * 1e-3) / 1e9,
+            "frac_hbm": decode_bytes() / (dec_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        },
+        "clocks": clocks,
+        "gpu_launches": 2 * args.steps,
+    }
+    if e2e is not None:
+        e2e_ms, h2d, d2h = e2e
+        line["e2e"] = {"value": elems / (e2e_ms * 1e-3), "unit": "elements/s",
+                       "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms,
+                       "steps": args.e2e_steps}
+    if cpu is not None:
+        line["cpu_baseline"] = cpu
+    print(json.dumps(line), flush=True)
+    barrier(world)
+    return line
+
+
+# ---------------------------------------------------------------- reference arm
+
+def bench_reference(args):
+    """The float64 oracle timed on the host cores: each step is a bounded
+    channel sample of the long-sequence scan."""
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return None
+    import oracle
+    oracle.load()
+    threads = oracle.max_threads()
+    ch = max(threads, args.ref_channels)
+    si = inputs.make_scan_inputs(SCAN, 3)
+    g = si.channels(np.arange(ch)).as_f64()
+    del si
+
+    def step():
+        oracle.scan(g["u"], g["delta"], g["A"], g["B"], g["C"], g["D"], g["z"], g["delta_bias"], True)
+
+    for _ in range(args.warmup):
+        step()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        step()
+    dt = (time.perf_counter() - t0) / args.steps
+    elems = ch * SCAN.seqlen * SCAN.dstate
+    value = elems / dt
+    line = {
+        "metric": METRIC, "impl": "reference", "value": value, "unit": "elements/s", "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": dt * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": ("long-sequence scan 1x5120x131072 d_state 16: float64 CPU oracle on a "
+                                f"{ch}-channel sample per step"), "parallelism": "host cores"},
+        "cpu_baseline": {"value": value, "unit": "elements/s", "cores": threads, "kind": "oracle",
+                         "sample": f"{ch} of 5120 channels x {SCAN.seqlen} steps x {SCAN.dstate} states"},
+        "e2e": {"value": value, "unit": "elements/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+    return line
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--e2e-steps", type=int, default=3)
+    ap.add_argument("--no-e2e", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0)
+    ap.add_argument("--ref-channels", type=int, default=64)
+    args = ap.parse_args(argv)
+    if args.impl == "ours":
+        args.warmup = max(args.warmup, 3)   # timing rule: at least 3 untimed warm-up steps
+    if args.impl == "reference":
+        return bench_reference(args)
+    return bench_ours(args)
+
+
+if __name__ == "__main__":
+    main()

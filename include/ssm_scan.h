@@ -1,0 +1,146 @@
+/*
+ * ssm_scan.h -- C ABI of the B300 (sm_103a) selective-scan library
+ * (libssmscan.so).
+ *
+ * Two operations, both from the Mamba selective state-space model:
+ *
+ *   ssm_scan_fwd      the full-sequence selective scan (prefill / training
+ *                     forward): "Efficient Scan" of the Mamba README
+ *                     ("Mamba: Selective State Space Models",
+ *                     eeshsaxena/mamba-ssm-implementation), together with the
+ *                     "Selective Mechanism" (input-dependent Delta, B, C) and the
+ *                     state-space equations of "Mathematical Foundation";
+ *   ssm_state_update  the single-token recurrent update used for
+ *                     constant-memory inference ("Efficient Scan", item 2:
+ *                     sequential scan, O(1) memory).
+ *
+ * Per (batch b, channel d) both compute, with h = 0 before the first step:
+ *
+ *   Delta_t = softplus(delta_raw[t] + delta_bias[d])     (softplus optional)
+ *   h_t[n]  = exp(Delta_t * A[d][n]) * h_{t-1}[n] + Delta_t * B[n][t] * u[t]
+ *   y_t     = sum_n C[n][t] * h_t[n] + D[d] * u[t]
+ *   out[t]  = y_t * silu(z[t])                           (gate optional)
+ *
+ * The pages name the discretisation step but print no formula; this library
+ * uses zero-order hold for A (exp(Delta A)) and the Euler rule for B
+ * (Delta B), and reads the gate of the "Mamba block with gated residuals" as
+ * a multiplication of y by silu(z).  Internally the state is float32 and
+ * exp is evaluated as exp2 of Delta * (A * log2 e).
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Memory: every array pointer is DEVICE memory owned by the caller.  The
+ *   library never allocates, frees, copies to the host or synchronises; it
+ *   only enqueues kernels on `stream` (a cudaStream_t; NULL = the legacy
+ *   default stream) and returns.  The caller must keep the buffers alive
+ *   until the work on `stream` has completed.
+ * - dtype: SSM_F32 or SSM_BF16 selects the element type of the activation
+ *   tensors (u/x, delta/dt, z, B, C, out).  A, D, delta_bias/dt_bias and the
+ *   SSM state are always float32.  bf16 outputs are rounded to nearest even.
+ * - Errors: every argument is validated on the host before anything is
+ *   enqueued; on any error nothing is written and nothing is launched.
+ *   A launch failure reported by the CUDA runtime returns SSM_ERR_LAUNCH.
+ *   Faults inside a kernel (e.g. a pointer to freed memory) surface as a CUDA
+ *   error at the caller's next synchronisation, as for any CUDA kernel.
+ * - Aliasing: `out` must not overlap any input array (SSM_ERR_ALIAS);
+ *   `last_state` must not overlap any input or `out`.  The decode `state` is
+ *   read and written in place by definition and must not overlap anything
+ *   else.
+ * - Alignment: every pointer must be aligned to its element size; the decode
+ *   state and A must be 16-byte aligned (SSM_ERR_ALIGN).
+ * - Supported d_state: 4, 8 or 16 (SSM_ERR_UNSUPPORTED otherwise).
+ * - Sizes are element counts; each must be > 0 (an empty tensor is
+ *   SSM_ERR_SHAPE), and batch*seqlen*dim must stay below 2^40.
+ */
+#ifndef SSM_SCAN_H
+#define SSM_SCAN_H
+
+#include <stdint.h>
+
+#if defined(__GNUC__)
+#define SSM_API __attribute__((visibility("default")))
+#else
+#define SSM_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum ssm_status {
+    SSM_OK = 0,
+    SSM_ERR_NULL = 1,         /* a required pointer is NULL                      */
+    SSM_ERR_SHAPE = 2,        /* a size is <= 0 or the problem is too large      */
+    SSM_ERR_ALIGN = 3,        /* a pointer is not aligned as documented          */
+    SSM_ERR_UNSUPPORTED = 4,  /* d_state not in {4, 8, 16}                        */
+    SSM_ERR_DTYPE = 5,        /* dtype is not SSM_F32 / SSM_BF16                 */
+    SSM_ERR_ALIAS = 6,        /* an output overlaps an input (or another output) */
+    SSM_ERR_LAUNCH = 7,       /* the CUDA runtime rejected a kernel launch       */
+    SSM_ERR_DEVICE = 8        /* no usable CUDA device / attribute query failed  */
+} ssm_status;
+
+typedef enum ssm_dtype {
+    SSM_F32 = 0,
+    SSM_BF16 = 1
+} ssm_dtype;
+
+/*
+ * ssm_scan_fwd -- full-sequence selective scan.
+ *
+ *   u           [batch][seqlen][dim]     dtype   input x of the SSM
+ *   delta       [batch][seqlen][dim]     dtype   Delta_raw (already projected)
+ *   A           [dim][dstate]            f32     state matrix (diagonal), < 0
+ *   B, C        [batch][dstate][seqlen]  dtype   input-dependent B_t, C_t
+ *                                                (shared by all channels)
+ *   D           [dim]                    f32     skip weight; NULL = 0
+ *   z           [batch][seqlen][dim]     dtype   gate input; NULL = no gate
+ *   delta_bias  [dim]                    f32     added to delta; NULL = 0
+ *   softplus_flag                                nonzero: Delta = softplus(.)
+ *   out         [batch][seqlen][dim]     dtype   written once (never read)
+ *   last_state  [batch][dim][dstate]     f32     h after the last step;
+ *                                                NULL = not written
+ *
+ * Returns SSM_OK once the work is enqueued on `stream`.
+ */
+SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A,
+                        const void* B, const void* C, const float* D,
+                        const void* z, const float* delta_bias, int softplus_flag,
+                        void* out, float* last_state,
+                        int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                        int dtype, void* stream);
+
+/*
+ * ssm_state_update -- one token of recurrent (constant-memory) inference.
+ *
+ *   state   [batch][dim][dstate]  f32    h_{t-1} on entry, h_t on return
+ *                                        (in place; 16-byte aligned)
+ *   x       [batch][dim]          dtype  this token's u
+ *   dt      [batch][dim]          dtype  this token's Delta_raw
+ *   A       [dim][dstate]         f32    (16-byte aligned)
+ *   B, C    [batch][dstate]       dtype  this token's B_t, C_t
+ *   D       [dim]                 f32    NULL = 0
+ *   z       [batch][dim]          dtype  NULL = no gate
+ *   dt_bias [dim]                 f32    NULL = 0
+ *   out     [batch][dim]          dtype  gated output y_t
+ *   dt_softplus                          nonzero: Delta = softplus(dt + dt_bias)
+ *
+ * Applied L times from a zero state to the tokens of a sequence, it computes
+ * the same recurrence as ssm_scan_fwd over that sequence.
+ */
+SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
+                            const float* A, const void* B, const void* C,
+                            const float* D, const void* z, const float* dt_bias,
+                            void* out, int64_t batch, int64_t dim, int64_t dstate,
+                            int dt_softplus, int dtype, void* stream);
+
+/* Static, human-readable name of a status code (never NULL). */
+SSM_API const char* ssm_status_string(int status);
+
+/* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
+SSM_API int ssm_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* SSM_SCAN_H */

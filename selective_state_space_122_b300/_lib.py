@@ -1,0 +1,147 @@
+"""ctypes binding of libssmscan.so (include/ssm_scan.h).
+
+Argument marshalling only: every step of the scan and of the decode update
+runs in the library's CUDA kernels.  PyTorch provides device memory and the
+current stream.  There is no CPU path: if the library is missing or no CUDA
+device is present the calls raise.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Tuple
+
+import torch
+
+PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(PKG, "libssmscan.so")
+
+SSM_F32 = 0
+SSM_BF16 = 1
+STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN",
+          4: "SSM_ERR_UNSUPPORTED", 5: "SSM_ERR_DTYPE", 6: "SSM_ERR_ALIAS",
+          7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE"}
+EXPORTS = ("ssm_scan_fwd", "ssm_state_update", "ssm_status_string", "ssm_version")
+
+_lib: Optional[ctypes.CDLL] = None
+
+
+class SSMError(RuntimeError):
+    def __init__(self, fn: str, code: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {code})")
+        self.code = code
+
+
+def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
+    """Load libssmscan.so and declare its signatures.  Raises if it is absent."""
+    global _lib
+    if _lib is not None and path == LIB_PATH:
+        return _lib
+    if not os.path.exists(path):
+        raise ImportError(f"{path} is missing: build it with "
+                          "`python -m selective_state_space_122_b300.build` (nvcc, sm_103a)")
+    lib = ctypes.CDLL(path)
+    vp, fp, i64, ci = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
+    lib.ssm_scan_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
+                                 i64, i64, i64, i64, ci, vp]
+    lib.ssm_scan_fwd.restype = ci
+    lib.ssm_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, vp,
+                                     i64, i64, i64, ci, ci, vp]
+    lib.ssm_state_update.restype = ci
+    lib.ssm_status_string.argtypes = [ci]
+    lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_version.argtypes = []
+    lib.ssm_version.restype = ci
+    if path == LIB_PATH:
+        _lib = lib
+    return lib
+
+
+def status_string(code: int) -> str:
+    return load_library().ssm_status_string(int(code)).decode()
+
+
+def _check(fn: str, code: int) -> None:
+    if code != 0:
+        raise SSMError(fn, code, status_string(code))
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.bfloat16:
+        return SSM_BF16
+    if t.dtype == torch.float32:
+        return SSM_F32
+    raise TypeError(f"activations must be float32 or bfloat16, got {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor], dtype=None, device=None) -> Optional[int]:
+    if t is None:
+        return None
+    if not t.is_cuda:
+        raise ValueError("every tensor must be on a CUDA device")
+    if device is not None and t.device != device:
+        raise ValueError("every tensor must be on the same CUDA device")
+    if not t.is_contiguous():
+        raise ValueError("every tensor must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"expected {dtype}, got {t.dtype}")
+    return t.data_ptr()
+
+
+def _stream(device: torch.device) -> int:
+    return torch.cuda.current_stream(device).cuda_stream
+
+
+def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
+                 C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
+                 delta_bias: Optional[torch.Tensor] = None, softplus: bool = True,
+                 out: Optional[torch.Tensor] = None, last_state: Optional[torch.Tensor] = None,
+                 return_last_state: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Selective scan over (batch, L, dim) activations; see ssm_scan.h.
+
+    B, C: (batch, dstate, L); A: (dim, dstate) f32; D, delta_bias: (dim,) f32.
+    Returns (out, last_state); last_state is (batch, dim, dstate) f32 when
+    requested (pass a buffer or set return_last_state).
+    """
+    lib = load_library()
+    dt = u.dtype
+    dev = u.device
+    bt, L, dim = u.shape
+    N = A.shape[1]
+    if out is None:
+        out = torch.empty_like(u)
+    if last_state is None and return_last_state:
+        last_state = torch.empty((bt, dim, N), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        code = lib.ssm_scan_fwd(_ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev),
+                                _ptr(B, dt, dev), _ptr(C, dt, dev), _ptr(D, torch.float32, dev),
+                                _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
+                                int(bool(softplus)), _ptr(out, dt, dev),
+                                _ptr(last_state, torch.float32, dev), bt, dim, L, N,
+                                _dtype_code(u), _stream(dev))
+    _check("ssm_scan_fwd", code)
+    return out, last_state
+
+
+def ssm_state_update(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,
+                     B: torch.Tensor, C: torch.Tensor, D: Optional[torch.Tensor] = None,
+                     z: Optional[torch.Tensor] = None, dt_bias: Optional[torch.Tensor] = None,
+                     dt_softplus: bool = True, out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step, in place on ``state`` (batch, dim, dstate) f32; see ssm_scan.h.
+
+    x, dt, z: (batch, dim); B, C: (batch, dstate).  Returns out (batch, dim).
+    """
+    lib = load_library()
+    ty = x.dtype
+    dev = x.device
+    bt, dim, N = state.shape
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(dev):
+        code = lib.ssm_state_update(_ptr(state, torch.float32, dev), _ptr(x, ty, dev), _ptr(dt, ty, dev),
+                                    _ptr(A, torch.float32, dev), _ptr(B, ty, dev), _ptr(C, ty, dev),
+                                    _ptr(D, torch.float32, dev), _ptr(z, ty, dev),
+                                    _ptr(dt_bias, torch.float32, dev), _ptr(out, ty, dev),
+                                    bt, dim, N, int(bool(dt_softplus)), _dtype_code(x), _stream(dev))
+    _check("ssm_state_update", code)
+    return out

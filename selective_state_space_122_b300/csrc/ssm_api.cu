@@ -1,0 +1,179 @@
+// ssm_api.cu -- the library's C ABI (declared in include/ssm_scan.h):
+// argument validation, work planning and kernel dispatch.  Nothing here
+// allocates, copies or synchronises; every check runs on the host before the
+// first launch, so a rejected call leaves every buffer untouched.
+#include <atomic>
+#include <cmath>
+#include <cstdint>
+#include <cstdlib>
+
+#include "../../include/ssm_scan.h"
+#include "ssm_internal.cuh"
+
+namespace {
+
+constexpr int64_t kMaxElems = int64_t(1) << 40;
+constexpr int kMaxDevices = 64;
+std::atomic<int> g_sm_count[kMaxDevices];
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+struct Span {
+    const void* p;
+    int64_t bytes;
+};
+
+bool overlap(Span a, Span b) {
+    if (!a.p || !b.p || a.bytes <= 0 || b.bytes <= 0) return false;
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(a.p), b0 = reinterpret_cast<uintptr_t>(b.p);
+    return a0 < b0 + (uintptr_t)b.bytes && b0 < a0 + (uintptr_t)a.bytes;
+}
+
+// Number of SMs of the current device (cached per device).
+ssm_status sm_count(int* out) {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return SSM_ERR_DEVICE;
+    if (dev < kMaxDevices) {
+        int c = g_sm_count[dev].load(std::memory_order_relaxed);
+        if (c > 0) {
+            *out = c;
+            return SSM_OK;
+        }
+    }
+    int c = 0;
+    if (cudaDeviceGetAttribute(&c, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || c <= 0)
+        return SSM_ERR_DEVICE;
+    if (dev < kMaxDevices) g_sm_count[dev].store(c, std::memory_order_relaxed);
+    *out = c;
+    return SSM_OK;
+}
+
+// Pick a compiled scan layout.  Every channel walks the sequence in order,
+// so a CTA's work is CW channels x L steps and its warps share it.  The
+// score is the work of the busiest SM scheduler (warps are the unit a
+// scheduler runs; a warp cannot migrate), times a per-layout cost factor:
+// split layouts pay ~2 extra FP32 operations per (t, state) and layouts with
+// few states per lane pay for the cross-lane y reduction.
+int plan_layout(int64_t batch, int64_t dim, int N, int sms) {
+    const int count = ssm::scan_layout_count(N);
+    const char* env = std::getenv("SSM_SCAN_LAYOUT");
+    if (env) {
+        const int l = std::atoi(env);
+        if (l >= 0 && l < count) return l;
+    }
+    const double schedulers = 4.0 * sms;
+    int best = 0;
+    double best_t = 1e300;
+    for (int l = 0; l < count; ++l) {
+        const ssm::ScanLayoutInfo li = ssm::scan_layout_info(N, l);
+        const int64_t ctas = batch * ((dim + li.CW - 1) / li.CW);
+        const double warps = double(ctas) * li.S;
+        const double per_warp = double(li.CW) / li.S;               // channels of work per warp
+        const double busiest = std::ceil(warps / schedulers) * per_warp;
+        double cost = (li.S * li.TL > 1) ? 1.15 : 1.0;
+        const int R = N / li.G;
+        cost *= 1.0 + 0.03 * (R > 1 ? R : 0);
+        const double t = busiest * cost;
+        if (t < best_t * 0.999) {
+            best_t = t;
+            best = l;
+        }
+    }
+    return best;
+}
+
+bool dstate_ok(int64_t n) { return n == 4 || n == 8 || n == 16; }
+
+}  // namespace
+
+extern "C" {
+
+const char* ssm_status_string(int status) {
+    switch (status) {
+        case SSM_OK: return "SSM_OK";
+        case SSM_ERR_NULL: return "SSM_ERR_NULL: a required pointer is NULL";
+        case SSM_ERR_SHAPE: return "SSM_ERR_SHAPE: a size is <= 0 or the problem is too large";
+        case SSM_ERR_ALIGN: return "SSM_ERR_ALIGN: a pointer is misaligned";
+        case SSM_ERR_UNSUPPORTED: return "SSM_ERR_UNSUPPORTED: d_state must be 4, 8 or 16";
+        case SSM_ERR_DTYPE: return "SSM_ERR_DTYPE: dtype must be SSM_F32 or SSM_BF16";
+        case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
+        case SSM_ERR_LAUNCH: return "SSM_ERR_LAUNCH: the CUDA runtime rejected a launch";
+        case SSM_ERR_DEVICE: return "SSM_ERR_DEVICE: no usable CUDA device";
+        default: return "unknown ssm_status";
+    }
+}
+
+int ssm_version(void) { return 100; }
+
+ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const float* delta_bias,
+                        int softplus_flag, void* out, float* last_state, int64_t batch,
+                        int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* stream) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
+    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
+    const uintptr_t ea = (uintptr_t)es;
+    if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
+        !aligned(out, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
+        (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+        return SSM_ERR_ALIGN;
+
+    const int64_t x_bytes = batch * seqlen * dim * es;
+    const int64_t bc_bytes = batch * dstate * seqlen * es;
+    const Span ins[] = {{u, x_bytes}, {delta, x_bytes}, {z, x_bytes}, {B, bc_bytes}, {C, bc_bytes},
+                        {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4}};
+    const Span so{out, x_bytes}, sl{last_state, batch * dim * dstate * 4};
+    for (const Span& s : ins)
+        if (overlap(so, s) || overlap(sl, s)) return SSM_ERR_ALIAS;
+    if (overlap(so, sl)) return SSM_ERR_ALIAS;
+
+    int sms = 0;
+    if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
+
+    ssm::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, out, last_state,
+                    batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
+    ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
+    const cudaError_t e = ssm::launch_scan_fwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+                                               plan, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
+                            const void* B, const void* C, const float* D, const void* z,
+                            const float* dt_bias, void* out, int64_t batch, int64_t dim,
+                            int64_t dstate, int dt_softplus, int dtype, void* stream) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (!state || !x || !dt || !A || !B || !C || !out) return SSM_ERR_NULL;
+    if (batch <= 0 || dim <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
+    if (batch * dim > kMaxElems / 16) return SSM_ERR_SHAPE;
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
+    const uintptr_t ea = (uintptr_t)es;
+    if (!aligned(state, 16) || !aligned(A, 16) || !aligned(x, ea) || !aligned(dt, ea) ||
+        !aligned(B, ea) || !aligned(C, ea) || !aligned(out, ea) || (z && !aligned(z, ea)) ||
+        (D && !aligned(D, 4)) || (dt_bias && !aligned(dt_bias, 4)))
+        return SSM_ERR_ALIGN;
+
+    const int64_t tok = batch * dim * es, bc = batch * dstate * es;
+    const Span ins[] = {{x, tok}, {dt, tok}, {z, tok}, {B, bc}, {C, bc},
+                        {A, dim * dstate * 4}, {D, dim * 4}, {dt_bias, dim * 4}};
+    const Span ss{state, batch * dim * dstate * 4}, so{out, tok};
+    for (const Span& s : ins)
+        if (overlap(ss, s) || overlap(so, s)) return SSM_ERR_ALIAS;
+    if (overlap(ss, so)) return SSM_ERR_ALIAS;
+
+    int sms = 0;
+    if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
+
+    ssm::UpdateArgs a{state, x, dt, A, B, C, D, z, dt_bias, out, batch, dim, (int)dstate,
+                      dt_softplus ? 1 : 0};
+    const cudaError_t e = ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+                                                   static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+}
+
+}  // extern "C"

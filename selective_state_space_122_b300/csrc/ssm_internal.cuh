@@ -1,0 +1,147 @@
+// ssm_internal.cuh -- parameter blocks and device helpers shared by the
+// library's kernels and its host entry points.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <cstdint>
+
+namespace ssm {
+
+constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLn2 = 0.69314718055994531f;
+
+enum class DType : int { F32 = 0, BF16 = 1 };
+
+// Arguments of one full-sequence scan; layouts as in ssm_scan.h.
+struct ScanArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    void* out;
+    float* last_state;
+    int64_t batch, dim, seqlen;
+    int dstate;
+    int softplus;
+};
+
+// Arguments of one decode step; layouts as in ssm_scan.h.
+struct UpdateArgs {
+    float* state;
+    const void* x;
+    const void* dt;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* dt_bias;
+    void* out;
+    int64_t batch, dim;
+    int dstate;
+    int softplus;
+};
+
+// One compiled layout of the scan kernel: G states per lane (the N / G
+// lanes of a channel are adjacent), S warps per CTA, TL time lanes per warp,
+// K steps per sub-chunk, CW channels per CTA.  S * TL > 1 splits every chunk
+// of S * TL * K steps into sub-chunks combined with the associative scan.
+struct ScanLayoutInfo {
+    int G, S, TL, K, CW;
+};
+
+struct ScanPlan {
+    int layout;  // index into the compiled layouts for this d_state
+};
+
+int scan_layout_count(int dstate);
+ScanLayoutInfo scan_layout_info(int dstate, int layout);
+cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s);
+cudaError_t launch_state_update(const UpdateArgs& a, DType dt, cudaStream_t s);
+
+// ---------------------------------------------------------------- device side
+
+__device__ __forceinline__ float to_f32(float v) { return v; }
+__device__ __forceinline__ float to_f32(__nv_bfloat16 v) { return __bfloat162float(v); }
+
+template <typename T> __device__ __forceinline__ T from_f32(float v);
+template <> __device__ __forceinline__ float from_f32<float>(float v) { return v; }
+template <> __device__ __forceinline__ __nv_bfloat16 from_f32<__nv_bfloat16>(float v) {
+    return __float2bfloat16_rn(v);
+}
+
+// 2^x on the special-function unit (one MUFU.EX2; flushes denormal results).
+__device__ __forceinline__ float ex2_approx(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float lg2_approx(float x) {
+    float y;
+    asm("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+__device__ __forceinline__ float rcp_approx(float x) {
+    float y;
+    asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// exp2 of the decay exponent.  kFast: the SFU instruction; otherwise the
+// CUDA math library's exp2f (float32 inputs, where speed is secondary).
+template <bool kFast>
+__device__ __forceinline__ float decay_exp2(float x) {
+    if constexpr (kFast) return ex2_approx(x);
+    else return exp2f(x);
+}
+
+// softplus(x) = log(1 + e^x).  Above 20 the correction log1p(e^-x) is below
+// 2.1e-9 and x itself is returned.
+__device__ __forceinline__ float softplus_acc(float x) {
+    return x > 20.f ? x : log1pf(expf(x));
+}
+
+// softplus on the special-function unit: e = 2^(x log2 e), then
+// log1p(e) = ln2 * log2(1 + e), or, for e < 2^-6 where 1 + e would drop
+// digits of e, the series e - e^2/2 + e^3/3 - e^4/4 (truncation < e^5/5,
+// i.e. relative error < 2e-9).  Above 15 the correction log1p(e^-x) < 3.1e-7
+// is dropped (relative error < 2.1e-8).
+__device__ __forceinline__ float softplus_fast(float x) {
+    const float e = ex2_approx(x * kLog2e);
+    const float via_log = kLn2 * lg2_approx(1.f + e);
+    const float series = e * fmaf(e, fmaf(e, fmaf(e, -0.25f, 0.33333334f), -0.5f), 1.f);
+    const float r = e < 0.015625f ? series : via_log;
+    return x > 15.f ? x : r;
+}
+
+// silu(z) = z / (1 + e^-z)
+__device__ __forceinline__ float silu_acc(float zv) {
+    return zv / (1.f + expf(-zv));
+}
+
+// silu on the special-function unit: one exp2 and one reciprocal.  For
+// z < -88 the exponential overflows to +inf and the result is -0.
+__device__ __forceinline__ float silu_fast(float zv) {
+    return zv * rcp_approx(1.f + ex2_approx(-zv * kLog2e));
+}
+
+template <bool kFast>
+__device__ __forceinline__ float softplus_f(float x) {
+    if constexpr (kFast) return softplus_fast(x);
+    else return softplus_acc(x);
+}
+
+template <bool kFast>
+__device__ __forceinline__ float silu_f(float zv) {
+    if constexpr (kFast) return silu_fast(zv);
+    else return silu_acc(zv);
+}
+
+}  // namespace ssm

@@ -70,11 +70,22 @@ SCAN_WORKLOADS = {0: TINY_F32, 1: LAYER_130M, 2: PREFILL_MID, 3: LONG_SEQ}
 
 
 def round_to_bf16_bits(x: np.ndarray) -> np.ndarray:
-    """float32 -> bfloat16 bit patterns (uint16), round to nearest even."""
+    """float32 -> bfloat16 bit patterns (uint16), round to nearest even.
+
+    Finite inputs only (the generators never draw NaN); works in 32-bit
+    integer arithmetic, in blocks, to keep the temporaries small."""
     x = np.ascontiguousarray(x, dtype=np.float32)
-    w = x.view(np.uint32).astype(np.uint64)
-    bias = ((w >> 16) & 1) + 0x7FFF
-    return ((w + bias) >> 16).astype(np.uint16)
+    w_all = x.view(np.uint32).reshape(-1)
+    out = np.empty(w_all.shape, np.uint16)
+    blk = 1 << 24
+    for i in range(0, w_all.size, blk):
+        w = w_all[i:i + blk]
+        r = (w >> np.uint32(16)) & np.uint32(1)
+        r += np.uint32(0x7FFF)
+        r += w
+        r >>= np.uint32(16)
+        out[i:i + blk] = r
+    return out.reshape(x.shape)
 
 
 def bf16_bits_to_f64(b: np.ndarray) -> np.ndarray:
@@ -125,6 +136,15 @@ class ScanInputs:
     D: Optional[np.ndarray]
     delta_bias: Optional[np.ndarray]
     softplus: bool = True
+
+    def channels(self, sel) -> "ScanInputs":
+        """The same inputs restricted to the channels ``sel`` (no arithmetic)."""
+        sel = np.asarray(sel)
+        pick = lambda a: None if a is None else np.ascontiguousarray(a[:, :, sel])
+        vec = lambda a: None if a is None else np.ascontiguousarray(a[sel])
+        shape = dataclasses.replace(self.shape, dim=int(sel.size))
+        return ScanInputs(shape, pick(self.u), pick(self.delta), pick(self.z), self.B, self.C,
+                          vec(self.A), vec(self.D), vec(self.delta_bias), self.softplus)
 
     def as_f64(self) -> dict:
         """Exact float64 copies of every input (for the oracle)."""

@@ -1,0 +1,119 @@
+"""The C ABI on the host: symbols, status strings and argument validation.
+
+Every call here is rejected by host-side validation before the library touches
+a device, so the tests run without a GPU (the pointers are never dereferenced).
+"""
+import ctypes
+import os
+import re
+
+import pytest
+import torch
+
+from selective_state_space_122_b300 import _lib, build
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ssm_scan.h")
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return _lib.load_library()
+
+
+def declared_functions():
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(ssm_[a-z_0-9]+)\s*\(", text)))
+
+
+def test_header_declares_the_documented_entry_points():
+    assert declared_functions() == sorted(_lib.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    out = os.popen(f"nm -D --defined-only {_lib.LIB_PATH}").read()
+    exported = set(re.findall(r" T (ssm_\w+)", out))
+    assert exported == set(declared_functions()), exported
+
+
+def test_status_strings(lib):
+    for code, name in _lib.STATUS.items():
+        assert lib.ssm_status_string(code).decode().startswith(name)
+    assert lib.ssm_status_string(99) == b"unknown ssm_status"
+    assert lib.ssm_version() >= 100
+
+
+P = 0x10000000          # fake, suitably aligned device addresses; never dereferenced
+MB = 1 << 20
+
+
+def scan_args(**kw):
+    a = dict(u=P, delta=P + 64 * MB, A=P + 128 * MB, B=P + 192 * MB, C=P + 256 * MB, D=P + 320 * MB,
+             z=P + 384 * MB, delta_bias=P + 448 * MB, softplus=1, out=P + 512 * MB,
+             last_state=P + 576 * MB, batch=2, dim=64, seqlen=128, dstate=16, dtype=1, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_scan(lib, a):
+    return lib.ssm_scan_fwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                            a["delta_bias"], a["softplus"], a["out"], a["last_state"], a["batch"],
+                            a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(u=None), 1), (dict(delta=None), 1), (dict(A=None), 1), (dict(B=None), 1),
+    (dict(C=None), 1), (dict(out=None), 1),
+    (dict(batch=0), 2), (dict(dim=0), 2), (dict(seqlen=0), 2), (dict(seqlen=-5), 2),
+    (dict(batch=70000), 2), (dict(dim=1 << 24, seqlen=1 << 20), 2),
+    (dict(dstate=3), 4), (dict(dstate=32), 4), (dict(dstate=0), 2),
+    (dict(dtype=2), 5), (dict(dtype=-1), 5),
+    (dict(u=P + 1), 3), (dict(out=P + 512 * MB + 1), 3), (dict(A=P + 128 * MB + 2), 3),
+    (dict(dtype=0, z=P + 384 * MB + 2), 3), (dict(last_state=P + 576 * MB + 2), 3),
+    (dict(out=P + 1024), 6), (dict(out=P + 256 * MB), 6), (dict(last_state=P + 512 * MB + 64), 6),
+    (dict(last_state=P + 128 * MB), 6),
+])
+def test_scan_rejects_bad_arguments(lib, kw, code):
+    assert call_scan(lib, scan_args(**kw)) == code
+
+
+def upd_args(**kw):
+    a = dict(state=P, x=P + 64 * MB, dt=P + 128 * MB, A=P + 192 * MB, B=P + 256 * MB, C=P + 320 * MB,
+             D=P + 384 * MB, z=P + 448 * MB, dt_bias=P + 512 * MB, out=P + 576 * MB,
+             batch=4, dim=64, dstate=16, softplus=1, dtype=1, stream=None)
+    a.update(kw)
+    return a
+
+
+def call_upd(lib, a):
+    return lib.ssm_state_update(a["state"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                a["dt_bias"], a["out"], a["batch"], a["dim"], a["dstate"], a["softplus"],
+                                a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(state=None), 1), (dict(x=None), 1), (dict(dt=None), 1), (dict(A=None), 1), (dict(out=None), 1),
+    (dict(batch=0), 2), (dict(dim=-1), 2), (dict(dstate=12), 4), (dict(dtype=7), 5),
+    (dict(state=P + 8), 3), (dict(A=P + 192 * MB + 4), 3), (dict(x=P + 64 * MB + 1), 3),
+    (dict(out=P + 64 * MB), 6), (dict(out=P + 100), 6), (dict(x=P + 2048), 6),
+])
+def test_update_rejects_bad_arguments(lib, kw, code):
+    assert call_upd(lib, upd_args(**kw)) == code
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="valid arguments would launch on a real device")
+def test_valid_call_without_device_reports_device_error(lib):
+    assert call_scan(lib, scan_args()) == 8
+    assert call_upd(lib, upd_args()) == 8
+
+
+def test_binding_raises_without_cuda_tensors():
+    u = torch.zeros(1, 8, 8)
+    A = torch.zeros(8, 4)
+    B = torch.zeros(1, 4, 8)
+    with pytest.raises(ValueError):
+        _lib.ssm_scan_fwd(u, u, A, B, B)

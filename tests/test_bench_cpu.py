@@ -1,0 +1,77 @@
+"""bench.py host logic on the CPU: accounting, peaks, and the multi-rank path
+(world size 2 over gloo: max-over-ranks timing and rank-0-only reporting)."""
+import json
+import os
+import socket
+import subprocess
+import sys
+
+import pytest
+import torch.multiprocessing as mp
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+sys.path.insert(0, ROOT)
+import bench  # noqa: E402
+
+
+def test_accounting_matches_the_workload():
+    s = bench.SCAN
+    assert (s.batch, s.dim, s.seqlen, s.dstate) == (1, 5120, 131072, 16)
+    assert bench.scan_elements() == 1 * 5120 * 131072 * 16
+    btd = 5120 * 131072
+    # u, delta, z in + out, bf16; B, C; A, D, bias; final state
+    assert bench.scan_bytes() == 8 * btd + 4 * 16 * 131072 + 5120 * 16 * 4 + 2 * 5120 * 4 + 5120 * 16 * 4
+    assert bench.scan_sfu_ops() == btd * (18 + 4)   # 18 ex2 + log and reciprocal at half rate
+    assert bench.decode_bytes() == (2 * 256 * 5120 * 16 * 4 + 4 * 256 * 5120 * 2 + 2 * 256 * 16 * 2
+                                    + 5120 * 16 * 4 + 2 * 5120 * 4)
+
+
+def test_peaks_fall_back_when_file_missing(tmp_path, monkeypatch):
+    monkeypatch.setattr(bench, "ROOT", str(tmp_path))
+    p = bench.load_peaks()
+    assert p["source"] == "fallback" and p["hbm_gbs"] == 6400.0
+    (tmp_path / "MEASURED_PEAKS.json").write_text(json.dumps({"hbm_gbs": 6500.0, "sm_max_mhz": 2000}))
+    p = bench.load_peaks()
+    assert p == {"hbm_gbs": 6500.0, "sm_max_mhz": 2000.0, "source": "measured"}
+
+
+def _free_port():
+    s = socket.socket()
+    s.bind(("127.0.0.1", 0))
+    port = s.getsockname()[1]
+    s.close()
+    return port
+
+
+def _rank(rank, world, port, q):
+    os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port), RANK=str(rank),
+                      WORLD_SIZE=str(world), LOCAL_RANK=str(rank))
+    r, w, lr = bench.dist_env()
+    bench.dist_init(w, "gloo")
+    m = bench.max_over_ranks(10.0 + r, w)
+    bench.barrier(w)
+    q.put((r, w, lr, m))
+    import torch.distributed as dist
+    dist.destroy_process_group()
+
+
+def test_two_rank_max_over_ranks_gloo():
+    ctx = mp.get_context("spawn")
+    q = ctx.Queue()
+    port = _free_port()
+    procs = [ctx.Process(target=_rank, args=(r, 2, port, q)) for r in range(2)]
+    for p in procs:
+        p.start()
+    res = sorted(q.get(timeout=120) for _ in procs)
+    for p in procs:
+        p.join(timeout=60)
+        assert p.exitcode == 0
+    assert [x[0] for x in res] == [0, 1] and all(x[1] == 2 for x in res)
+    assert all(x[3] == 11.0 for x in res), res
+
+
+def test_reference_arm_nonzero_rank_exits_without_work():
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1")
+    r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
+                        "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0 and r.stdout.strip() == ""

@@ -1,0 +1,186 @@
+"""GPU parity of ssm_scan_fwd against the float64 oracle, through the C ABI."""
+from __future__ import annotations
+
+import os
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import (LAYOUTS, check_out, check_state, dev, host_f64, scan_layout, scan_on_gpu,
+                      state_rel_err)
+from selective_state_space_122_b300 import inputs, ssm_scan_fwd
+
+pytestmark = pytest.mark.gpu
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def oracle_of(inp: inputs.ScanInputs, channels=None):
+    """Oracle result, optionally on a subset of channels only."""
+    f = (inp if channels is None else inp.channels(channels)).as_f64()
+    return oracle.scan(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"],
+                       f["delta_bias"], f["softplus"])
+
+
+def layouts(N):
+    return list(range(LAYOUTS[N]))
+
+
+# ------------------------------------------------------------ the five workloads
+
+@pytest.mark.parametrize("g", [None, 0, 1, 2, 3])
+def test_tiny_f32_against_golden(g):
+    inp = inputs.make_scan_inputs(inputs.TINY_F32, 0)
+    with scan_layout(g):
+        out, last = scan_on_gpu(inp)
+    ref = np.loadtxt(os.path.join(GOLDEN, "tiny_f32_out.txt")).reshape(out.shape)
+    ref_last = np.loadtxt(os.path.join(GOLDEN, "tiny_f32_last_state.txt")).reshape(last.shape)
+    check_out(host_f64(out), ref, inputs.F32)
+    check_state(host_f64(last), ref_last, inputs.F32)
+
+
+@pytest.fixture(scope="module")
+def layer130m():
+    inp = inputs.make_scan_inputs(inputs.LAYER_130M, 1)
+    return inp, oracle_of(inp)
+
+
+@pytest.mark.parametrize("g", [None] + list(range(LAYOUTS[16])))
+def test_layer130m_full(layer130m, g):
+    inp, (ref, ref_last) = layer130m
+    with scan_layout(g):
+        out, last = scan_on_gpu(inp)
+    check_out(host_f64(out), ref, inputs.BF16)
+    check_state(host_f64(last), ref_last, inputs.BF16)
+
+
+def test_prefill_mid_full_with_final_state():
+    inp = inputs.make_scan_inputs(inputs.PREFILL_MID, 2)
+    ref, ref_last = oracle_of(inp)
+    out, last = scan_on_gpu(inp)
+    check_out(host_f64(out), ref, inputs.BF16)
+    check_state(host_f64(last), ref_last, inputs.BF16)
+
+
+def long_seq_sample(dim):
+    """Channels spread over the whole width: both ends, tile seams, random picks."""
+    r = np.random.Generator(np.random.PCG64(99))
+    fixed = [0, 1, 7, 8, 31, 32, 33, 63, 64, 127, 128, dim // 2, dim - 33, dim - 2, dim - 1]
+    return np.unique(np.concatenate([fixed, r.choice(dim, 33, replace=False)]))
+
+
+def test_long_sequence_sampled_channels():
+    """Full 1 x 5120 x 131072 x 16 workload, in the launch configuration the
+    benchmark times; the oracle recomputes 48 channels over all 128K steps."""
+    inp = inputs.make_scan_inputs(inputs.LONG_SEQ, 3)
+    out, last = scan_on_gpu(inp)
+    sel = long_seq_sample(inputs.LONG_SEQ.dim)
+    ref, ref_last = oracle_of(inp, sel)
+    got = out[:, :, torch.as_tensor(sel, device=out.device)]
+    check_out(host_f64(got), ref, inputs.BF16)
+    check_state(host_f64(last[:, torch.as_tensor(sel, device=out.device)]), ref_last, inputs.BF16)
+    assert bool(torch.isfinite(out.float()).all()), "non-finite outputs somewhere in the 128K scan"
+
+
+# ------------------------------------------------------------ variants and edges
+
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+@pytest.mark.parametrize("N", [4, 8, 16])
+def test_random_A_all_layouts(dtype, N):
+    shape = inputs.ScanShape("randA", 2, 96, 300, N, dtype)
+    inp = inputs.make_scan_inputs(shape, 10 + N, random_a=True)
+    ref, ref_last = oracle_of(inp)
+    for g in layouts(N):
+        with scan_layout(g):
+            out, last = scan_on_gpu(inp)
+        check_out(host_f64(out), ref, dtype, f"out layout {g}")
+        check_state(host_f64(last), ref_last, dtype, f"state layout {g}")
+
+
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+@pytest.mark.parametrize("opts", [dict(softplus=False), dict(with_z=False), dict(with_d=False),
+                                  dict(with_bias=False),
+                                  dict(softplus=False, with_z=False, with_d=False, with_bias=False)],
+                         ids=["no-softplus", "no-gate", "no-D", "no-bias", "bare"])
+def test_optional_inputs(dtype, opts):
+    shape = inputs.ScanShape("opts", 2, 64, 200, 16, dtype)
+    inp = inputs.make_scan_inputs(shape, 20, **opts)
+    if not inp.softplus:
+        # without softplus the raw timestep is used as is: keep it positive and small
+        raw = np.abs(inputs.bf16_bits_to_f64(inp.delta) if dtype == inputs.BF16 else inp.delta) * 0.05
+        inp.delta = (inputs.round_to_bf16_bits(raw.astype(np.float32)) if dtype == inputs.BF16
+                     else raw.astype(np.float32))
+        if inp.delta_bias is not None:
+            inp.delta_bias = np.random.default_rng(1).uniform(1e-3, 2e-2, shape.dim).astype(np.float32)
+    ref, ref_last = oracle_of(inp)
+    for g in layouts(16):
+        with scan_layout(g):
+            out, last = scan_on_gpu(inp)
+        check_out(host_f64(out), ref, dtype, f"out layout {g}")
+        check_state(host_f64(last), ref_last, dtype, f"state layout {g}")
+
+
+@pytest.mark.parametrize("bt,dim,L,N", [(1, 1, 1, 4), (3, 37, 77, 16), (2, 100, 33, 8),
+                                         (1, 257, 65, 16), (5, 9, 31, 4), (2, 130, 1, 16)])
+def test_ragged_shapes(bt, dim, L, N):
+    for dtype in (inputs.F32, inputs.BF16):
+        inp = inputs.make_scan_inputs(inputs.ScanShape("ragged", bt, dim, L, N, dtype), dim + L)
+        ref, ref_last = oracle_of(inp)
+        for g in layouts(N):
+            with scan_layout(g):
+                out, last = scan_on_gpu(inp)
+            check_out(host_f64(out), ref, dtype, f"out layout {g}")
+            check_state(host_f64(last), ref_last, dtype, f"state layout {g}")
+
+
+@pytest.mark.parametrize("g", list(range(LAYOUTS[16])))
+def test_writes_stay_in_bounds(g):
+    """Outputs and the final state sit between guard words that must survive."""
+    shape = inputs.ScanShape("guard", 2, 45, 70, 16, inputs.BF16)
+    inp = inputs.make_scan_inputs(shape, 30)
+    n_out = 2 * 70 * 45
+    guard = 4096
+    buf = torch.full((n_out + 2 * guard,), 12345.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n_out].view(2, 70, 45)
+    sbuf = torch.full((2 * 45 * 16 + 2 * guard,), -7.0, dtype=torch.float32, device="cuda")
+    last = sbuf[guard:guard + 2 * 45 * 16].view(2, 45, 16)
+    with scan_layout(g):
+        ssm_scan_fwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D),
+                     dev(inp.z), dev(inp.delta_bias), True, out=out, last_state=last)
+    torch.cuda.synchronize()
+    assert bool((buf[:guard] == 12345.0).all()) and bool((buf[guard + n_out:] == 12345.0).all())
+    assert bool((sbuf[:guard] == -7.0).all()) and bool((sbuf[guard + 2 * 45 * 16:] == -7.0).all())
+    ref, ref_last = oracle_of(inp)
+    check_out(host_f64(out), ref, inputs.BF16)
+    check_state(host_f64(last), ref_last, inputs.BF16)
+
+
+def test_side_stream_and_determinism():
+    inp = inputs.make_scan_inputs(inputs.ScanShape("stream", 2, 256, 512, 16, inputs.BF16), 40)
+    args = [dev(x) for x in (inp.u, inp.delta, inp.A, inp.B, inp.C, inp.D, inp.z, inp.delta_bias)]
+    o1, s1 = ssm_scan_fwd(*args, True, return_last_state=True)
+    s = torch.cuda.Stream()
+    s.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(s):
+        o2, s2 = ssm_scan_fwd(*args, True, return_last_state=True)
+    torch.cuda.synchronize()
+    assert torch.equal(o1, o2) and torch.equal(s1, s2), "scan is not deterministic across streams"
+
+
+def test_zero_timestep_limit_on_gpu():
+    """Delta -> 0 (bias -1e4 under softplus): out = D u silu(z), state stays 0."""
+    inp = inputs.make_scan_inputs(inputs.ScanShape("dt0", 2, 64, 100, 16, inputs.F32), 50)
+    inp.delta_bias = np.full(64, -1e4, np.float32)
+    out, last = scan_on_gpu(inp)
+    z = inp.z.astype(np.float64)
+    ref = inp.D[None, None, :] * inp.u.astype(np.float64) * z / (1 + np.exp(-z))
+    check_out(host_f64(out), ref, inputs.F32)
+    assert float(host_f64(last).__abs__().max()) == 0.0
+
+
+def test_final_state_error_is_reported_not_hidden():
+    """The relative-L2 helper itself: a planted 1% error must fail the bar."""
+    r = np.random.default_rng(0).standard_normal((4, 8, 16))
+    assert state_rel_err(r * 1.01, r) > 1e-3
