@@ -9,27 +9,35 @@
 //
 // Work layout (one CTA = CW consecutive channels of one batch row, walking
 // the whole sequence chunk by chunk; the state never leaves the chip):
-//   * lane = (tl, c, g): channel c of the CTA, state group g (G consecutive
-//     states; the R = N / G lanes of a channel are adjacent), time lane tl;
-//   * a chunk of TC = S * TL * K steps is cut into S * TL sub-chunks of K
-//     steps, sub-chunk sc = warp * TL + tl;
-//   * S * TL == 1: one lane walks every step of the chunk with its states in
+//   * lane = (c, g): channel c of the CTA and state group g (G consecutive
+//     states; the R = N / G lanes of a channel are adjacent lanes);
+//   * a chunk of TC = S * K steps is cut into S sub-chunks of K steps, one
+//     per warp;
+//   * S == 1: the lane walks every step of the chunk with its states in
 //     registers (the sequential scan of "Efficient Scan");
-//   * S * TL > 1: each lane first runs its sub-chunk from a zero state,
-//     keeping exp(Delta A) and Delta B u of every step in registers; the
-//     sub-chunk summaries (prod exp(Delta A), local end state) are combined
-//     in order with the associative operator
+//   * S > 1: each warp first runs its sub-chunk from a zero state, keeping
+//     exp(Delta A) and Delta B u of every step in registers, and publishes
+//     the sub-chunk summary (prod exp(Delta A), local end state).  Each lane
+//     then folds the summaries of the earlier sub-chunks into the chunk's
+//     incoming state with the associative operator
 //         (a1, b1) o (a2, b2) = (a1 a2, a2 b1 + b2)
-//     ("Efficient Scan", parallel scan), giving each sub-chunk its true
-//     incoming state; a second sweep over the stored values then produces
-//     h_t and y_t.  No exponential is evaluated twice.
+//     ("Efficient Scan", parallel scan) and reruns its sub-chunk from the
+//     true incoming state over the stored values.  No exponential is
+//     evaluated twice; the last warp's final state is the next chunk's
+//     incoming state.
 //   * per (t, d) work (softplus, Delta u, D u, silu(z)) is done once per
-//     (t, d) per chunk into shared memory; the raw activations and B/C of
-//     chunk k+1 are fetched into registers while chunk k is computed;
-//   * y_t = sum over the R lanes of a channel: each lane holds K partial sums
-//     and a transposed butterfly leaves K / R finished sums per lane;
+//     (t, d) into shared memory; the raw activations and B/C of chunk k+1
+//     are fetched into registers while chunk k is computed;
+//   * y_t = sum over the R lanes of a channel: each lane keeps K partial
+//     sums and a transposed butterfly leaves K / R finished sums per lane;
 //   * the inner loop uses packed f32x2 multiplies / FMAs (two states per
 //     instruction) and one SFU ex2 per (t, state).
+//
+// Shared-memory layouts (chosen so warp-wide accesses stay at one wavefront
+// per 128 bytes): Delta / Delta u and D u / silu(z) as [channel][t] float2
+// rows (one 16-byte load = two steps); B and C as float rows, one per state,
+// t-contiguous, with the state of row j * R + g being g * G + j so the R
+// lanes of a channel read rows in distinct bank groups.
 #include <cstdint>
 #include <type_traits>
 
@@ -38,25 +46,6 @@
 namespace ssm {
 namespace {
 
-// ------------------------------------------------------------- f32x2 helpers
-
-__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
-    return d;
-}
-
-__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
-    float2 d;
-    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
-        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
-        : "=f"(d.x), "=f"(d.y)
-        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
-    return d;
-}
-
 template <bool kFast>
 __device__ __forceinline__ float2 exp2_2(float2 x) {
     return make_float2(decay_exp2<kFast>(x.x), decay_exp2<kFast>(x.y));
@@ -64,36 +53,40 @@ __device__ __forceinline__ float2 exp2_2(float2 x) {
 
 // ------------------------------------------------------------- configuration
 
-template <typename T, int N_, int G_, int S_, int TL_, int K_>
+template <typename T, int N_, int G_, int S_, int K_>
 struct Cfg {
-    static constexpr int N = N_, G = G_, S = S_, TL = TL_, K = K_;
+    static constexpr int N = N_, G = G_, S = S_, K = K_;
     static constexpr int R = N / G;                 // lanes per channel
-    static constexpr int CW = 32 / (R * TL);        // channels per CTA
+    static constexpr int CW = 32 / R;               // channels per CTA
     static constexpr int THREADS = 32 * S;
-    static constexpr int NSUB = S * TL;             // sub-chunks per chunk
-    static constexpr int TC = NSUB * K;             // steps per chunk
-    static constexpr bool kSplit = NSUB > 1;
+    static constexpr int TC = S * K;                // steps per chunk
+    static constexpr bool kSplit = S > 1;
     static constexpr int V = 16 / (int)sizeof(T);   // elements per 16-byte vector
-    static constexpr int PAIRS = TC * CW / 2;       // (t, channel pair) items per chunk
+    static constexpr int PAIRS = TC * CW / 2;       // (t, channel pair) prologue items per chunk
     static constexpr int PAIRS_PT = (PAIRS + THREADS - 1) / THREADS;
     static constexpr int BCV = 2 * N * TC / V;      // 16-byte vectors of B and C per chunk
     static constexpr int BCV_PT = (BCV + THREADS - 1) / THREADS;
     static constexpr int KR = K / R;                // finished sums per lane
-    static constexpr int CH_PT = (CW * N + THREADS - 1) / THREADS;  // combine chains per thread
-    static_assert(G % 2 == 0, "two states per packed instruction");
-    static_assert(N % G == 0 && R * TL <= 16 && 32 % (R * TL) == 0, "lane layout");
-    static_assert(K % R == 0, "transposed reduction needs K multiple of R");
-    static_assert((N * TC) % V == 0, "B/C chunk rows are whole vectors");
+    // row strides (floats): TCD for the float2 [c][t] rows, TCB for B/C rows
+    static constexpr int TCD = 2 * TC + 4;
+    static constexpr int TCB = TC + 4;
+    static_assert(G % 4 == 0, "states per lane come in 16-byte groups");
+    static_assert(N % G == 0 && R <= 16, "lane layout");
+    static_assert(K % 4 == 0 && K % R == 0 && (R == 1 || KR % 2 == 0), "steps per lane");
+    static_assert(TC % V == 0, "B/C chunk rows are whole vectors");
     // shared memory, in floats
-    static constexpr int OFF_DD = 0;                           // float2 [TC][CW]  (Delta, Delta u)
-    static constexpr int OFF_SG = OFF_DD + 2 * TC * CW;        // float2 [TC][CW]  (D u, silu z)
-    static constexpr int OFF_B = OFF_SG + 2 * TC * CW;         // float  [TC][N]
-    static constexpr int OFF_C = OFF_B + TC * N;               // float  [TC][N]
-    static constexpr int OFF_SUM = OFF_C + TC * N;             // float2 [NSUB][CW][N]
-    static constexpr int OFF_CIN = OFF_SUM + (kSplit ? 2 * NSUB * CW * N : 0);  // [NSUB][CW][N]
-    static constexpr int OFF_OUT = OFF_CIN + (kSplit ? NSUB * CW * N : 0);      // T [TC][CW]
-    static constexpr int SMEM_FLOATS = OFF_OUT + (TC * CW * (int)sizeof(T) + 3) / 4;
+    static constexpr int OFF_DD = 0;                       // [CW][TCD]  (Delta, Delta u) per t
+    static constexpr int OFF_SG = OFF_DD + CW * TCD;       // [CW][TCD]  (D u, silu z) per t
+    static constexpr int OFF_B = OFF_SG + CW * TCD;        // [N][TCB]
+    static constexpr int OFF_C = OFF_B + N * TCB;          // [N][TCB]
+    static constexpr int OFF_P = OFF_C + N * TCB;          // [S][CW][N]   sub-chunk decay products
+    static constexpr int OFF_H = OFF_P + (kSplit ? S * CW * N : 0);    // [S][CW][N] local end states
+    static constexpr int OFF_CAR = OFF_H + (kSplit ? S * CW * N : 0);  // [2][CW][N] chunk carries
+    static constexpr int OFF_OUT = OFF_CAR + (kSplit ? 2 * CW * N : 0);  // T [TC][CW]
+    static constexpr int SMEM_FLOATS = OFF_OUT + (TC * CW * (int)sizeof(T) + 15) / 16 * 4;
     static constexpr size_t SMEM_BYTES = sizeof(float) * SMEM_FLOATS;
+    // B/C row of state n
+    static __device__ __forceinline__ int brow(int n) { return (n % G) * R + n / G; }
 };
 
 // Per-launch facts the kernel needs beyond ScanArgs.
@@ -117,16 +110,27 @@ struct Pair<float> {
     static __device__ __forceinline__ type make(float a, float b) { return make_float2(a, b); }
 };
 
+__device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+
 template <typename CF, typename T, bool kFast>
 struct ScanKernel {
     using PT = typename Pair<T>::type;
-    static constexpr int N = CF::N, G = CF::G, R = CF::R, CW = CF::CW, K = CF::K;
-    static constexpr int TC = CF::TC, NSUB = CF::NSUB, V = CF::V;
+    static constexpr int N = CF::N, G = CF::G, R = CF::R, CW = CF::CW, K = CF::K, S = CF::S;
+    static constexpr int TC = CF::TC, V = CF::V, TCD = CF::TCD, TCB = CF::TCB, KR = CF::KR;
+    static constexpr int THREADS = CF::THREADS;
 
-    // ---- raw fetch of one chunk into registers (zero outside the tensor)
+    // ---- raw inputs of one chunk, held in registers between fetch and use
     struct Regs {
         PT u[CF::PAIRS_PT], dl[CF::PAIRS_PT], z[CF::PAIRS_PT];
         uint4 bc[CF::BCV_PT];
+    };
+
+    // Per-thread constants of the prologue's channel pair (a thread handles
+    // the same pair in every chunk because THREADS is a multiple of CW / 2).
+    struct PairConst {
+        float2 bias, dsk;
+        bool ok0, ok1;
     };
 
     static __device__ __forceinline__ PT load_pair(const T* base, int64_t row, int64_t d, int64_t dim,
@@ -148,8 +152,8 @@ struct ScanKernel {
         const T* zp = p.z ? static_cast<const T*>(p.z) + b * L * dim : nullptr;
 #pragma unroll
         for (int k = 0; k < CF::PAIRS_PT; ++k) {
-            const int idx = tid + k * CF::THREADS;
-            if (CF::PAIRS % CF::THREADS == 0 || idx < CF::PAIRS) {
+            const int idx = tid + k * THREADS;
+            if (CF::PAIRS % THREADS == 0 || idx < CF::PAIRS) {
                 const int t = idx / (CW / 2), cp = idx % (CW / 2);
                 const int64_t row = t0 + t, d = d0 + 2 * cp;
                 r.u[k] = load_pair(u, row, d, dim, L, geo.vec_x);
@@ -161,8 +165,8 @@ struct ScanKernel {
         const T* Cb = static_cast<const T*>(p.C) + b * N * L;
 #pragma unroll
         for (int k = 0; k < CF::BCV_PT; ++k) {
-            const int idx = tid + k * CF::THREADS;
-            if (CF::BCV % CF::THREADS == 0 || idx < CF::BCV) {
+            const int idx = tid + k * THREADS;
+            if (CF::BCV % THREADS == 0 || idx < CF::BCV) {
                 const int which = idx / (N * TC / V);
                 const int rem = idx % (N * TC / V);
                 const int n = rem / (TC / V), tv = rem % (TC / V);
@@ -184,49 +188,52 @@ struct ScanKernel {
     }
 
     // ---- per-(t, d) prologue from registers into shared memory
-    static __device__ __forceinline__ void prologue(const Regs& r, float* sm, const ScanArgs& p, int64_t d0,
-                                                    int64_t t0, int tid) {
-        float2* s_dd = reinterpret_cast<float2*>(sm + CF::OFF_DD);
-        float2* s_sg = reinterpret_cast<float2*>(sm + CF::OFF_SG);
+    static __device__ __forceinline__ void prologue(const Regs& r, const PairConst& pc, float* sm,
+                                                    const ScanArgs& p, int64_t t0, int tid) {
+        float* s_dd = sm + CF::OFF_DD;
+        float* s_sg = sm + CF::OFF_SG;
 #pragma unroll
         for (int k = 0; k < CF::PAIRS_PT; ++k) {
-            const int idx = tid + k * CF::THREADS;
-            if (CF::PAIRS % CF::THREADS == 0 || idx < CF::PAIRS) {
+            const int idx = tid + k * THREADS;
+            if (CF::PAIRS % THREADS == 0 || idx < CF::PAIRS) {
                 const int t = idx / (CW / 2), cp = idx % (CW / 2);
+                const bool row_ok = t0 + t < p.seqlen;
                 const float2 uv = Pair<T>::f(r.u[k]);
-                const float2 xv = Pair<T>::f(r.dl[k]);
                 const float2 zv = Pair<T>::f(r.z[k]);
-                const float ua[2] = {uv.x, uv.y}, xa[2] = {xv.x, xv.y}, za[2] = {zv.x, zv.y};
-#pragma unroll
-                for (int e = 0; e < 2; ++e) {
-                    const int c = 2 * cp + e;
-                    const int64_t d = d0 + c;
-                    const bool ok = d < p.dim && t0 + t < p.seqlen;
-                    float x = xa[e];
-                    if (p.delta_bias && ok) x += p.delta_bias[d];
-                    float dlt = p.softplus ? softplus_f<kFast>(x) : x;
-                    // padded steps / channels: Delta = 0 leaves the state unchanged
-                    dlt = ok ? dlt : 0.f;
-                    const float skip = (p.D && ok) ? p.D[d] * ua[e] : 0.f;
-                    const float gate = p.z ? silu_f<kFast>(za[e]) : 1.f;
-                    s_dd[t * CW + c] = make_float2(dlt, dlt * ua[e]);
-                    s_sg[t * CW + c] = make_float2(skip, gate);
-                }
+                const float2 x = add2(Pair<T>::f(r.dl[k]), pc.bias);
+                float2 dlt = p.softplus ? softplus_f2<kFast>(x) : x;
+                // padded steps / channels: Delta = 0 leaves the state unchanged
+                dlt.x = (row_ok && pc.ok0) ? dlt.x : 0.f;
+                dlt.y = (row_ok && pc.ok1) ? dlt.y : 0.f;
+                const float2 du = mul2(dlt, uv);
+                const float2 skip = mul2(pc.dsk, uv);
+                const float2 gate = p.z ? silu_f2<kFast>(zv) : splat2(1.f);
+                const int c = 2 * cp;
+                *reinterpret_cast<float2*>(s_dd + c * TCD + 2 * t) = make_float2(dlt.x, du.x);
+                *reinterpret_cast<float2*>(s_dd + (c + 1) * TCD + 2 * t) = make_float2(dlt.y, du.y);
+                *reinterpret_cast<float2*>(s_sg + c * TCD + 2 * t) = make_float2(skip.x, gate.x);
+                *reinterpret_cast<float2*>(s_sg + (c + 1) * TCD + 2 * t) = make_float2(skip.y, gate.y);
             }
         }
         float* s_B = sm + CF::OFF_B;
         float* s_C = sm + CF::OFF_C;
 #pragma unroll
         for (int k = 0; k < CF::BCV_PT; ++k) {
-            const int idx = tid + k * CF::THREADS;
-            if (CF::BCV % CF::THREADS == 0 || idx < CF::BCV) {
+            const int idx = tid + k * THREADS;
+            if (CF::BCV % THREADS == 0 || idx < CF::BCV) {
                 const int which = idx / (N * TC / V);
                 const int rem = idx % (N * TC / V);
                 const int n = rem / (TC / V), tv = rem % (TC / V);
-                float* dst = which ? s_C : s_B;
-                const T* e = reinterpret_cast<const T*>(&r.bc[k]);
+                float* dst = (which ? s_C : s_B) + CF::brow(n) * TCB + tv * V;
+                union {
+                    uint4 v;
+                    T e[V];
+                } w;
+                w.v = r.bc[k];
 #pragma unroll
-                for (int j = 0; j < V; ++j) dst[(tv * V + j) * N + n] = to_f32(e[j]);
+                for (int j = 0; j < V; j += 4)
+                    st4(dst + j, make_float4(to_f32(w.e[j]), to_f32(w.e[j + 1]), to_f32(w.e[j + 2]),
+                                             to_f32(w.e[j + 3])));
             }
         }
     }
@@ -238,61 +245,172 @@ struct ScanKernel {
         T* out = static_cast<T*>(p.out) + b * p.seqlen * p.dim;
 #pragma unroll
         for (int k = 0; k < CF::PAIRS_PT; ++k) {
-            const int idx = tid + k * CF::THREADS;
-            if (CF::PAIRS % CF::THREADS == 0 || idx < CF::PAIRS) {
+            const int idx = tid + k * THREADS;
+            if (CF::PAIRS % THREADS == 0 || idx < CF::PAIRS) {
                 const int t = idx / (CW / 2), cp = idx % (CW / 2);
                 const int64_t row = t0 + t, d = d0 + 2 * cp;
-                if (row >= p.seqlen) continue;
-                const T a = s_out[t * CW + 2 * cp], c = s_out[t * CW + 2 * cp + 1];
-                if (geo.vec_x && d + 1 < p.dim) {
-                    PT v;
-                    reinterpret_cast<T*>(&v)[0] = a;
-                    reinterpret_cast<T*>(&v)[1] = c;
-                    *reinterpret_cast<PT*>(out + row * p.dim + d) = v;
-                } else {
-                    if (d < p.dim) out[row * p.dim + d] = a;
-                    if (d + 1 < p.dim) out[row * p.dim + d + 1] = c;
+                if (row < p.seqlen) {
+                    const PT v = *reinterpret_cast<const PT*>(s_out + t * CW + 2 * cp);
+                    if (geo.vec_x && d + 1 < p.dim) {
+                        *reinterpret_cast<PT*>(out + row * p.dim + d) = v;
+                    } else {
+                        const float2 f = Pair<T>::f(v);
+                        if (d < p.dim) out[row * p.dim + d] = from_f32<T>(f.x);
+                        if (d + 1 < p.dim) out[row * p.dim + d + 1] = from_f32<T>(f.y);
+                    }
                 }
             }
         }
     }
 
-    // ---- y: transposed butterfly over the R lanes of a channel.  On return
-    // v[0..K/R) of lane g hold the full sums of steps g*K/R .. g*K/R + K/R - 1.
-    static __device__ __forceinline__ void reduce_lanes(float (&v)[K], int g) {
+    // ---- y: transposed butterfly over the R lanes of a channel.  After all
+    // levels v[0..K/R) of lane g hold the full sums of steps g*K/R + r.
+    template <int M, int LEN>
+    static __device__ __forceinline__ void reduce_level(float (&v)[K], int g) {
+        if constexpr (M >= 1) {
+            const bool upper = (g & M) != 0;
 #pragma unroll
-        for (int m = R / 2, len = K; m >= 1; m >>= 1, len >>= 1) {
-            const bool upper = (g & m) != 0;
-#pragma unroll
-            for (int r = 0; r < len / 2; ++r) {
-                const float send = upper ? v[r] : v[r + len / 2];
-                const float keep = upper ? v[r + len / 2] : v[r];
-                v[r] = keep + __shfl_xor_sync(0xffffffffu, send, m);
+            for (int r = 0; r < LEN / 2; ++r) {
+                const float send = upper ? v[r] : v[r + LEN / 2];
+                const float keep = upper ? v[r + LEN / 2] : v[r];
+                v[r] = keep + __shfl_xor_sync(0xffffffffu, send, M);
             }
+            reduce_level<M / 2, LEN / 2>(v, g);
         }
     }
 
     // ---- finished sums -> gated outputs in the shared out tile
-    static __device__ __forceinline__ void write_y(const float (&v)[K], float* sm, int sc, int c, int g) {
-        const float2* s_sg = reinterpret_cast<const float2*>(sm + CF::OFF_SG);
+    static __device__ __forceinline__ void write_y(const float (&v)[K], float* sm, int t_first, int c) {
+        const float* s_sg = sm + CF::OFF_SG + c * TCD;
         T* s_out = reinterpret_cast<T*>(sm + CF::OFF_OUT);
 #pragma unroll
-        for (int r = 0; r < CF::KR; ++r) {
-            const int t = sc * K + g * CF::KR + r;
-            const float2 sg = s_sg[t * CW + c];
-            s_out[t * CW + c] = from_f32<T>((v[r] + sg.x) * sg.y);
+        for (int r = 0; r < KR; r += 2) {
+            const int t = t_first + r;
+            const float4 sg = ld4(s_sg + 2 * t);  // (skip_t, gate_t, skip_t+1, gate_t+1)
+            const float2 y = mul2(add2(make_float2(v[r], v[r + 1]), make_float2(sg.x, sg.z)),
+                                  make_float2(sg.y, sg.w));
+            s_out[t * CW + c] = from_f32<T>(y.x);
+            s_out[(t + 1) * CW + c] = from_f32<T>(y.y);
+        }
+    }
+
+    // ---- one direct sweep over steps [t_first, t_first + K) from state h,
+    // producing the partial y sums of this lane's states in v.  B and C are
+    // read SW steps at a time (one 8- or 16-byte load per state and array).
+    static constexpr int SW = G <= 8 ? 4 : 2;
+    using VecSW = typename std::conditional<SW == 4, float4, float2>::type;
+
+    static __device__ __forceinline__ void sweep_direct(float2 (&h)[G / 2], const float2 (&A2)[G / 2],
+                                                        const float* sm, int c, int g, float (&v)[K]) {
+        const float* s_dd = sm + CF::OFF_DD + c * TCD;
+        const float* s_B = sm + CF::OFF_B;
+        const float* s_C = sm + CF::OFF_C;
+#pragma unroll
+        for (int i0 = 0; i0 < K; i0 += SW) {
+            VecSW bq[G], cq[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                bq[j] = *reinterpret_cast<const VecSW*>(s_B + (j * R + g) * TCB + i0);
+                cq[j] = *reinterpret_cast<const VecSW*>(s_C + (j * R + g) * TCB + i0);
+            }
+#pragma unroll
+            for (int i2 = 0; i2 < SW; i2 += 2) {
+                const float4 dd = ld4(s_dd + 2 * (i0 + i2));  // (Delta, Delta u) x two steps
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    const float2 dA = exp2_2<kFast>(mul2(splat2(dd.x), A2[j]));
+                    const float2 bv = make_float2(comp(bq[2 * j], i2), comp(bq[2 * j + 1], i2));
+                    h[j] = fma2(dA, h[j], mul2(splat2(dd.y), bv));
+                    acc0 = fma2(make_float2(comp(cq[2 * j], i2), comp(cq[2 * j + 1], i2)), h[j], acc0);
+                }
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    const float2 dA = exp2_2<kFast>(mul2(splat2(dd.z), A2[j]));
+                    const float2 bv = make_float2(comp(bq[2 * j], i2 + 1), comp(bq[2 * j + 1], i2 + 1));
+                    h[j] = fma2(dA, h[j], mul2(splat2(dd.w), bv));
+                    acc1 = fma2(make_float2(comp(cq[2 * j], i2 + 1), comp(cq[2 * j + 1], i2 + 1)), h[j], acc1);
+                }
+                const float2 pr = add2(make_float2(acc0.x, acc1.x), make_float2(acc0.y, acc1.y));
+                v[i0 + i2] = pr.x;
+                v[i0 + i2 + 1] = pr.y;
+            }
+        }
+    }
+
+    // ---- split layouts, pass 1: local scan of this warp's sub-chunk from a
+    // zero state, keeping exp(Delta A) and Delta B u; returns sum of Delta.
+    static __device__ __forceinline__ float sweep_local(float2 (&dA)[K][G / 2], float2 (&dBu)[K][G / 2],
+                                                        float2 (&hl)[G / 2], const float2 (&A2)[G / 2],
+                                                        const float* sm, int tf, int c, int g) {
+        const float* s_dd = sm + CF::OFF_DD + c * TCD;
+        const float* s_B = sm + CF::OFF_B;
+        float2 sdl = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < G / 2; ++j) hl[j] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int i0 = 0; i0 < K; i0 += 4) {
+            float4 bq[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) bq[j] = ld4(s_B + (j * R + g) * TCB + tf + i0);
+#pragma unroll
+            for (int i2 = 0; i2 < 4; i2 += 2) {
+                const float4 dd = ld4(s_dd + 2 * (tf + i0 + i2));
+                sdl = add2(sdl, make_float2(dd.x, dd.z));
+#pragma unroll
+                for (int s = 0; s < 2; ++s) {
+                    const int i = i0 + i2 + s;
+                    const float dlt = s ? dd.z : dd.x, du = s ? dd.w : dd.y;
+#pragma unroll
+                    for (int j = 0; j < G / 2; ++j) {
+                        dA[i][j] = exp2_2<kFast>(mul2(splat2(dlt), A2[j]));
+                        dBu[i][j] = mul2(splat2(du),
+                                         make_float2(comp(bq[2 * j], i2 + s), comp(bq[2 * j + 1], i2 + s)));
+                        hl[j] = fma2(dA[i][j], hl[j], dBu[i][j]);
+                    }
+                }
+            }
+        }
+        return sdl.x + sdl.y;
+    }
+
+    // ---- split layouts, pass 2: rerun the sub-chunk from its true incoming
+    // state h over the stored values, producing the partial y sums.
+    static __device__ __forceinline__ void sweep_replay(const float2 (&dA)[K][G / 2],
+                                                        const float2 (&dBu)[K][G / 2], float2 (&h)[G / 2],
+                                                        const float* sm, int tf, int g, float (&v)[K]) {
+        const float* s_C = sm + CF::OFF_C;
+#pragma unroll
+        for (int i0 = 0; i0 < K; i0 += 4) {
+            float4 cq[G];
+#pragma unroll
+            for (int j = 0; j < G; ++j) cq[j] = ld4(s_C + (j * R + g) * TCB + tf + i0);
+#pragma unroll
+            for (int i1 = 0; i1 < 4; i1 += 2) {
+                float2 acc0 = make_float2(0.f, 0.f), acc1 = make_float2(0.f, 0.f);
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    h[j] = fma2(dA[i0 + i1][j], h[j], dBu[i0 + i1][j]);
+                    acc0 = fma2(make_float2(comp(cq[2 * j], i1), comp(cq[2 * j + 1], i1)), h[j], acc0);
+                }
+#pragma unroll
+                for (int j = 0; j < G / 2; ++j) {
+                    h[j] = fma2(dA[i0 + i1 + 1][j], h[j], dBu[i0 + i1 + 1][j]);
+                    acc1 = fma2(make_float2(comp(cq[2 * j], i1 + 1), comp(cq[2 * j + 1], i1 + 1)), h[j], acc1);
+                }
+                const float2 pr = add2(make_float2(acc0.x, acc1.x), make_float2(acc0.y, acc1.y));
+                v[i0 + i1] = pr.x;
+                v[i0 + i1 + 1] = pr.y;
+            }
         }
     }
 
     static __device__ void run(const ScanArgs& p, const Geo& geo) {
-        extern __shared__ float sm[];
+        extern __shared__ __align__(16) float sm[];
         const int tid = threadIdx.x;
         const int warp = tid >> 5, lane = tid & 31;
         const int g = lane % R;
-        const int c = (lane / R) % CW;
-        const int tl = lane / (R * CW);
-        const int sc = warp * CF::TL + tl;           // sub-chunk of this lane
-        const int n0 = g * G;
+        const int c = lane / R;
         const int64_t b = blockIdx.y;
         const int64_t d0 = (int64_t)blockIdx.x * CW;
         const int64_t d = d0 + c;
@@ -300,144 +418,111 @@ struct ScanKernel {
         const int64_t L = p.seqlen;
         const int64_t nchunks = (L + TC - 1) / TC;
 
+        // decay exponents A * log2(e) of this lane's states g*G + (2j, 2j+1)
         float2 A2[G / 2];
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) {
-            const float a0 = valid ? p.A[d * N + n0 + 2 * j] : 0.f;
-            const float a1 = valid ? p.A[d * N + n0 + 2 * j + 1] : 0.f;
+            const float a0 = valid ? p.A[d * N + g * G + 2 * j] : 0.f;
+            const float a1 = valid ? p.A[d * N + g * G + 2 * j + 1] : 0.f;
             A2[j] = make_float2(a0 * kLog2e, a1 * kLog2e);
         }
-        const float2* s_dd = reinterpret_cast<const float2*>(sm + CF::OFF_DD);
-        const float* s_B = sm + CF::OFF_B;
-        const float* s_C = sm + CF::OFF_C;
 
-        // state: per lane (non-split) or per (channel, state) combine thread (split)
+        PairConst pc;
+        {
+            const int cp = tid % (CW / 2);
+            const int64_t dp = d0 + 2 * cp;
+            pc.ok0 = dp < p.dim;
+            pc.ok1 = dp + 1 < p.dim;
+            pc.bias = make_float2((p.delta_bias && pc.ok0) ? p.delta_bias[dp] : 0.f,
+                                  (p.delta_bias && pc.ok1) ? p.delta_bias[dp + 1] : 0.f);
+            pc.dsk = make_float2((p.D && pc.ok0) ? p.D[dp] : 0.f, (p.D && pc.ok1) ? p.D[dp + 1] : 0.f);
+        }
+
         float2 h[G / 2];
 #pragma unroll
         for (int j = 0; j < G / 2; ++j) h[j] = make_float2(0.f, 0.f);
-        // split: running state of the chains tid, tid + THREADS, ... (chain = c * N + n)
-        float carry[CF::CH_PT];
-#pragma unroll
-        for (int k = 0; k < CF::CH_PT; ++k) carry[k] = 0.f;
+        if constexpr (CF::kSplit) {
+            float* s_car = sm + CF::OFF_CAR;
+            for (int i = tid; i < CW * N; i += THREADS) s_car[i] = 0.f;
+        }
 
         Regs rg;
         fetch(rg, p, geo, b, d0, 0, tid);
-        prologue(rg, sm, p, d0, 0, tid);
+        prologue(rg, pc, sm, p, 0, tid);
         if (nchunks > 1) fetch(rg, p, geo, b, d0, TC, tid);
         __syncthreads();
 
         for (int64_t ch = 0; ch < nchunks; ++ch) {
             float v[K];
             if constexpr (!CF::kSplit) {
-#pragma unroll
-                for (int i = 0; i < K; ++i) {
-                    const int t = i;
-                    const float2 dd = s_dd[t * CW + c];
-                    const float2 x2 = make_float2(dd.x, dd.x), u2 = make_float2(dd.y, dd.y);
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int j = 0; j < G / 2; ++j) {
-                        const float2 bv = *reinterpret_cast<const float2*>(s_B + t * N + n0 + 2 * j);
-                        const float2 cv = *reinterpret_cast<const float2*>(s_C + t * N + n0 + 2 * j);
-                        const float2 dA = exp2_2<kFast>(mul2(x2, A2[j]));
-                        h[j] = fma2(dA, h[j], mul2(u2, bv));
-                        acc = fma2(cv, h[j], acc);
-                    }
-                    v[i] = acc.x + acc.y;
-                }
+                sweep_direct(h, A2, sm, c, g, v);
             } else {
-                // pass 1: local scan of this lane's sub-chunk from a zero state
-                float2 dA[K][G / 2], dBu[K][G / 2];
-                float2 hl[G / 2];
-                float sdl = 0.f;
+                const int tf = warp * K;  // this warp's sub-chunk
+                float2 dA[K][G / 2], dBu[K][G / 2], hl[G / 2];
+                const float sd = sweep_local(dA, dBu, hl, A2, sm, tf, c, g);
+                // sub-chunk summary (prod_i exp(Delta_i A), local end state)
+                float* s_P = sm + CF::OFF_P + (warp * CW + c) * N + g * G;
+                float* s_H = sm + CF::OFF_H + (warp * CW + c) * N + g * G;
 #pragma unroll
-                for (int j = 0; j < G / 2; ++j) hl[j] = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int i = 0; i < K; ++i) {
-                    const int t = sc * K + i;
-                    const float2 dd = s_dd[t * CW + c];
-                    const float2 x2 = make_float2(dd.x, dd.x), u2 = make_float2(dd.y, dd.y);
-                    sdl += dd.x;
-#pragma unroll
-                    for (int j = 0; j < G / 2; ++j) {
-                        const float2 bv = *reinterpret_cast<const float2*>(s_B + t * N + n0 + 2 * j);
-                        dA[i][j] = exp2_2<kFast>(mul2(x2, A2[j]));
-                        dBu[i][j] = mul2(u2, bv);
-                        hl[j] = fma2(dA[i][j], hl[j], dBu[i][j]);
-                    }
-                }
-                // sub-chunk summary: (prod_i exp(Delta_i A), local end state)
-                float2* s_sum = reinterpret_cast<float2*>(sm + CF::OFF_SUM);
-                const float2 s2 = make_float2(sdl, sdl);
-#pragma unroll
-                for (int j = 0; j < G / 2; ++j) {
-                    const float2 P = exp2_2<kFast>(mul2(s2, A2[j]));
-                    s_sum[(sc * CW + c) * N + n0 + 2 * j] = make_float2(P.x, hl[j].x);
-                    s_sum[(sc * CW + c) * N + n0 + 2 * j + 1] = make_float2(P.y, hl[j].y);
+                for (int j = 0; j < G / 2; j += 2) {
+                    const float2 P0 = exp2_2<kFast>(mul2(splat2(sd), A2[j]));
+                    const float2 P1 = exp2_2<kFast>(mul2(splat2(sd), A2[j + 1]));
+                    st4(s_P + 2 * j, make_float4(P0.x, P0.y, P1.x, P1.y));
+                    st4(s_H + 2 * j, make_float4(hl[j].x, hl[j].y, hl[j + 1].x, hl[j + 1].y));
                 }
                 __syncthreads();
-                // ordered combine of the sub-chunk summaries, one thread per chain
-                float* s_cin = sm + CF::OFF_CIN;
+                // incoming state: the chunk carry folded through sub-chunks 0 .. warp-1
+                const int par = (int)(ch & 1);
+                const float* s_car = sm + CF::OFF_CAR + par * CW * N + c * N + g * G;
 #pragma unroll
-                for (int k = 0; k < CF::CH_PT; ++k) {
-                    const int chain = tid + k * CF::THREADS;
-                    if (chain < CW * N) {
-                        float cr = carry[k];
+                for (int j = 0; j < G / 2; j += 2) {
+                    const float4 cr = ld4(s_car + 2 * j);
+                    h[j] = make_float2(cr.x, cr.y);
+                    h[j + 1] = make_float2(cr.z, cr.w);
+                }
+                for (int s = 0; s < warp; ++s) {
+                    const float* sp = sm + CF::OFF_P + (s * CW + c) * N + g * G;
+                    const float* sh = sm + CF::OFF_H + (s * CW + c) * N + g * G;
 #pragma unroll
-                        for (int s = 0; s < NSUB; ++s) {
-                            s_cin[s * CW * N + chain] = cr;
-                            const float2 ph = s_sum[s * CW * N + chain];
-                            cr = fmaf(ph.x, cr, ph.y);
-                        }
-                        carry[k] = cr;
+                    for (int j = 0; j < G / 2; j += 2) {
+                        const float4 P = ld4(sp + 2 * j), H = ld4(sh + 2 * j);
+                        h[j] = fma2(make_float2(P.x, P.y), h[j], make_float2(H.x, H.y));
+                        h[j + 1] = fma2(make_float2(P.z, P.w), h[j + 1], make_float2(H.z, H.w));
                     }
                 }
-                __syncthreads();
-                // pass 2: rerun the sub-chunk from its true incoming state
+                sweep_replay(dA, dBu, h, sm, tf, g, v);
+                // the last sub-chunk's final state is the next chunk's carry
+                if (warp == S - 1) {
+                    float* s_nc = sm + CF::OFF_CAR + (par ^ 1) * CW * N + c * N + g * G;
 #pragma unroll
-                for (int j = 0; j < G / 2; ++j)
-                    h[j] = *reinterpret_cast<const float2*>(s_cin + (sc * CW + c) * N + n0 + 2 * j);
-#pragma unroll
-                for (int i = 0; i < K; ++i) {
-                    const int t = sc * K + i;
-                    float2 acc = make_float2(0.f, 0.f);
-#pragma unroll
-                    for (int j = 0; j < G / 2; ++j) {
-                        const float2 cv = *reinterpret_cast<const float2*>(s_C + t * N + n0 + 2 * j);
-                        h[j] = fma2(dA[i][j], h[j], dBu[i][j]);
-                        acc = fma2(cv, h[j], acc);
-                    }
-                    v[i] = acc.x + acc.y;
+                    for (int j = 0; j < G / 2; j += 2)
+                        st4(s_nc + 2 * j, make_float4(h[j].x, h[j].y, h[j + 1].x, h[j + 1].y));
                 }
             }
-            reduce_lanes(v, g);
-            write_y(v, sm, sc, c, g);
+            reduce_level<R / 2, K>(v, g);
+            write_y(v, sm, (CF::kSplit ? warp * K : 0) + g * KR, c);
             __syncthreads();
             store_out(sm, p, geo, b, d0, ch * TC, tid);
             if (ch + 1 < nchunks) {
-                prologue(rg, sm, p, d0, (ch + 1) * TC, tid);
+                prologue(rg, pc, sm, p, (ch + 1) * TC, tid);
                 if (ch + 2 < nchunks) fetch(rg, p, geo, b, d0, (ch + 2) * TC, tid);
             }
             __syncthreads();
         }
 
-        if (p.last_state) {
+        if (p.last_state && valid) {
+            float* ls = p.last_state + (b * p.dim + d) * N + g * G;
             if constexpr (!CF::kSplit) {
-                if (valid) {
-                    float* ls = p.last_state + (b * p.dim + d) * N + n0;
 #pragma unroll
-                    for (int j = 0; j < G / 2; ++j) {
-                        ls[2 * j] = h[j].x;
-                        ls[2 * j + 1] = h[j].y;
-                    }
+                for (int j = 0; j < G / 2; ++j) {
+                    ls[2 * j] = h[j].x;
+                    ls[2 * j + 1] = h[j].y;
                 }
-            } else {
+            } else if (warp == 0) {
+                // after the last chunk the final state sits in the carry slot
+                const float* s_car = sm + CF::OFF_CAR + (int)(nchunks & 1) * CW * N + c * N + g * G;
 #pragma unroll
-                for (int k = 0; k < CF::CH_PT; ++k) {
-                    const int chain = tid + k * CF::THREADS;
-                    const int64_t dd = d0 + chain / N;
-                    if (chain < CW * N && dd < p.dim) p.last_state[(b * p.dim + dd) * N + chain % N] = carry[k];
-                }
+                for (int j = 0; j < G; ++j) ls[j] = s_car[j];
             }
         }
     }
@@ -448,9 +533,9 @@ __global__ void __launch_bounds__(CF::THREADS) scan_fwd_kernel(ScanArgs p, Geo g
     ScanKernel<CF, T, kFast>::run(p, geo);
 }
 
-template <typename T, int N, int G, int S, int TL, int K>
+template <typename T, int N, int G, int S, int K>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t s) {
-    using CF = Cfg<T, N, G, S, TL, K>;
+    using CF = Cfg<T, N, G, S, K>;
     constexpr bool kFast = !std::is_same<T, float>::value;
     auto kern = scan_fwd_kernel<CF, T, kFast>;
     if (CF::SMEM_BYTES > 48 * 1024) {
@@ -476,107 +561,76 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t s) {
     return cudaGetLastError();
 }
 
-// The layouts compiled in, by (d_state, dtype).  `plan.layout` indexes this
-// table; entry 0 of each list is the default for small problems.
-#define SSM_LAYOUTS_16(X)                                   \
-    X(16, 4, 1, 1, 16) /* 0: one warp, 8 channels       */ \
-    X(16, 8, 1, 1, 16) /* 1: one warp, 16 channels      */ \
-    X(16, 16, 1, 1, 16) /* 2: one warp, 32 channels     */ \
-    X(16, 4, 4, 1, 8)  /* 3: 4 warps x 8 steps, 8 ch    */ \
-    X(16, 4, 4, 2, 8)  /* 4: 8 sub-chunks, 4 channels   */ \
-    X(16, 4, 2, 2, 8)  /* 5: 4 sub-chunks, 4 channels   */ \
-    X(16, 8, 4, 1, 8)  /* 6: 4 warps, 16 channels       */ \
-    X(16, 2, 4, 1, 8)  /* 7: 4 warps, 4 channels, G=2   */
+// The layouts compiled in, per d_state: X(N, G, S, K).  G states per lane,
+// S warps (S > 1: time split), K steps per warp per chunk.
+#define SSM_LAYOUTS_16(X)                                     \
+    X(16, 4, 1, 16)  /* 0: one warp, 8 channels, direct    */ \
+    X(16, 8, 1, 16)  /* 1: one warp, 16 channels, direct   */ \
+    X(16, 16, 1, 8)  /* 2: one warp, 32 channels, direct   */ \
+    X(16, 4, 4, 8)   /* 3: 4 sub-chunks of 8, 8 channels   */ \
+    X(16, 4, 2, 8)   /* 4: 2 sub-chunks of 8, 8 channels   */ \
+    X(16, 8, 4, 4)   /* 5: 4 sub-chunks of 4, 16 channels  */ \
+    X(16, 4, 8, 8)   /* 6: 8 sub-chunks of 8, 8 channels   */
 
-template <typename T, int N>
-cudaError_t launch_layout(const ScanArgs& a, int layout, cudaStream_t s);
+#define SSM_LAYOUTS_8(X)                                      \
+    X(8, 4, 1, 16)   /* 0: one warp, 16 channels, direct   */ \
+    X(8, 8, 1, 8)    /* 1: one warp, 32 channels, direct   */ \
+    X(8, 4, 4, 8)    /* 2: 4 sub-chunks of 8, 16 channels  */ \
+    X(8, 8, 4, 4)    /* 3: 4 sub-chunks of 4, 32 channels  */
+
+#define SSM_LAYOUTS_4(X)                                      \
+    X(4, 4, 1, 8)    /* 0: one warp, 32 channels, direct   */ \
+    X(4, 4, 4, 8)    /* 1: 4 sub-chunks of 8, 32 channels  */
 
 template <typename T>
-cudaError_t launch_16(const ScanArgs& a, int layout, cudaStream_t s) {
+cudaError_t launch_layout(const ScanArgs& a, int layout, cudaStream_t s) {
     int i = 0;
-#define X(N, G, S, TL, K) \
-    if (layout == i++) return launch_cfg<T, N, G, S, TL, K>(a, s);
-    SSM_LAYOUTS_16(X)
+#define X(N_, G_, S_, K_) \
+    if (a.dstate == N_ && layout == i++) return launch_cfg<T, N_, G_, S_, K_>(a, s);
+    if (a.dstate == 16) {
+        SSM_LAYOUTS_16(X)
+    } else if (a.dstate == 8) {
+        SSM_LAYOUTS_8(X)
+    } else if (a.dstate == 4) {
+        SSM_LAYOUTS_4(X)
+    }
 #undef X
     return cudaErrorInvalidValue;
-}
-
-template <typename T>
-cudaError_t launch_8(const ScanArgs& a, int layout, cudaStream_t s) {
-    switch (layout) {
-        case 0: return launch_cfg<T, 8, 4, 1, 1, 16>(a, s);
-        case 1: return launch_cfg<T, 8, 8, 1, 1, 16>(a, s);
-        case 2: return launch_cfg<T, 8, 2, 4, 1, 8>(a, s);
-        case 3: return launch_cfg<T, 8, 4, 4, 1, 8>(a, s);
-        default: return cudaErrorInvalidValue;
-    }
-}
-
-template <typename T>
-cudaError_t launch_4(const ScanArgs& a, int layout, cudaStream_t s) {
-    switch (layout) {
-        case 0: return launch_cfg<T, 4, 4, 1, 1, 16>(a, s);
-        case 1: return launch_cfg<T, 4, 2, 1, 1, 16>(a, s);
-        case 2: return launch_cfg<T, 4, 2, 4, 1, 8>(a, s);
-        case 3: return launch_cfg<T, 4, 4, 4, 1, 8>(a, s);
-        default: return cudaErrorInvalidValue;
-    }
 }
 
 }  // namespace
 
 int scan_layout_count(int dstate) {
+    int n = 0;
+#define X(N_, G_, S_, K_) ++n;
     switch (dstate) {
-        case 16: {
-            int n = 0;
-#define X(N, G, S, TL, K) ++n;
-            SSM_LAYOUTS_16(X)
-#undef X
-            return n;
-        }
-        case 8: return 4;
-        case 4: return 4;
-        default: return 0;
+        case 16: SSM_LAYOUTS_16(X) break;
+        case 8: SSM_LAYOUTS_8(X) break;
+        case 4: SSM_LAYOUTS_4(X) break;
+        default: break;
     }
+#undef X
+    return n;
 }
 
 ScanLayoutInfo scan_layout_info(int dstate, int layout) {
     ScanLayoutInfo r{0, 0, 0, 0, 0};
-    auto set = [&](int G, int S, int TL, int K) {
-        const int R = dstate / G;
-        r = ScanLayoutInfo{G, S, TL, K, 32 / (R * TL)};
-    };
     int i = 0;
+#define X(N_, G_, S_, K_) \
+    if (layout == i++) r = ScanLayoutInfo{G_, S_, 1, K_, 32 / (N_ / G_)};
     switch (dstate) {
-        case 16:
-#define X(N, G, S, TL, K) \
-    if (layout == i++) set(G, S, TL, K);
-            SSM_LAYOUTS_16(X)
-#undef X
-            break;
-        case 8: {
-            const int t[4][4] = {{4, 1, 1, 16}, {8, 1, 1, 16}, {2, 4, 1, 8}, {4, 4, 1, 8}};
-            if (layout >= 0 && layout < 4) set(t[layout][0], t[layout][1], t[layout][2], t[layout][3]);
-            break;
-        }
-        case 4: {
-            const int t[4][4] = {{4, 1, 1, 16}, {2, 1, 1, 16}, {2, 4, 1, 8}, {4, 4, 1, 8}};
-            if (layout >= 0 && layout < 4) set(t[layout][0], t[layout][1], t[layout][2], t[layout][3]);
-            break;
-        }
+        case 16: SSM_LAYOUTS_16(X) break;
+        case 8: SSM_LAYOUTS_8(X) break;
+        case 4: SSM_LAYOUTS_4(X) break;
         default: break;
     }
+#undef X
     return r;
 }
 
 cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s) {
-    const bool f32 = dt == DType::F32;
-    switch (a.dstate) {
-        case 16: return f32 ? launch_16<float>(a, plan.layout, s) : launch_16<__nv_bfloat16>(a, plan.layout, s);
-        case 8: return f32 ? launch_8<float>(a, plan.layout, s) : launch_8<__nv_bfloat16>(a, plan.layout, s);
-        case 4: return f32 ? launch_4<float>(a, plan.layout, s) : launch_4<__nv_bfloat16>(a, plan.layout, s);
-        default: return cudaErrorInvalidValue;
-    }
+    return dt == DType::F32 ? launch_layout<float>(a, plan.layout, s)
+                            : launch_layout<__nv_bfloat16>(a, plan.layout, s);
 }
 
 }  // namespace ssm

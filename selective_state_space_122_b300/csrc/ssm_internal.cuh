@@ -132,6 +132,76 @@ __device__ __forceinline__ float silu_fast(float zv) {
     return zv * rcp_approx(1.f + ex2_approx(-zv * kLog2e));
 }
 
+// ---------------------------------------------------------------- f32x2
+// Packed two-lane float32 arithmetic (one instruction for two values).
+
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mul.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " add.rn.f32x2 rd, ra, rb;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y) : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 fma2(float2 a, float2 b, float2 c) {
+    float2 d;
+    asm("{\n .reg .b64 ra, rb, rc, rd;\n mov.b64 ra, {%2, %3};\n mov.b64 rb, {%4, %5};\n"
+        " mov.b64 rc, {%6, %7};\n fma.rn.f32x2 rd, ra, rb, rc;\n mov.b64 {%0, %1}, rd;\n}"
+        : "=f"(d.x), "=f"(d.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y), "f"(c.x), "f"(c.y));
+    return d;
+}
+
+__device__ __forceinline__ float2 splat2(float v) { return make_float2(v, v); }
+
+// Component i (a compile-time constant after unrolling) of a float4 / float2.
+__device__ __forceinline__ float comp(const float4& v, int i) {
+    return i == 0 ? v.x : (i == 1 ? v.y : (i == 2 ? v.z : v.w));
+}
+__device__ __forceinline__ float comp(const float2& v, int i) { return i == 0 ? v.x : v.y; }
+
+// softplus of two values with packed arithmetic; same method and bounds as
+// softplus_fast.
+__device__ __forceinline__ float2 softplus_fast2(float2 x) {
+    const float2 e = make_float2(ex2_approx(x.x * kLog2e), ex2_approx(x.y * kLog2e));
+    const float2 ope = add2(e, splat2(1.f));
+    const float2 via_log = mul2(splat2(kLn2), make_float2(lg2_approx(ope.x), lg2_approx(ope.y)));
+    const float2 poly = fma2(e, fma2(e, fma2(e, splat2(-0.25f), splat2(0.33333334f)), splat2(-0.5f)),
+                             splat2(1.f));
+    const float2 series = mul2(e, poly);
+    float2 r;
+    r.x = x.x > 15.f ? x.x : (e.x < 0.015625f ? series.x : via_log.x);
+    r.y = x.y > 15.f ? x.y : (e.y < 0.015625f ? series.y : via_log.y);
+    return r;
+}
+
+// silu of two values: z / (1 + 2^(-z log2 e)).
+__device__ __forceinline__ float2 silu_fast2(float2 z) {
+    const float2 nz = mul2(z, splat2(-kLog2e));
+    const float2 den = add2(make_float2(ex2_approx(nz.x), ex2_approx(nz.y)), splat2(1.f));
+    return mul2(z, make_float2(rcp_approx(den.x), rcp_approx(den.y)));
+}
+
+template <bool kFast>
+__device__ __forceinline__ float2 softplus_f2(float2 x) {
+    if constexpr (kFast) return softplus_fast2(x);
+    else return make_float2(softplus_acc(x.x), softplus_acc(x.y));
+}
+
+template <bool kFast>
+__device__ __forceinline__ float2 silu_f2(float2 z) {
+    if constexpr (kFast) return silu_fast2(z);
+    else return make_float2(silu_acc(z.x), silu_acc(z.y));
+}
+
 template <bool kFast>
 __device__ __forceinline__ float softplus_f(float x) {
     if constexpr (kFast) return softplus_fast(x);

@@ -9,103 +9,120 @@
 //     out   = (C . h + D x) * silu(z)
 //
 // The step is bound by HBM traffic on the state (2 * 4 * N bytes per
-// channel).  One thread owns one channel and all N of its states: N/4
-// independent 16-byte loads are in flight per thread, the per-channel terms
-// (softplus, silu, D x) are evaluated once, and y needs no cross-lane sum.
-// Consecutive threads take consecutive channels, so x/dt/z/out accesses are
-// coalesced and every byte of a warp's 32 * 4N-byte state block is used.
+// channel).  The state is walked as 16-byte quads (four states): quad i is
+// state words 4i..4i+3, i.e. channel i / Q, states 4 (i % Q) .. +3, with
+// Q = N / 4.  Thread t of a block handles quads base + j * THREADS + t for
+// j < J, so every warp-wide access touches 512 contiguous bytes; all J
+// quads (and their per-channel inputs) are loaded before any arithmetic so
+// J * 16 bytes of state per thread are in flight.  The Q lanes of a channel
+// are adjacent and add their partial C . h with xor shuffles.
 #include "ssm_internal.cuh"
 
 namespace ssm {
 namespace {
 
 constexpr int kThreads = 256;
+constexpr int kQuadsPerThread = 4;
+
+template <typename T>
+struct Quad;  // four consecutive activations of B or C
+template <>
+struct Quad<__nv_bfloat16> {
+    using type = uint2;
+    static __device__ __forceinline__ float4 f(type v) {
+        const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.x));
+        const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&v.y));
+        return make_float4(a.x, a.y, b.x, b.y);
+    }
+};
+template <>
+struct Quad<float> {
+    using type = float4;
+    static __device__ __forceinline__ float4 f(type v) { return v; }
+};
 
 template <typename T, int N, bool kFast, bool kVecBC>
 __global__ void __launch_bounds__(kThreads)
 state_update_kernel(UpdateArgs p) {
     static_assert(N % 4 == 0, "d_state must be a multiple of 4");
-    const int64_t bd = (int64_t)blockIdx.x * kThreads + threadIdx.x;
-    if (bd >= p.batch * p.dim) return;
-    const int64_t b = bd / p.dim, d = bd - b * p.dim;
+    constexpr int Q = N / 4;
+    constexpr int J = kQuadsPerThread;
+    const int64_t total = p.batch * p.dim * Q;
+    const int64_t base = (int64_t)blockIdx.x * (kThreads * J) + threadIdx.x;
+    const int q = threadIdx.x % Q;  // same for every j (kThreads is a multiple of Q)
 
-    float4* sp = reinterpret_cast<float4*>(p.state) + bd * (N / 4);
-    float4 s4[N / 4];
+    float4 s[J], a[J], bv[J], cv[J];
+    float xv[J], dl[J], zv[J], dd[J];
+    bool act[J];
 #pragma unroll
-    for (int q = 0; q < N / 4; ++q) s4[q] = sp[q];
+    for (int j = 0; j < J; ++j) {
+        const int64_t i = base + (int64_t)j * kThreads;
+        act[j] = i < total;
+        const int64_t ii = act[j] ? i : 0;   // inactive quads read quad 0 and store nothing
+        const int64_t bd = ii / Q;
+        const int64_t b = bd / p.dim, d = bd - b * p.dim;
+        s[j] = reinterpret_cast<const float4*>(p.state)[ii];
+        a[j] = reinterpret_cast<const float4*>(p.A)[d * Q + q];
+        const T* Bp = static_cast<const T*>(p.B) + b * N + 4 * q;
+        const T* Cp = static_cast<const T*>(p.C) + b * N + 4 * q;
+        if constexpr (kVecBC) {
+            bv[j] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Bp));
+            cv[j] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Cp));
+        } else {
+            bv[j] = make_float4(to_f32(Bp[0]), to_f32(Bp[1]), to_f32(Bp[2]), to_f32(Bp[3]));
+            cv[j] = make_float4(to_f32(Cp[0]), to_f32(Cp[1]), to_f32(Cp[2]), to_f32(Cp[3]));
+        }
+        xv[j] = to_f32(static_cast<const T*>(p.x)[bd]);
+        dl[j] = to_f32(static_cast<const T*>(p.dt)[bd]) + (p.dt_bias ? p.dt_bias[d] : 0.f);
+        zv[j] = p.z ? to_f32(static_cast<const T*>(p.z)[bd]) : 0.f;
+        dd[j] = p.D ? p.D[d] : 0.f;
+    }
 
-    const float xv = to_f32(static_cast<const T*>(p.x)[bd]);
-    float dl = to_f32(static_cast<const T*>(p.dt)[bd]);
-    if (p.dt_bias) dl += p.dt_bias[d];
-    if (p.softplus) dl = softplus_f<kFast>(dl);
-    const float gate = p.z ? silu_f<kFast>(to_f32(static_cast<const T*>(p.z)[bd])) : 1.f;
-    const float skip = p.D ? p.D[d] * xv : 0.f;
-    const float du = dl * xv;
-    const float dl2 = dl * kLog2e;
-
-    float Bv[N], Cv[N];
-    const T* Bp = static_cast<const T*>(p.B) + b * N;
-    const T* Cp = static_cast<const T*>(p.C) + b * N;
-    if constexpr (kVecBC) {
-        constexpr int kPer = 16 / sizeof(T);  // elements per 16-byte load
 #pragma unroll
-        for (int q = 0; q < N / kPer; ++q) {
-            const uint4 rb = reinterpret_cast<const uint4*>(Bp)[q];
-            const uint4 rc = reinterpret_cast<const uint4*>(Cp)[q];
-            const T* eb = reinterpret_cast<const T*>(&rb);
-            const T* ec = reinterpret_cast<const T*>(&rc);
+    for (int j = 0; j < J; ++j) {
+        const float dlt = p.softplus ? softplus_f<kFast>(dl[j]) : dl[j];
+        const float du = dlt * xv[j];
+        const float d2 = dlt * kLog2e;
+        const float hs[4] = {s[j].x, s[j].y, s[j].z, s[j].w};
+        const float av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
+        const float bb[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
+        const float cc[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
+        float h[4], y = 0.f;
 #pragma unroll
-            for (int j = 0; j < kPer; ++j) {
-                Bv[q * kPer + j] = to_f32(eb[j]);
-                Cv[q * kPer + j] = to_f32(ec[j]);
+        for (int k = 0; k < 4; ++k) {
+            const float dA = decay_exp2<kFast>(d2 * av[k]);
+            h[k] = fmaf(dA, hs[k], du * bb[k]);
+            y = fmaf(cc[k], h[k], y);
+        }
+#pragma unroll
+        for (int m = Q / 2; m >= 1; m >>= 1) y += __shfl_xor_sync(0xffffffffu, y, m);
+        const int64_t i = base + (int64_t)j * kThreads;
+        if (act[j]) {
+            reinterpret_cast<float4*>(p.state)[i] = make_float4(h[0], h[1], h[2], h[3]);
+            if (q == 0) {
+                const float gate = p.z ? silu_f<kFast>(zv[j]) : 1.f;
+                static_cast<T*>(p.out)[i / Q] = from_f32<T>((y + dd[j] * xv[j]) * gate);
             }
         }
-    } else {
-#pragma unroll
-        for (int n = 0; n < N; ++n) {
-            Bv[n] = to_f32(Bp[n]);
-            Cv[n] = to_f32(Cp[n]);
-        }
     }
-
-    const float4* ap = reinterpret_cast<const float4*>(p.A) + d * (N / 4);
-    float y = 0.f;
-#pragma unroll
-    for (int q = 0; q < N / 4; ++q) {
-        const float4 a = ap[q];
-        float h[4] = {s4[q].x, s4[q].y, s4[q].z, s4[q].w};
-        const float av[4] = {a.x, a.y, a.z, a.w};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float dA = decay_exp2<kFast>(dl2 * av[j]);
-            h[j] = fmaf(dA, h[j], du * Bv[4 * q + j]);
-            y = fmaf(Cv[4 * q + j], h[j], y);
-        }
-        s4[q] = make_float4(h[0], h[1], h[2], h[3]);
-    }
-#pragma unroll
-    for (int q = 0; q < N / 4; ++q) sp[q] = s4[q];
-    static_cast<T*>(p.out)[bd] = from_f32<T>((y + skip) * gate);
 }
 
 template <typename T, int N, bool kVec>
 cudaError_t launch_v(const UpdateArgs& a, cudaStream_t s) {
     constexpr bool kFast = !std::is_same<T, float>::value;
-    const int64_t total = a.batch * a.dim;
-    const int64_t blocks = (total + kThreads - 1) / kThreads;
+    const int64_t total = a.batch * a.dim * (N / 4);
+    const int64_t per_block = (int64_t)kThreads * kQuadsPerThread;
+    const int64_t blocks = (total + per_block - 1) / per_block;
     state_update_kernel<T, N, kFast, kVec><<<(unsigned)blocks, kThreads, 0, s>>>(a);
     return cudaGetLastError();
 }
 
 template <typename T, int N>
 cudaError_t launch_n(const UpdateArgs& a, cudaStream_t s) {
-    // 16-byte loads of a batch row's B and C need both rows 16-byte aligned.
-    const bool vec = (N * sizeof(T)) % 16 == 0 &&
-                     (reinterpret_cast<uintptr_t>(a.B) % 16) == 0 &&
-                     (reinterpret_cast<uintptr_t>(a.C) % 16) == 0;
-    if constexpr ((N * sizeof(T)) % 16 == 0) {
-        if (vec) return launch_v<T, N, true>(a, s);
-    }
+    // one vector load per quad of B / C needs both rows aligned to 4 elements
+    const uintptr_t al = 4 * sizeof(T);
+    const bool vec = (reinterpret_cast<uintptr_t>(a.B) % al) == 0 && (reinterpret_cast<uintptr_t>(a.C) % al) == 0;
+    if (vec) return launch_v<T, N, true>(a, s);
     return launch_v<T, N, false>(a, s);
 }
 

@@ -80,7 +80,7 @@ def check_state(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "last_
 
 
 # number of compiled scan layouts per d_state (selectable with SSM_SCAN_LAYOUT)
-LAYOUTS = {16: 8, 8: 4, 4: 4}
+LAYOUTS = {16: 7, 8: 4, 4: 2}
 
 
 @contextlib.contextmanager
