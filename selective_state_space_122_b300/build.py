@@ -1,9 +1,13 @@
-"""Build libssmscan.so (the C-ABI CUDA library) in-tree for sm_103a.
+"""Build the CUDA libraries in-tree for sm_103a.
 
     python -m selective_state_space_122_b300.build [--verbose]
 
-nvcc cross-compiles without a GPU.  The library statically links the CUDA
-runtime, so it only needs the driver at run time.
+* libssmscan.so -- the C-ABI selective-scan library (include/ssm_scan.h);
+* libssmpeak.so -- the arithmetic-unit throughput probes the benchmark uses
+  for its roofline denominators (not part of the scan path).
+
+nvcc cross-compiles without a GPU.  Both libraries statically link the CUDA
+runtime, so they only need the driver at run time.
 """
 from __future__ import annotations
 
@@ -16,6 +20,8 @@ PKG = os.path.dirname(os.path.abspath(__file__))
 ROOT = os.path.dirname(PKG)
 CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libssmscan.so")
+PEAK_LIB = os.path.join(PKG, "libssmpeak.so")
+PEAK_SOURCES = ["sfu_peak.cu"]
 SOURCES = ["ssm_api.cu", "scan_fwd.cu", "state_update.cu"]
 HEADERS = ["ssm_internal.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -33,25 +39,35 @@ def _inputs():
             + [os.path.join(ROOT, "include", "ssm_scan.h")])
 
 
-def up_to_date(out: str = LIB) -> bool:
+def up_to_date(out: str = LIB, inputs=None) -> bool:
     if not os.path.exists(out):
         return False
     t = os.path.getmtime(out)
-    return all(os.path.getmtime(p) <= t for p in _inputs())
+    return all(os.path.getmtime(p) <= t for p in (inputs or _inputs()))
 
 
-def build(out: str = LIB, verbose: bool = False, force: bool = False) -> str:
-    if not force and up_to_date(out):
-        return out
+def _nvcc(out: str, sources, verbose: bool) -> None:
     cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"),
            *(["-Xptxas", "-v"] if verbose else []),
-           "-o", out, *[os.path.join(CSRC, s) for s in SOURCES]]
+           "-o", out, *[os.path.join(CSRC, s) for s in sources]]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError("nvcc failed building libssmscan.so")
+        raise RuntimeError(f"nvcc failed building {os.path.basename(out)}")
     if verbose:
         sys.stderr.write(r.stderr)
+
+
+def build(out: str = LIB, verbose: bool = False, force: bool = False) -> str:
+    if force or not up_to_date(out):
+        _nvcc(out, SOURCES, verbose)
+    return out
+
+
+def build_peak(out: str = PEAK_LIB, verbose: bool = False, force: bool = False) -> str:
+    srcs = [os.path.join(CSRC, s) for s in PEAK_SOURCES]
+    if force or not up_to_date(out, srcs):
+        _nvcc(out, PEAK_SOURCES, verbose)
     return out
 
 
@@ -61,3 +77,4 @@ if __name__ == "__main__":
     ap.add_argument("--force", action="store_true")
     args = ap.parse_args()
     print(build(verbose=args.verbose, force=args.force or args.verbose))
+    print(build_peak(verbose=args.verbose, force=args.force or args.verbose))

@@ -1,0 +1,139 @@
+// sfu_peak.cu -- throughput probes for the arithmetic units the selective
+// scan leans on: the special-function unit (ex2, lg2, rcp) and the float32
+// pipe (packed f32x2 FMA).  Built into its own library (libssmpeak.so),
+// separate from the scan library; the benchmark uses it to measure the
+// denominators of the scan's arithmetic roofline on the GPU it runs on.
+//
+// Every probe runs `iters` iterations of U independent dependency chains per
+// thread, with enough resident warps to hide latency, so the result is the
+// unit's issue-limited throughput.  Each chain step is one instruction of the
+// probed kind plus, for the SFU probes, one float32 add that keeps the value
+// in a bounded range; the add goes to the float32 pipe and does not slow the
+// SFU unless issue itself binds.
+#include <cuda_runtime.h>
+
+#include <cstdint>
+
+#if defined(__GNUC__)
+#define PK_API extern "C" __attribute__((visibility("default")))
+#else
+#define PK_API extern "C"
+#endif
+
+namespace {
+
+constexpr int kU = 8;  // independent chains per thread
+
+__device__ __forceinline__ float ex2a(float x) {
+    float y;
+    asm volatile("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float lg2a(float x) {
+    float y;
+    asm volatile("lg2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+__device__ __forceinline__ float rcpa(float x) {
+    float y;
+    asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// kind 0: ex2, 1: lg2, 2: rcp.  x_{i+1} = f(x_i) - c keeps x in (-1, 0]
+// for ex2 (2^x in (0.5, 1]), in [1, 2) for lg2 (log2 in [0, 1), + 1) and
+// in [1, 2] for rcp (1/x in [0.5, 1], + 1).
+template <int kKind>
+__global__ void __launch_bounds__(256) sfu_kernel(float* sink, int iters, float seed) {
+    float v[kU];
+#pragma unroll
+    for (int i = 0; i < kU; ++i) v[i] = (kKind == 0 ? -0.25f : 1.25f) + seed * (threadIdx.x + i);
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < kU; ++i) {
+            if constexpr (kKind == 0) v[i] = ex2a(v[i]) - 1.0f;
+            else if constexpr (kKind == 1) v[i] = lg2a(v[i]) + 1.0f;
+            else v[i] = rcpa(v[i]) + 1.0f;
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kU; ++i) s += v[i];
+    if (s == 12345.678f) sink[threadIdx.x] = s;  // never true; keeps the chains live
+}
+
+// Packed float32 FMA throughput: each step is one fma.rn.f32x2 (two FMAs).
+__global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, float seed) {
+    unsigned long long v[kU];
+    const float a = 0.999f, b = 1e-3f;
+    unsigned long long A, Bq;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(A) : "f"(a), "f"(a));
+    asm("mov.b64 %0, {%1, %2};" : "=l"(Bq) : "f"(b), "f"(b));
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+        const float x = seed * (threadIdx.x + i);
+        asm("mov.b64 %0, {%1, %2};" : "=l"(v[i]) : "f"(x), "f"(x));
+    }
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < kU; ++i) asm volatile("fma.rn.f32x2 %0, %0, %1, %2;" : "+l"(v[i]) : "l"(A), "l"(Bq));
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+        float lo, hi;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v[i]));
+        s += lo + hi;
+    }
+    if (s == 12345.678f) sink[threadIdx.x] = s;
+}
+
+}  // namespace
+
+// Runs one probe and returns its throughput in operations per second
+// (ex2 / lg2 / rcp results, or scalar FMAs for kind 3), timed with CUDA
+// events around a single launch of `blocks_per_sm` x SM-count blocks of 256
+// threads.  Returns a negative value on any CUDA error.  Synchronises the
+// device; a measurement tool, not part of the scan path.
+PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1.0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1.0;
+    if (kind < 0 || kind > 3 || iters <= 0 || blocks_per_sm <= 0 || blocks_per_sm > 8) return -2.0;
+    float* sink = nullptr;
+    if (cudaMalloc(&sink, 256 * sizeof(float)) != cudaSuccess) return -1.0;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    const dim3 grid(sms * blocks_per_sm), block(256);
+    auto launch = [&]() {
+        switch (kind) {
+            case 0: sfu_kernel<0><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 1: sfu_kernel<1><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 2: sfu_kernel<2><<<grid, block>>>(sink, iters, 1e-7f); break;
+            default: ffma2_kernel<<<grid, block>>>(sink, iters, 1e-7f); break;
+        }
+    };
+    launch();  // warm-up
+    cudaEventRecord(e0);
+    launch();
+    cudaEventRecord(e1);
+    cudaEventSynchronize(e1);
+    float ms = 0.f;
+    const cudaError_t err = cudaEventElapsedTime(&ms, e0, e1);
+    const cudaError_t last = cudaGetLastError();
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaFree(sink);
+    if (err != cudaSuccess || last != cudaSuccess || ms <= 0.f) return -1.0;
+    const double per_thread = double(iters) * kU * (kind == 3 ? 2 : 1);
+    return per_thread * double(grid.x) * 256.0 / (ms * 1e-3);
+}
+
+// Number of SMs of the current device (so callers can normalise per SM).
+PK_API int ssmpk_sm_count(void) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
+    return sms;
+}
