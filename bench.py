@@ -36,14 +36,13 @@ from selective_state_space_122_b300 import inputs  # noqa: E402
 METRIC = "selective-scan elements (B·D·L·N)/s and achieved HBM GB/s vs roofline, 1 B300"
 SCAN = inputs.LONG_SEQ
 DECODE = inputs.DECODE_256
-# Special-function unit rates of a B300 SM, per clock (measured with a
-# dependent-chain microbenchmark: ex2 ~30/clk/SM, lg2/rcp/tanh ~15/clk/SM):
-EX2_PER_SM_PER_CLK = 32
-HALF_RATE_SFU_COST = 2            # lg2 and rcp occupy the unit twice as long as ex2
-# Transcendental work of the method per (b, t, d), in ex2-equivalents:
-#   N exps for exp(Delta A), softplus = exp + log, silu = exp + reciprocal.
-def sfu_ex2_equiv_per_td(n):
-    return (n + 2) + 2 * HALF_RATE_SFU_COST
+# Transcendental work of the method per (b, t, d): N exp2 for exp(Delta A),
+# softplus = exp2 + log2, silu = exp2 + reciprocal.  The rates of ex2, lg2 and
+# rcp are measured on the GPU by libssmpeak.so before the timed region.
+def sfu_ops_per_td(n):
+    return {"ex2": n + 2, "lg2": 1, "rcp": 1}
+
+
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "sm_max_mhz": 2032.0, "source": "fallback"}
 
 
@@ -61,9 +60,15 @@ def scan_bytes(s=SCAN, es=2):
             + s.dim * s.dstate * 4 + 2 * s.dim * 4 + s.batch * s.dim * s.dstate * 4)
 
 
-def scan_sfu_ops(s=SCAN):
-    """SFU work of one scan in ex2-equivalents (half-rate ops count twice)."""
-    return s.batch * s.seqlen * s.dim * sfu_ex2_equiv_per_td(s.dstate)
+def scan_sfu_seconds(rates, s=SCAN):
+    """Time the special-function unit alone needs for one scan at the measured rates."""
+    btd = s.batch * s.seqlen * s.dim
+    return sum(btd * k / rates[op] for op, k in sfu_ops_per_td(s.dstate).items())
+
+
+def scan_sfu_ex2_equiv(rates, s=SCAN):
+    """SFU work of one scan in ex2-equivalents: lg2 and rcp weighted by ex2_rate / their rate."""
+    return scan_sfu_seconds(rates, s) * rates["ex2"]
 
 
 def decode_elements(s=DECODE):
@@ -74,6 +79,26 @@ def decode_bytes(s=DECODE, es=2):
     """State read + written (fp32), x, dt, z read and out written, B, C, A, D, bias."""
     return (2 * s.batch * s.dim * s.dstate * 4 + 4 * s.batch * s.dim * es
             + 2 * s.batch * s.dstate * es + s.dim * s.dstate * 4 + 2 * s.dim * 4)
+
+
+def probe_units(device_index=0):
+    """Throughput of the special-function unit (ex2, lg2, rcp) and of packed
+    float32 FMA on this GPU, measured by libssmpeak.so (ops/s)."""
+    import ctypes
+    from selective_state_space_122_b300 import build as libbuild
+    path = libbuild.PEAK_LIB
+    if not os.path.exists(path):
+        return None
+    lib = ctypes.CDLL(path)
+    lib.ssmpk_probe.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int]
+    lib.ssmpk_probe.restype = ctypes.c_double
+    lib.ssmpk_sm_count.restype = ctypes.c_int
+    out = {}
+    for name, kind, iters in (("ex2", 0, 20000), ("lg2", 1, 10000), ("rcp", 2, 10000), ("ffma", 3, 40000)):
+        best = max(lib.ssmpk_probe(kind, iters, 4) for _ in range(3))
+        out[name] = best
+    out["sms"] = lib.ssmpk_sm_count()
+    return out
 
 
 def load_peaks():
@@ -200,6 +225,9 @@ def make_workload(device):
         "dec_host": (di, x, dt, z, B, C),
     }
     s = w["scan"]
+    from selective_state_space_122_b300 import scan_workspace_bytes
+    w["ws"] = torch.empty(scan_workspace_bytes(SCAN.batch, SCAN.dim, SCAN.seqlen, SCAN.dstate, torch.bfloat16),
+                          dtype=torch.uint8, device=device)
     w["scan_out"] = torch.empty_like(s["u"])
     w["scan_last"] = torch.empty((SCAN.batch, SCAN.dim, SCAN.dstate), dtype=torch.float32, device=device)
     w["dec_out"] = torch.empty_like(w["dec"]["x"])
@@ -213,7 +241,7 @@ def run_step(w, ev=None):
     if ev is not None:
         ev[0].record()
     ssm_scan_fwd(s["u"], s["delta"], s["A"], s["B"], s["C"], s["D"], s["z"], s["delta_bias"], True,
-                 out=w["scan_out"], last_state=w["scan_last"])
+                 out=w["scan_out"], last_state=w["scan_last"], workspace=w["ws"])
     if ev is not None:
         ev[1].record()
     ssm_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"], d["dt_bias"],
@@ -247,7 +275,8 @@ def run_e2e(w, steps, device):
         for k in dd:
             dd[k].copy_(hd[k], non_blocking=True)
         o, last = ssm_scan_fwd(ds["u"], ds["delta"], ds["A"], ds["B"], ds["C"], ds["D"], ds["z"],
-                               ds["delta_bias"], True, out=w["scan_out"], last_state=w["scan_last"])
+                               ds["delta_bias"], True, out=w["scan_out"], last_state=w["scan_last"],
+                               workspace=w["ws"])
         y = ssm_state_update(dd["state"], dd["x"], dd["dt"], dd["A"], dd["B"], dd["C"], dd["D"], dd["z"],
                              dd["dt_bias"], True, out=w["dec_out"])
         out_h.copy_(o, non_blocking=True)
@@ -299,6 +328,8 @@ def bench_ours(args):
     dist_init(world, "nccl")
     from selective_state_space_122_b300 import load_library
     load_library()
+    units = probe_units(local)
+    clocks_mhz_for_units = load_peaks()["sm_max_mhz"]   # per-clock figures are at the maximum SM clock
     w = make_workload(device)
     torch.cuda.synchronize()
 
@@ -345,10 +376,12 @@ def bench_ours(args):
     elems = (scan_elements() + decode_elements()) * world
     scan_avg = statistics.mean(scan_ms)
     dec_avg = statistics.mean(dec_ms)
-    sfu_peak = sms * EX2_PER_SM_PER_CLK * peaks["sm_max_mhz"] * 1e6      # ex2-equivalents/s
-    sfu_ach = scan_sfu_ops() / (scan_avg * 1e-3)
+    t_sfu = scan_sfu_seconds(units)
+    t_hbm = scan_bytes() / (peaks["hbm_gbs"] * 1e9)
+    sfu_equiv = scan_sfu_ex2_equiv(units)
+    sfu_ach = sfu_equiv / (scan_avg * 1e-3)
     hbm_ach = scan_bytes() / (scan_avg * 1e-3) / 1e9
-    t_roof_ms = max(scan_bytes() / (peaks["hbm_gbs"] * 1e9), scan_sfu_ops() / sfu_peak) * 1e3
+    t_roof_ms = max(t_hbm, t_sfu) * 1e3
     line = {
         "metric": METRIC,
         "value": elems / (ms_step * 1e-3),
@@ -376,18 +409,23 @@ def bench_ours(args):
             "bound": "alu",
             "unit": "G ex2-equiv/s",
             "achieved": sfu_ach / 1e9,
-            "peak": sfu_peak / 1e9,
-            "frac": sfu_ach / sfu_peak,
+            "peak": units["ex2"] / 1e9,
+            "frac": sfu_ach / units["ex2"],
             "traffic": None,
-            "kernel": "scan_fwd_kernel (long-sequence scan)",
-            "peak_source": (f"derived: {sms} SMs x {EX2_PER_SM_PER_CLK} ex2/clk x "
-                            f"{peaks['sm_max_mhz']:.0f} MHz max SM clock; work counted in ex2-equivalents "
-                            f"({sfu_ex2_equiv_per_td(SCAN.dstate)} per (b,t,d): N+2 ex2, log and "
-                            f"reciprocal at half rate)"),
-            "sfu_ex2_equiv_per_launch": scan_sfu_ops(),
+            "kernel": "ssm_scan_fwd: bc_stage_kernel + scan_relay_kernel (long-sequence scan)",
+            "peak_source": ("measured on this GPU by libssmpeak.so: ex2 %.1f, lg2 %.1f, rcp %.1f G/s, "
+                            "packed FMA %.1f TFLOP/s; SFU work per (b,t,d): N+2 ex2, 1 lg2, 1 rcp, "
+                            "lg2/rcp weighted by ex2_rate/their rate"
+                            % (units["ex2"] / 1e9, units["lg2"] / 1e9, units["rcp"] / 1e9,
+                               2 * units["ffma"] / 1e12)),
+            "sfu_ex2_equiv_per_launch": sfu_equiv,
+            "sfu_per_sm_per_clk": {k: units[k] / (sms * clocks_mhz_for_units * 1e6)
+                                   for k in ("ex2", "lg2", "rcp", "ffma")},
             "hbm": {"achieved_gbs": hbm_ach, "peak_gbs": peaks["hbm_gbs"],
                     "frac": hbm_ach / peaks["hbm_gbs"], "bytes_per_launch": scan_bytes(),
                     "peak_source": peaks["source"]},
+            "t_sfu_ms": t_sfu * 1e3,
+            "t_hbm_ms": t_hbm * 1e3,
             "t_roof_ms": t_roof_ms,
             "frac_of_roofline_time": t_roof_ms / scan_avg,
         },
@@ -398,7 +436,7 @@ def bench_ours(args):
             "frac_hbm": decode_bytes() / (dec_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
         },
         "clocks": clocks,
-        "gpu_launches": 2 * args.steps,
+        "gpu_launches": 3 * args.steps,
     }
     if e2e is not None:
         e2e_ms, h2d, d2h = e2e

@@ -99,6 +99,14 @@ typedef enum ssm_dtype {
  *   out         [batch][seqlen][dim]     dtype   written once (never read)
  *   last_state  [batch][dim][dstate]     f32     h after the last step;
  *                                                NULL = not written
+ *   workspace   device scratch, 16-byte aligned, workspace_bytes long, owned
+ *               by the caller; may be NULL (workspace_bytes 0).  With at least
+ *               ssm_scan_workspace_bytes(...) bytes the fast path runs (TMA
+ *               staging and the warp relay along the sequence); it also
+ *               needs 16-byte aligned u/delta/z/out/A/last_state and
+ *               dim * sizeof(dtype) a multiple of 16.  Otherwise a generic
+ *               kernel with the same results runs.  The workspace is
+ *               overwritten; it must not overlap any other argument.
  *
  * Returns SSM_OK once the work is enqueued on `stream`.
  */
@@ -107,7 +115,26 @@ SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A
                         const void* z, const float* delta_bias, int softplus_flag,
                         void* out, float* last_state,
                         int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
-                        int dtype, void* stream);
+                        int dtype, void* workspace, int64_t workspace_bytes, void* stream);
+
+/*
+ * ssm_scan_workspace_bytes -- bytes of workspace the fast path of
+ * ssm_scan_fwd needs for these sizes (batch * round_up(seqlen, 8) * 2 *
+ * dstate * 4: B and C staged as float32 rows).  Returns -1 for sizes or a
+ * dtype that ssm_scan_fwd would reject.  Pure host computation.
+ */
+SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                         int dtype);
+
+/*
+ * ssm_device_error -- the library's device error word: 0 if no kernel has
+ * reported a problem, otherwise a bit set (1: a staged-data wait timed out,
+ * 2: a state hand-off between warps timed out; the affected outputs are then
+ * incomplete).  Waits in the kernels are bounded (about one second), so a
+ * kernel never spins forever.  nonzero `clear` resets the word.  Reads device
+ * memory, so it synchronises with the device; -1 if the read fails.
+ */
+SSM_API int ssm_device_error(int clear);
 
 /*
  * ssm_state_update -- one token of recurrent (constant-memory) inference.

@@ -8,7 +8,8 @@ Public calls (thin wrappers over the C ABI in include/ssm_scan.h):
 The CUDA library ``libssmscan.so`` is loaded on first use; there is no CPU
 fallback.
 """
-from ._lib import (SSMError, load_library, ssm_scan_fwd, ssm_state_update,  # noqa: F401
-                   status_string)
+from ._lib import (SSMError, device_error, load_library, scan_workspace_bytes,  # noqa: F401
+                   ssm_scan_fwd, ssm_state_update, status_string)
 
-__all__ = ["ssm_scan_fwd", "ssm_state_update", "load_library", "status_string", "SSMError"]
+__all__ = ["ssm_scan_fwd", "ssm_state_update", "scan_workspace_bytes", "device_error",
+           "load_library", "status_string", "SSMError"]

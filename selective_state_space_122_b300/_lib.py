@@ -21,7 +21,8 @@ SSM_BF16 = 1
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN",
           4: "SSM_ERR_UNSUPPORTED", 5: "SSM_ERR_DTYPE", 6: "SSM_ERR_ALIAS",
           7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE"}
-EXPORTS = ("ssm_scan_fwd", "ssm_state_update", "ssm_status_string", "ssm_version")
+EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
+           "ssm_status_string", "ssm_version")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -43,8 +44,12 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib = ctypes.CDLL(path)
     vp, fp, i64, ci = ctypes.c_void_p, ctypes.c_void_p, ctypes.c_int64, ctypes.c_int
     lib.ssm_scan_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
-                                 i64, i64, i64, i64, ci, vp]
+                                 i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_fwd.restype = ci
+    lib.ssm_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
+    lib.ssm_scan_workspace_bytes.restype = i64
+    lib.ssm_device_error.argtypes = [ci]
+    lib.ssm_device_error.restype = ci
     lib.ssm_state_update.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, vp,
                                      i64, i64, i64, ci, ci, vp]
     lib.ssm_state_update.restype = ci
@@ -92,16 +97,30 @@ def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
+def scan_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, dtype: torch.dtype) -> int:
+    """Workspace bytes the fast path of ssm_scan_fwd needs (ssm_scan_workspace_bytes)."""
+    code = SSM_BF16 if dtype == torch.bfloat16 else SSM_F32
+    return int(load_library().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, code))
+
+
+def device_error(clear: bool = True) -> int:
+    """The library's device error word (0 = no kernel reported a problem); synchronises."""
+    return int(load_library().ssm_device_error(int(bool(clear))))
+
+
 def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor,
                  C: torch.Tensor, D: Optional[torch.Tensor] = None, z: Optional[torch.Tensor] = None,
                  delta_bias: Optional[torch.Tensor] = None, softplus: bool = True,
                  out: Optional[torch.Tensor] = None, last_state: Optional[torch.Tensor] = None,
-                 return_last_state: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                 return_last_state: bool = False,
+                 workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Selective scan over (batch, L, dim) activations; see ssm_scan.h.
 
     B, C: (batch, dstate, L); A: (dim, dstate) f32; D, delta_bias: (dim,) f32.
     Returns (out, last_state); last_state is (batch, dim, dstate) f32 when
-    requested (pass a buffer or set return_last_state).
+    requested (pass a buffer or set return_last_state).  ``workspace`` is a
+    uint8 CUDA tensor of at least scan_workspace_bytes(...) bytes; when None
+    one is allocated here (through PyTorch's caching allocator).
     """
     lib = load_library()
     dt = u.dtype
@@ -112,13 +131,17 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
         out = torch.empty_like(u)
     if last_state is None and return_last_state:
         last_state = torch.empty((bt, dim, N), dtype=torch.float32, device=dev)
+    if workspace is None:
+        nbytes = scan_workspace_bytes(bt, dim, L, N, dt)
+        workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes > 0 else None
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
         code = lib.ssm_scan_fwd(_ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev),
                                 _ptr(B, dt, dev), _ptr(C, dt, dev), _ptr(D, torch.float32, dev),
                                 _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
                                 int(bool(softplus)), _ptr(out, dt, dev),
                                 _ptr(last_state, torch.float32, dev), bt, dim, L, N,
-                                _dtype_code(u), _stream(dev))
+                                _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
     _check("ssm_scan_fwd", code)
     return out, last_state
 

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstdint>
 #include <cstdlib>
+#include <cstring>
 
 #include "../../include/ssm_scan.h"
 #include "ssm_internal.cuh"
@@ -105,10 +106,21 @@ const char* ssm_status_string(int status) {
 
 int ssm_version(void) { return 100; }
 
+int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
+    (void)dim;
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
+    if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
+        return -1;
+    return ssm::relay_workspace_bytes(batch, seqlen, (int)dstate);
+}
+
+int ssm_device_error(int clear) { return ssm::read_device_error(clear != 0); }
+
 ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                         const void* C, const float* D, const void* z, const float* delta_bias,
                         int softplus_flag, void* out, float* last_state, int64_t batch,
-                        int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* stream) {
+                        int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* workspace,
+                        int64_t workspace_bytes, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
@@ -131,14 +143,34 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
         if (overlap(so, s) || overlap(sl, s)) return SSM_ERR_ALIAS;
     if (overlap(so, sl)) return SSM_ERR_ALIAS;
 
+    if (workspace_bytes < 0 || (workspace && workspace_bytes == 0)) return SSM_ERR_SHAPE;
+    if (workspace) {
+        if (!aligned(workspace, 16)) return SSM_ERR_ALIGN;
+        const Span sw{workspace, workspace_bytes};
+        for (const Span& s : ins)
+            if (overlap(sw, s)) return SSM_ERR_ALIAS;
+        if (overlap(sw, so) || overlap(sw, sl)) return SSM_ERR_ALIAS;
+    }
+
     int sms = 0;
     if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
 
     ssm::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, out, last_state,
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
+    const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
+    const cudaStream_t st = static_cast<cudaStream_t>(stream);
+    // The relay path runs whenever its layout and workspace requirements
+    // hold; SSM_SCAN_PATH=generic forces the generic kernel (tests use it).
+    const char* force = std::getenv("SSM_SCAN_PATH");
+    const bool want_generic = force && std::strcmp(force, "generic") == 0;
+    if (!want_generic && workspace && workspace_bytes >= ssm::relay_workspace_bytes(batch, seqlen, (int)dstate) &&
+        ssm::relay_supported(a, dt)) {
+        const cudaError_t e = ssm::launch_scan_relay(a, dt, workspace, st);
+        return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    }
+    if (force && std::strcmp(force, "relay") == 0) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
-    const cudaError_t e = ssm::launch_scan_fwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
-                                               plan, static_cast<cudaStream_t>(stream));
+    const cudaError_t e = ssm::launch_scan_fwd(a, dt, plan, st);
     return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
 }
 

@@ -59,6 +59,14 @@ struct ScanPlan {
     int layout;  // index into the compiled layouts for this d_state
 };
 
+// Fast path (scan_relay.cu): warp relay over TMA-staged chunks.  Needs a
+// float32 workspace for the staged B and C (relay_workspace_bytes).
+int64_t relay_lpad(int64_t seqlen);
+int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate);
+bool relay_supported(const ScanArgs& a, DType dt);
+cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cudaStream_t s);
+int read_device_error(bool clear);
+
 int scan_layout_count(int dstate);
 ScanLayoutInfo scan_layout_info(int dstate, int layout);
 cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s);

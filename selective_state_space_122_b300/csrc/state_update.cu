@@ -9,20 +9,21 @@
 //     out   = (C . h + D x) * silu(z)
 //
 // The step is bound by HBM traffic on the state (2 * 4 * N bytes per
-// channel).  The state is walked as 16-byte quads (four states): quad i is
-// state words 4i..4i+3, i.e. channel i / Q, states 4 (i % Q) .. +3, with
-// Q = N / 4.  Thread t of a block handles quads base + j * THREADS + t for
-// j < J, so every warp-wide access touches 512 contiguous bytes; all J
-// quads (and their per-channel inputs) are loaded before any arithmetic so
-// J * 16 bytes of state per thread are in flight.  The Q lanes of a channel
-// are adjacent and add their partial C . h with xor shuffles.
+// channel).  One thread owns one (batch, channel): it streams the channel's N
+// float32 states in as 16-byte vectors, computes the per-channel terms
+// (softplus, Delta x, D x, silu(z)) once, updates the states with one SFU
+// exp2 each, and streams them back.  A block covers 32 consecutive channels
+// of 8 batch rows, so x/dt/z/out accesses are 64-byte coalesced runs, the
+// state of a warp is one contiguous 2 KB run, and each row of A is reused by
+// the block's 8 batch rows from L1.  State loads and stores use the
+// streaming (evict-first) cache policy: each state is touched once per step.
 #include "ssm_internal.cuh"
 
 namespace ssm {
 namespace {
 
-constexpr int kThreads = 256;
-constexpr int kQuadsPerThread = 4;
+constexpr int kDX = 32;   // channels per block
+constexpr int kBY = 8;    // batch rows per block
 
 template <typename T>
 struct Quad;  // four consecutive activations of B or C
@@ -42,78 +43,64 @@ struct Quad<float> {
 };
 
 template <typename T, int N, bool kFast, bool kVecBC>
-__global__ void __launch_bounds__(kThreads)
+__global__ void __launch_bounds__(kDX * kBY)
 state_update_kernel(UpdateArgs p) {
     static_assert(N % 4 == 0, "d_state must be a multiple of 4");
     constexpr int Q = N / 4;
-    constexpr int J = kQuadsPerThread;
-    const int64_t total = p.batch * p.dim * Q;
-    const int64_t base = (int64_t)blockIdx.x * (kThreads * J) + threadIdx.x;
-    const int q = threadIdx.x % Q;  // same for every j (kThreads is a multiple of Q)
+    const int64_t d = (int64_t)blockIdx.x * kDX + threadIdx.x;
+    const int64_t b = (int64_t)blockIdx.y * kBY + threadIdx.y;
+    if (d >= p.dim || b >= p.batch) return;
+    const int64_t bd = b * p.dim + d;
 
-    float4 s[J], a[J], bv[J], cv[J];
-    float xv[J], dl[J], zv[J], dd[J];
-    bool act[J];
+    float4* st = reinterpret_cast<float4*>(p.state) + bd * Q;
+    const float4* Ar = reinterpret_cast<const float4*>(p.A) + d * Q;
+    const T* Bp = static_cast<const T*>(p.B) + b * N;
+    const T* Cp = static_cast<const T*>(p.C) + b * N;
+    float4 s[Q], a[Q], bv[Q], cv[Q];
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const int64_t i = base + (int64_t)j * kThreads;
-        act[j] = i < total;
-        const int64_t ii = act[j] ? i : 0;   // inactive quads read quad 0 and store nothing
-        const int64_t bd = ii / Q;
-        const int64_t b = bd / p.dim, d = bd - b * p.dim;
-        s[j] = reinterpret_cast<const float4*>(p.state)[ii];
-        a[j] = reinterpret_cast<const float4*>(p.A)[d * Q + q];
-        const T* Bp = static_cast<const T*>(p.B) + b * N + 4 * q;
-        const T* Cp = static_cast<const T*>(p.C) + b * N + 4 * q;
+    for (int q = 0; q < Q; ++q) s[q] = __ldcs(st + q);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) a[q] = __ldg(Ar + q);
+#pragma unroll
+    for (int q = 0; q < Q; ++q) {
         if constexpr (kVecBC) {
-            bv[j] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Bp));
-            cv[j] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Cp));
+            bv[q] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Bp + 4 * q));
+            cv[q] = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Cp + 4 * q));
         } else {
-            bv[j] = make_float4(to_f32(Bp[0]), to_f32(Bp[1]), to_f32(Bp[2]), to_f32(Bp[3]));
-            cv[j] = make_float4(to_f32(Cp[0]), to_f32(Cp[1]), to_f32(Cp[2]), to_f32(Cp[3]));
+            bv[q] = make_float4(to_f32(Bp[4 * q]), to_f32(Bp[4 * q + 1]), to_f32(Bp[4 * q + 2]), to_f32(Bp[4 * q + 3]));
+            cv[q] = make_float4(to_f32(Cp[4 * q]), to_f32(Cp[4 * q + 1]), to_f32(Cp[4 * q + 2]), to_f32(Cp[4 * q + 3]));
         }
-        xv[j] = to_f32(static_cast<const T*>(p.x)[bd]);
-        dl[j] = to_f32(static_cast<const T*>(p.dt)[bd]) + (p.dt_bias ? p.dt_bias[d] : 0.f);
-        zv[j] = p.z ? to_f32(static_cast<const T*>(p.z)[bd]) : 0.f;
-        dd[j] = p.D ? p.D[d] : 0.f;
     }
+    const float xv = to_f32(static_cast<const T*>(p.x)[bd]);
+    float dl = to_f32(static_cast<const T*>(p.dt)[bd]) + (p.dt_bias ? __ldg(p.dt_bias + d) : 0.f);
+    const float zv = p.z ? to_f32(static_cast<const T*>(p.z)[bd]) : 0.f;
+    const float dd = p.D ? __ldg(p.D + d) : 0.f;
 
+    if (p.softplus) dl = softplus_f<kFast>(dl);
+    const float2 du2 = splat2(dl * xv);
+    const float2 d2 = splat2(dl * kLog2e);
+    float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
-    for (int j = 0; j < J; ++j) {
-        const float dlt = p.softplus ? softplus_f<kFast>(dl[j]) : dl[j];
-        const float du = dlt * xv[j];
-        const float d2 = dlt * kLog2e;
-        const float hs[4] = {s[j].x, s[j].y, s[j].z, s[j].w};
-        const float av[4] = {a[j].x, a[j].y, a[j].z, a[j].w};
-        const float bb[4] = {bv[j].x, bv[j].y, bv[j].z, bv[j].w};
-        const float cc[4] = {cv[j].x, cv[j].y, cv[j].z, cv[j].w};
-        float h[4], y = 0.f;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-            const float dA = decay_exp2<kFast>(d2 * av[k]);
-            h[k] = fmaf(dA, hs[k], du * bb[k]);
-            y = fmaf(cc[k], h[k], y);
-        }
-#pragma unroll
-        for (int m = Q / 2; m >= 1; m >>= 1) y += __shfl_xor_sync(0xffffffffu, y, m);
-        const int64_t i = base + (int64_t)j * kThreads;
-        if (act[j]) {
-            reinterpret_cast<float4*>(p.state)[i] = make_float4(h[0], h[1], h[2], h[3]);
-            if (q == 0) {
-                const float gate = p.z ? silu_f<kFast>(zv[j]) : 1.f;
-                static_cast<T*>(p.out)[i / Q] = from_f32<T>((y + dd[j] * xv[j]) * gate);
-            }
-        }
+    for (int q = 0; q < Q; ++q) {
+        const float2 e0 = mul2(d2, make_float2(a[q].x, a[q].y));
+        const float2 e1 = mul2(d2, make_float2(a[q].z, a[q].w));
+        const float2 dA0 = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
+        const float2 dA1 = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
+        const float2 h0 = fma2(dA0, make_float2(s[q].x, s[q].y), mul2(du2, make_float2(bv[q].x, bv[q].y)));
+        const float2 h1 = fma2(dA1, make_float2(s[q].z, s[q].w), mul2(du2, make_float2(bv[q].z, bv[q].w)));
+        acc = fma2(make_float2(cv[q].x, cv[q].y), h0, acc);
+        acc = fma2(make_float2(cv[q].z, cv[q].w), h1, acc);
+        __stcs(st + q, make_float4(h0.x, h0.y, h1.x, h1.y));
     }
+    const float gate = p.z ? silu_f<kFast>(zv) : 1.f;
+    static_cast<T*>(p.out)[bd] = from_f32<T>((acc.x + acc.y + dd * xv) * gate);
 }
 
 template <typename T, int N, bool kVec>
 cudaError_t launch_v(const UpdateArgs& a, cudaStream_t s) {
     constexpr bool kFast = !std::is_same<T, float>::value;
-    const int64_t total = a.batch * a.dim * (N / 4);
-    const int64_t per_block = (int64_t)kThreads * kQuadsPerThread;
-    const int64_t blocks = (total + per_block - 1) / per_block;
-    state_update_kernel<T, N, kFast, kVec><<<(unsigned)blocks, kThreads, 0, s>>>(a);
+    const dim3 grid((unsigned)((a.dim + kDX - 1) / kDX), (unsigned)((a.batch + kBY - 1) / kBY));
+    state_update_kernel<T, N, kFast, kVec><<<grid, dim3(kDX, kBY), 0, s>>>(a);
     return cudaGetLastError();
 }
 
@@ -128,6 +115,7 @@ cudaError_t launch_n(const UpdateArgs& a, cudaStream_t s) {
 
 template <typename T>
 cudaError_t launch_t(const UpdateArgs& a, cudaStream_t s) {
+    if (a.batch > 65535LL * kBY) return cudaErrorInvalidValue;
     switch (a.dstate) {
         case 4: return launch_n<T, 4>(a, s);
         case 8: return launch_n<T, 8>(a, s);

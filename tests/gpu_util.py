@@ -41,11 +41,12 @@ def host_f64(t: torch.Tensor) -> np.ndarray:
 
 
 def scan_on_gpu(inp: inputs.ScanInputs, want_state=True):
-    from selective_state_space_122_b300 import ssm_scan_fwd
+    from selective_state_space_122_b300 import device_error, ssm_scan_fwd
     u, dl, z, B, C = (dev(x) for x in (inp.u, inp.delta, inp.z, inp.B, inp.C))
     out, last = ssm_scan_fwd(u, dl, dev(inp.A), B, C, dev(inp.D), z, dev(inp.delta_bias),
                              inp.softplus, return_last_state=want_state)
     torch.cuda.synchronize()
+    assert device_error() == 0, "a scan kernel reported a timed-out wait"
     return out, last
 
 
@@ -79,22 +80,41 @@ def check_state(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "last_
         assert rel <= STATE_REL, f"{what}: relative L2 error {rel:.3e} > 1e-3"
 
 
-# number of compiled scan layouts per d_state (selectable with SSM_SCAN_LAYOUT)
+# number of compiled generic-kernel layouts per d_state (selectable with SSM_SCAN_LAYOUT)
 LAYOUTS = {16: 7, 8: 4, 4: 2}
+
+
+def relay_ok(dim: int, dtype: str) -> bool:
+    """Whether the relay (fast) path accepts this channel count: rows of
+    dim elements must be a multiple of 16 bytes for the TMA tensor maps."""
+    return (dim * (2 if dtype == inputs.BF16 else 4)) % 16 == 0
+
+
+def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
+    """Every way to run a scan of this shape: the relay path (when it accepts
+    the shape) and each generic layout."""
+    return (["relay"] if relay_ok(dim, dtype) else []) + list(range(LAYOUTS[N]))
 
 
 @contextlib.contextmanager
 def scan_layout(layout):
-    """Force one compiled scan layout (None = the library's own plan)."""
-    old = os.environ.get("SSM_SCAN_LAYOUT")
-    if layout is None:
-        os.environ.pop("SSM_SCAN_LAYOUT", None)
-    else:
+    """Force a path: None = the library's own choice, "relay" = the relay
+    kernel (an error if it cannot take the shape), an int = that layout of
+    the generic kernel."""
+    keys = ("SSM_SCAN_LAYOUT", "SSM_SCAN_PATH")
+    old = {k: os.environ.get(k) for k in keys}
+    for k in keys:
+        os.environ.pop(k, None)
+    if layout == "relay":
+        os.environ["SSM_SCAN_PATH"] = "relay"
+    elif layout is not None:
+        os.environ["SSM_SCAN_PATH"] = "generic"
         os.environ["SSM_SCAN_LAYOUT"] = str(layout)
     try:
         yield
     finally:
-        if old is None:
-            os.environ.pop("SSM_SCAN_LAYOUT", None)
-        else:
-            os.environ["SSM_SCAN_LAYOUT"] = old
+        for k, v in old.items():
+            if v is None:
+                os.environ.pop(k, None)
+            else:
+                os.environ[k] = v

@@ -54,7 +54,8 @@ MB = 1 << 20
 def scan_args(**kw):
     a = dict(u=P, delta=P + 64 * MB, A=P + 128 * MB, B=P + 192 * MB, C=P + 256 * MB, D=P + 320 * MB,
              z=P + 384 * MB, delta_bias=P + 448 * MB, softplus=1, out=P + 512 * MB,
-             last_state=P + 576 * MB, batch=2, dim=64, seqlen=128, dstate=16, dtype=1, stream=None)
+             last_state=P + 576 * MB, batch=2, dim=64, seqlen=128, dstate=16, dtype=1,
+             workspace=None, workspace_bytes=0, stream=None)
     a.update(kw)
     return a
 
@@ -62,7 +63,8 @@ def scan_args(**kw):
 def call_scan(lib, a):
     return lib.ssm_scan_fwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
                             a["delta_bias"], a["softplus"], a["out"], a["last_state"], a["batch"],
-                            a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["stream"])
+                            a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["workspace"],
+                            a["workspace_bytes"], a["stream"])
 
 
 @pytest.mark.parametrize("kw,code", [
@@ -76,6 +78,9 @@ def call_scan(lib, a):
     (dict(dtype=0, z=P + 384 * MB + 2), 3), (dict(last_state=P + 576 * MB + 2), 3),
     (dict(out=P + 1024), 6), (dict(out=P + 256 * MB), 6), (dict(last_state=P + 512 * MB + 64), 6),
     (dict(last_state=P + 128 * MB), 6),
+    (dict(workspace=P + 640 * MB, workspace_bytes=-1), 2), (dict(workspace=P + 640 * MB), 2),
+    (dict(workspace=P + 640 * MB + 8, workspace_bytes=MB), 3),
+    (dict(workspace=P + 1024, workspace_bytes=MB), 6), (dict(workspace=P + 510 * MB, workspace_bytes=4 * MB), 6),
 ])
 def test_scan_rejects_bad_arguments(lib, kw, code):
     assert call_scan(lib, scan_args(**kw)) == code
@@ -117,3 +122,13 @@ def test_binding_raises_without_cuda_tensors():
     B = torch.zeros(1, 4, 8)
     with pytest.raises(ValueError):
         _lib.ssm_scan_fwd(u, u, A, B, B)
+
+
+def test_workspace_size_query(lib):
+    # batch * round_up(seqlen, 8) * 2 * dstate * 4 bytes (B and C staged as float32 rows)
+    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 131072 * 2 * 16 * 4
+    assert lib.ssm_scan_workspace_bytes(3, 7, 77, 8, 0) == 3 * 80 * 2 * 8 * 4
+    assert lib.ssm_scan_workspace_bytes(1, 1, 1, 4, 1) == 8 * 2 * 4 * 4
+    assert lib.ssm_scan_workspace_bytes(1, 64, 64, 5, 1) == -1
+    assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
+    assert lib.ssm_scan_workspace_bytes(1, 64, 64, 16, 7) == -1

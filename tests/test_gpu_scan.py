@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (LAYOUTS, check_out, check_state, dev, host_f64, scan_layout, scan_on_gpu,
+from gpu_util import (LAYOUTS, check_out, check_state, dev, host_f64, paths, scan_layout, scan_on_gpu,
                       state_rel_err)
 from selective_state_space_122_b300 import inputs, ssm_scan_fwd
 
@@ -24,13 +24,13 @@ def oracle_of(inp: inputs.ScanInputs, channels=None):
                        f["delta_bias"], f["softplus"])
 
 
-def layouts(N):
-    return list(range(LAYOUTS[N]))
+def layouts(N, dim=64, dtype=inputs.BF16):
+    return paths(N, dim, dtype)
 
 
 # ------------------------------------------------------------ the five workloads
 
-@pytest.mark.parametrize("g", [None] + list(range(LAYOUTS[4])))
+@pytest.mark.parametrize("g", [None, "relay"] + list(range(LAYOUTS[4])))
 def test_tiny_f32_against_golden(g):
     inp = inputs.make_scan_inputs(inputs.TINY_F32, 0)
     with scan_layout(g):
@@ -47,7 +47,7 @@ def layer130m():
     return inp, oracle_of(inp)
 
 
-@pytest.mark.parametrize("g", [None] + list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("g", [None, "relay"] + list(range(LAYOUTS[16])))
 def test_layer130m_full(layer130m, g):
     inp, (ref, ref_last) = layer130m
     with scan_layout(g):
@@ -92,7 +92,7 @@ def test_random_A_all_layouts(dtype, N):
     shape = inputs.ScanShape("randA", 2, 96, 300, N, dtype)
     inp = inputs.make_scan_inputs(shape, 10 + N, random_a=True)
     ref, ref_last = oracle_of(inp)
-    for g in layouts(N):
+    for g in layouts(N, shape.dim, dtype):
         with scan_layout(g):
             out, last = scan_on_gpu(inp)
         check_out(host_f64(out), ref, dtype, f"out layout {g}")
@@ -115,7 +115,7 @@ def test_optional_inputs(dtype, opts):
         if inp.delta_bias is not None:
             inp.delta_bias = np.random.default_rng(1).uniform(1e-3, 2e-2, shape.dim).astype(np.float32)
     ref, ref_last = oracle_of(inp)
-    for g in layouts(16):
+    for g in layouts(16, shape.dim, dtype):
         with scan_layout(g):
             out, last = scan_on_gpu(inp)
         check_out(host_f64(out), ref, dtype, f"out layout {g}")
@@ -128,30 +128,45 @@ def test_ragged_shapes(bt, dim, L, N):
     for dtype in (inputs.F32, inputs.BF16):
         inp = inputs.make_scan_inputs(inputs.ScanShape("ragged", bt, dim, L, N, dtype), dim + L)
         ref, ref_last = oracle_of(inp)
-        for g in layouts(N):
+        for g in layouts(N, dim, dtype):
             with scan_layout(g):
                 out, last = scan_on_gpu(inp)
             check_out(host_f64(out), ref, dtype, f"out layout {g}")
             check_state(host_f64(last), ref_last, dtype, f"state layout {g}")
 
 
-@pytest.mark.parametrize("g", list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
+@pytest.mark.parametrize("bt,dim,L,N", [(1, 8, 1, 16), (2, 24, 77, 8), (3, 40, 65, 4), (1, 16, 7, 16),
+                                         (2, 72, 200, 16), (1, 48, 9, 8), (2, 8, 1000, 16)])
+def test_relay_ragged(bt, dim, L, N, dtype):
+    """The relay path on sequence ends that are not whole chunks, units whose
+    last channels fall beyond dim, and sequences shorter than one chunk."""
+    inp = inputs.make_scan_inputs(inputs.ScanShape("relay-ragged", bt, dim, L, N, dtype), 7 * dim + L)
+    ref, ref_last = oracle_of(inp)
+    with scan_layout("relay"):
+        out, last = scan_on_gpu(inp)
+    check_out(host_f64(out), ref, dtype)
+    check_state(host_f64(last), ref_last, dtype)
+
+
+@pytest.mark.parametrize("g", ["relay"] + list(range(LAYOUTS[16])))
 def test_writes_stay_in_bounds(g):
     """Outputs and the final state sit between guard words that must survive."""
-    shape = inputs.ScanShape("guard", 2, 45, 70, 16, inputs.BF16)
+    dim = 48 if g == "relay" else 45     # the relay path needs 16-byte rows
+    shape = inputs.ScanShape("guard", 2, dim, 70, 16, inputs.BF16)
     inp = inputs.make_scan_inputs(shape, 30)
-    n_out = 2 * 70 * 45
+    n_out = 2 * 70 * dim
     guard = 4096
     buf = torch.full((n_out + 2 * guard,), 12345.0, dtype=torch.bfloat16, device="cuda")
-    out = buf[guard:guard + n_out].view(2, 70, 45)
-    sbuf = torch.full((2 * 45 * 16 + 2 * guard,), -7.0, dtype=torch.float32, device="cuda")
-    last = sbuf[guard:guard + 2 * 45 * 16].view(2, 45, 16)
+    out = buf[guard:guard + n_out].view(2, 70, dim)
+    sbuf = torch.full((2 * dim * 16 + 2 * guard,), -7.0, dtype=torch.float32, device="cuda")
+    last = sbuf[guard:guard + 2 * dim * 16].view(2, dim, 16)
     with scan_layout(g):
         ssm_scan_fwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D),
                      dev(inp.z), dev(inp.delta_bias), True, out=out, last_state=last)
     torch.cuda.synchronize()
     assert bool((buf[:guard] == 12345.0).all()) and bool((buf[guard + n_out:] == 12345.0).all())
-    assert bool((sbuf[:guard] == -7.0).all()) and bool((sbuf[guard + 2 * 45 * 16:] == -7.0).all())
+    assert bool((sbuf[:guard] == -7.0).all()) and bool((sbuf[guard + 2 * dim * 16:] == -7.0).all())
     ref, ref_last = oracle_of(inp)
     check_out(host_f64(out), ref, inputs.BF16)
     check_state(host_f64(last), ref_last, inputs.BF16)
