@@ -102,7 +102,8 @@ typedef enum ssm_dtype {
  *   workspace   device scratch, 16-byte aligned, workspace_bytes long, owned
  *               by the caller; may be NULL (workspace_bytes 0).  With at least
  *               ssm_scan_workspace_bytes(...) bytes the fast path runs (TMA
- *               staging and the warp relay along the sequence); it also
+ *               staging; each warp scans a group of channels through
+ *               segments of the sequence, chained through the workspace); it also
  *               needs 16-byte aligned u/delta/z/out/A/last_state and
  *               dim * sizeof(dtype) a multiple of 16.  Otherwise a generic
  *               kernel with the same results runs.  The workspace is
@@ -119,9 +120,13 @@ SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A
 
 /*
  * ssm_scan_workspace_bytes -- bytes of workspace the fast path of
- * ssm_scan_fwd needs for these sizes (batch * round_up(seqlen, 8) * 2 *
- * dstate * 4: B and C staged as float32 rows).  Returns -1 for sizes or a
- * dtype that ssm_scan_fwd would reject.  Pure host computation.
+ * ssm_scan_fwd needs for these sizes: B and C staged as float32 rows
+ * (batch * round_up(seqlen, 32) * 2 * dstate * 4 bytes), then, for the
+ * segmented scan, the state handed between segments of each chain
+ * (chains * cw * dstate * 4, cw = 128 / dstate channels per chain,
+ * chains = batch * ceil(dim / cw)) and one int flag per chain, each part
+ * rounded up to 256 bytes.  Returns -1 for sizes or a dtype that
+ * ssm_scan_fwd would reject.  Pure host computation.
  */
 SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                          int dtype);
@@ -129,7 +134,8 @@ SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seq
 /*
  * ssm_device_error -- the library's device error word: 0 if no kernel has
  * reported a problem, otherwise a bit set (1: a staged-data wait timed out,
- * 2: a state hand-off between warps timed out; the affected outputs are then
+ * 2: a state hand-off between warps of a CTA timed out, 4: a state hand-off
+ * between sequence segments timed out; the affected outputs are then
  * incomplete).  Waits in the kernels are bounded (about one second), so a
  * kernel never spins forever.  nonzero `clear` resets the word.  Reads device
  * memory, so it synchronises with the device; -1 if the read fails.
@@ -162,6 +168,10 @@ SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
 
 /* Static, human-readable name of a status code (never NULL). */
 SSM_API const char* ssm_status_string(int status);
+
+/* The CUDA runtime's message for the calling thread's most recent
+ * SSM_ERR_LAUNCH (a static string; "no launch error" if there was none). */
+SSM_API const char* ssm_last_launch_error(void);
 
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 SSM_API int ssm_version(void);

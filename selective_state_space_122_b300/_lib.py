@@ -22,7 +22,7 @@ STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN"
           4: "SSM_ERR_UNSUPPORTED", 5: "SSM_ERR_DTYPE", 6: "SSM_ERR_ALIAS",
           7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
-           "ssm_status_string", "ssm_version")
+           "ssm_status_string", "ssm_last_launch_error", "ssm_version")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -55,6 +55,8 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_state_update.restype = ci
     lib.ssm_status_string.argtypes = [ci]
     lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_last_launch_error.argtypes = []
+    lib.ssm_last_launch_error.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []
     lib.ssm_version.restype = ci
     if path == LIB_PATH:
@@ -68,7 +70,10 @@ def status_string(code: int) -> str:
 
 def _check(fn: str, code: int) -> None:
     if code != 0:
-        raise SSMError(fn, code, status_string(code))
+        msg = status_string(code)
+        if code == 7:   # SSM_ERR_LAUNCH: add the CUDA runtime's own message
+            msg += f" [{load_library().ssm_last_launch_error().decode()}]"
+        raise SSMError(fn, code, msg)
 
 
 def _dtype_code(t: torch.Tensor) -> int:

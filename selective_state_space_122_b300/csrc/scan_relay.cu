@@ -47,6 +47,8 @@
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
+#include <algorithm>
+#include <cmath>
 #include <cstdint>
 #include <type_traits>
 
@@ -203,6 +205,7 @@ struct RelayCfg {
     static constexpr int CARRY = CW * N * 4;
     static constexpr int OFF_BAR = OFF_CARRY + W * CARRY;                // full[W][P], carry[W]
     static constexpr int SMEM = OFF_BAR + (W * P + W) * 8;
+    static_assert(SMEM <= 227 * 1024, "a CTA's shared memory must fit an SM");
 };
 
 struct RelayParams {
@@ -489,12 +492,360 @@ scan_relay_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     if (lane == 0) bulk_wait_all();
 }
 
+// ===================================================================
+// Segmented direct scan: one warp scans CW channels straight through
+// K-step chunks; every (batch, unit) chain is cut into S segments that
+// different warps take in turn, so the work divides evenly over all warps.
+// ===================================================================
+
+__device__ __forceinline__ float tanh_approx(float x) {
+    float y;
+    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
+
+// silu(z) = z * sigmoid(z) = (z/2) * (1 + tanh(z/2)): one SFU operation.
+// tanh.approx has an absolute error below 2^-10.9, so the gate is accurate to
+// about 5e-4 * |z| / 2 -- below the rounding of a bfloat16 output.
+template <bool kFast>
+__device__ __forceinline__ float2 seg_silu2(float2 z) {
+    if constexpr (kFast) {
+        const float2 hz = mul2(z, splat2(0.5f));
+        const float2 t = make_float2(tanh_approx(hz.x), tanh_approx(hz.y));
+        return fma2(hz, t, hz);
+    } else {
+        return make_float2(silu_acc(z.x), silu_acc(z.y));
+    }
+}
+
+template <typename T, int N_>
+struct SegCfg {
+    static constexpr int N = N_;
+    static constexpr int G = 4;                 // states per lane
+    static constexpr int R = N / G;             // lanes per channel
+    static constexpr int CW = 32 / R;           // channels per warp
+    // steps per chunk: 32, or 16 where 32-step float32 tiles of 32 channels
+    // would not fit four warps' rings in shared memory
+    static constexpr int K = (N == 4 && sizeof(T) == 4) ? 16 : 32;
+    static constexpr int P = 3;                 // chunks in flight per warp
+    static constexpr int WARPS = 4;             // independent workers per CTA (one per scheduler)
+    static constexpr int THREADS = 32 * WARPS;
+    static constexpr int KR = K / R;            // prologue items / finished steps per lane
+    static constexpr int ES = (int)sizeof(T);
+    static constexpr int TILE = K * CW * ES;
+    static constexpr int BC = K * 2 * N * 4;
+    static constexpr int align128(int x) { return (x + 127) / 128 * 128; }
+    static constexpr int SLOT_U = 0;
+    static constexpr int SLOT_D = align128(TILE);
+    static constexpr int SLOT_Z = SLOT_D + align128(TILE);
+    static constexpr int SLOT_BC = SLOT_Z + align128(TILE);
+    static constexpr int SLOT = align128(SLOT_BC + BC);
+    static constexpr int RS2 = 34;              // float2 stride of a step-pair row of the reduction buffer
+    static constexpr int W_RING = 0;
+    static constexpr int W_DP = W_RING + P * SLOT;                       // [K][CW] float4
+    static constexpr int W_RED = W_DP + K * CW * 16;                      // [K/2][RS2] float2
+    static constexpr int W_OUT = W_RED + (R > 1 ? align128((K / 2) * RS2 * 8) : 0);
+    static constexpr int OUT = align128(TILE);
+    static constexpr int W_BAR = W_OUT + 3 * OUT;
+    static constexpr int WARP_BYTES = align128(W_BAR + P * 8);
+    static constexpr int SMEM = WARPS * WARP_BYTES;
+    static_assert(SMEM <= 227 * 1024, "a CTA's shared memory must fit an SM");
+    static_assert(K % 8 == 0 && 32 % K == 0, "chunks tile the 32-step padded sequence");
+};
+
+struct SegParams {
+    const float* A;
+    const float* D;
+    const float* delta_bias;
+    const float* bc;        // staged B|C, [batch][lpad][2N] f32
+    float* last_state;
+    float* seg_state;       // [M][CW][N] f32: state handed between segments
+    int* seg_flag;          // [M]: number of finished segments of each chain
+    int dim, seqlen;
+    int64_t lpad;
+    int units;              // channel groups per batch row
+    int M;                  // chains = batch * units
+    int S;                  // segments per chain
+    int cps;                // chunks per segment
+    int workers;            // warps in the grid
+};
+
+__device__ __forceinline__ int ld_acquire(const int* p) {
+    int v;
+    asm volatile("ld.acquire.gpu.global.s32 %0, [%1];" : "=r"(v) : "l"(p) : "memory");
+    return v;
+}
+
+__device__ __forceinline__ void st_release(int* p, int v) {
+    asm volatile("st.release.gpu.global.s32 [%0], %1;" ::"l"(p), "r"(v) : "memory");
+}
+
+// Wait until *flag >= want; false after ~1 s.
+__device__ __forceinline__ bool flag_wait(const int* flag, int want) {
+    if (ld_acquire(flag) >= want) return true;
+    const unsigned long long t0 = globaltimer();
+    while (ld_acquire(flag) < want)
+        if (globaltimer() - t0 > kWaitLimitNs) return false;
+    return true;
+}
+
+template <typename T, int N, bool kFast, bool kSoftplus, bool kGate>
+__global__ void __launch_bounds__(SegCfg<T, N>::THREADS)
+scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
+                const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
+                const SegParams p) {
+    using CF = SegCfg<T, N>;
+    constexpr int K = CF::K, P = CF::P, R = CF::R, CW = CF::CW, KR = CF::KR, RS2 = CF::RS2;
+    extern __shared__ __align__(128) unsigned char smem[];
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int ch = lane / R, g = lane % R;
+    unsigned char* wbase = smem + warp * CF::WARP_BYTES;
+    float4* dp = reinterpret_cast<float4*>(wbase + CF::W_DP);
+    float2* red = reinterpret_cast<float2*>(wbase + CF::W_RED);
+    const uint32_t ring_s = smem_u32(wbase + CF::W_RING);
+    const uint32_t bar_full = smem_u32(wbase + CF::W_BAR);
+
+    const int L = p.seqlen;
+    const int nch = (L + K - 1) / K;
+    const int T_total = p.M * p.S;
+    const int wid = blockIdx.x * CF::WARPS + warp;
+
+    if (lane == 0) {
+        for (int i = 0; i < P; ++i) mbar_init(bar_full + 8u * i, 1);
+        fence_mbar_init();
+    }
+    __syncwarp();
+
+    constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
+    // Chunk stream of this warp: its tasks wid, wid + workers, ... in order, each
+    // task's chunks in order.  Lane 0 prefetches P chunks ahead along it.
+    int pf_task = wid, pf_c = 0, pf_end = 0, issued = 0;
+    auto task_span = [&](int task, int& cb, int& ce) {
+        const int sgm = task / p.M;
+        cb = sgm * p.cps;
+        ce = min(cb + p.cps, nch);
+    };
+    if (pf_task < T_total) task_span(pf_task, pf_c, pf_end);
+    auto issue_next = [&]() {   // lane 0 only; false once the stream is exhausted
+        while (pf_task < T_total && pf_c >= pf_end) {
+            pf_task += p.workers;
+            if (pf_task < T_total) task_span(pf_task, pf_c, pf_end);
+        }
+        if (pf_task >= T_total) return false;
+        const int m = pf_task % p.M;
+        const int bb = m / p.units, dd0 = (m - bb * p.units) * CW;
+        const int slot = issued % P;
+        const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
+        const uint32_t bar = bar_full + 8u * (uint32_t)slot;
+        const int t0 = pf_c * K;
+        mbar_expect_tx(bar, tx_bytes);
+        tma_load_3d(base + CF::SLOT_U, &tm_u, dd0, t0, bb, bar);
+        tma_load_3d(base + CF::SLOT_D, &tm_d, dd0, t0, bb, bar);
+        if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, dd0, t0, bb, bar);
+        bulk_load(base + CF::SLOT_BC, p.bc + ((size_t)bb * p.lpad + t0) * (2 * N), CF::BC, bar);
+        ++pf_c;
+        ++issued;
+        return true;
+    };
+    if (lane == 0)
+        for (int i = 0; i < P; ++i) issue_next();
+
+    int consumed = 0;   // chunks waited for (every lane tracks it)
+    int oslot = 0;
+    bool ok = true;
+    for (int task = wid; task < T_total && ok; task += p.workers) {
+        const int sgm = task / p.M, m = task - sgm * p.M;
+        const int b = m / p.units;
+        const int d0 = (m - b * p.units) * CW;
+        const int d = d0 + ch;
+        const bool ch_ok = d < p.dim;
+        const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
+
+        float2 A2[2];
+        {
+            const float4 a = ch_ok ? *reinterpret_cast<const float4*>(p.A + (size_t)d * N + 4 * g)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            A2[0] = make_float2(a.x * kLog2e, a.y * kLog2e);
+            A2[1] = make_float2(a.z * kLog2e, a.w * kLog2e);
+        }
+        const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
+        const float2 dskip2 = splat2((p.D && ch_ok) ? p.D[d] : 0.f);
+
+        // state entering the segment
+        float2 h0 = make_float2(0.f, 0.f), h1 = make_float2(0.f, 0.f);
+        float* hst = p.seg_state + ((size_t)m * CW + ch) * N + 4 * g;
+        if (sgm > 0) {
+            if (!__all_sync(0xffffffffu, flag_wait(p.seg_flag + m, sgm))) {
+                ok = false;
+                if (lane == 0) raise_error(4u);
+                break;
+            }
+            const float4 v = __ldcg(reinterpret_cast<const float4*>(hst));
+            h0 = make_float2(v.x, v.y);
+            h1 = make_float2(v.z, v.w);
+        }
+
+        for (int c = cb; c < ce; ++c) {
+            const int slot = consumed % P;
+            const unsigned char* sb = wbase + CF::W_RING + slot * CF::SLOT;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * (uint32_t)slot, (uint32_t)((consumed / P) & 1)))) {
+                ok = false;
+                if (lane == 0) raise_error(1u);
+                break;
+            }
+            ++consumed;
+            const int t0 = c * K;
+            const bool tail = t0 + K > L;
+
+            // ---- per-(t, d) terms of this lane's KR steps, as NP step pairs.
+            // Lane g owns steps g*KR .. g*KR+KR-1; it visits its pairs in an
+            // order rotated by g, so the R lanes of a channel read rows that
+            // fall in different banks (register index j is fixed, only the
+            // addresses rotate).
+            constexpr int NP = KR / 2;
+            const T* su = reinterpret_cast<const T*>(sb + CF::SLOT_U);
+            const T* sd = reinterpret_cast<const T*>(sb + CF::SLOT_D);
+            const T* sz = reinterpret_cast<const T*>(sb + CF::SLOT_Z);
+            float2 uk[NP], gate[NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int ta = g * KR + 2 * ((j + g) % NP), tb = ta + 1;
+                const float2 uv = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
+                const float2 xr = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
+                float2 dl = add2(xr, bias2);
+                if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
+                if (tail) dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + tb < L ? 1.f : 0.f));
+                const float2 du = mul2(dl, uv);
+                uk[j] = uv;
+                if constexpr (kGate) {
+                    const float2 zv = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
+                    gate[j] = seg_silu2<kFast>(zv);
+                } else {
+                    gate[j] = splat2(1.f);
+                }
+                dp[ta * CW + ch] = make_float4(dl.x, dl.x, du.x, du.x);
+                dp[tb * CW + ch] = make_float4(dl.y, dl.y, du.y, du.y);
+            }
+            __syncwarp();
+
+            // ---- the recurrence, in batches of KB steps: (A) exp(Delta A) and
+            // Delta B u of a batch, independent of the state; (B) the state
+            // chain; (C) the per-lane readout C . h.  A of batch b+1 is issued
+            // before B and C of batch b, so the SFU work of the next batch
+            // overlaps the dependent chain of this one.
+            const float* sbc = reinterpret_cast<const float*>(sb + CF::SLOT_BC);
+            constexpr int KB = 8, NB = K / KB;
+            float2 dA[2][KB][2], dB[2][KB][2];
+            float2 ys[R == 1 ? K / 2 : 1];
+            auto phaseA = [&](int bt, int buf) {
+#pragma unroll
+                for (int t = 0; t < KB; ++t) {
+                    const int tt = bt * KB + t;
+                    const float4 q = dp[tt * CW + ch];
+                    const float4 bq = *reinterpret_cast<const float4*>(sbc + tt * (2 * N) + 4 * g);
+                    const float2 e0 = mul2(make_float2(q.x, q.y), A2[0]);
+                    const float2 e1 = mul2(make_float2(q.x, q.y), A2[1]);
+                    dA[buf][t][0] = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
+                    dA[buf][t][1] = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
+                    dB[buf][t][0] = mul2(make_float2(q.z, q.w), make_float2(bq.x, bq.y));
+                    dB[buf][t][1] = mul2(make_float2(q.z, q.w), make_float2(bq.z, bq.w));
+                }
+            };
+            phaseA(0, 0);
+#pragma unroll
+            for (int bt = 0; bt < NB; ++bt) {
+                const int cur = bt & 1;
+                if (bt + 1 < NB) phaseA(bt + 1, cur ^ 1);
+#pragma unroll
+                for (int t = 0; t < KB; ++t) {
+                    h0 = fma2(dA[cur][t][0], h0, dB[cur][t][0]);
+                    h1 = fma2(dA[cur][t][1], h1, dB[cur][t][1]);
+                    dB[cur][t][0] = h0;
+                    dB[cur][t][1] = h1;
+                }
+#pragma unroll
+                for (int t = 0; t < KB; t += 2) {
+                    const int tt = bt * KB + t;
+                    const float4 c0 = *reinterpret_cast<const float4*>(sbc + tt * (2 * N) + N + 4 * g);
+                    const float4 c1 = *reinterpret_cast<const float4*>(sbc + (tt + 1) * (2 * N) + N + 4 * g);
+                    const float2 a0 = fma2(make_float2(c0.z, c0.w), dB[cur][t][1],
+                                           mul2(make_float2(c0.x, c0.y), dB[cur][t][0]));
+                    const float2 a1 = fma2(make_float2(c1.z, c1.w), dB[cur][t + 1][1],
+                                           mul2(make_float2(c1.x, c1.y), dB[cur][t + 1][0]));
+                    const float2 s2 = make_float2(a0.x + a0.y, a1.x + a1.y);
+                    if constexpr (R == 1) ys[tt / 2] = s2;
+                    else red[(tt / 2) * RS2 + lane] = s2;
+                }
+            }
+
+            // ---- sum the R lanes of each channel for this lane's pairs (same rotation)
+            float2 yv[NP];
+            if constexpr (R == 1) {
+#pragma unroll
+                for (int j = 0; j < NP; ++j) yv[j] = ys[j];
+            } else {
+                __syncwarp();
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    const float2* row = red + (g * NP + (j + g) % NP) * RS2 + ch * R;
+                    float2 sum = row[0];
+#pragma unroll
+                    for (int gg = 1; gg < R; ++gg) sum = add2(sum, row[gg]);
+                    yv[j] = sum;
+                }
+            }
+
+            // ---- D skip, gate, output tile (triple-buffered; lane 0 owns the TMA store groups)
+            T* so = reinterpret_cast<T*>(wbase + CF::W_OUT + oslot * CF::OUT);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                const int ta = g * KR + 2 * ((j + g) % NP);
+                const float2 y = mul2(fma2(dskip2, uk[j], yv[j]), gate[j]);
+                st_pair<T>(so + ta * CW + ch, so + (ta + 1) * CW + ch, y);
+            }
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) {
+                tma_store_3d(&tm_out, d0, t0, b, smem_u32(so));
+                bulk_commit();
+                issue_next();
+                bulk_wait_read<1>();
+            }
+            oslot = oslot == 2 ? 0 : oslot + 1;
+        }
+        if (!ok) break;
+
+        // state leaving the segment
+        if (sgm + 1 < p.S) {
+            __stcg(reinterpret_cast<float4*>(hst), make_float4(h0.x, h0.y, h1.x, h1.y));
+            __threadfence();
+            __syncwarp();
+            if (lane == 0) st_release(p.seg_flag + m, sgm + 1);
+        } else if (p.last_state && ch_ok) {
+            *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) =
+                make_float4(h0.x, h0.y, h1.x, h1.y);
+        }
+    }
+
+    // Drain: every issued load must land before shared memory is released.
+    if (!ok) {
+        const int iss = __shfl_sync(0xffffffffu, issued, 0);
+        for (int j = consumed; j < iss; ++j)
+            if (!mbar_wait(bar_full + 8u * (uint32_t)(j % P), (uint32_t)((j / P) & 1))) break;
+    }
+    if (lane == 0) bulk_wait_all();
+}
+
 // B and C (batch, N, L) -> staged float32 rows [batch][lpad][B_0..B_{N-1}, C_0..C_{N-1}],
 // zero beyond L.  One CTA per (64-step tile, batch row), transposed through shared memory.
 template <typename T, int N>
 __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, const T* __restrict__ C,
-                                                       float* __restrict__ bc, int64_t L, int64_t lpad) {
+                                                       float* __restrict__ bc, int64_t L, int64_t lpad,
+                                                       int* __restrict__ flags, int nflags) {
     constexpr int TT = 64;
+    if (flags && blockIdx.x == 0 && blockIdx.y == 0)
+        for (int i = threadIdx.x; i < nflags; i += blockDim.x) flags[i] = 0;
     __shared__ float tile[TT][2 * N + 1];
     const int64_t b = blockIdx.y;
     const int64_t t0 = (int64_t)blockIdx.x * TT;
@@ -554,7 +905,7 @@ cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
     {
         dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)a.batch);
         bc_stage_kernel<T, N><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
-                                                   a.seqlen, lpad);
+                                                   a.seqlen, lpad, nullptr, 0);
     }
     CUtensorMap mu, md, mz, mo;
     if (!make_map<T>(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
@@ -582,9 +933,131 @@ cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
     return cudaGetLastError();
 }
 
+// Work split of the segmented scan for one call.
+struct SegPlan {
+    int units, M, S, cps, workers, grid;
+};
+
+template <int N, int K>
+SegPlan seg_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms, int ctas_per_sm) {
+    constexpr int CW = 32 / (N / 4), WARPS = 4;
+    SegPlan pl{};
+    pl.units = (int)((dim + CW - 1) / CW);
+    pl.M = (int)(batch * pl.units);
+    const int nch = (int)((seqlen + K - 1) / K);
+    const int per_wave = sms * WARPS;
+    if (pl.M < per_wave) {
+        // fewer chains than schedulers: one task per chain
+        pl.grid = (pl.M + WARPS - 1) / WARPS;
+        pl.workers = pl.grid * WARPS;
+        pl.S = 1;
+        pl.cps = nch;
+        return pl;
+    }
+    int k = pl.M / per_wave;                       // warps per scheduler, at most what fits
+    if (k > ctas_per_sm) k = ctas_per_sm;
+    if (k < 1) k = 1;
+    pl.grid = sms * k;
+    pl.workers = pl.grid * WARPS;
+    // Segments per chain: the most even split of M * S tasks over the workers,
+    // with segments of at least four chunks and at most 64 segments.
+    int bestS = 1;
+    double best = 1e30;
+    const int smax = std::max(1, std::min(64, nch / 4));
+    for (int S = 1; S <= smax; ++S) {
+        const int cps = (nch + S - 1) / S;
+        const int s_eff = (nch + cps - 1) / cps;
+        const double tasks = double(pl.M) * s_eff / pl.workers;        // tasks per worker (mean)
+        const double slots = std::ceil(tasks);                           // the busiest worker
+        const double cost = slots * cps;                                 // chunks on the critical worker
+        if (cost < best * 0.999) {
+            best = cost;
+            bestS = S;
+        }
+    }
+    pl.cps = (nch + bestS - 1) / bestS;
+    pl.S = (nch + pl.cps - 1) / pl.cps;
+    return pl;
+}
+
+template <typename T, int N>
+cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
+    using CF = SegCfg<T, N>;
+    constexpr bool kFast = !std::is_same<T, float>::value;
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, SegParams);
+    static const Kern kerns[4] = {scan_seg_kernel<T, N, kFast, false, false>,
+                                  scan_seg_kernel<T, N, kFast, false, true>,
+                                  scan_seg_kernel<T, N, kFast, true, false>,
+                                  scan_seg_kernel<T, N, kFast, true, true>};
+    const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
+    static int occ[4] = {0, 0, 0, 0};
+    if (occ[which] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        if (o < 1) return cudaErrorInvalidConfiguration;
+        occ[which] = o;
+    }
+    const SegPlan pl = seg_plan<N, CF::K>(a.batch, a.dim, a.seqlen, sms, occ[which]);
+    const int64_t lpad = relay_lpad(a.seqlen);
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    float* bc = reinterpret_cast<float*>(w);
+    const int64_t bc_bytes = (a.batch * lpad * 2 * N * 4 + 255) / 256 * 256;
+    float* st = reinterpret_cast<float*>(w + bc_bytes);
+    const int64_t st_bytes = ((int64_t)pl.M * CF::CW * N * 4 + 255) / 256 * 256;
+    int* flags = reinterpret_cast<int*>(w + bc_bytes + st_bytes);
+    {
+        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)a.batch);
+        bc_stage_kernel<T, N><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
+                                                   a.seqlen, lpad, flags, pl.M);
+    }
+    CUtensorMap mu, md, mz, mo;
+    if (!make_map<T>(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
+        !make_map<T>(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
+        !make_map<T>(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
+        !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
+        return cudaErrorInvalidValue;
+    SegParams sp{a.A, a.D, a.delta_bias, bc, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
+                 pl.units, pl.M, pl.S, pl.cps, pl.workers};
+    void* args[] = {&mu, &md, &mz, &mo, &sp};
+    // Segments wait on segments of other warps: every CTA must be resident,
+    // which the cooperative launch guarantees (the grid never exceeds the
+    // occupancy the plan was sized with).
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
+                                       dim3(CF::THREADS), args, CF::SMEM, s);
+}
+
 }  // namespace
 
-int64_t relay_lpad(int64_t seqlen) { return (seqlen + 7) / 8 * 8; }
+int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
+    const int cw = 32 / (dstate / 4);
+    const int64_t units = (dim + cw - 1) / cw;
+    const int64_t M = batch * units;
+    const int64_t bc_bytes = (batch * relay_lpad(seqlen) * 2 * dstate * 4 + 255) / 256 * 256;
+    const int64_t st_bytes = (M * cw * dstate * 4 + 255) / 256 * 256;
+    return bc_bytes + st_bytes + (M * 4 + 255) / 256 * 256;
+}
+
+cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* ws, int sms, cudaStream_t s) {
+    if (dt == DType::F32) {
+        switch (a.dstate) {
+            case 4: return launch_seg_t<float, 4>(a, ws, sms, s);
+            case 8: return launch_seg_t<float, 8>(a, ws, sms, s);
+            case 16: return launch_seg_t<float, 16>(a, ws, sms, s);
+        }
+    } else {
+        switch (a.dstate) {
+            case 4: return launch_seg_t<__nv_bfloat16, 4>(a, ws, sms, s);
+            case 8: return launch_seg_t<__nv_bfloat16, 8>(a, ws, sms, s);
+            case 16: return launch_seg_t<__nv_bfloat16, 16>(a, ws, sms, s);
+        }
+    }
+    return cudaErrorInvalidValue;
+}
+
+int64_t relay_lpad(int64_t seqlen) { return (seqlen + 31) / 32 * 32; }
 
 int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate) {
     return batch * relay_lpad(seqlen) * 2 * dstate * (int64_t)sizeof(float);

@@ -23,6 +23,7 @@
 namespace {
 
 constexpr int kU = 8;  // independent chains per thread
+int g_threads = 256;   // block size of the next probe launch
 
 __device__ __forceinline__ float ex2a(float x) {
     float y;
@@ -59,7 +60,7 @@ __global__ void __launch_bounds__(256) sfu_kernel(float* sink, int iters, float 
     float s = 0.f;
 #pragma unroll
     for (int i = 0; i < kU; ++i) s += v[i];
-    if (s == 12345.678f) sink[threadIdx.x] = s;  // never true; keeps the chains live
+    if (s == 12345.678f) sink[threadIdx.x & 255] = s;  // never true; keeps the chains live
 }
 
 // Packed float32 FMA throughput: each step is one fma.rn.f32x2 (two FMAs).
@@ -85,10 +86,15 @@ __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, floa
         asm("mov.b64 {%0, %1}, %2;" : "=f"(lo), "=f"(hi) : "l"(v[i]));
         s += lo + hi;
     }
-    if (s == 12345.678f) sink[threadIdx.x] = s;
+    if (s == 12345.678f) sink[threadIdx.x & 255] = s;
 }
 
 }  // namespace
+
+// Same as ssmpk_probe but with an explicit block shape: `blocks_per_sm` x SM
+// count blocks of `threads` threads (a multiple of 32, at most 256), for
+// measuring how throughput depends on the number of warps per scheduler.
+PK_API double ssmpk_probe_shape(int kind, int iters, int blocks_per_sm, int threads);
 
 // Runs one probe and returns its throughput in operations per second
 // (ex2 / lg2 / rcp results, or scalar FMAs for kind 3), timed with CUDA
@@ -105,7 +111,7 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
     cudaEvent_t e0, e1;
     cudaEventCreate(&e0);
     cudaEventCreate(&e1);
-    const dim3 grid(sms * blocks_per_sm), block(256);
+    const dim3 grid(sms * blocks_per_sm), block(g_threads);
     auto launch = [&]() {
         switch (kind) {
             case 0: sfu_kernel<0><<<grid, block>>>(sink, iters, 1e-7f); break;
@@ -127,7 +133,15 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
     cudaFree(sink);
     if (err != cudaSuccess || last != cudaSuccess || ms <= 0.f) return -1.0;
     const double per_thread = double(iters) * kU * (kind == 3 ? 2 : 1);
-    return per_thread * double(grid.x) * 256.0 / (ms * 1e-3);
+    return per_thread * double(grid.x) * double(g_threads) / (ms * 1e-3);
+}
+
+PK_API double ssmpk_probe_shape(int kind, int iters, int blocks_per_sm, int threads) {
+    if (threads <= 0 || threads > 256 || threads % 32 != 0) return -2.0;
+    g_threads = threads;
+    const double r = ssmpk_probe(kind, iters, blocks_per_sm);
+    g_threads = 256;
+    return r;
 }
 
 // Number of SMs of the current device (so callers can normalise per SM).

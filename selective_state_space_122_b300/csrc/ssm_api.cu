@@ -2,6 +2,7 @@
 // argument validation, work planning and kernel dispatch.  Nothing here
 // allocates, copies or synchronises; every check runs on the host before the
 // first launch, so a rejected call leaves every buffer untouched.
+#include <algorithm>
 #include <atomic>
 #include <cmath>
 #include <cstdint>
@@ -85,6 +86,15 @@ int plan_layout(int64_t batch, int64_t dim, int N, int sms) {
 
 bool dstate_ok(int64_t n) { return n == 4 || n == 8 || n == 16; }
 
+// CUDA runtime error behind the calling thread's last SSM_ERR_LAUNCH.
+thread_local cudaError_t t_last_launch = cudaSuccess;
+
+ssm_status launch_status(cudaError_t e) {
+    if (e == cudaSuccess) return SSM_OK;
+    t_last_launch = e;
+    return SSM_ERR_LAUNCH;
+}
+
 }  // namespace
 
 extern "C" {
@@ -106,12 +116,17 @@ const char* ssm_status_string(int status) {
 
 int ssm_version(void) { return 100; }
 
+const char* ssm_last_launch_error(void) {
+    return t_last_launch == cudaSuccess ? "no launch error" : cudaGetErrorString(t_last_launch);
+}
+
 int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
-    (void)dim;
     if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
+    if (dim <= 0 || dim > (int64_t(1) << 31)) return -1;
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
-    return ssm::relay_workspace_bytes(batch, seqlen, (int)dstate);
+    return std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate),
+                    ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate));
 }
 
 int ssm_device_error(int clear) { return ssm::read_device_error(clear != 0); }
@@ -159,19 +174,25 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The relay path runs whenever its layout and workspace requirements
-    // hold; SSM_SCAN_PATH=generic forces the generic kernel (tests use it).
+    // The relay scan runs whenever its layout and workspace requirements hold;
+    // SSM_SCAN_PATH=seg|generic forces another kernel (tests use it).
     const char* force = std::getenv("SSM_SCAN_PATH");
+    // (chains * 64 segments must stay a 32-bit task count)
+    const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
+                         batch * ((dim + 127) / 128 * dstate) * 64 < (int64_t(1) << 31);
+    if (force && std::strcmp(force, "seg") == 0) {
+        if (!fast_ok || workspace_bytes < ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate))
+            return SSM_ERR_UNSUPPORTED;
+        return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
+    }
     const bool want_generic = force && std::strcmp(force, "generic") == 0;
-    if (!want_generic && workspace && workspace_bytes >= ssm::relay_workspace_bytes(batch, seqlen, (int)dstate) &&
-        ssm::relay_supported(a, dt)) {
-        const cudaError_t e = ssm::launch_scan_relay(a, dt, workspace, st);
-        return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    if (!want_generic && fast_ok &&
+        workspace_bytes >= ssm::relay_workspace_bytes(batch, seqlen, (int)dstate)) {
+        return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
     }
     if (force && std::strcmp(force, "relay") == 0) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
-    const cudaError_t e = ssm::launch_scan_fwd(a, dt, plan, st);
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
 }
 
 ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
@@ -203,9 +224,8 @@ ssm_status ssm_state_update(float* state, const void* x, const void* dt, const f
 
     ssm::UpdateArgs a{state, x, dt, A, B, C, D, z, dt_bias, out, batch, dim, (int)dstate,
                       dt_softplus ? 1 : 0};
-    const cudaError_t e = ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
-                                                   static_cast<cudaStream_t>(stream));
-    return e == cudaSuccess ? SSM_OK : SSM_ERR_LAUNCH;
+    return launch_status(ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+                                                  static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

@@ -1,0 +1,132 @@
+"""Profiling drivers for the selective-scan library (run on a CUDA device).
+
+    python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
+           [--N N] [--iters K] [--path relay|seg|generic]
+    python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K]
+    python -m selective_state_space_122_b300.profile units
+
+``scan`` runs ssm_scan_fwd on seeded on-device bf16 inputs shaped like the
+pages' workloads (u, delta_raw, z, B, C ~ N(0, 1); A = -(1..N); D = 1;
+delta_bias = softplus^-1(dt), dt log-uniform in [1e-3, 0.1]) and prints the
+CUDA-event time of each call: the command behind the ncu captures of the scan
+kernels.  ``decode`` does the same for one ssm_state_update step.  ``units``
+prints the measured SFU (ex2) and packed-FMA throughput at 1, 2 and 8 warps
+per scheduler (libssmpeak.so).
+"""
+from __future__ import annotations
+
+import argparse
+import ctypes
+import math
+import os
+import sys
+
+import torch
+
+from . import build as libbuild
+from ._lib import device_error, scan_workspace_bytes, ssm_scan_fwd, ssm_state_update
+
+
+def _inputs(batch, dim, L, N, dev, seed=0):
+    g = torch.Generator(device=dev)
+    g.manual_seed(seed)
+    u = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
+    dl = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
+    z = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
+    B = torch.randn(batch, N, L, device=dev, generator=g).bfloat16()
+    C = torch.randn(batch, N, L, device=dev, generator=g).bfloat16()
+    A = -torch.arange(1, N + 1, device=dev, dtype=torch.float32).repeat(dim, 1).contiguous()
+    D = torch.ones(dim, device=dev)
+    dt = torch.exp(torch.empty(dim, device=dev).uniform_(math.log(1e-3), math.log(0.1), generator=g))
+    bias = dt + torch.log(-torch.expm1(-dt))
+    return u, dl, z, B, C, A, D, bias
+
+
+def cmd_scan(a):
+    if a.path:
+        os.environ["SSM_SCAN_PATH"] = a.path
+    dev = torch.device("cuda", 0)
+    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev)
+    out = torch.empty_like(u)
+    last = torch.empty(a.batch, a.dim, a.N, device=dev)
+    ws = torch.empty(max(16, scan_workspace_bytes(a.batch, a.dim, a.L, a.N, torch.bfloat16)),
+                     dtype=torch.uint8, device=dev)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    elems = a.batch * a.dim * a.L * a.N
+    for i in range(a.iters):
+        e0.record()
+        ssm_scan_fwd(u, dl, A, B, C, D, z, bias, True, out=out, last_state=last, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"scan {a.batch}x{a.dim}x{a.L} N{a.N} iter {i}: {ms:.3f} ms "
+              f"({elems / (ms * 1e-3) / 1e9:.1f} G elements/s)", flush=True)
+    err = device_error()
+    print("device error word:", err)
+    return 0 if err == 0 else 1
+
+
+def cmd_decode(a):
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(1)
+    st = torch.randn(a.batch, a.dim, a.N, device=dev, generator=g) * 0.1
+    x, dt, z = (torch.randn(a.batch, a.dim, device=dev, generator=g).bfloat16() for _ in range(3))
+    B, C = (torch.randn(a.batch, a.N, device=dev, generator=g).bfloat16() for _ in range(2))
+    A = -torch.arange(1, a.N + 1, device=dev, dtype=torch.float32).repeat(a.dim, 1).contiguous()
+    D = torch.ones(a.dim, device=dev)
+    bias = torch.full((a.dim,), -4.0, device=dev)
+    out = torch.empty_like(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nbytes = 2 * st.numel() * 4 + 4 * x.numel() * 2
+    for i in range(a.iters):
+        e0.record()
+        ssm_state_update(st, x, dt, A, B, C, D, z, bias, True, out=out)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"decode {a.batch}x{a.dim} N{a.N} iter {i}: {ms * 1e3:.1f} us "
+              f"({nbytes / (ms * 1e-3) / 1e9:.0f} GB/s)", flush=True)
+    return 0
+
+
+def cmd_units(a):
+    lib = ctypes.CDLL(libbuild.PEAK_LIB)
+    lib.ssmpk_probe_shape.argtypes = [ctypes.c_int] * 4
+    lib.ssmpk_probe_shape.restype = ctypes.c_double
+    lib.ssmpk_sm_count.restype = ctypes.c_int
+    sms = lib.ssmpk_sm_count()
+    clk = torch.cuda.get_device_properties(0)
+    del clk
+    for name, kind, iters in (("ex2", 0, 20000), ("packed FMA", 3, 40000)):
+        for bps, thr in ((1, 128), (2, 128), (4, 256)):
+            r = max(lib.ssmpk_probe_shape(kind, iters, bps, thr) for _ in range(3))
+            wps = bps * thr // 32 / 4
+            print(f"{name:10s} {wps:3.0f} warp(s)/scheduler: {r / 1e9:9.1f} G/s "
+                  f"= {r / (sms * a.clock_mhz * 1e6):6.2f} per clock per SM (at {a.clock_mhz:.0f} MHz)")
+    return 0
+
+
+def main(argv=None):
+    ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
+    sub = ap.add_subparsers(dest="cmd", required=True)
+    s = sub.add_parser("scan")
+    s.add_argument("--batch", type=int, default=1)
+    s.add_argument("--dim", type=int, default=5120)
+    s.add_argument("--L", type=int, default=16384)
+    s.add_argument("--N", type=int, default=16)
+    s.add_argument("--iters", type=int, default=3)
+    s.add_argument("--path", default=None, choices=[None, "relay", "seg", "generic"])
+    d = sub.add_parser("decode")
+    d.add_argument("--batch", type=int, default=256)
+    d.add_argument("--dim", type=int, default=5120)
+    d.add_argument("--N", type=int, default=16)
+    d.add_argument("--iters", type=int, default=5)
+    u = sub.add_parser("units")
+    u.add_argument("--clock-mhz", type=float, default=2032.0)
+    a = ap.parse_args(argv)
+    return {"scan": cmd_scan, "decode": cmd_decode, "units": cmd_units}[a.cmd](a)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

@@ -91,22 +91,22 @@ def relay_ok(dim: int, dtype: str) -> bool:
 
 
 def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
-    """Every way to run a scan of this shape: the relay path (when it accepts
-    the shape) and each generic layout."""
-    return (["relay"] if relay_ok(dim, dtype) else []) + list(range(LAYOUTS[N]))
+    """Every way to run a scan of this shape: the segmented and relay paths
+    (when they accept the shape) and each generic layout."""
+    return (["seg", "relay"] if relay_ok(dim, dtype) else []) + list(range(LAYOUTS[N]))
 
 
 @contextlib.contextmanager
 def scan_layout(layout):
-    """Force a path: None = the library's own choice, "relay" = the relay
-    kernel (an error if it cannot take the shape), an int = that layout of
-    the generic kernel."""
+    """Force a path: None = the library's own choice, "seg" / "relay" = that
+    TMA kernel (an error if it cannot take the shape), an int = that layout
+    of the generic kernel."""
     keys = ("SSM_SCAN_LAYOUT", "SSM_SCAN_PATH")
     old = {k: os.environ.get(k) for k in keys}
     for k in keys:
         os.environ.pop(k, None)
-    if layout == "relay":
-        os.environ["SSM_SCAN_PATH"] = "relay"
+    if layout in ("relay", "seg"):
+        os.environ["SSM_SCAN_PATH"] = layout
     elif layout is not None:
         os.environ["SSM_SCAN_PATH"] = "generic"
         os.environ["SSM_SCAN_LAYOUT"] = str(layout)

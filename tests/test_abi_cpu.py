@@ -124,11 +124,23 @@ def test_binding_raises_without_cuda_tensors():
         _lib.ssm_scan_fwd(u, u, A, B, B)
 
 
+def _ws_expected(batch, dim, seqlen, dstate):
+    """B and C staged as float32 rows (sequence padded to 32 steps), plus, for
+    the segmented scan, one float32 state per (chain, channel, state) and one
+    int flag per chain; each part rounded up to 256 bytes."""
+    up = lambda x: (x + 255) // 256 * 256
+    lpad = (seqlen + 31) // 32 * 32
+    bc = batch * lpad * 2 * dstate * 4
+    cw = 32 // (dstate // 4)
+    chains = batch * ((dim + cw - 1) // cw)
+    return max(bc, up(bc) + up(chains * cw * dstate * 4) + up(chains * 4))
+
+
 def test_workspace_size_query(lib):
-    # batch * round_up(seqlen, 8) * 2 * dstate * 4 bytes (B and C staged as float32 rows)
-    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 131072 * 2 * 16 * 4
-    assert lib.ssm_scan_workspace_bytes(3, 7, 77, 8, 0) == 3 * 80 * 2 * 8 * 4
-    assert lib.ssm_scan_workspace_bytes(1, 1, 1, 4, 1) == 8 * 2 * 4 * 4
+    for args in [(1, 5120, 131072, 16), (3, 7, 77, 8), (1, 1, 1, 4), (8, 2048, 2048, 16), (2, 100, 33, 8)]:
+        assert lib.ssm_scan_workspace_bytes(*args, 1) == _ws_expected(*args), args
+    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 16777216 + 327680 + 2560
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 5, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
+    assert lib.ssm_scan_workspace_bytes(1, 0, 64, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 16, 7) == -1
