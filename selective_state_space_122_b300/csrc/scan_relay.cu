@@ -527,7 +527,7 @@ struct SegCfg {
     // steps per chunk: 32, or 16 where 32-step float32 tiles of 32 channels
     // would not fit four warps' rings in shared memory
     static constexpr int K = (N == 4 && sizeof(T) == 4) ? 16 : 32;
-    static constexpr int P = 3;                 // chunks in flight per warp
+    static constexpr int P = 4;                 // chunks in flight per warp (a power of two)
     static constexpr int WARPS = 4;             // independent workers per CTA (one per scheduler)
     static constexpr int THREADS = 32 * WARPS;
     static constexpr int KR = K / R;            // prologue items / finished steps per lane
@@ -551,6 +551,7 @@ struct SegCfg {
     static constexpr int SMEM = WARPS * WARP_BYTES;
     static_assert(SMEM <= 227 * 1024, "a CTA's shared memory must fit an SM");
     static_assert(K % 8 == 0 && 32 % K == 0, "chunks tile the 32-step padded sequence");
+    static_assert((P & (P - 1)) == 0, "ring depth is a power of two");
 };
 
 struct SegParams {
@@ -590,7 +591,7 @@ __device__ __forceinline__ bool flag_wait(const int* flag, int want) {
 }
 
 template <typename T, int N, bool kFast, bool kSoftplus, bool kGate>
-__global__ void __launch_bounds__(SegCfg<T, N>::THREADS)
+__global__ void __launch_bounds__(SegCfg<T, N>::THREADS, 1)
 scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
                 const SegParams p) {
@@ -620,30 +621,36 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
     // Chunk stream of this warp: its tasks wid, wid + workers, ... in order, each
     // task's chunks in order.  Lane 0 prefetches P chunks ahead along it.
+    // Prefetch cursor (lane 0): the task, its first chunk's TMA coordinates
+    // and B/C source, cached per task so a chunk costs only additions.
     int pf_task = wid, pf_c = 0, pf_end = 0, issued = 0;
-    auto task_span = [&](int task, int& cb, int& ce) {
-        const int sgm = task / p.M;
-        cb = sgm * p.cps;
-        ce = min(cb + p.cps, nch);
+    int pf_b = 0, pf_d0 = 0;
+    const float* pf_bc = nullptr;
+    auto pf_enter = [&](int task) {
+        const int sgm = task / p.M, m = task - sgm * p.M;
+        pf_b = m / p.units;
+        pf_d0 = (m - pf_b * p.units) * CW;
+        pf_c = sgm * p.cps;
+        pf_end = min(pf_c + p.cps, nch);
+        pf_bc = p.bc + ((size_t)pf_b * p.lpad + (size_t)pf_c * K) * (2 * N);
     };
-    if (pf_task < T_total) task_span(pf_task, pf_c, pf_end);
+    if (pf_task < T_total) pf_enter(pf_task);
     auto issue_next = [&]() {   // lane 0 only; false once the stream is exhausted
         while (pf_task < T_total && pf_c >= pf_end) {
             pf_task += p.workers;
-            if (pf_task < T_total) task_span(pf_task, pf_c, pf_end);
+            if (pf_task < T_total) pf_enter(pf_task);
         }
         if (pf_task >= T_total) return false;
-        const int m = pf_task % p.M;
-        const int bb = m / p.units, dd0 = (m - bb * p.units) * CW;
-        const int slot = issued % P;
+        const int slot = issued & (P - 1);
         const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
         const uint32_t bar = bar_full + 8u * (uint32_t)slot;
         const int t0 = pf_c * K;
         mbar_expect_tx(bar, tx_bytes);
-        tma_load_3d(base + CF::SLOT_U, &tm_u, dd0, t0, bb, bar);
-        tma_load_3d(base + CF::SLOT_D, &tm_d, dd0, t0, bb, bar);
-        if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, dd0, t0, bb, bar);
-        bulk_load(base + CF::SLOT_BC, p.bc + ((size_t)bb * p.lpad + t0) * (2 * N), CF::BC, bar);
+        tma_load_3d(base + CF::SLOT_U, &tm_u, pf_d0, t0, pf_b, bar);
+        tma_load_3d(base + CF::SLOT_D, &tm_d, pf_d0, t0, pf_b, bar);
+        if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, pf_d0, t0, pf_b, bar);
+        bulk_load(base + CF::SLOT_BC, pf_bc, CF::BC, bar);
+        pf_bc += K * 2 * N;
         ++pf_c;
         ++issued;
         return true;
@@ -687,7 +694,7 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
         }
 
         for (int c = cb; c < ce; ++c) {
-            const int slot = consumed % P;
+            const int slot = consumed & (P - 1);
             const unsigned char* sb = wbase + CF::W_RING + slot * CF::SLOT;
             if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * (uint32_t)slot, (uint32_t)((consumed / P) & 1)))) {
                 ok = false;
@@ -707,76 +714,83 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const T* su = reinterpret_cast<const T*>(sb + CF::SLOT_U);
             const T* sd = reinterpret_cast<const T*>(sb + CF::SLOT_D);
             const T* sz = reinterpret_cast<const T*>(sb + CF::SLOT_Z);
-            float2 uk[NP], gate[NP];
+            // All shared-memory loads of the phase come first, then the math,
+            // then the stores: the tiles, the Delta buffer and the reduction
+            // buffer are all shared memory, so a load placed after a store
+            // could not be moved above it.
+            float2 uk[NP], xr[NP], zr[NP], gate[NP];
+            int tas[NP];
 #pragma unroll
             for (int j = 0; j < NP; ++j) {
-                const int ta = g * KR + 2 * ((j + g) % NP), tb = ta + 1;
-                const float2 uv = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
-                const float2 xr = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
-                float2 dl = add2(xr, bias2);
+                tas[j] = g * KR + 2 * ((j + g) % NP);
+                const int ta = tas[j], tb = ta + 1;
+                uk[j] = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
+                xr[j] = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
+                if constexpr (kGate) zr[j] = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
+            }
+            float4 dpv[2 * NP];
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                float2 dl = add2(xr[j], bias2);
                 if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
-                if (tail) dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + tb < L ? 1.f : 0.f));
-                const float2 du = mul2(dl, uv);
-                uk[j] = uv;
-                if constexpr (kGate) {
-                    const float2 zv = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
-                    gate[j] = seg_silu2<kFast>(zv);
-                } else {
-                    gate[j] = splat2(1.f);
-                }
-                dp[ta * CW + ch] = make_float4(dl.x, dl.x, du.x, du.x);
-                dp[tb * CW + ch] = make_float4(dl.y, dl.y, du.y, du.y);
+                if (tail) dl = mul2(dl, make_float2(t0 + tas[j] < L ? 1.f : 0.f, t0 + tas[j] + 1 < L ? 1.f : 0.f));
+                const float2 du = mul2(dl, uk[j]);
+                if constexpr (kGate) gate[j] = seg_silu2<kFast>(zr[j]);
+                else gate[j] = splat2(1.f);
+                dpv[2 * j] = make_float4(dl.x, dl.x, du.x, du.x);
+                dpv[2 * j + 1] = make_float4(dl.y, dl.y, du.y, du.y);
+            }
+#pragma unroll
+            for (int j = 0; j < NP; ++j) {
+                dp[tas[j] * CW + ch] = dpv[2 * j];
+                dp[(tas[j] + 1) * CW + ch] = dpv[2 * j + 1];
             }
             __syncwarp();
 
-            // ---- the recurrence, in batches of KB steps: (A) exp(Delta A) and
-            // Delta B u of a batch, independent of the state; (B) the state
-            // chain; (C) the per-lane readout C . h.  A of batch b+1 is issued
-            // before B and C of batch b, so the SFU work of the next batch
-            // overlaps the dependent chain of this one.
+            // ---- the recurrence as a software pipeline over the chunk's K steps:
+            // step t loads the Delta/B/C rows of step t+LA, evaluates
+            // exp(Delta A) and Delta B u of step t+EA, advances the state by
+            // step t (one packed FMA per two states: the only serial work) and
+            // reads out C_t . h_t.  Everything is unrolled, so the stages of
+            // different steps interleave in the instruction stream.
             const float* sbc = reinterpret_cast<const float*>(sb + CF::SLOT_BC);
-            constexpr int KB = 8, NB = K / KB;
-            float2 dA[2][KB][2], dB[2][KB][2];
-            float2 ys[R == 1 ? K / 2 : 1];
-            auto phaseA = [&](int bt, int buf) {
-#pragma unroll
-                for (int t = 0; t < KB; ++t) {
-                    const int tt = bt * KB + t;
-                    const float4 q = dp[tt * CW + ch];
-                    const float4 bq = *reinterpret_cast<const float4*>(sbc + tt * (2 * N) + 4 * g);
-                    const float2 e0 = mul2(make_float2(q.x, q.y), A2[0]);
-                    const float2 e1 = mul2(make_float2(q.x, q.y), A2[1]);
-                    dA[buf][t][0] = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
-                    dA[buf][t][1] = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
-                    dB[buf][t][0] = mul2(make_float2(q.z, q.w), make_float2(bq.x, bq.y));
-                    dB[buf][t][1] = mul2(make_float2(q.z, q.w), make_float2(bq.z, bq.w));
-                }
+            constexpr int LA = 4, EA = 2;
+            float4 qv[K], bv[K], cv[K];
+            float2 dA[K][2], dB[K][2];
+            float2 s2v[K / 2];
+            auto load_step = [&](int t) {
+                qv[t] = dp[t * CW + ch];
+                bv[t] = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + 4 * g);
+                cv[t] = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + N + 4 * g);
             };
-            phaseA(0, 0);
+            auto exp_step = [&](int t) {
+                const float2 e0 = mul2(make_float2(qv[t].x, qv[t].y), A2[0]);
+                const float2 e1 = mul2(make_float2(qv[t].x, qv[t].y), A2[1]);
+                dA[t][0] = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
+                dA[t][1] = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
+                dB[t][0] = mul2(make_float2(qv[t].z, qv[t].w), make_float2(bv[t].x, bv[t].y));
+                dB[t][1] = mul2(make_float2(qv[t].z, qv[t].w), make_float2(bv[t].z, bv[t].w));
+            };
 #pragma unroll
-            for (int bt = 0; bt < NB; ++bt) {
-                const int cur = bt & 1;
-                if (bt + 1 < NB) phaseA(bt + 1, cur ^ 1);
+            for (int t = 0; t < LA; ++t) load_step(t);
 #pragma unroll
-                for (int t = 0; t < KB; ++t) {
-                    h0 = fma2(dA[cur][t][0], h0, dB[cur][t][0]);
-                    h1 = fma2(dA[cur][t][1], h1, dB[cur][t][1]);
-                    dB[cur][t][0] = h0;
-                    dB[cur][t][1] = h1;
-                }
+            for (int t = 0; t < EA; ++t) exp_step(t);
+            float2 acc_prev = make_float2(0.f, 0.f);
 #pragma unroll
-                for (int t = 0; t < KB; t += 2) {
-                    const int tt = bt * KB + t;
-                    const float4 c0 = *reinterpret_cast<const float4*>(sbc + tt * (2 * N) + N + 4 * g);
-                    const float4 c1 = *reinterpret_cast<const float4*>(sbc + (tt + 1) * (2 * N) + N + 4 * g);
-                    const float2 a0 = fma2(make_float2(c0.z, c0.w), dB[cur][t][1],
-                                           mul2(make_float2(c0.x, c0.y), dB[cur][t][0]));
-                    const float2 a1 = fma2(make_float2(c1.z, c1.w), dB[cur][t + 1][1],
-                                           mul2(make_float2(c1.x, c1.y), dB[cur][t + 1][0]));
-                    const float2 s2 = make_float2(a0.x + a0.y, a1.x + a1.y);
-                    if constexpr (R == 1) ys[tt / 2] = s2;
-                    else red[(tt / 2) * RS2 + lane] = s2;
-                }
+            for (int t = 0; t < K; ++t) {
+                if (t + LA < K) load_step(t + LA);
+                if (t + EA < K) exp_step(t + EA);
+                h0 = fma2(dA[t][0], h0, dB[t][0]);
+                h1 = fma2(dA[t][1], h1, dB[t][1]);
+                const float2 acc = fma2(make_float2(cv[t].z, cv[t].w), h1, mul2(make_float2(cv[t].x, cv[t].y), h0));
+                if (t & 1) s2v[t / 2] = make_float2(acc_prev.x + acc_prev.y, acc.x + acc.y);
+                acc_prev = acc;
+            }
+            float2 ys[R == 1 ? K / 2 : 1];
+#pragma unroll
+            for (int t = 0; t < K / 2; ++t) {
+                if constexpr (R == 1) ys[t] = s2v[t];
+                else red[t * RS2 + lane] = s2v[t];
             }
 
             // ---- sum the R lanes of each channel for this lane's pairs (same rotation)
@@ -786,31 +800,39 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 for (int j = 0; j < NP; ++j) yv[j] = ys[j];
             } else {
                 __syncwarp();
+                float2 pr[NP][R];
 #pragma unroll
                 for (int j = 0; j < NP; ++j) {
                     const float2* row = red + (g * NP + (j + g) % NP) * RS2 + ch * R;
-                    float2 sum = row[0];
 #pragma unroll
-                    for (int gg = 1; gg < R; ++gg) sum = add2(sum, row[gg]);
+                    for (int gg = 0; gg < R; ++gg) pr[j][gg] = row[gg];
+                }
+#pragma unroll
+                for (int j = 0; j < NP; ++j) {
+                    float2 sum = pr[j][0];
+#pragma unroll
+                    for (int gg = 1; gg < R; ++gg) sum = add2(sum, pr[j][gg]);
                     yv[j] = sum;
                 }
             }
 
-            // ---- D skip, gate, output tile (triple-buffered; lane 0 owns the TMA store groups)
+            // ---- D skip, gate, output tile (triple-buffered; lane 0 owns the TMA
+            // store groups: before this tile is rewritten, the store that last
+            // read it -- three chunks ago -- must have finished reading)
             T* so = reinterpret_cast<T*>(wbase + CF::W_OUT + oslot * CF::OUT);
+            if (lane == 0) bulk_wait_read<2>();
+            __syncwarp();
+            float2 yo[NP];
 #pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                const int ta = g * KR + 2 * ((j + g) % NP);
-                const float2 y = mul2(fma2(dskip2, uk[j], yv[j]), gate[j]);
-                st_pair<T>(so + ta * CW + ch, so + (ta + 1) * CW + ch, y);
-            }
+            for (int j = 0; j < NP; ++j) yo[j] = mul2(fma2(dskip2, uk[j], yv[j]), gate[j]);
+#pragma unroll
+            for (int j = 0; j < NP; ++j) st_pair<T>(so + tas[j] * CW + ch, so + (tas[j] + 1) * CW + ch, yo[j]);
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
                 tma_store_3d(&tm_out, d0, t0, b, smem_u32(so));
                 bulk_commit();
                 issue_next();
-                bulk_wait_read<1>();
             }
             oslot = oslot == 2 ? 0 : oslot + 1;
         }
@@ -832,7 +854,7 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (!ok) {
         const int iss = __shfl_sync(0xffffffffu, issued, 0);
         for (int j = consumed; j < iss; ++j)
-            if (!mbar_wait(bar_full + 8u * (uint32_t)(j % P), (uint32_t)((j / P) & 1))) break;
+            if (!mbar_wait(bar_full + 8u * (uint32_t)(j & (P - 1)), (uint32_t)((j / P) & 1))) break;
     }
     if (lane == 0) bulk_wait_all();
 }
