@@ -76,7 +76,9 @@ typedef enum ssm_status {
     SSM_ERR_DTYPE = 5,        /* dtype is not SSM_F32 / SSM_BF16                 */
     SSM_ERR_ALIAS = 6,        /* an output overlaps an input (or another output) */
     SSM_ERR_LAUNCH = 7,       /* the CUDA runtime rejected a kernel launch       */
-    SSM_ERR_DEVICE = 8        /* no usable CUDA device / attribute query failed  */
+    SSM_ERR_DEVICE = 8,       /* no usable CUDA device / attribute query failed  */
+    SSM_ERR_SCRATCH = 9       /* ssm_scan_fwd_noalloc: the sizes need more scratch
+                                 than the library's fixed array holds             */
 } ssm_status;
 
 typedef enum ssm_dtype {
@@ -168,6 +170,40 @@ SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
 
 /* Static, human-readable name of a status code (never NULL). */
 SSM_API const char* ssm_status_string(int status);
+
+/*
+ * ssm_scan_fwd_noalloc -- ssm_scan_fwd for callers that cannot allocate.
+ *
+ * The pages have no counterpart: this is a deployment variant of the scan.
+ * Some callers cannot call cudaMalloc where they run the scan -- code inside
+ * a framework whose allocator owns all device memory, allocation-free hot
+ * loops, or plain C callers with no allocator to hand a workspace from.  This
+ * entry point takes the same arguments as ssm_scan_fwd minus the workspace
+ * and uses instead a scratch array that lives in the library: a file-scope
+ * device array of ssm_scan_noalloc_max_workspace_bytes() bytes (32 MiB) that
+ * every GPU loading the library holds until the process exits.  It performs
+ * no allocation of any kind; the caller still passes every input and output.
+ *
+ * - Sizes whose workspace (ssm_scan_workspace_bytes) exceeds the array are
+ *   rejected with SSM_ERR_SCRATCH before anything is enqueued; invalid
+ *   arguments get the same codes as ssm_scan_fwd.
+ * - The first call on each device looks up the array's device address
+ *   (cudaGetSymbolAddress, with that device current) and caches it; make that
+ *   first call before any stream capture.
+ * - All calls on a device share the one array, and each call overwrites it
+ *   (the parts that must start at zero are cleared by the call itself).
+ *   Calls that overlap on the GPU -- on different streams, or from different
+ *   host threads without ordering -- race on it: serialise them.
+ */
+SSM_API ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A,
+                                const void* B, const void* C, const float* D,
+                                const void* z, const float* delta_bias, int softplus_flag,
+                                void* out, float* last_state,
+                                int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                int dtype, void* stream);
+
+/* Size in bytes of ssm_scan_fwd_noalloc's fixed scratch array. */
+SSM_API int64_t ssm_scan_noalloc_max_workspace_bytes(void);
 
 /* The CUDA runtime's message for the calling thread's most recent
  * SSM_ERR_LAUNCH (a static string; "no launch error" if there was none). */

@@ -20,9 +20,10 @@ SSM_F32 = 0
 SSM_BF16 = 1
 STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN",
           4: "SSM_ERR_UNSUPPORTED", 5: "SSM_ERR_DTYPE", 6: "SSM_ERR_ALIAS",
-          7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE"}
+          7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE", 9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
-           "ssm_status_string", "ssm_last_launch_error", "ssm_version")
+           "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
+           "ssm_scan_noalloc_max_workspace_bytes")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -55,6 +56,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_state_update.restype = ci
     lib.ssm_status_string.argtypes = [ci]
     lib.ssm_status_string.restype = ctypes.c_char_p
+    lib.ssm_scan_fwd_noalloc.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
+                                         i64, i64, i64, i64, ci, vp]
+    lib.ssm_scan_fwd_noalloc.restype = ci
+    lib.ssm_scan_noalloc_max_workspace_bytes.argtypes = []
+    lib.ssm_scan_noalloc_max_workspace_bytes.restype = i64
     lib.ssm_last_launch_error.argtypes = []
     lib.ssm_last_launch_error.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []

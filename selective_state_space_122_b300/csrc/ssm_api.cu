@@ -110,6 +110,8 @@ const char* ssm_status_string(int status) {
         case SSM_ERR_ALIAS: return "SSM_ERR_ALIAS: an output overlaps an input";
         case SSM_ERR_LAUNCH: return "SSM_ERR_LAUNCH: the CUDA runtime rejected a launch";
         case SSM_ERR_DEVICE: return "SSM_ERR_DEVICE: no usable CUDA device";
+        case SSM_ERR_SCRATCH:
+            return "SSM_ERR_SCRATCH: the sizes need more scratch than ssm_scan_fwd_noalloc's fixed array holds";
         default: return "unknown ssm_status";
     }
 }
