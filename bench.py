@@ -412,7 +412,7 @@ def bench_ours(args):
             "peak": units["ex2"] / 1e9,
             "frac": sfu_ach / units["ex2"],
             "traffic": None,
-            "kernel": "ssm_scan_fwd: bc_stage_kernel + scan_relay_kernel (long-sequence scan)",
+            "kernel": "ssm_scan_fwd: bc_stage_kernel + scan_seg_kernel (long-sequence scan)",
             "peak_source": ("measured on this GPU by libssmpeak.so: ex2 %.1f, lg2 %.1f, rcp %.1f G/s, "
                             "packed FMA %.1f TFLOP/s; SFU work per (b,t,d): N+2 ex2, 1 lg2, 1 rcp, "
                             "lg2/rcp weighted by ex2_rate/their rate"

@@ -121,14 +121,15 @@ SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A
                         int dtype, void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
- * ssm_scan_workspace_bytes -- bytes of workspace the fast path of
- * ssm_scan_fwd needs for these sizes: B and C staged as float32 rows
- * (batch * round_up(seqlen, 32) * 2 * dstate * 4 bytes), then, for the
- * segmented scan, the state handed between segments of each chain
- * (chains * cw * dstate * 4, cw = 128 / dstate channels per chain,
+ * ssm_scan_workspace_bytes -- bytes of workspace the fast paths of
+ * ssm_scan_fwd need for these sizes: the larger of (a) B and C staged as
+ * float32 rows, batch * round_up(seqlen, 64) * 2 * dstate * 4 bytes (relay
+ * kernel), and (b) B and C staged in the activation dtype (same count of
+ * elements), the state handed between sequence segments of each chain
+ * (chains * cw * dstate * 4 bytes, cw = 128 / dstate channels per chain,
  * chains = batch * ceil(dim / cw)) and one int flag per chain, each part
- * rounded up to 256 bytes.  Returns -1 for sizes or a dtype that
- * ssm_scan_fwd would reject.  Pure host computation.
+ * rounded up to 256 bytes (segmented kernel).  Returns -1 for sizes or a
+ * dtype that ssm_scan_fwd would reject.  Pure host computation.
  */
 SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                          int dtype);

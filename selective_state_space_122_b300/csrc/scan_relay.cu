@@ -518,22 +518,37 @@ __device__ __forceinline__ float2 seg_silu2(float2 z) {
     }
 }
 
+// Four consecutive staged values as float32: one 8-byte shared load and a
+// bit-shift unpack for bf16, one 16-byte load for float32.
+template <typename T>
+__device__ __forceinline__ float4 ld_quad(const T* p);
+template <>
+__device__ __forceinline__ float4 ld_quad<float>(const float* p) {
+    return *reinterpret_cast<const float4*>(p);
+}
+template <>
+__device__ __forceinline__ float4 ld_quad<__nv_bfloat16>(const __nv_bfloat16* p) {
+    const uint2 w = *reinterpret_cast<const uint2*>(p);
+    return make_float4(__uint_as_float(w.x << 16), __uint_as_float(w.x & 0xffff0000u),
+                       __uint_as_float(w.y << 16), __uint_as_float(w.y & 0xffff0000u));
+}
+
 template <typename T, int N_>
 struct SegCfg {
     static constexpr int N = N_;
     static constexpr int G = 4;                 // states per lane
     static constexpr int R = N / G;             // lanes per channel
-    static constexpr int CW = 32 / R;           // channels per warp
-    // steps per chunk: 32, or 16 where 32-step float32 tiles of 32 channels
-    // would not fit four warps' rings in shared memory
-    static constexpr int K = (N == 4 && sizeof(T) == 4) ? 16 : 32;
-    static constexpr int P = 4;                 // chunks in flight per warp (a power of two)
-    static constexpr int WARPS = 4;             // independent workers per CTA (one per scheduler)
-    static constexpr int THREADS = 32 * WARPS;
-    static constexpr int KR = K / R;            // prologue items / finished steps per lane
+    static constexpr int CW = 32 / R;           // channels per chain (one warp-width)
+    // Steps per chunk: 64 for 16 states in bf16 (per-chunk costs spread over
+    // more steps), 16 for 4 states (32-channel tiles), 32 otherwise.
+    static constexpr int K = (N == 16 && sizeof(T) == 2) ? 64 : (N == 4 ? 16 : 32);
+    static constexpr int P = (N == 8 && sizeof(T) == 4) ? 2 : 4;   // ring slots per pair (a power of two)
+    static constexpr int PAIRS = 4;             // (main, helper) warp pairs per CTA: one per scheduler
+    static constexpr int THREADS = 64 * PAIRS;
+    static constexpr int KR = K / R;            // items / finished steps per lane
     static constexpr int ES = (int)sizeof(T);
     static constexpr int TILE = K * CW * ES;
-    static constexpr int BC = K * 2 * N * 4;
+    static constexpr int BC = K * 2 * N * ES;   // staged B|C rows, in the activation type
     static constexpr int align128(int x) { return (x + 127) / 128 * 128; }
     static constexpr int SLOT_U = 0;
     static constexpr int SLOT_D = align128(TILE);
@@ -541,24 +556,27 @@ struct SegCfg {
     static constexpr int SLOT_BC = SLOT_Z + align128(TILE);
     static constexpr int SLOT = align128(SLOT_BC + BC);
     static constexpr int RS2 = 34;              // float2 stride of a step-pair row of the reduction buffer
-    static constexpr int W_RING = 0;
-    static constexpr int W_DP = W_RING + P * SLOT;                       // [K][CW] float4
-    static constexpr int W_RED = W_DP + K * CW * 16;                      // [K/2][RS2] float2
-    static constexpr int W_OUT = W_RED + (R > 1 ? align128((K / 2) * RS2 * 8) : 0);
+    static constexpr int HALF = K * CW * 8;     // one float2 per (step, channel)
+    // per-pair layout
+    static constexpr int P_RING = 0;                              // [P] slots
+    static constexpr int P_DP = P_RING + P * SLOT;                 // [2][K][CW] float2 (Delta, Delta u)
+    static constexpr int P_SG = P_DP + 2 * HALF;                   // [2][K][CW] float2 (u, silu z)
+    static constexpr int P_RED = P_SG + 2 * HALF;                  // [K/2][RS2] float2
+    static constexpr int P_OUT = P_RED + (R > 1 ? align128((K / 2) * RS2 * 8) : 0);   // [3] out tiles
     static constexpr int OUT = align128(TILE);
-    static constexpr int W_BAR = W_OUT + 3 * OUT;
-    static constexpr int WARP_BYTES = align128(W_BAR + P * 8);
-    static constexpr int SMEM = WARPS * WARP_BYTES;
+    static constexpr int P_BAR = P_OUT + 3 * OUT;                  // full[P], dpf[2], done[2]
+    static constexpr int PAIR_BYTES = align128(P_BAR + (P + 4) * 8);
+    static constexpr int SMEM = PAIRS * PAIR_BYTES;
     static_assert(SMEM <= 227 * 1024, "a CTA's shared memory must fit an SM");
-    static_assert(K % 8 == 0 && 32 % K == 0, "chunks tile the 32-step padded sequence");
-    static_assert((P & (P - 1)) == 0, "ring depth is a power of two");
+    static_assert(K % 8 == 0 && 64 % K == 0, "chunks tile the 64-step padded sequence");
+    static_assert((P & (P - 1)) == 0 && P >= 2, "ring depth is a power of two, at least two");
 };
 
 struct SegParams {
     const float* A;
     const float* D;
     const float* delta_bias;
-    const float* bc;        // staged B|C, [batch][lpad][2N] f32
+    const void* bc;         // staged B|C, [batch][lpad][2N] in the activation type
     float* last_state;
     float* seg_state;       // [M][CW][N] f32: state handed between segments
     int* seg_flag;          // [M]: number of finished segments of each chain
@@ -568,7 +586,7 @@ struct SegParams {
     int M;                  // chains = batch * units
     int S;                  // segments per chain
     int cps;                // chunks per segment
-    int workers;            // warps in the grid
+    int workers;            // (main, helper) pairs in the grid
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -590,6 +608,19 @@ __device__ __forceinline__ bool flag_wait(const int* flag, int want) {
     return true;
 }
 
+// One worker is a (main, helper) pair of warps on the same scheduler; it
+// walks its tasks (segment s of chain m, task = s * M + m) in slot order.
+//   helper: issues the TMA loads of its chunks (P in flight), then for each
+//           chunk computes the per-(t, d) terms -- Delta = softplus(delta_raw
+//           + bias), Delta u, u, silu(z) -- into a double buffer and signals
+//           "prologue done";
+//   main:   waits for it, runs the recurrence over the chunk (exp(Delta A),
+//           Delta B u, the state update, the per-lane readout C . h), sums the
+//           R lanes of each channel, applies D u and the gate, stores the
+//           output tile by TMA and signals "chunk done", which frees the
+//           double buffer and the ring slot for the helper.
+// The scheduler interleaves the helper's SFU-heavy prologue with the main
+// warp's dependency stalls.
 template <typename T, int N, bool kFast, bool kSoftplus, bool kGate>
 __global__ void __launch_bounds__(SegCfg<T, N>::THREADS, 1)
 scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
@@ -597,70 +628,158 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 const SegParams p) {
     using CF = SegCfg<T, N>;
     constexpr int K = CF::K, P = CF::P, R = CF::R, CW = CF::CW, KR = CF::KR, RS2 = CF::RS2;
+    constexpr int NP = KR / 2;
     extern __shared__ __align__(128) unsigned char smem[];
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int pair = warp % CF::PAIRS;
+    const bool helper = warp >= CF::PAIRS;
     const int ch = lane / R, g = lane % R;
-    unsigned char* wbase = smem + warp * CF::WARP_BYTES;
-    float4* dp = reinterpret_cast<float4*>(wbase + CF::W_DP);
-    float2* red = reinterpret_cast<float2*>(wbase + CF::W_RED);
-    const uint32_t ring_s = smem_u32(wbase + CF::W_RING);
-    const uint32_t bar_full = smem_u32(wbase + CF::W_BAR);
+    unsigned char* pb = smem + pair * CF::PAIR_BYTES;
+    const uint32_t ring_s = smem_u32(pb + CF::P_RING);
+    const uint32_t bar_full = smem_u32(pb + CF::P_BAR);
+    const uint32_t bar_dpf = bar_full + 8u * P;
+    const uint32_t bar_done = bar_dpf + 16u;
+    float2* dpb = reinterpret_cast<float2*>(pb + CF::P_DP);
+    float2* sgb = reinterpret_cast<float2*>(pb + CF::P_SG);
+    float2* red = reinterpret_cast<float2*>(pb + CF::P_RED);
 
     const int L = p.seqlen;
     const int nch = (L + K - 1) / K;
     const int T_total = p.M * p.S;
-    const int wid = blockIdx.x * CF::WARPS + warp;
+    const int wid = blockIdx.x * CF::PAIRS + pair;
 
-    if (lane == 0) {
+    if (helper && lane == 0) {
         for (int i = 0; i < P; ++i) mbar_init(bar_full + 8u * i, 1);
+        for (int i = 0; i < 4; ++i) mbar_init(bar_dpf + 8u * i, 1);   // dpf[2], done[2]
         fence_mbar_init();
     }
-    __syncwarp();
+    __syncthreads();
 
-    constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
-    // Chunk stream of this warp: its tasks wid, wid + workers, ... in order, each
-    // task's chunks in order.  Lane 0 prefetches P chunks ahead along it.
-    // Prefetch cursor (lane 0): the task, its first chunk's TMA coordinates
-    // and B/C source, cached per task so a chunk costs only additions.
-    int pf_task = wid, pf_c = 0, pf_end = 0, issued = 0;
-    int pf_b = 0, pf_d0 = 0;
-    const float* pf_bc = nullptr;
-    auto pf_enter = [&](int task) {
-        const int sgm = task / p.M, m = task - sgm * p.M;
-        pf_b = m / p.units;
-        pf_d0 = (m - pf_b * p.units) * CW;
-        pf_c = sgm * p.cps;
-        pf_end = min(pf_c + p.cps, nch);
-        pf_bc = p.bc + ((size_t)pf_b * p.lpad + (size_t)pf_c * K) * (2 * N);
-    };
-    if (pf_task < T_total) pf_enter(pf_task);
-    auto issue_next = [&]() {   // lane 0 only; false once the stream is exhausted
-        while (pf_task < T_total && pf_c >= pf_end) {
-            pf_task += p.workers;
-            if (pf_task < T_total) pf_enter(pf_task);
-        }
-        if (pf_task >= T_total) return false;
-        const int slot = issued & (P - 1);
-        const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
-        const uint32_t bar = bar_full + 8u * (uint32_t)slot;
-        const int t0 = pf_c * K;
-        mbar_expect_tx(bar, tx_bytes);
-        tma_load_3d(base + CF::SLOT_U, &tm_u, pf_d0, t0, pf_b, bar);
-        tma_load_3d(base + CF::SLOT_D, &tm_d, pf_d0, t0, pf_b, bar);
-        if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, pf_d0, t0, pf_b, bar);
-        bulk_load(base + CF::SLOT_BC, pf_bc, CF::BC, bar);
-        pf_bc += K * 2 * N;
-        ++pf_c;
-        ++issued;
-        return true;
-    };
-    if (lane == 0)
-        for (int i = 0; i < P; ++i) issue_next();
+    // this lane's items of a chunk, as NP step pairs in an order rotated by g
+    // (conflict-free shared-memory rows); the same mapping on both warps
+    int tas[NP];
+#pragma unroll
+    for (int j = 0; j < NP; ++j) tas[j] = g * KR + 2 * ((j + g) % NP);
 
-    int consumed = 0;   // chunks waited for (every lane tracks it)
-    int oslot = 0;
     bool ok = true;
+    if (helper) {
+        // ------------------------------------------------------------ helper
+        constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
+        int pf_task = wid, pf_c = 0, pf_end = 0, issued = 0;
+        int pf_b = 0, pf_d0 = 0;
+        const T* pf_bc = nullptr;
+        auto pf_enter = [&](int task) {
+            const int sgm = task / p.M, m = task - sgm * p.M;
+            pf_b = m / p.units;
+            pf_d0 = (m - pf_b * p.units) * CW;
+            pf_c = sgm * p.cps;
+            pf_end = min(pf_c + p.cps, nch);
+            pf_bc = static_cast<const T*>(p.bc) + ((size_t)pf_b * p.lpad + (size_t)pf_c * K) * (2 * N);
+        };
+        if (pf_task < T_total) pf_enter(pf_task);
+        auto issue_next = [&]() {   // lane 0 only
+            while (pf_task < T_total && pf_c >= pf_end) {
+                pf_task += p.workers;
+                if (pf_task < T_total) pf_enter(pf_task);
+            }
+            if (pf_task >= T_total) return;
+            const int slot = issued & (P - 1);
+            const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
+            const uint32_t bar = bar_full + 8u * (uint32_t)slot;
+            const int t0 = pf_c * K;
+            mbar_expect_tx(bar, tx_bytes);
+            tma_load_3d(base + CF::SLOT_U, &tm_u, pf_d0, t0, pf_b, bar);
+            tma_load_3d(base + CF::SLOT_D, &tm_d, pf_d0, t0, pf_b, bar);
+            if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, pf_d0, t0, pf_b, bar);
+            bulk_load(base + CF::SLOT_BC, pf_bc, CF::BC, bar);
+            pf_bc += K * 2 * N;
+            ++pf_c;
+            ++issued;
+        };
+        if (lane == 0)
+            for (int i = 0; i < P; ++i) issue_next();
+
+        int j = 0;        // chunk sequence number of this worker
+        int landed = 0;   // chunks whose loads this warp has waited for
+        for (int task = wid; task < T_total && ok; task += p.workers) {
+            const int sgm = task / p.M, m = task - sgm * p.M;
+            const int b = m / p.units;
+            const int d = (m - b * p.units) * CW + ch;
+            const bool ch_ok = d < p.dim;
+            const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
+            const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
+            for (int c = cb; c < ce; ++c, ++j) {
+                const int buf = j & 1;
+                if (j >= 2) {
+                    // the main warp finished chunk j-2: its buffers and ring slot are free
+                    if (!__all_sync(0xffffffffu, mbar_wait(bar_done + 8u * buf, (uint32_t)(((j - 2) >> 1) & 1)))) {
+                        ok = false;
+                        if (lane == 0) raise_error(2u);
+                        break;
+                    }
+                    if (lane == 0) issue_next();
+                }
+                const int slot = j & (P - 1);
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(1u);
+                    break;
+                }
+                ++landed;
+                const unsigned char* sb = pb + CF::P_RING + slot * CF::SLOT;
+                const T* su = reinterpret_cast<const T*>(sb + CF::SLOT_U);
+                const T* sd = reinterpret_cast<const T*>(sb + CF::SLOT_D);
+                const T* sz = reinterpret_cast<const T*>(sb + CF::SLOT_Z);
+                const int t0 = c * K;
+                const bool tail = t0 + K > L;
+                float2 uk[NP], xr[NP], zr[NP];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    const int ta = tas[q], tb = ta + 1;
+                    uk[q] = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
+                    xr[q] = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
+                    if constexpr (kGate) zr[q] = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
+                }
+                float2 dpv[2 * NP], sgv[2 * NP];
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    float2 dl = add2(xr[q], bias2);
+                    if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
+                    if (tail) dl = mul2(dl, make_float2(t0 + tas[q] < L ? 1.f : 0.f, t0 + tas[q] + 1 < L ? 1.f : 0.f));
+                    const float2 du = mul2(dl, uk[q]);
+                    float2 gt = splat2(1.f);
+                    if constexpr (kGate) gt = seg_silu2<kFast>(zr[q]);
+                    dpv[2 * q] = make_float2(dl.x, du.x);
+                    dpv[2 * q + 1] = make_float2(dl.y, du.y);
+                    sgv[2 * q] = make_float2(uk[q].x, gt.x);
+                    sgv[2 * q + 1] = make_float2(uk[q].y, gt.y);
+                }
+                float2* dp = dpb + buf * (K * CW);
+                float2* sg = sgb + buf * (K * CW);
+#pragma unroll
+                for (int q = 0; q < NP; ++q) {
+                    dp[tas[q] * CW + ch] = dpv[2 * q];
+                    dp[(tas[q] + 1) * CW + ch] = dpv[2 * q + 1];
+                    sg[tas[q] * CW + ch] = sgv[2 * q];
+                    sg[(tas[q] + 1) * CW + ch] = sgv[2 * q + 1];
+                }
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_dpf + 8u * buf);
+            }
+        }
+        // Drain: every issued load must land before shared memory is released.
+        if (!ok) {
+            const int iss = __shfl_sync(0xffffffffu, issued, 0);
+            for (int k = landed; k < iss; ++k)
+                if (!mbar_wait(bar_full + 8u * (uint32_t)(k & (P - 1)), (uint32_t)((k / P) & 1))) break;
+        }
+        return;
+    }
+
+    // ---------------------------------------------------------------- main
+    int j = 0;
+    int oslot = 0;
     for (int task = wid; task < T_total && ok; task += p.workers) {
         const int sgm = task / p.M, m = task - sgm * p.M;
         const int b = m / p.units;
@@ -676,7 +795,6 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             A2[0] = make_float2(a.x * kLog2e, a.y * kLog2e);
             A2[1] = make_float2(a.z * kLog2e, a.w * kLog2e);
         }
-        const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
         const float2 dskip2 = splat2((p.D && ch_ok) ? p.D[d] : 0.f);
 
         // state entering the segment
@@ -693,83 +811,43 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             h1 = make_float2(v.z, v.w);
         }
 
-        for (int c = cb; c < ce; ++c) {
-            const int slot = consumed & (P - 1);
-            const unsigned char* sb = wbase + CF::W_RING + slot * CF::SLOT;
-            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * (uint32_t)slot, (uint32_t)((consumed / P) & 1)))) {
+        for (int c = cb; c < ce; ++c, ++j) {
+            const int buf = j & 1;
+            const int slot = j & (P - 1);
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_dpf + 8u * buf, (uint32_t)((j >> 1) & 1)) &&
+                                             mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1)))) {
                 ok = false;
-                if (lane == 0) raise_error(1u);
+                if (lane == 0) raise_error(2u);
                 break;
             }
-            ++consumed;
             const int t0 = c * K;
-            const bool tail = t0 + K > L;
-
-            // ---- per-(t, d) terms of this lane's KR steps, as NP step pairs.
-            // Lane g owns steps g*KR .. g*KR+KR-1; it visits its pairs in an
-            // order rotated by g, so the R lanes of a channel read rows that
-            // fall in different banks (register index j is fixed, only the
-            // addresses rotate).
-            constexpr int NP = KR / 2;
-            const T* su = reinterpret_cast<const T*>(sb + CF::SLOT_U);
-            const T* sd = reinterpret_cast<const T*>(sb + CF::SLOT_D);
-            const T* sz = reinterpret_cast<const T*>(sb + CF::SLOT_Z);
-            // All shared-memory loads of the phase come first, then the math,
-            // then the stores: the tiles, the Delta buffer and the reduction
-            // buffer are all shared memory, so a load placed after a store
-            // could not be moved above it.
-            float2 uk[NP], xr[NP], zr[NP], gate[NP];
-            int tas[NP];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                tas[j] = g * KR + 2 * ((j + g) % NP);
-                const int ta = tas[j], tb = ta + 1;
-                uk[j] = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
-                xr[j] = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
-                if constexpr (kGate) zr[j] = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
-            }
-            float4 dpv[2 * NP];
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                float2 dl = add2(xr[j], bias2);
-                if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
-                if (tail) dl = mul2(dl, make_float2(t0 + tas[j] < L ? 1.f : 0.f, t0 + tas[j] + 1 < L ? 1.f : 0.f));
-                const float2 du = mul2(dl, uk[j]);
-                if constexpr (kGate) gate[j] = seg_silu2<kFast>(zr[j]);
-                else gate[j] = splat2(1.f);
-                dpv[2 * j] = make_float4(dl.x, dl.x, du.x, du.x);
-                dpv[2 * j + 1] = make_float4(dl.y, dl.y, du.y, du.y);
-            }
-#pragma unroll
-            for (int j = 0; j < NP; ++j) {
-                dp[tas[j] * CW + ch] = dpv[2 * j];
-                dp[(tas[j] + 1) * CW + ch] = dpv[2 * j + 1];
-            }
-            __syncwarp();
+            const float2* dp = dpb + buf * (K * CW);
+            const float2* sg = sgb + buf * (K * CW);
+            const T* sbc = reinterpret_cast<const T*>(pb + CF::P_RING + slot * CF::SLOT + CF::SLOT_BC);
 
             // ---- the recurrence as a software pipeline over the chunk's K steps:
             // step t loads the Delta/B/C rows of step t+LA, evaluates
             // exp(Delta A) and Delta B u of step t+EA, advances the state by
             // step t (one packed FMA per two states: the only serial work) and
-            // reads out C_t . h_t.  Everything is unrolled, so the stages of
-            // different steps interleave in the instruction stream.
-            const float* sbc = reinterpret_cast<const float*>(sb + CF::SLOT_BC);
+            // reads out C_t . h_t.
             constexpr int LA = 4, EA = 2;
-            float4 qv[K], bv[K], cv[K];
+            float2 qv[K];
+            float4 bv[K], cv[K];
             float2 dA[K][2], dB[K][2];
             float2 s2v[K / 2];
             auto load_step = [&](int t) {
                 qv[t] = dp[t * CW + ch];
-                bv[t] = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + 4 * g);
-                cv[t] = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + N + 4 * g);
+                bv[t] = ld_quad<T>(sbc + t * (2 * N) + 4 * g);
+                cv[t] = ld_quad<T>(sbc + t * (2 * N) + N + 4 * g);
             };
             auto exp_step = [&](int t) {
-                const float2 e0 = mul2(make_float2(qv[t].x, qv[t].y), A2[0]);
-                const float2 e1 = mul2(make_float2(qv[t].x, qv[t].y), A2[1]);
+                const float2 dl2 = splat2(qv[t].x), du2 = splat2(qv[t].y);
+                const float2 e0 = mul2(dl2, A2[0]);
+                const float2 e1 = mul2(dl2, A2[1]);
                 dA[t][0] = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
                 dA[t][1] = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
-                dB[t][0] = mul2(make_float2(qv[t].z, qv[t].w), make_float2(bv[t].x, bv[t].y));
-                dB[t][1] = mul2(make_float2(qv[t].z, qv[t].w), make_float2(bv[t].z, bv[t].w));
+                dB[t][0] = mul2(du2, make_float2(bv[t].x, bv[t].y));
+                dB[t][1] = mul2(du2, make_float2(bv[t].z, bv[t].w));
             };
 #pragma unroll
             for (int t = 0; t < LA; ++t) load_step(t);
@@ -786,53 +864,57 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 if (t & 1) s2v[t / 2] = make_float2(acc_prev.x + acc_prev.y, acc.x + acc.y);
                 acc_prev = acc;
             }
-            float2 ys[R == 1 ? K / 2 : 1];
-#pragma unroll
-            for (int t = 0; t < K / 2; ++t) {
-                if constexpr (R == 1) ys[t] = s2v[t];
-                else red[t * RS2 + lane] = s2v[t];
-            }
 
             // ---- sum the R lanes of each channel for this lane's pairs (same rotation)
             float2 yv[NP];
             if constexpr (R == 1) {
 #pragma unroll
-                for (int j = 0; j < NP; ++j) yv[j] = ys[j];
+                for (int q = 0; q < NP; ++q) yv[q] = s2v[tas[q] / 2];
             } else {
+#pragma unroll
+                for (int t = 0; t < K / 2; ++t) red[t * RS2 + lane] = s2v[t];
                 __syncwarp();
                 float2 pr[NP][R];
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    const float2* row = red + (g * NP + (j + g) % NP) * RS2 + ch * R;
+                for (int q = 0; q < NP; ++q) {
+                    const float2* row = red + (tas[q] / 2) * RS2 + ch * R;
 #pragma unroll
-                    for (int gg = 0; gg < R; ++gg) pr[j][gg] = row[gg];
+                    for (int gg = 0; gg < R; ++gg) pr[q][gg] = row[gg];
                 }
 #pragma unroll
-                for (int j = 0; j < NP; ++j) {
-                    float2 sum = pr[j][0];
+                for (int q = 0; q < NP; ++q) {
+                    float2 sum = pr[q][0];
 #pragma unroll
-                    for (int gg = 1; gg < R; ++gg) sum = add2(sum, pr[j][gg]);
-                    yv[j] = sum;
+                    for (int gg = 1; gg < R; ++gg) sum = add2(sum, pr[q][gg]);
+                    yv[q] = sum;
                 }
             }
 
-            // ---- D skip, gate, output tile (triple-buffered; lane 0 owns the TMA
-            // store groups: before this tile is rewritten, the store that last
-            // read it -- three chunks ago -- must have finished reading)
-            T* so = reinterpret_cast<T*>(wbase + CF::W_OUT + oslot * CF::OUT);
+            // ---- D u, gate, output tile (triple-buffered; lane 0 owns the TMA
+            // store groups: before a tile is rewritten, the store that read it
+            // three chunks ago must have finished reading)
+            float2 sgl[2 * NP];
+#pragma unroll
+            for (int q = 0; q < NP; ++q) {
+                sgl[2 * q] = sg[tas[q] * CW + ch];
+                sgl[2 * q + 1] = sg[(tas[q] + 1) * CW + ch];
+            }
+            T* so = reinterpret_cast<T*>(pb + CF::P_OUT + oslot * CF::OUT);
             if (lane == 0) bulk_wait_read<2>();
             __syncwarp();
-            float2 yo[NP];
 #pragma unroll
-            for (int j = 0; j < NP; ++j) yo[j] = mul2(fma2(dskip2, uk[j], yv[j]), gate[j]);
-#pragma unroll
-            for (int j = 0; j < NP; ++j) st_pair<T>(so + tas[j] * CW + ch, so + (tas[j] + 1) * CW + ch, yo[j]);
+            for (int q = 0; q < NP; ++q) {
+                const float2 uq = make_float2(sgl[2 * q].x, sgl[2 * q + 1].x);
+                const float2 gq = make_float2(sgl[2 * q].y, sgl[2 * q + 1].y);
+                const float2 y = mul2(fma2(dskip2, uq, yv[q]), gq);
+                st_pair<T>(so + tas[q] * CW + ch, so + (tas[q] + 1) * CW + ch, y);
+            }
             fence_async_smem();
             __syncwarp();
             if (lane == 0) {
                 tma_store_3d(&tm_out, d0, t0, b, smem_u32(so));
                 bulk_commit();
-                issue_next();
+                mbar_arrive(bar_done + 8u * buf);   // buffers and ring slot of chunk j are free
             }
             oslot = oslot == 2 ? 0 : oslot + 1;
         }
@@ -849,21 +931,15 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
                 make_float4(h0.x, h0.y, h1.x, h1.y);
         }
     }
-
-    // Drain: every issued load must land before shared memory is released.
-    if (!ok) {
-        const int iss = __shfl_sync(0xffffffffu, issued, 0);
-        for (int j = consumed; j < iss; ++j)
-            if (!mbar_wait(bar_full + 8u * (uint32_t)(j & (P - 1)), (uint32_t)((j / P) & 1))) break;
-    }
     if (lane == 0) bulk_wait_all();
 }
 
-// B and C (batch, N, L) -> staged float32 rows [batch][lpad][B_0..B_{N-1}, C_0..C_{N-1}],
-// zero beyond L.  One CTA per (64-step tile, batch row), transposed through shared memory.
-template <typename T, int N>
+// B and C (batch, N, L) -> staged rows [batch][lpad][B_0..B_{N-1}, C_0..C_{N-1}] of
+// type O (float32 for the relay kernel; the activation type for the segmented
+// kernel, so that its per-step reads move half the bytes), zero beyond L.  One CTA per (64-step tile, batch row), transposed through shared memory.
+template <typename T, int N, typename O = float>
 __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, const T* __restrict__ C,
-                                                       float* __restrict__ bc, int64_t L, int64_t lpad,
+                                                       O* __restrict__ bc, int64_t L, int64_t lpad,
                                                        int* __restrict__ flags, int nflags) {
     constexpr int TT = 64;
     if (flags && blockIdx.x == 0 && blockIdx.y == 0)
@@ -881,7 +957,7 @@ __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, 
     for (int i = threadIdx.x; i < 2 * N * TT; i += blockDim.x) {
         const int t = i / (2 * N), col = i % (2 * N);
         const int64_t tt = t0 + t;
-        if (tt < lpad) bc[(b * lpad + tt) * (2 * N) + col] = tile[t][col];
+        if (tt < lpad) bc[(b * lpad + tt) * (2 * N) + col] = from_f32<O>(tile[t][col]);
     }
 }
 
@@ -962,7 +1038,7 @@ struct SegPlan {
 
 template <int N, int K>
 SegPlan seg_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms, int ctas_per_sm) {
-    constexpr int CW = 32 / (N / 4), WARPS = 4;
+    constexpr int CW = 32 / (N / 4), WARPS = 4;   // workers (warp pairs) per CTA
     SegPlan pl{};
     pl.units = (int)((dim + CW - 1) / CW);
     pl.M = (int)(batch * pl.units);
@@ -1025,15 +1101,15 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
     const SegPlan pl = seg_plan<N, CF::K>(a.batch, a.dim, a.seqlen, sms, occ[which]);
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
-    float* bc = reinterpret_cast<float*>(w);
-    const int64_t bc_bytes = (a.batch * lpad * 2 * N * 4 + 255) / 256 * 256;
+    T* bc = reinterpret_cast<T*>(w);
+    const int64_t bc_bytes = (a.batch * lpad * 2 * N * (int64_t)sizeof(T) + 255) / 256 * 256;
     float* st = reinterpret_cast<float*>(w + bc_bytes);
     const int64_t st_bytes = ((int64_t)pl.M * CF::CW * N * 4 + 255) / 256 * 256;
     int* flags = reinterpret_cast<int*>(w + bc_bytes + st_bytes);
     {
         dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)a.batch);
-        bc_stage_kernel<T, N><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
-                                                   a.seqlen, lpad, flags, pl.M);
+        bc_stage_kernel<T, N, T><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
+                                                      a.seqlen, lpad, flags, pl.M);
     }
     CUtensorMap mu, md, mz, mo;
     if (!make_map<T>(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
@@ -1053,11 +1129,11 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
 
 }  // namespace
 
-int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
+int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes) {
     const int cw = 32 / (dstate / 4);
     const int64_t units = (dim + cw - 1) / cw;
     const int64_t M = batch * units;
-    const int64_t bc_bytes = (batch * relay_lpad(seqlen) * 2 * dstate * 4 + 255) / 256 * 256;
+    const int64_t bc_bytes = (batch * relay_lpad(seqlen) * 2 * dstate * elem_bytes + 255) / 256 * 256;
     const int64_t st_bytes = (M * cw * dstate * 4 + 255) / 256 * 256;
     return bc_bytes + st_bytes + (M * 4 + 255) / 256 * 256;
 }
@@ -1079,7 +1155,7 @@ cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* ws, int sms, cuda
     return cudaErrorInvalidValue;
 }
 
-int64_t relay_lpad(int64_t seqlen) { return (seqlen + 31) / 32 * 32; }
+int64_t relay_lpad(int64_t seqlen) { return (seqlen + 63) / 64 * 64; }
 
 int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate) {
     return batch * relay_lpad(seqlen) * 2 * dstate * (int64_t)sizeof(float);

@@ -128,7 +128,7 @@ int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
     return std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate),
-                    ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate));
+                    ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4));
 }
 
 int ssm_device_error(int clear) { return ssm::read_device_error(clear != 0); }
@@ -176,23 +176,23 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The relay scan runs whenever its layout and workspace requirements hold;
-    // SSM_SCAN_PATH=seg|generic forces another kernel (tests use it).
+    // The segmented scan runs whenever its layout and workspace requirements
+    // hold; SSM_SCAN_PATH=relay|generic forces another kernel (tests use it).
     const char* force = std::getenv("SSM_SCAN_PATH");
     // (chains * 64 segments must stay a 32-bit task count)
     const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
                          batch * ((dim + 127) / 128 * dstate) * 64 < (int64_t(1) << 31);
-    if (force && std::strcmp(force, "seg") == 0) {
-        if (!fast_ok || workspace_bytes < ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate))
+    if (force && std::strcmp(force, "relay") == 0) {
+        if (!fast_ok || workspace_bytes < ssm::relay_workspace_bytes(batch, seqlen, (int)dstate))
             return SSM_ERR_UNSUPPORTED;
-        return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
+        return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
     }
     const bool want_generic = force && std::strcmp(force, "generic") == 0;
     if (!want_generic && fast_ok &&
-        workspace_bytes >= ssm::relay_workspace_bytes(batch, seqlen, (int)dstate)) {
-        return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
+        workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es)) {
+        return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
     }
-    if (force && std::strcmp(force, "relay") == 0) return SSM_ERR_UNSUPPORTED;
+    if (force && std::strcmp(force, "seg") == 0) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
     return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
 }

@@ -67,7 +67,7 @@ bool relay_supported(const ScanArgs& a, DType dt);
 cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cudaStream_t s);
 // Segmented direct scan (scan_relay.cu): needs staged B/C plus the segment
 // hand-off state and flags (seg_workspace_bytes).
-int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
+int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes);
 cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
 int read_device_error(bool clear);
 

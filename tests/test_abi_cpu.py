@@ -124,22 +124,25 @@ def test_binding_raises_without_cuda_tensors():
         _lib.ssm_scan_fwd(u, u, A, B, B)
 
 
-def _ws_expected(batch, dim, seqlen, dstate):
-    """B and C staged as float32 rows (sequence padded to 32 steps), plus, for
-    the segmented scan, one float32 state per (chain, channel, state) and one
-    int flag per chain; each part rounded up to 256 bytes."""
+def _ws_expected(batch, dim, seqlen, dstate, es):
+    """The larger of the two fast paths' needs: B and C staged as float32 rows
+    (sequence padded to 64 steps), or B and C staged in the activation type
+    (es bytes) plus one float32 state per (chain, channel, state) and one int
+    flag per chain, each part rounded up to 256 bytes."""
     up = lambda x: (x + 255) // 256 * 256
-    lpad = (seqlen + 31) // 32 * 32
-    bc = batch * lpad * 2 * dstate * 4
+    lpad = (seqlen + 63) // 64 * 64
     cw = 32 // (dstate // 4)
     chains = batch * ((dim + cw - 1) // cw)
-    return max(bc, up(bc) + up(chains * cw * dstate * 4) + up(chains * 4))
+    relay = batch * lpad * 2 * dstate * 4
+    seg = up(batch * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
+    return max(relay, seg)
 
 
 def test_workspace_size_query(lib):
     for args in [(1, 5120, 131072, 16), (3, 7, 77, 8), (1, 1, 1, 4), (8, 2048, 2048, 16), (2, 100, 33, 8)]:
-        assert lib.ssm_scan_workspace_bytes(*args, 1) == _ws_expected(*args), args
-    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 16777216 + 327680 + 2560
+        assert lib.ssm_scan_workspace_bytes(*args, 1) == _ws_expected(*args, 2), args
+        assert lib.ssm_scan_workspace_bytes(*args, 0) == _ws_expected(*args, 4), args
+    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 0) == 16777216 + 327680 + 2560
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 5, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 0, 64, 16, 1) == -1
