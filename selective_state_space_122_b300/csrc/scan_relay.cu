@@ -52,118 +52,13 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "scan_common.cuh"
 #include "ssm_internal.cuh"
 
 namespace ssm {
 
-__device__ unsigned int g_device_error = 0;
-
 namespace {
 
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
-
-// ------------------------------------------------------------- PTX wrappers
-
-__device__ __forceinline__ uint32_t smem_u32(const void* p) {
-    return static_cast<uint32_t>(__cvta_generic_to_shared(p));
-}
-
-__device__ __forceinline__ unsigned long long globaltimer() {
-    unsigned long long t;
-    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
-    return t;
-}
-
-__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
-    asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
-}
-
-__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
-    asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
-}
-
-__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
-    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
-}
-
-__device__ __forceinline__ bool mbar_try(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-__device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
-    uint32_t ok;
-    asm volatile(
-        "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
-        " selp.u32 %0, 1, 0, p;\n}"
-        : "=r"(ok)
-        : "r"(bar), "r"(parity)
-        : "memory");
-    return ok != 0;
-}
-
-#ifndef SSM_RELAY_SPIN
-#define SSM_RELAY_SPIN 0
-#endif
-
-// Wait for the phase with the given parity to complete; false after ~1 s.
-__device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
-    const unsigned long long t0 = globaltimer();
-    while (!(SSM_RELAY_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)))
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
-    return true;
-}
-
-__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (SSM_RELAY_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
-    return mbar_wait_slow(bar, parity);
-}
-
-__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
-                                            uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes, uint32_t bar) {
-    asm volatile(
-        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
-        ::"r"(dst), "l"(reinterpret_cast<uint64_t>(src)), "r"(bytes), "r"(bar)
-        : "memory");
-}
-
-__device__ __forceinline__ void tma_store_3d(const CUtensorMap* map, int c0, int c1, int c2, uint32_t src) {
-    asm volatile("cp.async.bulk.tensor.3d.global.shared::cta.bulk_group [%0, {%1, %2, %3}], [%4];"
-                 ::"l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(src)
-                 : "memory");
-}
-
-__device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
-
-template <int Nn>
-__device__ __forceinline__ void bulk_wait_read() {
-    asm volatile("cp.async.bulk.wait_group.read %0;" ::"n"(Nn) : "memory");
-}
-
-__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
-
-__device__ __forceinline__ void fence_async_smem() {
-    asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
-}
-
-__device__ __forceinline__ void fence_mbar_init() {
-    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-}
-
-__device__ __forceinline__ void raise_error(unsigned int bit) { atomicOr(&g_device_error, bit); }
 
 // ------------------------------------------------------------- configuration
 
@@ -220,41 +115,6 @@ struct RelayParams {
     int has_z;
 };
 
-template <typename T>
-__device__ __forceinline__ float ld_elem(const T* p);
-template <>
-__device__ __forceinline__ float ld_elem<float>(const float* p) { return *p; }
-template <>
-__device__ __forceinline__ float ld_elem<__nv_bfloat16>(const __nv_bfloat16* p) { return __bfloat162float(*p); }
-
-template <typename T>
-__device__ __forceinline__ void st_pair(T* p0, T* p1, float2 v);
-template <>
-__device__ __forceinline__ void st_pair<float>(float* p0, float* p1, float2 v) {
-    *p0 = v.x;
-    *p1 = v.y;
-}
-template <>
-__device__ __forceinline__ void st_pair<__nv_bfloat16>(__nv_bfloat16* p0, __nv_bfloat16* p1, float2 v) {
-    const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
-    *p0 = b.x;
-    *p1 = b.y;
-}
-
-// softplus(x) = max(x, 0) + log1p(exp(-|x|)) with log1p(e) = ln2 * log2(1 + e):
-// branch-free, absolute error about 1e-7 (the rounding of 1 + e).
-__device__ __forceinline__ float2 softplus_lean2(float2 x) {
-    const float2 e = make_float2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
-    const float2 w = add2(e, splat2(1.f));
-    const float2 l = make_float2(lg2_approx(w.x), lg2_approx(w.y));
-    return fma2(l, splat2(kLn2), make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
-}
-
-template <bool kFast>
-__device__ __forceinline__ float2 relay_softplus2(float2 x) {
-    if constexpr (kFast) return softplus_lean2(x);
-    else return make_float2(softplus_acc(x.x), softplus_acc(x.y));
-}
 
 template <typename T, int N, bool kFast, bool kSoftplus, bool kGate>
 __global__ void __launch_bounds__(RelayCfg<T, N>::THREADS, RelayCfg<T, N>::MIN_CTAS)
@@ -498,25 +358,6 @@ scan_relay_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
 // different warps take in turn, so the work divides evenly over all warps.
 // ===================================================================
 
-__device__ __forceinline__ float tanh_approx(float x) {
-    float y;
-    asm("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
-    return y;
-}
-
-// silu(z) = z * sigmoid(z) = (z/2) * (1 + tanh(z/2)): one SFU operation.
-// tanh.approx has an absolute error below 2^-10.9, so the gate is accurate to
-// about 5e-4 * |z| / 2 -- below the rounding of a bfloat16 output.
-template <bool kFast>
-__device__ __forceinline__ float2 seg_silu2(float2 z) {
-    if constexpr (kFast) {
-        const float2 hz = mul2(z, splat2(0.5f));
-        const float2 t = make_float2(tanh_approx(hz.x), tanh_approx(hz.y));
-        return fma2(hz, t, hz);
-    } else {
-        return make_float2(silu_acc(z.x), silu_acc(z.y));
-    }
-}
 
 // Four consecutive staged values as float32: one 8-byte shared load and a
 // bit-shift unpack for bf16, one 16-byte load for float32.

@@ -127,11 +127,17 @@ int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int
     if (dim <= 0 || dim > (int64_t(1) << 31)) return -1;
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
-    return std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate),
-                    ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4));
+    int64_t need = std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate),
+                            ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4));
+    if (dtype == SSM_BF16) need = std::max(need, ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate));
+    return need;
 }
 
-int ssm_device_error(int clear) { return ssm::read_device_error(clear != 0); }
+int ssm_device_error(int clear) {
+    const int a = ssm::read_device_error(clear != 0);
+    const int b = ssm::read_tmem_device_error(clear != 0);
+    return (a < 0 || b < 0) ? -1 : (a | b);
+}
 
 ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
                         const void* C, const float* D, const void* z, const float* delta_bias,
@@ -176,8 +182,9 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The segmented scan runs whenever its layout and workspace requirements
-    // hold; SSM_SCAN_PATH=relay|generic forces another kernel (tests use it).
+    // The tensor-memory scan runs whenever its requirements hold (bf16, 16
+    // states), else the segmented scan; SSM_SCAN_PATH=tmem|seg|relay|generic
+    // forces one kernel (tests use it).
     const char* force = std::getenv("SSM_SCAN_PATH");
     // (chains * 64 segments must stay a 32-bit task count)
     const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
@@ -188,11 +195,19 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
         return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
     }
     const bool want_generic = force && std::strcmp(force, "generic") == 0;
+    const bool want_seg = force && std::strcmp(force, "seg") == 0;
+    const bool tmem_ok = fast_ok && ssm::tmem_supported(a, dt) &&
+                         workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate);
+    if (force && std::strcmp(force, "tmem") == 0) {
+        if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st));
+    }
+    if (!want_generic && !want_seg && tmem_ok) return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st));
     if (!want_generic && fast_ok &&
         workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es)) {
         return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
     }
-    if (force && std::strcmp(force, "seg") == 0) return SSM_ERR_UNSUPPORTED;
+    if (want_seg) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
     return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
 }

@@ -69,6 +69,13 @@ cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cuda
 // hand-off state and flags (seg_workspace_bytes).
 int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes);
 cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
+
+// Tensor-memory scan (scan_tmem.cu): bf16 activations, 16 states.  Workspace:
+// the staged one-hot MMA operands of B and C plus the segment hand-off state.
+bool tmem_supported(const ScanArgs& a, DType dt);
+int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
+cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
+int read_tmem_device_error(bool clear);
 int read_device_error(bool clear);
 
 int scan_layout_count(int dstate);

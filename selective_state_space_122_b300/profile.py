@@ -1,7 +1,7 @@
 """Profiling drivers for the selective-scan library (run on a CUDA device).
 
     python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
-           [--N N] [--iters K] [--path relay|seg|generic]
+           [--N N] [--iters K] [--path tmem|seg|relay|generic]
     python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K]
     python -m selective_state_space_122_b300.profile units
 
@@ -116,7 +116,7 @@ def main(argv=None):
     s.add_argument("--L", type=int, default=16384)
     s.add_argument("--N", type=int, default=16)
     s.add_argument("--iters", type=int, default=3)
-    s.add_argument("--path", default=None, choices=[None, "relay", "seg", "generic"])
+    s.add_argument("--path", default=None, choices=[None, "tmem", "relay", "seg", "generic"])
     d = sub.add_parser("decode")
     d.add_argument("--batch", type=int, default=256)
     d.add_argument("--dim", type=int, default=5120)

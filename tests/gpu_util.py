@@ -90,22 +90,30 @@ def relay_ok(dim: int, dtype: str) -> bool:
     return (dim * (2 if dtype == inputs.BF16 else 4)) % 16 == 0
 
 
+def tmem_ok(N: int, dim: int, dtype: str) -> bool:
+    """Whether the tensor-memory path takes the shape: bf16, 16 states, TMA rows."""
+    return N == 16 and dtype == inputs.BF16 and relay_ok(dim, dtype)
+
+
 def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
-    """Every way to run a scan of this shape: the segmented and relay paths
-    (when they accept the shape) and each generic layout."""
-    return (["seg", "relay"] if relay_ok(dim, dtype) else []) + list(range(LAYOUTS[N]))
+    """Every way to run a scan of this shape: the tensor-memory, segmented and
+    relay paths (when they accept the shape) and each generic layout."""
+    fast = ["seg", "relay"] if relay_ok(dim, dtype) else []
+    if tmem_ok(N, dim, dtype):
+        fast = ["tmem"] + fast
+    return fast + list(range(LAYOUTS[N]))
 
 
 @contextlib.contextmanager
 def scan_layout(layout):
-    """Force a path: None = the library's own choice, "seg" / "relay" = that
-    TMA kernel (an error if it cannot take the shape), an int = that layout
-    of the generic kernel."""
+    """Force a path: None = the library's own choice, "tmem" / "seg" / "relay"
+    = that TMA kernel (an error if it cannot take the shape), an int = that
+    layout of the generic kernel."""
     keys = ("SSM_SCAN_LAYOUT", "SSM_SCAN_PATH")
     old = {k: os.environ.get(k) for k in keys}
     for k in keys:
         os.environ.pop(k, None)
-    if layout in ("relay", "seg"):
+    if layout in ("relay", "seg", "tmem"):
         os.environ["SSM_SCAN_PATH"] = layout
     elif layout is not None:
         os.environ["SSM_SCAN_PATH"] = "generic"

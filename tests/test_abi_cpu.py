@@ -125,17 +125,23 @@ def test_binding_raises_without_cuda_tensors():
 
 
 def _ws_expected(batch, dim, seqlen, dstate, es):
-    """The larger of the two fast paths' needs: B and C staged as float32 rows
-    (sequence padded to 64 steps), or B and C staged in the activation type
-    (es bytes) plus one float32 state per (chain, channel, state) and one int
-    flag per chain, each part rounded up to 256 bytes."""
+    """The largest of the fast paths' needs, each part rounded up to 256 bytes:
+    B and C staged as float32 rows (sequence padded to 64 steps); B and C
+    staged in the activation type (es bytes) plus one float32 state per
+    (chain, channel, state) and one int flag per chain; and, for bf16 with 16
+    states, the tensor-memory path's one-hot operands (32 float32 per step)
+    plus its state and flags over 32-channel CTA groups of four warps."""
     up = lambda x: (x + 255) // 256 * 256
     lpad = (seqlen + 63) // 64 * 64
     cw = 32 // (dstate // 4)
     chains = batch * ((dim + cw - 1) // cw)
     relay = batch * lpad * 2 * dstate * 4
     seg = up(batch * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
-    return max(relay, seg)
+    need = max(relay, seg)
+    if es == 2 and dstate == 16:
+        tchains = batch * ((dim + 31) // 32) * 4
+        need = max(need, up(batch * lpad * 32 * 4) + up(tchains * 8 * 16 * 4) + up(tchains * 4))
+    return need
 
 
 def test_workspace_size_query(lib):
@@ -143,6 +149,7 @@ def test_workspace_size_query(lib):
         assert lib.ssm_scan_workspace_bytes(*args, 1) == _ws_expected(*args, 2), args
         assert lib.ssm_scan_workspace_bytes(*args, 0) == _ws_expected(*args, 4), args
     assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 0) == 16777216 + 327680 + 2560
+    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 16777216 + 327680 + 2560
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 5, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 0, 64, 16, 1) == -1

@@ -8,7 +8,7 @@ import pytest
 import torch
 
 import oracle
-from gpu_util import (LAYOUTS, check_out, check_state, dev, host_f64, paths, scan_layout, scan_on_gpu,
+from gpu_util import (LAYOUTS, tmem_ok, check_out, check_state, dev, host_f64, paths, scan_layout, scan_on_gpu,
                       state_rel_err)
 from selective_state_space_122_b300 import inputs, ssm_scan_fwd
 
@@ -47,7 +47,7 @@ def layer130m():
     return inp, oracle_of(inp)
 
 
-@pytest.mark.parametrize("g", [None, "seg", "relay"] + list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("g", [None, "tmem", "seg", "relay"] + list(range(LAYOUTS[16])))
 def test_layer130m_full(layer130m, g):
     inp, (ref, ref_last) = layer130m
     with scan_layout(g):
@@ -138,16 +138,34 @@ def test_ragged_shapes(bt, dim, L, N):
 @pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
 @pytest.mark.parametrize("bt,dim,L,N", [(1, 8, 1, 16), (2, 24, 77, 8), (3, 40, 65, 4), (1, 16, 7, 16),
                                          (2, 72, 200, 16), (1, 48, 9, 8), (2, 8, 1000, 16)])
-@pytest.mark.parametrize("path", ["seg", "relay"])
+@pytest.mark.parametrize("path", ["tmem", "seg", "relay"])
 def test_tma_paths_ragged(bt, dim, L, N, dtype, path):
     """The TMA paths on sequence ends that are not whole chunks, units whose
     last channels fall beyond dim, and sequences shorter than one chunk."""
+    if path == "tmem" and not tmem_ok(N, dim, dtype):
+        pytest.skip("the tensor-memory path takes bf16 with 16 states only")
     inp = inputs.make_scan_inputs(inputs.ScanShape("tma-ragged", bt, dim, L, N, dtype), 7 * dim + L)
     ref, ref_last = oracle_of(inp)
     with scan_layout(path):
         out, last = scan_on_gpu(inp)
     check_out(host_f64(out), ref, dtype)
     check_state(host_f64(last), ref_last, dtype)
+
+
+@pytest.mark.parametrize("bt,dim,L", [(1, 5120, 4096), (1, 5120, 20000), (5, 1024, 777), (2, 4800, 3000)])
+def test_tmem_multisegment_schedule(bt, dim, L):
+    """The tensor-memory path with more 32-channel groups than SMs: each group's
+    sequence is cut into segments taken by different CTAs in turn, the state
+    handed on through the workspace.  The oracle recomputes a spread of
+    channels, all segments of each."""
+    inp = inputs.make_scan_inputs(inputs.ScanShape("tmem-multi", bt, dim, L, 16, inputs.BF16), 13 * bt + L)
+    with scan_layout("tmem"):
+        out, last = scan_on_gpu(inp)
+    sel = long_seq_sample(dim)
+    ref, ref_last = oracle_of(inp, sel)
+    idx = torch.as_tensor(sel, device=out.device)
+    check_out(host_f64(out[:, :, idx]), ref, inputs.BF16)
+    check_state(host_f64(last[:, idx]), ref_last, inputs.BF16)
 
 
 @pytest.mark.parametrize("bt,dim,L,N", [(1, 5120, 4096, 16), (4, 2400, 1000, 8), (8, 2400, 520, 4),
@@ -166,10 +184,10 @@ def test_seg_multisegment_schedule(bt, dim, L, N):
     check_state(host_f64(last[:, idx]), ref_last, inputs.BF16)
 
 
-@pytest.mark.parametrize("g", ["seg", "relay"] + list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("g", ["tmem", "seg", "relay"] + list(range(LAYOUTS[16])))
 def test_writes_stay_in_bounds(g):
     """Outputs and the final state sit between guard words that must survive."""
-    dim = 48 if g in ("seg", "relay") else 45     # the TMA paths need 16-byte rows
+    dim = 48 if g in ("tmem", "seg", "relay") else 45     # the TMA paths need 16-byte rows
     shape = inputs.ScanShape("guard", 2, dim, 70, 16, inputs.BF16)
     inp = inputs.make_scan_inputs(shape, 30)
     n_out = 2 * 70 * dim
