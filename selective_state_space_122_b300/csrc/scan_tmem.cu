@@ -143,8 +143,12 @@ struct TmCfg {
     static constexpr int K = 32;                // steps per chunk
     static constexpr int KR = K / R;            // steps per lane in the per-(t, d) phase
     static constexpr int NP = KR / 2;           // step pairs per lane
-    static constexpr int P = 4;                 // ring slots
-    static constexpr int THREADS = 32 * (WARPS + 1);
+    static constexpr int P = 8;                 // input ring slots (a power of two)
+    static constexpr int OB = 3;                // output tiles
+    static constexpr int W_LOAD = WARPS;        // role warps: TMA loads,
+    static constexpr int W_MMA = WARPS + 1;     //   the one-hot MMA,
+    static constexpr int W_STORE = WARPS + 2;   //   output stores
+    static constexpr int THREADS = 32 * (WARPS + 3);
     static constexpr int ROWB = CC * 2;         // bytes of a bf16 tile row
     static_assert(ROWB == 64 || ROWB == 128, "tile rows are 64 or 128 bytes (swizzled)");
     static constexpr int TILE = K * ROWB;
@@ -159,15 +163,16 @@ struct TmCfg {
     static constexpr int SLOT_X = 3 * al(TILE, 1024);
     static constexpr int SLOT = al(SLOT_X + OPB, 1024);
     static constexpr int A_OP = P * SLOT;                    // 128 x 8 tf32 selector, 4 KB
-    static constexpr int W_BASE = A_OP + 4096;
+    static constexpr int OUT = A_OP + 4096;                  // OB swizzled output tiles
+    static constexpr int OUTT = al(TILE, 1024);
+    static constexpr int W_BASE = OUT + OB * OUTT;
     static constexpr int DPS = CW + 2;                       // float2 stride of a dp row (conflict-free stores)
     static constexpr int RS2 = 33;                           // float2 stride of a reduction row
     static constexpr int W_RED = al(K * DPS * 8, 128);
-    static constexpr int W_OUT = W_RED + (R > 1 ? al((K / 2) * RS2 * 8, 128) : 0);
-    static constexpr int OUTT = al(K * CW * 2, 128);
-    static constexpr int W_BYTES = W_OUT + 3 * OUTT;
-    static constexpr int BAR = W_BASE + WARPS * W_BYTES;     // full[P] empty[P] tfull[2] tempty[2] taddr
-    static constexpr int USED = BAR + (2 * P + 4) * 8 + 16;
+    static constexpr int W_BYTES = W_RED + (R > 1 ? al((K / 2) * RS2 * 8, 128) : 0);
+    static constexpr int BAR = W_BASE + WARPS * W_BYTES;     // full[P] empty[P] tfull[2] tempty[2] ofull[OB] oempty[OB]
+    static constexpr int NBAR = 2 * P + 4 + 2 * OB;
+    static constexpr int USED = BAR + NBAR * 8 + 16;         // + the TMEM address
     // Over half of an SM's shared memory (plus 1 KB to align the base), so a
     // CTA never shares its SM: the 512 TMEM columns it allocates are free.
     static constexpr int SMEM = (USED + 1024 > 120 * 1024) ? USED + 1024 : 120 * 1024;
@@ -208,13 +213,38 @@ __device__ __forceinline__ bool tm_flag_wait(const int* flag, int want) {
 }
 
 // Byte offset of element (row x, column c) of a bf16 tile whose rows are
-// ROWB bytes, written by TMA with the matching swizzle (16-byte chunk index
+// ROWB bytes, laid out by TMA with the matching swizzle (16-byte chunk index
 // XOR address bits 7 and up).
 template <int ROWB>
 __device__ __forceinline__ uint32_t swz(int x, int c) {
     const uint32_t o = (uint32_t)(x * ROWB + c * 2);
     return o ^ (((o >> 7) & (uint32_t)(ROWB / 16 - 1)) << 4);
 }
+
+// The chunks a CTA walks: its tasks (segment s of chain m, task = s * M + m,
+// every workers-th task from blockIdx.x), each a run of chunks.
+struct ChunkCursor {
+    int task, c, end, b, d0;
+    __device__ void enter(const TmParams& p, int nch, int cc) {
+        const int sgm = task / p.M, m = task - sgm * p.M;
+        b = m / p.units;
+        d0 = (m - b * p.units) * cc;
+        c = sgm * p.cps;
+        end = min(c + p.cps, nch);
+    }
+    __device__ void start(const TmParams& p, int nch, int cc) {
+        task = blockIdx.x;
+        if (task < p.M * p.S) enter(p, nch, cc);
+    }
+    // move to the next chunk; false when the CTA has none left
+    __device__ bool valid(const TmParams& p, int nch, int cc) {
+        while (task < p.M * p.S && c >= end) {
+            task += p.workers;
+            if (task < p.M * p.S) enter(p, nch, cc);
+        }
+        return task < p.M * p.S;
+    }
+};
 
 template <int N, bool kSoftplus, bool kGate>
 __global__ void __launch_bounds__(TmCfg<N>::THREADS, 1)
@@ -223,7 +253,8 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                  const TmParams p) {
     using CF = TmCfg<N>;
     using T = __nv_bfloat16;
-    constexpr int K = CF::K, P = CF::P, R = CF::R, CW = CF::CW, CC = CF::CC, KR = CF::KR, NP = CF::NP;
+    constexpr int K = CF::K, P = CF::P, OB = CF::OB, R = CF::R, CW = CF::CW, CC = CF::CC, KR = CF::KR,
+                  NP = CF::NP;
     constexpr int DPS = CF::DPS, RS2 = CF::RS2;
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     // 1024-byte aligned base: the swizzle pattern follows absolute address bits
@@ -235,11 +266,12 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
     const uint32_t bar_empty = bar_full + 8u * P;
     const uint32_t bar_tfull = bar_empty + 8u * P;
     const uint32_t bar_tempty = bar_tfull + 16u;
-    uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(smem + CF::BAR + (2 * P + 4) * 8);
+    const uint32_t bar_ofull = bar_tempty + 16u;
+    const uint32_t bar_oempty = bar_ofull + 8u * OB;
+    uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(smem + CF::BAR + CF::NBAR * 8);
 
     const int L = p.seqlen;
     const int nch = (L + K - 1) / K;
-    const int T_total = p.M * p.S;
 
     // one-hot selector S[r][k] = (k == g(r)), K-major without swizzle: the
     // 8-row x 16-byte core matrix of rows 8 rg.. and k-half kh at rg*256 + kh*128
@@ -260,9 +292,13 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
             mbar_init(bar_tfull + 8u * i, 1);
             mbar_init(bar_tempty + 8u * i, CF::WARPS);
         }
+        for (int i = 0; i < OB; ++i) {
+            mbar_init(bar_ofull + 8u * i, CF::WARPS);
+            mbar_init(bar_oempty + 8u * i, 1);
+        }
         fence_mbar_init();
     }
-    if (warp == CF::WARPS) {
+    if (warp == CF::W_LOAD) {
         tmem_alloc(smem_u32(taddr_slot), CF::TMEM_COLS);
         tmem_relinquish();
     }
@@ -271,62 +307,61 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
     tc_fence_after();
     const uint32_t tmem = *taddr_slot;
 
-    if (warp == CF::WARPS) {
-        // ------------------------------------------------------------ producer
+    // chunks this CTA walks (the same sequence for every role)
+    int total = 0;
+    for (int task = blockIdx.x; task < p.M * p.S; task += p.workers) {
+        const int sgm = task / p.M;
+        total += min((sgm + 1) * p.cps, nch) - sgm * p.cps;
+    }
+
+    if (warp == CF::W_LOAD) {
+        // ------------------------------------------------------------ TMA loads
         if (lane == 0) {
-            int total = 0;
-            for (int task = blockIdx.x; task < T_total; task += p.workers) {
-                const int sgm = task / p.M;
-                total += min((sgm + 1) * p.cps, nch) - sgm * p.cps;
-            }
             constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::OPB);
-            int ld_task = blockIdx.x, ld_c = 0, ld_end = 0, ld_b = 0, ld_d0 = 0;
-            const float* ld_x = nullptr;
-            auto enter = [&](int task) {
-                const int sgm = task / p.M, m = task - sgm * p.M;
-                ld_b = m / p.units;
-                ld_d0 = (m - ld_b * p.units) * CC;
-                ld_c = sgm * p.cps;
-                ld_end = min(ld_c + p.cps, nch);
-                ld_x = p.xop + ((size_t)ld_b * p.lpad + (size_t)ld_c * K) * 32;
-            };
-            if (ld_task < T_total) enter(ld_task);
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
             int issued = 0;
             auto issue = [&]() {
-                while (ld_task < T_total && ld_c >= ld_end) {
-                    ld_task += p.workers;
-                    if (ld_task < T_total) enter(ld_task);
-                }
-                if (ld_task >= T_total) return;
+                if (!cur.valid(p, nch, CC)) return;
                 const int slot = issued & (P - 1);
                 const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
                 const uint32_t bar = bar_full + 8u * (uint32_t)slot;
-                const int t0 = ld_c * K;
+                const int t0 = cur.c * K;
                 mbar_expect_tx(bar, tx_bytes);
-                tma_load_3d(base + CF::SLOT_U, &tm_u, ld_d0, t0, ld_b, bar);
-                tma_load_3d(base + CF::SLOT_D, &tm_d, ld_d0, t0, ld_b, bar);
-                if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, ld_d0, t0, ld_b, bar);
-                bulk_load(base + CF::SLOT_X, ld_x, CF::OPB, bar);
-                ld_x += K * 32;
-                ++ld_c;
+                tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
+                tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
+                if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
+                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.b * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
+                ++cur.c;
                 ++issued;
             };
             for (int i = 0; i < P && i < total; ++i) issue();
-
+            for (int j = 0; j + P < total; ++j) {
+                // slot j % P is free once every consumer has read chunk j's
+                // tiles and seen its MMA (the reader of X) complete
+                if (!mbar_wait(bar_empty + 8u * (uint32_t)(j & (P - 1)), (uint32_t)((j / P) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                issue();
+            }
+            // the CTA's shared memory outlives every copy into it
+            for (int k = max(0, issued - P); k < issued; ++k)
+                if (!mbar_wait(bar_full + 8u * (uint32_t)(k & (P - 1)), (uint32_t)((k / P) & 1))) break;
+        }
+    } else if (warp == CF::W_MMA) {
+        // ------------------------------------------------------------ one-hot MMA
+        if (lane == 0) {
             const uint64_t adesc = smem_desc(smem_u32(smem + CF::A_OP), 128, 256);
             constexpr uint32_t idesc = idesc_tf32(128, CF::TCOLS);
-            bool ok = true;
-            int landed = 0, mmas = 0;
+            int mmas = 0;
             for (int j = 0; j < total; ++j) {
                 const int slot = j & (P - 1), tb = j & 1;
                 if (!mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1))) {
-                    ok = false;
                     raise_error(1u);
                     break;
                 }
-                ++landed;
                 if (j >= 2 && !mbar_wait(bar_tempty + 8u * tb, (uint32_t)(((j - 2) >> 1) & 1))) {
-                    ok = false;
                     raise_error(2u);
                     break;
                 }
@@ -338,24 +373,29 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                 mma_tf32(tmem + (uint32_t)(tb * CF::TCOLS), adesc, bdesc, idesc);
                 mma_commit(bar_tfull + 8u * tb);
                 ++mmas;
-                if (j + P < total) {
-                    // the slot is free once every consumer has read its tiles
-                    // and seen this chunk's MMA complete
-                    if (!mbar_wait(bar_empty + 8u * slot, (uint32_t)((j / P) & 1))) {
-                        ok = false;
-                        raise_error(2u);
-                        break;
-                    }
-                    issue();
+            }
+            // tensor memory is released only after the last MMAs completed
+            for (int k = max(0, mmas - 2); k < mmas; ++k)
+                if (!mbar_wait(bar_tfull + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1))) break;
+        }
+    } else if (warp == CF::W_STORE) {
+        // ------------------------------------------------------------ output stores
+        if (lane == 0) {
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
+            for (int j = 0; j < total && cur.valid(p, nch, CC); ++j, ++cur.c) {
+                const int o = j % OB;
+                if (!mbar_wait(bar_ofull + 8u * o, (uint32_t)((j / OB) & 1))) {
+                    raise_error(2u);
+                    break;
                 }
+                tma_store_3d(&tm_out, cur.d0, cur.c * K, cur.b, smem_u32(smem + CF::OUT + o * CF::OUTT));
+                bulk_commit();
+                // the store before this one has read its tile: hand it back
+                bulk_wait_read<1>();
+                if (j >= 1) mbar_arrive(bar_oempty + 8u * (uint32_t)((j - 1) % OB));
             }
-            if (!ok) {
-                // let issued copies land and the last MMA finish before the
-                // shared and tensor memory are released
-                for (int k = landed; k < issued; ++k)
-                    if (!mbar_wait(bar_full + 8u * (uint32_t)(k & (P - 1)), (uint32_t)((k / P) & 1))) break;
-                if (mmas > 0) mbar_wait(bar_tfull + 8u * (uint32_t)((mmas - 1) & 1), (uint32_t)(((mmas - 1) >> 1) & 1));
-            }
+            bulk_wait_all();
         }
     } else {
         // ------------------------------------------------------------ consumers
@@ -363,7 +403,6 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
         const int ch = lane / R, g = lane % R;
         float2* dp = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES);
         float2* red = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES + CF::W_RED);
-        unsigned char* outb = smem + CF::W_BASE + w * CF::W_BYTES + CF::W_OUT;
         const uint32_t tlane = tmem + ((uint32_t)(32 * w) << 16);
 
         int tas[NP];
@@ -371,13 +410,12 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
         for (int q = 0; q < NP; ++q) tas[q] = g * KR + 2 * ((q + g * (CW / 8)) % NP);
 
         bool ok = true;
-        int j = 0, oslot = 0;
-        for (int task = blockIdx.x; task < T_total && ok; task += p.workers) {
+        int j = 0;
+        for (int task = blockIdx.x; task < p.M * p.S && ok; task += p.workers) {
             const int sgm = task / p.M, m = task - sgm * p.M;
             const int b = m / p.units;
             const int dcta = (m - b * p.units) * CC;
-            const int dw = dcta + w * CW;
-            const int d = dw + ch;
+            const int d = dcta + w * CW + ch;
             const bool ch_ok = d < p.dim;
             const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
             const int chain = m * CF::WARPS + w;
@@ -536,23 +574,25 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                     }
                 }
 
-                // ---- D u, gate, output tile (triple-buffered; before a tile is
-                // rewritten, the store that read it three chunks ago has finished)
-                T* so = reinterpret_cast<T*>(outb + oslot * CF::OUTT);
-                if (lane == 0) bulk_wait_read<2>();
-                __syncwarp();
+                // ---- D u and the gate into the CTA's output tile j % OB, once the
+                // store that last read it (chunk j - OB) has finished
+                const int o = j % OB;
+                if (j >= OB &&
+                    !__all_sync(0xffffffffu, mbar_wait(bar_oempty + 8u * o, (uint32_t)(((j / OB) - 1) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(2u);
+                    break;
+                }
+                unsigned char* so = smem + CF::OUT + o * CF::OUTT;
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     const float2 y = mul2(fma2(dskip2, uk[q], yv[q]), gate[q]);
-                    st_pair<T>(so + tas[q] * CW + ch, so + (tas[q] + 1) * CW + ch, y);
+                    st_pair<T>(reinterpret_cast<T*>(so + swz<CF::ROWB>(tas[q], w * CW + ch)),
+                               reinterpret_cast<T*>(so + swz<CF::ROWB>(tas[q] + 1, w * CW + ch)), y);
                 }
                 fence_async_smem();
                 __syncwarp();
-                if (lane == 0 && dw < p.dim) {   // a group wholly past dim has nothing to store
-                    tma_store_3d(&tm_out, dw, t0, b, smem_u32(so));
-                    bulk_commit();
-                }
-                oslot = oslot == 2 ? 0 : oslot + 1;
+                if (lane == 0) mbar_arrive(bar_ofull + 8u * o);
             }
             if (!ok) break;
 
@@ -567,16 +607,434 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                     make_float4(h0.x, h0.y, h1.x, h1.y);
             }
         }
-        if (lane == 0) bulk_wait_all();
     }
 
     // every warp ends here: the tensor memory is released exactly once
     tc_fence_before();
     __syncthreads();
-    if (warp == CF::WARPS) {
+    if (warp == CF::W_LOAD) {
         __syncwarp();
         tc_fence_after();
         tmem_dealloc(tmem, CF::TMEM_COLS);
+    }
+}
+
+// ===================================================================
+// Two states per lane: 8 consumer warps, two per TMEM lane quarter (both read
+// the same rows: B and C do not depend on the channel), so every scheduler
+// runs two independent recurrences.  A lane keeps states 2g, 2g+1 of its
+// channel (lane = channel * 8 + g); a warp covers 4 channels, a CTA 32.
+// ===================================================================
+
+constexpr int tm_al(int x, int a) { return (x + a - 1) / a * a; }
+
+struct Tm2Cfg {
+    static constexpr int N = 16;
+    static constexpr int G = 2;                 // states per lane
+    static constexpr int R = N / G;             // lanes per channel (8)
+    static constexpr int CW = 32 / R;           // channels per consumer warp (4)
+    static constexpr int WARPS = 8;             // consumer warps, two per lane quarter
+    static constexpr int CC = WARPS * CW;       // channels per CTA (32)
+    static constexpr int K = 64;                // steps per chunk
+    static constexpr int NI = (K / 2) * CW / 32;   // (step pair, channel) items per lane (4)
+    static constexpr int SG = 8;                // steps per TMEM load group (32 columns)
+    static constexpr int P = 4;                 // input ring slots
+    static constexpr int OB = 3;                // output tiles
+    static constexpr int W_LOAD = WARPS, W_MMA = WARPS + 1, W_STORE = WARPS + 2;
+    static constexpr int THREADS = 32 * (WARPS + 3);
+    static constexpr int ROWB = CC * 2;         // 64-byte tile rows
+    static constexpr int TILE = K * ROWB;
+    static constexpr int OPB = K * 4 * 8 * 4;   // X: 4 columns x 8 tf32 per step
+    static constexpr int TCOLS = 4 * K;         // TMEM columns of a chunk (256)
+    static constexpr int TMEM_COLS = 2 * TCOLS;
+    static_assert(TCOLS <= 256 && TMEM_COLS <= 512, "one MMA per chunk, two chunks of TMEM");
+    static constexpr int SLOT_U = 0;
+    static constexpr int SLOT_D = tm_al(TILE, 1024);
+    static constexpr int SLOT_Z = 2 * tm_al(TILE, 1024);
+    static constexpr int SLOT_X = 3 * tm_al(TILE, 1024);
+    static constexpr int SLOT = tm_al(SLOT_X + OPB, 1024);
+    static constexpr int A_OP = P * SLOT;
+    static constexpr int OUT = A_OP + 4096;
+    static constexpr int OUTT = tm_al(TILE, 1024);
+    static constexpr int W_BASE = OUT + OB * OUTT;
+    static constexpr int DPS = K + 4;           // float2 stride of a channel's dp row (conflict-free 16-byte stores)
+    static constexpr int RS2 = 33;              // float2 stride of a reduction row
+    static constexpr int W_RED = tm_al(CW * DPS * 8, 128);
+    static constexpr int W_BYTES = W_RED + tm_al((K / 2) * RS2 * 8, 128);
+    static constexpr int BAR = W_BASE + WARPS * W_BYTES;
+    static constexpr int NBAR = 2 * P + 4 + 2 * OB;
+    static constexpr int USED = BAR + NBAR * 8 + 16;
+    static constexpr int SMEM = (USED + 1024 > 120 * 1024) ? USED + 1024 : 120 * 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+};
+
+template <bool kSoftplus, bool kGate>
+__global__ void __launch_bounds__(Tm2Cfg::THREADS, 1)
+scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
+                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
+                  const TmParams p) {
+    using CF = Tm2Cfg;
+    using T = __nv_bfloat16;
+    constexpr int N = CF::N, K = CF::K, P = CF::P, OB = CF::OB, R = CF::R, CW = CF::CW, CC = CF::CC,
+                  NI = CF::NI, SG = CF::SG;
+    constexpr int DPS = CF::DPS, RS2 = CF::RS2;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring_s = smem_u32(smem);
+    const uint32_t bar_full = smem_u32(smem + CF::BAR);
+    const uint32_t bar_empty = bar_full + 8u * P;
+    const uint32_t bar_tfull = bar_empty + 8u * P;
+    const uint32_t bar_tempty = bar_tfull + 16u;
+    const uint32_t bar_ofull = bar_tempty + 16u;
+    const uint32_t bar_oempty = bar_ofull + 8u * OB;
+    uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(smem + CF::BAR + CF::NBAR * 8);
+
+    const int L = p.seqlen;
+    const int nch = (L + K - 1) / K;
+
+    // selector S[r][k] = (k == g(r)), g = lane % 8 (all 8 k used)
+    {
+        float* sa = reinterpret_cast<float*>(smem + CF::A_OP);
+        for (int e = threadIdx.x; e < 128 * 8; e += CF::THREADS) {
+            const int r = e >> 3, k = e & 7;
+            sa[(r >> 3) * 64 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3)] = (k == ((r & 31) % R)) ? 1.f : 0.f;
+        }
+    }
+    fence_async_smem();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P; ++i) {
+            mbar_init(bar_full + 8u * i, 1);
+            mbar_init(bar_empty + 8u * i, CF::WARPS);
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_tfull + 8u * i, 1);
+            mbar_init(bar_tempty + 8u * i, CF::WARPS);
+        }
+        for (int i = 0; i < OB; ++i) {
+            mbar_init(bar_ofull + 8u * i, CF::WARPS);
+            mbar_init(bar_oempty + 8u * i, 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == CF::W_LOAD) {
+        tmem_alloc(smem_u32(taddr_slot), CF::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *taddr_slot;
+
+    int total = 0;
+    for (int task = blockIdx.x; task < p.M * p.S; task += p.workers) {
+        const int sgm = task / p.M;
+        total += min((sgm + 1) * p.cps, nch) - sgm * p.cps;
+    }
+
+    if (warp == CF::W_LOAD) {
+        if (lane == 0) {
+            constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::OPB);
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
+            int issued = 0;
+            auto issue = [&]() {
+                if (!cur.valid(p, nch, CC)) return;
+                const int slot = issued & (P - 1);
+                const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
+                const uint32_t bar = bar_full + 8u * (uint32_t)slot;
+                const int t0 = cur.c * K;
+                mbar_expect_tx(bar, tx_bytes);
+                tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
+                tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
+                if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
+                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.b * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
+                ++cur.c;
+                ++issued;
+            };
+            for (int i = 0; i < P && i < total; ++i) issue();
+            for (int j = 0; j + P < total; ++j) {
+                if (!mbar_wait(bar_empty + 8u * (uint32_t)(j & (P - 1)), (uint32_t)((j / P) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                issue();
+            }
+            for (int k = max(0, issued - P); k < issued; ++k)
+                if (!mbar_wait(bar_full + 8u * (uint32_t)(k & (P - 1)), (uint32_t)((k / P) & 1))) break;
+        }
+    } else if (warp == CF::W_MMA) {
+        if (lane == 0) {
+            const uint64_t adesc = smem_desc(smem_u32(smem + CF::A_OP), 128, 256);
+            constexpr uint32_t idesc = idesc_tf32(128, CF::TCOLS);
+            int mmas = 0;
+            for (int j = 0; j < total; ++j) {
+                const int slot = j & (P - 1), tb = j & 1;
+                if (!mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1))) {
+                    raise_error(1u);
+                    break;
+                }
+                if (j >= 2 && !mbar_wait(bar_tempty + 8u * tb, (uint32_t)(((j - 2) >> 1) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                tc_fence_after();
+                // X of this slot: per step pair, the k-half 0 core matrix (8
+                // rows of 16 bytes) then the k-half 1 one (LBO 128); step
+                // pairs 256 bytes apart (SBO)
+                const uint64_t bdesc = smem_desc(ring_s + (uint32_t)(slot * CF::SLOT + CF::SLOT_X), 128, 256);
+                mma_tf32(tmem + (uint32_t)(tb * CF::TCOLS), adesc, bdesc, idesc);
+                mma_commit(bar_tfull + 8u * tb);
+                ++mmas;
+            }
+            for (int k = max(0, mmas - 2); k < mmas; ++k)
+                if (!mbar_wait(bar_tfull + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1))) break;
+        }
+    } else if (warp == CF::W_STORE) {
+        if (lane == 0) {
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
+            for (int j = 0; j < total && cur.valid(p, nch, CC); ++j, ++cur.c) {
+                const int o = j % OB;
+                if (!mbar_wait(bar_ofull + 8u * o, (uint32_t)((j / OB) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                tma_store_3d(&tm_out, cur.d0, cur.c * K, cur.b, smem_u32(smem + CF::OUT + o * CF::OUTT));
+                bulk_commit();
+                bulk_wait_read<1>();
+                if (j >= 1) mbar_arrive(bar_oempty + 8u * (uint32_t)((j - 1) % OB));
+            }
+            bulk_wait_all();
+        }
+    } else {
+        // ------------------------------------------------------------ consumers
+        const int w = warp;
+        const int ch = lane / R, g = lane % R;      // recurrence: channel, state pair
+        const int ich = lane & (CW - 1);           // per-(t, d) items: channel
+        float2* dp = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES);
+        float2* red = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES + CF::W_RED);
+        const uint32_t tlane = tmem + ((uint32_t)(32 * (w & 3)) << 16);
+        int ipv[NI];   // step pair of each item
+#pragma unroll
+        for (int i = 0; i < NI; ++i) ipv[i] = (lane + 32 * i) / CW;
+
+        bool ok = true;
+        int j = 0;
+        for (int task = blockIdx.x; task < p.M * p.S && ok; task += p.workers) {
+            const int sgm = task / p.M, m = task - sgm * p.M;
+            const int b = m / p.units;
+            const int dcta = (m - b * p.units) * CC;
+            const int d = dcta + w * CW + ch;
+            const int di = dcta + w * CW + ich;
+            const bool ch_ok = d < p.dim, it_ok = di < p.dim;
+            const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
+            const int chain = m * CF::WARPS + w;
+
+            float2 A2 = make_float2(0.f, 0.f);
+            if (ch_ok) {
+                const float2 a = *reinterpret_cast<const float2*>(p.A + (size_t)d * N + 2 * g);
+                A2 = make_float2(a.x * kLog2e, a.y * kLog2e);
+            }
+            const float2 dskip2 = splat2((p.D && it_ok) ? p.D[di] : 0.f);
+            const float2 bias2 = splat2((p.delta_bias && it_ok) ? p.delta_bias[di] : 0.f);
+
+            float2 h = make_float2(0.f, 0.f);
+            float* hst = p.seg_state + ((size_t)chain * CW + ch) * N + 2 * g;
+            if (sgm > 0) {
+                if (!__all_sync(0xffffffffu, tm_flag_wait(p.seg_flag + chain, sgm))) {
+                    ok = false;
+                    if (lane == 0) raise_error(4u);
+                    break;
+                }
+                h = __ldcg(reinterpret_cast<const float2*>(hst));
+            }
+
+            for (int c = cb; c < ce; ++c, ++j) {
+                const int slot = j & (P - 1), tb = j & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(1u);
+                    break;
+                }
+                const int t0 = c * K;
+                const unsigned char* sb = smem + slot * CF::SLOT;
+
+                // ---- per-(t, d) terms of this lane's items (step pair, channel)
+                float2 uk[NI], gate[NI];
+                {
+                    float2 dpv[2 * NI];
+#pragma unroll
+                    for (int i = 0; i < NI; ++i) {
+                        const int ta = 2 * ipv[i];
+                        const uint32_t oa = swz<CF::ROWB>(ta, w * CW + ich);
+                        const uint32_t ob = swz<CF::ROWB>(ta + 1, w * CW + ich);
+                        const float2 uv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + oa)),
+                                                      ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + ob)));
+                        const float2 xr = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + oa)),
+                                                      ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + ob)));
+                        float2 dl = add2(xr, bias2);
+                        if constexpr (kSoftplus) dl = relay_softplus2<true>(dl);
+                        if (t0 + K > L)
+                            dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + ta + 1 < L ? 1.f : 0.f));
+                        const float2 du = mul2(dl, uv);
+                        dpv[2 * i] = make_float2(dl.x, du.x);
+                        dpv[2 * i + 1] = make_float2(dl.y, du.y);
+                        uk[i] = uv;
+                        if constexpr (kGate) {
+                            const float2 zv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_Z + oa)),
+                                                          ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_Z + ob)));
+                            gate[i] = seg_silu2<true>(zv);
+                        } else {
+                            gate[i] = splat2(1.f);
+                        }
+                    }
+#pragma unroll
+                    for (int i = 0; i < NI; ++i)
+                        *reinterpret_cast<float4*>(dp + ich * DPS + 2 * ipv[i]) =
+                            make_float4(dpv[2 * i].x, dpv[2 * i].y, dpv[2 * i + 1].x, dpv[2 * i + 1].y);
+                }
+                __syncwarp();
+
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * tb, (uint32_t)((j >> 1) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(2u);
+                    break;
+                }
+                tc_fence_after();
+                if (lane == 0) mbar_arrive(bar_empty + 8u * slot);
+
+                // the output tile j % OB is free once the store of chunk j - OB read it
+                const int o = j % OB;
+                if (j >= OB &&
+                    !__all_sync(0xffffffffu, mbar_wait(bar_oempty + 8u * o, (uint32_t)(((j / OB) - 1) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(2u);
+                    break;
+                }
+                unsigned char* so = smem + CF::OUT + o * CF::OUTT;
+
+                // ---- the recurrence over the chunk's K steps (software-pipelined
+                // as in the four-state kernel); B and C of 8 steps per TMEM load.
+                // Each step pair's partial sums go to the reduction buffer as they
+                // are made; after every 16 steps the lane sums the 8 partials of
+                // one of its items (the items of step pairs 8q .. 8q+7) and writes
+                // that item's output, overlapping the following steps.
+                constexpr int LA = 4, EA = 2, NG = K / SG;
+                const uint32_t tcol = tlane + (uint32_t)(tb * CF::TCOLS);
+                uint32_t gv[NG][32];
+                tmem_ld32(tcol, gv[0]);
+                tmem_wait(gv[0]);
+                tmem_ld32(tcol + 32, gv[1]);
+                float2 qv[K], dA[K], dB[K];
+                auto bc = [&](int t, int i) { return __uint_as_float(gv[t / SG][(t % SG) * 4 + i]); };
+                // Delta and Delta u of steps t, t+1 (t even) in one 16-byte load
+                auto load_step = [&](int t) {
+                    if ((t & 1) == 0) {
+                        const float4 v = *reinterpret_cast<const float4*>(dp + ch * DPS + t);
+                        qv[t] = make_float2(v.x, v.y);
+                        qv[t + 1] = make_float2(v.z, v.w);
+                    }
+                };
+                auto finish_item = [&](int q) {
+                    const float2* row = red + ipv[q] * RS2 + ich * R;
+                    float2 pr[R];
+#pragma unroll
+                    for (int gg = 0; gg < R; ++gg) pr[gg] = row[gg];
+                    const float2 a0 = add2(pr[0], pr[1]), a1 = add2(pr[2], pr[3]);
+                    const float2 a2 = add2(pr[4], pr[5]), a3 = add2(pr[6], pr[7]);
+                    const float2 yv = add2(add2(a0, a1), add2(a2, a3));
+                    const float2 y = mul2(fma2(dskip2, uk[q], yv), gate[q]);
+                    st_pair<T>(reinterpret_cast<T*>(so + swz<CF::ROWB>(2 * ipv[q], w * CW + ich)),
+                               reinterpret_cast<T*>(so + swz<CF::ROWB>(2 * ipv[q] + 1, w * CW + ich)), y);
+                };
+                auto exp_step = [&](int t) {
+                    const float2 e = mul2(splat2(qv[t].x), A2);
+                    dA[t] = make_float2(decay_exp2<true>(e.x), decay_exp2<true>(e.y));
+                    dB[t] = mul2(splat2(qv[t].y), make_float2(bc(t, 0), bc(t, 1)));
+                };
+#pragma unroll
+                for (int t = 0; t < LA + 2; ++t) load_step(t);
+#pragma unroll
+                for (int t = 0; t < EA; ++t) exp_step(t);
+                float s_prev = 0.f;
+#pragma unroll
+                for (int t = 0; t < K; ++t) {
+                    if (t + EA < K && ((t + EA) % SG) == 0) {
+                        const int gr = (t + EA) / SG;
+                        tmem_wait(gv[gr]);
+                        if (gr + 1 < NG) tmem_ld32(tcol + 32u * (uint32_t)(gr + 1), gv[gr + 1]);
+                    }
+                    if (t + LA + 1 < K) load_step(t + LA + 1);
+                    if (t + EA < K) exp_step(t + EA);
+                    h = fma2(dA[t], h, dB[t]);
+                    const float2 cy = mul2(make_float2(bc(t, 2), bc(t, 3)), h);
+                    const float sy = cy.x + cy.y;
+                    if (t & 1) red[(t / 2) * RS2 + lane] = make_float2(s_prev, sy);
+                    s_prev = sy;
+                    if ((t % 16) == 15 && t / 16 < NI) {
+                        __syncwarp();
+                        finish_item(t / 16);
+                    }
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_tempty + 8u * tb);
+                fence_async_smem();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_ofull + 8u * o);
+            }
+            if (!ok) break;
+
+            if (sgm + 1 < p.S) {
+                __stcg(reinterpret_cast<float2*>(hst), h);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) tm_st_release(p.seg_flag + chain, sgm + 1);
+            } else if (p.last_state && ch_ok) {
+                *reinterpret_cast<float2*>(p.last_state + ((size_t)b * p.dim + d) * N + 2 * g) = h;
+            }
+        }
+    }
+
+    tc_fence_before();
+    __syncthreads();
+    if (warp == CF::W_LOAD) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, CF::TMEM_COLS);
+    }
+}
+
+// X operands for two states per lane: per step pair a 256-byte block, the
+// k-half-0 core matrix then the k-half-1 one, row 4 (t & 1) + j holding
+// X[k, 4t + j] for k in the half: B_t[2k + j] (j < 2), C_t[2k + j - 2].
+__global__ void __launch_bounds__(256) tm2_stage_kernel(const __nv_bfloat16* __restrict__ B,
+                                                        const __nv_bfloat16* __restrict__ C, float* __restrict__ xop,
+                                                        int L, int64_t lpad, int* flags, int nflags) {
+    constexpr int N = 16;
+    __shared__ float sb[2][N][65];
+    const int b = blockIdx.y;
+    const int t0 = blockIdx.x * 64;
+    if (flags) {
+        const size_t nthr = (size_t)gridDim.x * gridDim.y * blockDim.x;
+        for (size_t i = ((size_t)blockIdx.y * gridDim.x + blockIdx.x) * blockDim.x + threadIdx.x; i < (size_t)nflags;
+             i += nthr)
+            flags[i] = 0;
+    }
+    for (int e = threadIdx.x; e < 2 * N * 64; e += 256) {
+        const int which = e / (N * 64), n = (e / 64) % N, t = e % 64;
+        const __nv_bfloat16* src = which ? C : B;
+        sb[which][n][t] = (t0 + t < L) ? __bfloat162float(src[((size_t)b * N + n) * L + t0 + t]) : 0.f;
+    }
+    __syncthreads();
+    float* dst = xop + ((size_t)b * lpad + t0) * 32;
+    for (int e = threadIdx.x; e < 64 * 32; e += 256) {
+        const int pair = e / 64, wi = e % 64;
+        const int kh = wi / 32, row = (wi % 32) / 4, kk = wi % 4;
+        const int t = 2 * pair + row / 4, jj = row % 4, k = 4 * kh + kk;
+        dst[e] = sb[jj >> 1][2 * k + (jj & 1)][t];
     }
 }
 
@@ -676,15 +1134,6 @@ TmPlan tm_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
     return pl;
 }
 
-template <int N>
-int64_t tm_ws_bytes(int64_t batch, int64_t dim, int64_t seqlen) {
-    using CF = TmCfg<N>;
-    const int64_t units = (dim + CF::CC - 1) / CF::CC;
-    const int64_t chains = batch * units * CF::WARPS;
-    const int64_t x_bytes = (batch * relay_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
-    const int64_t st_bytes = (chains * CF::CW * N * 4 + 255) / 256 * 256;
-    return x_bytes + st_bytes + (chains * 4 + 255) / 256 * 256;
-}
 
 template <int N>
 cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
@@ -723,13 +1172,84 @@ cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) 
     if (!tm_make_map(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
         !tm_make_map(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
         !tm_make_map(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
-        !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K, CU_TENSOR_MAP_SWIZZLE_NONE))
+        !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw))
         return cudaErrorInvalidValue;
     TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
                 pl.units, pl.M, pl.S, pl.cps, pl.grid};
     void* args[] = {&mu, &md, &mz, &mo, &tp};
     // Segments wait on segments of other CTAs: every CTA must be resident,
     // which the cooperative launch guarantees (one CTA per SM, grid <= SMs).
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
+                                       dim3(CF::THREADS), args, CF::SMEM, s);
+}
+
+cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
+    using CF = Tm2Cfg;
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TmParams);
+    static const Kern kerns[4] = {scan_tmem2_kernel<false, false>, scan_tmem2_kernel<false, true>,
+                                  scan_tmem2_kernel<true, false>, scan_tmem2_kernel<true, true>};
+    const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
+    static int occ[4] = {0, 0, 0, 0};
+    if (occ[which] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        if (o != 1) return cudaErrorInvalidConfiguration;
+        occ[which] = o;
+    }
+    // the work split depends only on the CTA's channel count and chunk length
+    TmPlan pl{};
+    {
+        pl.units = (int)((a.dim + CF::CC - 1) / CF::CC);
+        pl.M = (int)(a.batch * pl.units);
+        const int nch = (int)((a.seqlen + CF::K - 1) / CF::K);
+        if (pl.M <= sms) {
+            pl.grid = pl.M;
+            pl.S = 1;
+            pl.cps = nch;
+        } else {
+            pl.grid = sms;
+            int bestS = 1;
+            double best = 1e30;
+            const int smax = std::max(1, std::min(64, nch / 4));
+            for (int S = 1; S <= smax; ++S) {
+                const int cps = (nch + S - 1) / S;
+                const int s_eff = (nch + cps - 1) / cps;
+                const double cost = std::ceil(double(pl.M) * s_eff / pl.grid) * cps;
+                if (cost < best * 0.999) {
+                    best = cost;
+                    bestS = S;
+                }
+            }
+            pl.cps = (nch + bestS - 1) / bestS;
+            pl.S = (nch + pl.cps - 1) / pl.cps;
+        }
+    }
+    const int64_t lpad = relay_lpad(a.seqlen);
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    float* xop = reinterpret_cast<float*>(w);
+    const int64_t x_bytes = (a.batch * lpad * 32 * 4 + 255) / 256 * 256;
+    const int64_t chains = (int64_t)pl.M * CF::WARPS;
+    float* st = reinterpret_cast<float*>(w + x_bytes);
+    const int64_t st_bytes = (chains * CF::CW * CF::N * 4 + 255) / 256 * 256;
+    int* flags = reinterpret_cast<int*>(w + x_bytes + st_bytes);
+    {
+        dim3 grid((unsigned)(lpad / 64), (unsigned)a.batch);
+        tm2_stage_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.B),
+                                              static_cast<const __nv_bfloat16*>(a.C), xop, (int)a.seqlen, lpad, flags,
+                                              (int)chains);
+    }
+    CUtensorMap mu, md, mz, mo;
+    if (!tm_make_map(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
+                pl.units, pl.M, pl.S, pl.cps, pl.grid};
+    void* args[] = {&mu, &md, &mz, &mo, &tp};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
                                        dim3(CF::THREADS), args, CF::SMEM, s);
 }
@@ -744,11 +1264,18 @@ bool tmem_supported(const ScanArgs& a, DType dt) {
 }
 
 int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
-    return dstate == 16 ? tm_ws_bytes<16>(batch, dim, seqlen) : 0;
+    if (dstate != 16) return 0;
+    // both variants: staged operands, one f32 state per (channel, state) of
+    // every 32-channel group, and one flag per consumer warp of each group
+    const int64_t groups = batch * ((dim + 31) / 32);
+    const int64_t x_bytes = (batch * relay_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
+    const int64_t st_bytes = (groups * 32 * 16 * 4 + 255) / 256 * 256;
+    return x_bytes + st_bytes + (groups * 8 * 4 + 255) / 256 * 256;
 }
 
-cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s) {
+cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant) {
     if (dt != DType::BF16 || a.dstate != 16) return cudaErrorInvalidValue;
+    if (variant == 2) return launch_tmem2(a, workspace, sms, s);
     return launch_tmem_t<16>(a, workspace, sms, s);
 }
 

@@ -182,9 +182,9 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
-    // The tensor-memory scan runs whenever its requirements hold (bf16, 16
-    // states), else the segmented scan; SSM_SCAN_PATH=tmem|seg|relay|generic
-    // forces one kernel (tests use it).
+    // The tensor-memory scan (two states per lane) runs whenever its
+    // requirements hold (bf16, 16 states), else the segmented scan;
+    // SSM_SCAN_PATH=tmem2|tmem|seg|relay|generic forces one kernel (tests use it).
     const char* force = std::getenv("SSM_SCAN_PATH");
     // (chains * 64 segments must stay a 32-bit task count)
     const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
@@ -198,11 +198,12 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
     const bool want_seg = force && std::strcmp(force, "seg") == 0;
     const bool tmem_ok = fast_ok && ssm::tmem_supported(a, dt) &&
                          workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate);
-    if (force && std::strcmp(force, "tmem") == 0) {
+    if (force && (std::strcmp(force, "tmem") == 0 || std::strcmp(force, "tmem2") == 0)) {
         if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
-        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st));
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, force[4] == '2' ? 2 : 4));
     }
-    if (!want_generic && !want_seg && tmem_ok) return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st));
+    if (!want_generic && !want_seg && tmem_ok)
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 2));
     if (!want_generic && fast_ok &&
         workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es)) {
         return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));

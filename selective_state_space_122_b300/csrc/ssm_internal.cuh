@@ -74,7 +74,8 @@ cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* workspace, int sm
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
 bool tmem_supported(const ScanArgs& a, DType dt);
 int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
-cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
+// variant 2: two states per lane (8 consumer warps); otherwise four.
+cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant);
 int read_tmem_device_error(bool clear);
 int read_device_error(bool clear);
 

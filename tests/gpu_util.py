@@ -100,20 +100,20 @@ def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
     relay paths (when they accept the shape) and each generic layout."""
     fast = ["seg", "relay"] if relay_ok(dim, dtype) else []
     if tmem_ok(N, dim, dtype):
-        fast = ["tmem"] + fast
+        fast = ["tmem", "tmem2"] + fast
     return fast + list(range(LAYOUTS[N]))
 
 
 @contextlib.contextmanager
 def scan_layout(layout):
-    """Force a path: None = the library's own choice, "tmem" / "seg" / "relay"
-    = that TMA kernel (an error if it cannot take the shape), an int = that
-    layout of the generic kernel."""
+    """Force a path: None = the library's own choice, "tmem" / "tmem2" (four
+    or two states per lane) / "seg" / "relay" = that TMA kernel (an error if
+    it cannot take the shape), an int = that layout of the generic kernel."""
     keys = ("SSM_SCAN_LAYOUT", "SSM_SCAN_PATH")
     old = {k: os.environ.get(k) for k in keys}
     for k in keys:
         os.environ.pop(k, None)
-    if layout in ("relay", "seg", "tmem"):
+    if layout in ("relay", "seg", "tmem", "tmem2"):
         os.environ["SSM_SCAN_PATH"] = layout
     elif layout is not None:
         os.environ["SSM_SCAN_PATH"] = "generic"

@@ -130,7 +130,8 @@ def _ws_expected(batch, dim, seqlen, dstate, es):
     staged in the activation type (es bytes) plus one float32 state per
     (chain, channel, state) and one int flag per chain; and, for bf16 with 16
     states, the tensor-memory path's one-hot operands (32 float32 per step)
-    plus its state and flags over 32-channel CTA groups of four warps."""
+    plus its state and one flag per consumer warp (up to eight) of each
+    32-channel group."""
     up = lambda x: (x + 255) // 256 * 256
     lpad = (seqlen + 63) // 64 * 64
     cw = 32 // (dstate // 4)
@@ -139,8 +140,8 @@ def _ws_expected(batch, dim, seqlen, dstate, es):
     seg = up(batch * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
     need = max(relay, seg)
     if es == 2 and dstate == 16:
-        tchains = batch * ((dim + 31) // 32) * 4
-        need = max(need, up(batch * lpad * 32 * 4) + up(tchains * 8 * 16 * 4) + up(tchains * 4))
+        groups = batch * ((dim + 31) // 32)
+        need = max(need, up(batch * lpad * 32 * 4) + up(groups * 32 * 16 * 4) + up(groups * 8 * 4))
     return need
 
 
@@ -149,7 +150,7 @@ def test_workspace_size_query(lib):
         assert lib.ssm_scan_workspace_bytes(*args, 1) == _ws_expected(*args, 2), args
         assert lib.ssm_scan_workspace_bytes(*args, 0) == _ws_expected(*args, 4), args
     assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 0) == 16777216 + 327680 + 2560
-    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 16777216 + 327680 + 2560
+    assert lib.ssm_scan_workspace_bytes(1, 5120, 131072, 16, 1) == 16777216 + 327680 + 5120
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 5, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 0, 64, 16, 1) == -1
