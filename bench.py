@@ -52,6 +52,11 @@ def scan_elements(s=SCAN):
     return s.batch * s.dim * s.seqlen * s.dstate
 
 
+# Measured DRAM bytes of one full-size launch of the scan kernel (see the
+# "traffic" entry of the roofline object).
+SCAN_TRAFFIC_BYTES = 654.4e6 * 8
+
+
 def scan_bytes(s=SCAN, es=2):
     """Algorithmic HBM bytes of one scan: u, delta, z read and out written once
     per (b, t, d); B and C once; A, D, delta_bias once; final state written."""
@@ -411,8 +416,12 @@ def bench_ours(args):
             "achieved": sfu_ach / 1e9,
             "peak": units["ex2"] / 1e9,
             "frac": sfu_ach / units["ex2"],
-            "traffic": None,
-            "kernel": "ssm_scan_fwd: bc_stage_kernel + scan_seg_kernel (long-sequence scan)",
+            # dram__bytes_read.sum + dram__bytes_write.sum of scan_tmem2_kernel from one
+            # ncu capture of the same workload cut to L = 16384 (654.4 MB), scaled by
+            # 131072 / 16384 (traffic grows in proportion to L)
+            "traffic": SCAN_TRAFFIC_BYTES,
+            "traffic_source": "ncu, scan_tmem2_kernel at L=16384 x 8",
+            "kernel": "ssm_scan_fwd: tm2_stage_kernel + scan_tmem2_kernel (long-sequence scan)",
             "peak_source": ("measured on this GPU by libssmpeak.so: ex2 %.1f, lg2 %.1f, rcp %.1f G/s, "
                             "packed FMA %.1f TFLOP/s; SFU work per (b,t,d): N+2 ex2, 1 lg2, 1 rcp, "
                             "lg2/rcp weighted by ex2_rate/their rate"
