@@ -49,6 +49,8 @@ def load(path: Optional[str] = None):
     dp = ctypes.POINTER(ctypes.c_double)
     lib.oracle_scan.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp] + [ctypes.c_int] * 4
     lib.oracle_scan.restype = ctypes.c_int
+    lib.oracle_scan_from.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 4
+    lib.oracle_scan_from.restype = ctypes.c_int
     lib.oracle_step.argtypes = [dp] * 9 + [ctypes.c_int, dp] + [ctypes.c_int] * 3
     lib.oracle_step.restype = ctypes.c_int
     lib.oracle_softplus.argtypes = [ctypes.c_double]
@@ -74,23 +76,24 @@ def _f64(a):
 
 
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
-         want_last_state=True, lib=None):
+         want_last_state=True, lib=None, initial_state=None):
     """Full-sequence selective scan.
 
     u, delta, z: (batch, L, dim); B, C: (batch, N, L); A: (dim, N);
-    D, delta_bias: (dim,).  Returns (out (batch, L, dim), last_state
-    (batch, dim, N) or None), float64.
+    D, delta_bias: (dim,); initial_state: (batch, dim, N) or None (zero).
+    Returns (out (batch, L, dim), last_state (batch, dim, N) or None), float64.
     """
     lib = lib or load()
-    u, delta, A, B, C, D, z, delta_bias = map(_f64, (u, delta, A, B, C, D, z, delta_bias))
+    u, delta, A, B, C, D, z, delta_bias, h0 = map(_f64, (u, delta, A, B, C, D, z, delta_bias, initial_state))
     bt, L, dim = u.shape
     N = A.shape[1]
     assert delta.shape == u.shape and A.shape == (dim, N)
     assert B.shape == (bt, N, L) and C.shape == (bt, N, L)
+    assert h0 is None or h0.shape == (bt, dim, N)
     out = np.empty_like(u)
     last = np.empty((bt, dim, N)) if want_last_state else None
-    rc = lib.oracle_scan(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                         int(bool(softplus)), _p(out), _p(last), bt, dim, L, N)
+    rc = lib.oracle_scan_from(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                              int(bool(softplus)), _p(h0), _p(out), _p(last), bt, dim, L, N)
     if rc != 0:
         raise ValueError(f"oracle_scan rejected its arguments (code {rc})")
     return out, last

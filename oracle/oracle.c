@@ -21,7 +21,10 @@
  *    for A and the Euler rule for B:  dA = exp(Delta*A),  dB*u = Delta*B*u.
  *  - same page, "Efficient Scan", item 2 (sequential scan for inference): the
  *    recurrence h_t = dA_t * h_{t-1} + dB_t * u_t run one step at a time with a
- *    constant-size state, starting from h = 0.
+ *    constant-size state, starting from h = 0 -- or, for a scan that continues
+ *    an earlier one (a prompt processed in pieces, or a scan resumed after
+ *    recurrent steps), from the state the earlier part left:
+ *    oracle_scan_from takes that state as h_{-1}.
  *  - readout y_t = C_t . h_t + D * u_t (the y equation above, with h_t taken
  *    after the step-t update), then the Mamba block's gate
  *    ("Features": "Mamba block with gated residuals"): y_t *= silu(z_t).
@@ -36,6 +39,7 @@
  *   A                : [dim][dstate]
  *   D, delta_bias    : [dim]
  *   last_state       : [batch][dim][dstate]
+ *   initial_state    : [batch][dim][dstate]  (oracle_scan_from only)
  * Decode step:
  *   state            : [batch][dim][dstate]  (updated in place)
  *   x, dt, z, out    : [batch][dim]
@@ -95,14 +99,16 @@ static int check_dims(int batch, int dim, int seqlen, int dstate) {
     return 0;
 }
 
-/* Full-sequence scan of every (batch, channel), independently.  The OpenMP
- * loop only distributes whole independent channels across threads; each
- * channel's arithmetic is the sequential definition above. */
-int oracle_scan(const double* u, const double* delta, const double* A,
-                const double* B, const double* C, const double* D,
-                const double* z, const double* delta_bias, int softplus_flag,
-                double* out, double* last_state,
-                int batch, int dim, int seqlen, int dstate) {
+/* Full-sequence scan of every (batch, channel), independently, starting from
+ * initial_state (h = 0 where it is NULL).  The OpenMP loop only distributes
+ * whole independent channels across threads; each channel's arithmetic is the
+ * sequential definition above.  last_state may be the same array as
+ * initial_state (each channel reads its initial state before it writes). */
+int oracle_scan_from(const double* u, const double* delta, const double* A,
+                     const double* B, const double* C, const double* D,
+                     const double* z, const double* delta_bias, int softplus_flag,
+                     const double* initial_state, double* out, double* last_state,
+                     int batch, int dim, int seqlen, int dstate) {
     if (!u || !delta || !A || !B || !C || !out) return 1;
     if (check_dims(batch, dim, seqlen, dstate)) return 2;
     const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
@@ -111,7 +117,8 @@ int oracle_scan(const double* u, const double* delta, const double* A,
     for (long long bd = 0; bd < total; ++bd) {
         const ptrdiff_t b = bd / Dm, d = bd % Dm;
         double h[ORACLE_MAX_DSTATE];
-        for (ptrdiff_t n = 0; n < N; ++n) h[n] = 0.0;
+        for (ptrdiff_t n = 0; n < N; ++n)
+            h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;
         const double* Bb = B + b * N * L;
         const double* Cb = C + b * N * L;
         const double Dd = D ? D[d] : 0.0;
@@ -125,6 +132,16 @@ int oracle_scan(const double* u, const double* delta, const double* A,
             for (ptrdiff_t n = 0; n < N; ++n) last_state[(b * Dm + d) * N + n] = h[n];
     }
     return 0;
+}
+
+/* The scan from h = 0. */
+int oracle_scan(const double* u, const double* delta, const double* A,
+                const double* B, const double* C, const double* D,
+                const double* z, const double* delta_bias, int softplus_flag,
+                double* out, double* last_state,
+                int batch, int dim, int seqlen, int dstate) {
+    return oracle_scan_from(u, delta, A, B, C, D, z, delta_bias, softplus_flag, NULL,
+                            out, last_state, batch, dim, seqlen, dstate);
 }
 
 /* Single-token recurrent update ("Efficient Scan", item 2): the same step as

@@ -18,7 +18,11 @@ disagrees with an independent route to the same answer:
 * invariances:   linear in u, causal, unchanged by B -> cB, C -> C/c, and
                  equivariant under a permutation of channels;
 * decode:        chaining the single-token update over L tokens from a zero
-                 state reproduces the full scan exactly.
+                 state reproduces the full scan exactly;
+* initial state: the unrolled sum with the initial state's decay term
+                 exp(A_n sum_{r<=t} Delta_r) h0_n added, and a sequence cut
+                 anywhere and scanned in two pieces (the second from the first's
+                 final state) reproducing the whole scan exactly.
 
 Softplus and sigmoid are taken from numpy/scipy library routines here
 (``np.logaddexp``, ``scipy.special.expit``), never from the oracle.
@@ -74,9 +78,10 @@ def _close(got, ref, rel=REL, what=""):
     assert err <= rel * scale, f"{what}: max|err| {err:.3e} > {rel:.1e} * {scale:.3e}"
 
 
-def brute_force(case):
-    """y_t = sum_n C[n,t] sum_{s<=t} exp(A_n sum_{r=s+1..t} Delta_r) Delta_s B[n,s] u_s
-    + D u_t, times silu(z_t); also the state after the last step."""
+def brute_force(case, h0=None):
+    """y_t = sum_n C[n,t] (exp(A_n sum_{r<=t} Delta_r) h0_n
+    + sum_{s<=t} exp(A_n sum_{r=s+1..t} Delta_r) Delta_s B[n,s] u_s) + D u_t, times
+    silu(z_t) (h0 = 0 unless given); also the state after the last step."""
     u, A, B, C = case["u"], case["A"], case["B"], case["C"]
     bt, L, dim = u.shape
     N = A.shape[1]
@@ -88,6 +93,8 @@ def brute_force(case):
         for d in range(dim):
             for t in range(L):
                 h = np.zeros(N)
+                if h0 is not None:
+                    h += np.exp(A[d] * float(np.sum(dlt[b, :t + 1, d]))) * h0[b, d]
                 for s in range(t + 1):
                     span = float(np.sum(dlt[b, s + 1:t + 1, d]))
                     h += np.exp(A[d] * span) * dlt[b, s, d] * B[b, :, s] * u[b, s, d]
@@ -97,9 +104,9 @@ def brute_force(case):
     return y * _gate(case), last
 
 
-def run_oracle(case, lib):
+def run_oracle(case, lib, h0=None):
     return oracle.scan(case["u"], case["delta"], case["A"], case["B"], case["C"], case["D"],
-                       case["z"], case["delta_bias"], case["softplus"], lib=lib)
+                       case["z"], case["delta_bias"], case["softplus"], lib=lib, initial_state=h0)
 
 
 # --------------------------------------------------------------------------- pins
@@ -269,6 +276,37 @@ def pin_decode_chain_equals_scan(lib):
         assert np.array_equal(state, last), "decode chain final state differs from scan"
 
 
+def pin_initial_state_brute_force(lib):
+    for seed, kw in [(91, {}), (92, dict(softplus=False, with_z=False)), (93, dict(random_a=False, N=3))]:
+        case = tiny_case(seed, **kw)
+        bt, L, dim = case["u"].shape
+        h0 = _rng(seed + 100).standard_normal((bt, dim, case["A"].shape[1]))
+        out, last = run_oracle(case, lib, h0)
+        ref, ref_last = brute_force(case, h0)
+        _close(out, ref, what=f"initial-state brute out seed {seed}")
+        _close(last, ref_last, what=f"initial-state brute last_state seed {seed}")
+
+
+def _cut(case, lo, hi):
+    c = dict(case)
+    for k in ("u", "delta", "z"):
+        if case[k] is not None:
+            c[k] = np.ascontiguousarray(case[k][:, lo:hi])
+    for k in ("B", "C"):
+        c[k] = np.ascontiguousarray(case[k][:, :, lo:hi])
+    return c
+
+
+def pin_split_equals_whole(lib):
+    for seed, cut in [(95, 1), (96, 7), (97, 11)]:
+        case = tiny_case(seed, bt=2, L=12, dim=3, N=4)
+        out, last = run_oracle(case, lib)
+        o1, s1 = run_oracle(_cut(case, 0, cut), lib)
+        o2, s2 = run_oracle(_cut(case, cut, 12), lib, s1)
+        assert np.array_equal(np.concatenate([o1, o2], axis=1), out), f"split at {cut} changed the output"
+        assert np.array_equal(s2, last), f"split at {cut} changed the final state"
+
+
 def pin_scalar_functions(lib):
     sp = lambda x: oracle.softplus(x, lib=lib)
     si = lambda x: oracle.silu(x, lib=lib)
@@ -288,4 +326,4 @@ def pin_scalar_functions(lib):
 ALL_PINS = [pin_brute_force, pin_time_invariant_convolution, pin_associative_scan,
             pin_delta_to_zero, pin_memoryless_limit, pin_linear_in_u, pin_causal,
             pin_bc_scale, pin_channel_permutation, pin_decode_chain_equals_scan,
-            pin_scalar_functions]
+            pin_initial_state_brute_force, pin_split_equals_whole, pin_scalar_functions]

@@ -33,6 +33,10 @@ MUTATIONS = [
      "last_state[(b * N + n) * Dm + d] = h[n];"),
     ("decode ignores dt bias", "timestep(dt[i], dt_bias, (int)d, dt_softplus)",
      "timestep(dt[i], NULL, (int)d, dt_softplus)"),
+    ("initial state ignored", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
+     "h[n] = 0.0;"),
+    ("initial state read transposed", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
+     "h[n] = initial_state ? initial_state[(b * N + n) * Dm + d] : 0.0;"),
 ]
 
 
