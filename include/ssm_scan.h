@@ -87,7 +87,7 @@ typedef enum ssm_dtype {
 } ssm_dtype;
 
 /*
- * ssm_scan_fwd -- full-sequence selective scan.
+ * ssm_scan_fwd -- full-sequence selective scan, from h = 0.
  *
  *   u           [batch][seqlen][dim]     dtype   input x of the SSM
  *   delta       [batch][seqlen][dim]     dtype   Delta_raw (already projected)
@@ -121,15 +121,46 @@ SSM_API ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A
                         int dtype, void* workspace, int64_t workspace_bytes, void* stream);
 
 /*
+ * ssm_scan_fwd_from_state -- the same scan, starting from a given state
+ * instead of zero: h_{-1} = initial_state.  A scan that continues an earlier
+ * one -- a long prompt processed in pieces, or a sequence resumed after
+ * ssm_state_update steps -- passes the state the earlier part left
+ * ("Mamba: Selective State Space Models" README, "Efficient Scan": the
+ * recurrent mode carries a constant-size state).
+ *
+ *   initial_state  [batch][dim][dstate]  f32   read once per channel before its
+ *                                              first step; NULL = zero (exactly
+ *                                              ssm_scan_fwd)
+ *
+ * Every other argument is as in ssm_scan_fwd.  initial_state may be the same
+ * array as last_state (resume in place: each channel's initial state is read
+ * before its final state is written); otherwise it must not overlap any
+ * output, input or the workspace (SSM_ERR_ALIAS).  It must be aligned to 4
+ * bytes, and to 16 bytes for the fast paths.  Scanning a sequence in pieces,
+ * each from the previous piece's last_state, gives the whole scan's output
+ * and final state up to float32 rounding.
+ */
+SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A,
+                                           const void* B, const void* C, const float* D,
+                                           const void* z, const float* delta_bias, int softplus_flag,
+                                           const float* initial_state, void* out, float* last_state,
+                                           int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                           int dtype, void* workspace, int64_t workspace_bytes,
+                                           void* stream);
+
+/*
  * ssm_scan_workspace_bytes -- bytes of workspace the fast paths of
- * ssm_scan_fwd need for these sizes: the larger of (a) B and C staged as
+ * ssm_scan_fwd need for these sizes: the largest of (a) B and C staged as
  * float32 rows, batch * round_up(seqlen, 64) * 2 * dstate * 4 bytes (relay
- * kernel), and (b) B and C staged in the activation dtype (same count of
+ * kernel); (b) B and C staged in the activation dtype (same count of
  * elements), the state handed between sequence segments of each chain
  * (chains * cw * dstate * 4 bytes, cw = 128 / dstate channels per chain,
- * chains = batch * ceil(dim / cw)) and one int flag per chain, each part
- * rounded up to 256 bytes (segmented kernel).  Returns -1 for sizes or a
- * dtype that ssm_scan_fwd would reject.  Pure host computation.
+ * chains = batch * ceil(dim / cw)) and one int flag per chain (segmented
+ * kernel); and, for bf16 with dstate 16, (c) the tensor-memory kernels'
+ * staged operand (batch * round_up(seqlen, 64) * 32 * 4 bytes), their
+ * segment state (groups * 32 * 16 * 4 bytes, groups = batch * ceil(dim / 32))
+ * and groups * 8 int flags; each part rounded up to 256 bytes.  Returns -1
+ * for sizes or a dtype that ssm_scan_fwd would reject.  Pure host computation.
  */
 SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                          int dtype);

@@ -23,7 +23,7 @@ STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN"
           7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE", 9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
            "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
-           "ssm_scan_noalloc_max_workspace_bytes")
+           "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -47,6 +47,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_scan_fwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, fp,
                                  i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_fwd.restype = ci
+    lib.ssm_scan_fwd_from_state.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, fp,
+                                            i64, i64, i64, i64, ci, vp, i64, vp]
+    lib.ssm_scan_fwd_from_state.restype = ci
     lib.ssm_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
     lib.ssm_scan_workspace_bytes.restype = i64
     lib.ssm_device_error.argtypes = [ci]
@@ -124,7 +127,8 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                  delta_bias: Optional[torch.Tensor] = None, softplus: bool = True,
                  out: Optional[torch.Tensor] = None, last_state: Optional[torch.Tensor] = None,
                  return_last_state: bool = False,
-                 workspace: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+                 workspace: Optional[torch.Tensor] = None,
+                 initial_state: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Selective scan over (batch, L, dim) activations; see ssm_scan.h.
 
     B, C: (batch, dstate, L); A: (dim, dstate) f32; D, delta_bias: (dim,) f32.
@@ -132,6 +136,8 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
     requested (pass a buffer or set return_last_state).  ``workspace`` is a
     uint8 CUDA tensor of at least scan_workspace_bytes(...) bytes; when None
     one is allocated here (through PyTorch's caching allocator).
+    ``initial_state`` (batch, dim, dstate) f32 starts the scan from that state
+    (ssm_scan_fwd_from_state); it may be the ``last_state`` tensor itself.
     """
     lib = load_library()
     dt = u.dtype
@@ -147,13 +153,25 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes > 0 else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        code = lib.ssm_scan_fwd(_ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev),
-                                _ptr(B, dt, dev), _ptr(C, dt, dev), _ptr(D, torch.float32, dev),
-                                _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
-                                int(bool(softplus)), _ptr(out, dt, dev),
-                                _ptr(last_state, torch.float32, dev), bt, dim, L, N,
-                                _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
-    _check("ssm_scan_fwd", code)
+        if initial_state is None:
+            code = lib.ssm_scan_fwd(_ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev),
+                                    _ptr(B, dt, dev), _ptr(C, dt, dev), _ptr(D, torch.float32, dev),
+                                    _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
+                                    int(bool(softplus)), _ptr(out, dt, dev),
+                                    _ptr(last_state, torch.float32, dev), bt, dim, L, N,
+                                    _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+            _check("ssm_scan_fwd", code)
+        else:
+            if tuple(initial_state.shape) != (bt, dim, N):
+                raise ValueError(f"initial_state must be {(bt, dim, N)}, got {tuple(initial_state.shape)}")
+            code = lib.ssm_scan_fwd_from_state(
+                _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
+                _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev),
+                _ptr(delta_bias, torch.float32, dev), int(bool(softplus)),
+                _ptr(initial_state, torch.float32, dev), _ptr(out, dt, dev),
+                _ptr(last_state, torch.float32, dev), bt, dim, L, N, _dtype_code(u),
+                _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+            _check("ssm_scan_fwd_from_state", code)
     return out, last_state
 
 

@@ -438,12 +438,19 @@ struct ScanKernel {
             pc.dsk = make_float2((p.D && pc.ok0) ? p.D[dp] : 0.f, (p.D && pc.ok1) ? p.D[dp + 1] : 0.f);
         }
 
+        // state before the first step: the caller's initial state, else zero
         float2 h[G / 2];
 #pragma unroll
-        for (int j = 0; j < G / 2; ++j) h[j] = make_float2(0.f, 0.f);
+        for (int j = 0; j < G / 2; ++j) {
+            const float* h0 = p.h0 + (b * p.dim + d) * N + g * G + 2 * j;
+            h[j] = (p.h0 && valid) ? make_float2(h0[0], h0[1]) : make_float2(0.f, 0.f);
+        }
         if constexpr (CF::kSplit) {
             float* s_car = sm + CF::OFF_CAR;
-            for (int i = tid; i < CW * N; i += THREADS) s_car[i] = 0.f;
+            for (int i = tid; i < CW * N; i += THREADS) {
+                const int64_t dc = d0 + i / N;
+                s_car[i] = (p.h0 && dc < p.dim) ? p.h0[(b * p.dim + dc) * N + i % N] : 0.f;
+            }
         }
 
         Regs rg;

@@ -113,6 +113,7 @@ struct RelayParams {
     int64_t lpad;
     int softplus;
     int has_z;
+    const float* h0;        // initial state or null
 };
 
 
@@ -152,7 +153,11 @@ scan_relay_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         for (int i = 0; i < W; ++i) mbar_init(bar0 + 8u * (W * P + i), 1);
         fence_mbar_init();
     }
-    for (int i = threadIdx.x; i < CW * N; i += CF::THREADS) carry0[i] = 0.f;
+    // the state entering chunk 0: the caller's initial state, else zero
+    for (int i = threadIdx.x; i < CW * N; i += CF::THREADS) {
+        const int dc = d0 + i / N;
+        carry0[i] = (p.h0 && dc < p.dim) ? p.h0[((size_t)b * p.dim + dc) * N + i % N] : 0.f;
+    }
     __syncthreads();
     if (threadIdx.x == 0) mbar_arrive(bar_cin);   // chunk 0's state (zeros) is ready
 
@@ -428,6 +433,7 @@ struct SegParams {
     int S;                  // segments per chain
     int cps;                // chunks per segment
     int workers;            // (main, helper) pairs in the grid
+    const float* h0;        // initial state (batch, dim, N) or null
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -650,6 +656,10 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             const float4 v = __ldcg(reinterpret_cast<const float4*>(hst));
             h0 = make_float2(v.x, v.y);
             h1 = make_float2(v.z, v.w);
+        } else if (p.h0 && ch_ok) {
+            const float4 v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.dim + d) * N + 4 * g);
+            h0 = make_float2(v.x, v.y);
+            h1 = make_float2(v.z, v.w);
         }
 
         for (int c = cb; c < ce; ++c, ++j) {
@@ -853,7 +863,7 @@ cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
         !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
         return cudaErrorInvalidValue;
     RelayParams rp{a.A, a.D, a.delta_bias, bc, a.last_state, (int)a.dim, (int)a.seqlen, lpad, a.softplus,
-                   a.z != nullptr};
+                   a.z != nullptr, a.h0};
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, RelayParams);
     static const Kern kerns[4] = {scan_relay_kernel<T, N, kFast, false, false>,
                                   scan_relay_kernel<T, N, kFast, false, true>,
@@ -959,7 +969,7 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
         return cudaErrorInvalidValue;
     SegParams sp{a.A, a.D, a.delta_bias, bc, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                 pl.units, pl.M, pl.S, pl.cps, pl.workers};
+                 pl.units, pl.M, pl.S, pl.cps, pl.workers, a.h0};
     void* args[] = {&mu, &md, &mz, &mo, &sp};
     // Segments wait on segments of other warps: every CTA must be resident,
     // which the cooperative launch guarantees (the grid never exceeds the
@@ -1006,7 +1016,7 @@ bool relay_supported(const ScanArgs& a, DType dt) {
     const int64_t es = dt == DType::BF16 ? 2 : 4;
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (!al16(a.u) || !al16(a.delta) || !al16(a.out) || (a.z && !al16(a.z)) || !al16(a.A) ||
-        (a.last_state && !al16(a.last_state)))
+        (a.last_state && !al16(a.last_state)) || (a.h0 && !al16(a.h0)))
         return false;
     if ((a.dim * es) % 16 != 0) return false;
     if (a.dim > (int64_t(1) << 31) - 64 || a.seqlen > (int64_t(1) << 31) - 64 || a.batch > 65535) return false;

@@ -194,6 +194,7 @@ struct TmParams {
     int S;                  // segments per chain
     int cps;                // chunks per segment
     int workers;            // CTAs in the grid
+    const float* h0;        // initial state (batch, dim, N) or null
 };
 
 __device__ __forceinline__ int tm_ld_acquire(const int* p) {
@@ -439,6 +440,10 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                     break;
                 }
                 const float4 v = __ldcg(reinterpret_cast<const float4*>(hst));
+                h0 = make_float2(v.x, v.y);
+                h1 = make_float2(v.z, v.w);
+            } else if (p.h0 && ch_ok) {
+                const float4 v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.dim + d) * N + 4 * g);
                 h0 = make_float2(v.x, v.y);
                 h1 = make_float2(v.z, v.w);
             }
@@ -849,6 +854,8 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                     break;
                 }
                 h = __ldcg(reinterpret_cast<const float2*>(hst));
+            } else if (p.h0 && ch_ok) {
+                h = *reinterpret_cast<const float2*>(p.h0 + ((size_t)b * p.dim + d) * N + 2 * g);
             }
 
             for (int c = cb; c < ce; ++c, ++j) {
@@ -1175,7 +1182,7 @@ cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) 
         !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw))
         return cudaErrorInvalidValue;
     TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                pl.units, pl.M, pl.S, pl.cps, pl.grid};
+                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0};
     void* args[] = {&mu, &md, &mz, &mo, &tp};
     // Segments wait on segments of other CTAs: every CTA must be resident,
     // which the cooperative launch guarantees (one CTA per SM, grid <= SMs).
@@ -1248,7 +1255,7 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                pl.units, pl.M, pl.S, pl.cps, pl.grid};
+                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0};
     void* args[] = {&mu, &md, &mz, &mo, &tp};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
                                        dim3(CF::THREADS), args, CF::SMEM, s);

@@ -139,11 +139,11 @@ int ssm_device_error(int clear) {
     return (a < 0 || b < 0) ? -1 : (a | b);
 }
 
-ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
-                        const void* C, const float* D, const void* z, const float* delta_bias,
-                        int softplus_flag, void* out, float* last_state, int64_t batch,
-                        int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* workspace,
-                        int64_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, const float* delta_bias,
+                                   int softplus_flag, const float* initial_state, void* out, float* last_state,
+                                   int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype,
+                                   void* workspace, int64_t workspace_bytes, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
@@ -154,7 +154,8 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
     const uintptr_t ea = (uintptr_t)es;
     if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
         !aligned(out, ea) || (z && !aligned(z, ea)) || !aligned(A, 4) || (D && !aligned(D, 4)) ||
-        (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)))
+        (delta_bias && !aligned(delta_bias, 4)) || (last_state && !aligned(last_state, 4)) ||
+        (initial_state && !aligned(initial_state, 4)))
         return SSM_ERR_ALIGN;
 
     const int64_t x_bytes = batch * seqlen * dim * es;
@@ -165,6 +166,15 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
     for (const Span& s : ins)
         if (overlap(so, s) || overlap(sl, s)) return SSM_ERR_ALIAS;
     if (overlap(so, sl)) return SSM_ERR_ALIAS;
+    // the initial state is an input; it may be the final-state array itself
+    // (resume in place), but must not overlap any other output or input
+    const Span sh{initial_state, batch * dim * dstate * 4};
+    if (initial_state) {
+        if (overlap(so, sh)) return SSM_ERR_ALIAS;
+        if (overlap(sl, sh) && initial_state != last_state) return SSM_ERR_ALIAS;
+        for (const Span& s : ins)
+            if (overlap(sh, s)) return SSM_ERR_ALIAS;
+    }
 
     if (workspace_bytes < 0 || (workspace && workspace_bytes == 0)) return SSM_ERR_SHAPE;
     if (workspace) {
@@ -172,14 +182,14 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
         const Span sw{workspace, workspace_bytes};
         for (const Span& s : ins)
             if (overlap(sw, s)) return SSM_ERR_ALIAS;
-        if (overlap(sw, so) || overlap(sw, sl)) return SSM_ERR_ALIAS;
+        if (overlap(sw, so) || overlap(sw, sl) || overlap(sw, sh)) return SSM_ERR_ALIAS;
     }
 
     int sms = 0;
     if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
 
     ssm::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, out, last_state,
-                    batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0};
+                    batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0, initial_state};
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The tensor-memory scan (two states per lane) runs whenever its
@@ -211,6 +221,15 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
     if (want_seg) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
     return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
+}
+
+ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
+                        const void* C, const float* D, const void* z, const float* delta_bias,
+                        int softplus_flag, void* out, float* last_state, int64_t batch,
+                        int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* workspace,
+                        int64_t workspace_bytes, void* stream) {
+    return ssm_scan_fwd_from_state(u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, out, last_state,
+                                   batch, dim, seqlen, dstate, dtype, workspace, workspace_bytes, stream);
 }
 
 ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,

@@ -28,6 +28,7 @@ struct ScanArgs {
     int64_t batch, dim, seqlen;
     int dstate;
     int softplus;
+    const float* h0;        // initial state (batch, dim, dstate) f32, or null for zero
 };
 
 // Arguments of one decode step; layouts as in ssm_scan.h.

@@ -86,6 +86,33 @@ def test_scan_rejects_bad_arguments(lib, kw, code):
     assert call_scan(lib, scan_args(**kw)) == code
 
 
+def call_scan_from(lib, a, h0):
+    return lib.ssm_scan_fwd_from_state(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                       a["delta_bias"], a["softplus"], h0, a["out"], a["last_state"],
+                                       a["batch"], a["dim"], a["seqlen"], a["dstate"], a["dtype"],
+                                       a["workspace"], a["workspace_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("h0,code", [
+    (P + 704 * MB + 2, 3),             # misaligned
+    (P + 512 * MB + 64, 6),            # inside out
+    (P + 64 * MB, 6),                  # inside delta (an input)
+    (P + 576 * MB + 64, 6),            # overlaps last_state without being it
+])
+def test_scan_from_state_rejects_bad_initial_state(lib, h0, code):
+    assert call_scan_from(lib, scan_args(), h0) == code
+
+
+def test_scan_from_state_validates_like_scan(lib):
+    """Same host checks as ssm_scan_fwd (only argument sets that are rejected
+    before anything is enqueued: these addresses are fake)."""
+    for kw in (dict(u=None), dict(dstate=3), dict(u=P + 1), dict(out=P + 1024), dict(batch=0)):
+        assert call_scan_from(lib, scan_args(**kw), None) == call_scan(lib, scan_args(**kw))
+        assert call_scan_from(lib, scan_args(**kw), P + 704 * MB) == call_scan(lib, scan_args(**kw))
+    # an initial state inside the workspace
+    assert call_scan_from(lib, scan_args(workspace=P + 704 * MB, workspace_bytes=MB), P + 704 * MB) == 6
+
+
 def upd_args(**kw):
     a = dict(state=P, x=P + 64 * MB, dt=P + 128 * MB, A=P + 192 * MB, B=P + 256 * MB, C=P + 320 * MB,
              D=P + 384 * MB, z=P + 448 * MB, dt_bias=P + 512 * MB, out=P + 576 * MB,
