@@ -51,6 +51,10 @@ def load(path: Optional[str] = None):
     lib.oracle_scan.restype = ctypes.c_int
     lib.oracle_scan_from.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 4
     lib.oracle_scan_from.restype = ctypes.c_int
+    lib.oracle_conv1d.argtypes = [dp, dp, dp, ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 4
+    lib.oracle_conv1d.restype = ctypes.c_int
+    lib.oracle_conv1d_update.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp] + [ctypes.c_int] * 3
+    lib.oracle_conv1d_update.restype = ctypes.c_int
     lib.oracle_step.argtypes = [dp] * 9 + [ctypes.c_int, dp] + [ctypes.c_int] * 3
     lib.oracle_step.restype = ctypes.c_int
     lib.oracle_softplus.argtypes = [ctypes.c_double]
@@ -111,6 +115,39 @@ def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, 
                          _p(dt_bias), int(bool(dt_softplus)), _p(out), bt, dim, N)
     if rc != 0:
         raise ValueError(f"oracle_step rejected its arguments (code {rc})")
+    return out
+
+
+def conv1d(x, w, bias=None, silu=True, state_in=None, want_state=True, lib=None):
+    """Depthwise causal convolution (+ SiLU).  x: (batch, L, dim); w: (dim, W);
+    bias: (dim,); state_in: (batch, dim, W-1) or None (zeros).  Returns
+    (out (batch, L, dim), state_out (batch, dim, W-1) or None), float64."""
+    lib = lib or load()
+    x, w, bias, state_in = map(_f64, (x, w, bias, state_in))
+    bt, L, dim = x.shape
+    W = w.shape[1]
+    assert w.shape == (dim, W) and (state_in is None or state_in.shape == (bt, dim, W - 1))
+    out = np.empty_like(x)
+    st = np.empty((bt, dim, W - 1)) if want_state else None
+    rc = lib.oracle_conv1d(_p(x), _p(w), _p(bias), int(bool(silu)), _p(state_in), _p(out), _p(st),
+                           bt, dim, L, W)
+    if rc != 0:
+        raise ValueError(f"oracle_conv1d rejected its arguments (code {rc})")
+    return out, st
+
+
+def conv1d_update(state, x, w, bias=None, silu=True, lib=None):
+    """One decode step; ``state`` (batch, dim, W-1) float64 is updated in place.
+    x: (batch, dim).  Returns out (batch, dim)."""
+    lib = lib or load()
+    assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
+    x, w, bias = map(_f64, (x, w, bias))
+    bt, dim = x.shape
+    W = w.shape[1]
+    out = np.empty_like(x)
+    rc = lib.oracle_conv1d_update(_p(state), _p(x), _p(w), _p(bias), int(bool(silu)), _p(out), bt, dim, W)
+    if rc != 0:
+        raise ValueError(f"oracle_conv1d_update rejected its arguments (code {rc})")
     return out
 
 

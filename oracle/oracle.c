@@ -166,6 +166,75 @@ int oracle_step(double* state, const double* x, const double* dt,
 }
 
 /* Scalar helpers exposed so the pins can test them against closed forms. */
+/* Depthwise causal convolution over time, per channel, width W, then the
+ * optional SiLU: the local convolution that produces the scan input u in the
+ * Mamba block ("d_conv: local convolution width" in the pages' usage examples).
+ * Reading adopted (the pages give only the width): PyTorch Conv1d's
+ * cross-correlation with W-1 steps of left padding, truncated to L outputs,
+ *     y_t = bias[d] + sum_{k=0}^{W-1} w[d][k] * x_{t-(W-1)+k},
+ * where x_s for s < 0 is the carried state state_in[b][d][(W-1)+s] (the W-1
+ * inputs before this sequence, oldest first), or 0 without one.  state_out
+ * (nullable) receives the W-1 last inputs, oldest first.  x, out:
+ * [batch][seqlen][dim]; w: [dim][W]; state: [batch][dim][W-1]. */
+static double conv_input(const double* x, const double* state_in, ptrdiff_t b, ptrdiff_t d,
+                         ptrdiff_t s, ptrdiff_t L, ptrdiff_t Dm, int W) {
+    if (s >= 0) return x[(b * L + s) * Dm + d];
+    return state_in ? state_in[(b * Dm + d) * (W - 1) + (W - 1) + s] : 0.0;
+}
+
+int oracle_conv1d(const double* x, const double* w, const double* bias, int silu_flag,
+                  const double* state_in, double* out, double* state_out,
+                  int batch, int dim, int seqlen, int width) {
+    if (!x || !w || !out) return 1;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || width < 1) return 2;
+    const ptrdiff_t L = seqlen, Dm = dim;
+    const int W = width;
+    const long long total = (long long)batch * dim;
+#pragma omp parallel for schedule(dynamic, 1)
+    for (long long bd = 0; bd < total; ++bd) {
+        const ptrdiff_t b = bd / Dm, d = bd % Dm;
+        for (ptrdiff_t t = 0; t < L; ++t) {
+            double acc = bias ? bias[d] : 0.0;
+            for (int k = 0; k < W; ++k)
+                acc += w[d * W + k] * conv_input(x, state_in, b, d, t - (W - 1) + k, L, Dm, W);
+            out[(b * L + t) * Dm + d] = silu_flag ? silu(acc) : acc;
+        }
+    }
+    if (state_out) {
+        /* gather every channel's last inputs first: state_out may be state_in */
+        const long long n = total * (W - 1);
+        double* tmp = (double*)malloc((size_t)(n > 0 ? n : 1) * sizeof(double));
+        if (!tmp) return 3;
+        for (long long bd = 0; bd < total; ++bd)
+            for (int k = 0; k < W - 1; ++k)
+                tmp[bd * (W - 1) + k] = conv_input(x, state_in, bd / Dm, bd % Dm, L - (W - 1) + k, L, Dm, W);
+        for (long long i = 0; i < n; ++i) state_out[i] = tmp[i];
+        free(tmp);
+    }
+    return 0;
+}
+
+/* One decode step of the convolution: the window is the carried state
+ * (oldest first) followed by the new input; the state then drops its oldest
+ * entry and appends the new input. */
+int oracle_conv1d_update(double* state, const double* x, const double* w, const double* bias,
+                         int silu_flag, double* out, int batch, int dim, int width) {
+    if (!state || !x || !w || !out) return 1;
+    if (batch <= 0 || dim <= 0 || width < 1) return 2;
+    const int W = width;
+    for (long long bd = 0; bd < (long long)batch * dim; ++bd) {
+        const ptrdiff_t d = bd % dim;
+        double* st = state + bd * (W - 1);
+        double acc = bias ? bias[d] : 0.0;
+        for (int k = 0; k < W - 1; ++k) acc += w[d * W + k] * st[k];
+        acc += w[d * W + W - 1] * x[bd];
+        out[bd] = silu_flag ? silu(acc) : acc;
+        for (int k = 0; k + 1 < W - 1; ++k) st[k] = st[k + 1];
+        if (W > 1) st[W - 2] = x[bd];
+    }
+    return 0;
+}
+
 double oracle_softplus(double x) { return softplus(x); }
 double oracle_silu(double x) { return silu(x); }
 

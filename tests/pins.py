@@ -22,7 +22,11 @@ disagrees with an independent route to the same answer:
 * initial state: the unrolled sum with the initial state's decay term
                  exp(A_n sum_{r<=t} Delta_r) h0_n added, and a sequence cut
                  anywhere and scanned in two pieces (the second from the first's
-                 final state) reproducing the whole scan exactly.
+                 final state) reproducing the whole scan exactly;
+* causal conv:   the impulse response is the reversed taps; numpy.convolve of
+                 the carried state followed by the input gives every output and
+                 the final state; a split sequence and a chain of decode steps
+                 reproduce the whole convolution exactly.
 
 Softplus and sigmoid are taken from numpy/scipy library routines here
 (``np.logaddexp``, ``scipy.special.expit``), never from the oracle.
@@ -307,6 +311,60 @@ def pin_split_equals_whole(lib):
         assert np.array_equal(s2, last), f"split at {cut} changed the final state"
 
 
+def conv_case(seed, bt=2, L=10, dim=3, W=4, with_bias=True, with_state=True):
+    r = _rng(seed)
+    return dict(x=r.standard_normal((bt, L, dim)), w=r.standard_normal((dim, W)),
+                bias=r.standard_normal(dim) if with_bias else None,
+                state=r.standard_normal((bt, dim, W - 1)) if with_state else None)
+
+
+def pin_conv_impulse(lib):
+    for W in (2, 3, 4):
+        c = conv_case(120 + W, bt=1, L=12, dim=2, W=W, with_bias=False, with_state=False)
+        x = np.zeros((1, 12, 2))
+        x[0, 5, 1] = 1.0
+        out, _ = oracle.conv1d(x, c["w"], None, False, None, lib=lib)
+        want = np.zeros((12,))
+        want[5:5 + W] = c["w"][1, ::-1]
+        assert np.array_equal(out[0, :, 1], want), f"impulse response, width {W}"
+        assert np.array_equal(out[0, :, 0], np.zeros(12)), "impulse leaked into another channel"
+
+
+def pin_conv_numpy(lib):
+    for seed, kw in [(130, {}), (131, dict(with_state=False)), (132, dict(W=2, with_bias=False)),
+                     (133, dict(L=2, W=4)), (134, dict(L=1, W=3))]:
+        c = conv_case(seed, **kw)
+        for silu in (False, True):
+            out, st = oracle.conv1d(c["x"], c["w"], c["bias"], silu, c["state"], lib=lib)
+            bt, L, dim = c["x"].shape
+            W = c["w"].shape[1]
+            for b in range(bt):
+                for d in range(dim):
+                    prev = np.zeros(W - 1) if c["state"] is None else c["state"][b, d]
+                    seq = np.concatenate([prev, c["x"][b, :, d]])
+                    y = np.convolve(seq, c["w"][d, ::-1], mode="valid")
+                    y = y + (0.0 if c["bias"] is None else c["bias"][d])
+                    if silu:
+                        y = y * expit(y)
+                    _close(out[b, :, d], y, what=f"conv seed {seed} ({b},{d})")
+                    assert np.array_equal(st[b, d], seq[len(seq) - (W - 1):]), f"conv state seed {seed}"
+
+
+def pin_conv_split_and_decode(lib):
+    c = conv_case(140, bt=2, L=11, dim=3, W=4)
+    out, st = oracle.conv1d(c["x"], c["w"], c["bias"], True, c["state"], lib=lib)
+    for cut in (1, 2, 7):
+        o1, s1 = oracle.conv1d(np.ascontiguousarray(c["x"][:, :cut]), c["w"], c["bias"], True, c["state"], lib=lib)
+        o2, s2 = oracle.conv1d(np.ascontiguousarray(c["x"][:, cut:]), c["w"], c["bias"], True, s1, lib=lib)
+        assert np.array_equal(np.concatenate([o1, o2], axis=1), out), f"conv split at {cut}"
+        assert np.array_equal(s2, st), f"conv split state at {cut}"
+    state = c["state"].copy()
+    for t in range(11):
+        o = oracle.conv1d_update(state, np.ascontiguousarray(c["x"][:, t]), c["w"], c["bias"], True, lib=lib)
+        assert np.array_equal(o, out[:, t]), f"conv decode step {t}"
+    assert np.array_equal(state, st), "conv decode final state"
+
+
 def pin_scalar_functions(lib):
     sp = lambda x: oracle.softplus(x, lib=lib)
     si = lambda x: oracle.silu(x, lib=lib)
@@ -326,4 +384,5 @@ def pin_scalar_functions(lib):
 ALL_PINS = [pin_brute_force, pin_time_invariant_convolution, pin_associative_scan,
             pin_delta_to_zero, pin_memoryless_limit, pin_linear_in_u, pin_causal,
             pin_bc_scale, pin_channel_permutation, pin_decode_chain_equals_scan,
-            pin_initial_state_brute_force, pin_split_equals_whole, pin_scalar_functions]
+            pin_initial_state_brute_force, pin_split_equals_whole, pin_conv_impulse, pin_conv_numpy,
+            pin_conv_split_and_decode, pin_scalar_functions]

@@ -35,6 +35,12 @@ MUTATIONS = [
      "timestep(dt[i], NULL, (int)d, dt_softplus)"),
     ("initial state ignored", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
      "h[n] = 0.0;"),
+    ("conv taps reversed", "acc += w[d * W + k] * conv_input(", "acc += w[d * W + (W - 1 - k)] * conv_input("),
+    ("conv state oldest-last", "state_in[(b * Dm + d) * (W - 1) + (W - 1) + s]", "state_in[(b * Dm + d) * (W - 1) - 1 - s]"),
+    ("conv without bias", "double acc = bias ? bias[d] : 0.0;\n            for (int k = 0; k < W; ++k)",
+     "double acc = 0.0;\n            for (int k = 0; k < W; ++k)"),
+    ("conv decode shifts the wrong way", "for (int k = 0; k + 1 < W - 1; ++k) st[k] = st[k + 1];",
+     "for (int k = W - 2; k > 0; --k) st[k] = st[k - 1];"),
     ("initial state read transposed", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
      "h[n] = initial_state ? initial_state[(b * N + n) * Dm + d] : 0.0;"),
 ]
