@@ -201,6 +201,47 @@ SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
                             int dt_softplus, int dtype, void* stream);
 
 /* Static, human-readable name of a status code (never NULL). */
+/*
+ * ssm_conv1d_fwd -- depthwise causal convolution over time (+ SiLU): the step
+ * that produces the scan input u in the Mamba block (width d_conv, the
+ * "local convolution width" of the pages' usage examples).  Per channel d,
+ *     y_t   = bias[d] + sum_{k=0}^{width-1} weight[d][k] * x_{t-(width-1)+k}
+ *     out_t = silu(y_t) if silu_flag else y_t
+ * where x_s for s < 0 is conv_state_in[b][d][(width-1)+s] (the width-1
+ * inputs before the sequence, oldest first) or 0 when conv_state_in is NULL.
+ *
+ *   x, out          [batch][seqlen][dim]     dtype
+ *   weight          [dim][width]             f32
+ *   bias            [dim]                    f32   NULL = 0
+ *   conv_state_in   [batch][dim][width-1]    f32   NULL = zeros
+ *   conv_state_out  [batch][dim][width-1]    f32   NULL = not written; the
+ *                   width-1 last inputs, oldest first (a later call's
+ *                   conv_state_in, or ssm_conv1d_update's state)
+ *
+ * width 1..4 (SSM_ERR_UNSUPPORTED above).  conv_state_out may be
+ * conv_state_in itself (in place); out and conv_state_out must not overlap any
+ * other argument (SSM_ERR_ALIAS).  Pointers aligned to their element size;
+ * rows of dim * sizeof(dtype) a multiple of 16 with 16-byte aligned x and out
+ * take 16-byte vectors.  Enqueued on `stream`.
+ */
+SSM_API ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias, int silu_flag,
+                                  const float* conv_state_in, void* out, float* conv_state_out,
+                                  int64_t batch, int64_t dim, int64_t seqlen, int64_t width, int dtype,
+                                  void* stream);
+
+/*
+ * ssm_conv1d_update -- one decode step of the same convolution: the window is
+ * conv_state (oldest first) followed by x; out = silu?(bias + weight . window);
+ * conv_state then drops its oldest input and appends x (in place).
+ *
+ *   conv_state  [batch][dim][width-1]  f32    read and written (NULL only for width 1)
+ *   x, out      [batch][dim]           dtype
+ *   weight, bias as in ssm_conv1d_fwd
+ */
+SSM_API ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weight, const float* bias,
+                                     int silu_flag, void* out, int64_t batch, int64_t dim, int64_t width,
+                                     int dtype, void* stream);
+
 SSM_API const char* ssm_status_string(int status);
 
 /*

@@ -2,14 +2,18 @@
 
 Public calls (thin wrappers over the C ABI in include/ssm_scan.h):
 
-* ``ssm_scan_fwd``     -- full-sequence scan (prefill / training forward);
-* ``ssm_state_update`` -- single-token recurrent update (decode).
+* ``ssm_scan_fwd``     -- full-sequence scan (prefill / training forward),
+                          optionally from an initial state (``initial_state=``);
+* ``ssm_state_update`` -- single-token recurrent update (decode);
+* ``conv1d_fwd``       -- the depthwise causal conv1d (+ SiLU) that produces the
+                          scan input, with a carried conv state;
+* ``conv1d_update``    -- its single-token decode step.
 
 The CUDA library ``libssmscan.so`` is loaded on first use; there is no CPU
 fallback.
 """
-from ._lib import (SSMError, device_error, load_library, scan_workspace_bytes,  # noqa: F401
-                   ssm_scan_fwd, ssm_state_update, status_string)
+from ._lib import (SSMError, conv1d_fwd, conv1d_update, device_error, load_library,  # noqa: F401
+                   scan_workspace_bytes, ssm_scan_fwd, ssm_state_update, status_string)
 
-__all__ = ["ssm_scan_fwd", "ssm_state_update", "scan_workspace_bytes", "device_error",
-           "load_library", "status_string", "SSMError"]
+__all__ = ["ssm_scan_fwd", "ssm_state_update", "conv1d_fwd", "conv1d_update", "scan_workspace_bytes",
+           "device_error", "load_library", "status_string", "SSMError"]

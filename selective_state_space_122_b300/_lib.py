@@ -23,7 +23,8 @@ STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN"
           7: "SSM_ERR_LAUNCH", 8: "SSM_ERR_DEVICE", 9: "SSM_ERR_SCRATCH"}
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
            "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
-           "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state")
+           "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state", "ssm_conv1d_fwd",
+           "ssm_conv1d_update")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -50,6 +51,10 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_scan_fwd_from_state.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, fp,
                                             i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_fwd_from_state.restype = ci
+    lib.ssm_conv1d_fwd.argtypes = [vp, fp, fp, ci, fp, vp, fp, i64, i64, i64, i64, ci, vp]
+    lib.ssm_conv1d_fwd.restype = ci
+    lib.ssm_conv1d_update.argtypes = [fp, vp, fp, fp, ci, vp, i64, i64, i64, ci, vp]
+    lib.ssm_conv1d_update.restype = ci
     lib.ssm_scan_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
     lib.ssm_scan_workspace_bytes.restype = i64
     lib.ssm_device_error.argtypes = [ci]
@@ -173,6 +178,49 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                 _ptr(workspace, None, dev), ws_bytes, _stream(dev))
             _check("ssm_scan_fwd_from_state", code)
     return out, last_state
+
+
+def conv1d_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,
+               silu: bool = True, state_in: Optional[torch.Tensor] = None, out: Optional[torch.Tensor] = None,
+               state_out: Optional[torch.Tensor] = None,
+               return_state: bool = False) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
+    """Depthwise causal conv1d (+ SiLU) over (batch, L, dim); see ssm_scan.h.
+    weight: (dim, W) f32; bias: (dim,) f32; state_in / state_out: (batch, dim,
+    W-1) f32 (state_out may be state_in).  Returns (out, state_out)."""
+    lib = load_library()
+    dt, dev = x.dtype, x.device
+    bt, L, dim = x.shape
+    W = weight.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    if state_out is None and return_state:
+        state_out = torch.empty((bt, dim, W - 1), dtype=torch.float32, device=dev)
+    with torch.cuda.device(dev):
+        code = lib.ssm_conv1d_fwd(_ptr(x, dt, dev), _ptr(weight, torch.float32, dev),
+                                  _ptr(bias, torch.float32, dev), int(bool(silu)),
+                                  _ptr(state_in, torch.float32, dev), _ptr(out, dt, dev),
+                                  _ptr(state_out, torch.float32, dev), bt, dim, L, W, _dtype_code(x),
+                                  _stream(dev))
+    _check("ssm_conv1d_fwd", code)
+    return out, state_out
+
+
+def conv1d_update(state: torch.Tensor, x: torch.Tensor, weight: torch.Tensor,
+                  bias: Optional[torch.Tensor] = None, silu: bool = True,
+                  out: Optional[torch.Tensor] = None) -> torch.Tensor:
+    """One decode step of the conv, in place on ``state`` (batch, dim, W-1) f32."""
+    lib = load_library()
+    dt, dev = x.dtype, x.device
+    bt, dim = x.shape
+    W = weight.shape[1]
+    if out is None:
+        out = torch.empty_like(x)
+    with torch.cuda.device(dev):
+        code = lib.ssm_conv1d_update(_ptr(state, torch.float32, dev), _ptr(x, dt, dev),
+                                     _ptr(weight, torch.float32, dev), _ptr(bias, torch.float32, dev),
+                                     int(bool(silu)), _ptr(out, dt, dev), bt, dim, W, _dtype_code(x), _stream(dev))
+    _check("ssm_conv1d_update", code)
+    return out
 
 
 def ssm_state_update(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: torch.Tensor,

@@ -232,6 +232,61 @@ ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const 
                                    batch, dim, seqlen, dstate, dtype, workspace, workspace_bytes, stream);
 }
 
+ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias, int silu_flag,
+                          const float* conv_state_in, void* out, float* conv_state_out, int64_t batch,
+                          int64_t dim, int64_t seqlen, int64_t width, int dtype, void* stream) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (!x || !weight || !out) return SSM_ERR_NULL;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || width <= 0) return SSM_ERR_SHAPE;
+    if (width > 4) return SSM_ERR_UNSUPPORTED;
+    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 4) || (bias && !aligned(bias, 4)) ||
+        (conv_state_in && !aligned(conv_state_in, 4)) || (conv_state_out && !aligned(conv_state_out, 4)))
+        return SSM_ERR_ALIGN;
+    const int64_t x_bytes = batch * seqlen * dim * es, st_bytes = batch * dim * (width - 1) * 4;
+    const Span sx{x, x_bytes}, sw{weight, dim * width * 4}, sb{bias, dim * 4}, si{conv_state_in, st_bytes};
+    const Span so{out, x_bytes}, sso{conv_state_out, st_bytes};
+    for (const Span& s : {sx, sw, sb, si})
+        if (overlap(so, s)) return SSM_ERR_ALIAS;
+    for (const Span& s : {sx, sw, sb, so})
+        if (overlap(sso, s)) return SSM_ERR_ALIAS;
+    // the carried state may be updated in place, but not overlap partially
+    if (overlap(si, sso) && conv_state_in != conv_state_out) return SSM_ERR_ALIAS;
+    int sms = 0;
+    if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
+    ssm::ConvArgs a{x, weight, bias, conv_state_in, out, conv_state_out, batch, dim, seqlen, (int)width,
+                    silu_flag ? 1 : 0};
+    return launch_status(ssm::launch_conv1d_fwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+                                                static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weight, const float* bias,
+                             int silu_flag, void* out, int64_t batch, int64_t dim, int64_t width, int dtype,
+                             void* stream) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (!x || !weight || !out || (width > 1 && !conv_state)) return SSM_ERR_NULL;
+    if (batch <= 0 || dim <= 0 || width <= 0) return SSM_ERR_SHAPE;
+    if (width > 4) return SSM_ERR_UNSUPPORTED;
+    if (batch * dim > kMaxElems / 16) return SSM_ERR_SHAPE;
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
+    if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 4) || (bias && !aligned(bias, 4)) ||
+        (conv_state && !aligned(conv_state, 4)))
+        return SSM_ERR_ALIGN;
+    const Span sx{x, batch * dim * es}, sw{weight, dim * width * 4}, sb{bias, dim * 4};
+    const Span so{out, batch * dim * es}, ss{conv_state, batch * dim * (width - 1) * 4};
+    for (const Span& s : {sx, sw, sb, ss})
+        if (overlap(so, s)) return SSM_ERR_ALIAS;
+    for (const Span& s : {sx, sw, sb})
+        if (overlap(ss, s)) return SSM_ERR_ALIAS;
+    int sms = 0;
+    if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
+    ssm::ConvArgs a{x, weight, bias, nullptr, out, conv_state, batch, dim, 1, (int)width, silu_flag ? 1 : 0};
+    return launch_status(ssm::launch_conv1d_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+                                                   static_cast<cudaStream_t>(stream)));
+}
+
 ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
                             const void* B, const void* C, const float* D, const void* z,
                             const float* dt_bias, void* out, int64_t batch, int64_t dim,

@@ -71,6 +71,23 @@ cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cuda
 int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes);
 cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
 
+// Depthwise causal conv1d (+ SiLU) and its decode step (conv1d.cu); layouts
+// as in ssm_scan.h.  For the decode step, state_out is the state updated in
+// place and state_in is unused.
+struct ConvArgs {
+    const void* x;
+    const float* w;
+    const float* bias;
+    const float* state_in;
+    void* out;
+    float* state_out;
+    int64_t batch, dim, seqlen;
+    int width;
+    int silu;
+};
+cudaError_t launch_conv1d_fwd(const ConvArgs& a, DType dt, cudaStream_t s);
+cudaError_t launch_conv1d_update(const ConvArgs& a, DType dt, cudaStream_t s);
+
 // Tensor-memory scan (scan_tmem.cu): bf16 activations, 16 states.  Workspace:
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
 bool tmem_supported(const ScanArgs& a, DType dt);

@@ -3,6 +3,7 @@
     python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
            [--N N] [--iters K] [--path tmem|seg|relay|generic]
     python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K]
+    python -m selective_state_space_122_b300.profile conv [--batch B] [--dim D] [--L L] [--W W] [--iters K]
     python -m selective_state_space_122_b300.profile units
 
 ``scan`` runs ssm_scan_fwd on seeded on-device bf16 inputs shaped like the
@@ -90,6 +91,29 @@ def cmd_decode(a):
     return 0
 
 
+def cmd_conv(a):
+    from ._lib import conv1d_fwd
+    dev = torch.device("cuda", 0)
+    g = torch.Generator(device=dev)
+    g.manual_seed(2)
+    x = torch.randn(a.batch, a.L, a.dim, device=dev, generator=g).bfloat16()
+    w = torch.randn(a.dim, a.W, device=dev, generator=g) * 0.5
+    bias = torch.randn(a.dim, device=dev, generator=g) * 0.5
+    st = torch.zeros(a.batch, a.dim, a.W - 1, device=dev)
+    out = torch.empty_like(x)
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    nbytes = 2 * x.numel() * 2
+    for i in range(a.iters):
+        e0.record()
+        conv1d_fwd(x, w, bias, True, st, out=out, state_out=st)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"conv {a.batch}x{a.L}x{a.dim} W{a.W} iter {i}: {ms:.3f} ms "
+              f"({nbytes / (ms * 1e-3) / 1e9:.0f} GB/s)", flush=True)
+    return 0
+
+
 def cmd_units(a):
     lib = ctypes.CDLL(libbuild.PEAK_LIB)
     lib.ssmpk_probe_shape.argtypes = [ctypes.c_int] * 4
@@ -122,10 +146,16 @@ def main(argv=None):
     d.add_argument("--dim", type=int, default=5120)
     d.add_argument("--N", type=int, default=16)
     d.add_argument("--iters", type=int, default=5)
+    cv = sub.add_parser("conv")
+    cv.add_argument("--batch", type=int, default=1)
+    cv.add_argument("--dim", type=int, default=5120)
+    cv.add_argument("--L", type=int, default=131072)
+    cv.add_argument("--W", type=int, default=4)
+    cv.add_argument("--iters", type=int, default=5)
     u = sub.add_parser("units")
     u.add_argument("--clock-mhz", type=float, default=2032.0)
     a = ap.parse_args(argv)
-    return {"scan": cmd_scan, "decode": cmd_decode, "units": cmd_units}[a.cmd](a)
+    return {"scan": cmd_scan, "decode": cmd_decode, "conv": cmd_conv, "units": cmd_units}[a.cmd](a)
 
 
 if __name__ == "__main__":

@@ -113,6 +113,36 @@ def test_scan_from_state_validates_like_scan(lib):
     assert call_scan_from(lib, scan_args(workspace=P + 704 * MB, workspace_bytes=MB), P + 704 * MB) == 6
 
 
+def call_conv(lib, **kw):
+    a = dict(x=P, w=P + 64 * MB, bias=P + 128 * MB, silu=1, st_in=P + 192 * MB, out=P + 256 * MB,
+             st_out=P + 320 * MB, batch=2, dim=64, seqlen=128, width=4, dtype=1, stream=None)
+    a.update(kw)
+    return lib.ssm_conv1d_fwd(a["x"], a["w"], a["bias"], a["silu"], a["st_in"], a["out"], a["st_out"], a["batch"],
+                              a["dim"], a["seqlen"], a["width"], a["dtype"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(x=None), 1), (dict(w=None), 1), (dict(out=None), 1), (dict(seqlen=0), 2), (dict(width=0), 2),
+    (dict(width=5), 4), (dict(dtype=3), 5), (dict(x=P + 1), 3), (dict(st_out=P + 320 * MB + 2), 3),
+    (dict(out=P + 64), 6), (dict(out=P + 64 * MB), 6), (dict(st_out=P + 8), 6),
+    (dict(st_out=P + 192 * MB + 4), 6),
+])
+def test_conv1d_rejects_bad_arguments(lib, kw, code):
+    assert call_conv(lib, **kw) == code
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(state=None), 1), (dict(x=None), 1), (dict(width=7), 4), (dict(batch=0), 2),
+    (dict(out=P + 8), 6), (dict(state=P + 64 * MB + 4), 6), (dict(state=P + 2), 3),
+])
+def test_conv1d_update_rejects_bad_arguments(lib, kw, code):
+    a = dict(state=P + 192 * MB, x=P, w=P + 64 * MB, bias=P + 128 * MB, silu=1, out=P + 256 * MB,
+             batch=2, dim=64, width=4, dtype=1, stream=None)
+    a.update(kw)
+    assert lib.ssm_conv1d_update(a["state"], a["x"], a["w"], a["bias"], a["silu"], a["out"], a["batch"],
+                                 a["dim"], a["width"], a["dtype"], a["stream"]) == code
+
+
 def upd_args(**kw):
     a = dict(state=P, x=P + 64 * MB, dt=P + 128 * MB, A=P + 192 * MB, B=P + 256 * MB, C=P + 320 * MB,
              D=P + 384 * MB, z=P + 448 * MB, dt_bias=P + 512 * MB, out=P + 576 * MB,
