@@ -51,6 +51,8 @@ def load(path: Optional[str] = None):
     lib.oracle_scan.restype = ctypes.c_int
     lib.oracle_scan_from.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 4
     lib.oracle_scan_from.restype = ctypes.c_int
+    lib.oracle_scan_bwd.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 9 + [ctypes.c_int] * 4
+    lib.oracle_scan_bwd.restype = ctypes.c_int
     lib.oracle_conv1d.argtypes = [dp, dp, dp, ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 4
     lib.oracle_conv1d.restype = ctypes.c_int
     lib.oracle_conv1d_update.argtypes = [dp, dp, dp, dp, ctypes.c_int, dp] + [ctypes.c_int] * 3
@@ -116,6 +118,27 @@ def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, 
     if rc != 0:
         raise ValueError(f"oracle_step rejected its arguments (code {rc})")
     return out
+
+
+def scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, lib=None):
+    """Gradients of L = sum(dout * out) of the scan (from h = 0) with respect to
+    every input.  Returns a dict du, ddelta (batch, L, dim); dA (dim, N); dB, dC
+    (batch, N, L); dD, ddelta_bias (dim,) or None; dz (batch, L, dim) or None."""
+    lib = lib or load()
+    u, delta, A, B, C, D, z, delta_bias, dout = map(_f64, (u, delta, A, B, C, D, z, delta_bias, dout))
+    bt, L, dim = u.shape
+    N = A.shape[1]
+    g = dict(du=np.empty_like(u), ddelta=np.empty_like(u), dA=np.empty_like(A), dB=np.empty_like(B),
+             dC=np.empty_like(C), dD=None if D is None else np.empty(dim),
+             dz=None if z is None else np.empty_like(u),
+             ddelta_bias=None if delta_bias is None else np.empty(dim))
+    rc = lib.oracle_scan_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                             int(bool(softplus)), _p(dout), _p(g["du"]), _p(g["ddelta"]), _p(g["dA"]),
+                             _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]), _p(g["ddelta_bias"]),
+                             bt, dim, L, N)
+    if rc != 0:
+        raise ValueError(f"oracle_scan_bwd rejected its arguments (code {rc})")
+    return g
 
 
 def conv1d(x, w, bias=None, silu=True, state_in=None, want_state=True, lib=None):

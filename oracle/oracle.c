@@ -166,6 +166,102 @@ int oracle_step(double* state, const double* x, const double* dt,
 }
 
 /* Scalar helpers exposed so the pins can test them against closed forms. */
+/* Backward of the full-sequence scan (from h = 0): given dout = dL/d out,
+ * every input's gradient, by the adjoint of the recurrence above (the
+ * gradients the "training" mode of the pages' "Efficient Scan" needs).  With
+ *   x_t = delta_raw_t + bias,  Delta_t = softplus(x_t) (or x_t),
+ *   a_t[n] = exp(Delta_t A[n]),  h_t = a_t h_{t-1} + Delta_t B_t u_t,
+ *   y_t = C_t . h_t + D u_t,  out_t = y_t g_t,  g_t = silu(z_t) (or 1),
+ * the adjoint state lambda_t = dL/dh_t runs backwards:
+ *   dy_t = dout_t g_t,  lambda_t = C_t dy_t + a_{t+1} lambda_{t+1}  (lambda_L = 0),
+ * and
+ *   dC_t[n] += dy_t h_t[n]            dB_t[n] += lambda_t[n] Delta_t u_t
+ *   du_t     = D dy_t + sum_n lambda_t[n] Delta_t B_t[n]
+ *   dDelta_t = sum_n lambda_t[n] (A[n] a_t[n] h_{t-1}[n] + B_t[n] u_t)
+ *   dA[n]   += lambda_t[n] Delta_t a_t[n] h_{t-1}[n]
+ *   dD      += dy_t u_t,   dz_t = dout_t y_t silu'(z_t)
+ *   ddelta_raw_t = dDelta_t softplus'(x_t) (= dDelta_t without softplus),
+ *   dbias  += ddelta_raw_t.
+ * B and C are shared by all channels, so dB and dC sum over channels.  Every
+ * output array is overwritten; dz, dD and dbias may be NULL when z, D or the
+ * bias is absent.  Sequential (no threads): each output sums over channels. */
+static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
+
+int oracle_scan_bwd(const double* u, const double* delta, const double* A,
+                    const double* B, const double* C, const double* D,
+                    const double* z, const double* delta_bias, int softplus_flag,
+                    const double* dout, double* du, double* ddelta, double* dA,
+                    double* dB, double* dC, double* dD, double* dz, double* dbias,
+                    int batch, int dim, int seqlen, int dstate) {
+    if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return 1;
+    if (check_dims(batch, dim, seqlen, dstate)) return 2;
+    const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
+    for (ptrdiff_t i = 0; i < Dm * N; ++i) dA[i] = 0.0;
+    for (ptrdiff_t i = 0; i < (ptrdiff_t)batch * N * L; ++i) dB[i] = dC[i] = 0.0;
+    if (dD) for (ptrdiff_t d = 0; d < Dm; ++d) dD[d] = 0.0;
+    if (dbias) for (ptrdiff_t d = 0; d < Dm; ++d) dbias[d] = 0.0;
+    double* hs = (double*)malloc((size_t)(L + 1) * N * sizeof(double));   /* h_{-1} .. h_{L-1} */
+    double* dls = (double*)malloc((size_t)L * sizeof(double));
+    double* ys = (double*)malloc((size_t)L * sizeof(double));
+    if (!hs || !dls || !ys) { free(hs); free(dls); free(ys); return 3; }
+    for (ptrdiff_t b = 0; b < batch; ++b)
+        for (ptrdiff_t d = 0; d < Dm; ++d) {
+            const double* Ar = A + d * N;
+            const double* Bb = B + b * N * L;
+            const double* Cb = C + b * N * L;
+            const double Dd = D ? D[d] : 0.0;
+            /* forward, keeping every state */
+            for (ptrdiff_t n = 0; n < N; ++n) hs[n] = 0.0;
+            for (ptrdiff_t t = 0; t < L; ++t) {
+                const ptrdiff_t i = (b * L + t) * Dm + d;
+                const double dlt = timestep(delta[i], delta_bias, (int)d, softplus_flag);
+                dls[t] = dlt;
+                double y = 0.0;
+                for (ptrdiff_t n = 0; n < N; ++n) {
+                    const double h = exp(dlt * Ar[n]) * hs[t * N + n] + (dlt * Bb[n * L + t]) * u[i];
+                    hs[(t + 1) * N + n] = h;
+                    y += Cb[n * L + t] * h;
+                }
+                ys[t] = y + Dd * u[i];
+            }
+            /* backward */
+            double lam[ORACLE_MAX_DSTATE], anext[ORACLE_MAX_DSTATE];
+            for (ptrdiff_t n = 0; n < N; ++n) lam[n] = anext[n] = 0.0;
+            for (ptrdiff_t t = L - 1; t >= 0; --t) {
+                const ptrdiff_t i = (b * L + t) * Dm + d;
+                const double dlt = dls[t];
+                const double g = z ? silu(z[i]) : 1.0;
+                const double dy = dout[i] * g;
+                if (z && dz) {
+                    const double sg = sigmoid(z[i]);
+                    dz[i] = dout[i] * ys[t] * sg * (1.0 + z[i] * (1.0 - sg));
+                }
+                double dut = Dd * dy, ddl = 0.0;
+                for (ptrdiff_t n = 0; n < N; ++n) {
+                    const double a = exp(dlt * Ar[n]);
+                    const double hprev = hs[t * N + n], h = hs[(t + 1) * N + n];
+                    lam[n] = Cb[n * L + t] * dy + anext[n] * lam[n];
+                    dC[(b * N + n) * L + t] += dy * h;
+                    dB[(b * N + n) * L + t] += lam[n] * dlt * u[i];
+                    dut += lam[n] * dlt * Bb[n * L + t];
+                    ddl += lam[n] * (Ar[n] * a * hprev + Bb[n * L + t] * u[i]);
+                    dA[d * N + n] += lam[n] * dlt * a * hprev;
+                    anext[n] = a;
+                }
+                du[i] = dut;
+                if (dD) dD[d] += dy * u[i];
+                const double xr = delta[i] + (delta_bias ? delta_bias[d] : 0.0);
+                const double dx = softplus_flag ? ddl * sigmoid(xr) : ddl;
+                ddelta[i] = dx;
+                if (dbias) dbias[d] += dx;
+            }
+        }
+    free(hs);
+    free(dls);
+    free(ys);
+    return 0;
+}
+
 /* Depthwise causal convolution over time, per channel, width W, then the
  * optional SiLU: the local convolution that produces the scan input u in the
  * Mamba block ("d_conv: local convolution width" in the pages' usage examples).

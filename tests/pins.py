@@ -26,7 +26,11 @@ disagrees with an independent route to the same answer:
 * causal conv:   the impulse response is the reversed taps; numpy.convolve of
                  the carried state followed by the input gives every output and
                  the final state; a split sequence and a chain of decode steps
-                 reproduce the whole convolution exactly.
+                 reproduce the whole convolution exactly;
+* backward:      central finite differences of L = sum(dout * out) through the
+                 forward oracle for every input; and L = <du, u> (out is
+                 linear in u), L = <dB, B> = <dC, C> without the D skip (out
+                 is then linear in B and in C).
 
 Softplus and sigmoid are taken from numpy/scipy library routines here
 (``np.logaddexp``, ``scipy.special.expit``), never from the oracle.
@@ -365,6 +369,57 @@ def pin_conv_split_and_decode(lib):
     assert np.array_equal(state, st), "conv decode final state"
 
 
+def _loss(case, dout, lib):
+    out, _ = run_oracle(case, lib)
+    return float(np.sum(dout * out))
+
+
+def _grads(case, dout, lib):
+    return oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], case["D"], case["z"],
+                           case["delta_bias"], case["softplus"], dout, lib=lib)
+
+
+GRAD_OF = {"u": "du", "delta": "ddelta", "A": "dA", "B": "dB", "C": "dC", "D": "dD", "z": "dz",
+           "delta_bias": "ddelta_bias"}
+
+
+def pin_bwd_finite_differences(lib):
+    for seed, kw in [(201, {}), (202, dict(softplus=False)), (203, dict(with_z=False, with_d=False, with_bias=False)),
+                     (204, dict(random_a=False, N=2))]:
+        case = tiny_case(seed, bt=2, L=6, dim=2, N=kw.pop("N", 3), **kw)
+        dout = _rng(seed + 50).standard_normal(case["u"].shape)
+        g = _grads(case, dout, lib)
+        for name, gname in GRAD_OF.items():
+            if case[name] is None:
+                continue
+            base = case[name]
+            fd = np.zeros_like(base)
+            for idx in np.ndindex(base.shape):
+                eps = 1e-6 * max(1.0, abs(float(base[idx])))
+                for sgn in (1.0, -1.0):
+                    c = dict(case)
+                    c[name] = base.copy()
+                    c[name][idx] += sgn * eps
+                    fd[idx] += sgn * _loss(c, dout, lib) / (2.0 * eps)
+            scale = max(1.0, float(np.max(np.abs(fd))))
+            err = float(np.max(np.abs(g[gname] - fd)))
+            assert err <= 2e-6 * scale, f"d{name} seed {seed}: |analytic - finite difference| {err:.2e}"
+
+
+def pin_bwd_homogeneity(lib):
+    for seed in (211, 212):
+        case = tiny_case(seed, bt=2, L=9, dim=3, N=4)
+        dout = _rng(seed + 1).standard_normal(case["u"].shape)
+        lval = _loss(case, dout, lib)
+        g = _grads(case, dout, lib)
+        _close(np.array([np.sum(g["du"] * case["u"])]), np.array([lval]), what="<du, u> = L")
+        case = tiny_case(seed, bt=2, L=9, dim=3, N=4, with_d=False)
+        lval = _loss(case, dout, lib)
+        g = _grads(case, dout, lib)
+        _close(np.array([np.sum(g["dB"] * case["B"])]), np.array([lval]), what="<dB, B> = L")
+        _close(np.array([np.sum(g["dC"] * case["C"])]), np.array([lval]), what="<dC, C> = L")
+
+
 def pin_scalar_functions(lib):
     sp = lambda x: oracle.softplus(x, lib=lib)
     si = lambda x: oracle.silu(x, lib=lib)
@@ -385,4 +440,4 @@ ALL_PINS = [pin_brute_force, pin_time_invariant_convolution, pin_associative_sca
             pin_delta_to_zero, pin_memoryless_limit, pin_linear_in_u, pin_causal,
             pin_bc_scale, pin_channel_permutation, pin_decode_chain_equals_scan,
             pin_initial_state_brute_force, pin_split_equals_whole, pin_conv_impulse, pin_conv_numpy,
-            pin_conv_split_and_decode, pin_scalar_functions]
+            pin_conv_split_and_decode, pin_bwd_finite_differences, pin_bwd_homogeneity, pin_scalar_functions]

@@ -41,6 +41,11 @@ MUTATIONS = [
      "double acc = 0.0;\n            for (int k = 0; k < W; ++k)"),
     ("conv decode shifts the wrong way", "for (int k = 0; k + 1 < W - 1; ++k) st[k] = st[k + 1];",
      "for (int k = W - 2; k > 0; --k) st[k] = st[k - 1];"),
+    ("adjoint without decay", "lam[n] = Cb[n * L + t] * dy + anext[n] * lam[n];", "lam[n] = Cb[n * L + t] * dy + lam[n];"),
+    ("dA uses h_t", "dA[d * N + n] += lam[n] * dlt * a * hprev;", "dA[d * N + n] += lam[n] * dlt * a * h;"),
+    ("dDelta drops B u", "ddl += lam[n] * (Ar[n] * a * hprev + Bb[n * L + t] * u[i]);", "ddl += lam[n] * (Ar[n] * a * hprev);"),
+    ("softplus derivative sign", "ddl * sigmoid(xr)", "ddl * sigmoid(-xr)"),
+    ("dB without Delta", "dB[(b * N + n) * L + t] += lam[n] * dlt * u[i];", "dB[(b * N + n) * L + t] += lam[n] * u[i];"),
     ("initial state read transposed", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
      "h[n] = initial_state ? initial_state[(b * N + n) * Dm + d] : 0.0;"),
 ]
