@@ -202,6 +202,44 @@ SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
 
 /* Static, human-readable name of a status code (never NULL). */
 /*
+ * ssm_scan_bwd -- backward of ssm_scan_fwd (from h = 0): the gradients of a
+ * loss L with respect to every input, given dout = dL/d out, by the adjoint
+ * recurrence lambda_t = C_t dy_t + exp(Delta_{t+1} A) lambda_{t+1},
+ * dy_t = dout_t silu(z_t) (the training mode of the pages' "Efficient Scan").
+ *
+ *   inputs       as ssm_scan_fwd: u, delta, A, B, C, D, z, delta_bias, softplus_flag
+ *   dout         [batch][seqlen][dim]     dtype
+ *   du, ddelta   [batch][seqlen][dim]     dtype   (ddelta = dL/d delta_raw)
+ *   dz           [batch][seqlen][dim]     dtype   NULL = not computed (ignored without z)
+ *   dA           [dim][dstate]            f32
+ *   dB, dC       [batch][dstate][seqlen]  f32     (summed over channels)
+ *   dD           [dim]                    f32     NULL = not computed (ignored without D)
+ *   ddelta_bias  [dim]                    f32     NULL = not computed (ignored without a bias)
+ *   workspace    at least ssm_scan_bwd_workspace_bytes(...) bytes, 16-byte
+ *                aligned, owned by the caller: the state entering every chunk
+ *
+ * All gradients are overwritten (the float32 ones are zeroed on `stream` and
+ * accumulated with atomics, so their summation order, and the last bits, may
+ * vary from run to run).  Outputs must not overlap each other or any input
+ * (SSM_ERR_ALIAS); a missing or short workspace is SSM_ERR_NULL /
+ * SSM_ERR_SHAPE.
+ */
+SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                float* dD, void* dz, float* ddelta_bias, int64_t batch, int64_t dim,
+                                int64_t seqlen, int64_t dstate, int dtype, void* workspace,
+                                int64_t workspace_bytes, void* stream);
+
+/*
+ * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs:
+ * batch * dim * ceil(seqlen / K) * dstate * 4 bytes (K = 32 steps per chunk,
+ * 16 for dstate 4), at least 16; -1 for sizes or a dtype it would reject.
+ */
+SSM_API int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                             int dtype);
+
+/*
  * ssm_conv1d_fwd -- depthwise causal convolution over time (+ SiLU): the step
  * that produces the scan input u in the Mamba block (width d_conv, the
  * "local convolution width" of the pages' usage examples).  Per channel d,

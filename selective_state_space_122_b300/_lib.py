@@ -24,7 +24,7 @@ STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN"
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
            "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
            "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state", "ssm_conv1d_fwd",
-           "ssm_conv1d_update")
+           "ssm_conv1d_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_bytes")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -51,6 +51,11 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_scan_fwd_from_state.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, fp,
                                             i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_fwd_from_state.restype = ci
+    lib.ssm_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, fp, fp, fp, fp, vp, fp,
+                                 i64, i64, i64, i64, ci, vp, i64, vp]
+    lib.ssm_scan_bwd.restype = ci
+    lib.ssm_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
+    lib.ssm_scan_bwd_workspace_bytes.restype = i64
     lib.ssm_conv1d_fwd.argtypes = [vp, fp, fp, ci, fp, vp, fp, i64, i64, i64, i64, ci, vp]
     lib.ssm_conv1d_fwd.restype = ci
     lib.ssm_conv1d_update.argtypes = [fp, vp, fp, fp, ci, vp, i64, i64, i64, ci, vp]
@@ -178,6 +183,39 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                 _ptr(workspace, None, dev), ws_bytes, _stream(dev))
             _check("ssm_scan_fwd_from_state", code)
     return out, last_state
+
+
+def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
+                 D: Optional[torch.Tensor], z: Optional[torch.Tensor], delta_bias: Optional[torch.Tensor],
+                 softplus: bool, dout: torch.Tensor, workspace: Optional[torch.Tensor] = None) -> dict:
+    """Gradients of the scan (from h = 0) given dout; see ssm_scan.h.  Returns a
+    dict du, ddelta, dz (activation dtype; dz None without z), dA, dB, dC, dD,
+    ddelta_bias (float32; None without D / bias)."""
+    lib = load_library()
+    dt, dev = u.dtype, u.device
+    bt, L, dim = u.shape
+    N = A.shape[1]
+    f32 = dict(dtype=torch.float32, device=dev)
+    g = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u), dz=None if z is None else torch.empty_like(u),
+             dA=torch.empty(dim, N, **f32), dB=torch.empty(bt, N, L, **f32), dC=torch.empty(bt, N, L, **f32),
+             dD=None if D is None else torch.empty(dim, **f32),
+             ddelta_bias=None if delta_bias is None else torch.empty(dim, **f32))
+    if workspace is None:
+        nbytes = int(lib.ssm_scan_bwd_workspace_bytes(bt, dim, L, N, _dtype_code(u)))
+        if nbytes < 0:
+            raise ValueError("ssm_scan_bwd: sizes or dtype rejected")
+        workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
+    ws_bytes = workspace.numel() * workspace.element_size()
+    with torch.cuda.device(dev):
+        code = lib.ssm_scan_bwd(
+            _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
+            _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
+            int(bool(softplus)), _ptr(dout, dt, dev), _ptr(g["du"], dt, dev), _ptr(g["ddelta"], dt, dev),
+            _ptr(g["dA"], torch.float32, dev), _ptr(g["dB"], torch.float32, dev), _ptr(g["dC"], torch.float32, dev),
+            _ptr(g["dD"], torch.float32, dev), _ptr(g["dz"], dt, dev), _ptr(g["ddelta_bias"], torch.float32, dev),
+            bt, dim, L, N, _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+    _check("ssm_scan_bwd", code)
+    return g
 
 
 def conv1d_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tensor] = None,

@@ -287,6 +287,56 @@ ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weig
                                                    static_cast<cudaStream_t>(stream)));
 }
 
+int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || dim > (int64_t(1) << 31) ||
+        seqlen > (int64_t(1) << 40))
+        return -1;
+    return std::max<int64_t>(16, ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate));
+}
+
+ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                        const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD,
+                        void* dz, float* ddelta_bias, int64_t batch, int64_t dim, int64_t seqlen,
+                        int64_t dstate, int dtype, void* workspace, int64_t workspace_bytes, void* stream) {
+    if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
+    if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC || !workspace)
+        return SSM_ERR_NULL;
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
+    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    if (workspace_bytes < ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate)) return SSM_ERR_SHAPE;
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
+    const uintptr_t ea = (uintptr_t)es;
+    if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) || !aligned(dout, ea) ||
+        (z && !aligned(z, ea)) || !aligned(du, ea) || !aligned(ddelta, ea) || (dz && !aligned(dz, ea)) ||
+        !aligned(A, 4) || (D && !aligned(D, 4)) || (delta_bias && !aligned(delta_bias, 4)) || !aligned(dA, 4) ||
+        !aligned(dB, 4) || !aligned(dC, 4) || (dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4)) ||
+        !aligned(workspace, 16))
+        return SSM_ERR_ALIGN;
+    const int64_t x_bytes = batch * seqlen * dim * es, bc_bytes = batch * dstate * seqlen * es;
+    const Span ins[] = {{u, x_bytes}, {delta, x_bytes}, {z, x_bytes}, {dout, x_bytes}, {B, bc_bytes},
+                        {C, bc_bytes}, {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4}};
+    const Span outs[] = {{du, x_bytes}, {ddelta, x_bytes}, {dz, x_bytes}, {dA, dim * dstate * 4},
+                         {dB, batch * dstate * seqlen * 4}, {dC, batch * dstate * seqlen * 4}, {dD, dim * 4},
+                         {ddelta_bias, dim * 4}, {workspace, workspace_bytes}};
+    for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
+        for (const Span& s : ins)
+            if (overlap(outs[i], s)) return SSM_ERR_ALIAS;
+        for (size_t j = i + 1; j < sizeof(outs) / sizeof(outs[0]); ++j)
+            if (overlap(outs[i], outs[j])) return SSM_ERR_ALIAS;
+    }
+    int sms = 0;
+    if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
+    ssm::BwdArgs a{u, delta, A, B, C, D, z, delta_bias, softplus_flag ? 1 : 0, dout, du, ddelta, dA, dB, dC,
+                   D ? dD : nullptr, z ? dz : nullptr, delta_bias ? ddelta_bias : nullptr, batch, dim, seqlen,
+                   (int)dstate};
+    return launch_status(ssm::launch_scan_bwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32, workspace,
+                                              static_cast<cudaStream_t>(stream)));
+}
+
 ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
                             const void* B, const void* C, const float* D, const void* z,
                             const float* dt_bias, void* out, int64_t batch, int64_t dim,

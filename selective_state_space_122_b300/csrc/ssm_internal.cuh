@@ -88,6 +88,34 @@ struct ConvArgs {
 cudaError_t launch_conv1d_fwd(const ConvArgs& a, DType dt, cudaStream_t s);
 cudaError_t launch_conv1d_update(const ConvArgs& a, DType dt, cudaStream_t s);
 
+// Backward of the scan (scan_bwd.cu); layouts as in ssm_scan.h.  dD, dz and
+// dbias may be null (not computed).  Workspace: the state entering every
+// chunk (bwd_workspace_bytes).
+struct BwdArgs {
+    const void* u;
+    const void* delta;
+    const float* A;
+    const void* B;
+    const void* C;
+    const float* D;
+    const void* z;
+    const float* delta_bias;
+    int softplus;
+    const void* dout;
+    void* du;
+    void* ddelta;
+    float* dA;
+    float* dB;
+    float* dC;
+    float* dD;
+    void* dz;
+    float* dbias;
+    int64_t batch, dim, seqlen;
+    int dstate;
+};
+int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
+cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, cudaStream_t s);
+
 // Tensor-memory scan (scan_tmem.cu): bf16 activations, 16 states.  Workspace:
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
 bool tmem_supported(const ScanArgs& a, DType dt);

@@ -4,6 +4,7 @@
            [--N N] [--iters K] [--path tmem|seg|relay|generic]
     python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K]
     python -m selective_state_space_122_b300.profile conv [--batch B] [--dim D] [--L L] [--W W] [--iters K]
+    python -m selective_state_space_122_b300.profile bwd [--batch B] [--dim D] [--L L] [--N N] [--iters K]
     python -m selective_state_space_122_b300.profile units
 
 ``scan`` runs ssm_scan_fwd on seeded on-device bf16 inputs shaped like the
@@ -91,6 +92,25 @@ def cmd_decode(a):
     return 0
 
 
+def cmd_bwd(a):
+    from ._lib import ssm_scan_bwd
+    dev = torch.device("cuda", 0)
+    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev)
+    dout = torch.randn_like(u, dtype=torch.float32).bfloat16()
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    elems = a.batch * a.dim * a.L * a.N
+    ws = None
+    for i in range(a.iters):
+        e0.record()
+        ssm_scan_bwd(u, dl, A, B, C, D, z, bias, True, dout, workspace=ws)
+        e1.record()
+        torch.cuda.synchronize()
+        ms = e0.elapsed_time(e1)
+        print(f"bwd {a.batch}x{a.dim}x{a.L} N{a.N} iter {i}: {ms:.3f} ms "
+              f"({elems / (ms * 1e-3) / 1e9:.1f} G elements/s)", flush=True)
+    return 0
+
+
 def cmd_conv(a):
     from ._lib import conv1d_fwd
     dev = torch.device("cuda", 0)
@@ -146,6 +166,12 @@ def main(argv=None):
     d.add_argument("--dim", type=int, default=5120)
     d.add_argument("--N", type=int, default=16)
     d.add_argument("--iters", type=int, default=5)
+    bw = sub.add_parser("bwd")
+    bw.add_argument("--batch", type=int, default=8)
+    bw.add_argument("--dim", type=int, default=2048)
+    bw.add_argument("--L", type=int, default=2048)
+    bw.add_argument("--N", type=int, default=16)
+    bw.add_argument("--iters", type=int, default=3)
     cv = sub.add_parser("conv")
     cv.add_argument("--batch", type=int, default=1)
     cv.add_argument("--dim", type=int, default=5120)
@@ -155,7 +181,7 @@ def main(argv=None):
     u = sub.add_parser("units")
     u.add_argument("--clock-mhz", type=float, default=2032.0)
     a = ap.parse_args(argv)
-    return {"scan": cmd_scan, "decode": cmd_decode, "conv": cmd_conv, "units": cmd_units}[a.cmd](a)
+    return {"scan": cmd_scan, "decode": cmd_decode, "conv": cmd_conv, "bwd": cmd_bwd, "units": cmd_units}[a.cmd](a)
 
 
 if __name__ == "__main__":

@@ -143,6 +143,25 @@ def test_conv1d_update_rejects_bad_arguments(lib, kw, code):
                                  a["dim"], a["width"], a["dtype"], a["stream"]) == code
 
 
+@pytest.mark.parametrize("kw,code", [
+    (dict(ws=None), 1), (dict(du=None), 1), (dict(dstate=3), 4), (dict(seqlen=0), 2), (dict(dtype=7), 5),
+    (dict(ws_bytes=16), 2), (dict(du=P), 6), (dict(dA=P + 128 * MB + 4), 6), (dict(ws=P + 1088 * MB + 8), 3),
+])
+def test_scan_bwd_rejects_bad_arguments(lib, kw, code):
+    """Host checks of ssm_scan_bwd (fake addresses; every case is rejected before
+    anything is enqueued)."""
+    a = dict(u=P, delta=P + 64 * MB, A=P + 128 * MB, B=P + 192 * MB, C=P + 256 * MB, D=P + 320 * MB,
+             z=P + 384 * MB, bias=P + 448 * MB, dout=P + 512 * MB, du=P + 576 * MB, dd=P + 640 * MB,
+             dA=P + 704 * MB, dB=P + 768 * MB, dC=P + 832 * MB, dD=P + 896 * MB, dz=P + 960 * MB,
+             db=P + 1024 * MB, ws=P + 1088 * MB, ws_bytes=64 * MB, batch=2, dim=64, seqlen=128, dstate=16,
+             dtype=1)
+    a.update(kw)
+    assert lib.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], 1, a["dout"],
+                            a["du"], a["dd"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["db"], a["batch"],
+                            a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
+    assert lib.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16, 1) == 2 * 64 * 8 * 16 * 4
+
+
 def upd_args(**kw):
     a = dict(state=P, x=P + 64 * MB, dt=P + 128 * MB, A=P + 192 * MB, B=P + 256 * MB, C=P + 320 * MB,
              D=P + 384 * MB, z=P + 448 * MB, dt_bias=P + 512 * MB, out=P + 576 * MB,

@@ -1,0 +1,61 @@
+"""The scan's backward (ssm_scan_bwd) against the float64 adjoint oracle."""
+from __future__ import annotations
+
+import dataclasses
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from gpu_util import dev, host_f64
+from selective_state_space_122_b300 import inputs, ssm_scan_bwd
+
+pytestmark = pytest.mark.gpu
+
+
+def _close(got, ref, rel, what, rounded=False):
+    """|got - ref| <= rel * max(rms(ref), max|ref| / 50) elementwise (gradients
+    that sum many terms are compared on the scale of the whole tensor), plus
+    the half-ulp 2^-8 |ref| of a bf16 output when ``rounded``."""
+    got = np.asarray(got, dtype=np.float64)
+    scale = max(float(np.sqrt(np.mean(ref ** 2))), float(np.max(np.abs(ref))) / 50.0, 1e-30)
+    bound = rel * scale + (2.0 ** -8 * np.abs(ref) if rounded else 0.0)
+    excess = np.abs(got - ref) - bound
+    assert float(np.max(excess)) <= 0.0, (f"{what}: max|err| {float(np.max(np.abs(got - ref))):.3e}, "
+                                          f"bound {rel:.0e} x {scale:.3e}")
+
+
+@pytest.mark.parametrize("bt,dim,L,N,dtype,kw", [
+    (2, 24, 77, 16, inputs.F32, {}),
+    (1, 40, 100, 8, inputs.F32, dict(softplus=False)),
+    (2, 70, 65, 4, inputs.F32, dict(with_z=False, with_d=False, with_bias=False)),
+    (2, 64, 300, 16, inputs.BF16, {}),
+    (3, 48, 129, 8, inputs.BF16, dict(random_a=True)),
+    (1, 16, 1, 16, inputs.F32, {}),
+    (2, 256, 2048, 16, inputs.BF16, {}),
+])
+def test_scan_bwd_matches_adjoint_oracle(bt, dim, L, N, dtype, kw):
+    inp = inputs.make_scan_inputs(inputs.ScanShape("bwd", bt, dim, L, N, dtype), 1200 + dim + L, **kw)
+    if not inp.softplus:
+        # without softplus the raw timestep is used as is: keep it positive and
+        # small so the recurrence stays bounded (float32 cases only)
+        assert dtype == inputs.F32
+        inp = dataclasses.replace(inp, delta=(np.abs(inp.delta) * 0.05).astype(np.float32), delta_bias=None)
+    r = np.random.Generator(np.random.PCG64(1300 + L))
+    dout = inputs._activation(r, (bt, L, dim), dtype)
+    f = inp.as_f64()
+    dout_f = inputs.bf16_bits_to_f64(dout) if dtype == inputs.BF16 else dout.astype(np.float64)
+    ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"], f["delta_bias"],
+                          f["softplus"], dout_f)
+    g = ssm_scan_bwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D), dev(inp.z),
+                     dev(inp.delta_bias), inp.softplus, dev(dout))
+    torch.cuda.synchronize()
+    # float32 math throughout; bf16 outputs (du, ddelta, dz) carry their own rounding
+    bf = dtype == inputs.BF16
+    for k in ("du", "ddelta", "dz"):
+        if ref[k] is not None:
+            _close(host_f64(g[k]), ref[k], 1e-4, k, rounded=bf)
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        if ref[k] is not None:
+            _close(host_f64(g[k]), ref[k], 1e-4, k)
