@@ -116,7 +116,8 @@ __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<floa
 template <typename CF, typename T, bool kFast>
 struct ScanKernel {
     using PT = typename Pair<T>::type;
-    static constexpr int N = CF::N, G = CF::G, R = CF::R, CW = CF::CW, K = CF::K, S = CF::S;
+    static constexpr int N = CF::N, G = CF::G, R = CF::R, CW = CF::CW, K = CF::K;
+    [[maybe_unused]] static constexpr int S = CF::S;
     static constexpr int TC = CF::TC, V = CF::V, TCD = CF::TCD, TCB = CF::TCB, KR = CF::KR;
     static constexpr int THREADS = CF::THREADS;
 
