@@ -93,7 +93,7 @@ __device__ __forceinline__ void st_vec(T* p, const Vec<T, V>& v) {
 
 // One thread: channels c0 .. c0+V-1 of batch row b, steps t0 .. t0+TT-1.
 template <typename T, int V, int W, bool kSilu, bool kFast>
-__global__ void __launch_bounds__(kConvThreads, 3)
+__global__ void __launch_bounds__(kConvThreads)
 conv1d_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const float* __restrict__ bias,
                   const float* __restrict__ state_in, T* __restrict__ out, int64_t L, int64_t dim, int64_t nvec,
                   int64_t ntile) {
@@ -130,35 +130,63 @@ conv1d_fwd_kernel(const T* __restrict__ x, const float* __restrict__ w, const fl
     }
     const T* xp = x + (b * L + t0) * dim + c0;
     T* op = out + (b * L + t0) * dim + c0;
-    // kBatch steps' loads are issued together, then their outputs computed and
-    // stored: 64-128 bytes in flight per thread, within a register budget that
-    // keeps 3 CTAs per SM resident (the kernel is bound by bytes in flight)
-    constexpr int kBatch = V == 8 ? 4 : 8;
-    for (int64_t tb = t0; tb < t1; tb += kBatch, xp += kBatch * dim, op += kBatch * dim) {
-        const int n = (int)min((int64_t)kBatch, t1 - tb);
-        Vec<T, V> xv[kBatch];
+    auto step = [&](const Vec<T, V>& xv, T* o) {
+        Vec<T, V> ov;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u)
-            if (u < n) xv[u] = ld_vec<T, V>(xp + u * dim);
+        for (int i = 0; i < V; ++i) {
+            const float xc = to_f(xv.e[i]);
+            float acc = br[i];
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-            if (u >= n) break;
-            Vec<T, V> ov;
+            for (int k = 0; k < W - 1; ++k) acc = fmaf(wr[i][k], win[k][i], acc);
+            acc = fmaf(wr[i][W - 1], xc, acc);
+            if constexpr (kSilu) acc = conv_silu<kFast>(acc);
+            ov.e[i] = from_f<T>(acc);
 #pragma unroll
-            for (int i = 0; i < V; ++i) {
-                const float xc = to_f(xv[u].e[i]);
-                float acc = br[i];
-#pragma unroll
-                for (int k = 0; k < W - 1; ++k) acc = fmaf(wr[i][k], win[k][i], acc);
-                acc = fmaf(wr[i][W - 1], xc, acc);
-                if constexpr (kSilu) acc = conv_silu<kFast>(acc);
-                ov.e[i] = from_f<T>(acc);
-#pragma unroll
-                for (int k = 0; k + 1 < W - 1; ++k) win[k][i] = win[k + 1][i];
-                if constexpr (W > 1) win[W - 2][i] = xc;
-            }
-            st_vec<T, V>(op + u * dim, ov);
+            for (int k = 0; k + 1 < W - 1; ++k) win[k][i] = win[k + 1][i];
+            if constexpr (W > 1) win[W - 2][i] = xc;
         }
+        st_vec<T, V>(o, ov);
+    };
+    if constexpr (V * sizeof(T) == 16) {
+        // 16-byte rows: each thread streams its column through a private ring of
+        // kRing steps in shared memory, filled by asynchronous copies kGroup
+        // steps at a time, so kRing * 16 bytes per thread are in flight without
+        // holding registers (the kernel is bound by bytes in flight).
+        constexpr int kGroup = 4, kRing = 16, kGroups = kRing / kGroup;
+        __shared__ __align__(16) unsigned char ring[kRing][kConvThreads][16];
+        const int nst = (int)(t1 - t0);
+        auto issue = [&](int g) {
+            if (g * kGroup < nst) {
+#pragma unroll
+                for (int u = 0; u < kGroup; ++u) {
+                    const int s = g * kGroup + u;
+                    if (s < nst) {
+                        const uint32_t dst = (uint32_t)__cvta_generic_to_shared(&ring[s % kRing][threadIdx.x][0]);
+                        asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(xp + (int64_t)s * dim)
+                                     : "memory");
+                    }
+                }
+            }
+            asm volatile("cp.async.commit_group;" ::: "memory");
+        };
+#pragma unroll
+        for (int g = 0; g < kGroups; ++g) issue(g);
+        for (int g = 0; g * kGroup < nst; ++g) {
+            asm volatile("cp.async.wait_group %0;" ::"n"(kGroups - 1) : "memory");
+#pragma unroll
+            for (int u = 0; u < kGroup; ++u) {
+                const int s = g * kGroup + u;
+                if (s < nst) {
+                    Vec<T, V> xv;
+                    memcpy(&xv, &ring[s % kRing][threadIdx.x][0], 16);
+                    step(xv, op + (int64_t)s * dim);
+                }
+            }
+            issue(g + kGroups);   // into the slots just read
+        }
+        asm volatile("cp.async.wait_group 0;" ::: "memory");
+    } else {
+        for (int64_t t = t0; t < t1; ++t, xp += dim, op += dim) step(ld_vec<T, V>(xp), op);
     }
 }
 
