@@ -54,7 +54,7 @@ def scan_elements(s=SCAN):
 
 # Measured DRAM bytes of one full-size launch of the scan kernel (see the
 # "traffic" entry of the roofline object).
-SCAN_TRAFFIC_BYTES = 654.4e6 * 8
+SCAN_TRAFFIC_BYTES = 654.86e6 * 8
 
 
 def scan_bytes(s=SCAN, es=2):
@@ -417,7 +417,7 @@ def bench_ours(args):
             "peak": units["ex2"] / 1e9,
             "frac": sfu_ach / units["ex2"],
             # dram__bytes_read.sum + dram__bytes_write.sum of scan_tmem2_kernel from one
-            # ncu capture of the same workload cut to L = 16384 (654.4 MB), scaled by
+            # ncu capture of the same workload cut to L = 16384 (654.86 MB), scaled by
             # 131072 / 16384 (traffic grows in proportion to L)
             "traffic": SCAN_TRAFFIC_BYTES,
             "traffic_source": "ncu, scan_tmem2_kernel at L=16384 x 8",
