@@ -233,8 +233,8 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
 
 /*
  * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs:
- * batch * dim * ceil(seqlen / K) * dstate * 4 bytes (K = 32 steps per chunk,
- * 16 for dstate 4), at least 16; -1 for sizes or a dtype it would reject.
+ * batch * dim * ceil(seqlen / 8) * dstate * 4 bytes (the state entering
+ * every 8-step chunk), at least 16; -1 for sizes or a dtype it would reject.
  */
 SSM_API int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                              int dtype);

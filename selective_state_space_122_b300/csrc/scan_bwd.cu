@@ -15,17 +15,18 @@
 //     dD = sum dy_t u_t,   dz_t = dout_t y_t silu'(z_t),
 //     ddelta_raw_t = dDelta_t softplus'(x_t),   dbias = sum ddelta_raw_t.
 //
-// Work decomposition: a CTA owns CC channels of one batch row (one lane per
-// (channel, state): N lanes per channel, 8 warps) and the whole sequence.
+// Work decomposition: a CTA owns CC channels of one batch row (four states
+// per lane: N/4 lanes per channel, 4 warps) and the whole sequence.
 //   pass 1: the forward recurrence, storing the state entering every K-step
 //           chunk in the workspace;
 //   pass 2: the chunks in reverse order: per chunk, stage u, delta_raw, z,
 //           dout and B, C in shared memory, evaluate the per-(t, d) terms once,
 //           recompute the chunk's states from its checkpoint into registers,
-//           then run the adjoint backwards over the chunk; sums over a
-//           channel's states are warp shuffles; sums over the CTA's channels
-//           (dB, dC) are warp shuffles into per-warp shared-memory partials,
-//           added up and flushed to global memory once per chunk.
+//           with their decays, then run the adjoint backwards over the chunk;
+//           sums over a channel's states are in-lane sums plus warp shuffles
+//           over its N/4 lanes; each lane's dB and dC terms go to its own
+//           shared-memory slots, summed over the CTA's channels with 16-byte
+//           loads and added to global memory once per chunk.
 // dA, dB, dC, dD and dbias accumulate with atomics across CTAs and batch rows
 // (the launcher zeroes them first).
 #include <cuda_bf16.h>
@@ -40,11 +41,32 @@ namespace ssm {
 
 namespace {
 
-constexpr int kBwdThreads = 256;   // 8 warps
+constexpr int kBwdThreads = 128;   // 4 warps
 
-// steps per chunk (the staged tiles and the per-warp dB/dC partials fit the
-// 48 KB of static shared memory for every state count)
-__host__ __device__ constexpr int bwd_chunk(int) { return 16; }
+// Layout of one CTA: four states per lane (G), R = N / 4 lanes per channel,
+// 32 / R channels per warp, four warps; K steps per chunk.
+template <int N>
+struct BwdCfg {
+    static constexpr int G = 4;
+    static constexpr int R = N / G;
+    static constexpr int CPW = 32 / R;
+    static constexpr int CC = CPW * (kBwdThreads / 32);   // channels per CTA
+    static constexpr int K = 8;
+    // dynamic shared memory, float offsets
+    static constexpr int T_CH = K * CC;                    // one per-(t, d) array
+    static constexpr int O_U = 0, O_DL = T_CH, O_DY = 2 * T_CH, O_Y = 3 * T_CH, O_DU = 4 * T_CH, O_DD = 5 * T_CH;
+    static constexpr int O_X = 6 * T_CH, O_Z = 7 * T_CH, O_DO = 8 * T_CH;
+    static constexpr int O_B = 9 * T_CH, O_C = O_B + N * K;
+    static constexpr int O_P = O_C + N * K;                // [K][lanes of the CTA][8]: dC (4), dB (4)
+    static constexpr int O_DD_CH = O_P + K * kBwdThreads * 8;
+    static constexpr int O_DB_CH = O_DD_CH + CC;
+    static constexpr int FLOATS = O_DB_CH + CC;
+    static constexpr int SMEM = FLOATS * 4;
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+};
+
+// steps per chunk (the workspace holds the state entering every chunk)
+__host__ __device__ constexpr int bwd_chunk(int) { return 8; }
 
 template <typename T>
 __device__ __forceinline__ float bw_ld(const T* p, int64_t i) {
@@ -60,25 +82,48 @@ __device__ __forceinline__ void bw_st(T* p, int64_t i, float v) {
 __device__ __forceinline__ float bw_sigmoid(float v) { return 1.f / (1.f + expf(-v)); }
 __device__ __forceinline__ float bw_softplus(float v) { return fmaxf(v, 0.f) + log1pf(expf(-fabsf(v))); }
 
-// sum over the N lanes of one channel (lanes n = 0 .. N-1 of a group)
-template <int N>
-__device__ __forceinline__ float group_sum(float v) {
+// exp(x): the SFU exp2 for bf16 activations (relative error ~2^-22, far below
+// the bf16 output rounding), the accurate library exp for float32.
+template <bool kFast>
+__device__ __forceinline__ float bw_exp(float x) {
+    if constexpr (kFast) {
+        float y;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x * 1.4426950408889634f));
+        return y;
+    } else {
+        return expf(x);
+    }
+}
+
+// sum over the R lanes of one channel
+template <int R>
+__device__ __forceinline__ float chan_sum(float v) {
 #pragma unroll
-    for (int o = N / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+    for (int o = R / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
     return v;
 }
 
 template <typename T, int N>
-__global__ void __launch_bounds__(kBwdThreads, 2)
+__global__ void __launch_bounds__(kBwdThreads)
 scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
-    constexpr int K = bwd_chunk(N);
-    constexpr int CPW = 32 / N;                  // channels per warp
-    constexpr int CC = CPW * (kBwdThreads / 32); // channels per CTA
-    __shared__ float s_u[K][CC], s_dl[K][CC], s_dy[K][CC], s_y[K][CC], s_du[K][CC], s_dd[K][CC];
-    __shared__ float s_x[K][CC], s_z[K][CC], s_do[K][CC];
-    __shared__ float s_B[N][K], s_C[N][K];
-    __shared__ float s_pB[kBwdThreads / 32][N][K], s_pC[kBwdThreads / 32][N][K];   // per-warp partials
-    __shared__ float s_dD[CC], s_db[CC];
+    using CF = BwdCfg<N>;
+    constexpr int K = CF::K, R = CF::R, CPW = CF::CPW, CC = CF::CC, G = CF::G;
+    constexpr bool kFast = !std::is_same<T, float>::value;
+    extern __shared__ __align__(16) float sm[];
+    float* s_u = sm + CF::O_U;
+    float* s_dl = sm + CF::O_DL;
+    float* s_dy = sm + CF::O_DY;
+    float* s_y = sm + CF::O_Y;
+    float* s_du = sm + CF::O_DU;
+    float* s_dd = sm + CF::O_DD;
+    float* s_x = sm + CF::O_X;
+    float* s_z = sm + CF::O_Z;
+    float* s_do = sm + CF::O_DO;
+    float* s_B = sm + CF::O_B;      // [N][K]
+    float* s_C = sm + CF::O_C;
+    float* s_P = sm + CF::O_P;      // [K][kBwdThreads][8]
+    float* s_dDc = sm + CF::O_DD_CH;
+    float* s_dbc = sm + CF::O_DB_CH;
 
     const T* u = static_cast<const T*>(p.u);
     const T* dr = static_cast<const T*>(p.delta);
@@ -87,100 +132,158 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
     const T* zg = static_cast<const T*>(p.z);
     const T* dout = static_cast<const T*>(p.dout);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int n = lane % N;
-    const int cl = warp * CPW + lane / N;        // channel within the CTA
+    const int g = lane % R;                       // states 4g .. 4g+3
+    const int cl = warp * CPW + lane / R;         // channel within the CTA
     const int64_t b = blockIdx.y;
     const int64_t d0 = (int64_t)blockIdx.x * CC;
     const int64_t d = d0 + cl;
     const bool ch_ok = d < p.dim;
     const int64_t L = p.seqlen, dim = p.dim;
     const int64_t nch = (L + K - 1) / K;
-    const float An = ch_ok ? p.A[d * N + n] : 0.f;
+    float An[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) An[j] = ch_ok ? p.A[d * N + G * g + j] : 0.f;
     const float Dd = (p.D && ch_ok) ? p.D[d] : 0.f;
 
-    for (int i = tid; i < CC; i += kBwdThreads) s_dD[i] = s_db[i] = 0.f;
+    for (int i = tid; i < CC; i += kBwdThreads) s_dDc[i] = s_dbc[i] = 0.f;
 
-    // per-(t, d) loads and terms of chunk c into shared memory
-    auto stage = [&](int64_t c, bool backward) {
+    // A chunk's inputs are fetched into registers one chunk ahead (their
+    // global-memory latency overlaps the previous chunk's work), then turned
+    // into the per-(t, d) terms in shared memory.
+    constexpr int IT = (K * CC + kBwdThreads - 1) / kBwdThreads;   // (t, d) items per thread
+    constexpr int BT = (N * K + kBwdThreads - 1) / kBwdThreads;    // (n, t) items per thread
+    struct Pre {
+        float u[IT], xr[IT], z[IT], dov[IT], Bv[BT], Cv[BT];
+        bool ok[IT];
+    };
+    auto fetch = [&](int64_t c, bool backward, Pre& r) {
         const int64_t t0 = c * K;
-        for (int i = tid; i < K * CC; i += kBwdThreads) {
+#pragma unroll
+        for (int q = 0; q < IT; ++q) {
+            const int i = tid + q * kBwdThreads;
             const int k = i / CC, cc = i % CC;
             const int64_t t = t0 + k, dd = d0 + cc;
-            const bool ok = t < L && dd < dim;
+            const bool ok = i < K * CC && t < L && dd < dim;
             const int64_t gi = (b * L + t) * dim + dd;
-            const float xr = ok ? bw_ld(dr, gi) + (p.delta_bias ? p.delta_bias[dd] : 0.f) : 0.f;
-            const float dl = ok ? (p.softplus ? bw_softplus(xr) : xr) : 0.f;
-            s_u[k][cc] = ok ? bw_ld(u, gi) : 0.f;
-            s_dl[k][cc] = dl;
-            if (backward) {
-                const float zv = (ok && zg) ? bw_ld(zg, gi) : 0.f;
-                const float dov = ok ? bw_ld(dout, gi) : 0.f;
-                s_x[k][cc] = xr;
-                s_z[k][cc] = zv;
-                s_do[k][cc] = dov;
-                s_dy[k][cc] = zg ? dov * zv * bw_sigmoid(zv) : dov;
-            }
+            r.ok[q] = ok;
+            r.xr[q] = ok ? bw_ld(dr, gi) + (p.delta_bias ? p.delta_bias[dd] : 0.f) : 0.f;
+            r.u[q] = ok ? bw_ld(u, gi) : 0.f;
+            r.z[q] = (backward && ok && zg) ? bw_ld(zg, gi) : 0.f;
+            r.dov[q] = (backward && ok) ? bw_ld(dout, gi) : 0.f;
         }
-        for (int i = tid; i < N * K; i += kBwdThreads) {
+#pragma unroll
+        for (int q = 0; q < BT; ++q) {
+            const int i = tid + q * kBwdThreads;
             const int nn = i / K, k = i % K;
             const int64_t t = t0 + k;
-            const bool ok = t < L;
-            s_B[nn][k] = ok ? bw_ld(Bg, (b * N + nn) * L + t) : 0.f;
-            if (backward) s_C[nn][k] = ok ? bw_ld(Cg, (b * N + nn) * L + t) : 0.f;
+            const bool ok = i < N * K && t < L;
+            r.Bv[q] = ok ? bw_ld(Bg, (b * N + nn) * L + t) : 0.f;
+            r.Cv[q] = (backward && ok) ? bw_ld(Cg, (b * N + nn) * L + t) : 0.f;
+        }
+    };
+    auto commit = [&](const Pre& r, bool backward) {
+#pragma unroll
+        for (int q = 0; q < IT; ++q) {
+            const int i = tid + q * kBwdThreads;
+            if (i >= K * CC) continue;
+            const float xr = r.xr[q];
+            s_u[i] = r.u[q];
+            s_dl[i] = r.ok[q] ? (p.softplus ? bw_softplus(xr) : xr) : 0.f;
+            if (backward) {
+                s_x[i] = xr;
+                s_z[i] = r.z[q];
+                s_do[i] = r.dov[q];
+                s_dy[i] = zg ? r.dov[q] * r.z[q] * bw_sigmoid(r.z[q]) : r.dov[q];
+            }
+        }
+#pragma unroll
+        for (int q = 0; q < BT; ++q) {
+            const int i = tid + q * kBwdThreads;
+            if (i >= N * K) continue;
+            s_B[i] = r.Bv[q];
+            if (backward) s_C[i] = r.Cv[q];
         }
         __syncthreads();
     };
 
     // ---- pass 1: forward, checkpoint the state entering each chunk
-    float h = 0.f;
+    float h[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) h[j] = 0.f;
+    Pre pre;
+    fetch(0, false, pre);
     for (int64_t c = 0; c < nch; ++c) {
-        stage(c, false);
-        if (ch_ok) ckpt[((b * dim + d) * nch + c) * N + n] = h;
-#pragma unroll 8
-        for (int k = 0; k < K; ++k) h = expf(s_dl[k][cl] * An) * h + s_dl[k][cl] * s_B[n][k] * s_u[k][cl];
+        commit(pre, false);
+        if (c + 1 < nch) fetch(c + 1, false, pre);
+        if (ch_ok)
+            *reinterpret_cast<float4*>(ckpt + ((b * dim + d) * nch + c) * N + G * g) = make_float4(h[0], h[1], h[2], h[3]);
+#pragma unroll
+        for (int k = 0; k < K; ++k) {
+            const float dl = s_dl[k * CC + cl], du = dl * s_u[k * CC + cl];
+#pragma unroll
+            for (int j = 0; j < G; ++j) h[j] = bw_exp<kFast>(dl * An[j]) * h[j] + du * s_B[(G * g + j) * K + k];
+        }
         __syncthreads();
     }
 
     // ---- pass 2: chunks in reverse
-    float lam = 0.f, anext = 0.f, dA_acc = 0.f;
+    float lam[G], anext[G], dA_acc[G];
+#pragma unroll
+    for (int j = 0; j < G; ++j) lam[j] = anext[j] = dA_acc[j] = 0.f;
+    fetch(nch - 1, true, pre);
     for (int64_t c = nch - 1; c >= 0; --c) {
-        stage(c, true);
+        commit(pre, true);
+        if (c > 0) fetch(c - 1, true, pre);
         const int64_t t0 = c * K;
-        const float h_in = ch_ok ? ckpt[((b * dim + d) * nch + c) * N + n] : 0.f;
-        float hk[K];
-        float hc = h_in;
+        float hin[G];
+        {
+            const float4 v = ch_ok ? *reinterpret_cast<const float4*>(ckpt + ((b * dim + d) * nch + c) * N + G * g)
+                                   : make_float4(0.f, 0.f, 0.f, 0.f);
+            hin[0] = v.x; hin[1] = v.y; hin[2] = v.z; hin[3] = v.w;
+        }
+        // recompute the chunk's states and decays; y_t for dz
+        float hk[K][G], ak[K][G];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            hc = expf(s_dl[k][cl] * An) * hc + s_dl[k][cl] * s_B[n][k] * s_u[k][cl];
-            hk[k] = hc;
-            const float yp = group_sum<N>(s_C[n][k] * hc);
-            if (n == 0) s_y[k][cl] = yp + Dd * s_u[k][cl];
+            const float dl = s_dl[k * CC + cl], du = dl * s_u[k * CC + cl];
+            float yp = 0.f;
+#pragma unroll
+            for (int j = 0; j < G; ++j) {
+                const float a = bw_exp<kFast>(dl * An[j]);
+                const float hp = k > 0 ? hk[k - 1][j] : hin[j];
+                ak[k][j] = a;
+                hk[k][j] = a * hp + du * s_B[(G * g + j) * K + k];
+                yp = fmaf(s_C[(G * g + j) * K + k], hk[k][j], yp);
+            }
+            yp = chan_sum<R>(yp);
+            if (g == 0) s_y[k * CC + cl] = yp + Dd * s_u[k * CC + cl];
         }
+        // the adjoint, backwards over the chunk
 #pragma unroll
         for (int k = K - 1; k >= 0; --k) {
-            const float dl = s_dl[k][cl], uu = s_u[k][cl], dy = s_dy[k][cl];
-            const float a = expf(dl * An);
-            const float hprev = k > 0 ? hk[k - 1] : h_in;
-            lam = s_C[n][k] * dy + anext * lam;
-            // dC, dB terms summed over the warp's channels (lanes n, n+N, ...)
-            float pc = dy * hk[k], pb = lam * dl * uu;
+            const float dl = s_dl[k * CC + cl], uu = s_u[k * CC + cl], dy = s_dy[k * CC + cl];
+            float pc[G], pb[G], dup = 0.f, ddp = 0.f;
 #pragma unroll
-            for (int o = N; o < 32; o <<= 1) {
-                pc += __shfl_xor_sync(0xffffffffu, pc, o);
-                pb += __shfl_xor_sync(0xffffffffu, pb, o);
+            for (int j = 0; j < G; ++j) {
+                const float Bv = s_B[(G * g + j) * K + k];
+                const float hp = k > 0 ? hk[k - 1][j] : hin[j];
+                lam[j] = fmaf(anext[j], lam[j], s_C[(G * g + j) * K + k] * dy);
+                pc[j] = dy * hk[k][j];
+                pb[j] = lam[j] * dl * uu;
+                dup = fmaf(lam[j] * dl, Bv, dup);
+                ddp = fmaf(lam[j], fmaf(An[j] * ak[k][j], hp, Bv * uu), ddp);
+                dA_acc[j] = fmaf(lam[j] * dl * ak[k][j], hp, dA_acc[j]);
+                anext[j] = ak[k][j];
             }
-            if (lane < N) {
-                s_pC[warp][n][k] = pc;
-                s_pB[warp][n][k] = pb;
+            float4* pp = reinterpret_cast<float4*>(s_P + ((size_t)k * kBwdThreads + tid) * 8);
+            pp[0] = make_float4(pc[0], pc[1], pc[2], pc[3]);
+            pp[1] = make_float4(pb[0], pb[1], pb[2], pb[3]);
+            dup = chan_sum<R>(dup);
+            ddp = chan_sum<R>(ddp);
+            if (g == 0) {
+                s_du[k * CC + cl] = fmaf(Dd, dy, dup);
+                s_dd[k * CC + cl] = ddp;
             }
-            const float dup = group_sum<N>(lam * dl * s_B[n][k]);
-            const float ddp = group_sum<N>(lam * (An * a * hprev + s_B[n][k] * uu));
-            if (n == 0) {
-                s_du[k][cl] = Dd * dy + dup;
-                s_dd[k][cl] = ddp;
-            }
-            dA_acc += lam * dl * a * hprev;
-            anext = a;
         }
         __syncthreads();
         // per-(t, d) outputs of the chunk
@@ -189,47 +292,68 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
             const int64_t t = t0 + k, dd = d0 + cc;
             if (t >= L || dd >= dim) continue;
             const int64_t gi = (b * L + t) * dim + dd;
-            const float ddl = s_dd[k][cc];
-            const float dx = p.softplus ? ddl * bw_sigmoid(s_x[k][cc]) : ddl;
-            bw_st(static_cast<T*>(p.du), gi, s_du[k][cc]);
+            const float ddl = s_dd[i];
+            const float dx = p.softplus ? ddl * bw_sigmoid(s_x[i]) : ddl;
+            bw_st(static_cast<T*>(p.du), gi, s_du[i]);
             bw_st(static_cast<T*>(p.ddelta), gi, dx);
-            atomicAdd(&s_db[cc], dx);
-            atomicAdd(&s_dD[cc], s_dy[k][cc] * s_u[k][cc]);
+            atomicAdd(&s_dbc[cc], dx);
+            atomicAdd(&s_dDc[cc], s_dy[i] * s_u[i]);
             if (zg && p.dz) {
-                const float zv = s_z[k][cc], sg = bw_sigmoid(zv);
-                bw_st(static_cast<T*>(p.dz), gi, s_do[k][cc] * s_y[k][cc] * sg * (1.f + zv * (1.f - sg)));
+                const float zv = s_z[i], sg = bw_sigmoid(zv);
+                bw_st(static_cast<T*>(p.dz), gi, s_do[i] * s_y[i] * sg * (1.f + zv * (1.f - sg)));
             }
         }
-        // dB, dC of the chunk: the warps' partials summed, one global atomic
-        // per (state, step)
-        for (int i = tid; i < N * K; i += kBwdThreads) {
-            const int nn = i / K, k = i % K;
-            const int64_t t = t0 + k;
-            if (t >= L) continue;
-            float sb = 0.f, sc = 0.f;
-#pragma unroll
-            for (int w = 0; w < kBwdThreads / 32; ++w) {
-                sb += s_pB[w][nn][k];
-                sc += s_pC[w][nn][k];
+        // dB, dC of the chunk: every (step, state quad, B-or-C) summed over the
+        // CTA's channels (parts of the channel range per thread when there are
+        // fewer such sums than threads), then added to global memory
+        {
+            constexpr int SUMS = K * R * 2;
+            constexpr int PARTS = SUMS >= kBwdThreads ? 1 : kBwdThreads / SUMS;
+            constexpr int CPP = CC / PARTS;
+            for (int i = tid; i < SUMS * PARTS; i += kBwdThreads) {
+                const int part = i / SUMS, sidx = i % SUMS;
+                const int k = sidx / (2 * R), gq = (sidx / 2) % R, which = sidx % 2;
+                const int64_t t = t0 + k;
+                if (t >= L) continue;
+                float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+                for (int cc = part * CPP; cc < (part + 1) * CPP; ++cc) {
+                    // the lane of channel cc holding state quad gq
+                    const int ln = (cc / CPW) * 32 + (cc % CPW) * R + gq;
+                    const float4 v = reinterpret_cast<const float4*>(s_P + ((size_t)k * kBwdThreads + ln) * 8)[which];
+                    acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
+                }
+                float* dst = (which ? p.dB : p.dC) + (b * N + G * gq) * L + t;
+                atomicAdd(dst, acc.x);
+                atomicAdd(dst + L, acc.y);
+                atomicAdd(dst + 2 * L, acc.z);
+                atomicAdd(dst + 3 * L, acc.w);
             }
-            atomicAdd(p.dB + (b * N + nn) * L + t, sb);
-            atomicAdd(p.dC + (b * N + nn) * L + t, sc);
         }
         __syncthreads();
     }
-    if (ch_ok) atomicAdd(p.dA + d * N + n, dA_acc);
+    if (ch_ok) {
+#pragma unroll
+        for (int j = 0; j < G; ++j) atomicAdd(p.dA + d * N + G * g + j, dA_acc[j]);
+    }
     for (int i = tid; i < CC; i += kBwdThreads) {
         if (d0 + i >= dim) continue;
-        if (p.dD) atomicAdd(p.dD + d0 + i, s_dD[i]);
-        if (p.dbias) atomicAdd(p.dbias + d0 + i, s_db[i]);
+        if (p.dD) atomicAdd(p.dD + d0 + i, s_dDc[i]);
+        if (p.dbias) atomicAdd(p.dbias + d0 + i, s_dbc[i]);
     }
 }
 
 template <typename T, int N>
 cudaError_t launch_bwd_t(const BwdArgs& a, float* ckpt, cudaStream_t s) {
-    constexpr int CC = (32 / N) * (kBwdThreads / 32);
-    dim3 grid((unsigned)((a.dim + CC - 1) / CC), (unsigned)a.batch);
-    scan_bwd_kernel<T, N><<<grid, kBwdThreads, 0, s>>>(a, ckpt);
+    using CF = BwdCfg<N>;
+    static bool attr = false;
+    if (!attr) {
+        const cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                                   CF::SMEM);
+        if (e != cudaSuccess) return e;
+        attr = true;
+    }
+    dim3 grid((unsigned)((a.dim + CF::CC - 1) / CF::CC), (unsigned)a.batch);
+    scan_bwd_kernel<T, N><<<grid, kBwdThreads, CF::SMEM, s>>>(a, ckpt);
     return cudaGetLastError();
 }
 

@@ -159,7 +159,7 @@ def test_scan_bwd_rejects_bad_arguments(lib, kw, code):
     assert lib.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], 1, a["dout"],
                             a["du"], a["dd"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["db"], a["batch"],
                             a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
-    assert lib.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16, 1) == 2 * 64 * 8 * 16 * 4
+    assert lib.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16, 1) == 2 * 64 * 16 * 16 * 4
 
 
 def upd_args(**kw):
