@@ -103,8 +103,10 @@ __device__ __forceinline__ float chan_sum(float v) {
     return v;
 }
 
+// Four CTAs per SM (at most 128 registers a thread, a few hundred bytes of
+// spills): the batch x dim/32 CTAs of the training shapes then run in one wave.
 template <typename T, int N>
-__global__ void __launch_bounds__(kBwdThreads)
+__global__ void __launch_bounds__(kBwdThreads, 4)
 scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
     using CF = BwdCfg<N>;
     constexpr int K = CF::K, R = CF::R, CPW = CF::CPW, CC = CF::CC, G = CF::G;
