@@ -103,10 +103,11 @@ __device__ __forceinline__ float chan_sum(float v) {
     return v;
 }
 
-// Four CTAs per SM (at most 128 registers a thread, a few hundred bytes of
-// spills): the batch x dim/32 CTAs of the training shapes then run in one wave.
-template <typename T, int N>
-__global__ void __launch_bounds__(kBwdThreads, 4)
+// kTight: a register budget for four CTAs per SM (at most 128 registers a
+// thread, a few hundred bytes of spills), taken when the grid would not fit
+// the GPU in one wave otherwise; small grids keep every register.
+template <typename T, int N, bool kTight>
+__global__ void __launch_bounds__(kBwdThreads, kTight ? 4 : 1)
 scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
     using CF = BwdCfg<N>;
     constexpr int K = CF::K, R = CF::R, CPW = CF::CPW, CC = CF::CC, G = CF::G;
@@ -345,17 +346,24 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
 }
 
 template <typename T, int N>
-cudaError_t launch_bwd_t(const BwdArgs& a, float* ckpt, cudaStream_t s) {
+cudaError_t launch_bwd_t(const BwdArgs& a, float* ckpt, int sms, cudaStream_t s) {
     using CF = BwdCfg<N>;
     static bool attr = false;
     if (!attr) {
-        const cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                   CF::SMEM);
+        cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, false>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        if (e == cudaSuccess)
+            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                     CF::SMEM);
         if (e != cudaSuccess) return e;
         attr = true;
     }
     dim3 grid((unsigned)((a.dim + CF::CC - 1) / CF::CC), (unsigned)a.batch);
-    scan_bwd_kernel<T, N><<<grid, kBwdThreads, CF::SMEM, s>>>(a, ckpt);
+    // with every register a thread, about two CTAs fit an SM
+    if ((int64_t)grid.x * grid.y > 2 * (int64_t)sms)
+        scan_bwd_kernel<T, N, true><<<grid, kBwdThreads, CF::SMEM, s>>>(a, ckpt);
+    else
+        scan_bwd_kernel<T, N, false><<<grid, kBwdThreads, CF::SMEM, s>>>(a, ckpt);
     return cudaGetLastError();
 }
 
@@ -366,7 +374,7 @@ int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dsta
     return batch * dim * ((seqlen + k - 1) / k) * dstate * 4;
 }
 
-cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, cudaStream_t s) {
+cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms, cudaStream_t s) {
     // the accumulated gradients start from zero
     const int64_t N = a.dstate;
     cudaError_t e = cudaMemsetAsync(a.dA, 0, a.dim * N * 4, s);
@@ -378,9 +386,9 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, cudaStr
     float* ck = static_cast<float*>(workspace);
     const bool bf = dt == DType::BF16;
     switch (a.dstate) {
-        case 4: return bf ? launch_bwd_t<__nv_bfloat16, 4>(a, ck, s) : launch_bwd_t<float, 4>(a, ck, s);
-        case 8: return bf ? launch_bwd_t<__nv_bfloat16, 8>(a, ck, s) : launch_bwd_t<float, 8>(a, ck, s);
-        case 16: return bf ? launch_bwd_t<__nv_bfloat16, 16>(a, ck, s) : launch_bwd_t<float, 16>(a, ck, s);
+        case 4: return bf ? launch_bwd_t<__nv_bfloat16, 4>(a, ck, sms, s) : launch_bwd_t<float, 4>(a, ck, sms, s);
+        case 8: return bf ? launch_bwd_t<__nv_bfloat16, 8>(a, ck, sms, s) : launch_bwd_t<float, 8>(a, ck, sms, s);
+        case 16: return bf ? launch_bwd_t<__nv_bfloat16, 16>(a, ck, sms, s) : launch_bwd_t<float, 16>(a, ck, sms, s);
         default: return cudaErrorInvalidValue;
     }
 }

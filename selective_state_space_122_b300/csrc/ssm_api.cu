@@ -334,7 +334,7 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
                    D ? dD : nullptr, z ? dz : nullptr, delta_bias ? ddelta_bias : nullptr, batch, dim, seqlen,
                    (int)dstate};
     return launch_status(ssm::launch_scan_bwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32, workspace,
-                                              static_cast<cudaStream_t>(stream)));
+                                              sms, static_cast<cudaStream_t>(stream)));
 }
 
 ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,

@@ -114,7 +114,7 @@ struct BwdArgs {
     int dstate;
 };
 int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
-cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, cudaStream_t s);
+cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
 
 // Tensor-memory scan (scan_tmem.cu): bf16 activations, 16 states.  Workspace:
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
