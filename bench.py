@@ -24,6 +24,7 @@ import os
 import statistics
 import subprocess
 import sys
+import tempfile
 import time
 
 import numpy as np
@@ -162,7 +163,8 @@ class ClockSampler:
         self.path = None
 
     def __enter__(self):
-        out_dir = os.path.join(ROOT, "gpurun_out")
+        # the samples are also kept as a file: SSM_BENCH_CLOCK_DIR, else the temp directory
+        out_dir = os.environ.get("SSM_BENCH_CLOCK_DIR") or tempfile.gettempdir()
         os.makedirs(out_dir, exist_ok=True)
         self.path = os.path.join(out_dir, f"clocks_rank{self.gpu}.csv")
         try:

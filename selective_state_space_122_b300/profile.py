@@ -140,8 +140,6 @@ def cmd_units(a):
     lib.ssmpk_probe_shape.restype = ctypes.c_double
     lib.ssmpk_sm_count.restype = ctypes.c_int
     sms = lib.ssmpk_sm_count()
-    clk = torch.cuda.get_device_properties(0)
-    del clk
     for name, kind, iters in (("ex2", 0, 20000), ("packed FMA", 3, 40000)):
         for bps, thr in ((1, 128), (2, 128), (4, 256)):
             r = max(lib.ssmpk_probe_shape(kind, iters, bps, thr) for _ in range(3))
