@@ -122,7 +122,7 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
     float* s_x = sm + CF::O_X;
     float* s_z = sm + CF::O_Z;
     float* s_do = sm + CF::O_DO;
-    float* s_B = sm + CF::O_B;      // [N][K]
+    float* s_B = sm + CF::O_B;      // [K][N]
     float* s_C = sm + CF::O_C;
     float* s_P = sm + CF::O_P;      // [K][kBwdThreads][8]
     float* s_dDc = sm + CF::O_DD_CH;
@@ -203,86 +203,96 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         for (int q = 0; q < BT; ++q) {
             const int i = tid + q * kBwdThreads;
             if (i >= N * K) continue;
-            s_B[i] = r.Bv[q];
-            if (backward) s_C[i] = r.Cv[q];
+            const int nn = i / K, k = i % K;
+            s_B[k * N + nn] = r.Bv[q];
+            if (backward) s_C[k * N + nn] = r.Cv[q];
         }
         __syncthreads();
     };
 
     // ---- pass 1: forward, checkpoint the state entering each chunk
-    float h[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) h[j] = 0.f;
+    const float2 A01 = make_float2(An[0], An[1]), A23 = make_float2(An[2], An[3]);
+    float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
     Pre pre;
     fetch(0, false, pre);
     for (int64_t c = 0; c < nch; ++c) {
         commit(pre, false);
         if (c + 1 < nch) fetch(c + 1, false, pre);
         if (ch_ok)
-            *reinterpret_cast<float4*>(ckpt + ((b * dim + d) * nch + c) * N + G * g) = make_float4(h[0], h[1], h[2], h[3]);
+            *reinterpret_cast<float4*>(ckpt + ((b * dim + d) * nch + c) * N + G * g) =
+                make_float4(h01.x, h01.y, h23.x, h23.y);
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            const float dl = s_dl[k * CC + cl], du = dl * s_u[k * CC + cl];
-#pragma unroll
-            for (int j = 0; j < G; ++j) h[j] = bw_exp<kFast>(dl * An[j]) * h[j] + du * s_B[(G * g + j) * K + k];
+            const float dl = s_dl[k * CC + cl];
+            const float2 dl2 = splat2(dl), du2 = splat2(dl * s_u[k * CC + cl]);
+            const float4 Bq = *reinterpret_cast<const float4*>(s_B + k * N + G * g);
+            const float2 e01 = mul2(dl2, A01), e23 = mul2(dl2, A23);
+            h01 = fma2(make_float2(bw_exp<kFast>(e01.x), bw_exp<kFast>(e01.y)), h01, mul2(du2, make_float2(Bq.x, Bq.y)));
+            h23 = fma2(make_float2(bw_exp<kFast>(e23.x), bw_exp<kFast>(e23.y)), h23, mul2(du2, make_float2(Bq.z, Bq.w)));
         }
         __syncthreads();
     }
 
     // ---- pass 2: chunks in reverse
-    float lam[G], anext[G], dA_acc[G];
-#pragma unroll
-    for (int j = 0; j < G; ++j) lam[j] = anext[j] = dA_acc[j] = 0.f;
+    float2 lam01 = make_float2(0.f, 0.f), lam23 = lam01, an01 = lam01, an23 = lam01, dA01 = lam01, dA23 = lam01;
     fetch(nch - 1, true, pre);
     for (int64_t c = nch - 1; c >= 0; --c) {
         commit(pre, true);
         if (c > 0) fetch(c - 1, true, pre);
         const int64_t t0 = c * K;
-        float hin[G];
+        float2 hin01, hin23;
         {
             const float4 v = ch_ok ? *reinterpret_cast<const float4*>(ckpt + ((b * dim + d) * nch + c) * N + G * g)
                                    : make_float4(0.f, 0.f, 0.f, 0.f);
-            hin[0] = v.x; hin[1] = v.y; hin[2] = v.z; hin[3] = v.w;
+            hin01 = make_float2(v.x, v.y);
+            hin23 = make_float2(v.z, v.w);
         }
-        // recompute the chunk's states and decays; y_t for dz
-        float hk[K][G], ak[K][G];
+        // recompute the chunk's states and decays (pairs of states per packed
+        // operation); y_t for dz
+        float2 hk01[K], hk23[K], ak01[K], ak23[K];
 #pragma unroll
         for (int k = 0; k < K; ++k) {
-            const float dl = s_dl[k * CC + cl], du = dl * s_u[k * CC + cl];
-            float yp = 0.f;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float a = bw_exp<kFast>(dl * An[j]);
-                const float hp = k > 0 ? hk[k - 1][j] : hin[j];
-                ak[k][j] = a;
-                hk[k][j] = a * hp + du * s_B[(G * g + j) * K + k];
-                yp = fmaf(s_C[(G * g + j) * K + k], hk[k][j], yp);
-            }
-            yp = chan_sum<R>(yp);
-            if (g == 0) s_y[k * CC + cl] = yp + Dd * s_u[k * CC + cl];
+            const float dl = s_dl[k * CC + cl], uu = s_u[k * CC + cl];
+            const float2 dl2 = splat2(dl), du2 = splat2(dl * uu);
+            const float4 Bq = *reinterpret_cast<const float4*>(s_B + k * N + G * g);
+            const float4 Cq = *reinterpret_cast<const float4*>(s_C + k * N + G * g);
+            const float2 e01 = mul2(dl2, A01), e23 = mul2(dl2, A23);
+            ak01[k] = make_float2(bw_exp<kFast>(e01.x), bw_exp<kFast>(e01.y));
+            ak23[k] = make_float2(bw_exp<kFast>(e23.x), bw_exp<kFast>(e23.y));
+            hk01[k] = fma2(ak01[k], k > 0 ? hk01[k - 1] : hin01, mul2(du2, make_float2(Bq.x, Bq.y)));
+            hk23[k] = fma2(ak23[k], k > 0 ? hk23[k - 1] : hin23, mul2(du2, make_float2(Bq.z, Bq.w)));
+            const float2 yv = fma2(make_float2(Cq.z, Cq.w), hk23[k], mul2(make_float2(Cq.x, Cq.y), hk01[k]));
+            const float yp = chan_sum<R>(yv.x + yv.y);
+            if (g == 0) s_y[k * CC + cl] = yp + Dd * uu;
         }
         // the adjoint, backwards over the chunk
 #pragma unroll
         for (int k = K - 1; k >= 0; --k) {
             const float dl = s_dl[k * CC + cl], uu = s_u[k * CC + cl], dy = s_dy[k * CC + cl];
-            float pc[G], pb[G], dup = 0.f, ddp = 0.f;
-#pragma unroll
-            for (int j = 0; j < G; ++j) {
-                const float Bv = s_B[(G * g + j) * K + k];
-                const float hp = k > 0 ? hk[k - 1][j] : hin[j];
-                lam[j] = fmaf(anext[j], lam[j], s_C[(G * g + j) * K + k] * dy);
-                pc[j] = dy * hk[k][j];
-                pb[j] = lam[j] * dl * uu;
-                dup = fmaf(lam[j] * dl, Bv, dup);
-                ddp = fmaf(lam[j], fmaf(An[j] * ak[k][j], hp, Bv * uu), ddp);
-                dA_acc[j] = fmaf(lam[j] * dl * ak[k][j], hp, dA_acc[j]);
-                anext[j] = ak[k][j];
-            }
+            const float2 dl2 = splat2(dl), uu2 = splat2(uu), dy2 = splat2(dy);
+            const float4 Bq = *reinterpret_cast<const float4*>(s_B + k * N + G * g);
+            const float4 Cq = *reinterpret_cast<const float4*>(s_C + k * N + G * g);
+            const float2 B01 = make_float2(Bq.x, Bq.y), B23 = make_float2(Bq.z, Bq.w);
+            const float2 hp01 = k > 0 ? hk01[k - 1] : hin01, hp23 = k > 0 ? hk23[k - 1] : hin23;
+            lam01 = fma2(an01, lam01, mul2(make_float2(Cq.x, Cq.y), dy2));
+            lam23 = fma2(an23, lam23, mul2(make_float2(Cq.z, Cq.w), dy2));
+            const float2 ld01 = mul2(lam01, dl2), ld23 = mul2(lam23, dl2);       // lambda Delta
+            const float2 pc01 = mul2(dy2, hk01[k]), pc23 = mul2(dy2, hk23[k]);   // dC terms
+            const float2 pb01 = mul2(ld01, uu2), pb23 = mul2(ld23, uu2);         // dB terms
+            const float2 duv = fma2(ld23, B23, mul2(ld01, B01));
+            // A a h_{t-1} + B u, per state
+            const float2 t01 = fma2(mul2(A01, ak01[k]), hp01, mul2(B01, uu2));
+            const float2 t23 = fma2(mul2(A23, ak23[k]), hp23, mul2(B23, uu2));
+            const float2 ddv = fma2(lam23, t23, mul2(lam01, t01));
+            dA01 = fma2(mul2(ld01, ak01[k]), hp01, dA01);
+            dA23 = fma2(mul2(ld23, ak23[k]), hp23, dA23);
+            an01 = ak01[k];
+            an23 = ak23[k];
             float4* pp = reinterpret_cast<float4*>(s_P + ((size_t)k * kBwdThreads + tid) * 8);
-            pp[0] = make_float4(pc[0], pc[1], pc[2], pc[3]);
-            pp[1] = make_float4(pb[0], pb[1], pb[2], pb[3]);
-            dup = chan_sum<R>(dup);
-            ddp = chan_sum<R>(ddp);
+            pp[0] = make_float4(pc01.x, pc01.y, pc23.x, pc23.y);
+            pp[1] = make_float4(pb01.x, pb01.y, pb23.x, pb23.y);
+            const float dup = chan_sum<R>(duv.x + duv.y);
+            const float ddp = chan_sum<R>(ddv.x + ddv.y);
             if (g == 0) {
                 s_du[k * CC + cl] = fmaf(Dd, dy, dup);
                 s_dd[k * CC + cl] = ddp;
@@ -335,8 +345,11 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         __syncthreads();
     }
     if (ch_ok) {
-#pragma unroll
-        for (int j = 0; j < G; ++j) atomicAdd(p.dA + d * N + G * g + j, dA_acc[j]);
+        float* da = p.dA + d * N + G * g;
+        atomicAdd(da, dA01.x);
+        atomicAdd(da + 1, dA01.y);
+        atomicAdd(da + 2, dA23.x);
+        atomicAdd(da + 3, dA23.y);
     }
     for (int i = tid; i < CC; i += kBwdThreads) {
         if (d0 + i >= dim) continue;
