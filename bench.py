@@ -170,7 +170,7 @@ class ClockSampler:
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(["nvidia-smi", "-i", str(self.gpu), f"--query-gpu={self.QUERY}",
-                                          "--format=csv,noheader,nounits", "-lms", "200"],
+                                          "--format=csv,noheader,nounits", "-lms", "50"],
                                          stdout=self.f, stderr=subprocess.DEVNULL)
             time.sleep(0.3)
         except OSError:
@@ -206,8 +206,14 @@ class ClockSampler:
                     reasons.add(n)
         if not sm:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax), "samples": len(sm),
-                "power_w_max": max(power) if power else None, "reasons": sorted(reasons)}
+        # "under load": the samples drawing at least half the peak power seen (the
+        # sampler also runs a moment before and after the timed region)
+        pk = max(power) if power else 0.0
+        loaded = [c for c, w in zip(sm, power) if w >= 0.5 * pk] if power else sm
+        loaded = loaded or sm
+        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
+                "samples_under_load": len(loaded), "power_w_max": pk if power else None,
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- our arm
@@ -565,7 +571,7 @@ def bench_reference(args):
 def main(argv=None):
     ap = argparse.ArgumentParser(description=__doc__.split("\n\n")[0])
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--steps", type=int, default=40)
     ap.add_argument("--warmup", type=int, default=3)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--e2e-steps", type=int, default=3)
