@@ -59,6 +59,12 @@ def load(path: Optional[str] = None):
     lib.oracle_conv1d_update.restype = ctypes.c_int
     lib.oracle_step.argtypes = [dp] * 9 + [ctypes.c_int, dp] + [ctypes.c_int] * 3
     lib.oracle_step.restype = ctypes.c_int
+    lib.oracle_scan_grouped.argtypes = [dp] * 8 + [ctypes.c_int, dp, dp, dp] + [ctypes.c_int] * 5
+    lib.oracle_scan_grouped.restype = ctypes.c_int
+    lib.oracle_step_grouped.argtypes = [dp] * 9 + [ctypes.c_int, dp] + [ctypes.c_int] * 4
+    lib.oracle_step_grouped.restype = ctypes.c_int
+    lib.oracle_scan_bwd_grouped.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 9 + [ctypes.c_int] * 5
+    lib.oracle_scan_bwd_grouped.restype = ctypes.c_int
     lib.oracle_softplus.argtypes = [ctypes.c_double]
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_silu.argtypes = [ctypes.c_double]
@@ -81,11 +87,18 @@ def _f64(a):
     return None if a is None else np.ascontiguousarray(a, dtype=np.float64)
 
 
+def _groups(B, lead, tail):
+    """Number of B/C groups: B is lead + (N, ...) for one group, lead +
+    (ngroups, N, ...) for several."""
+    return 1 if B.ndim == len(lead) + 1 + len(tail) else B.shape[len(lead)]
+
+
 def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
          want_last_state=True, lib=None, initial_state=None):
     """Full-sequence selective scan.
 
-    u, delta, z: (batch, L, dim); B, C: (batch, N, L); A: (dim, N);
+    u, delta, z: (batch, L, dim); B, C: (batch, N, L), or (batch, ngroups, N, L)
+    with channel d reading group d // (dim // ngroups); A: (dim, N);
     D, delta_bias: (dim,); initial_state: (batch, dim, N) or None (zero).
     Returns (out (batch, L, dim), last_state (batch, dim, N) or None), float64.
     """
@@ -93,13 +106,15 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
     u, delta, A, B, C, D, z, delta_bias, h0 = map(_f64, (u, delta, A, B, C, D, z, delta_bias, initial_state))
     bt, L, dim = u.shape
     N = A.shape[1]
+    G = _groups(B, (bt,), (L,))
     assert delta.shape == u.shape and A.shape == (dim, N)
-    assert B.shape == (bt, N, L) and C.shape == (bt, N, L)
+    shape = (bt, N, L) if B.ndim == 3 else (bt, G, N, L)
+    assert B.shape == shape and C.shape == shape
     assert h0 is None or h0.shape == (bt, dim, N)
     out = np.empty_like(u)
     last = np.empty((bt, dim, N)) if want_last_state else None
-    rc = lib.oracle_scan_from(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                              int(bool(softplus)), _p(h0), _p(out), _p(last), bt, dim, L, N)
+    rc = lib.oracle_scan_grouped(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                 int(bool(softplus)), _p(h0), _p(out), _p(last), bt, dim, L, N, G)
     if rc != 0:
         raise ValueError(f"oracle_scan rejected its arguments (code {rc})")
     return out, last
@@ -107,14 +122,17 @@ def scan(u, delta, A, B, C, D=None, z=None, delta_bias=None, softplus=True,
 
 def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, lib=None):
     """One recurrent update.  ``state`` (batch, dim, N) float64 is updated in
-    place; x, dt, z: (batch, dim); B, C: (batch, N).  Returns out (batch, dim)."""
+    place; x, dt, z: (batch, dim); B, C: (batch, N) or (batch, ngroups, N).
+    Returns out (batch, dim)."""
     lib = lib or load()
     assert state.dtype == np.float64 and state.flags["C_CONTIGUOUS"]
     x, dt, A, B, C, D, z, dt_bias = map(_f64, (x, dt, A, B, C, D, z, dt_bias))
     bt, dim, N = state.shape
+    G = _groups(B, (bt,), ())
+    assert B.shape == C.shape and B.shape[-1] == N
     out = np.empty((bt, dim))
-    rc = lib.oracle_step(_p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z),
-                         _p(dt_bias), int(bool(dt_softplus)), _p(out), bt, dim, N)
+    rc = lib.oracle_step_grouped(_p(state), _p(x), _p(dt), _p(A), _p(B), _p(C), _p(D), _p(z),
+                                 _p(dt_bias), int(bool(dt_softplus)), _p(out), bt, dim, N, G)
     if rc != 0:
         raise ValueError(f"oracle_step rejected its arguments (code {rc})")
     return out
@@ -123,19 +141,22 @@ def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, 
 def scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, lib=None):
     """Gradients of L = sum(dout * out) of the scan (from h = 0) with respect to
     every input.  Returns a dict du, ddelta (batch, L, dim); dA (dim, N); dB, dC
-    (batch, N, L); dD, ddelta_bias (dim,) or None; dz (batch, L, dim) or None."""
+    shaped like B and C ((batch, N, L) or (batch, ngroups, N, L)); dD,
+    ddelta_bias (dim,) or None; dz (batch, L, dim) or None."""
     lib = lib or load()
     u, delta, A, B, C, D, z, delta_bias, dout = map(_f64, (u, delta, A, B, C, D, z, delta_bias, dout))
     bt, L, dim = u.shape
     N = A.shape[1]
+    G = _groups(B, (bt,), (L,))
+    assert B.shape == C.shape and B.shape[-2:] == (N, L)
     g = dict(du=np.empty_like(u), ddelta=np.empty_like(u), dA=np.empty_like(A), dB=np.empty_like(B),
              dC=np.empty_like(C), dD=None if D is None else np.empty(dim),
              dz=None if z is None else np.empty_like(u),
              ddelta_bias=None if delta_bias is None else np.empty(dim))
-    rc = lib.oracle_scan_bwd(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                             int(bool(softplus)), _p(dout), _p(g["du"]), _p(g["ddelta"]), _p(g["dA"]),
-                             _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]), _p(g["ddelta_bias"]),
-                             bt, dim, L, N)
+    rc = lib.oracle_scan_bwd_grouped(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                     int(bool(softplus)), _p(dout), _p(g["du"]), _p(g["ddelta"]), _p(g["dA"]),
+                                     _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]), _p(g["ddelta_bias"]),
+                                     bt, dim, L, N, G)
     if rc != 0:
         raise ValueError(f"oracle_scan_bwd rejected its arguments (code {rc})")
     return g

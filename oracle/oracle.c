@@ -35,7 +35,9 @@
  *
  * Layouts (row-major):
  *   u, delta, z, out : [batch][seqlen][dim]
- *   B, C             : [batch][dstate][seqlen]
+ *   B, C             : [batch][dstate][seqlen], or [batch][ngroups][dstate][seqlen]
+ *                      for the grouped entry points (channel d reads group
+ *                      d / (dim / ngroups); one group is the plain layout)
  *   A                : [dim][dstate]
  *   D, delta_bias    : [dim]
  *   last_state       : [batch][dim][dstate]
@@ -43,7 +45,12 @@
  * Decode step:
  *   state            : [batch][dim][dstate]  (updated in place)
  *   x, dt, z, out    : [batch][dim]
- *   B, C             : [batch][dstate]
+ *   B, C             : [batch][dstate], or [batch][ngroups][dstate] (grouped)
+ *
+ * Grouped B and C.  The pages give B and C as functions of the input shared by
+ * every channel of a sequence.  The grouped entry points widen this the plain
+ * way: the channels are cut into ngroups equal consecutive blocks and each
+ * block has its own B_t and C_t; with one block this is the pages' model.
  */
 #include <math.h>
 #include <stddef.h>
@@ -99,18 +106,27 @@ static int check_dims(int batch, int dim, int seqlen, int dstate) {
     return 0;
 }
 
+static int check_groups(int dim, int ngroups) {
+    return (ngroups <= 0 || dim % ngroups != 0) ? 1 : 0;
+}
+
+/* Index of the B/C block that channel d of batch row b reads. */
+static ptrdiff_t bc_block(ptrdiff_t b, ptrdiff_t d, ptrdiff_t dim, ptrdiff_t ngroups) {
+    return b * ngroups + d / (dim / ngroups);
+}
+
 /* Full-sequence scan of every (batch, channel), independently, starting from
  * initial_state (h = 0 where it is NULL).  The OpenMP loop only distributes
  * whole independent channels across threads; each channel's arithmetic is the
  * sequential definition above.  last_state may be the same array as
  * initial_state (each channel reads its initial state before it writes). */
-int oracle_scan_from(const double* u, const double* delta, const double* A,
-                     const double* B, const double* C, const double* D,
-                     const double* z, const double* delta_bias, int softplus_flag,
-                     const double* initial_state, double* out, double* last_state,
-                     int batch, int dim, int seqlen, int dstate) {
+int oracle_scan_grouped(const double* u, const double* delta, const double* A,
+                        const double* B, const double* C, const double* D,
+                        const double* z, const double* delta_bias, int softplus_flag,
+                        const double* initial_state, double* out, double* last_state,
+                        int batch, int dim, int seqlen, int dstate, int ngroups) {
     if (!u || !delta || !A || !B || !C || !out) return 1;
-    if (check_dims(batch, dim, seqlen, dstate)) return 2;
+    if (check_dims(batch, dim, seqlen, dstate) || check_groups(dim, ngroups)) return 2;
     const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
     const long long total = (long long)batch * dim;
 #pragma omp parallel for schedule(dynamic, 1)
@@ -119,8 +135,9 @@ int oracle_scan_from(const double* u, const double* delta, const double* A,
         double h[ORACLE_MAX_DSTATE];
         for (ptrdiff_t n = 0; n < N; ++n)
             h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;
-        const double* Bb = B + b * N * L;
-        const double* Cb = C + b * N * L;
+        const ptrdiff_t blk = bc_block(b, d, Dm, ngroups);
+        const double* Bb = B + blk * N * L;
+        const double* Cb = C + blk * N * L;
         const double Dd = D ? D[d] : 0.0;
         for (ptrdiff_t t = 0; t < L; ++t) {
             const ptrdiff_t i = (b * L + t) * Dm + d;
@@ -132,6 +149,16 @@ int oracle_scan_from(const double* u, const double* delta, const double* A,
             for (ptrdiff_t n = 0; n < N; ++n) last_state[(b * Dm + d) * N + n] = h[n];
     }
     return 0;
+}
+
+/* The scan from a given state, with B and C shared by all channels. */
+int oracle_scan_from(const double* u, const double* delta, const double* A,
+                     const double* B, const double* C, const double* D,
+                     const double* z, const double* delta_bias, int softplus_flag,
+                     const double* initial_state, double* out, double* last_state,
+                     int batch, int dim, int seqlen, int dstate) {
+    return oracle_scan_grouped(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state,
+                               out, last_state, batch, dim, seqlen, dstate, 1);
 }
 
 /* The scan from h = 0. */
@@ -146,12 +173,13 @@ int oracle_scan(const double* u, const double* delta, const double* A,
 
 /* Single-token recurrent update ("Efficient Scan", item 2): the same step as
  * the scan's body, applied once to a caller-held state. */
-int oracle_step(double* state, const double* x, const double* dt,
-                const double* A, const double* B, const double* C,
-                const double* D, const double* z, const double* dt_bias,
-                int dt_softplus, double* out, int batch, int dim, int dstate) {
+int oracle_step_grouped(double* state, const double* x, const double* dt,
+                        const double* A, const double* B, const double* C,
+                        const double* D, const double* z, const double* dt_bias,
+                        int dt_softplus, double* out, int batch, int dim, int dstate,
+                        int ngroups) {
     if (!state || !x || !dt || !A || !B || !C || !out) return 1;
-    if (check_dims(batch, dim, 1, dstate)) return 2;
+    if (check_dims(batch, dim, 1, dstate) || check_groups(dim, ngroups)) return 2;
     const ptrdiff_t Dm = dim, N = dstate;
     const long long total = (long long)batch * dim;
 #pragma omp parallel for schedule(static)
@@ -159,13 +187,21 @@ int oracle_step(double* state, const double* x, const double* dt,
         const ptrdiff_t b = bd / Dm, d = bd % Dm;
         const ptrdiff_t i = b * Dm + d;
         const double dlt = timestep(dt[i], dt_bias, (int)d, dt_softplus);
-        out[i] = one_step(state + i * N, A + d * N, (int)N, B + b * N, C + b * N, 1,
+        const ptrdiff_t blk = bc_block(b, d, Dm, ngroups);
+        out[i] = one_step(state + i * N, A + d * N, (int)N, B + blk * N, C + blk * N, 1,
                           x[i], dlt, D ? D[d] : 0.0, z ? z + i : NULL);
     }
     return 0;
 }
 
-/* Scalar helpers exposed so the pins can test them against closed forms. */
+int oracle_step(double* state, const double* x, const double* dt,
+                const double* A, const double* B, const double* C,
+                const double* D, const double* z, const double* dt_bias,
+                int dt_softplus, double* out, int batch, int dim, int dstate) {
+    return oracle_step_grouped(state, x, dt, A, B, C, D, z, dt_bias, dt_softplus, out,
+                               batch, dim, dstate, 1);
+}
+
 /* Backward of the full-sequence scan (from h = 0): given dout = dL/d out,
  * every input's gradient, by the adjoint of the recurrence above (the
  * gradients the "training" mode of the pages' "Efficient Scan" needs).  With
@@ -182,22 +218,23 @@ int oracle_step(double* state, const double* x, const double* dt,
  *   dD      += dy_t u_t,   dz_t = dout_t y_t silu'(z_t)
  *   ddelta_raw_t = dDelta_t softplus'(x_t) (= dDelta_t without softplus),
  *   dbias  += ddelta_raw_t.
- * B and C are shared by all channels, so dB and dC sum over channels.  Every
+ * B and C are shared by all channels (of a group, in the grouped form), so dB
+ * and dC sum over those channels.  Every
  * output array is overwritten; dz, dD and dbias may be NULL when z, D or the
  * bias is absent.  Sequential (no threads): each output sums over channels. */
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
 
-int oracle_scan_bwd(const double* u, const double* delta, const double* A,
-                    const double* B, const double* C, const double* D,
-                    const double* z, const double* delta_bias, int softplus_flag,
-                    const double* dout, double* du, double* ddelta, double* dA,
-                    double* dB, double* dC, double* dD, double* dz, double* dbias,
-                    int batch, int dim, int seqlen, int dstate) {
+int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* A,
+                            const double* B, const double* C, const double* D,
+                            const double* z, const double* delta_bias, int softplus_flag,
+                            const double* dout, double* du, double* ddelta, double* dA,
+                            double* dB, double* dC, double* dD, double* dz, double* dbias,
+                            int batch, int dim, int seqlen, int dstate, int ngroups) {
     if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return 1;
-    if (check_dims(batch, dim, seqlen, dstate)) return 2;
+    if (check_dims(batch, dim, seqlen, dstate) || check_groups(dim, ngroups)) return 2;
     const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
     for (ptrdiff_t i = 0; i < Dm * N; ++i) dA[i] = 0.0;
-    for (ptrdiff_t i = 0; i < (ptrdiff_t)batch * N * L; ++i) dB[i] = dC[i] = 0.0;
+    for (ptrdiff_t i = 0; i < (ptrdiff_t)batch * ngroups * N * L; ++i) dB[i] = dC[i] = 0.0;
     if (dD) for (ptrdiff_t d = 0; d < Dm; ++d) dD[d] = 0.0;
     if (dbias) for (ptrdiff_t d = 0; d < Dm; ++d) dbias[d] = 0.0;
     double* hs = (double*)malloc((size_t)(L + 1) * N * sizeof(double));   /* h_{-1} .. h_{L-1} */
@@ -207,8 +244,9 @@ int oracle_scan_bwd(const double* u, const double* delta, const double* A,
     for (ptrdiff_t b = 0; b < batch; ++b)
         for (ptrdiff_t d = 0; d < Dm; ++d) {
             const double* Ar = A + d * N;
-            const double* Bb = B + b * N * L;
-            const double* Cb = C + b * N * L;
+            const ptrdiff_t blk = bc_block(b, d, Dm, ngroups);
+            const double* Bb = B + blk * N * L;
+            const double* Cb = C + blk * N * L;
             const double Dd = D ? D[d] : 0.0;
             /* forward, keeping every state */
             for (ptrdiff_t n = 0; n < N; ++n) hs[n] = 0.0;
@@ -241,8 +279,8 @@ int oracle_scan_bwd(const double* u, const double* delta, const double* A,
                     const double a = exp(dlt * Ar[n]);
                     const double hprev = hs[t * N + n], h = hs[(t + 1) * N + n];
                     lam[n] = Cb[n * L + t] * dy + anext[n] * lam[n];
-                    dC[(b * N + n) * L + t] += dy * h;
-                    dB[(b * N + n) * L + t] += lam[n] * dlt * u[i];
+                    dC[(blk * N + n) * L + t] += dy * h;
+                    dB[(blk * N + n) * L + t] += lam[n] * dlt * u[i];
                     dut += lam[n] * dlt * Bb[n * L + t];
                     ddl += lam[n] * (Ar[n] * a * hprev + Bb[n * L + t] * u[i]);
                     dA[d * N + n] += lam[n] * dlt * a * hprev;
@@ -260,6 +298,16 @@ int oracle_scan_bwd(const double* u, const double* delta, const double* A,
     free(dls);
     free(ys);
     return 0;
+}
+
+int oracle_scan_bwd(const double* u, const double* delta, const double* A,
+                    const double* B, const double* C, const double* D,
+                    const double* z, const double* delta_bias, int softplus_flag,
+                    const double* dout, double* du, double* ddelta, double* dA,
+                    double* dB, double* dC, double* dD, double* dz, double* dbias,
+                    int batch, int dim, int seqlen, int dstate) {
+    return oracle_scan_bwd_grouped(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dout, du,
+                                   ddelta, dA, dB, dC, dD, dz, dbias, batch, dim, seqlen, dstate, 1);
 }
 
 /* Depthwise causal convolution over time, per channel, width W, then the
@@ -331,6 +379,7 @@ int oracle_conv1d_update(double* state, const double* x, const double* w, const 
     return 0;
 }
 
+/* Scalar helpers exposed so the pins can test them against closed forms. */
 double oracle_softplus(double x) { return softplus(x); }
 double oracle_silu(double x) { return silu(x); }
 

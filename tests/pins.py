@@ -27,6 +27,9 @@ disagrees with an independent route to the same answer:
                  the carried state followed by the input gives every output and
                  the final state; a split sequence and a chain of decode steps
                  reproduce the whole convolution exactly;
+* groups:        with B and C per channel group, the unrolled sum reading each
+                 channel's own group, the grouped decode chain, and finite
+                 differences of the grouped gradients;
 * backward:      central finite differences of L = sum(dout * out) through the
                  forward oracle for every input; and L = <du, u> (out is
                  linear in u), L = <dB, B> = <dC, C> without the D skip (out
@@ -52,13 +55,14 @@ def _rng(seed):
 
 
 def tiny_case(seed, bt=2, L=12, dim=3, N=4, random_a=True, softplus=True,
-              with_z=True, with_d=True, with_bias=True):
+              with_z=True, with_d=True, with_bias=True, groups=None):
     r = _rng(seed)
     u = r.standard_normal((bt, L, dim))
     delta = r.standard_normal((bt, L, dim)) * 0.5
     z = r.standard_normal((bt, L, dim)) if with_z else None
-    B = r.standard_normal((bt, N, L))
-    C = r.standard_normal((bt, N, L))
+    bc_shape = (bt, N, L) if groups is None else (bt, groups, N, L)
+    B = r.standard_normal(bc_shape)
+    C = r.standard_normal(bc_shape)
     if random_a:
         A = -np.exp(r.standard_normal((dim, N)))
     else:
@@ -89,24 +93,27 @@ def _close(got, ref, rel=REL, what=""):
 def brute_force(case, h0=None):
     """y_t = sum_n C[n,t] (exp(A_n sum_{r<=t} Delta_r) h0_n
     + sum_{s<=t} exp(A_n sum_{r=s+1..t} Delta_r) Delta_s B[n,s] u_s) + D u_t, times
-    silu(z_t) (h0 = 0 unless given); also the state after the last step."""
+    silu(z_t) (h0 = 0 unless given); also the state after the last step.  With
+    grouped B, C of shape (batch, G, N, L), channel d takes block d // (dim // G)."""
     u, A, B, C = case["u"], case["A"], case["B"], case["C"]
     bt, L, dim = u.shape
     N = A.shape[1]
+    per = dim // (1 if B.ndim == 3 else B.shape[1])
     dlt = _timestep(case)
     Dv = np.zeros(dim) if case["D"] is None else case["D"]
     y = np.zeros_like(u)
     last = np.zeros((bt, dim, N))
     for b in range(bt):
         for d in range(dim):
+            Bd, Cd = (B[b], C[b]) if B.ndim == 3 else (B[b, d // per], C[b, d // per])
             for t in range(L):
                 h = np.zeros(N)
                 if h0 is not None:
                     h += np.exp(A[d] * float(np.sum(dlt[b, :t + 1, d]))) * h0[b, d]
                 for s in range(t + 1):
                     span = float(np.sum(dlt[b, s + 1:t + 1, d]))
-                    h += np.exp(A[d] * span) * dlt[b, s, d] * B[b, :, s] * u[b, s, d]
-                y[b, t, d] = float(np.dot(C[b, :, t], h)) + Dv[d] * u[b, t, d]
+                    h += np.exp(A[d] * span) * dlt[b, s, d] * Bd[:, s] * u[b, s, d]
+                y[b, t, d] = float(np.dot(Cd[:, t], h)) + Dv[d] * u[b, t, d]
                 if t == L - 1:
                     last[b, d] = h
     return y * _gate(case), last
@@ -301,7 +308,7 @@ def _cut(case, lo, hi):
         if case[k] is not None:
             c[k] = np.ascontiguousarray(case[k][:, lo:hi])
     for k in ("B", "C"):
-        c[k] = np.ascontiguousarray(case[k][:, :, lo:hi])
+        c[k] = np.ascontiguousarray(case[k][..., lo:hi])
     return c
 
 
@@ -420,6 +427,68 @@ def pin_bwd_homogeneity(lib):
         _close(np.array([np.sum(g["dC"] * case["C"])]), np.array([lval]), what="<dC, C> = L")
 
 
+def pin_grouped_brute_force(lib):
+    """B and C per channel group: the unrolled sum with each channel reading
+    its own group's B and C; with ngroups = dim every channel has its own."""
+    for seed, kw in [(301, dict(dim=4, groups=2)), (302, dict(dim=6, groups=3, softplus=False)),
+                     (303, dict(dim=3, groups=3, N=2)), (304, dict(dim=4, groups=1))]:
+        case = tiny_case(seed, L=9, **kw)
+        bt, _, dim = case["u"].shape
+        h0 = _rng(seed + 7).standard_normal((bt, dim, case["A"].shape[1]))
+        for init in (None, h0):
+            out, last = run_oracle(case, lib, init)
+            ref, ref_last = brute_force(case, init)
+            _close(out, ref, what=f"grouped brute out seed {seed}")
+            _close(last, ref_last, what=f"grouped brute last_state seed {seed}")
+
+
+def pin_grouped_decode_chain(lib):
+    """The grouped decode step chained over L tokens reproduces the grouped scan
+    exactly, and one decode step from a random state equals the one-step
+    unrolled sum (decay of the state plus the new input's term)."""
+    case = tiny_case(311, bt=2, L=8, dim=6, N=3, groups=3)
+    bt, L, dim = case["u"].shape
+    N = case["A"].shape[1]
+    out, last = run_oracle(case, lib)
+    state = np.zeros((bt, dim, N))
+    for t in range(L):
+        o = oracle.step(state, case["u"][:, t, :], case["delta"][:, t, :], case["A"],
+                        np.ascontiguousarray(case["B"][:, :, :, t]), np.ascontiguousarray(case["C"][:, :, :, t]),
+                        case["D"], case["z"][:, t, :], case["delta_bias"], case["softplus"], lib=lib)
+        assert np.array_equal(o, out[:, t, :]), f"grouped decode step {t} differs from the grouped scan"
+    assert np.array_equal(state, last), "grouped decode chain final state differs from the grouped scan"
+    one = _cut(case, 0, 1)
+    h0 = _rng(312).standard_normal((bt, dim, N))
+    ref, ref_last = brute_force(one, h0)
+    st = h0.copy()
+    o = oracle.step(st, one["u"][:, 0, :], one["delta"][:, 0, :], one["A"], np.ascontiguousarray(one["B"][..., 0]),
+                    np.ascontiguousarray(one["C"][..., 0]), one["D"], one["z"][:, 0, :], one["delta_bias"],
+                    one["softplus"], lib=lib)
+    _close(o, ref[:, 0, :], what="grouped decode step vs brute force")
+    _close(st, ref_last, what="grouped decode state vs brute force")
+
+
+def pin_grouped_bwd_finite_differences(lib):
+    """Grouped gradients: dB and dC sum over the channels of each group only."""
+    case = tiny_case(321, bt=2, L=5, dim=4, N=2, groups=2)
+    dout = _rng(322).standard_normal(case["u"].shape)
+    g = _grads(case, dout, lib)
+    assert g["dB"].shape == case["B"].shape and g["dC"].shape == case["C"].shape
+    for name, gname in GRAD_OF.items():
+        base = case[name]
+        fd = np.zeros_like(base)
+        for idx in np.ndindex(base.shape):
+            eps = 1e-6 * max(1.0, abs(float(base[idx])))
+            for sgn in (1.0, -1.0):
+                c = dict(case)
+                c[name] = base.copy()
+                c[name][idx] += sgn * eps
+                fd[idx] += sgn * _loss(c, dout, lib) / (2.0 * eps)
+        scale = max(1.0, float(np.max(np.abs(fd))))
+        err = float(np.max(np.abs(g[gname] - fd)))
+        assert err <= 2e-6 * scale, f"grouped d{name}: |analytic - finite difference| {err:.2e}"
+
+
 def pin_scalar_functions(lib):
     sp = lambda x: oracle.softplus(x, lib=lib)
     si = lambda x: oracle.silu(x, lib=lib)
@@ -440,4 +509,6 @@ ALL_PINS = [pin_brute_force, pin_time_invariant_convolution, pin_associative_sca
             pin_delta_to_zero, pin_memoryless_limit, pin_linear_in_u, pin_causal,
             pin_bc_scale, pin_channel_permutation, pin_decode_chain_equals_scan,
             pin_initial_state_brute_force, pin_split_equals_whole, pin_conv_impulse, pin_conv_numpy,
-            pin_conv_split_and_decode, pin_bwd_finite_differences, pin_bwd_homogeneity, pin_scalar_functions]
+            pin_conv_split_and_decode, pin_bwd_finite_differences, pin_bwd_homogeneity,
+            pin_grouped_brute_force, pin_grouped_decode_chain, pin_grouped_bwd_finite_differences,
+            pin_scalar_functions]

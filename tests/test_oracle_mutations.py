@@ -45,9 +45,16 @@ MUTATIONS = [
     ("dA uses h_t", "dA[d * N + n] += lam[n] * dlt * a * hprev;", "dA[d * N + n] += lam[n] * dlt * a * h;"),
     ("dDelta drops B u", "ddl += lam[n] * (Ar[n] * a * hprev + Bb[n * L + t] * u[i]);", "ddl += lam[n] * (Ar[n] * a * hprev);"),
     ("softplus derivative sign", "ddl * sigmoid(xr)", "ddl * sigmoid(-xr)"),
-    ("dB without Delta", "dB[(b * N + n) * L + t] += lam[n] * dlt * u[i];", "dB[(b * N + n) * L + t] += lam[n] * u[i];"),
+    ("dB without Delta", "dB[(blk * N + n) * L + t] += lam[n] * dlt * u[i];",
+     "dB[(blk * N + n) * L + t] += lam[n] * u[i];"),
     ("initial state read transposed", "h[n] = initial_state ? initial_state[(b * Dm + d) * N + n] : 0.0;",
      "h[n] = initial_state ? initial_state[(b * N + n) * Dm + d] : 0.0;"),
+    ("group taken as channel remainder", "return b * ngroups + d / (dim / ngroups);",
+     "return b * ngroups + d % ngroups;"),
+    ("group batch stride dropped", "return b * ngroups + d / (dim / ngroups);", "return b + d / (dim / ngroups);"),
+    ("decode ignores groups", "B + blk * N, C + blk * N, 1,", "B + b * N, C + b * N, 1,"),
+    ("grouped dC summed into the batch row", "dC[(blk * N + n) * L + t] += dy * h;",
+     "dC[(b * N + n) * L + t] += dy * h;"),
 ]
 
 
