@@ -166,6 +166,40 @@ SSM_API int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seq
                                          int dtype);
 
 /*
+ * ssm_scan_fwd_grouped -- the scan with B and C per channel group.  The
+ * pages' B_t and C_t are functions of the input shared by every channel of a
+ * sequence ("Selective Mechanism"); here the dim channels are cut into
+ * ngroups equal consecutive blocks of gch = dim / ngroups channels, and each
+ * block has its own B_t and C_t:
+ *
+ *   B, C   [batch][ngroups][dstate][seqlen]  dtype   channel d reads block
+ *                                                    [b][d / gch]
+ *
+ * ngroups = 1 is exactly ssm_scan_fwd_from_state.  ngroups must divide dim
+ * (SSM_ERR_SHAPE otherwise, and for ngroups <= 0).  Every other argument is
+ * as in ssm_scan_fwd_from_state.  Path choice: the tensor-memory kernels take
+ * bf16 / dstate 16 when gch is a multiple of 32 and batch * ngroups <= 65535;
+ * the segmented kernel when gch is a multiple of 128 / dstate; any other
+ * group size runs on the generic kernel (no workspace needed there).  The
+ * workspace is sized by ssm_scan_workspace_bytes_grouped.
+ */
+SSM_API ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A, const void* B,
+                                        const void* C, const float* D, const void* z, const float* delta_bias,
+                                        int softplus_flag, const float* initial_state, void* out,
+                                        float* last_state, int64_t batch, int64_t dim, int64_t seqlen,
+                                        int64_t dstate, int64_t ngroups, int dtype, void* workspace,
+                                        int64_t workspace_bytes, void* stream);
+
+/*
+ * ssm_scan_workspace_bytes_grouped -- ssm_scan_workspace_bytes for B and C
+ * with ngroups groups: the staged B/C parts (a), (b) and the staged operand
+ * of (c) grow by the factor ngroups, the rest is unchanged.  -1 also when
+ * ngroups does not divide dim.
+ */
+SSM_API int64_t ssm_scan_workspace_bytes_grouped(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                                 int64_t ngroups, int dtype);
+
+/*
  * ssm_device_error -- the library's device error word: 0 if no kernel has
  * reported a problem, otherwise a bit set (1: a staged-data wait timed out,
  * 2: a state hand-off between warps of a CTA timed out, 4: a state hand-off
@@ -200,7 +234,21 @@ SSM_API ssm_status ssm_state_update(float* state, const void* x, const void* dt,
                             void* out, int64_t batch, int64_t dim, int64_t dstate,
                             int dt_softplus, int dtype, void* stream);
 
-/* Static, human-readable name of a status code (never NULL). */
+/*
+ * ssm_state_update_grouped -- ssm_state_update with B and C per channel
+ * group (as ssm_scan_fwd_grouped):
+ *
+ *   B, C    [batch][ngroups][dstate]  dtype   channel d reads [b][d / (dim / ngroups)]
+ *
+ * ngroups = 1 is exactly ssm_state_update; ngroups must divide dim
+ * (SSM_ERR_SHAPE otherwise).
+ */
+SSM_API ssm_status ssm_state_update_grouped(float* state, const void* x, const void* dt, const float* A,
+                                            const void* B, const void* C, const float* D, const void* z,
+                                            const float* dt_bias, void* out, int64_t batch, int64_t dim,
+                                            int64_t dstate, int64_t ngroups, int dt_softplus, int dtype,
+                                            void* stream);
+
 /*
  * ssm_scan_bwd -- backward of ssm_scan_fwd (from h = 0): the gradients of a
  * loss L with respect to every input, given dout = dL/d out, by the adjoint
@@ -230,6 +278,21 @@ SSM_API ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A
                                 float* dD, void* dz, float* ddelta_bias, int64_t batch, int64_t dim,
                                 int64_t seqlen, int64_t dstate, int dtype, void* workspace,
                                 int64_t workspace_bytes, void* stream);
+
+/*
+ * ssm_scan_bwd_grouped -- ssm_scan_bwd with B and C per channel group (as
+ * ssm_scan_fwd_grouped): B, C, dB and dC are [batch][ngroups][dstate][seqlen],
+ * and dB, dC of a group sum over that group's channels only.  ngroups = 1 is
+ * exactly ssm_scan_bwd; ngroups must divide dim (SSM_ERR_SHAPE otherwise).
+ * The workspace is the same as ssm_scan_bwd's.
+ */
+SSM_API ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A, const void* B,
+                                        const void* C, const float* D, const void* z, const float* delta_bias,
+                                        int softplus_flag, const void* dout, void* du, void* ddelta, float* dA,
+                                        float* dB, float* dC, float* dD, void* dz, float* ddelta_bias,
+                                        int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                        int64_t ngroups, int dtype, void* workspace, int64_t workspace_bytes,
+                                        void* stream);
 
 /*
  * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs:
@@ -280,6 +343,7 @@ SSM_API ssm_status ssm_conv1d_update(float* conv_state, const void* x, const flo
                                      int silu_flag, void* out, int64_t batch, int64_t dim, int64_t width,
                                      int dtype, void* stream);
 
+/* Static, human-readable name of a status code (never NULL). */
 SSM_API const char* ssm_status_string(int status);
 
 /*

@@ -24,7 +24,8 @@ STATUS = {0: "SSM_OK", 1: "SSM_ERR_NULL", 2: "SSM_ERR_SHAPE", 3: "SSM_ERR_ALIGN"
 EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_state_update",
            "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
            "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state", "ssm_conv1d_fwd",
-           "ssm_conv1d_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_bytes")
+           "ssm_conv1d_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_bytes", "ssm_scan_fwd_grouped",
+           "ssm_scan_workspace_bytes_grouped", "ssm_state_update_grouped", "ssm_scan_bwd_grouped")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -54,6 +55,17 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_scan_bwd.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, fp, fp, fp, fp, vp, fp,
                                  i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_bwd.restype = ci
+    lib.ssm_scan_fwd_grouped.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, fp,
+                                         i64, i64, i64, i64, i64, ci, vp, i64, vp]
+    lib.ssm_scan_fwd_grouped.restype = ci
+    lib.ssm_scan_workspace_bytes_grouped.argtypes = [i64, i64, i64, i64, i64, ci]
+    lib.ssm_scan_workspace_bytes_grouped.restype = i64
+    lib.ssm_scan_bwd_grouped.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, fp, fp, fp, fp, vp, fp,
+                                         i64, i64, i64, i64, i64, ci, vp, i64, vp]
+    lib.ssm_scan_bwd_grouped.restype = ci
+    lib.ssm_state_update_grouped.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, vp,
+                                             i64, i64, i64, i64, ci, ci, vp]
+    lib.ssm_state_update_grouped.restype = ci
     lib.ssm_scan_bwd_workspace_bytes.argtypes = [i64, i64, i64, i64, ci]
     lib.ssm_scan_bwd_workspace_bytes.restype = i64
     lib.ssm_conv1d_fwd.argtypes = [vp, fp, fp, ci, fp, vp, fp, i64, i64, i64, i64, ci, vp]
@@ -121,10 +133,27 @@ def _stream(device: torch.device) -> int:
     return torch.cuda.current_stream(device).cuda_stream
 
 
-def scan_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, dtype: torch.dtype) -> int:
-    """Workspace bytes the fast path of ssm_scan_fwd needs (ssm_scan_workspace_bytes)."""
+def scan_workspace_bytes(batch: int, dim: int, seqlen: int, dstate: int, dtype: torch.dtype,
+                         ngroups: int = 1) -> int:
+    """Workspace bytes the fast path of ssm_scan_fwd needs (ssm_scan_workspace_bytes,
+    or ssm_scan_workspace_bytes_grouped for B/C with several channel groups)."""
     code = SSM_BF16 if dtype == torch.bfloat16 else SSM_F32
-    return int(load_library().ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, code))
+    lib = load_library()
+    if ngroups == 1:
+        return int(lib.ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, code))
+    return int(lib.ssm_scan_workspace_bytes_grouped(batch, dim, seqlen, dstate, ngroups, code))
+
+
+def _bc_groups(B: torch.Tensor, C: torch.Tensor, lead: tuple, N: int, tail: tuple, fn: str) -> int:
+    """Number of channel groups of B and C: shaped lead + (N,) + tail for one
+    group, lead + (ngroups, N) + tail for several.  The device buffers are read
+    over exactly that extent, so any other shape is rejected here."""
+    G = 1 if B.dim() == len(lead) + 1 + len(tail) else int(B.shape[len(lead)]) if B.dim() > len(lead) else 0
+    want = (*lead, N, *tail) if B.dim() == len(lead) + 1 + len(tail) else (*lead, G, N, *tail)
+    if G <= 0 or tuple(B.shape) != want or tuple(C.shape) != want:
+        raise ValueError(f"{fn}: B and C must be {(*lead, N, *tail)} or {(*lead, 'ngroups', N, *tail)}, "
+                         f"got {tuple(B.shape)} and {tuple(C.shape)}")
+    return G
 
 
 def device_error(clear: bool = True) -> int:
@@ -141,7 +170,9 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                  initial_state: Optional[torch.Tensor] = None) -> Tuple[torch.Tensor, Optional[torch.Tensor]]:
     """Selective scan over (batch, L, dim) activations; see ssm_scan.h.
 
-    B, C: (batch, dstate, L); A: (dim, dstate) f32; D, delta_bias: (dim,) f32.
+    B, C: (batch, dstate, L), or (batch, ngroups, dstate, L) for B and C per
+    channel group (channel d reads group d // (dim // ngroups);
+    ssm_scan_fwd_grouped); A: (dim, dstate) f32; D, delta_bias: (dim,) f32.
     Returns (out, last_state); last_state is (batch, dim, dstate) f32 when
     requested (pass a buffer or set return_last_state).  ``workspace`` is a
     uint8 CUDA tensor of at least scan_workspace_bytes(...) bytes; when None
@@ -154,16 +185,28 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
     dev = u.device
     bt, L, dim = u.shape
     N = A.shape[1]
+    G = _bc_groups(B, C, (bt,), N, (L,), "ssm_scan_fwd")
     if out is None:
         out = torch.empty_like(u)
     if last_state is None and return_last_state:
         last_state = torch.empty((bt, dim, N), dtype=torch.float32, device=dev)
     if workspace is None:
-        nbytes = scan_workspace_bytes(bt, dim, L, N, dt)
+        nbytes = scan_workspace_bytes(bt, dim, L, N, dt, G)
         workspace = torch.empty(max(nbytes, 16), dtype=torch.uint8, device=dev) if nbytes > 0 else None
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    if initial_state is not None and tuple(initial_state.shape) != (bt, dim, N):
+        raise ValueError(f"initial_state must be {(bt, dim, N)}, got {tuple(initial_state.shape)}")
     with torch.cuda.device(dev):
-        if initial_state is None:
+        if G != 1:
+            code = lib.ssm_scan_fwd_grouped(
+                _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
+                _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev),
+                _ptr(delta_bias, torch.float32, dev), int(bool(softplus)),
+                _ptr(initial_state, torch.float32, dev), _ptr(out, dt, dev),
+                _ptr(last_state, torch.float32, dev), bt, dim, L, N, G, _dtype_code(u),
+                _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+            _check("ssm_scan_fwd_grouped", code)
+        elif initial_state is None:
             code = lib.ssm_scan_fwd(_ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev),
                                     _ptr(B, dt, dev), _ptr(C, dt, dev), _ptr(D, torch.float32, dev),
                                     _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
@@ -172,8 +215,6 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                                     _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
             _check("ssm_scan_fwd", code)
         else:
-            if tuple(initial_state.shape) != (bt, dim, N):
-                raise ValueError(f"initial_state must be {(bt, dim, N)}, got {tuple(initial_state.shape)}")
             code = lib.ssm_scan_fwd_from_state(
                 _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
                 _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev),
@@ -190,14 +231,17 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                  softplus: bool, dout: torch.Tensor, workspace: Optional[torch.Tensor] = None) -> dict:
     """Gradients of the scan (from h = 0) given dout; see ssm_scan.h.  Returns a
     dict du, ddelta, dz (activation dtype; dz None without z), dA, dB, dC, dD,
-    ddelta_bias (float32; None without D / bias)."""
+    ddelta_bias (float32; None without D / bias).  B, C may be grouped as in
+    ssm_scan_fwd; dB, dC then have their shape (ssm_scan_bwd_grouped)."""
     lib = load_library()
     dt, dev = u.dtype, u.device
     bt, L, dim = u.shape
     N = A.shape[1]
+    G = _bc_groups(B, C, (bt,), N, (L,), "ssm_scan_bwd")
     f32 = dict(dtype=torch.float32, device=dev)
     g = dict(du=torch.empty_like(u), ddelta=torch.empty_like(u), dz=None if z is None else torch.empty_like(u),
-             dA=torch.empty(dim, N, **f32), dB=torch.empty(bt, N, L, **f32), dC=torch.empty(bt, N, L, **f32),
+             dA=torch.empty(dim, N, **f32), dB=torch.empty(tuple(B.shape), **f32),
+             dC=torch.empty(tuple(C.shape), **f32),
              dD=None if D is None else torch.empty(dim, **f32),
              ddelta_bias=None if delta_bias is None else torch.empty(dim, **f32))
     if workspace is None:
@@ -207,14 +251,14 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
     with torch.cuda.device(dev):
-        code = lib.ssm_scan_bwd(
+        code = lib.ssm_scan_bwd_grouped(
             _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
             _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
             int(bool(softplus)), _ptr(dout, dt, dev), _ptr(g["du"], dt, dev), _ptr(g["ddelta"], dt, dev),
             _ptr(g["dA"], torch.float32, dev), _ptr(g["dB"], torch.float32, dev), _ptr(g["dC"], torch.float32, dev),
             _ptr(g["dD"], torch.float32, dev), _ptr(g["dz"], dt, dev), _ptr(g["ddelta_bias"], torch.float32, dev),
-            bt, dim, L, N, _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
-    _check("ssm_scan_bwd", code)
+            bt, dim, L, N, G, _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+    _check("ssm_scan_bwd_grouped" if G != 1 else "ssm_scan_bwd", code)
     return g
 
 
@@ -267,19 +311,22 @@ def ssm_state_update(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: 
                      dt_softplus: bool = True, out: Optional[torch.Tensor] = None) -> torch.Tensor:
     """One decode step, in place on ``state`` (batch, dim, dstate) f32; see ssm_scan.h.
 
-    x, dt, z: (batch, dim); B, C: (batch, dstate).  Returns out (batch, dim).
+    x, dt, z: (batch, dim); B, C: (batch, dstate), or (batch, ngroups, dstate)
+    for B and C per channel group (ssm_state_update_grouped).  Returns out
+    (batch, dim).
     """
     lib = load_library()
     ty = x.dtype
     dev = x.device
     bt, dim, N = state.shape
+    G = _bc_groups(B, C, (bt,), N, (), "ssm_state_update")
     if out is None:
         out = torch.empty_like(x)
     with torch.cuda.device(dev):
-        code = lib.ssm_state_update(_ptr(state, torch.float32, dev), _ptr(x, ty, dev), _ptr(dt, ty, dev),
-                                    _ptr(A, torch.float32, dev), _ptr(B, ty, dev), _ptr(C, ty, dev),
-                                    _ptr(D, torch.float32, dev), _ptr(z, ty, dev),
-                                    _ptr(dt_bias, torch.float32, dev), _ptr(out, ty, dev),
-                                    bt, dim, N, int(bool(dt_softplus)), _dtype_code(x), _stream(dev))
-    _check("ssm_state_update", code)
+        code = lib.ssm_state_update_grouped(_ptr(state, torch.float32, dev), _ptr(x, ty, dev), _ptr(dt, ty, dev),
+                                            _ptr(A, torch.float32, dev), _ptr(B, ty, dev), _ptr(C, ty, dev),
+                                            _ptr(D, torch.float32, dev), _ptr(z, ty, dev),
+                                            _ptr(dt_bias, torch.float32, dev), _ptr(out, ty, dev),
+                                            bt, dim, N, G, int(bool(dt_softplus)), _dtype_code(x), _stream(dev))
+    _check("ssm_state_update_grouped" if G != 1 else "ssm_state_update", code)
     return out

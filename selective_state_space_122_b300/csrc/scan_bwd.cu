@@ -138,9 +138,18 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
     const int g = lane % R;                       // states 4g .. 4g+3
     const int cl = warp * CPW + lane / R;         // channel within the CTA
     const int64_t b = blockIdx.y;
-    const int64_t d0 = (int64_t)blockIdx.x * CC;
+    // CTA -> (B/C group, block of CC channels within it): the CTAs of a group
+    // cover its channels [grp * gch, dend) only, so every CTA reads and adds
+    // to one B/C block
+    // (channel indices stay below 2^31: the host rejects larger dims)
+    const int gch = (int)p.gch;
+    const int bpg = (gch + CC - 1) / CC;
+    const int grp = (int)blockIdx.x / bpg;
+    const int d0 = grp * gch + ((int)blockIdx.x - grp * bpg) * CC;
+    const int dend = d0 + min(CC, (grp + 1) * gch - d0);
+    const int64_t blk = b * p.ngroups + grp;
     const int64_t d = d0 + cl;
-    const bool ch_ok = d < p.dim;
+    const bool ch_ok = d < dend;
     const int64_t L = p.seqlen, dim = p.dim;
     const int64_t nch = (L + K - 1) / K;
     float An[G];
@@ -166,7 +175,7 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
             const int i = tid + q * kBwdThreads;
             const int k = i / CC, cc = i % CC;
             const int64_t t = t0 + k, dd = d0 + cc;
-            const bool ok = i < K * CC && t < L && dd < dim;
+            const bool ok = i < K * CC && t < L && dd < dend;
             const int64_t gi = (b * L + t) * dim + dd;
             r.ok[q] = ok;
             r.xr[q] = ok ? bw_ld(dr, gi) + (p.delta_bias ? p.delta_bias[dd] : 0.f) : 0.f;
@@ -180,8 +189,8 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
             const int nn = i / K, k = i % K;
             const int64_t t = t0 + k;
             const bool ok = i < N * K && t < L;
-            r.Bv[q] = ok ? bw_ld(Bg, (b * N + nn) * L + t) : 0.f;
-            r.Cv[q] = (backward && ok) ? bw_ld(Cg, (b * N + nn) * L + t) : 0.f;
+            r.Bv[q] = ok ? bw_ld(Bg, (blk * N + nn) * L + t) : 0.f;
+            r.Cv[q] = (backward && ok) ? bw_ld(Cg, (blk * N + nn) * L + t) : 0.f;
         }
     };
     auto commit = [&](const Pre& r, bool backward) {
@@ -303,7 +312,7 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         for (int i = tid; i < K * CC; i += kBwdThreads) {
             const int k = i / CC, cc = i % CC;
             const int64_t t = t0 + k, dd = d0 + cc;
-            if (t >= L || dd >= dim) continue;
+            if (t >= L || dd >= dend) continue;
             const int64_t gi = (b * L + t) * dim + dd;
             const float ddl = s_dd[i];
             const float dx = p.softplus ? ddl * bw_sigmoid(s_x[i]) : ddl;
@@ -335,7 +344,7 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
                     const float4 v = reinterpret_cast<const float4*>(s_P + ((size_t)k * kBwdThreads + ln) * 8)[which];
                     acc.x += v.x; acc.y += v.y; acc.z += v.z; acc.w += v.w;
                 }
-                float* dst = (which ? p.dB : p.dC) + (b * N + G * gq) * L + t;
+                float* dst = (which ? p.dB : p.dC) + (blk * N + G * gq) * L + t;
                 atomicAdd(dst, acc.x);
                 atomicAdd(dst + L, acc.y);
                 atomicAdd(dst + 2 * L, acc.z);
@@ -352,7 +361,7 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         atomicAdd(da + 3, dA23.y);
     }
     for (int i = tid; i < CC; i += kBwdThreads) {
-        if (d0 + i >= dim) continue;
+        if (d0 + i >= dend) continue;
         if (p.dD) atomicAdd(p.dD + d0 + i, s_dDc[i]);
         if (p.dbias) atomicAdd(p.dbias + d0 + i, s_dbc[i]);
     }
@@ -371,7 +380,9 @@ cudaError_t launch_bwd_t(const BwdArgs& a, float* ckpt, int sms, cudaStream_t s)
         if (e != cudaSuccess) return e;
         attr = true;
     }
-    dim3 grid((unsigned)((a.dim + CF::CC - 1) / CF::CC), (unsigned)a.batch);
+    const int64_t gx = a.ngroups * ((a.gch + CF::CC - 1) / CF::CC);
+    if (gx > 0x7fffffff) return cudaErrorInvalidValue;
+    dim3 grid((unsigned)gx, (unsigned)a.batch);
     // with every register a thread, about two CTAs fit an SM
     if ((int64_t)grid.x * grid.y > 2 * (int64_t)sms)
         scan_bwd_kernel<T, N, true><<<grid, kBwdThreads, CF::SMEM, s>>>(a, ckpt);
@@ -391,8 +402,8 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms
     // the accumulated gradients start from zero
     const int64_t N = a.dstate;
     cudaError_t e = cudaMemsetAsync(a.dA, 0, a.dim * N * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(a.dB, 0, a.batch * N * a.seqlen * 4, s);
-    if (e == cudaSuccess) e = cudaMemsetAsync(a.dC, 0, a.batch * N * a.seqlen * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dB, 0, a.batch * a.ngroups * N * a.seqlen * 4, s);
+    if (e == cudaSuccess) e = cudaMemsetAsync(a.dC, 0, a.batch * a.ngroups * N * a.seqlen * 4, s);
     if (e == cudaSuccess && a.dD) e = cudaMemsetAsync(a.dD, 0, a.dim * 4, s);
     if (e == cudaSuccess && a.dbias) e = cudaMemsetAsync(a.dbias, 0, a.dim * 4, s);
     if (e != cudaSuccess) return e;

@@ -93,6 +93,8 @@ struct Cfg {
 struct Geo {
     int vec_x;   // u/delta/z/out rows allow paired (2-element) accesses
     int vec_bc;  // B/C rows allow 16-byte accesses
+    int64_t bpg; // CTAs per channel group (B/C block): the CTAs of a group
+                 // cover its channels only, so every CTA reads one B/C block
 };
 
 template <typename T>
@@ -113,7 +115,9 @@ struct Pair<float> {
 __device__ __forceinline__ float4 ld4(const float* p) { return *reinterpret_cast<const float4*>(p); }
 __device__ __forceinline__ void st4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
 
-template <typename CF, typename T, bool kFast>
+// kGrouped: B and C per channel group (the CTAs of a group cover its channels
+// only); without it the CTA's channels are a plain block of the row.
+template <typename CF, typename T, bool kFast, bool kGrouped>
 struct ScanKernel {
     using PT = typename Pair<T>::type;
     static constexpr int N = CF::N, G = CF::G, R = CF::R, CW = CF::CW, K = CF::K;
@@ -134,19 +138,21 @@ struct ScanKernel {
         bool ok0, ok1;
     };
 
+    // channels [.., dend) of row `row` (row stride dim)
     static __device__ __forceinline__ PT load_pair(const T* base, int64_t row, int64_t d, int64_t dim,
-                                                   int64_t L, bool vec) {
-        if (row < L && d + 1 < dim && vec) return *reinterpret_cast<const PT*>(base + row * dim + d);
+                                                   int64_t dend, int64_t L, bool vec) {
+        if (row < L && d + 1 < dend && vec) return *reinterpret_cast<const PT*>(base + row * dim + d);
         float a = 0.f, b = 0.f;
         if (row < L) {
-            if (d < dim) a = to_f32(base[row * dim + d]);
-            if (d + 1 < dim) b = to_f32(base[row * dim + d + 1]);
+            if (d < dend) a = to_f32(base[row * dim + d]);
+            if (d + 1 < dend) b = to_f32(base[row * dim + d + 1]);
         }
         return Pair<T>::make(a, b);
     }
 
+    // blk: the B/C block (batch row * ngroups + group) of the CTA's channels
     static __device__ __forceinline__ void fetch(Regs& r, const ScanArgs& p, const Geo& geo, int64_t b,
-                                                 int64_t d0, int64_t t0, int tid) {
+                                                 int64_t blk, int64_t d0, int64_t dend, int64_t t0, int tid) {
         const int64_t L = p.seqlen, dim = p.dim;
         const T* u = static_cast<const T*>(p.u) + b * L * dim;
         const T* dl = static_cast<const T*>(p.delta) + b * L * dim;
@@ -157,13 +163,13 @@ struct ScanKernel {
             if (CF::PAIRS % THREADS == 0 || idx < CF::PAIRS) {
                 const int t = idx / (CW / 2), cp = idx % (CW / 2);
                 const int64_t row = t0 + t, d = d0 + 2 * cp;
-                r.u[k] = load_pair(u, row, d, dim, L, geo.vec_x);
-                r.dl[k] = load_pair(dl, row, d, dim, L, geo.vec_x);
-                r.z[k] = zp ? load_pair(zp, row, d, dim, L, geo.vec_x) : Pair<T>::make(0.f, 0.f);
+                r.u[k] = load_pair(u, row, d, dim, dend, L, geo.vec_x);
+                r.dl[k] = load_pair(dl, row, d, dim, dend, L, geo.vec_x);
+                r.z[k] = zp ? load_pair(zp, row, d, dim, dend, L, geo.vec_x) : Pair<T>::make(0.f, 0.f);
             }
         }
-        const T* Bb = static_cast<const T*>(p.B) + b * N * L;
-        const T* Cb = static_cast<const T*>(p.C) + b * N * L;
+        const T* Bb = static_cast<const T*>(p.B) + blk * N * L;
+        const T* Cb = static_cast<const T*>(p.C) + blk * N * L;
 #pragma unroll
         for (int k = 0; k < CF::BCV_PT; ++k) {
             const int idx = tid + k * THREADS;
@@ -241,7 +247,7 @@ struct ScanKernel {
 
     // ---- out tile (shared) -> global, pairs of channels per access
     static __device__ __forceinline__ void store_out(const float* sm, const ScanArgs& p, const Geo& geo,
-                                                     int64_t b, int64_t d0, int64_t t0, int tid) {
+                                                     int64_t b, int64_t d0, int64_t dend, int64_t t0, int tid) {
         const T* s_out = reinterpret_cast<const T*>(sm + CF::OFF_OUT);
         T* out = static_cast<T*>(p.out) + b * p.seqlen * p.dim;
 #pragma unroll
@@ -252,12 +258,12 @@ struct ScanKernel {
                 const int64_t row = t0 + t, d = d0 + 2 * cp;
                 if (row < p.seqlen) {
                     const PT v = *reinterpret_cast<const PT*>(s_out + t * CW + 2 * cp);
-                    if (geo.vec_x && d + 1 < p.dim) {
+                    if (geo.vec_x && d + 1 < dend) {
                         *reinterpret_cast<PT*>(out + row * p.dim + d) = v;
                     } else {
                         const float2 f = Pair<T>::f(v);
-                        if (d < p.dim) out[row * p.dim + d] = from_f32<T>(f.x);
-                        if (d + 1 < p.dim) out[row * p.dim + d + 1] = from_f32<T>(f.y);
+                        if (d < dend) out[row * p.dim + d] = from_f32<T>(f.x);
+                        if (d + 1 < dend) out[row * p.dim + d + 1] = from_f32<T>(f.y);
                     }
                 }
             }
@@ -413,9 +419,23 @@ struct ScanKernel {
         const int g = lane % R;
         const int c = lane / R;
         const int64_t b = blockIdx.y;
-        const int64_t d0 = (int64_t)blockIdx.x * CW;
+        // CTA -> (channel group, block of CW channels within the group); the
+        // host keeps dim below 2^31, so channel indices fit 32 bits
+        int64_t d0, dend, blk;
+        if constexpr (kGrouped) {
+            const int gch = (int)p.gch, bpg = (int)geo.bpg;
+            const int grp = (int)blockIdx.x / bpg;
+            const int c0 = grp * gch + ((int)blockIdx.x - grp * bpg) * CW;
+            d0 = c0;
+            dend = c0 + min(CW, (grp + 1) * gch - c0);
+            blk = b * p.ngroups + grp;
+        } else {
+            d0 = (int64_t)blockIdx.x * CW;
+            dend = p.dim;
+            blk = b;
+        }
         const int64_t d = d0 + c;
-        const bool valid = d < p.dim;
+        const bool valid = d < dend;
         const int64_t L = p.seqlen;
         const int64_t nchunks = (L + TC - 1) / TC;
 
@@ -432,8 +452,8 @@ struct ScanKernel {
         {
             const int cp = tid % (CW / 2);
             const int64_t dp = d0 + 2 * cp;
-            pc.ok0 = dp < p.dim;
-            pc.ok1 = dp + 1 < p.dim;
+            pc.ok0 = dp < dend;
+            pc.ok1 = dp + 1 < dend;
             pc.bias = make_float2((p.delta_bias && pc.ok0) ? p.delta_bias[dp] : 0.f,
                                   (p.delta_bias && pc.ok1) ? p.delta_bias[dp + 1] : 0.f);
             pc.dsk = make_float2((p.D && pc.ok0) ? p.D[dp] : 0.f, (p.D && pc.ok1) ? p.D[dp + 1] : 0.f);
@@ -450,14 +470,14 @@ struct ScanKernel {
             float* s_car = sm + CF::OFF_CAR;
             for (int i = tid; i < CW * N; i += THREADS) {
                 const int64_t dc = d0 + i / N;
-                s_car[i] = (p.h0 && dc < p.dim) ? p.h0[(b * p.dim + dc) * N + i % N] : 0.f;
+                s_car[i] = (p.h0 && dc < dend) ? p.h0[(b * p.dim + dc) * N + i % N] : 0.f;
             }
         }
 
         Regs rg;
-        fetch(rg, p, geo, b, d0, 0, tid);
+        fetch(rg, p, geo, b, blk, d0, dend, 0, tid);
         prologue(rg, pc, sm, p, 0, tid);
-        if (nchunks > 1) fetch(rg, p, geo, b, d0, TC, tid);
+        if (nchunks > 1) fetch(rg, p, geo, b, blk, d0, dend, TC, tid);
         __syncthreads();
 
         for (int64_t ch = 0; ch < nchunks; ++ch) {
@@ -510,10 +530,10 @@ struct ScanKernel {
             reduce_level<R / 2, K>(v, g);
             write_y(v, sm, (CF::kSplit ? warp * K : 0) + g * KR, c);
             __syncthreads();
-            store_out(sm, p, geo, b, d0, ch * TC, tid);
+            store_out(sm, p, geo, b, d0, dend, ch * TC, tid);
             if (ch + 1 < nchunks) {
                 prologue(rg, pc, sm, p, (ch + 1) * TC, tid);
-                if (ch + 2 < nchunks) fetch(rg, p, geo, b, d0, (ch + 2) * TC, tid);
+                if (ch + 2 < nchunks) fetch(rg, p, geo, b, blk, d0, dend, (ch + 2) * TC, tid);
             }
             __syncthreads();
         }
@@ -536,34 +556,39 @@ struct ScanKernel {
     }
 };
 
-template <typename CF, typename T, bool kFast>
+template <typename CF, typename T, bool kFast, bool kGrouped>
 __global__ void __launch_bounds__(CF::THREADS) scan_fwd_kernel(ScanArgs p, Geo geo) {
-    ScanKernel<CF, T, kFast>::run(p, geo);
+    ScanKernel<CF, T, kFast, kGrouped>::run(p, geo);
 }
 
 template <typename T, int N, int G, int S, int K>
 cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t s) {
     using CF = Cfg<T, N, G, S, K>;
     constexpr bool kFast = !std::is_same<T, float>::value;
-    auto kern = scan_fwd_kernel<CF, T, kFast>;
+    auto kern = a.ngroups == 1 ? scan_fwd_kernel<CF, T, kFast, false> : scan_fwd_kernel<CF, T, kFast, true>;
     if (CF::SMEM_BYTES > 48 * 1024) {
-        static bool attr_set = false;  // once per instantiation
-        if (!attr_set) {
+        static bool attr_set[2] = {false, false};  // once per kernel instantiation
+        const int gi = a.ngroups == 1 ? 0 : 1;
+        if (!attr_set[gi]) {
             const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                                        (int)CF::SMEM_BYTES);
             if (e != cudaSuccess) return e;
-            attr_set = true;
+            attr_set[gi] = true;
         }
     }
     const size_t es = sizeof(T);
     Geo geo;
-    geo.vec_x = (a.dim % 2 == 0) && (reinterpret_cast<uintptr_t>(a.u) % (2 * es) == 0) &&
+    // paired accesses need even channel indices: an even row length and,
+    // with groups, an even group size (every CTA starts at a group boundary)
+    geo.vec_x = (a.dim % 2 == 0) && (a.gch % 2 == 0) && (reinterpret_cast<uintptr_t>(a.u) % (2 * es) == 0) &&
                 (reinterpret_cast<uintptr_t>(a.delta) % (2 * es) == 0) &&
                 (!a.z || reinterpret_cast<uintptr_t>(a.z) % (2 * es) == 0) &&
                 (reinterpret_cast<uintptr_t>(a.out) % (2 * es) == 0);
     geo.vec_bc = (a.seqlen % CF::V == 0) && (reinterpret_cast<uintptr_t>(a.B) % 16 == 0) &&
                  (reinterpret_cast<uintptr_t>(a.C) % 16 == 0);
-    const int64_t gx = (a.dim + CF::CW - 1) / CF::CW;
+    geo.bpg = (a.gch + CF::CW - 1) / CF::CW;
+    const int64_t gx = a.ngroups * geo.bpg;
+    if (gx > 0x7fffffff) return cudaErrorInvalidValue;
     dim3 grid((unsigned)gx, (unsigned)a.batch);
     kern<<<grid, CF::THREADS, CF::SMEM_BYTES, s>>>(a, geo);
     return cudaGetLastError();

@@ -107,13 +107,14 @@ struct RelayParams {
     const float* A;
     const float* D;
     const float* delta_bias;
-    const float* bc;        // staged B|C, [batch][lpad][2N] f32
+    const float* bc;        // staged B|C, [batch * ngroups][lpad][2N] f32
     float* last_state;
     int dim, seqlen;
     int64_t lpad;
     int softplus;
     int has_z;
     const float* h0;        // initial state or null
+    int ngroups, gch;       // B/C groups, channels a group (a multiple of CW)
 };
 
 
@@ -171,7 +172,7 @@ scan_relay_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
     }
     const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
     const float2 dskip2 = splat2((p.D && ch_ok) ? p.D[d] : 0.f);
-    const float* bc_b = p.bc + (size_t)b * p.lpad * (2 * N);
+    const float* bc_b = p.bc + ((size_t)b * p.ngroups + (size_t)(d0 / p.gch)) * p.lpad * (2 * N);
     constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
     const uint32_t ring_s = smem_u32(ring);
 
@@ -422,7 +423,7 @@ struct SegParams {
     const float* A;
     const float* D;
     const float* delta_bias;
-    const void* bc;         // staged B|C, [batch][lpad][2N] in the activation type
+    const void* bc;         // staged B|C, [batch * ngroups][lpad][2N] in the activation type
     float* last_state;
     float* seg_state;       // [M][CW][N] f32: state handed between segments
     int* seg_flag;          // [M]: number of finished segments of each chain
@@ -434,6 +435,7 @@ struct SegParams {
     int cps;                // chunks per segment
     int workers;            // (main, helper) pairs in the grid
     const float* h0;        // initial state (batch, dim, N) or null
+    int ngroups, gch;       // B/C groups, channels a group (a multiple of CW)
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -522,7 +524,8 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             pf_d0 = (m - pf_b * p.units) * CW;
             pf_c = sgm * p.cps;
             pf_end = min(pf_c + p.cps, nch);
-            pf_bc = static_cast<const T*>(p.bc) + ((size_t)pf_b * p.lpad + (size_t)pf_c * K) * (2 * N);
+            const size_t blk = (size_t)pf_b * p.ngroups + (size_t)(pf_d0 / p.gch);
+            pf_bc = static_cast<const T*>(p.bc) + (blk * p.lpad + (size_t)pf_c * K) * (2 * N);
         };
         if (pf_task < T_total) pf_enter(pf_task);
         auto issue_next = [&]() {   // lane 0 only
@@ -787,7 +790,8 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 
 // B and C (batch, N, L) -> staged rows [batch][lpad][B_0..B_{N-1}, C_0..C_{N-1}] of
 // type O (float32 for the relay kernel; the activation type for the segmented
-// kernel, so that its per-step reads move half the bytes), zero beyond L.  One CTA per (64-step tile, batch row), transposed through shared memory.
+// kernel, so that its per-step reads move half the bytes), zero beyond L.  One CTA per (64-step tile, B/C block:
+// batch row, or batch row and channel group), transposed through shared memory.
 template <typename T, int N, typename O = float>
 __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, const T* __restrict__ C,
                                                        O* __restrict__ bc, int64_t L, int64_t lpad,
@@ -852,7 +856,7 @@ cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
     const int64_t lpad = relay_lpad(a.seqlen);
     float* bc = static_cast<float*>(ws);
     {
-        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)a.batch);
+        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)(a.batch * a.ngroups));
         bc_stage_kernel<T, N><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
                                                    a.seqlen, lpad, nullptr, 0);
     }
@@ -863,7 +867,7 @@ cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
         !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
         return cudaErrorInvalidValue;
     RelayParams rp{a.A, a.D, a.delta_bias, bc, a.last_state, (int)a.dim, (int)a.seqlen, lpad, a.softplus,
-                   a.z != nullptr, a.h0};
+                   a.z != nullptr, a.h0, (int)a.ngroups, (int)a.gch};
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, RelayParams);
     static const Kern kerns[4] = {scan_relay_kernel<T, N, kFast, false, false>,
                                   scan_relay_kernel<T, N, kFast, false, true>,
@@ -953,12 +957,12 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     T* bc = reinterpret_cast<T*>(w);
-    const int64_t bc_bytes = (a.batch * lpad * 2 * N * (int64_t)sizeof(T) + 255) / 256 * 256;
+    const int64_t bc_bytes = (a.batch * a.ngroups * lpad * 2 * N * (int64_t)sizeof(T) + 255) / 256 * 256;
     float* st = reinterpret_cast<float*>(w + bc_bytes);
     const int64_t st_bytes = ((int64_t)pl.M * CF::CW * N * 4 + 255) / 256 * 256;
     int* flags = reinterpret_cast<int*>(w + bc_bytes + st_bytes);
     {
-        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)a.batch);
+        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)(a.batch * a.ngroups));
         bc_stage_kernel<T, N, T><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
                                                       a.seqlen, lpad, flags, pl.M);
     }
@@ -969,7 +973,7 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
         return cudaErrorInvalidValue;
     SegParams sp{a.A, a.D, a.delta_bias, bc, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                 pl.units, pl.M, pl.S, pl.cps, pl.workers, a.h0};
+                 pl.units, pl.M, pl.S, pl.cps, pl.workers, a.h0, (int)a.ngroups, (int)a.gch};
     void* args[] = {&mu, &md, &mz, &mo, &sp};
     // Segments wait on segments of other warps: every CTA must be resident,
     // which the cooperative launch guarantees (the grid never exceeds the
@@ -980,11 +984,12 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
 
 }  // namespace
 
-int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes) {
+int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes,
+                            int64_t ngroups) {
     const int cw = 32 / (dstate / 4);
     const int64_t units = (dim + cw - 1) / cw;
     const int64_t M = batch * units;
-    const int64_t bc_bytes = (batch * relay_lpad(seqlen) * 2 * dstate * elem_bytes + 255) / 256 * 256;
+    const int64_t bc_bytes = (batch * ngroups * relay_lpad(seqlen) * 2 * dstate * elem_bytes + 255) / 256 * 256;
     const int64_t st_bytes = (M * cw * dstate * 4 + 255) / 256 * 256;
     return bc_bytes + st_bytes + (M * 4 + 255) / 256 * 256;
 }
@@ -1008,8 +1013,8 @@ cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* ws, int sms, cuda
 
 int64_t relay_lpad(int64_t seqlen) { return (seqlen + 63) / 64 * 64; }
 
-int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate) {
-    return batch * relay_lpad(seqlen) * 2 * dstate * (int64_t)sizeof(float);
+int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate, int64_t ngroups) {
+    return batch * ngroups * relay_lpad(seqlen) * 2 * dstate * (int64_t)sizeof(float);
 }
 
 bool relay_supported(const ScanArgs& a, DType dt) {
@@ -1020,6 +1025,9 @@ bool relay_supported(const ScanArgs& a, DType dt) {
         return false;
     if ((a.dim * es) % 16 != 0) return false;
     if (a.dim > (int64_t(1) << 31) - 64 || a.seqlen > (int64_t(1) << 31) - 64 || a.batch > 65535) return false;
+    // B/C groups: the staging grid has one row per (batch row, group), and
+    // every CTA or warp's block of 32 / (N / 4) channels lies in one group
+    if (a.ngroups != 1 && (a.batch * a.ngroups > 65535 || a.gch % (32 / (a.dstate / 4)) != 0)) return false;
     if (a.dim * a.seqlen * es >= (int64_t(1) << 40)) return false;
     return encode_fn() != nullptr;
 }

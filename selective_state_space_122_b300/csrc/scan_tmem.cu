@@ -183,7 +183,7 @@ struct TmParams {
     const float* A;
     const float* D;
     const float* delta_bias;
-    const float* xop;       // staged X operands, [batch][lpad / K][K][8][4] f32
+    const float* xop;       // staged X operands, [batch * ngroups][lpad / K][K][8][4] f32
     float* last_state;
     float* seg_state;       // [M * WARPS][CW][N] f32: state handed between segments
     int* seg_flag;          // [M * WARPS]: finished segments of each warp's channel group
@@ -195,6 +195,7 @@ struct TmParams {
     int cps;                // chunks per segment
     int workers;            // CTAs in the grid
     const float* h0;        // initial state (batch, dim, N) or null
+    int ngroups, gch;       // B/C groups, channels a group (a multiple of 32)
 };
 
 __device__ __forceinline__ int tm_ld_acquire(const int* p) {
@@ -225,11 +226,12 @@ __device__ __forceinline__ uint32_t swz(int x, int c) {
 // The chunks a CTA walks: its tasks (segment s of chain m, task = s * M + m,
 // every workers-th task from blockIdx.x), each a run of chunks.
 struct ChunkCursor {
-    int task, c, end, b, d0;
+    int task, c, end, b, d0, xb;   // xb: the B/C block (X operands) of the channels
     __device__ void enter(const TmParams& p, int nch, int cc) {
         const int sgm = task / p.M, m = task - sgm * p.M;
         b = m / p.units;
         d0 = (m - b * p.units) * cc;
+        xb = b * p.ngroups + d0 / p.gch;
         c = sgm * p.cps;
         end = min(c + p.cps, nch);
     }
@@ -332,7 +334,7 @@ scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant
                 tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
                 tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
                 if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
-                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.b * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
+                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.xb * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
                 ++cur.c;
                 ++issued;
             };
@@ -754,7 +756,7 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                 tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
                 tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
                 if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
-                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.b * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
+                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.xb * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
                 ++cur.c;
                 ++issued;
             };
@@ -1163,13 +1165,13 @@ cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) 
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
-    const int64_t x_bytes = (a.batch * lpad * 32 * 4 + 255) / 256 * 256;
+    const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
     const int64_t chains = (int64_t)pl.M * CF::WARPS;
     float* st = reinterpret_cast<float*>(w + x_bytes);
     const int64_t st_bytes = (chains * CF::CW * N * 4 + 255) / 256 * 256;
     int* flags = reinterpret_cast<int*>(w + x_bytes + st_bytes);
     {
-        dim3 grid((unsigned)(lpad / 64), (unsigned)a.batch);
+        dim3 grid((unsigned)(lpad / 64), (unsigned)(a.batch * a.ngroups));
         tm_stage_kernel<N><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.B),
                                                 static_cast<const __nv_bfloat16*>(a.C), xop, (int)a.seqlen, lpad,
                                                 flags, (int)chains);
@@ -1182,7 +1184,7 @@ cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) 
         !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw))
         return cudaErrorInvalidValue;
     TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0};
+                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0, (int)a.ngroups, (int)a.gch};
     void* args[] = {&mu, &md, &mz, &mo, &tp};
     // Segments wait on segments of other CTAs: every CTA must be resident,
     // which the cooperative launch guarantees (one CTA per SM, grid <= SMs).
@@ -1237,13 +1239,13 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
-    const int64_t x_bytes = (a.batch * lpad * 32 * 4 + 255) / 256 * 256;
+    const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
     const int64_t chains = (int64_t)pl.M * CF::WARPS;
     float* st = reinterpret_cast<float*>(w + x_bytes);
     const int64_t st_bytes = (chains * CF::CW * CF::N * 4 + 255) / 256 * 256;
     int* flags = reinterpret_cast<int*>(w + x_bytes + st_bytes);
     {
-        dim3 grid((unsigned)(lpad / 64), (unsigned)a.batch);
+        dim3 grid((unsigned)(lpad / 64), (unsigned)(a.batch * a.ngroups));
         tm2_stage_kernel<<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.B),
                                               static_cast<const __nv_bfloat16*>(a.C), xop, (int)a.seqlen, lpad, flags,
                                               (int)chains);
@@ -1255,7 +1257,7 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B))
         return cudaErrorInvalidValue;
     TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0};
+                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0, (int)a.ngroups, (int)a.gch};
     void* args[] = {&mu, &md, &mz, &mo, &tp};
     return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
                                        dim3(CF::THREADS), args, CF::SMEM, s);
@@ -1266,16 +1268,19 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
 bool tmem_supported(const ScanArgs& a, DType dt) {
     if (dt != DType::BF16 || a.dstate != 16) return false;
     if (!relay_supported(a, dt)) return false;
+    // B/C groups: every CTA's 32 channels lie in one group
+    if (a.ngroups != 1 && a.gch % 32 != 0) return false;
     // the total task count (chains * 64 segments) stays a 32-bit int
     return a.batch * ((a.dim + 31) / 32) * 64 < (int64_t(1) << 31);
 }
 
-int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate) {
+int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int64_t ngroups) {
     if (dstate != 16) return 0;
-    // both variants: staged operands, one f32 state per (channel, state) of
-    // every 32-channel group, and one flag per consumer warp of each group
+    // both variants: staged operands (per B/C block), one f32 state per
+    // (channel, state) of every 32-channel group, and one flag per consumer
+    // warp of each group
     const int64_t groups = batch * ((dim + 31) / 32);
-    const int64_t x_bytes = (batch * relay_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
+    const int64_t x_bytes = (batch * ngroups * relay_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
     const int64_t st_bytes = (groups * 32 * 16 * 4 + 255) / 256 * 256;
     return x_bytes + st_bytes + (groups * 8 * 4 + 255) / 256 * 256;
 }

@@ -122,15 +122,22 @@ const char* ssm_last_launch_error(void) {
     return t_last_launch == cudaSuccess ? "no launch error" : cudaGetErrorString(t_last_launch);
 }
 
-int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
+int64_t ssm_scan_workspace_bytes_grouped(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                                         int64_t ngroups, int dtype) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
-    if (dim <= 0 || dim > (int64_t(1) << 31)) return -1;
+    if (dim <= 0 || dim >= (int64_t(1) << 31)) return -1;
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
-    int64_t need = std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate),
-                            ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4));
-    if (dtype == SSM_BF16) need = std::max(need, ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate));
+    if (ngroups <= 0 || dim % ngroups != 0) return -1;
+    int64_t need = std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate, ngroups),
+                            ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4,
+                                                     ngroups));
+    if (dtype == SSM_BF16) need = std::max(need, ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate, ngroups));
     return need;
+}
+
+int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
+    return ssm_scan_workspace_bytes_grouped(batch, dim, seqlen, dstate, 1, dtype);
 }
 
 int ssm_device_error(int clear) {
@@ -139,16 +146,17 @@ int ssm_device_error(int clear) {
     return (a < 0 || b < 0) ? -1 : (a | b);
 }
 
-ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A, const void* B,
-                                   const void* C, const float* D, const void* z, const float* delta_bias,
-                                   int softplus_flag, const float* initial_state, void* out, float* last_state,
-                                   int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype,
-                                   void* workspace, int64_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const float* initial_state, void* out, float* last_state, int64_t batch,
+                                int64_t dim, int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype,
+                                void* workspace, int64_t workspace_bytes, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (ngroups <= 0 || dim % ngroups != 0) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
-    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
     if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     const uintptr_t ea = (uintptr_t)es;
@@ -159,7 +167,7 @@ ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float
         return SSM_ERR_ALIGN;
 
     const int64_t x_bytes = batch * seqlen * dim * es;
-    const int64_t bc_bytes = batch * dstate * seqlen * es;
+    const int64_t bc_bytes = batch * ngroups * dstate * seqlen * es;
     const Span ins[] = {{u, x_bytes}, {delta, x_bytes}, {z, x_bytes}, {B, bc_bytes}, {C, bc_bytes},
                         {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4}};
     const Span so{out, x_bytes}, sl{last_state, batch * dim * dstate * 4};
@@ -190,6 +198,8 @@ ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float
 
     ssm::ScanArgs a{u, delta, A, B, C, D, z, delta_bias, out, last_state,
                     batch, dim, seqlen, (int)dstate, softplus_flag ? 1 : 0, initial_state};
+    a.ngroups = ngroups;
+    a.gch = dim / ngroups;
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The tensor-memory scan (two states per lane) runs whenever its
@@ -200,14 +210,14 @@ ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float
     const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
                          batch * ((dim + 127) / 128 * dstate) * 64 < (int64_t(1) << 31);
     if (force && std::strcmp(force, "relay") == 0) {
-        if (!fast_ok || workspace_bytes < ssm::relay_workspace_bytes(batch, seqlen, (int)dstate))
+        if (!fast_ok || workspace_bytes < ssm::relay_workspace_bytes(batch, seqlen, (int)dstate, ngroups))
             return SSM_ERR_UNSUPPORTED;
         return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
     }
     const bool want_generic = force && std::strcmp(force, "generic") == 0;
     const bool want_seg = force && std::strcmp(force, "seg") == 0;
     const bool tmem_ok = fast_ok && ssm::tmem_supported(a, dt) &&
-                         workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate);
+                         workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate, ngroups);
     if (force && (std::strcmp(force, "tmem") == 0 || std::strcmp(force, "tmem2") == 0)) {
         if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
         return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, force[4] == '2' ? 2 : 4));
@@ -215,12 +225,21 @@ ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float
     if (!want_generic && !want_seg && tmem_ok)
         return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 2));
     if (!want_generic && fast_ok &&
-        workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es)) {
+        workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es, ngroups)) {
         return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
     }
     if (want_seg) return SSM_ERR_UNSUPPORTED;
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
     return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
+}
+
+ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, const float* delta_bias,
+                                   int softplus_flag, const float* initial_state, void* out, float* last_state,
+                                   int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype,
+                                   void* workspace, int64_t workspace_bytes, void* stream) {
+    return ssm_scan_fwd_grouped(u, delta, A, B, C, D, z, delta_bias, softplus_flag, initial_state, out, last_state,
+                                batch, dim, seqlen, dstate, 1, dtype, workspace, workspace_bytes, stream);
 }
 
 ssm_status ssm_scan_fwd(const void* u, const void* delta, const float* A, const void* B,
@@ -239,7 +258,7 @@ ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
     if (!x || !weight || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || width <= 0) return SSM_ERR_SHAPE;
     if (width > 4) return SSM_ERR_UNSUPPORTED;
-    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
     if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 4) || (bias && !aligned(bias, 4)) ||
@@ -289,23 +308,25 @@ ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weig
 
 int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
-    if (batch <= 0 || dim <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || dim > (int64_t(1) << 31) ||
+    if (batch <= 0 || dim <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || dim >= (int64_t(1) << 31) ||
         seqlen > (int64_t(1) << 40))
         return -1;
     return std::max<int64_t>(16, ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate));
 }
 
-ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                        const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                        const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD,
-                        void* dz, float* ddelta_bias, int64_t batch, int64_t dim, int64_t seqlen,
-                        int64_t dstate, int dtype, void* workspace, int64_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                float* dD, void* dz, float* ddelta_bias, int64_t batch, int64_t dim,
+                                int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype, void* workspace,
+                                int64_t workspace_bytes, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC || !workspace)
         return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (ngroups <= 0 || dim % ngroups != 0) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
-    if (batch > 65535 || dim > (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
+    if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
     if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
     if (workspace_bytes < ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
@@ -316,11 +337,12 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
         !aligned(dB, 4) || !aligned(dC, 4) || (dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4)) ||
         !aligned(workspace, 16))
         return SSM_ERR_ALIGN;
-    const int64_t x_bytes = batch * seqlen * dim * es, bc_bytes = batch * dstate * seqlen * es;
+    const int64_t x_bytes = batch * seqlen * dim * es, bc_bytes = batch * ngroups * dstate * seqlen * es;
+    const int64_t gbc_bytes = batch * ngroups * dstate * seqlen * 4;
     const Span ins[] = {{u, x_bytes}, {delta, x_bytes}, {z, x_bytes}, {dout, x_bytes}, {B, bc_bytes},
                         {C, bc_bytes}, {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4}};
     const Span outs[] = {{du, x_bytes}, {ddelta, x_bytes}, {dz, x_bytes}, {dA, dim * dstate * 4},
-                         {dB, batch * dstate * seqlen * 4}, {dC, batch * dstate * seqlen * 4}, {dD, dim * 4},
+                         {dB, gbc_bytes}, {dC, gbc_bytes}, {dD, dim * 4},
                          {ddelta_bias, dim * 4}, {workspace, workspace_bytes}};
     for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
         for (const Span& s : ins)
@@ -333,17 +355,30 @@ ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const 
     ssm::BwdArgs a{u, delta, A, B, C, D, z, delta_bias, softplus_flag ? 1 : 0, dout, du, ddelta, dA, dB, dC,
                    D ? dD : nullptr, z ? dz : nullptr, delta_bias ? ddelta_bias : nullptr, batch, dim, seqlen,
                    (int)dstate};
+    a.ngroups = ngroups;
+    a.gch = dim / ngroups;
     return launch_status(ssm::launch_scan_bwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32, workspace,
                                               sms, static_cast<cudaStream_t>(stream)));
 }
 
-ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
-                            const void* B, const void* C, const float* D, const void* z,
-                            const float* dt_bias, void* out, int64_t batch, int64_t dim,
-                            int64_t dstate, int dt_softplus, int dtype, void* stream) {
+ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                        const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                        const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC, float* dD,
+                        void* dz, float* ddelta_bias, int64_t batch, int64_t dim, int64_t seqlen,
+                        int64_t dstate, int dtype, void* workspace, int64_t workspace_bytes, void* stream) {
+    return ssm_scan_bwd_grouped(u, delta, A, B, C, D, z, delta_bias, softplus_flag, dout, du, ddelta, dA, dB, dC,
+                                dD, dz, ddelta_bias, batch, dim, seqlen, dstate, 1, dtype, workspace,
+                                workspace_bytes, stream);
+}
+
+ssm_status ssm_state_update_grouped(float* state, const void* x, const void* dt, const float* A, const void* B,
+                                    const void* C, const float* D, const void* z, const float* dt_bias, void* out,
+                                    int64_t batch, int64_t dim, int64_t dstate, int64_t ngroups, int dt_softplus,
+                                    int dtype, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!state || !x || !dt || !A || !B || !C || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
+    if (ngroups <= 0 || dim % ngroups != 0 || dim >= (int64_t(1) << 31)) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
     if (batch * dim > kMaxElems / 16) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
@@ -353,7 +388,7 @@ ssm_status ssm_state_update(float* state, const void* x, const void* dt, const f
         (D && !aligned(D, 4)) || (dt_bias && !aligned(dt_bias, 4)))
         return SSM_ERR_ALIGN;
 
-    const int64_t tok = batch * dim * es, bc = batch * dstate * es;
+    const int64_t tok = batch * dim * es, bc = batch * ngroups * dstate * es;
     const Span ins[] = {{x, tok}, {dt, tok}, {z, tok}, {B, bc}, {C, bc},
                         {A, dim * dstate * 4}, {D, dim * 4}, {dt_bias, dim * 4}};
     const Span ss{state, batch * dim * dstate * 4}, so{out, tok};
@@ -366,8 +401,18 @@ ssm_status ssm_state_update(float* state, const void* x, const void* dt, const f
 
     ssm::UpdateArgs a{state, x, dt, A, B, C, D, z, dt_bias, out, batch, dim, (int)dstate,
                       dt_softplus ? 1 : 0};
+    a.ngroups = ngroups;
+    a.gch = dim / ngroups;
     return launch_status(ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
                                                   static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_state_update(float* state, const void* x, const void* dt, const float* A,
+                            const void* B, const void* C, const float* D, const void* z,
+                            const float* dt_bias, void* out, int64_t batch, int64_t dim,
+                            int64_t dstate, int dt_softplus, int dtype, void* stream) {
+    return ssm_state_update_grouped(state, x, dt, A, B, C, D, z, dt_bias, out, batch, dim, dstate, 1, dt_softplus,
+                                    dtype, stream);
 }
 
 }  // extern "C"

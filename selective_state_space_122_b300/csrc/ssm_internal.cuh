@@ -29,6 +29,10 @@ struct ScanArgs {
     int dstate;
     int softplus;
     const float* h0;        // initial state (batch, dim, dstate) f32, or null for zero
+    // B and C per channel group: (batch, ngroups, dstate, seqlen); channel d
+    // reads block b * ngroups + d / gch (gch = dim / ngroups channels a group)
+    int64_t ngroups = 1;
+    int64_t gch = 0;
 };
 
 // Arguments of one decode step; layouts as in ssm_scan.h.
@@ -46,6 +50,8 @@ struct UpdateArgs {
     int64_t batch, dim;
     int dstate;
     int softplus;
+    int64_t ngroups = 1;   // B, C: (batch, ngroups, dstate); channel d reads group d / gch
+    int64_t gch = 0;
 };
 
 // One compiled layout of the scan kernel: G states per lane (the N / G
@@ -63,12 +69,13 @@ struct ScanPlan {
 // Fast path (scan_relay.cu): warp relay over TMA-staged chunks.  Needs a
 // float32 workspace for the staged B and C (relay_workspace_bytes).
 int64_t relay_lpad(int64_t seqlen);
-int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate);
+int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate, int64_t ngroups);
 bool relay_supported(const ScanArgs& a, DType dt);
 cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cudaStream_t s);
 // Segmented direct scan (scan_relay.cu): needs staged B/C plus the segment
 // hand-off state and flags (seg_workspace_bytes).
-int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes);
+int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes,
+                            int64_t ngroups);
 cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
 
 // Depthwise causal conv1d (+ SiLU) and its decode step (conv1d.cu); layouts
@@ -112,6 +119,8 @@ struct BwdArgs {
     float* dbias;
     int64_t batch, dim, seqlen;
     int dstate;
+    int64_t ngroups = 1;   // B, C, dB, dC: (batch, ngroups, dstate, seqlen)
+    int64_t gch = 0;       // channels a group (dim / ngroups)
 };
 int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);
@@ -119,7 +128,7 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms
 // Tensor-memory scan (scan_tmem.cu): bf16 activations, 16 states.  Workspace:
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
 bool tmem_supported(const ScanArgs& a, DType dt);
-int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
+int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int64_t ngroups);
 // variant 2: two states per lane (8 consumer warps); otherwise four.
 cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant);
 int read_tmem_device_error(bool clear);

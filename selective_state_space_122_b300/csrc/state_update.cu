@@ -54,8 +54,10 @@ state_update_kernel(UpdateArgs p) {
 
     float4* st = reinterpret_cast<float4*>(p.state) + bd * Q;
     const float4* Ar = reinterpret_cast<const float4*>(p.A) + d * Q;
-    const T* Bp = static_cast<const T*>(p.B) + b * N;
-    const T* Cp = static_cast<const T*>(p.C) + b * N;
+    // B/C block of this channel: batch row b, group d / gch
+    const int64_t blk = b * p.ngroups + (int64_t)((uint32_t)d / (uint32_t)p.gch);
+    const T* Bp = static_cast<const T*>(p.B) + blk * N;
+    const T* Cp = static_cast<const T*>(p.C) + blk * N;
     float4 s[Q], a[Q], bv[Q], cv[Q];
 #pragma unroll
     for (int q = 0; q < Q; ++q) s[q] = __ldcs(st + q);

@@ -21,8 +21,9 @@ Recipe (one numpy ``Generator(PCG64(seed))`` per workload):
 
 Layouts follow the (batch, length, dim) convention of the Mamba block:
 u, delta, z, out are (batch, L, D) channel-contiguous; B and C are
-(batch, N, L) time-contiguous; A is (D, N); D and delta_bias are (D,);
-states are (batch, D, N).
+(batch, N, L) time-contiguous, or (batch, G, N, L) with B and C per channel
+group (drawn in the same order, G times as many values); A is (D, N); D and
+delta_bias are (D,); states are (batch, D, N).
 """
 from __future__ import annotations
 
@@ -130,8 +131,8 @@ class ScanInputs:
     u: np.ndarray          # (batch, L, D)   f32 or bf16 bits (uint16)
     delta: np.ndarray      # (batch, L, D)
     z: Optional[np.ndarray]
-    B: np.ndarray          # (batch, N, L)
-    C: np.ndarray          # (batch, N, L)
+    B: np.ndarray          # (batch, N, L), or (batch, G, N, L) per channel group
+    C: np.ndarray          # same shape as B
     A: np.ndarray          # (D, N) f32
     D: Optional[np.ndarray]
     delta_bias: Optional[np.ndarray]
@@ -157,15 +158,17 @@ class ScanInputs:
 
 def make_scan_inputs(shape: ScanShape, seed: int, *, random_a: bool = False,
                      with_z: bool = True, with_d: bool = True,
-                     with_bias: bool = True, softplus: bool = True) -> ScanInputs:
-    """Seeded inputs for a full-sequence scan of ``shape``."""
+                     with_bias: bool = True, softplus: bool = True, ngroups: int = 1) -> ScanInputs:
+    """Seeded inputs for a full-sequence scan of ``shape``; ngroups > 1 draws
+    B and C per channel group, shaped (batch, ngroups, N, L)."""
     rng = np.random.Generator(np.random.PCG64(seed))
     bt, L, D, N, dt = shape.batch, shape.seqlen, shape.dim, shape.dstate, shape.dtype
     u = _activation(rng, (bt, L, D), dt)
     delta = _activation(rng, (bt, L, D), dt)
     z = _activation(rng, (bt, L, D), dt)
-    B = _activation(rng, (bt, N, L), dt)
-    C = _activation(rng, (bt, N, L), dt)
+    bc = (bt, N, L) if ngroups == 1 else (bt, ngroups, N, L)
+    B = _activation(rng, bc, dt)
+    C = _activation(rng, bc, dt)
     bias = _delta_bias(rng, D)
     A = a_random(rng, D, N) if random_a else a_s4d_real(D, N)
     return ScanInputs(shape, u, delta, z if with_z else None, B, C, A,
@@ -182,14 +185,16 @@ class DecodeInputs:
     dt_bias: np.ndarray
     rng: np.random.Generator
 
-    def token(self):
-        """Next token: x, dt, z (batch, D) and B, C (batch, N) in the workload dtype."""
+    def token(self, ngroups: int = 1):
+        """Next token: x, dt, z (batch, D) and B, C (batch, N), or (batch,
+        ngroups, N) per channel group, in the workload dtype."""
         s = self.shape
         x = _activation(self.rng, (s.batch, s.dim), s.dtype)
         dt = _activation(self.rng, (s.batch, s.dim), s.dtype)
         z = _activation(self.rng, (s.batch, s.dim), s.dtype)
-        B = _activation(self.rng, (s.batch, s.dstate), s.dtype)
-        C = _activation(self.rng, (s.batch, s.dstate), s.dtype)
+        bc = (s.batch, s.dstate) if ngroups == 1 else (s.batch, ngroups, s.dstate)
+        B = _activation(self.rng, bc, s.dtype)
+        C = _activation(self.rng, bc, s.dtype)
         return x, dt, z, B, C
 
 

@@ -200,24 +200,24 @@ def test_binding_raises_without_cuda_tensors():
         _lib.ssm_scan_fwd(u, u, A, B, B)
 
 
-def _ws_expected(batch, dim, seqlen, dstate, es):
+def _ws_expected(batch, dim, seqlen, dstate, es, ngroups=1):
     """The largest of the fast paths' needs, each part rounded up to 256 bytes:
     B and C staged as float32 rows (sequence padded to 64 steps); B and C
     staged in the activation type (es bytes) plus one float32 state per
     (chain, channel, state) and one int flag per chain; and, for bf16 with 16
     states, the tensor-memory path's one-hot operands (32 float32 per step)
     plus its state and one flag per consumer warp (up to eight) of each
-    32-channel group."""
+    32-channel group.  Staged B/C (and operands) are per (batch row, B/C group)."""
     up = lambda x: (x + 255) // 256 * 256
     lpad = (seqlen + 63) // 64 * 64
     cw = 32 // (dstate // 4)
     chains = batch * ((dim + cw - 1) // cw)
-    relay = batch * lpad * 2 * dstate * 4
-    seg = up(batch * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
+    relay = batch * ngroups * lpad * 2 * dstate * 4
+    seg = up(batch * ngroups * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
     need = max(relay, seg)
     if es == 2 and dstate == 16:
         groups = batch * ((dim + 31) // 32)
-        need = max(need, up(batch * lpad * 32 * 4) + up(groups * 32 * 16 * 4) + up(groups * 8 * 4))
+        need = max(need, up(batch * ngroups * lpad * 32 * 4) + up(groups * 32 * 16 * 4) + up(groups * 8 * 4))
     return need
 
 
@@ -231,3 +231,82 @@ def test_workspace_size_query(lib):
     assert lib.ssm_scan_workspace_bytes(1, 64, 0, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 0, 64, 16, 1) == -1
     assert lib.ssm_scan_workspace_bytes(1, 64, 64, 16, 7) == -1
+
+
+def test_grouped_workspace_size_query(lib):
+    for args, G in [((1, 5120, 8192, 16), 8), ((3, 96, 77, 8), 3), ((2, 64, 100, 4), 64), ((8, 2048, 2048, 16), 1)]:
+        for dt, es in ((1, 2), (0, 4)):
+            assert lib.ssm_scan_workspace_bytes_grouped(*args, G, dt) == _ws_expected(*args, es, G), (args, G)
+        assert lib.ssm_scan_workspace_bytes_grouped(*args, 1, 1) == lib.ssm_scan_workspace_bytes(*args, 1)
+    for G in (0, -2, 3, 65):
+        assert lib.ssm_scan_workspace_bytes_grouped(2, 64, 128, 16, G, 1) == -1, G
+
+
+def call_scan_grouped(lib, a, ngroups, h0=None):
+    return lib.ssm_scan_fwd_grouped(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                    a["delta_bias"], a["softplus"], h0, a["out"], a["last_state"],
+                                    a["batch"], a["dim"], a["seqlen"], a["dstate"], ngroups, a["dtype"],
+                                    a["workspace"], a["workspace_bytes"], a["stream"])
+
+
+@pytest.mark.parametrize("kw,ngroups,code", [
+    ({}, 0, 2), ({}, -1, 2), ({}, 3, 2), ({}, 128, 2), (dict(dim=96), 64, 2),
+    (dict(u=None), 4, 1), (dict(dstate=3), 4, 4), (dict(dtype=9), 4, 5), (dict(B=P + 192 * MB + 1), 4, 3),
+    # out just past B's one-group extent (2*16*128 bf16) but inside its 4-group extent
+    (dict(out=P + 192 * MB + 3 * 8192), 4, 6),
+    (dict(last_state=P + 256 * MB + 30000), 4, 6),
+])
+def test_scan_grouped_rejects_bad_arguments(lib, kw, ngroups, code):
+    """Host checks of ssm_scan_fwd_grouped: ngroups must divide dim, and B, C
+    span batch * ngroups * dstate * seqlen elements (fake addresses; every case
+    is rejected before anything is enqueued)."""
+    assert call_scan_grouped(lib, scan_args(**kw), ngroups) == code
+
+
+def test_scan_grouped_one_group_validates_like_scan(lib):
+    for kw in (dict(u=None), dict(dstate=3), dict(u=P + 1), dict(out=P + 1024), dict(batch=0)):
+        assert call_scan_grouped(lib, scan_args(**kw), 1) == call_scan(lib, scan_args(**kw))
+
+
+@pytest.mark.parametrize("kw,ngroups,code", [
+    ({}, 0, 2), ({}, 5, 2), (dict(x=None), 2, 1), (dict(dstate=12), 2, 4),
+    # out just past B's one-group extent (4*16 bf16) but inside its 8-group extent
+    (dict(out=P + 256 * MB + 256), 8, 6),
+])
+def test_update_grouped_rejects_bad_arguments(lib, kw, ngroups, code):
+    a = upd_args(**kw)
+    assert lib.ssm_state_update_grouped(a["state"], a["x"], a["dt"], a["A"], a["B"], a["C"], a["D"], a["z"],
+                                        a["dt_bias"], a["out"], a["batch"], a["dim"], a["dstate"], ngroups,
+                                        a["softplus"], a["dtype"], a["stream"]) == code
+
+
+@pytest.mark.parametrize("kw,ngroups,code", [
+    ({}, 0, 2), ({}, 7, 2), (dict(ws=None), 2, 1),
+    # dC 512 KB after dB: apart for one group (dB 2*16*128 f32 = 16 KB), overlapping
+    # for 64 groups (1 MB)
+    (dict(dC=P + 768 * MB + 512 * 1024), 64, 6),
+])
+def test_scan_bwd_grouped_rejects_bad_arguments(lib, kw, ngroups, code):
+    a = dict(u=P, delta=P + 64 * MB, A=P + 128 * MB, B=P + 192 * MB, C=P + 256 * MB, D=P + 320 * MB,
+             z=P + 384 * MB, bias=P + 448 * MB, dout=P + 512 * MB, du=P + 576 * MB, dd=P + 640 * MB,
+             dA=P + 704 * MB, dB=P + 768 * MB, dC=P + 832 * MB, dD=P + 896 * MB, dz=P + 960 * MB,
+             db=P + 1024 * MB, ws=P + 1088 * MB, ws_bytes=64 * MB, batch=2, dim=64, seqlen=128, dstate=16,
+             dtype=1)
+    a.update(kw)
+    assert lib.ssm_scan_bwd_grouped(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], 1,
+                                    a["dout"], a["du"], a["dd"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"],
+                                    a["db"], a["batch"], a["dim"], a["seqlen"], a["dstate"], ngroups, a["dtype"],
+                                    a["ws"], a["ws_bytes"], None) == code
+
+
+def test_binding_checks_bc_shapes():
+    """The binding rejects B / C whose shape is neither (batch, N, L) nor
+    (batch, ngroups, N, L) before anything reaches the library."""
+    u = torch.zeros(2, 8, 8)
+    A = torch.zeros(8, 4)
+    for B in (torch.zeros(2, 4, 9), torch.zeros(2, 2, 3, 8), torch.zeros(1, 4, 8)):
+        with pytest.raises(ValueError, match="B and C must be"):
+            _lib.ssm_scan_fwd(u, u, A, B, B)
+    st = torch.zeros(2, 8, 4)
+    with pytest.raises(ValueError, match="B and C must be"):
+        _lib.ssm_state_update(st, u[:, 0], u[:, 0], A, torch.zeros(2, 2, 5), torch.zeros(2, 2, 5))
