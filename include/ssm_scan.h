@@ -50,7 +50,7 @@
  *   state and A must be 16-byte aligned (SSM_ERR_ALIGN).
  * - Supported d_state: 4, 8 or 16 (SSM_ERR_UNSUPPORTED otherwise).
  * - Sizes are element counts; each must be > 0 (an empty tensor is
- *   SSM_ERR_SHAPE), and batch*seqlen*dim must stay below 2^40.
+ *   SSM_ERR_SHAPE), dim must stay below 2^31 and batch*seqlen*dim below 2^40.
  */
 #ifndef SSM_SCAN_H
 #define SSM_SCAN_H

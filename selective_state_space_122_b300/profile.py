@@ -1,17 +1,18 @@
 """Profiling drivers for the selective-scan library (run on a CUDA device).
 
     python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
-           [--N N] [--iters K] [--path tmem|seg|relay|generic]
-    python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K]
+           [--N N] [--iters K] [--path tmem2|tmem|seg|relay|generic] [--ngroups G]
+    python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K] [--ngroups G]
     python -m selective_state_space_122_b300.profile conv [--batch B] [--dim D] [--L L] [--W W] [--iters K]
-    python -m selective_state_space_122_b300.profile bwd [--batch B] [--dim D] [--L L] [--N N] [--iters K]
+    python -m selective_state_space_122_b300.profile bwd [--batch B] [--dim D] [--L L] [--N N] [--iters K] [--ngroups G]
     python -m selective_state_space_122_b300.profile units
 
 ``scan`` runs ssm_scan_fwd on seeded on-device bf16 inputs shaped like the
 pages' workloads (u, delta_raw, z, B, C ~ N(0, 1); A = -(1..N); D = 1;
 delta_bias = softplus^-1(dt), dt log-uniform in [1e-3, 0.1]) and prints the
 CUDA-event time of each call: the command behind the ncu captures of the scan
-kernels.  ``decode`` does the same for one ssm_state_update step.  ``units``
+kernels.  ``decode`` does the same for one ssm_state_update step.  --ngroups
+draws B and C per channel group (the grouped entry points).  ``units``
 prints the measured SFU (ex2) and packed-FMA throughput at 1, 2 and 8 warps
 per scheduler (libssmpeak.so).
 """
@@ -29,14 +30,15 @@ from . import build as libbuild
 from ._lib import device_error, scan_workspace_bytes, ssm_scan_fwd, ssm_state_update
 
 
-def _inputs(batch, dim, L, N, dev, seed=0):
+def _inputs(batch, dim, L, N, dev, seed=0, ngroups=1):
     g = torch.Generator(device=dev)
     g.manual_seed(seed)
     u = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
     dl = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
     z = torch.randn(batch, L, dim, device=dev, generator=g).bfloat16()
-    B = torch.randn(batch, N, L, device=dev, generator=g).bfloat16()
-    C = torch.randn(batch, N, L, device=dev, generator=g).bfloat16()
+    bc = (batch, N, L) if ngroups == 1 else (batch, ngroups, N, L)
+    B = torch.randn(*bc, device=dev, generator=g).bfloat16()
+    C = torch.randn(*bc, device=dev, generator=g).bfloat16()
     A = -torch.arange(1, N + 1, device=dev, dtype=torch.float32).repeat(dim, 1).contiguous()
     D = torch.ones(dim, device=dev)
     dt = torch.exp(torch.empty(dim, device=dev).uniform_(math.log(1e-3), math.log(0.1), generator=g))
@@ -48,10 +50,10 @@ def cmd_scan(a):
     if a.path:
         os.environ["SSM_SCAN_PATH"] = a.path
     dev = torch.device("cuda", 0)
-    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev)
+    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev, ngroups=a.ngroups)
     out = torch.empty_like(u)
     last = torch.empty(a.batch, a.dim, a.N, device=dev)
-    ws = torch.empty(max(16, scan_workspace_bytes(a.batch, a.dim, a.L, a.N, torch.bfloat16)),
+    ws = torch.empty(max(16, scan_workspace_bytes(a.batch, a.dim, a.L, a.N, torch.bfloat16, a.ngroups)),
                      dtype=torch.uint8, device=dev)
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     elems = a.batch * a.dim * a.L * a.N
@@ -61,7 +63,7 @@ def cmd_scan(a):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        print(f"scan {a.batch}x{a.dim}x{a.L} N{a.N} iter {i}: {ms:.3f} ms "
+        print(f"scan {a.batch}x{a.dim}x{a.L} N{a.N} G{a.ngroups} iter {i}: {ms:.3f} ms "
               f"({elems / (ms * 1e-3) / 1e9:.1f} G elements/s)", flush=True)
     err = device_error()
     print("device error word:", err)
@@ -74,7 +76,8 @@ def cmd_decode(a):
     g.manual_seed(1)
     st = torch.randn(a.batch, a.dim, a.N, device=dev, generator=g) * 0.1
     x, dt, z = (torch.randn(a.batch, a.dim, device=dev, generator=g).bfloat16() for _ in range(3))
-    B, C = (torch.randn(a.batch, a.N, device=dev, generator=g).bfloat16() for _ in range(2))
+    bc = (a.batch, a.N) if a.ngroups == 1 else (a.batch, a.ngroups, a.N)
+    B, C = (torch.randn(*bc, device=dev, generator=g).bfloat16() for _ in range(2))
     A = -torch.arange(1, a.N + 1, device=dev, dtype=torch.float32).repeat(a.dim, 1).contiguous()
     D = torch.ones(a.dim, device=dev)
     bias = torch.full((a.dim,), -4.0, device=dev)
@@ -87,7 +90,7 @@ def cmd_decode(a):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        print(f"decode {a.batch}x{a.dim} N{a.N} iter {i}: {ms * 1e3:.1f} us "
+        print(f"decode {a.batch}x{a.dim} N{a.N} G{a.ngroups} iter {i}: {ms * 1e3:.1f} us "
               f"({nbytes / (ms * 1e-3) / 1e9:.0f} GB/s)", flush=True)
     return 0
 
@@ -95,7 +98,7 @@ def cmd_decode(a):
 def cmd_bwd(a):
     from ._lib import ssm_scan_bwd
     dev = torch.device("cuda", 0)
-    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev)
+    u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev, ngroups=a.ngroups)
     dout = torch.randn_like(u, dtype=torch.float32).bfloat16()
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     elems = a.batch * a.dim * a.L * a.N
@@ -106,7 +109,7 @@ def cmd_bwd(a):
         e1.record()
         torch.cuda.synchronize()
         ms = e0.elapsed_time(e1)
-        print(f"bwd {a.batch}x{a.dim}x{a.L} N{a.N} iter {i}: {ms:.3f} ms "
+        print(f"bwd {a.batch}x{a.dim}x{a.L} N{a.N} G{a.ngroups} iter {i}: {ms:.3f} ms "
               f"({elems / (ms * 1e-3) / 1e9:.1f} G elements/s)", flush=True)
     return 0
 
@@ -158,18 +161,21 @@ def main(argv=None):
     s.add_argument("--L", type=int, default=16384)
     s.add_argument("--N", type=int, default=16)
     s.add_argument("--iters", type=int, default=3)
-    s.add_argument("--path", default=None, choices=[None, "tmem", "relay", "seg", "generic"])
+    s.add_argument("--path", default=None, choices=[None, "tmem2", "tmem", "relay", "seg", "generic"])
+    s.add_argument("--ngroups", type=int, default=1)
     d = sub.add_parser("decode")
     d.add_argument("--batch", type=int, default=256)
     d.add_argument("--dim", type=int, default=5120)
     d.add_argument("--N", type=int, default=16)
     d.add_argument("--iters", type=int, default=5)
+    d.add_argument("--ngroups", type=int, default=1)
     bw = sub.add_parser("bwd")
     bw.add_argument("--batch", type=int, default=8)
     bw.add_argument("--dim", type=int, default=2048)
     bw.add_argument("--L", type=int, default=2048)
     bw.add_argument("--N", type=int, default=16)
     bw.add_argument("--iters", type=int, default=3)
+    bw.add_argument("--ngroups", type=int, default=1)
     cv = sub.add_parser("conv")
     cv.add_argument("--batch", type=int, default=1)
     cv.add_argument("--dim", type=int, default=5120)
