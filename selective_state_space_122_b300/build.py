@@ -7,11 +7,13 @@
   for its roofline denominators (not part of the scan path).
 
 nvcc cross-compiles without a GPU.  Both libraries statically link the CUDA
-runtime, so they only need the driver at run time.
+runtime, so they only need the driver at run time.  The sources compile to
+objects in parallel (under _build/ next to this file), then link once.
 """
 from __future__ import annotations
 
 import argparse
+import concurrent.futures
 import os
 import subprocess
 import sys
@@ -25,8 +27,9 @@ PEAK_SOURCES = ["sfu_peak.cu"]
 SOURCES = ["ssm_api.cu", "scan_fwd.cu", "scan_relay.cu", "scan_tmem.cu", "state_update.cu", "conv1d.cu", "scan_bwd.cu", "noalloc.cu"]
 HEADERS = ["ssm_internal.cuh", "scan_common.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
-NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden",
-              "--shared", "-cudart", "static"]
+COMPILE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]
+LINK_FLAGS = ["--shared", "-cudart", "static"]
+OBJ_DIR = os.path.join(PKG, "_build")
 
 
 def nvcc() -> str:
@@ -46,16 +49,30 @@ def up_to_date(out: str = LIB, inputs=None) -> bool:
     return all(os.path.getmtime(p) <= t for p in (inputs or _inputs()))
 
 
-def _nvcc(out: str, sources, verbose: bool) -> None:
-    cmd = [nvcc(), *ARCH, *NVCC_FLAGS, "-I", os.path.join(ROOT, "include"),
-           *(["-Xptxas", "-v"] if verbose else []),
-           "-o", out, *[os.path.join(CSRC, s) for s in sources]]
+def _run(cmd, what: str, verbose: bool) -> None:
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         sys.stderr.write(r.stdout + r.stderr)
-        raise RuntimeError(f"nvcc failed building {os.path.basename(out)}")
+        raise RuntimeError(f"nvcc failed building {what}")
     if verbose:
         sys.stderr.write(r.stderr)
+
+
+def _nvcc(out: str, sources, verbose: bool) -> None:
+    """Compile every source to an object (in parallel), then link the shared library."""
+    os.makedirs(OBJ_DIR, exist_ok=True)
+    stem = os.path.splitext(os.path.basename(out))[0]
+    objs = [os.path.join(OBJ_DIR, f"{stem}.{os.path.splitext(s)[0]}.o") for s in sources]
+
+    def compile_one(src_obj):
+        src, obj = src_obj
+        _run([nvcc(), *ARCH, *COMPILE_FLAGS, "-I", os.path.join(ROOT, "include"),
+              *(["-Xptxas", "-v"] if verbose else []), "-c", "-o", obj, os.path.join(CSRC, src)], src, verbose)
+
+    workers = max(1, min(len(sources), os.cpu_count() or 1))
+    with concurrent.futures.ThreadPoolExecutor(max_workers=workers) as pool:
+        list(pool.map(compile_one, zip(sources, objs)))
+    _run([nvcc(), *ARCH, *LINK_FLAGS, "-o", out, *objs], os.path.basename(out), verbose)
 
 
 def build(out: str = LIB, verbose: bool = False, force: bool = False) -> str:
