@@ -152,7 +152,7 @@ def barrier(world):
 # ---------------------------------------------------------------- clocks
 
 class ClockSampler:
-    """nvidia-smi sampled every 200 ms while the timed region runs."""
+    """nvidia-smi sampled every 50 ms while the timed region runs."""
     QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
@@ -189,31 +189,44 @@ class ClockSampler:
     def summary(self):
         if self.proc is None or not self.path or not os.path.exists(self.path):
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
-        sm, smax, reasons, power = [], [], set(), []
-        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
-        for line in open(self.path):
-            f = [x.strip() for x in line.split(",")]
-            if len(f) < 9:
-                continue
-            try:
-                sm.append(float(f[1]))
-                smax.append(float(f[2]))
-                power.append(float(f[3]))
-            except ValueError:
-                continue
-            for n, v in zip(names, f[5:9]):
-                if v.lower() == "active":
-                    reasons.add(n)
-        if not sm:
-            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
-        # "under load": the samples drawing at least half the peak power seen (the
-        # sampler also runs a moment before and after the timed region)
-        pk = max(power) if power else 0.0
-        loaded = [c for c, w in zip(sm, power) if w >= 0.5 * pk] if power else sm
-        loaded = loaded or sm
-        return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
-                "samples_under_load": len(loaded), "power_w_max": pk if power else None,
-                "reasons": sorted(reasons)}
+        return summarize_clock_samples(open(self.path).read().splitlines())
+
+
+def summarize_clock_samples(lines):
+    """Clock record of the timed region from nvidia-smi CSV rows (the QUERY
+    fields, no header, no units): the median SM clock over the samples under
+    load (drawing at least half the peak power seen; the sampler also runs a
+    moment before and after the timed region), the maximum clock, and every
+    throttle reason seen active.  A row whose power reads as unavailable still
+    counts for the clocks and the reasons."""
+    sm, smax, power, reasons = [], [], [], set()
+    names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+    for line in lines:
+        f = [x.strip() for x in line.split(",")]
+        if len(f) < 9:
+            continue
+        try:
+            c, cm = float(f[1]), float(f[2])
+        except ValueError:
+            continue
+        try:
+            w = float(f[3])
+        except ValueError:
+            w = None
+        sm.append(c)
+        smax.append(cm)
+        power.append(w)
+        for n, v in zip(names, f[5:9]):
+            if v.lower() == "active":
+                reasons.add(n)
+    if not sm:
+        return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+    known = [w for w in power if w is not None]
+    pk = max(known) if known else None
+    loaded = [c for c, w in zip(sm, power) if w is not None and w >= 0.5 * pk] if known else []
+    loaded = loaded or sm
+    return {"sm_mhz": statistics.median(loaded), "sm_max_mhz": max(smax), "samples": len(sm),
+            "samples_under_load": len(loaded), "power_w_max": pk, "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------- our arm

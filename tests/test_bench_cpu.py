@@ -78,3 +78,27 @@ def test_reference_arm_nonzero_rank_exits_without_work():
     r = subprocess.run([sys.executable, os.path.join(ROOT, "bench.py"), "--impl", "reference",
                         "--steps", "1", "--warmup", "0"], env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0 and r.stdout.strip() == ""
+
+
+def test_clock_summary_takes_the_median_under_load_and_every_reason():
+    rows = [
+        "0, 1200, 2032, 90.5, 0x0, Not Active, Not Active, Not Active, Not Active",       # before the region
+        "0, 2032, 2032, 700.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1980, 2032, 900.0, 0x4, Not Active, Not Active, Not Active, Active",          # power cap
+        "0, 2010, 2032, [N/A], 0x0, Not Active, Not Active, Not Active, Not Active",      # power unreadable
+        "0, 2020, 2032, 880.0, 0x0, Not Active, Not Active, Not Active, Not Active",
+        "0, 1150, 2032, 95.0, 0x0, Not Active, Not Active, Not Active, Not Active",       # after the region
+        "garbage line",
+    ]
+    s = bench.summarize_clock_samples(rows)
+    assert s["samples"] == 6 and s["samples_under_load"] == 3
+    assert s["sm_mhz"] == 2020.0 and s["sm_max_mhz"] == 2032.0 and s["power_w_max"] == 900.0
+    assert s["reasons"] == ["sw_power_cap"]
+    hot = rows[:1] + ["0, 1700, 2032, 800.0, 0x40, Not Active, Active, Not Active, Not Active"]
+    assert bench.summarize_clock_samples(hot)["reasons"] == ["hw_thermal_slowdown"]
+    # no power readings at all: every sample counts
+    nopw = [r.replace("700.0", "[N/A]").replace("900.0", "[N/A]").replace("880.0", "[N/A]")
+            .replace("90.5", "[N/A]").replace("95.0", "[N/A]") for r in rows]
+    s = bench.summarize_clock_samples(nopw)
+    assert s["samples_under_load"] == 6 and s["power_w_max"] is None and s["sm_mhz"] == 1995.0
+    assert bench.summarize_clock_samples([])["reasons"] == ["no samples"]
