@@ -114,7 +114,7 @@ struct RelayParams {
     int softplus;
     int has_z;
     const float* h0;        // initial state or null
-    int ngroups, gch;       // B/C groups, channels a group (a multiple of CW)
+    int ngroups, gch;       // B/C groups, channels per group (a multiple of CW)
 };
 
 
@@ -435,7 +435,7 @@ struct SegParams {
     int cps;                // chunks per segment
     int workers;            // (main, helper) pairs in the grid
     const float* h0;        // initial state (batch, dim, N) or null
-    int ngroups, gch;       // B/C groups, channels a group (a multiple of CW)
+    int ngroups, gch;       // B/C groups, channels per group (a multiple of CW)
 };
 
 __device__ __forceinline__ int ld_acquire(const int* p) {
@@ -788,10 +788,11 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
     if (lane == 0) bulk_wait_all();
 }
 
-// B and C (batch, N, L) -> staged rows [batch][lpad][B_0..B_{N-1}, C_0..C_{N-1}] of
+// B and C (rows, N, L) -> staged rows [rows][lpad][B_0..B_{N-1}, C_0..C_{N-1}] of
 // type O (float32 for the relay kernel; the activation type for the segmented
-// kernel, so that its per-step reads move half the bytes), zero beyond L.  One CTA per (64-step tile, B/C block:
-// batch row, or batch row and channel group), transposed through shared memory.
+// kernel, so that its per-step reads move half the bytes), zero beyond L; rows =
+// batch, or batch * ngroups for B and C per channel group.  One CTA per
+// (64-step tile, row), transposed through shared memory.
 template <typename T, int N, typename O = float>
 __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, const T* __restrict__ C,
                                                        O* __restrict__ bc, int64_t L, int64_t lpad,

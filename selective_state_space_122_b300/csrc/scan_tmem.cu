@@ -195,7 +195,7 @@ struct TmParams {
     int cps;                // chunks per segment
     int workers;            // CTAs in the grid
     const float* h0;        // initial state (batch, dim, N) or null
-    int ngroups, gch;       // B/C groups, channels a group (a multiple of 32)
+    int ngroups, gch;       // B/C groups, channels per group (a multiple of 32)
 };
 
 __device__ __forceinline__ int tm_ld_acquire(const int* p) {

@@ -30,7 +30,7 @@ struct ScanArgs {
     int softplus;
     const float* h0;        // initial state (batch, dim, dstate) f32, or null for zero
     // B and C per channel group: (batch, ngroups, dstate, seqlen); channel d
-    // reads block b * ngroups + d / gch (gch = dim / ngroups channels a group)
+    // reads block b * ngroups + d / gch (gch = dim / ngroups channels per group)
     int64_t ngroups = 1;
     int64_t gch = 0;
 };
@@ -120,7 +120,7 @@ struct BwdArgs {
     int64_t batch, dim, seqlen;
     int dstate;
     int64_t ngroups = 1;   // B, C, dB, dC: (batch, ngroups, dstate, seqlen)
-    int64_t gch = 0;       // channels a group (dim / ngroups)
+    int64_t gch = 0;       // channels per group (dim / ngroups)
 };
 int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);

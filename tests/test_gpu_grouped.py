@@ -51,14 +51,14 @@ def _oracle(inp, h0=None):
 
 
 @pytest.mark.parametrize("bt,dim,L,N,dtype,G", [
-    (2, 128, 300, 16, inputs.BF16, 4),     # 32 channels a group: every path
+    (2, 128, 300, 16, inputs.BF16, 4),     # 32 channels per group: every path
     (2, 256, 200, 16, inputs.BF16, 2),
-    (2, 72, 130, 16, inputs.BF16, 9),      # 8 a group: segmented, relay, generic
-    (2, 30, 77, 16, inputs.BF16, 10),      # 3 a group (odd): generic only
-    (3, 64, 65, 8, inputs.F32, 4),         # 16 a group
-    (2, 64, 50, 4, inputs.F32, 2),         # 32 a group
-    (1, 96, 100, 8, inputs.BF16, 12),      # 8 a group, below the 8-state block of 16
-    (2, 40, 33, 4, inputs.F32, 40),        # one channel a group
+    (2, 72, 130, 16, inputs.BF16, 9),      # 8 per group: segmented, relay, generic
+    (2, 30, 77, 16, inputs.BF16, 10),      # 3 per group (odd): generic only
+    (3, 64, 65, 8, inputs.F32, 4),         # 16 per group
+    (2, 64, 50, 4, inputs.F32, 2),         # 32 per group
+    (1, 96, 100, 8, inputs.BF16, 12),      # 8 per group, below the 8-state block of 16
+    (2, 40, 33, 4, inputs.F32, 40),        # one channel per group
 ])
 def test_grouped_scan_every_path(bt, dim, L, N, dtype, G):
     inp = inputs.make_scan_inputs(inputs.ScanShape("grp", bt, dim, L, N, dtype), 2000 + dim + L, ngroups=G)
@@ -78,7 +78,7 @@ def test_fast_path_rejects_group_sizes_it_cannot_take(path):
     """Forcing a kernel onto groups that split its channel block is
     SSM_ERR_UNSUPPORTED, before anything is launched."""
     inp = inputs.make_scan_inputs(inputs.ScanShape("grp-rej", 2, 64, 64, 16, inputs.BF16), 2100, ngroups=16)
-    t = _device(inp)                       # 4 channels a group
+    t = _device(inp)                       # 4 channels per group
     with scan_layout(path), pytest.raises(SSMError) as e:
         _scan(t, inp.softplus)
     assert e.value.code == 4
@@ -141,7 +141,7 @@ def test_grouped_decode_step(dtype, N, bt, dim, G):
 @pytest.mark.parametrize("bt,dim,L,N,dtype,G", [
     (2, 64, 300, 16, inputs.BF16, 4),
     (2, 48, 77, 8, inputs.F32, 3),
-    (1, 30, 65, 16, inputs.F32, 10),       # 3 channels a group
+    (1, 30, 65, 16, inputs.F32, 10),       # 3 channels per group
     (2, 256, 1024, 16, inputs.BF16, 2),
 ])
 def test_grouped_bwd(bt, dim, L, N, dtype, G):
