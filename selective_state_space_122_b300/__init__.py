@@ -4,6 +4,9 @@ Public calls (thin wrappers over the C ABI in include/ssm_scan.h):
 
 * ``ssm_scan_fwd``     -- full-sequence scan (prefill / training forward),
                           optionally from an initial state (``initial_state=``);
+                          B and C shaped (batch, ngroups, N, L) give every group
+                          of dim / ngroups channels its own B and C (also for
+                          ``ssm_state_update`` and ``ssm_scan_bwd``);
 * ``ssm_state_update`` -- single-token recurrent update (decode);
 * ``ssm_scan_bwd``     -- the scan's backward (every input's gradient);
 * ``conv1d_fwd``       -- the depthwise causal conv1d (+ SiLU) that produces the
