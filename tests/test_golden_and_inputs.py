@@ -52,3 +52,21 @@ def test_decode_generator():
     assert 0.05 < float(np.std(d.state0)) < 0.2
     x, dt, z, B, C = d.token()
     assert x.shape == (4, 8) and B.shape == (4, 16) and x.dtype == np.uint16
+
+
+def test_grouped_draws_keep_the_one_group_stream():
+    """ngroups = 1 draws exactly the plain inputs; ngroups > 1 draws B and C as
+    (batch, ngroups, N, L) in the same order (u, delta, z, then B, then C), so
+    the activations drawn before them are unchanged."""
+    shape = inputs.ScanShape("g", 2, 24, 10, 4, inputs.BF16)
+    a = inputs.make_scan_inputs(shape, 5)
+    b = inputs.make_scan_inputs(shape, 5, ngroups=1)
+    for k in ("u", "delta", "z", "B", "C", "A", "D", "delta_bias"):
+        assert np.array_equal(getattr(a, k), getattr(b, k)), k
+    g = inputs.make_scan_inputs(shape, 5, ngroups=3)
+    assert g.B.shape == (2, 3, 4, 10) and g.C.shape == (2, 3, 4, 10)
+    for k in ("u", "delta", "z"):
+        assert np.array_equal(getattr(a, k), getattr(g, k)), k
+    d = inputs.make_decode_inputs(inputs.DecodeShape("g", 3, 8, 4, inputs.F32), 9)
+    x, dt, z, B, C = d.token(ngroups=2)
+    assert B.shape == (3, 2, 4) and C.shape == (3, 2, 4) and x.shape == (3, 8)
