@@ -72,3 +72,23 @@ def test_conv1d_pieces_and_in_place_state(dtype):
         torch.cuda.synchronize()
         check_out(host_f64(go), ro, dtype, "conv decode out")
         _check_state(host_f64(state), ost, "conv decode state")
+
+
+def test_conv1d_long_sequence_sampled():
+    """The long-sequence shape (1 x 131072 x 5120, width 4, bf16, SiLU, carried
+    state) in one call, against the oracle on sampled channels over every step:
+    the kernel's full tile grid and its 16-byte vector path at full size."""
+    bt, L, dim, W = 1, 131072, 5120, 4
+    r = np.random.Generator(np.random.PCG64(4242))
+    x = inputs._activation(r, (bt, L, dim), inputs.BF16)
+    w = (r.standard_normal((dim, W)) * 0.5).astype(np.float32)
+    bias = (r.standard_normal(dim) * 0.5).astype(np.float32)
+    st = r.standard_normal((bt, dim, W - 1)).astype(np.float32)
+    out, got_st = conv1d_fwd(dev(x), dev(w), dev(bias), True, dev(st), return_state=True)
+    torch.cuda.synchronize()
+    sel = np.unique(np.concatenate([np.arange(0, 16), np.arange(2001, dim, 389), np.arange(dim - 9, dim)]))
+    xs = inputs.bf16_bits_to_f64(np.ascontiguousarray(x[:, :, sel]))
+    ref, ref_st = oracle.conv1d(xs, w[sel], bias[sel], True, st[:, sel].astype(np.float64))
+    idx = torch.as_tensor(sel, device=out.device)
+    check_out(host_f64(out[:, :, idx]), ref, inputs.BF16, "long conv out")
+    _check_state(host_f64(got_st[:, idx]), ref_st, "long conv state")

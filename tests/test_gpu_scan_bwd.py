@@ -59,3 +59,23 @@ def test_scan_bwd_matches_adjoint_oracle(bt, dim, L, N, dtype, kw):
     for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
         if ref[k] is not None:
             _close(host_f64(g[k]), ref[k], 1e-4, k)
+
+
+def test_scan_bwd_prefill_shape():
+    """The mid-size prefill shape (8 x 2048 x 2048, d_state 16, bf16) in one
+    call -- 512 CTAs under the 4-CTA register budget -- against the adjoint
+    oracle on every output element."""
+    bt, dim, L, N, dtype = 8, 2048, 2048, 16, inputs.BF16
+    inp = inputs.make_scan_inputs(inputs.PREFILL_MID, 1400)
+    r = np.random.Generator(np.random.PCG64(1401))
+    dout = inputs._activation(r, (bt, L, dim), dtype)
+    g = ssm_scan_bwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D), dev(inp.z),
+                     dev(inp.delta_bias), inp.softplus, dev(dout))
+    torch.cuda.synchronize()
+    f = inp.as_f64()
+    ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"], f["delta_bias"],
+                          f["softplus"], inputs.bf16_bits_to_f64(dout))
+    for k in ("du", "ddelta", "dz"):
+        _close(host_f64(g[k]), ref[k], 1e-4, k, rounded=True)
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
+        _close(host_f64(g[k]), ref[k], 1e-4, k)
