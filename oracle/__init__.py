@@ -65,6 +65,9 @@ def load(path: Optional[str] = None):
     lib.oracle_step_grouped.restype = ctypes.c_int
     lib.oracle_scan_bwd_grouped.argtypes = [dp] * 8 + [ctypes.c_int] + [dp] * 9 + [ctypes.c_int] * 5
     lib.oracle_scan_bwd_grouped.restype = ctypes.c_int
+    lib.oracle_scan_bwd_from.argtypes = ([dp] * 8 + [ctypes.c_int] + [dp] * 3 + [dp] * 9
+                                         + [ctypes.c_int] * 5)
+    lib.oracle_scan_bwd_from.restype = ctypes.c_int
     lib.oracle_softplus.argtypes = [ctypes.c_double]
     lib.oracle_softplus.restype = ctypes.c_double
     lib.oracle_silu.argtypes = [ctypes.c_double]
@@ -138,13 +141,19 @@ def step(state, x, dt, A, B, C, D=None, z=None, dt_bias=None, dt_softplus=True, 
     return out
 
 
-def scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, lib=None):
+def scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, lib=None, initial_state=None, dlast=None):
     """Gradients of L = sum(dout * out) of the scan (from h = 0) with respect to
     every input.  Returns a dict du, ddelta (batch, L, dim); dA (dim, N); dB, dC
     shaped like B and C ((batch, N, L) or (batch, ngroups, N, L)); dD,
-    ddelta_bias (dim,) or None; dz (batch, L, dim) or None."""
+    ddelta_bias (dim,) or None; dz (batch, L, dim) or None.
+
+    initial_state (batch, dim, N) starts the forward scan from that state, and
+    dlast (batch, dim, N) is dL/d last_state (the final state's part of the
+    loss); both default to zero.  The dict also holds dinitial_state =
+    dL/d initial_state (batch, dim, N)."""
     lib = lib or load()
     u, delta, A, B, C, D, z, delta_bias, dout = map(_f64, (u, delta, A, B, C, D, z, delta_bias, dout))
+    h0, dl = _f64(initial_state), _f64(dlast)
     bt, L, dim = u.shape
     N = A.shape[1]
     G = _groups(B, (bt,), (L,))
@@ -152,11 +161,13 @@ def scan_bwd(u, delta, A, B, C, D, z, delta_bias, softplus, dout, lib=None):
     g = dict(du=np.empty_like(u), ddelta=np.empty_like(u), dA=np.empty_like(A), dB=np.empty_like(B),
              dC=np.empty_like(C), dD=None if D is None else np.empty(dim),
              dz=None if z is None else np.empty_like(u),
-             ddelta_bias=None if delta_bias is None else np.empty(dim))
-    rc = lib.oracle_scan_bwd_grouped(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
-                                     int(bool(softplus)), _p(dout), _p(g["du"]), _p(g["ddelta"]), _p(g["dA"]),
-                                     _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]), _p(g["ddelta_bias"]),
-                                     bt, dim, L, N, G)
+             ddelta_bias=None if delta_bias is None else np.empty(dim), dinitial_state=np.empty((bt, dim, N)))
+    for a in (h0, dl):
+        assert a is None or a.shape == (bt, dim, N)
+    rc = lib.oracle_scan_bwd_from(_p(u), _p(delta), _p(A), _p(B), _p(C), _p(D), _p(z), _p(delta_bias),
+                                  int(bool(softplus)), _p(h0), _p(dout), _p(dl), _p(g["du"]), _p(g["ddelta"]),
+                                  _p(g["dA"]), _p(g["dB"]), _p(g["dC"]), _p(g["dD"]), _p(g["dz"]),
+                                  _p(g["ddelta_bias"]), _p(g["dinitial_state"]), bt, dim, L, N, G)
     if rc != 0:
         raise ValueError(f"oracle_scan_bwd rejected its arguments (code {rc})")
     return g

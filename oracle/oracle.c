@@ -221,15 +221,25 @@ int oracle_step(double* state, const double* x, const double* dt,
  * B and C are shared by all channels (of a group, in the grouped form), so dB
  * and dC sum over those channels.  Every
  * output array is overwritten; dz, dD and dbias may be NULL when z, D or the
- * bias is absent.  Sequential (no threads): each output sums over channels. */
+ * bias is absent.  Sequential (no threads): each output sums over channels.
+ *
+ * oracle_scan_bwd_from is the backward of the scan from a given state
+ * (oracle_scan_from) whose final state also enters the loss: with h_{-1} =
+ * initial_state (0 when NULL) and dlast = dL/d last_state (0 when NULL), the
+ * adjoint starts from lambda_{L-1} = C_{L-1} dy_{L-1} + dlast, and
+ *   dinitial = dL/dh_{-1} = a_0 lambda_0
+ * is written when dinitial is not NULL.  A sequence cut in two pieces is
+ * differentiated piece by piece: the second piece's dinitial is the first
+ * piece's dlast. */
 static double sigmoid(double v) { return 1.0 / (1.0 + exp(-v)); }
 
-int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* A,
-                            const double* B, const double* C, const double* D,
-                            const double* z, const double* delta_bias, int softplus_flag,
-                            const double* dout, double* du, double* ddelta, double* dA,
-                            double* dB, double* dC, double* dD, double* dz, double* dbias,
-                            int batch, int dim, int seqlen, int dstate, int ngroups) {
+int oracle_scan_bwd_from(const double* u, const double* delta, const double* A,
+                         const double* B, const double* C, const double* D,
+                         const double* z, const double* delta_bias, int softplus_flag,
+                         const double* initial_state, const double* dout, const double* dlast,
+                         double* du, double* ddelta, double* dA, double* dB, double* dC,
+                         double* dD, double* dz, double* dbias, double* dinitial,
+                         int batch, int dim, int seqlen, int dstate, int ngroups) {
     if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC) return 1;
     if (check_dims(batch, dim, seqlen, dstate) || check_groups(dim, ngroups)) return 2;
     const ptrdiff_t L = seqlen, Dm = dim, N = dstate;
@@ -248,8 +258,9 @@ int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* 
             const double* Bb = B + blk * N * L;
             const double* Cb = C + blk * N * L;
             const double Dd = D ? D[d] : 0.0;
-            /* forward, keeping every state */
-            for (ptrdiff_t n = 0; n < N; ++n) hs[n] = 0.0;
+            const ptrdiff_t sbase = (b * Dm + d) * N;
+            /* forward from h_{-1}, keeping every state */
+            for (ptrdiff_t n = 0; n < N; ++n) hs[n] = initial_state ? initial_state[sbase + n] : 0.0;
             for (ptrdiff_t t = 0; t < L; ++t) {
                 const ptrdiff_t i = (b * L + t) * Dm + d;
                 const double dlt = timestep(delta[i], delta_bias, (int)d, softplus_flag);
@@ -263,8 +274,12 @@ int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* 
                 ys[t] = y + Dd * u[i];
             }
             /* backward */
+            /* lambda "after" the last step is dlast, carried into step L-1 with weight 1 */
             double lam[ORACLE_MAX_DSTATE], anext[ORACLE_MAX_DSTATE];
-            for (ptrdiff_t n = 0; n < N; ++n) lam[n] = anext[n] = 0.0;
+            for (ptrdiff_t n = 0; n < N; ++n) {
+                lam[n] = dlast ? dlast[sbase + n] : 0.0;
+                anext[n] = 1.0;
+            }
             for (ptrdiff_t t = L - 1; t >= 0; --t) {
                 const ptrdiff_t i = (b * L + t) * Dm + d;
                 const double dlt = dls[t];
@@ -293,11 +308,25 @@ int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* 
                 ddelta[i] = dx;
                 if (dbias) dbias[d] += dx;
             }
+            /* h_0 = a_0 h_{-1} + ...: the adjoint of the initial state */
+            if (dinitial)
+                for (ptrdiff_t n = 0; n < N; ++n) dinitial[sbase + n] = anext[n] * lam[n];
         }
     free(hs);
     free(dls);
     free(ys);
     return 0;
+}
+
+int oracle_scan_bwd_grouped(const double* u, const double* delta, const double* A,
+                            const double* B, const double* C, const double* D,
+                            const double* z, const double* delta_bias, int softplus_flag,
+                            const double* dout, double* du, double* ddelta, double* dA,
+                            double* dB, double* dC, double* dD, double* dz, double* dbias,
+                            int batch, int dim, int seqlen, int dstate, int ngroups) {
+    return oracle_scan_bwd_from(u, delta, A, B, C, D, z, delta_bias, softplus_flag, NULL, dout, NULL,
+                                du, ddelta, dA, dB, dC, dD, dz, dbias, NULL, batch, dim, seqlen, dstate,
+                                ngroups);
 }
 
 int oracle_scan_bwd(const double* u, const double* delta, const double* A,

@@ -30,6 +30,9 @@ disagrees with an independent route to the same answer:
 * groups:        with B and C per channel group, the unrolled sum reading each
                  channel's own group, the grouped decode chain, and finite
                  differences of the grouped gradients;
+* backward from a state: finite differences of <dout, out> + <dlast,
+                 last_state> for every input and the initial state, and a
+                 sequence differentiated in two pieces equal to the whole;
 * backward:      central finite differences of L = sum(dout * out) through the
                  forward oracle for every input; and L = <du, u> (out is
                  linear in u), L = <dB, B> = <dC, C> without the D skip (out
@@ -489,6 +492,73 @@ def pin_grouped_bwd_finite_differences(lib):
         assert err <= 2e-6 * scale, f"grouped d{name}: |analytic - finite difference| {err:.2e}"
 
 
+def _grads_from(case, dout, h0, dlast, lib):
+    return oracle.scan_bwd(case["u"], case["delta"], case["A"], case["B"], case["C"], case["D"], case["z"],
+                           case["delta_bias"], case["softplus"], dout, lib=lib, initial_state=h0, dlast=dlast)
+
+
+def pin_bwd_from_state_finite_differences(lib):
+    """Backward of the scan from a given state, with the final state in the
+    loss: central finite differences of L = <dout, out> + <dlast, last_state>
+    for every input and for the initial state (dinitial_state)."""
+    # (without softplus and bias, Delta = 0.3 |delta_raw| >= 0 keeps the recurrence bounded)
+    for seed, kw in [(331, dict(dim=2)),
+                     (332, dict(dim=4, groups=2, with_z=False, softplus=False, with_bias=False))]:
+        case = tiny_case(seed, bt=2, L=6, N=3, **kw)
+        bt, L, dim = case["u"].shape
+        N = case["A"].shape[1]
+        r = _rng(seed + 1)
+        h0 = r.standard_normal((bt, dim, N))
+        dlast = r.standard_normal((bt, dim, N))
+        dout = r.standard_normal(case["u"].shape)
+
+        def loss(c, h):
+            out, last = run_oracle(c, lib, h)
+            return float(np.sum(dout * out) + np.sum(dlast * last))
+
+        g = _grads_from(case, dout, h0, dlast, lib)
+        for name, gname in list(GRAD_OF.items()) + [("initial_state", "dinitial_state")]:
+            base = h0 if name == "initial_state" else case[name]
+            if base is None:
+                continue
+            fd = np.zeros_like(base)
+            for idx in np.ndindex(base.shape):
+                eps = 1e-6 * max(1.0, abs(float(base[idx])))
+                for sgn in (1.0, -1.0):
+                    pert = base.copy()
+                    pert[idx] += sgn * eps
+                    c, h = (case, pert) if name == "initial_state" else (dict(case, **{name: pert}), h0)
+                    fd[idx] += sgn * loss(c, h) / (2.0 * eps)
+            scale = max(1.0, float(np.max(np.abs(fd))))
+            err = float(np.max(np.abs(g[gname] - fd)))
+            assert err <= 2e-6 * scale, f"from-state d{name} seed {seed}: |analytic - finite difference| {err:.2e}"
+
+
+def pin_bwd_split_equals_whole(lib):
+    """A sequence cut in two and differentiated piece by piece -- the second
+    piece from the first piece's final state, the first piece taking the
+    second piece's dinitial_state as its dlast -- gives the whole backward."""
+    for seed, cut in [(341, 1), (342, 5), (343, 9)]:
+        case = tiny_case(seed, bt=2, L=10, dim=3, N=4)
+        bt, L, dim = case["u"].shape
+        r = _rng(seed + 7)
+        h0 = r.standard_normal((bt, dim, 4))
+        dlast = r.standard_normal((bt, dim, 4))
+        dout = r.standard_normal(case["u"].shape)
+        whole = _grads_from(case, dout, h0, dlast, lib)
+        c1, c2 = _cut(case, 0, cut), _cut(case, cut, L)
+        _, hmid = run_oracle(c1, lib, h0)
+        g2 = _grads_from(c2, np.ascontiguousarray(dout[:, cut:]), hmid, dlast, lib)
+        g1 = _grads_from(c1, np.ascontiguousarray(dout[:, :cut]), h0, g2["dinitial_state"], lib)
+        for k in ("du", "ddelta", "dz"):
+            _close(np.concatenate([g1[k], g2[k]], axis=1), whole[k], what=f"split backward {k}, cut {cut}")
+        for k in ("dB", "dC"):
+            _close(np.concatenate([g1[k], g2[k]], axis=-1), whole[k], what=f"split backward {k}, cut {cut}")
+        for k in ("dA", "dD", "ddelta_bias"):
+            _close(g1[k] + g2[k], whole[k], what=f"split backward {k}, cut {cut}")
+        _close(g1["dinitial_state"], whole["dinitial_state"], what=f"split backward dinitial, cut {cut}")
+
+
 def pin_scalar_functions(lib):
     sp = lambda x: oracle.softplus(x, lib=lib)
     si = lambda x: oracle.silu(x, lib=lib)
@@ -511,4 +581,4 @@ ALL_PINS = [pin_brute_force, pin_time_invariant_convolution, pin_associative_sca
             pin_initial_state_brute_force, pin_split_equals_whole, pin_conv_impulse, pin_conv_numpy,
             pin_conv_split_and_decode, pin_bwd_finite_differences, pin_bwd_homogeneity,
             pin_grouped_brute_force, pin_grouped_decode_chain, pin_grouped_bwd_finite_differences,
-            pin_scalar_functions]
+            pin_bwd_from_state_finite_differences, pin_bwd_split_equals_whole, pin_scalar_functions]

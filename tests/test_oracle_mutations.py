@@ -55,6 +55,11 @@ MUTATIONS = [
     ("decode ignores groups", "B + blk * N, C + blk * N, 1,", "B + b * N, C + b * N, 1,"),
     ("grouped dC summed into the batch row", "dC[(blk * N + n) * L + t] += dy * h;",
      "dC[(b * N + n) * L + t] += dy * h;"),
+    ("backward ignores the initial state", "hs[n] = initial_state ? initial_state[sbase + n] : 0.0;",
+     "hs[n] = 0.0;"),
+    ("final-state adjoint ignored", "lam[n] = dlast ? dlast[sbase + n] : 0.0;", "lam[n] = 0.0;"),
+    ("initial-state adjoint without the first decay", "dinitial[sbase + n] = anext[n] * lam[n];",
+     "dinitial[sbase + n] = lam[n];"),
 ]
 
 
