@@ -295,6 +295,33 @@ SSM_API ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const 
                                         void* stream);
 
 /*
+ * ssm_scan_bwd_from_state -- the backward of ssm_scan_fwd_from_state (and of
+ * its grouped form) when the final state also enters the loss: the forward
+ * starts from h_{-1} = initial_state, the adjoint starts from
+ * lambda_{L-1} = C_{L-1} dy_{L-1} + dlast, and
+ *
+ *   initial_state   [batch][dim][dstate]  f32  NULL = zero
+ *   dlast           [batch][dim][dstate]  f32  dL/d last_state; NULL = zero
+ *   dinitial_state  [batch][dim][dstate]  f32  dL/d initial_state = exp(Delta_0 A) lambda_0;
+ *                                              NULL = not computed
+ *
+ * all three 16-byte aligned (SSM_ERR_ALIGN).  A sequence processed in pieces
+ * is differentiated piece by piece, last piece first: each piece's
+ * dinitial_state is the dlast of the piece before it.  Every other argument
+ * is as in ssm_scan_bwd_grouped (ngroups = 1 for shared B and C); the two
+ * inputs may not overlap an output, and dinitial_state may not overlap an
+ * input or another output (SSM_ERR_ALIAS).
+ */
+SSM_API ssm_status ssm_scan_bwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                           const void* C, const float* D, const void* z, const float* delta_bias,
+                                           int softplus_flag, const float* initial_state, const void* dout,
+                                           const float* dlast, void* du, void* ddelta, float* dA, float* dB,
+                                           float* dC, float* dD, void* dz, float* ddelta_bias,
+                                           float* dinitial_state, int64_t batch, int64_t dim, int64_t seqlen,
+                                           int64_t dstate, int64_t ngroups, int dtype, void* workspace,
+                                           int64_t workspace_bytes, void* stream);
+
+/*
  * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs:
  * batch * dim * ceil(seqlen / 8) * dstate * 4 bytes (the state entering
  * every 8-step chunk), at least 16; -1 for sizes or a dtype it would reject.

@@ -25,7 +25,8 @@ EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_
            "ssm_status_string", "ssm_last_launch_error", "ssm_version", "ssm_scan_fwd_noalloc",
            "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state", "ssm_conv1d_fwd",
            "ssm_conv1d_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_bytes", "ssm_scan_fwd_grouped",
-           "ssm_scan_workspace_bytes_grouped", "ssm_state_update_grouped", "ssm_scan_bwd_grouped")
+           "ssm_scan_workspace_bytes_grouped", "ssm_state_update_grouped", "ssm_scan_bwd_grouped",
+           "ssm_scan_bwd_from_state")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -63,6 +64,9 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_scan_bwd_grouped.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, vp, vp, vp, fp, fp, fp, fp, vp, fp,
                                          i64, i64, i64, i64, i64, ci, vp, i64, vp]
     lib.ssm_scan_bwd_grouped.restype = ci
+    lib.ssm_scan_bwd_from_state.argtypes = [vp, vp, fp, vp, vp, fp, vp, fp, ci, fp, vp, fp, vp, vp, fp, fp, fp, fp,
+                                            vp, fp, fp, i64, i64, i64, i64, i64, ci, vp, i64, vp]
+    lib.ssm_scan_bwd_from_state.restype = ci
     lib.ssm_state_update_grouped.argtypes = [fp, vp, vp, fp, vp, vp, fp, vp, fp, vp,
                                              i64, i64, i64, i64, ci, ci, vp]
     lib.ssm_state_update_grouped.restype = ci
@@ -228,11 +232,16 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
 
 def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch.Tensor, C: torch.Tensor,
                  D: Optional[torch.Tensor], z: Optional[torch.Tensor], delta_bias: Optional[torch.Tensor],
-                 softplus: bool, dout: torch.Tensor, workspace: Optional[torch.Tensor] = None) -> dict:
+                 softplus: bool, dout: torch.Tensor, workspace: Optional[torch.Tensor] = None,
+                 initial_state: Optional[torch.Tensor] = None, dlast: Optional[torch.Tensor] = None) -> dict:
     """Gradients of the scan (from h = 0) given dout; see ssm_scan.h.  Returns a
     dict du, ddelta, dz (activation dtype; dz None without z), dA, dB, dC, dD,
     ddelta_bias (float32; None without D / bias).  B, C may be grouped as in
-    ssm_scan_fwd; dB, dC then have their shape (ssm_scan_bwd_grouped)."""
+    ssm_scan_fwd; dB, dC then have their shape (ssm_scan_bwd_grouped).
+    ``initial_state`` (the forward's starting state) and ``dlast`` (dL/d
+    last_state), both (batch, dim, dstate) f32, make it the backward of the
+    scan from a state (ssm_scan_bwd_from_state); the dict then also holds
+    ``dinitial_state`` = dL/d initial_state."""
     lib = load_library()
     dt, dev = u.dtype, u.device
     bt, L, dim = u.shape
@@ -250,6 +259,23 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
             raise ValueError("ssm_scan_bwd: sizes or dtype rejected")
         workspace = torch.empty(nbytes, dtype=torch.uint8, device=dev)
     ws_bytes = workspace.numel() * workspace.element_size()
+    if initial_state is not None or dlast is not None:
+        for name, t in (("initial_state", initial_state), ("dlast", dlast)):
+            if t is not None and tuple(t.shape) != (bt, dim, N):
+                raise ValueError(f"ssm_scan_bwd: {name} must be {(bt, dim, N)}, got {tuple(t.shape)}")
+        g["dinitial_state"] = torch.empty(bt, dim, N, **f32)
+        with torch.cuda.device(dev):
+            code = lib.ssm_scan_bwd_from_state(
+                _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
+                _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev),
+                _ptr(delta_bias, torch.float32, dev), int(bool(softplus)), _ptr(initial_state, torch.float32, dev),
+                _ptr(dout, dt, dev), _ptr(dlast, torch.float32, dev), _ptr(g["du"], dt, dev),
+                _ptr(g["ddelta"], dt, dev), _ptr(g["dA"], torch.float32, dev), _ptr(g["dB"], torch.float32, dev),
+                _ptr(g["dC"], torch.float32, dev), _ptr(g["dD"], torch.float32, dev), _ptr(g["dz"], dt, dev),
+                _ptr(g["ddelta_bias"], torch.float32, dev), _ptr(g["dinitial_state"], torch.float32, dev),
+                bt, dim, L, N, G, _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
+        _check("ssm_scan_bwd_from_state", code)
+        return g
     with torch.cuda.device(dev):
         code = lib.ssm_scan_bwd_grouped(
             _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),

@@ -219,9 +219,15 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         __syncthreads();
     };
 
-    // ---- pass 1: forward, checkpoint the state entering each chunk
+    // ---- pass 1: forward from h_{-1} (the given state, else zero),
+    // checkpoint the state entering each chunk
     const float2 A01 = make_float2(An[0], An[1]), A23 = make_float2(An[2], An[3]);
     float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
+    if (p.h0 && ch_ok) {
+        const float4 v = *reinterpret_cast<const float4*>(p.h0 + (b * dim + d) * N + G * g);
+        h01 = make_float2(v.x, v.y);
+        h23 = make_float2(v.z, v.w);
+    }
     Pre pre;
     fetch(0, false, pre);
     for (int64_t c = 0; c < nch; ++c) {
@@ -242,8 +248,15 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         __syncthreads();
     }
 
-    // ---- pass 2: chunks in reverse
-    float2 lam01 = make_float2(0.f, 0.f), lam23 = lam01, an01 = lam01, an23 = lam01, dA01 = lam01, dA23 = lam01;
+    // ---- pass 2: chunks in reverse.  The adjoint "after" the last step is
+    // dL/d last_state (zero when absent), carried into step L-1 with weight 1.
+    float2 lam01 = make_float2(0.f, 0.f), lam23 = lam01, dA01 = lam01, dA23 = lam01;
+    float2 an01 = make_float2(1.f, 1.f), an23 = an01;
+    if (p.dlast && ch_ok) {
+        const float4 v = *reinterpret_cast<const float4*>(p.dlast + (b * dim + d) * N + G * g);
+        lam01 = make_float2(v.x, v.y);
+        lam23 = make_float2(v.z, v.w);
+    }
     fetch(nch - 1, true, pre);
     for (int64_t c = nch - 1; c >= 0; --c) {
         commit(pre, true);
@@ -353,6 +366,10 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
         }
         __syncthreads();
     }
+    // h_0 = a_0 h_{-1} + ...: the adjoint of the initial state is a_0 lambda_0
+    if (p.dh0 && ch_ok)
+        *reinterpret_cast<float4*>(p.dh0 + (b * dim + d) * N + G * g) =
+            make_float4(an01.x * lam01.x, an01.y * lam01.y, an23.x * lam23.x, an23.y * lam23.y);
     if (ch_ok) {
         float* da = p.dA + d * N + G * g;
         atomicAdd(da, dA01.x);

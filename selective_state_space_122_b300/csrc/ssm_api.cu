@@ -314,12 +314,13 @@ int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen,
     return std::max<int64_t>(16, ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate));
 }
 
-ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                                const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
-                                float* dD, void* dz, float* ddelta_bias, int64_t batch, int64_t dim,
-                                int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype, void* workspace,
-                                int64_t workspace_bytes, void* stream) {
+ssm_status ssm_scan_bwd_from_state(const void* u, const void* delta, const float* A, const void* B,
+                                   const void* C, const float* D, const void* z, const float* delta_bias,
+                                   int softplus_flag, const float* initial_state, const void* dout,
+                                   const float* dlast, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                   float* dD, void* dz, float* ddelta_bias, float* dinitial_state, int64_t batch,
+                                   int64_t dim, int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype,
+                                   void* workspace, int64_t workspace_bytes, void* stream) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !dout || !du || !ddelta || !dA || !dB || !dC || !workspace)
         return SSM_ERR_NULL;
@@ -335,15 +336,18 @@ ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A
         (z && !aligned(z, ea)) || !aligned(du, ea) || !aligned(ddelta, ea) || (dz && !aligned(dz, ea)) ||
         !aligned(A, 4) || (D && !aligned(D, 4)) || (delta_bias && !aligned(delta_bias, 4)) || !aligned(dA, 4) ||
         !aligned(dB, 4) || !aligned(dC, 4) || (dD && !aligned(dD, 4)) || (ddelta_bias && !aligned(ddelta_bias, 4)) ||
-        !aligned(workspace, 16))
+        !aligned(workspace, 16) || (initial_state && !aligned(initial_state, 16)) || (dlast && !aligned(dlast, 16)) ||
+        (dinitial_state && !aligned(dinitial_state, 16)))
         return SSM_ERR_ALIGN;
     const int64_t x_bytes = batch * seqlen * dim * es, bc_bytes = batch * ngroups * dstate * seqlen * es;
     const int64_t gbc_bytes = batch * ngroups * dstate * seqlen * 4;
+    const int64_t st_bytes = batch * dim * dstate * 4;
     const Span ins[] = {{u, x_bytes}, {delta, x_bytes}, {z, x_bytes}, {dout, x_bytes}, {B, bc_bytes},
-                        {C, bc_bytes}, {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4}};
+                        {C, bc_bytes}, {A, dim * dstate * 4}, {D, dim * 4}, {delta_bias, dim * 4},
+                        {initial_state, st_bytes}, {dlast, st_bytes}};
     const Span outs[] = {{du, x_bytes}, {ddelta, x_bytes}, {dz, x_bytes}, {dA, dim * dstate * 4},
                          {dB, gbc_bytes}, {dC, gbc_bytes}, {dD, dim * 4},
-                         {ddelta_bias, dim * 4}, {workspace, workspace_bytes}};
+                         {ddelta_bias, dim * 4}, {workspace, workspace_bytes}, {dinitial_state, st_bytes}};
     for (size_t i = 0; i < sizeof(outs) / sizeof(outs[0]); ++i) {
         for (const Span& s : ins)
             if (overlap(outs[i], s)) return SSM_ERR_ALIAS;
@@ -357,8 +361,22 @@ ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A
                    (int)dstate};
     a.ngroups = ngroups;
     a.gch = dim / ngroups;
+    a.h0 = initial_state;
+    a.dlast = dlast;
+    a.dh0 = dinitial_state;
     return launch_status(ssm::launch_scan_bwd(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32, workspace,
                                               sms, static_cast<cudaStream_t>(stream)));
+}
+
+ssm_status ssm_scan_bwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const void* dout, void* du, void* ddelta, float* dA, float* dB, float* dC,
+                                float* dD, void* dz, float* ddelta_bias, int64_t batch, int64_t dim,
+                                int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype, void* workspace,
+                                int64_t workspace_bytes, void* stream) {
+    return ssm_scan_bwd_from_state(u, delta, A, B, C, D, z, delta_bias, softplus_flag, nullptr, dout, nullptr, du,
+                                   ddelta, dA, dB, dC, dD, dz, ddelta_bias, nullptr, batch, dim, seqlen, dstate,
+                                   ngroups, dtype, workspace, workspace_bytes, stream);
 }
 
 ssm_status ssm_scan_bwd(const void* u, const void* delta, const float* A, const void* B, const void* C,

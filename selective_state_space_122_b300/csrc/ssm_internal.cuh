@@ -121,6 +121,11 @@ struct BwdArgs {
     int dstate;
     int64_t ngroups = 1;   // B, C, dB, dC: (batch, ngroups, dstate, seqlen)
     int64_t gch = 0;       // channels per group (dim / ngroups)
+    // scan from a given state whose final state enters the loss (all nullable):
+    // h_{-1}, dL/d last_state in, dL/d h_{-1} out; (batch, dim, dstate) f32
+    const float* h0 = nullptr;
+    const float* dlast = nullptr;
+    float* dh0 = nullptr;
 };
 int64_t bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate);
 cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms, cudaStream_t s);

@@ -310,3 +310,26 @@ def test_binding_checks_bc_shapes():
     st = torch.zeros(2, 8, 4)
     with pytest.raises(ValueError, match="B and C must be"):
         _lib.ssm_state_update(st, u[:, 0], u[:, 0], A, torch.zeros(2, 2, 5), torch.zeros(2, 2, 5))
+
+
+@pytest.mark.parametrize("kw,code", [
+    (dict(h0=P + 1200 * MB + 4), 3), (dict(dlast=P + 1264 * MB + 8), 3), (dict(dh0=P + 1328 * MB + 4), 3),
+    (dict(dh0=P + 704 * MB), 6),                  # the initial-state gradient inside dA
+    (dict(dh0=P + 1200 * MB), 6),                 # ... over the initial state (an input)
+    (dict(h0=P + 576 * MB), 6),                   # the initial state inside du (an output)
+    (dict(dlast=P + 640 * MB + 64), 6),           # dlast inside ddelta
+    (dict(ngroups=3), 2), (dict(du=None), 1),
+])
+def test_scan_bwd_from_state_rejects_bad_arguments(lib, kw, code):
+    """Host checks of ssm_scan_bwd_from_state (fake addresses; every case is
+    rejected before anything is enqueued)."""
+    a = dict(u=P, delta=P + 64 * MB, A=P + 128 * MB, B=P + 192 * MB, C=P + 256 * MB, D=P + 320 * MB,
+             z=P + 384 * MB, bias=P + 448 * MB, dout=P + 512 * MB, du=P + 576 * MB, dd=P + 640 * MB,
+             dA=P + 704 * MB, dB=P + 768 * MB, dC=P + 832 * MB, dD=P + 896 * MB, dz=P + 960 * MB,
+             db=P + 1024 * MB, ws=P + 1088 * MB, ws_bytes=64 * MB, h0=P + 1200 * MB, dlast=P + 1264 * MB,
+             dh0=P + 1328 * MB, batch=2, dim=64, seqlen=128, dstate=16, ngroups=1, dtype=1)
+    a.update(kw)
+    assert lib.ssm_scan_bwd_from_state(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], 1,
+                                       a["h0"], a["dout"], a["dlast"], a["du"], a["dd"], a["dA"], a["dB"], a["dC"],
+                                       a["dD"], a["dz"], a["db"], a["dh0"], a["batch"], a["dim"], a["seqlen"],
+                                       a["dstate"], a["ngroups"], a["dtype"], a["ws"], a["ws_bytes"], None) == code

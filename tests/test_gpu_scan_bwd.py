@@ -79,3 +79,32 @@ def test_scan_bwd_prefill_shape():
         _close(host_f64(g[k]), ref[k], 1e-4, k, rounded=True)
     for k in ("dA", "dB", "dC", "dD", "ddelta_bias"):
         _close(host_f64(g[k]), ref[k], 1e-4, k)
+
+
+@pytest.mark.parametrize("bt,dim,L,N,dtype,G", [
+    (2, 64, 300, 16, inputs.BF16, 1),
+    (1, 40, 100, 8, inputs.F32, 2),
+    (2, 96, 129, 4, inputs.F32, 1),
+    (2, 128, 77, 16, inputs.BF16, 4),
+])
+def test_scan_bwd_from_state(bt, dim, L, N, dtype, G):
+    """The backward of the scan from a given state whose final state enters the
+    loss (ssm_scan_bwd_from_state) against the oracle, dL/d initial_state
+    included."""
+    inp = inputs.make_scan_inputs(inputs.ScanShape("bwd-h0", bt, dim, L, N, dtype), 1500 + dim + L, ngroups=G)
+    r = np.random.Generator(np.random.PCG64(1600 + L))
+    dout = inputs._activation(r, (bt, L, dim), dtype)
+    h0 = (r.standard_normal((bt, dim, N)) * 0.5).astype(np.float32)
+    dlast = r.standard_normal((bt, dim, N)).astype(np.float32)
+    f = inp.as_f64()
+    dout_f = inputs.bf16_bits_to_f64(dout) if dtype == inputs.BF16 else dout.astype(np.float64)
+    ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"], f["delta_bias"],
+                          f["softplus"], dout_f, initial_state=h0.astype(np.float64), dlast=dlast.astype(np.float64))
+    g = ssm_scan_bwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D), dev(inp.z),
+                     dev(inp.delta_bias), inp.softplus, dev(dout), initial_state=dev(h0), dlast=dev(dlast))
+    torch.cuda.synchronize()
+    bf = dtype == inputs.BF16
+    for k in ("du", "ddelta", "dz"):
+        _close(host_f64(g[k]), ref[k], 1e-4, k, rounded=bf)
+    for k in ("dA", "dB", "dC", "dD", "ddelta_bias", "dinitial_state"):
+        _close(host_f64(g[k]), ref[k], 1e-4, k)
