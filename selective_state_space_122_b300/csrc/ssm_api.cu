@@ -20,6 +20,14 @@ std::atomic<int> g_sm_count[kMaxDevices];
 
 bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
 
+// a * b > limit for positive a, b, without forming the (possibly overflowing) product
+bool prod_exceeds(int64_t a, int64_t b, int64_t limit) { return a > limit / b; }
+
+// batch * seqlen * dim above the element limit (all positive)
+bool too_many_elems(int64_t batch, int64_t seqlen, int64_t dim) {
+    return prod_exceeds(batch, seqlen, kMaxElems) || prod_exceeds(batch * seqlen, dim, kMaxElems);
+}
+
 struct Span {
     const void* p;
     int64_t bytes;
@@ -128,7 +136,7 @@ int64_t ssm_scan_workspace_bytes_grouped(int64_t batch, int64_t dim, int64_t seq
     if (dim <= 0 || dim >= (int64_t(1) << 31)) return -1;
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
-    if (ngroups <= 0 || dim % ngroups != 0) return -1;
+    if (ngroups <= 0 || dim % ngroups != 0 || too_many_elems(batch, seqlen, dim)) return -1;
     int64_t need = std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate, ngroups),
                             ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4,
                                                      ngroups));
@@ -157,7 +165,7 @@ ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A
     if (ngroups <= 0 || dim % ngroups != 0) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
     if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
-    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    if (too_many_elems(batch, seqlen, dim)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     const uintptr_t ea = (uintptr_t)es;
     if (!aligned(u, ea) || !aligned(delta, ea) || !aligned(B, ea) || !aligned(C, ea) ||
@@ -259,7 +267,7 @@ ssm_status ssm_conv1d_fwd(const void* x, const float* weight, const float* bias,
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || width <= 0) return SSM_ERR_SHAPE;
     if (width > 4) return SSM_ERR_UNSUPPORTED;
     if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
-    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    if (too_many_elems(batch, seqlen, dim)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 4) || (bias && !aligned(bias, 4)) ||
         (conv_state_in && !aligned(conv_state_in, 4)) || (conv_state_out && !aligned(conv_state_out, 4)))
@@ -288,7 +296,7 @@ ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weig
     if (!x || !weight || !out || (width > 1 && !conv_state)) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || width <= 0) return SSM_ERR_SHAPE;
     if (width > 4) return SSM_ERR_UNSUPPORTED;
-    if (batch * dim > kMaxElems / 16) return SSM_ERR_SHAPE;
+    if (prod_exceeds(batch, dim, kMaxElems / 16)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     if (!aligned(x, es) || !aligned(out, es) || !aligned(weight, 4) || (bias && !aligned(bias, 4)) ||
         (conv_state && !aligned(conv_state, 4)))
@@ -309,7 +317,7 @@ ssm_status ssm_conv1d_update(float* conv_state, const void* x, const float* weig
 int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate, int dtype) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return -1;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || dim >= (int64_t(1) << 31) ||
-        seqlen > (int64_t(1) << 40))
+        seqlen > (int64_t(1) << 40) || too_many_elems(batch, seqlen, dim))
         return -1;
     return std::max<int64_t>(16, ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate));
 }
@@ -328,7 +336,7 @@ ssm_status ssm_scan_bwd_from_state(const void* u, const void* delta, const float
     if (ngroups <= 0 || dim % ngroups != 0) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
     if (batch > 65535 || dim >= (int64_t(1) << 31) || seqlen > (int64_t(1) << 40)) return SSM_ERR_SHAPE;
-    if (batch * seqlen > kMaxElems || (batch * seqlen) * dim > kMaxElems) return SSM_ERR_SHAPE;
+    if (too_many_elems(batch, seqlen, dim)) return SSM_ERR_SHAPE;
     if (workspace_bytes < ssm::bwd_workspace_bytes(batch, dim, seqlen, (int)dstate)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     const uintptr_t ea = (uintptr_t)es;
@@ -398,7 +406,7 @@ ssm_status ssm_state_update_grouped(float* state, const void* x, const void* dt,
     if (batch <= 0 || dim <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
     if (ngroups <= 0 || dim % ngroups != 0 || dim >= (int64_t(1) << 31)) return SSM_ERR_SHAPE;
     if (!dstate_ok(dstate)) return SSM_ERR_UNSUPPORTED;
-    if (batch * dim > kMaxElems / 16) return SSM_ERR_SHAPE;
+    if (prod_exceeds(batch, dim, kMaxElems / 16)) return SSM_ERR_SHAPE;
     const int64_t es = dtype == SSM_BF16 ? 2 : 4;
     const uintptr_t ea = (uintptr_t)es;
     if (!aligned(state, 16) || !aligned(A, 16) || !aligned(x, ea) || !aligned(dt, ea) ||

@@ -333,3 +333,18 @@ def test_scan_bwd_from_state_rejects_bad_arguments(lib, kw, code):
                                        a["h0"], a["dout"], a["dlast"], a["du"], a["dd"], a["dA"], a["dB"], a["dC"],
                                        a["dD"], a["dz"], a["db"], a["dh0"], a["batch"], a["dim"], a["seqlen"],
                                        a["dstate"], a["ngroups"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
+
+
+def test_size_products_that_overflow_64_bits_are_rejected(lib):
+    """batch * seqlen * dim (or batch * dim) beyond 64 bits must not wrap into
+    an accepted size: every such call is SSM_ERR_SHAPE before anything else."""
+    big = dict(batch=1, seqlen=1 << 40, dim=1 << 30)     # 2^70 elements
+    assert call_scan(lib, scan_args(**big)) == 2
+    assert call_scan_grouped(lib, scan_args(**big), 1) == 2
+    assert lib.ssm_scan_workspace_bytes(1, 1 << 30, 1 << 40, 16, 1) == -1
+    assert lib.ssm_scan_workspace_bytes_grouped(1, 1 << 30, 1 << 40, 16, 1, 1) == -1
+    assert lib.ssm_scan_bwd_workspace_bytes(1, 1 << 30, 1 << 40, 16, 1) == -1
+    assert call_conv(lib, batch=1, seqlen=1 << 40, dim=1 << 30) == 2
+    assert call_upd(lib, upd_args(batch=1 << 62, dim=4)) == 2
+    a = dict(state=P + 192 * MB, x=P, w=P + 64 * MB, bias=P + 128 * MB, out=P + 256 * MB)
+    assert lib.ssm_conv1d_update(a["state"], a["x"], a["w"], a["bias"], 1, a["out"], 1 << 62, 4, 4, 1, None) == 2
