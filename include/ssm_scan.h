@@ -2,7 +2,7 @@
  * ssm_scan.h -- C ABI of the B300 (sm_103a) selective-scan library
  * (libssmscan.so).
  *
- * Two operations, both from the Mamba selective state-space model:
+ * Two operations of the Mamba selective state-space model at the core:
  *
  *   ssm_scan_fwd      the full-sequence selective scan (prefill / training
  *                     forward): "Efficient Scan" of the Mamba README
@@ -13,6 +13,12 @@
  *   ssm_state_update  the single-token recurrent update used for
  *                     constant-memory inference ("Efficient Scan", item 2:
  *                     sequential scan, O(1) memory).
+ *
+ * and around them: the scan from a given state (ssm_scan_fwd_from_state), B
+ * and C per channel group (the *_grouped calls), the scan's backward
+ * (ssm_scan_bwd, ssm_scan_bwd_from_state), the depthwise causal conv1d that
+ * produces the scan input (ssm_conv1d_fwd, ssm_conv1d_update), and the scan
+ * without a caller workspace (ssm_scan_fwd_noalloc).
  *
  * Per (batch b, channel d) both compute, with h = 0 before the first step:
  *
