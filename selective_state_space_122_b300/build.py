@@ -7,7 +7,7 @@
   for its roofline denominators (not part of the scan path).
 
 nvcc cross-compiles without a GPU.  Both libraries statically link the CUDA
-runtime, so they only need the driver at run time.  The sources compile to
+runtime, so they only need the NVIDIA GPU driver at run time.  The sources compile to
 objects in parallel (under _build/ next to this file), then link once.
 """
 from __future__ import annotations
