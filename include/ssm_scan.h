@@ -392,9 +392,10 @@ SSM_API const char* ssm_status_string(int status);
  * every GPU loading the library holds until the process exits.  It performs
  * no allocation of any kind; the caller still passes every input and output.
  *
- * - Sizes whose workspace (ssm_scan_workspace_bytes) exceeds the array are
- *   rejected with SSM_ERR_SCRATCH before anything is enqueued; invalid
- *   arguments get the same codes as ssm_scan_fwd.
+ * - Invalid arguments get the same codes as ssm_scan_fwd, checked first;
+ *   valid sizes whose workspace (ssm_scan_workspace_bytes) exceeds the array
+ *   are then rejected with SSM_ERR_SCRATCH.  Either way nothing is enqueued
+ *   and the device is not touched.
  * - The first call on each device looks up the array's device address
  *   (cudaGetSymbolAddress, with that device current) and caches it; make that
  *   first call before any stream capture.

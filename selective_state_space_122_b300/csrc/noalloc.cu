@@ -56,12 +56,15 @@ ssm_status ssm_scan_fwd_noalloc(const void* u, const void* delta, const float* A
                                 const void* C, const float* D, const void* z, const float* delta_bias,
                                 int softplus_flag, void* out, float* last_state, int64_t batch,
                                 int64_t dim, int64_t seqlen, int64_t dstate, int dtype, void* stream) {
+    // the scan's own checks first (dtype, pointers, sizes, alignment,
+    // aliasing), so an invalid call gets the code ssm_scan_fwd would return;
+    // only a valid call can be refused for its size
+    if (const int chk = ssm::check_scan_call(u, delta, A, B, C, D, z, delta_bias, nullptr, out, last_state, batch,
+                                             dim, seqlen, dstate, 1, dtype, nullptr, 0);
+        chk != SSM_OK)
+        return static_cast<ssm_status>(chk);
     const int64_t need = ssm_scan_workspace_bytes(batch, dim, seqlen, dstate, dtype);
-    if (need < 0) {
-        // the sizes or dtype are invalid: let the scan report the exact error
-        return ssm_scan_fwd(u, delta, A, B, C, D, z, delta_bias, softplus_flag, out, last_state, batch, dim,
-                            seqlen, dstate, dtype, nullptr, 0, stream);
-    }
+    if (need < 0) return SSM_ERR_SHAPE;
     if (need > kNoAllocScratchBytes) return SSM_ERR_SCRATCH;
     void* scratch = nullptr;
     if (ssm_status st = scratch_for_current_device(&scratch); st != SSM_OK) return st;

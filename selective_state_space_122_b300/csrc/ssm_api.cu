@@ -154,11 +154,16 @@ int ssm_device_error(int clear) {
     return (a < 0 || b < 0) ? -1 : (a | b);
 }
 
-ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
-                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
-                                const float* initial_state, void* out, float* last_state, int64_t batch,
-                                int64_t dim, int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype,
-                                void* workspace, int64_t workspace_bytes, void* stream) {
+}  // extern "C"
+
+namespace ssm {
+
+// Every host-side check of a (grouped) scan call: dtype, pointers, sizes,
+// alignment and aliasing, in that order.  Nothing touches the device.
+int check_scan_call(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* delta_bias, const float* initial_state, const void* out,
+                    const float* last_state, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                    int64_t ngroups, int dtype, const void* workspace, int64_t workspace_bytes) {
     if (dtype != SSM_F32 && dtype != SSM_BF16) return SSM_ERR_DTYPE;
     if (!u || !delta || !A || !B || !C || !out) return SSM_ERR_NULL;
     if (batch <= 0 || dim <= 0 || seqlen <= 0 || dstate <= 0) return SSM_ERR_SHAPE;
@@ -200,6 +205,23 @@ ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A
             if (overlap(sw, s)) return SSM_ERR_ALIAS;
         if (overlap(sw, so) || overlap(sw, sl) || overlap(sw, sh)) return SSM_ERR_ALIAS;
     }
+    return SSM_OK;
+}
+
+}  // namespace ssm
+
+extern "C" {
+
+ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A, const void* B, const void* C,
+                                const float* D, const void* z, const float* delta_bias, int softplus_flag,
+                                const float* initial_state, void* out, float* last_state, int64_t batch,
+                                int64_t dim, int64_t seqlen, int64_t dstate, int64_t ngroups, int dtype,
+                                void* workspace, int64_t workspace_bytes, void* stream) {
+    if (const int chk = ssm::check_scan_call(u, delta, A, B, C, D, z, delta_bias, initial_state, out, last_state,
+                                             batch, dim, seqlen, dstate, ngroups, dtype, workspace, workspace_bytes);
+        chk != SSM_OK)
+        return static_cast<ssm_status>(chk);
+    const int64_t es = dtype == SSM_BF16 ? 2 : 4;
 
     int sms = 0;
     if (ssm_status st = sm_count(&sms); st != SSM_OK) return st;
@@ -229,6 +251,10 @@ ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A
     if (force && (std::strcmp(force, "tmem") == 0 || std::strcmp(force, "tmem2") == 0)) {
         if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
         return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, force[4] == '2' ? 2 : 4));
+    }
+    if (force && std::strcmp(force, "ws") == 0) {
+        if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 3));
     }
     if (!want_generic && !want_seg && tmem_ok)
         return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 2));

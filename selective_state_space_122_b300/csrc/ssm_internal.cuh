@@ -139,6 +139,13 @@ cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int s
 int read_tmem_device_error(bool clear);
 int read_device_error(bool clear);
 
+// Every host-side check of a scan call (ssm_api.cu): returns SSM_OK or the
+// ssm_status code the call would return, touching no device state.
+int check_scan_call(const void* u, const void* delta, const float* A, const void* B, const void* C, const float* D,
+                    const void* z, const float* delta_bias, const float* initial_state, const void* out,
+                    const float* last_state, int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
+                    int64_t ngroups, int dtype, const void* workspace, int64_t workspace_bytes);
+
 int scan_layout_count(int dstate);
 ScanLayoutInfo scan_layout_info(int dstate, int layout);
 cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s);

@@ -348,3 +348,35 @@ def test_size_products_that_overflow_64_bits_are_rejected(lib):
     assert call_upd(lib, upd_args(batch=1 << 62, dim=4)) == 2
     a = dict(state=P + 192 * MB, x=P, w=P + 64 * MB, bias=P + 128 * MB, out=P + 256 * MB)
     assert lib.ssm_conv1d_update(a["state"], a["x"], a["w"], a["bias"], 1, a["out"], 1 << 62, 4, 4, 1, None) == 2
+
+
+def _noalloc_call(lib, **kw):
+    """ssm_scan_fwd_noalloc on fake, non-overlapping addresses (never dereferenced:
+    every case here is refused on the host)."""
+    G = 1 << 30
+    a = dict(u=P, delta=P + G, A=P + 2 * G, B=P + 3 * G, C=P + 4 * G, D=None, z=None, delta_bias=None,
+             out=P + 5 * G, last=None, batch=4, dim=64, seqlen=131072, dstate=16, dtype=_lib.SSM_BF16)
+    a.update(kw)
+    return lib.ssm_scan_fwd_noalloc(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["delta_bias"], 1,
+                                    a["out"], a["last"], a["batch"], a["dim"], a["seqlen"], a["dstate"], a["dtype"],
+                                    None)
+
+
+def test_noalloc_rejects_sizes_beyond_its_scratch(lib):
+    """A valid call whose workspace exceeds the fixed array is SSM_ERR_SCRATCH,
+    decided on the host before the device is touched."""
+    cap = lib.ssm_scan_noalloc_max_workspace_bytes()
+    assert cap == 32 << 20
+    # batch 4 x 131072 steps x N 16: 4 * 131072 * 128 bytes of staged B/C > 32 MiB
+    assert lib.ssm_scan_workspace_bytes(4, 64, 131072, 16, _lib.SSM_BF16) > cap
+    code = _noalloc_call(lib)
+    assert code == 9 and _lib.status_string(code).startswith("SSM_ERR_SCRATCH")
+
+
+@pytest.mark.parametrize("kw,code", [(dict(u=None), 1), (dict(out=P + 1), 3), (dict(out=P + 64), 6),
+                                     (dict(dtype=7), 5), (dict(dstate=5), 4), (dict(batch=0), 2)],
+                         ids=["null", "misaligned", "alias", "dtype", "dstate", "shape"])
+def test_noalloc_checks_arguments_before_its_scratch(lib, kw, code):
+    """Over-large sizes with a bad argument get the scan's own code for that
+    argument, not SSM_ERR_SCRATCH: the argument checks come first."""
+    assert _noalloc_call(lib, **kw) == code

@@ -4,8 +4,10 @@ Callers inside a framework whose allocator owns the device memory, or code
 that must not allocate in its hot loop, cannot hand ssm_scan_fwd a workspace;
 ssm_scan_fwd_noalloc runs the same scan on a fixed scratch array inside the
 library instead.  These tests call it through the C ABI and compare it with
-ssm_scan_fwd on the same inputs, twice in a row (every call reuses the one
-array).  This file is collected last on purpose.
+ssm_scan_fwd, twice in a row on different inputs (every call reuses the one
+array, so the second call must not lean on what the first left there).  Its
+refusal of sizes beyond the array is pure host logic, tested in the CPU suite
+(test_abi_cpu.py).  This file is collected last on purpose.
 """
 from __future__ import annotations
 
@@ -40,25 +42,15 @@ def _noalloc(lib, inp, out, last):
                          ids=lambda s: s.name)
 def test_noalloc_matches_scan_two_calls_in_a_row(shape):
     lib = _lib.load_library()
-    inp = inputs.make_scan_inputs(shape, 91)
-    ref_out, ref_last = ssm_scan_fwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C),
-                                     dev(inp.D), dev(inp.z), dev(inp.delta_bias), True, return_last_state=True)
-    torch.cuda.synchronize()
-    for _ in range(2):
+    # two calls in a row on different seeded inputs: state or flags the first
+    # call left in the shared array must not leak into the second's result
+    for seed in (91, 92):
+        inp = inputs.make_scan_inputs(shape, seed)
+        ref_out, ref_last = ssm_scan_fwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C),
+                                         dev(inp.D), dev(inp.z), dev(inp.delta_bias), True, return_last_state=True)
+        torch.cuda.synchronize()
         out = torch.full_like(ref_out, float("nan"))
         last = torch.full_like(ref_last, float("nan"))
         assert _noalloc(lib, inp, out, last) == 0
-        check_out(host_f64(out), host_f64(ref_out), shape.dtype, "noalloc out", rounded_sides=2)
-        check_state(host_f64(last), host_f64(ref_last), shape.dtype, "noalloc last_state")
-
-
-def test_noalloc_rejects_sizes_beyond_its_scratch():
-    lib = _lib.load_library()
-    cap = lib.ssm_scan_noalloc_max_workspace_bytes()
-    assert cap == 32 << 20
-    # batch 4 x 131072 steps x N 16: 4 * 131072 * 128 bytes of staged B/C > 32 MiB
-    assert lib.ssm_scan_workspace_bytes(4, 64, 131072, 16, _lib.SSM_BF16) > cap
-    fake = 0x10000000   # never dereferenced: the size check comes first
-    code = lib.ssm_scan_fwd_noalloc(fake, fake + (1 << 30), fake, fake, fake, None, None, None, 1,
-                                    fake + (2 << 30), None, 4, 64, 131072, 16, _lib.SSM_BF16, None)
-    assert code == 9 and _lib.status_string(code).startswith("SSM_ERR_SCRATCH")
+        check_out(host_f64(out), host_f64(ref_out), shape.dtype, f"noalloc out (seed {seed})", rounded_sides=2)
+        check_state(host_f64(last), host_f64(ref_last), shape.dtype, f"noalloc last_state (seed {seed})")
