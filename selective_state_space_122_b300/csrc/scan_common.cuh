@@ -144,18 +144,36 @@ __device__ __forceinline__ void st_pair<__nv_bfloat16>(__nv_bfloat16* p0, __nv_b
     *p1 = b.y;
 }
 
-// softplus(x) = max(x, 0) + log1p(exp(-|x|)) with log1p(e) = ln2 * log2(1 + e):
-// branch-free, absolute error about 1e-7 (the rounding of 1 + e).
-__device__ __forceinline__ float2 softplus_lean2(float2 x) {
+// log1p(e) for e in [0, 1] as e * q(e), q a degree-7 polynomial fitted to
+// log1p(e) / e on [0, 1] (least-squares iterated towards the minimax
+// relative error; q(0) = 1 exactly).  Relative error below 4e-7 over the
+// whole interval when evaluated in float32, so log1p(e) keeps every digit the
+// bf16 inputs carry down to e -> 0, where ln2 * log2(1 + e) would lose
+// them to the rounding of 1 + e.
+__device__ __forceinline__ float2 log1p_unit2(float2 e) {
+    float2 q = splat2(-8.778980002e-03f);
+    q = fma2(q, e, splat2(4.498671740e-02f));
+    q = fma2(q, e, splat2(-1.090230048e-01f));
+    q = fma2(q, e, splat2(1.784721315e-01f));
+    q = fma2(q, e, splat2(-2.453686744e-01f));
+    q = fma2(q, e, splat2(3.328406513e-01f));
+    q = fma2(q, e, splat2(-4.999817908e-01f));
+    q = fma2(q, e, splat2(1.f));
+    return mul2(q, e);
+}
+
+// softplus(x) = max(x, 0) + log1p(e^-|x|) for two values: one SFU exp2 each
+// and the polynomial log1p above.  Relative error below 1e-6 for every x
+// (the e^-|x| of ex2.approx and the polynomial); large |x| needs no special
+// case (e underflows to 0 and the result is max(x, 0)).
+__device__ __forceinline__ float2 softplus_poly2(float2 x) {
     const float2 e = make_float2(ex2_approx(-fabsf(x.x) * kLog2e), ex2_approx(-fabsf(x.y) * kLog2e));
-    const float2 w = add2(e, splat2(1.f));
-    const float2 l = make_float2(lg2_approx(w.x), lg2_approx(w.y));
-    return fma2(l, splat2(kLn2), make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)));
+    return add2(make_float2(fmaxf(x.x, 0.f), fmaxf(x.y, 0.f)), log1p_unit2(e));
 }
 
 template <bool kFast>
 __device__ __forceinline__ float2 relay_softplus2(float2 x) {
-    if constexpr (kFast) return softplus_lean2(x);
+    if constexpr (kFast) return softplus_poly2(x);
     else return make_float2(softplus_acc(x.x), softplus_acc(x.y));
 }
 
