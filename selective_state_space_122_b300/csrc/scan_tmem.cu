@@ -1047,6 +1047,494 @@ __global__ void __launch_bounds__(256) tm2_stage_kernel(const __nv_bfloat16* __r
     }
 }
 
+// ===================================================================
+// Warp-specialised scan: four states per lane, the per-(t, d) work on
+// separate warps.
+//
+// The recurrence warps (one per TMEM lane quarter) do only the per-element
+// work: a lane keeps states 4g .. 4g+3 of one channel (lane = c + 8 g, eight
+// channels per warp), reads Delta and Delta u of its channel with one 16-byte
+// shared load per step (stored duplicated, {Delta, Delta, Delta u, Delta u},
+// so the packed multiplies take them as they are), B and C from tensor memory
+// (the one-hot product of the four-state layout), and sums C . h over its
+// four states.  The four partial sums of a channel are combined over the
+// channel's four lanes where the output is made: every lane stores its
+// partial sum of each step into a shared buffer (one 4-byte store per step,
+// 128 contiguous bytes per warp), which costs the recurrence far less than
+// any exchange between its lanes.
+//
+// The aux warps (one per scheduler as well) do the per-(t, d) work on both
+// sides of the recurrence: per chunk, lane (channel octet, step) reads eight
+// channels of u, delta_raw and z with one 16-byte load each, computes Delta
+// (softplus with a polynomial log1p, accurate for every Delta), Delta u,
+// D u and silu(z), and writes the recurrence's input rows; one chunk later
+// it reads the four partial sums of each of its items back (one 16-byte
+// load), adds them and D u, applies the gate and writes eight bf16 outputs
+// with one 16-byte store into the output tile.
+//
+// Work split, TMA ring, one-hot MMA, segments and bounded waits are those of
+// the kernels above.
+// ===================================================================
+
+struct WsCfg {
+    static constexpr int N = 16;
+    static constexpr int G = 4;                 // states per lane
+    static constexpr int CW = 8;                // channels per recurrence warp
+    static constexpr int RW = 4;                // recurrence warps = TMEM lane quarters
+    static constexpr int AW = 4;                // aux warps
+    static constexpr int CC = RW * CW;          // channels per CTA (32)
+    static constexpr int K = 32;                // steps per chunk
+    static constexpr int P = 6;                 // input ring slots
+    static constexpr int OB = 3;                // output tiles
+    static constexpr int W_AUX = RW;
+    static constexpr int W_LOAD = RW + AW, W_MMA = W_LOAD + 1, W_STORE = W_LOAD + 2;
+    static constexpr int THREADS = 32 * (W_STORE + 1);
+    static constexpr int ROWB = CC * 2;         // 64-byte tile rows
+    static constexpr int TILE = K * ROWB;
+    static constexpr int OPB = K * 8 * 16;      // X: 8 columns x 4 tf32 per step
+    static constexpr int TCOLS = 8 * K;         // TMEM columns of a chunk (256)
+    static constexpr int TMEM_COLS = 2 * TCOLS;
+    static_assert(TCOLS <= 256 && TMEM_COLS <= 512, "one MMA per chunk, two chunks of TMEM");
+    static constexpr int SLOT_U = 0;
+    static constexpr int SLOT_D = tm_al(TILE, 1024);
+    static constexpr int SLOT_Z = 2 * tm_al(TILE, 1024);
+    static constexpr int SLOT_X = 3 * tm_al(TILE, 1024);
+    static constexpr int SLOT = tm_al(SLOT_X + OPB, 1024);
+    static constexpr int A_OP = P * SLOT;                 // 128 x 8 tf32 selector
+    static constexpr int REC = A_OP + 4096;               // [2][K][CC] float4 {Delta, Delta, Delta u, Delta u}
+    static constexpr int REC_BYTES = K * CC * 16;
+    static constexpr int YB = REC + 2 * REC_BYTES;        // [2][K][CC][4] f32 partial readouts
+    static constexpr int YB_BYTES = K * CC * 16;
+    static constexpr int OUT = tm_al(YB + 2 * YB_BYTES, 1024);
+    static constexpr int OUTT = tm_al(TILE, 1024);
+    static constexpr int BAR = OUT + OB * OUTT;
+    // full[P] empty[P] ready[2] done[2] ofull[OB] oempty[OB]
+    static constexpr int NBAR = 2 * P + 4 + 2 * OB;
+    static constexpr int USED = BAR + NBAR * 8 + 16;
+    // over half of an SM's shared memory: one CTA per SM, so its 512 TMEM
+    // columns are always free
+    static constexpr int SMEM = (USED + 1024 > 120 * 1024) ? USED + 1024 : 120 * 1024;
+    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
+};
+
+// Byte offset of the 16-byte group o of row r of a 64-byte-row tile laid out
+// by TMA with the 64-byte swizzle (group index XOR address bits 7-8).
+__device__ __forceinline__ uint32_t swz64_group(int r, int o) {
+    return (uint32_t)(r * 64 + ((o ^ ((r >> 1) & 3)) << 4));
+}
+
+// bf16 pair (one 32-bit word) -> two floats
+__device__ __forceinline__ float2 bf2_to_f2(uint32_t w) {
+    return make_float2(__uint_as_float(w << 16), __uint_as_float(w & 0xffff0000u));
+}
+
+__device__ __forceinline__ uint32_t f2_to_bf2(float2 v) {
+    const __nv_bfloat162 b = __floats2bfloat162_rn(v.x, v.y);
+    return *reinterpret_cast<const uint32_t*>(&b);
+}
+
+// 16-byte slot (t, channel) of a chunk's recurrence input rows and of its
+// partial readouts, XOR-swizzled within each channel octet so that the aux
+// warps' accesses (one channel octet, 8 steps per quarter-warp) and the
+// recurrence warps' (8 channels of one step) are free of bank conflicts.
+__device__ __forceinline__ int ws_rec_slot(int t, int col) { return t * 32 + (col ^ (t & 7)); }
+
+template <bool kSoftplus, bool kGate>
+__global__ void __launch_bounds__(WsCfg::THREADS, 1)
+scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
+               const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
+               const TmParams p) {
+    using CF = WsCfg;
+    constexpr int N = CF::N, K = CF::K, P = CF::P, OB = CF::OB, CC = CF::CC;
+    extern __shared__ __align__(1024) unsigned char smem_raw[];
+    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
+
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const uint32_t ring_s = smem_u32(smem);
+    const uint32_t bar_full = smem_u32(smem + CF::BAR);
+    const uint32_t bar_empty = bar_full + 8u * P;
+    // ready[b]: chunk j (b = j & 1) may be scanned -- its MMA has filled TMEM
+    // buffer b and the aux warps have written its recurrence rows (after
+    // finishing the output of chunk j - 2, so the partial-sum buffer is free);
+    // done[b]: the recurrence warps have finished chunk j -- TMEM buffer,
+    // recurrence rows and partial sums of b may be read or reused
+    const uint32_t bar_ready = bar_empty + 8u * P;
+    const uint32_t bar_done = bar_ready + 16u;
+    const uint32_t bar_ofull = bar_done + 16u;
+    const uint32_t bar_oempty = bar_ofull + 8u * OB;
+    uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(smem + CF::BAR + CF::NBAR * 8);
+
+    const int L = p.seqlen;
+    const int nch = (L + K - 1) / K;
+
+    // selector S[r][k] = (k == g(r)), g = (lane of the quarter) / 8; k < 4 used
+    {
+        float* sa = reinterpret_cast<float*>(smem + CF::A_OP);
+        for (int e = threadIdx.x; e < 128 * 8; e += CF::THREADS) {
+            const int r = e >> 3, k = e & 7;
+            sa[(r >> 3) * 64 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3)] = (k == ((r & 31) >> 3)) ? 1.f : 0.f;
+        }
+    }
+    fence_async_smem();
+    if (threadIdx.x == 0) {
+        for (int i = 0; i < P; ++i) {
+            mbar_init(bar_full + 8u * i, 1);
+            mbar_init(bar_empty + 8u * i, CF::AW + 1);   // the aux warps and the MMA's completion
+        }
+        for (int i = 0; i < 2; ++i) {
+            mbar_init(bar_ready + 8u * i, CF::AW + 1);   // the aux warps and the MMA's completion
+            mbar_init(bar_done + 8u * i, CF::RW);
+        }
+        for (int i = 0; i < OB; ++i) {
+            mbar_init(bar_ofull + 8u * i, CF::AW);
+            mbar_init(bar_oempty + 8u * i, 1);
+        }
+        fence_mbar_init();
+    }
+    if (warp == CF::W_LOAD) {
+        tmem_alloc(smem_u32(taddr_slot), CF::TMEM_COLS);
+        tmem_relinquish();
+    }
+    tc_fence_before();
+    __syncthreads();
+    tc_fence_after();
+    const uint32_t tmem = *taddr_slot;
+
+    // chunks this CTA walks (the same sequence for every role)
+    int total = 0;
+    for (int task = blockIdx.x; task < p.M * p.S; task += p.workers) {
+        const int sgm = task / p.M;
+        total += min((sgm + 1) * p.cps, nch) - sgm * p.cps;
+    }
+
+    if (warp == CF::W_LOAD) {
+        // ------------------------------------------------------------ TMA loads
+        if (lane == 0) {
+            constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::OPB);
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
+            int issued = 0;
+            auto issue = [&]() {
+                if (!cur.valid(p, nch, CC)) return;
+                const int slot = issued % P;
+                const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
+                const uint32_t bar = bar_full + 8u * (uint32_t)slot;
+                const int t0 = cur.c * K;
+                mbar_expect_tx(bar, tx_bytes);
+                tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
+                tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
+                if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
+                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.xb * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
+                ++cur.c;
+                ++issued;
+            };
+            for (int i = 0; i < P && i < total; ++i) issue();
+            for (int j = 0; j + P < total; ++j) {
+                // slot j % P is free once the aux warps have read chunk j's
+                // tiles and its MMA (the reader of X) has completed
+                if (!mbar_wait(bar_empty + 8u * (uint32_t)(j % P), (uint32_t)((j / P) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                issue();
+            }
+            // the CTA's shared memory outlives every copy into it
+            for (int k = max(0, issued - P); k < issued; ++k)
+                if (!mbar_wait(bar_full + 8u * (uint32_t)(k % P), (uint32_t)((k / P) & 1))) break;
+        }
+    } else if (warp == CF::W_MMA) {
+        // ------------------------------------------------------------ one-hot MMA
+        if (lane == 0) {
+            const uint64_t adesc = smem_desc(smem_u32(smem + CF::A_OP), 128, 256);
+            constexpr uint32_t idesc = idesc_tf32(128, CF::TCOLS);
+            int mmas = 0;
+            for (int j = 0; j < total; ++j) {
+                const int slot = j % P, tb = j & 1;
+                if (!mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1))) {
+                    raise_error(1u);
+                    break;
+                }
+                if (j >= 2 && !mbar_wait(bar_done + 8u * tb, (uint32_t)(((j - 2) >> 1) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                tc_fence_after();
+                // X: one 8-row x 16-byte core matrix per step (SBO 128); the
+                // second k-half aliases the first (LBO 0) and meets zeros
+                const uint64_t bdesc = smem_desc(ring_s + (uint32_t)(slot * CF::SLOT + CF::SLOT_X), 0, 128);
+                mma_tf32(tmem + (uint32_t)(tb * CF::TCOLS), adesc, bdesc, idesc);
+                mma_commit(bar_ready + 8u * tb);
+                mma_commit(bar_empty + 8u * slot);
+                ++mmas;
+            }
+            // tensor memory is released only after the last MMAs completed
+            for (int k = max(0, mmas - 2); k < mmas; ++k)
+                if (!mbar_wait(bar_ready + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1))) break;
+        }
+    } else if (warp == CF::W_STORE) {
+        // ------------------------------------------------------------ output stores
+        if (lane == 0) {
+            ChunkCursor cur;
+            cur.start(p, nch, CC);
+            for (int j = 0; j < total && cur.valid(p, nch, CC); ++j, ++cur.c) {
+                const int o = j % OB;
+                if (!mbar_wait(bar_ofull + 8u * o, (uint32_t)((j / OB) & 1))) {
+                    raise_error(2u);
+                    break;
+                }
+                tma_store_3d(&tm_out, cur.d0, cur.c * K, cur.b, smem_u32(smem + CF::OUT + o * CF::OUTT));
+                bulk_commit();
+                // the store before this one has read its tile: hand it back
+                bulk_wait_read<1>();
+                if (j >= 1) mbar_arrive(bar_oempty + 8u * (uint32_t)((j - 1) % OB));
+            }
+            bulk_wait_all();
+        }
+    } else if (warp >= CF::W_AUX) {
+        // ------------------------------------------------------------ aux: per-(t, d) work
+        const int a = warp - CF::W_AUX;
+        const int oct = lane >> 3, ts = lane & 7;
+        const int trow = 8 * a + ts;               // step of the chunk this lane serves
+        float4* rec = reinterpret_cast<float4*>(smem + CF::REC);
+        const float4* pb = reinterpret_cast<const float4*>(smem + CF::YB);
+        ChunkCursor cur;
+        cur.start(p, nch, CC);
+        int ptask = -1;
+        float2 bias2[4], dsk2[4];
+        bool ok = true;
+
+        // Delta, Delta u into the recurrence rows of chunk j; keeps D u and
+        // silu(z) of this lane's eight items for the chunk's output
+        auto prologue = [&](int j, float2 (&du)[4], float2 (&sg)[4]) -> bool {
+            if (!cur.valid(p, nch, CC)) return false;
+            if (cur.task != ptask) {
+                ptask = cur.task;
+#pragma unroll
+                for (int k = 0; k < 4; ++k) {
+                    float v[2], dd[2];
+#pragma unroll
+                    for (int h = 0; h < 2; ++h) {
+                        const int d = cur.d0 + 8 * oct + 2 * k + h;
+                        v[h] = (p.delta_bias && d < p.dim) ? p.delta_bias[d] : 0.f;
+                        dd[h] = (p.D && d < p.dim) ? p.D[d] : 0.f;
+                    }
+                    bias2[k] = make_float2(v[0], v[1]);
+                    dsk2[k] = make_float2(dd[0], dd[1]);
+                }
+            }
+            const bool valid = cur.c * K + trow < L;
+            ++cur.c;
+            const int slot = j % P;
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1)))) {
+                if (lane == 0) raise_error(1u);
+                return false;
+            }
+            if (j >= 2 &&
+                !__all_sync(0xffffffffu, mbar_wait(bar_done + 8u * (j & 1), (uint32_t)(((j - 2) >> 1) & 1)))) {
+                if (lane == 0) raise_error(2u);
+                return false;
+            }
+            const unsigned char* sb = smem + slot * CF::SLOT;
+            const uint32_t off = swz64_group(trow, oct);
+            const uint4 uw = *reinterpret_cast<const uint4*>(sb + CF::SLOT_U + off);
+            const uint4 xw = *reinterpret_cast<const uint4*>(sb + CF::SLOT_D + off);
+            uint4 zw = make_uint4(0u, 0u, 0u, 0u);
+            if constexpr (kGate) zw = *reinterpret_cast<const uint4*>(sb + CF::SLOT_Z + off);
+            const uint32_t uv[4] = {uw.x, uw.y, uw.z, uw.w}, xv[4] = {xw.x, xw.y, xw.z, xw.w},
+                           zv[4] = {zw.x, zw.y, zw.z, zw.w};
+            float4* rrow = rec + (j & 1) * K * CC;
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                const float2 u2 = bf2_to_f2(uv[k]);
+                float2 dl = add2(bf2_to_f2(xv[k]), bias2[k]);
+                if constexpr (kSoftplus) dl = softplus_poly2(dl);
+                if (!valid) dl = splat2(0.f);
+                const float2 dlu = mul2(dl, u2);
+                rrow[ws_rec_slot(trow, 8 * oct + 2 * k)] = make_float4(dl.x, dl.x, dlu.x, dlu.x);
+                rrow[ws_rec_slot(trow, 8 * oct + 2 * k + 1)] = make_float4(dl.y, dl.y, dlu.y, dlu.y);
+                du[k] = mul2(dsk2[k], u2);
+                if constexpr (kGate) sg[k] = seg_silu2<true>(bf2_to_f2(zv[k]));
+                else sg[k] = splat2(1.f);
+            }
+            __syncwarp();
+            if (lane == 0) {
+                mbar_arrive(bar_ready + 8u * (j & 1));
+                mbar_arrive(bar_empty + 8u * slot);
+            }
+            return true;
+        };
+
+        // (readout + D u) * silu(z) of chunk j into its output tile
+        auto epilogue = [&](int j, const float2 (&du)[4], const float2 (&sg)[4]) -> bool {
+            if (!__all_sync(0xffffffffu, mbar_wait(bar_done + 8u * (j & 1), (uint32_t)((j >> 1) & 1)))) {
+                if (lane == 0) raise_error(2u);
+                return false;
+            }
+            const int o = j % OB;
+            if (j >= OB &&
+                !__all_sync(0xffffffffu, mbar_wait(bar_oempty + 8u * o, (uint32_t)(((j / OB) - 1) & 1)))) {
+                if (lane == 0) raise_error(2u);
+                return false;
+            }
+            const float4* pr = pb + (j & 1) * K * CC;
+            uint32_t ov[4];
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+                // the four lanes' partial sums of channels 2k, 2k+1 of the octet
+                const float4 a = pr[ws_rec_slot(trow, 8 * oct + 2 * k)];
+                const float4 b = pr[ws_rec_slot(trow, 8 * oct + 2 * k + 1)];
+                const float2 s = add2(add2(make_float2(a.x, b.x), make_float2(a.y, b.y)),
+                                      add2(make_float2(a.z, b.z), make_float2(a.w, b.w)));
+                ov[k] = f2_to_bf2(mul2(add2(s, du[k]), sg[k]));
+            }
+            *reinterpret_cast<uint4*>(smem + CF::OUT + o * CF::OUTT + swz64_group(trow, oct)) =
+                make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            fence_async_smem();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(bar_ofull + 8u * o);
+            return true;
+        };
+
+        float2 du_a[4], sg_a[4], du_b[4], sg_b[4];
+        int j = 0;
+        while (ok && j < total) {
+            ok = prologue(j, du_a, sg_a);
+            if (ok && j >= 1) ok = epilogue(j - 1, du_b, sg_b);
+            ++j;
+            if (!ok || j >= total) break;
+            ok = prologue(j, du_b, sg_b);
+            if (ok) ok = epilogue(j - 1, du_a, sg_a);
+            ++j;
+        }
+        if (ok && total > 0) {
+            if ((total - 1) & 1) epilogue(total - 1, du_b, sg_b);
+            else epilogue(total - 1, du_a, sg_a);
+        }
+    } else {
+        // ------------------------------------------------------------ recurrence
+        const int w = warp;
+        const int c = lane & 7, g = lane >> 3;       // channel of the warp, state group
+        const int col = CF::CW * w + c;              // channel of the CTA
+        const uint32_t tlane = tmem + ((uint32_t)(32 * w) << 16);
+        const float4* rec = reinterpret_cast<const float4*>(smem + CF::REC);
+        float* pb = reinterpret_cast<float*>(smem + CF::YB);
+
+        bool ok = true;
+        int j = 0;
+        for (int task = blockIdx.x; task < p.M * p.S && ok; task += p.workers) {
+            const int sgm = task / p.M, m = task - sgm * p.M;
+            const int b = m / p.units;
+            const int d = (m - b * p.units) * CC + col;
+            const bool ch_ok = d < p.dim;
+            const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
+            const int chain = m * CF::RW + w;
+
+            float2 A01 = make_float2(0.f, 0.f), A23 = make_float2(0.f, 0.f);
+            if (ch_ok) {
+                const float4 av = *reinterpret_cast<const float4*>(p.A + (size_t)d * N + 4 * g);
+                A01 = make_float2(av.x * kLog2e, av.y * kLog2e);
+                A23 = make_float2(av.z * kLog2e, av.w * kLog2e);
+            }
+            float2 h01 = make_float2(0.f, 0.f), h23 = make_float2(0.f, 0.f);
+            float* hst = p.seg_state + ((size_t)chain * CF::CW + c) * N + 4 * g;
+            if (sgm > 0) {
+                if (!__all_sync(0xffffffffu, tm_flag_wait(p.seg_flag + chain, sgm))) {
+                    ok = false;
+                    if (lane == 0) raise_error(4u);
+                    break;
+                }
+                const float4 v = __ldcg(reinterpret_cast<const float4*>(hst));
+                h01 = make_float2(v.x, v.y);
+                h23 = make_float2(v.z, v.w);
+            } else if (p.h0 && ch_ok) {
+                const float4 v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.dim + d) * N + 4 * g);
+                h01 = make_float2(v.x, v.y);
+                h23 = make_float2(v.z, v.w);
+            }
+
+            for (int cc = cb; cc < ce; ++cc, ++j) {
+                const int tb = j & 1;
+                if (!__all_sync(0xffffffffu, mbar_wait(bar_ready + 8u * tb, (uint32_t)((j >> 1) & 1)))) {
+                    ok = false;
+                    if (lane == 0) raise_error(2u);
+                    break;
+                }
+                tc_fence_after();
+                const float4* rr = rec + tb * K * CC;
+                float* pr = pb + tb * K * CC * 4;
+
+                // Steps of the chunk, software-pipelined: step t loads the
+                // inputs of step t + LA, evaluates exp(Delta A) and Delta B u of
+                // step t + EA and advances the state by step t.  B and C come
+                // from TMEM four steps (32 columns) per load, one load ahead.
+                constexpr int LA = 6, EA = 3, NG = K / 4;
+                const uint32_t tcol = tlane + (uint32_t)(tb * CF::TCOLS);
+                uint32_t gv[NG][32];
+                tmem_ld32(tcol, gv[0]);
+                tmem_wait(gv[0]);
+                tmem_ld32(tcol + 32, gv[1]);
+                float4 qv[K];
+                float2 dA[K][2], dB[K][2];
+                auto bc = [&](int t, int i) { return __uint_as_float(gv[t >> 2][(t & 3) * 8 + i]); };
+                auto load_step = [&](int t) { qv[t] = rr[ws_rec_slot(t, col)]; };
+                auto exp_step = [&](int t) {
+                    const float2 dl = make_float2(qv[t].x, qv[t].y), dlu = make_float2(qv[t].z, qv[t].w);
+                    const float2 e0 = mul2(dl, A01), e1 = mul2(dl, A23);
+                    dA[t][0] = make_float2(ex2_approx(e0.x), ex2_approx(e0.y));
+                    dA[t][1] = make_float2(ex2_approx(e1.x), ex2_approx(e1.y));
+                    dB[t][0] = mul2(dlu, make_float2(bc(t, 0), bc(t, 1)));
+                    dB[t][1] = mul2(dlu, make_float2(bc(t, 2), bc(t, 3)));
+                };
+#pragma unroll
+                for (int t = 0; t < LA; ++t) load_step(t);
+#pragma unroll
+                for (int t = 0; t < EA; ++t) exp_step(t);
+#pragma unroll
+                for (int t = 0; t < K; ++t) {
+                    if (t + EA < K && ((t + EA) & 3) == 0) {
+                        const int gr = (t + EA) >> 2;
+                        tmem_wait(gv[gr]);
+                        if (gr + 1 < NG) tmem_ld32(tcol + 32u * (uint32_t)(gr + 1), gv[gr + 1]);
+                    }
+                    if (t + LA < K) load_step(t + LA);
+                    if (t + EA < K) exp_step(t + EA);
+                    h01 = fma2(dA[t][0], h01, dB[t][0]);
+                    h23 = fma2(dA[t][1], h23, dB[t][1]);
+                    const float2 r = fma2(make_float2(bc(t, 6), bc(t, 7)), h23,
+                                          mul2(make_float2(bc(t, 4), bc(t, 5)), h01));
+                    // this lane's share of C_t . h_t, summed with the channel's
+                    // other three lanes by the aux warps
+                    pr[ws_rec_slot(t, col) * 4 + g] = r.x + r.y;
+                }
+                tc_fence_before();
+                __syncwarp();
+                if (lane == 0) mbar_arrive(bar_done + 8u * tb);
+            }
+            if (!ok) break;
+
+            // state leaving the segment
+            const float4 hv = make_float4(h01.x, h01.y, h23.x, h23.y);
+            if (sgm + 1 < p.S) {
+                __stcg(reinterpret_cast<float4*>(hst), hv);
+                __threadfence();
+                __syncwarp();
+                if (lane == 0) tm_st_release(p.seg_flag + chain, sgm + 1);
+            } else if (p.last_state && ch_ok) {
+                *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) = hv;
+            }
+        }
+    }
+
+    // every warp ends here: the tensor memory is released exactly once
+    tc_fence_before();
+    __syncthreads();
+    if (warp == CF::W_LOAD) {
+        __syncwarp();
+        tc_fence_after();
+        tmem_dealloc(tmem, CF::TMEM_COLS);
+    }
+}
+
 // X operands of every chunk: [batch][t][j][k] f32 with X[k, 8t + j] =
 // B_t[4k + j] (j < 4), C_t[4k + j - 4] (j >= 4), zero for k >= N / 4 and for
 // t >= L; also zeroes the segment flags.
@@ -1263,6 +1751,50 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
                                        dim3(CF::THREADS), args, CF::SMEM, s);
 }
 
+cudaError_t launch_ws(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
+    using CF = WsCfg;
+    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TmParams);
+    static const Kern kerns[4] = {scan_ws_kernel<false, false>, scan_ws_kernel<false, true>,
+                                  scan_ws_kernel<true, false>, scan_ws_kernel<true, true>};
+    const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
+    static int occ[4] = {0, 0, 0, 0};
+    if (occ[which] == 0) {
+        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        int o = 0;
+        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
+        if (e != cudaSuccess) return e;
+        if (o != 1) return cudaErrorInvalidConfiguration;
+        occ[which] = o;
+    }
+    const TmPlan pl = tm_plan<16>(a.batch, a.dim, a.seqlen, sms);
+    const int64_t lpad = relay_lpad(a.seqlen);
+    unsigned char* w = static_cast<unsigned char*>(ws);
+    float* xop = reinterpret_cast<float*>(w);
+    const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
+    const int64_t chains = (int64_t)pl.M * CF::RW;
+    float* st = reinterpret_cast<float*>(w + x_bytes);
+    const int64_t st_bytes = (chains * CF::CW * CF::N * 4 + 255) / 256 * 256;
+    int* flags = reinterpret_cast<int*>(w + x_bytes + st_bytes);
+    {
+        dim3 grid((unsigned)(lpad / 64), (unsigned)(a.batch * a.ngroups));
+        tm_stage_kernel<16><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.B),
+                                                 static_cast<const __nv_bfloat16*>(a.C), xop, (int)a.seqlen, lpad,
+                                                 flags, (int)chains);
+    }
+    CUtensorMap mu, md, mz, mo;
+    if (!tm_make_map(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B) ||
+        !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, CU_TENSOR_MAP_SWIZZLE_64B))
+        return cudaErrorInvalidValue;
+    TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
+                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0, (int)a.ngroups, (int)a.gch};
+    void* args[] = {&mu, &md, &mz, &mo, &tp};
+    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
+                                       dim3(CF::THREADS), args, CF::SMEM, s);
+}
+
 }  // namespace
 
 bool tmem_supported(const ScanArgs& a, DType dt) {
@@ -1287,6 +1819,7 @@ int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dst
 
 cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant) {
     if (dt != DType::BF16 || a.dstate != 16) return cudaErrorInvalidValue;
+    if (variant == 3) return launch_ws(a, workspace, sms, s);
     if (variant == 2) return launch_tmem2(a, workspace, sms, s);
     return launch_tmem_t<16>(a, workspace, sms, s);
 }

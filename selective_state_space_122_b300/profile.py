@@ -161,7 +161,7 @@ def main(argv=None):
     s.add_argument("--L", type=int, default=16384)
     s.add_argument("--N", type=int, default=16)
     s.add_argument("--iters", type=int, default=3)
-    s.add_argument("--path", default=None, choices=[None, "tmem2", "tmem", "relay", "seg", "generic"])
+    s.add_argument("--path", default=None, choices=[None, "ws", "tmem2", "tmem", "relay", "seg", "generic"])
     s.add_argument("--ngroups", type=int, default=1)
     d = sub.add_parser("decode")
     d.add_argument("--batch", type=int, default=256)

@@ -100,7 +100,7 @@ def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
     relay paths (when they accept the shape) and each generic layout."""
     fast = ["seg", "relay"] if relay_ok(dim, dtype) else []
     if tmem_ok(N, dim, dtype):
-        fast = ["tmem", "tmem2"] + fast
+        fast = ["ws", "tmem", "tmem2"] + fast
     return fast + list(range(LAYOUTS[N]))
 
 
@@ -113,7 +113,7 @@ def scan_layout(layout):
     old = {k: os.environ.get(k) for k in keys}
     for k in keys:
         os.environ.pop(k, None)
-    if layout in ("relay", "seg", "tmem", "tmem2"):
+    if layout in ("relay", "seg", "tmem", "tmem2", "ws"):
         os.environ["SSM_SCAN_PATH"] = layout
     elif layout is not None:
         os.environ["SSM_SCAN_PATH"] = "generic"

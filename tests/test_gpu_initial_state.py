@@ -96,7 +96,7 @@ def test_resume_in_place(g):
     check_state(host_f64(state), ref_last, inputs.BF16, "in-place state")
 
 
-@pytest.mark.parametrize("path", ["tmem2", "tmem", "seg"])
+@pytest.mark.parametrize("path", ["ws", "tmem2", "tmem", "seg"])
 def test_initial_state_multisegment(path):
     """Many segments per chain: only each chain's first segment reads the
     initial state; the rest continue from the state handed through the workspace."""
