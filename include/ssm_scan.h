@@ -421,6 +421,50 @@ SSM_API const char* ssm_last_launch_error(void);
 /* Library version as MAJOR*10000 + MINOR*100 + PATCH. */
 SSM_API int ssm_version(void);
 
+/* Scan kernels that ssm_force_scan_path can select. */
+typedef enum ssm_scan_path {
+    SSM_PATH_AUTO = 0,     /* the library's own choice (the default)                  */
+    SSM_PATH_TMEM2 = 1,    /* tensor-memory kernel, two states per lane (bf16, N 16)  */
+    SSM_PATH_WS = 2,       /* warp-specialised tensor-memory kernel, four states per
+                              lane (bf16, N 16)                                        */
+    SSM_PATH_SEG = 3,      /* segmented TMA kernel                                     */
+    SSM_PATH_GENERIC = 4   /* generic kernel (no workspace, any alignment)            */
+} ssm_scan_path;
+
+/*
+ * ssm_force_scan_path -- diagnostics for tests and benchmarks that compare
+ * the scan kernels (no counterpart on the pages): every ssm_scan_fwd* call
+ * that follows, in this process and on every device, runs the given kernel
+ * instead of the library's own choice.  generic_layout selects one compiled
+ * layout of the generic kernel (-1 = its planner's choice; ignored for the
+ * other paths).  A forced kernel that cannot take a call's shape, alignment
+ * or workspace makes that call return SSM_ERR_UNSUPPORTED before anything is
+ * enqueued.  The setting is an atomic process-wide value read once per call;
+ * SSM_PATH_AUTO restores the default.  Returns SSM_ERR_SHAPE for an unknown
+ * path.  Production callers never need it.
+ */
+SSM_API ssm_status ssm_force_scan_path(int path, int generic_layout);
+
+/*
+ * ssm_debug_wait_test -- test hook for the kernels' bounded waits (no
+ * counterpart on the pages).  Every wait in the library's kernels gives up
+ * after a limit (1 s), sets a bit in the device error word, lets its CTA
+ * drain its copies and free its tensor memory, and returns; this hook makes
+ * that path run on purpose, without any fault:
+ *   withhold_flag != 0: in the scans that follow, the first sequence segment
+ *     of channel group 0 keeps its state hand-off flag unset, so the segment
+ *     after it (when the call is cut into segments: more 32-channel groups
+ *     than SMs, or 128/N-channel groups than warps for the segmented kernel)
+ *     waits until the limit and gives up (bit 4), and the warps that wait on
+ *     it give up in turn.  Those calls' outputs are undefined.
+ *   wait_limit_ns: the limit of every wait from now on (<= 0: the default).
+ * ssm_debug_wait_test(0, 0) restores the defaults.  Writes two words of
+ * device memory on the current device (a synchronous copy); call it only
+ * while no scan runs.  Returns SSM_ERR_DEVICE if the copy fails.  Production
+ * callers never need it.
+ */
+SSM_API ssm_status ssm_debug_wait_test(int withhold_flag, int64_t wait_limit_ns);
+
 #ifdef __cplusplus
 }
 #endif

@@ -16,8 +16,9 @@ Public calls (thin wrappers over the C ABI in include/ssm_scan.h):
 The CUDA library ``libssmscan.so`` is loaded on first use; there is no CPU
 fallback.
 """
-from ._lib import (SSMError, conv1d_fwd, conv1d_update, device_error, load_library,  # noqa: F401
-                   scan_workspace_bytes, ssm_scan_bwd, ssm_scan_fwd, ssm_state_update, status_string)
+from ._lib import (SSMError, conv1d_fwd, conv1d_update, device_error, force_scan_path,  # noqa: F401
+                   load_library, scan_workspace_bytes, ssm_scan_bwd, ssm_scan_fwd, ssm_state_update,
+                   status_string)
 
 __all__ = ["ssm_scan_fwd", "ssm_state_update", "ssm_scan_bwd", "conv1d_fwd", "conv1d_update", "scan_workspace_bytes",
-           "device_error", "load_library", "status_string", "SSMError"]
+           "device_error", "force_scan_path", "load_library", "status_string", "SSMError"]

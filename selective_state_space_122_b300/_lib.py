@@ -26,7 +26,7 @@ EXPORTS = ("ssm_scan_fwd", "ssm_scan_workspace_bytes", "ssm_device_error", "ssm_
            "ssm_scan_noalloc_max_workspace_bytes", "ssm_scan_fwd_from_state", "ssm_conv1d_fwd",
            "ssm_conv1d_update", "ssm_scan_bwd", "ssm_scan_bwd_workspace_bytes", "ssm_scan_fwd_grouped",
            "ssm_scan_workspace_bytes_grouped", "ssm_state_update_grouped", "ssm_scan_bwd_grouped",
-           "ssm_scan_bwd_from_state")
+           "ssm_scan_bwd_from_state", "ssm_force_scan_path", "ssm_debug_wait_test")
 
 _lib: Optional[ctypes.CDLL] = None
 
@@ -94,9 +94,22 @@ def load_library(path: str = LIB_PATH) -> ctypes.CDLL:
     lib.ssm_last_launch_error.restype = ctypes.c_char_p
     lib.ssm_version.argtypes = []
     lib.ssm_version.restype = ci
+    lib.ssm_force_scan_path.argtypes = [ci, ci]
+    lib.ssm_force_scan_path.restype = ci
+    lib.ssm_debug_wait_test.argtypes = [ci, i64]
+    lib.ssm_debug_wait_test.restype = ci
     if path == LIB_PATH:
         _lib = lib
     return lib
+
+
+SCAN_PATHS = {None: 0, "tmem2": 1, "ws": 2, "seg": 3, "generic": 4}
+
+
+def force_scan_path(path: Optional[str] = None, generic_layout: int = -1) -> None:
+    """Diagnostics: make every later scan call run one kernel (ssm_force_scan_path).
+    path: None (the library's own choice), "tmem2", "ws", "seg" or "generic"."""
+    _check("ssm_force_scan_path", load_library().ssm_force_scan_path(SCAN_PATHS[path], int(generic_layout)))
 
 
 def status_string(code: int) -> str:

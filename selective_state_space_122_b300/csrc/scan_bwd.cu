@@ -35,6 +35,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "device_memo.h"
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -387,16 +388,21 @@ scan_bwd_kernel(const BwdArgs p, float* __restrict__ ckpt) {
 template <typename T, int N>
 cudaError_t launch_bwd_t(const BwdArgs& a, float* ckpt, int sms, cudaStream_t s) {
     using CF = BwdCfg<N>;
-    static bool attr = false;
-    if (!attr) {
-        cudaError_t e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, false>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e == cudaSuccess)
-            e = cudaFuncSetAttribute(scan_bwd_kernel<T, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                     CF::SMEM);
-        if (e != cudaSuccess) return e;
-        attr = true;
-    }
+    // shared-memory size of both instantiations, set once per device
+    static DeviceMemo memo;
+    int dev = 0, set = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    cudaError_t err = cudaSuccess;
+    if (!memo.get(dev, [&](int& r) {
+            err = cudaFuncSetAttribute(scan_bwd_kernel<T, N, false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       CF::SMEM);
+            if (err == cudaSuccess)
+                err = cudaFuncSetAttribute(scan_bwd_kernel<T, N, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                           CF::SMEM);
+            r = 1;
+            return err == cudaSuccess;
+        }, &set))
+        return err;
     const int64_t gx = a.ngroups * ((a.gch + CF::CC - 1) / CF::CC);
     if (gx > 0x7fffffff) return cudaErrorInvalidValue;
     dim3 grid((unsigned)gx, (unsigned)a.batch);

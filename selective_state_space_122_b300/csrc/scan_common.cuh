@@ -18,7 +18,20 @@ namespace {
 
 static __device__ unsigned int g_device_error = 0;
 
-constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;  // 1 s
+// Limit of every bounded wait, in nanoseconds: 1 s unless the wait test hook
+// (ssm_debug_wait_test) shortened it.
+constexpr unsigned long long kWaitLimitNs = 1000ull * 1000ull * 1000ull;
+static __device__ unsigned long long g_wait_limit_ns = kWaitLimitNs;
+// Nonzero only under the wait test hook: the first segment of chain 0 keeps
+// its hand-off flag unset, so the segment after it waits until the limit.
+static __device__ int g_withhold_flag = 0;
+
+__device__ __forceinline__ unsigned long long wait_limit_ns() {
+    return *reinterpret_cast<volatile unsigned long long*>(&g_wait_limit_ns);
+}
+__device__ __forceinline__ bool withhold_handoff(int chain, int sgm) {
+    return chain == 0 && sgm == 0 && *reinterpret_cast<volatile int*>(&g_withhold_flag) != 0;
+}
 
 // ------------------------------------------------------------- PTX wrappers
 
@@ -74,7 +87,7 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
     while (!(SSM_RELAY_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)))
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > wait_limit_ns()) return false;
     return true;
 }
 

@@ -41,6 +41,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "device_memo.h"
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -567,14 +568,18 @@ cudaError_t launch_cfg(const ScanArgs& a, cudaStream_t s) {
     constexpr bool kFast = !std::is_same<T, float>::value;
     auto kern = a.ngroups == 1 ? scan_fwd_kernel<CF, T, kFast, false> : scan_fwd_kernel<CF, T, kFast, true>;
     if (CF::SMEM_BYTES > 48 * 1024) {
-        static bool attr_set[2] = {false, false};  // once per kernel instantiation
+        // once per kernel instantiation and device
+        static DeviceMemo memo[2];
         const int gi = a.ngroups == 1 ? 0 : 1;
-        if (!attr_set[gi]) {
-            const cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                                       (int)CF::SMEM_BYTES);
-            if (e != cudaSuccess) return e;
-            attr_set[gi] = true;
-        }
+        int dev = 0, set = 0;
+        if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+        cudaError_t err = cudaSuccess;
+        if (!memo[gi].get(dev, [&](int& r) {
+                err = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)CF::SMEM_BYTES);
+                r = 1;
+                return err == cudaSuccess;
+            }, &set))
+            return err;
     }
     const size_t es = sizeof(T);
     Geo geo;

@@ -1,5 +1,6 @@
-// scan_relay.cu -- the selective scan's fast path on sm_103a: TMA-staged
-// chunks, float32 state in registers, and a warp relay along the sequence.
+// scan_relay.cu -- the segmented selective scan (float32 activations, or
+// d_state 4 / 8), the B/C staging kernel it shares with the tensor-memory
+// kernels' hosts, and the TMA capability checks of the fast paths.
 //
 // Computes, per (batch b, channel d), the recurrence of the Mamba selective
 // SSM ("Mamba: Selective State Space Models" README, "State Space Model",
@@ -8,42 +9,19 @@
 //     h_t     = exp(Delta_t A) * h_{t-1} + Delta_t B_t u_t
 //     out_t   = (C_t . h_t + D u_t) * silu(z_t)
 //
-// Work decomposition
-// ------------------
-// A CTA owns one "unit": CW = 32 / R consecutive channels of one batch row,
-// where R = N / 4 lanes share a channel and each lane keeps 4 of its N states
-// in registers (lane = channel * R + g, states 4g .. 4g+3).  The sequence is
-// cut into chunks of K steps; chunk c belongs to warp c % W of the CTA.  A
-// warp handles its chunk in three phases:
-//   1. precompute, independent of the state: the per-(t, d) terms (softplus,
-//      Delta u, D u, silu(z)), then for every step and state exp(Delta A)
-//      and Delta B u, kept in registers;
-//   2. the relay: wait for the state entering the chunk (written by the warp
-//      of chunk c - 1), run h = dA h + dBu over the K steps (one packed FMA
-//      per two states per step: the only serial work), and hand the state
-//      leaving the chunk to the warp of chunk c + 1;
-//   3. readout: y_t = C_t . h_t from the kept h_t, a transposed butterfly
-//      over the R lanes of each channel, the D skip and silu gate, and a TMA
-//      store of the chunk's output tile.
-// Every exponential is evaluated once, by whichever warp owns the chunk, in
-// parallel with the other warps; only phase 2 is sequential along the
-// sequence, which is the "Efficient Scan" sequential recurrence with its
-// expensive part hoisted off the critical path.
+// A lane keeps 4 of a channel's N states in registers (R = N / 4 lanes per
+// channel).  Pairs of warps on one scheduler scan CW = 32 / R channels of one
+// batch row straight through K-step chunks: a helper warp issues the TMA
+// loads of the u, delta_raw and z tiles and computes the per-(t, d) terms into
+// a double buffer, the main warp runs the recurrence with B and C from the
+// staged rows in shared memory, the readout over the R lanes of each channel
+// and the output store.  Every (batch, channel group) chain is cut into S
+// segments taken by different warps in turn; the state passes between
+// segments through the workspace under a bounded release/acquire flag wait.
 //
-// Data movement
-// -------------
-// u, delta_raw and z tiles (K steps x CW channels) arrive by TMA
-// (cp.async.bulk.tensor.3d over the (dim, seqlen, batch) tensor, so ragged
-// sequence ends are zero-filled per batch row and ragged channel ends are
-// clipped); B and C arrive as one bulk copy per chunk from a float32
-// [batch][t][B_0..B_{N-1} C_0..C_{N-1}] staging buffer written by
-// bc_stage_kernel (the B and C of a step are shared by every channel, so
-// they are converted and transposed once instead of once per CTA).  Each warp
-// keeps P chunks in flight in its own ring.  Output tiles leave by TMA store.
-//
-// Waits are bounded: an mbarrier wait that exceeds ~1 s sets a bit in the
-// device error word (ssm_device_error) and the warp stops early; nothing in
-// the kernel can spin forever.
+// Waits are bounded: a wait that exceeds ~1 s sets a bit in the device error
+// word (ssm_device_error) and the warp stops early; nothing in the kernel can
+// spin forever.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 
@@ -52,6 +30,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "device_memo.h"
 #include "scan_common.cuh"
 #include "ssm_internal.cuh"
 
@@ -59,304 +38,6 @@ namespace ssm {
 
 namespace {
 
-
-// ------------------------------------------------------------- configuration
-
-template <typename T, int N_>
-struct RelayCfg {
-    static constexpr int N = N_;
-    static constexpr int G = 4;                 // states per lane
-    static constexpr int R = N / G;             // lanes per channel
-    static constexpr int CW = 32 / R;           // channels per unit (CTA)
-    static constexpr int W = 4;                 // relay warps per CTA
-    static constexpr int K = 8;                 // steps per warp-chunk
-    static constexpr int P = 3;                 // chunks in flight per warp
-    static constexpr int THREADS = 32 * W;
-    // CTAs per SM the register budget is sized for: five for d_state 16, whose
-    // units are the smallest (8 channels) and most numerous; four otherwise.
-    static constexpr int MIN_CTAS = N == 16 ? 5 : 4;
-    static constexpr int KR = K / R;            // prologue items / finished sums per lane
-    static_assert(KR >= 2 && KR % 2 == 0, "items per lane come in pairs of steps");
-    static constexpr int ES = (int)sizeof(T);
-    static constexpr int TILE = K * CW * ES;    // one u / delta / z / out tile
-    static constexpr int BC_ROW = 2 * N * 4;    // one staged step of B and C (f32)
-    static constexpr int BC = K * BC_ROW;       // one chunk of B and C
-    static constexpr int align128(int x) { return (x + 127) / 128 * 128; }
-    // per-warp ring slot: u | delta | z | BC
-    static constexpr int SLOT_U = 0;
-    static constexpr int SLOT_D = align128(TILE);
-    static constexpr int SLOT_Z = SLOT_D + align128(TILE);
-    static constexpr int SLOT_BC = SLOT_Z + align128(TILE);
-    static constexpr int SLOT = align128(SLOT_BC + BC);
-    // CTA layout
-    static constexpr int OFF_RING = 0;                                   // [W][P] slots
-    static constexpr int OFF_DP = OFF_RING + W * P * SLOT;               // [W][K][CW] float4
-    static constexpr int DP = K * CW * 16;
-    static constexpr int OFF_OUT = OFF_DP + W * DP;                      // [W][3] out tiles
-    static constexpr int OUT = align128(TILE);
-    static constexpr int OFF_RED = OFF_OUT + W * 3 * OUT;                // [W][32][K/2+1] float4
-    static constexpr int RED = R > 1 ? 32 * (K / 2 + 1) * 16 : 0;
-    static constexpr int OFF_CARRY = OFF_RED + W * RED;                  // [W][CW][N] float
-    static constexpr int CARRY = CW * N * 4;
-    static constexpr int OFF_BAR = OFF_CARRY + W * CARRY;                // full[W][P], carry[W]
-    static constexpr int SMEM = OFF_BAR + (W * P + W) * 8;
-    static_assert(SMEM <= 227 * 1024, "a CTA's shared memory must fit an SM");
-};
-
-struct RelayParams {
-    const float* A;
-    const float* D;
-    const float* delta_bias;
-    const float* bc;        // staged B|C, [batch * ngroups][lpad][2N] f32
-    float* last_state;
-    int dim, seqlen;
-    int64_t lpad;
-    int softplus;
-    int has_z;
-    const float* h0;        // initial state or null
-    int ngroups, gch;       // B/C groups, channels per group (a multiple of CW)
-};
-
-
-template <typename T, int N, bool kFast, bool kSoftplus, bool kGate>
-__global__ void __launch_bounds__(RelayCfg<T, N>::THREADS, RelayCfg<T, N>::MIN_CTAS)
-scan_relay_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
-                  const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
-                  const RelayParams p) {
-    using CF = RelayCfg<T, N>;
-    constexpr int K = CF::K, W = CF::W, P = CF::P, R = CF::R, CW = CF::CW, KR = CF::KR;
-    constexpr int RS = K / 2 + 1;            // float4 stride of a lane's row in the reduction buffer
-    extern __shared__ __align__(128) unsigned char smem[];
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const int ch = lane / R, g = lane % R;
-    const int b = blockIdx.y;
-    const int d0 = blockIdx.x * CW;
-    const int d = d0 + ch;
-    const bool ch_ok = d < p.dim;
-    const int L = p.seqlen;
-    const int nch = (L + K - 1) / K;
-
-    unsigned char* ring = smem + CF::OFF_RING + warp * P * CF::SLOT;
-    float4* dp = reinterpret_cast<float4*>(smem + CF::OFF_DP + warp * CF::DP);
-    float4* red = reinterpret_cast<float4*>(smem + CF::OFF_RED + warp * CF::RED);
-    const uint32_t bar0 = smem_u32(smem + CF::OFF_BAR);
-    const uint32_t bar_full = bar0 + 8u * (uint32_t)(warp * P);
-    const uint32_t bar_cin = bar0 + 8u * (uint32_t)(W * P + warp);                 // carry into my chunks
-    const uint32_t bar_cout = bar0 + 8u * (uint32_t)(W * P + (warp + 1) % W);      // carry into the next warp's
-    float* carry0 = reinterpret_cast<float*>(smem + CF::OFF_CARRY);
-    const float* cin = carry0 + warp * CF::CW * N + ch * N + 4 * g;
-    float* cout = carry0 + ((warp + 1) % W) * CF::CW * N + ch * N + 4 * g;
-
-    // ---- barriers, and the zero state entering chunk 0 (carry slot 0)
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < W * P; ++i) mbar_init(bar0 + 8u * i, 1);
-        for (int i = 0; i < W; ++i) mbar_init(bar0 + 8u * (W * P + i), 1);
-        fence_mbar_init();
-    }
-    // the state entering chunk 0: the caller's initial state, else zero
-    for (int i = threadIdx.x; i < CW * N; i += CF::THREADS) {
-        const int dc = d0 + i / N;
-        carry0[i] = (p.h0 && dc < p.dim) ? p.h0[((size_t)b * p.dim + dc) * N + i % N] : 0.f;
-    }
-    __syncthreads();
-    if (threadIdx.x == 0) mbar_arrive(bar_cin);   // chunk 0's state (zeros) is ready
-
-    // ---- per-lane constants
-    float2 A2[2];
-    {
-        const float4 a = ch_ok ? *reinterpret_cast<const float4*>(p.A + (size_t)d * N + 4 * g)
-                               : make_float4(0.f, 0.f, 0.f, 0.f);
-        A2[0] = make_float2(a.x * kLog2e, a.y * kLog2e);
-        A2[1] = make_float2(a.z * kLog2e, a.w * kLog2e);
-    }
-    const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
-    const float2 dskip2 = splat2((p.D && ch_ok) ? p.D[d] : 0.f);
-    const float* bc_b = p.bc + ((size_t)b * p.ngroups + (size_t)(d0 / p.gch)) * p.lpad * (2 * N);
-    constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::BC);
-    const uint32_t ring_s = smem_u32(ring);
-
-    auto issue = [&](int c, int slot) {  // loads of chunk c into ring slot `slot` (lane 0 only)
-        const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
-        const uint32_t bar = bar_full + 8u * (uint32_t)slot;
-        mbar_expect_tx(bar, tx_bytes);
-        const int t0 = c * K;
-        tma_load_3d(base + CF::SLOT_U, &tm_u, d0, t0, b, bar);
-        tma_load_3d(base + CF::SLOT_D, &tm_d, d0, t0, b, bar);
-        if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, d0, t0, b, bar);
-        bulk_load(base + CF::SLOT_BC, bc_b + (size_t)t0 * (2 * N), CF::BC, bar);
-    };
-    if (lane == 0) {
-#pragma unroll
-        for (int j = 0; j < P; ++j)
-            if (warp + j * W < nch) issue(warp + j * W, j);
-    }
-
-    int slot = 0;
-    uint32_t fpar = 0;        // parity of the ring slot's current phase
-    uint32_t cpar = 0;        // parity of the carry barrier's current phase
-    int oslot = 0;            // output tile of the current chunk
-    int consumed = 0;         // chunks whose loads this warp has waited for
-    int issued = 0;           // chunks whose loads this warp has issued
-#pragma unroll
-    for (int j = 0; j < P; ++j) issued += (warp + j * W < nch) ? 1 : 0;
-    bool ok = true;
-    for (int c = warp; c < nch; c += W) {
-        const unsigned char* sb = ring + slot * CF::SLOT;
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * (uint32_t)slot, fpar))) {
-            ok = false;
-            if (lane == 0) raise_error(1u);
-            break;
-        }
-        ++consumed;
-        const int t0 = c * K;
-
-        // ---- phase 1a: per-(t, d) terms of this lane's KR steps
-        const T* su = reinterpret_cast<const T*>(sb + CF::SLOT_U);
-        const T* sd = reinterpret_cast<const T*>(sb + CF::SLOT_D);
-        const T* sz = reinterpret_cast<const T*>(sb + CF::SLOT_Z);
-        float2 skip[KR / 2], gate[KR / 2];
-        const bool tail = t0 + K > L;
-#pragma unroll
-        for (int i = 0; i < KR; i += 2) {
-            const int ta = g * KR + i, tb = ta + 1;
-            const float2 uv = make_float2(ld_elem(su + ta * CW + ch), ld_elem(su + tb * CW + ch));
-            const float2 xr = make_float2(ld_elem(sd + ta * CW + ch), ld_elem(sd + tb * CW + ch));
-            float2 dl = add2(xr, bias2);
-            if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
-            if (tail)   // steps past the end: Delta = 0 leaves the state unchanged
-                dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + tb < L ? 1.f : 0.f));
-            const float2 du = mul2(dl, uv);
-            skip[i / 2] = mul2(dskip2, uv);
-            if constexpr (kGate) {
-                const float2 zv = make_float2(ld_elem(sz + ta * CW + ch), ld_elem(sz + tb * CW + ch));
-                gate[i / 2] = silu_f2<kFast>(zv);
-            } else {
-                gate[i / 2] = splat2(1.f);
-            }
-            dp[ta * CW + ch] = make_float4(dl.x, dl.x, du.x, du.x);
-            dp[tb * CW + ch] = make_float4(dl.y, dl.y, du.y, du.y);
-        }
-        __syncwarp();
-
-        // ---- phase 1b: exp(Delta A) and Delta B u for every step and state
-        const float* sbc = reinterpret_cast<const float*>(sb + CF::SLOT_BC);
-        float2 dA[K][2], hb[K][2];
-#pragma unroll
-        for (int t = 0; t < K; ++t) {
-            const float4 q = dp[t * CW + ch];
-            const float4 bq = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + 4 * g);
-            const float2 e0 = mul2(make_float2(q.x, q.y), A2[0]);
-            const float2 e1 = mul2(make_float2(q.x, q.y), A2[1]);
-            dA[t][0] = make_float2(decay_exp2<kFast>(e0.x), decay_exp2<kFast>(e0.y));
-            dA[t][1] = make_float2(decay_exp2<kFast>(e1.x), decay_exp2<kFast>(e1.y));
-            hb[t][0] = mul2(make_float2(q.z, q.w), make_float2(bq.x, bq.y));
-            hb[t][1] = mul2(make_float2(q.z, q.w), make_float2(bq.z, bq.w));
-        }
-
-        // ---- phase 2: the relay (the only sequential work)
-        if (!__all_sync(0xffffffffu, mbar_wait(bar_cin, cpar))) {
-            ok = false;
-            if (lane == 0) raise_error(2u);
-            break;
-        }
-        cpar ^= 1u;
-        float2 h0, h1;
-        {
-            const float4 cr = *reinterpret_cast<const float4*>(cin);
-            h0 = make_float2(cr.x, cr.y);
-            h1 = make_float2(cr.z, cr.w);
-        }
-#pragma unroll
-        for (int t = 0; t < K; ++t) {
-            h0 = fma2(dA[t][0], h0, hb[t][0]);
-            h1 = fma2(dA[t][1], h1, hb[t][1]);
-            hb[t][0] = h0;
-            hb[t][1] = h1;
-        }
-        // hand the state to the next chunk's warp (after the last chunk nobody waits)
-        *reinterpret_cast<float4*>(cout) = make_float4(h0.x, h0.y, h1.x, h1.y);
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bar_cout);
-        if (c == nch - 1 && p.last_state && ch_ok)
-            *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) =
-                make_float4(h0.x, h0.y, h1.x, h1.y);
-
-        // ---- phase 3: readout C_t . h_t as (even-state, odd-state) partial pairs
-        float2 yv[KR / 2 * 2];   // finished y of this lane's KR steps, in pairs
-        if constexpr (R == 1) {
-#pragma unroll
-            for (int t = 0; t < K; t += 2) {
-                const float4 c0 = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + N + 4 * g);
-                const float4 c1 = *reinterpret_cast<const float4*>(sbc + (t + 1) * (2 * N) + N + 4 * g);
-                const float2 a0 = fma2(make_float2(c0.z, c0.w), hb[t][1], mul2(make_float2(c0.x, c0.y), hb[t][0]));
-                const float2 a1 =
-                    fma2(make_float2(c1.z, c1.w), hb[t + 1][1], mul2(make_float2(c1.x, c1.y), hb[t + 1][0]));
-                yv[t / 2] = make_float2(a0.x + a0.y, a1.x + a1.y);
-            }
-        } else {
-            // every lane publishes its partial pairs, then sums the R partials of its KR steps
-            float4* mine = red + lane * RS;
-#pragma unroll
-            for (int t = 0; t < K; t += 2) {
-                const float4 c0 = *reinterpret_cast<const float4*>(sbc + t * (2 * N) + N + 4 * g);
-                const float4 c1 = *reinterpret_cast<const float4*>(sbc + (t + 1) * (2 * N) + N + 4 * g);
-                const float2 a0 = fma2(make_float2(c0.z, c0.w), hb[t][1], mul2(make_float2(c0.x, c0.y), hb[t][0]));
-                const float2 a1 =
-                    fma2(make_float2(c1.z, c1.w), hb[t + 1][1], mul2(make_float2(c1.x, c1.y), hb[t + 1][0]));
-                mine[t / 2] = make_float4(a0.x, a0.y, a1.x, a1.y);
-            }
-            __syncwarp();
-#pragma unroll
-            for (int q = 0; q < KR / 2; ++q) {
-                const int tp = g * (KR / 2) + q;
-                float2 s0 = make_float2(0.f, 0.f), s1 = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int gg = 0; gg < R; ++gg) {
-                    const float4 v = red[(ch * R + gg) * RS + tp];
-                    s0 = add2(s0, make_float2(v.x, v.y));
-                    s1 = add2(s1, make_float2(v.z, v.w));
-                }
-                yv[q] = make_float2(s0.x + s0.y, s1.x + s1.y);
-            }
-        }
-
-        // ---- gate, output tile (triple-buffered; lane 0 owns the TMA store groups,
-        // and after committing chunk k's store it waits until chunk k-1's has
-        // read its tile, so the tile written next is always free)
-        T* so = reinterpret_cast<T*>(smem + CF::OFF_OUT + (warp * 3 + oslot) * CF::OUT);
-#pragma unroll
-        for (int i = 0; i < KR; i += 2) {
-            const int ta = g * KR + i;
-            const float2 y = mul2(add2(yv[i / 2], skip[i / 2]), gate[i / 2]);
-            st_pair<T>(so + ta * CW + ch, so + (ta + 1) * CW + ch, y);
-        }
-        fence_async_smem();
-        __syncwarp();
-        const bool refill = c + P * W < nch;
-        if (lane == 0) {
-            tma_store_3d(&tm_out, d0, t0, b, smem_u32(so));
-            bulk_commit();
-            if (refill) issue(c + P * W, slot);   // refill this slot
-            bulk_wait_read<1>();
-        }
-        issued += refill ? 1 : 0;
-        oslot = oslot == 2 ? 0 : oslot + 1;
-        if (++slot == P) {
-            slot = 0;
-            fpar ^= 1u;
-        }
-    }
-
-
-    // Drain: every issued load must land before the CTA's shared memory is
-    // released, and every store must have read its tile.
-    if (!ok) {
-        for (int j = consumed; j < issued; ++j)
-            if (!mbar_wait(bar_full + 8u * (uint32_t)(j % P), (uint32_t)((j / P) & 1))) break;
-    }
-    if (lane == 0) bulk_wait_all();
-}
 
 // ===================================================================
 // Segmented direct scan: one warp scans CW channels straight through
@@ -453,7 +134,7 @@ __device__ __forceinline__ bool flag_wait(const int* flag, int want) {
     if (ld_acquire(flag) >= want) return true;
     const unsigned long long t0 = globaltimer();
     while (ld_acquire(flag) < want)
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > wait_limit_ns()) return false;
     return true;
 }
 
@@ -779,7 +460,7 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
             __stcg(reinterpret_cast<float4*>(hst), make_float4(h0.x, h0.y, h1.x, h1.y));
             __threadfence();
             __syncwarp();
-            if (lane == 0) st_release(p.seg_flag + m, sgm + 1);
+            if (lane == 0 && !withhold_handoff(m, sgm)) st_release(p.seg_flag + m, sgm + 1);
         } else if (p.last_state && ch_ok) {
             *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) =
                 make_float4(h0.x, h0.y, h1.x, h1.y);
@@ -789,11 +470,11 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 }
 
 // B and C (rows, N, L) -> staged rows [rows][lpad][B_0..B_{N-1}, C_0..C_{N-1}] of
-// type O (float32 for the relay kernel; the activation type for the segmented
-// kernel, so that its per-step reads move half the bytes), zero beyond L; rows =
+// type O (the activation type, so that the segmented kernel's per-step reads
+// move half the bytes of float32), zero beyond L; rows =
 // batch, or batch * ngroups for B and C per channel group.  One CTA per
 // (64-step tile, row), transposed through shared memory.
-template <typename T, int N, typename O = float>
+template <typename T, int N, typename O>
 __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, const T* __restrict__ C,
                                                        O* __restrict__ bc, int64_t L, int64_t lpad,
                                                        int* __restrict__ flags, int nflags) {
@@ -819,18 +500,18 @@ __global__ void __launch_bounds__(256) bc_stage_kernel(const T* __restrict__ B, 
 
 // ------------------------------------------------------------- host side
 
+// The driver's tensor-map encoder (one process-wide entry point), looked up
+// once; the initialisation of a function-local static is thread-safe.
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -848,43 +529,6 @@ bool make_map(CUtensorMap* m, const void* base, int64_t dim, int64_t L, int64_t 
     return fn(m, dt, 3, const_cast<void*>(base), gdim, gstride, box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
               CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
-template <typename T, int N>
-cudaError_t launch_relay_t(const ScanArgs& a, void* ws, cudaStream_t s) {
-    using CF = RelayCfg<T, N>;
-    constexpr bool kFast = !std::is_same<T, float>::value;
-    const int64_t lpad = relay_lpad(a.seqlen);
-    float* bc = static_cast<float*>(ws);
-    {
-        dim3 grid((unsigned)((lpad + 63) / 64), (unsigned)(a.batch * a.ngroups));
-        bc_stage_kernel<T, N><<<grid, 256, 0, s>>>(static_cast<const T*>(a.B), static_cast<const T*>(a.C), bc,
-                                                   a.seqlen, lpad, nullptr, 0);
-    }
-    CUtensorMap mu, md, mz, mo;
-    if (!make_map<T>(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
-        !make_map<T>(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
-        !make_map<T>(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CW, CF::K) ||
-        !make_map<T>(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CW, CF::K))
-        return cudaErrorInvalidValue;
-    RelayParams rp{a.A, a.D, a.delta_bias, bc, a.last_state, (int)a.dim, (int)a.seqlen, lpad, a.softplus,
-                   a.z != nullptr, a.h0, (int)a.ngroups, (int)a.gch};
-    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, RelayParams);
-    static const Kern kerns[4] = {scan_relay_kernel<T, N, kFast, false, false>,
-                                  scan_relay_kernel<T, N, kFast, false, true>,
-                                  scan_relay_kernel<T, N, kFast, true, false>,
-                                  scan_relay_kernel<T, N, kFast, true, true>};
-    const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
-    static bool attr[4] = {false, false, false, false};
-    if (!attr[which]) {
-        const cudaError_t e =
-            cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        attr[which] = true;
-    }
-    dim3 grid((unsigned)((a.dim + CF::CW - 1) / CF::CW), (unsigned)a.batch);
-    kerns[which]<<<grid, CF::THREADS, CF::SMEM, s>>>(mu, md, mz, mo, rp);
-    return cudaGetLastError();
 }
 
 // Work split of the segmented scan for one call.
@@ -944,17 +588,20 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
                                   scan_seg_kernel<T, N, kFast, true, false>,
                                   scan_seg_kernel<T, N, kFast, true, true>};
     const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
-    static int occ[4] = {0, 0, 0, 0};
-    if (occ[which] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        if (o < 1) return cudaErrorInvalidConfiguration;
-        occ[which] = o;
-    }
-    const SegPlan pl = seg_plan<N, CF::K>(a.batch, a.dim, a.seqlen, sms, occ[which]);
+    // shared-memory size set and resident CTAs per SM measured, once per device
+    static DeviceMemo memo[4];
+    int dev = 0, occ = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    cudaError_t err = cudaSuccess;
+    if (!memo[which].get(dev, [&](int& r) {
+            err = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kerns[which], CF::THREADS, CF::SMEM);
+            if (err == cudaSuccess && r < 1) err = cudaErrorInvalidConfiguration;
+            return err == cudaSuccess;
+        }, &occ))
+        return err;
+    const SegPlan pl = seg_plan<N, CF::K>(a.batch, a.dim, a.seqlen, sms, occ);
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     T* bc = reinterpret_cast<T*>(w);
@@ -1014,10 +661,6 @@ cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* ws, int sms, cuda
 
 int64_t relay_lpad(int64_t seqlen) { return (seqlen + 63) / 64 * 64; }
 
-int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate, int64_t ngroups) {
-    return batch * ngroups * relay_lpad(seqlen) * 2 * dstate * (int64_t)sizeof(float);
-}
-
 bool relay_supported(const ScanArgs& a, DType dt) {
     const int64_t es = dt == DType::BF16 ? 2 : 4;
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
@@ -1033,21 +676,10 @@ bool relay_supported(const ScanArgs& a, DType dt) {
     return encode_fn() != nullptr;
 }
 
-cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* ws, cudaStream_t s) {
-    if (dt == DType::F32) {
-        switch (a.dstate) {
-            case 4: return launch_relay_t<float, 4>(a, ws, s);
-            case 8: return launch_relay_t<float, 8>(a, ws, s);
-            case 16: return launch_relay_t<float, 16>(a, ws, s);
-        }
-    } else {
-        switch (a.dstate) {
-            case 4: return launch_relay_t<__nv_bfloat16, 4>(a, ws, s);
-            case 8: return launch_relay_t<__nv_bfloat16, 8>(a, ws, s);
-            case 16: return launch_relay_t<__nv_bfloat16, 16>(a, ws, s);
-        }
-    }
-    return cudaErrorInvalidValue;
+int set_wait_test_seg(int withhold, unsigned long long limit_ns) {
+    if (cudaMemcpyToSymbol(g_withhold_flag, &withhold, sizeof(withhold)) != cudaSuccess) return -1;
+    if (cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(limit_ns)) != cudaSuccess) return -1;
+    return 0;
 }
 
 int read_device_error(bool clear) {

@@ -10,38 +10,35 @@
 //
 // Why tensor memory
 // -----------------
-// A lane keeps 4 of a channel's N states (lane = channel * R + g, R = N / 4,
-// states 4g .. 4g+3), so at every step it needs 4 values of B_t and 4 of
-// C_t -- the same 8 values for all channels.  Read from shared memory, that
-// is 32 bytes per lane per step through the load/store unit, which bounds the
-// scan well before the SFU does.  Here a one-hot matrix product writes them
-// into tensor memory instead, already in per-lane order: with
+// A lane keeps G of a channel's 16 states (G = 2 in scan_tmem2_kernel, 4 in
+// scan_ws_kernel; lane group g holds states G g .. G g + G - 1), so at every
+// step it needs G values of B_t and G of C_t -- the same values for all
+// channels.  Read from shared memory, that is 8 G bytes per lane per step
+// through the load/store unit, which bounds the scan well before the SFU
+// does.  Here a one-hot matrix product writes them into tensor memory
+// instead, already in per-lane order: with a selector
 //     S[r, k] = 1 if k == g(r) else 0          (128 x 8, one row per lane)
-//     X[k, 8t + j] = B_t[4k + j] (j < 4),  C_t[4k + j - 4] (j >= 4)
-// the product D = S X (tcgen05.mma, kind::tf32, f32 accumulate) has in row r
-// exactly the quads lane r needs, and the lane fetches a step's 8 values with
-// a quarter of one tcgen05.ld.  The product is exact: B and C are bfloat16
-// values (8-bit significands, exactly representable in tf32), multiplied by
-// 1 or 0 and summed with zeros.
+// and X[k, :] the B and C values of lane group k step after step, the
+// product D = S X (tcgen05.mma, kind::tf32, f32 accumulate) has in row r
+// exactly the values lane r needs, and the lane fetches several steps of them
+// with one tcgen05.ld.  The product is exact: B and C are bfloat16 values
+// (8-bit significands, exactly representable in tf32), multiplied by 1 or 0
+// and summed with zeros.
 //
 // Work decomposition
 // ------------------
-// A CTA owns CC = 4 * CW consecutive channels of one batch row (CW = 32 / R
-// per consumer warp) and walks a segment of the sequence in chunks of K
-// steps.  Every (batch, channel group) chain is cut into S segments; task
-// i = s * M + m (segment s of chain m) goes to CTA i mod W in slot i div W,
-// so a segment's predecessor always sits in an earlier slot (W <= M) and the
-// state passes between segments through the workspace with a bounded
-// release/acquire flag wait; the launch is cooperative, so every CTA a
-// segment may wait on is resident.
-//   producer warp: TMA loads of the u, delta_raw and z tiles (64- or 128-byte
-//     rows, hardware-swizzled so the consumers' column reads are free of bank
-//     conflicts) and of the chunk's staged X operand; then the one-hot MMA
-//     into one of two TMEM buffers;
-//   consumer warps (the four TMEM lane quarters): the per-(t, d) terms
-//     (softplus, Delta u, silu(z)), the recurrence with B and C from TMEM, the
-//     readout summed over the R lanes of each channel, D u and the gate, and a
-//     TMA store of the output tile.
+// A CTA (one per SM) owns 32 consecutive channels of one batch row and walks
+// a segment of the sequence in chunks.  Every (batch, channel group) chain is
+// cut into S segments; task i = s * M + m (segment s of chain m) goes to CTA
+// i mod W in slot i div W, so a segment's predecessor always sits in an
+// earlier slot (W <= M) and the state passes between segments through the
+// workspace with a bounded release/acquire flag wait; the launch is
+// cooperative, so every CTA a segment may wait on is resident.  A loader
+// warp issues the TMA loads of the u, delta_raw and z tiles (64-byte rows,
+// hardware-swizzled so that column reads are free of bank conflicts) and of
+// the chunk's staged X operand, an MMA warp the one-hot product into one of
+// two TMEM buffers, a store warp the TMA stores of the output tiles; the
+// compute warps of the two kernels are described with each.
 //
 // Every wait is bounded (~1 s, %globaltimer); on giving up a warp sets a bit
 // in the device error word, drains its own copies and the CTA still frees its
@@ -54,6 +51,7 @@
 #include <cstdint>
 #include <type_traits>
 
+#include "device_memo.h"
 #include "scan_common.cuh"
 #include "ssm_internal.cuh"
 
@@ -132,53 +130,6 @@ __host__ __device__ constexpr uint32_t idesc_tf32(int m, int n) {
 
 // ------------------------------------------------------------- configuration
 
-template <int N_>
-struct TmCfg {
-    static constexpr int N = N_;
-    static constexpr int G = 4;                 // states per lane
-    static constexpr int R = N / G;             // lanes per channel
-    static constexpr int CW = 32 / R;           // channels per consumer warp
-    static constexpr int WARPS = 4;             // consumer warps = TMEM lane quarters
-    static constexpr int CC = WARPS * CW;       // channels per CTA
-    static constexpr int K = 32;                // steps per chunk
-    static constexpr int KR = K / R;            // steps per lane in the per-(t, d) phase
-    static constexpr int NP = KR / 2;           // step pairs per lane
-    static constexpr int P = 8;                 // input ring slots (a power of two)
-    static constexpr int OB = 3;                // output tiles
-    static constexpr int W_LOAD = WARPS;        // role warps: TMA loads,
-    static constexpr int W_MMA = WARPS + 1;     //   the one-hot MMA,
-    static constexpr int W_STORE = WARPS + 2;   //   output stores
-    static constexpr int THREADS = 32 * (WARPS + 3);
-    static constexpr int ROWB = CC * 2;         // bytes of a bf16 tile row
-    static_assert(ROWB == 64 || ROWB == 128, "tile rows are 64 or 128 bytes (swizzled)");
-    static constexpr int TILE = K * ROWB;
-    static constexpr int OPB = K * 8 * 16;      // X operand of a chunk: 8 columns of 4 tf32 per step
-    static constexpr int TCOLS = 8 * K;         // TMEM columns of a chunk
-    static constexpr int TMEM_COLS = 2 * TCOLS; // two buffers
-    static_assert(TCOLS <= 256 && TMEM_COLS <= 512, "one MMA per chunk, two chunks of TMEM");
-    static constexpr int al(int x, int a) { return (x + a - 1) / a * a; }
-    static constexpr int SLOT_U = 0;
-    static constexpr int SLOT_D = al(TILE, 1024);
-    static constexpr int SLOT_Z = 2 * al(TILE, 1024);
-    static constexpr int SLOT_X = 3 * al(TILE, 1024);
-    static constexpr int SLOT = al(SLOT_X + OPB, 1024);
-    static constexpr int A_OP = P * SLOT;                    // 128 x 8 tf32 selector, 4 KB
-    static constexpr int OUT = A_OP + 4096;                  // OB swizzled output tiles
-    static constexpr int OUTT = al(TILE, 1024);
-    static constexpr int W_BASE = OUT + OB * OUTT;
-    static constexpr int DPS = CW + 2;                       // float2 stride of a dp row (conflict-free stores)
-    static constexpr int RS2 = 33;                           // float2 stride of a reduction row
-    static constexpr int W_RED = al(K * DPS * 8, 128);
-    static constexpr int W_BYTES = W_RED + (R > 1 ? al((K / 2) * RS2 * 8, 128) : 0);
-    static constexpr int BAR = W_BASE + WARPS * W_BYTES;     // full[P] empty[P] tfull[2] tempty[2] ofull[OB] oempty[OB]
-    static constexpr int NBAR = 2 * P + 4 + 2 * OB;
-    static constexpr int USED = BAR + NBAR * 8 + 16;         // + the TMEM address
-    // Over half of an SM's shared memory (plus 1 KB to align the base), so a
-    // CTA never shares its SM: the 512 TMEM columns it allocates are free.
-    static constexpr int SMEM = (USED + 1024 > 120 * 1024) ? USED + 1024 : 120 * 1024;
-    static_assert(SMEM <= 227 * 1024, "shared memory of one CTA");
-};
-
 struct TmParams {
     const float* A;
     const float* D;
@@ -210,7 +161,7 @@ __device__ __forceinline__ bool tm_flag_wait(const int* flag, int want) {
     if (tm_ld_acquire(flag) >= want) return true;
     const unsigned long long t0 = globaltimer();
     while (tm_ld_acquire(flag) < want)
-        if (globaltimer() - t0 > kWaitLimitNs) return false;
+        if (globaltimer() - t0 > wait_limit_ns()) return false;
     return true;
 }
 
@@ -248,383 +199,6 @@ struct ChunkCursor {
         return task < p.M * p.S;
     }
 };
-
-template <int N, bool kSoftplus, bool kGate>
-__global__ void __launch_bounds__(TmCfg<N>::THREADS, 1)
-scan_tmem_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__ CUtensorMap tm_d,
-                 const __grid_constant__ CUtensorMap tm_z, const __grid_constant__ CUtensorMap tm_out,
-                 const TmParams p) {
-    using CF = TmCfg<N>;
-    using T = __nv_bfloat16;
-    constexpr int K = CF::K, P = CF::P, OB = CF::OB, R = CF::R, CW = CF::CW, CC = CF::CC, KR = CF::KR,
-                  NP = CF::NP;
-    constexpr int DPS = CF::DPS, RS2 = CF::RS2;
-    extern __shared__ __align__(1024) unsigned char smem_raw[];
-    // 1024-byte aligned base: the swizzle pattern follows absolute address bits
-    unsigned char* smem = smem_raw + ((1024u - (smem_u32(smem_raw) & 1023u)) & 1023u);
-
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    const uint32_t ring_s = smem_u32(smem);
-    const uint32_t bar_full = smem_u32(smem + CF::BAR);
-    const uint32_t bar_empty = bar_full + 8u * P;
-    const uint32_t bar_tfull = bar_empty + 8u * P;
-    const uint32_t bar_tempty = bar_tfull + 16u;
-    const uint32_t bar_ofull = bar_tempty + 16u;
-    const uint32_t bar_oempty = bar_ofull + 8u * OB;
-    uint32_t* taddr_slot = reinterpret_cast<uint32_t*>(smem + CF::BAR + CF::NBAR * 8);
-
-    const int L = p.seqlen;
-    const int nch = (L + K - 1) / K;
-
-    // one-hot selector S[r][k] = (k == g(r)), K-major without swizzle: the
-    // 8-row x 16-byte core matrix of rows 8 rg.. and k-half kh at rg*256 + kh*128
-    {
-        float* sa = reinterpret_cast<float*>(smem + CF::A_OP);
-        for (int e = threadIdx.x; e < 128 * 8; e += CF::THREADS) {
-            const int r = e >> 3, k = e & 7;
-            sa[(r >> 3) * 64 + (k >> 2) * 32 + (r & 7) * 4 + (k & 3)] = (k == ((r & 31) % R)) ? 1.f : 0.f;
-        }
-    }
-    fence_async_smem();
-    if (threadIdx.x == 0) {
-        for (int i = 0; i < P; ++i) {
-            mbar_init(bar_full + 8u * i, 1);
-            mbar_init(bar_empty + 8u * i, CF::WARPS);
-        }
-        for (int i = 0; i < 2; ++i) {
-            mbar_init(bar_tfull + 8u * i, 1);
-            mbar_init(bar_tempty + 8u * i, CF::WARPS);
-        }
-        for (int i = 0; i < OB; ++i) {
-            mbar_init(bar_ofull + 8u * i, CF::WARPS);
-            mbar_init(bar_oempty + 8u * i, 1);
-        }
-        fence_mbar_init();
-    }
-    if (warp == CF::W_LOAD) {
-        tmem_alloc(smem_u32(taddr_slot), CF::TMEM_COLS);
-        tmem_relinquish();
-    }
-    tc_fence_before();
-    __syncthreads();
-    tc_fence_after();
-    const uint32_t tmem = *taddr_slot;
-
-    // chunks this CTA walks (the same sequence for every role)
-    int total = 0;
-    for (int task = blockIdx.x; task < p.M * p.S; task += p.workers) {
-        const int sgm = task / p.M;
-        total += min((sgm + 1) * p.cps, nch) - sgm * p.cps;
-    }
-
-    if (warp == CF::W_LOAD) {
-        // ------------------------------------------------------------ TMA loads
-        if (lane == 0) {
-            constexpr uint32_t tx_bytes = (uint32_t)((kGate ? 3 : 2) * CF::TILE + CF::OPB);
-            ChunkCursor cur;
-            cur.start(p, nch, CC);
-            int issued = 0;
-            auto issue = [&]() {
-                if (!cur.valid(p, nch, CC)) return;
-                const int slot = issued & (P - 1);
-                const uint32_t base = ring_s + (uint32_t)(slot * CF::SLOT);
-                const uint32_t bar = bar_full + 8u * (uint32_t)slot;
-                const int t0 = cur.c * K;
-                mbar_expect_tx(bar, tx_bytes);
-                tma_load_3d(base + CF::SLOT_U, &tm_u, cur.d0, t0, cur.b, bar);
-                tma_load_3d(base + CF::SLOT_D, &tm_d, cur.d0, t0, cur.b, bar);
-                if constexpr (kGate) tma_load_3d(base + CF::SLOT_Z, &tm_z, cur.d0, t0, cur.b, bar);
-                bulk_load(base + CF::SLOT_X, p.xop + ((size_t)cur.xb * p.lpad + (size_t)t0) * 32, CF::OPB, bar);
-                ++cur.c;
-                ++issued;
-            };
-            for (int i = 0; i < P && i < total; ++i) issue();
-            for (int j = 0; j + P < total; ++j) {
-                // slot j % P is free once every consumer has read chunk j's
-                // tiles and seen its MMA (the reader of X) complete
-                if (!mbar_wait(bar_empty + 8u * (uint32_t)(j & (P - 1)), (uint32_t)((j / P) & 1))) {
-                    raise_error(2u);
-                    break;
-                }
-                issue();
-            }
-            // the CTA's shared memory outlives every copy into it
-            for (int k = max(0, issued - P); k < issued; ++k)
-                if (!mbar_wait(bar_full + 8u * (uint32_t)(k & (P - 1)), (uint32_t)((k / P) & 1))) break;
-        }
-    } else if (warp == CF::W_MMA) {
-        // ------------------------------------------------------------ one-hot MMA
-        if (lane == 0) {
-            const uint64_t adesc = smem_desc(smem_u32(smem + CF::A_OP), 128, 256);
-            constexpr uint32_t idesc = idesc_tf32(128, CF::TCOLS);
-            int mmas = 0;
-            for (int j = 0; j < total; ++j) {
-                const int slot = j & (P - 1), tb = j & 1;
-                if (!mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1))) {
-                    raise_error(1u);
-                    break;
-                }
-                if (j >= 2 && !mbar_wait(bar_tempty + 8u * tb, (uint32_t)(((j - 2) >> 1) & 1))) {
-                    raise_error(2u);
-                    break;
-                }
-                tc_fence_after();
-                // X of this slot: 8-row core matrices of 16-byte rows, one per
-                // step (SBO 128); the second k-half aliases the first (LBO 0),
-                // which the selector multiplies by zero.
-                const uint64_t bdesc = smem_desc(ring_s + (uint32_t)(slot * CF::SLOT + CF::SLOT_X), 0, 128);
-                mma_tf32(tmem + (uint32_t)(tb * CF::TCOLS), adesc, bdesc, idesc);
-                mma_commit(bar_tfull + 8u * tb);
-                ++mmas;
-            }
-            // tensor memory is released only after the last MMAs completed
-            for (int k = max(0, mmas - 2); k < mmas; ++k)
-                if (!mbar_wait(bar_tfull + 8u * (uint32_t)(k & 1), (uint32_t)((k >> 1) & 1))) break;
-        }
-    } else if (warp == CF::W_STORE) {
-        // ------------------------------------------------------------ output stores
-        if (lane == 0) {
-            ChunkCursor cur;
-            cur.start(p, nch, CC);
-            for (int j = 0; j < total && cur.valid(p, nch, CC); ++j, ++cur.c) {
-                const int o = j % OB;
-                if (!mbar_wait(bar_ofull + 8u * o, (uint32_t)((j / OB) & 1))) {
-                    raise_error(2u);
-                    break;
-                }
-                tma_store_3d(&tm_out, cur.d0, cur.c * K, cur.b, smem_u32(smem + CF::OUT + o * CF::OUTT));
-                bulk_commit();
-                // the store before this one has read its tile: hand it back
-                bulk_wait_read<1>();
-                if (j >= 1) mbar_arrive(bar_oempty + 8u * (uint32_t)((j - 1) % OB));
-            }
-            bulk_wait_all();
-        }
-    } else {
-        // ------------------------------------------------------------ consumers
-        const int w = warp;
-        const int ch = lane / R, g = lane % R;
-        float2* dp = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES);
-        float2* red = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES + CF::W_RED);
-        const uint32_t tlane = tmem + ((uint32_t)(32 * w) << 16);
-
-        int tas[NP];
-#pragma unroll
-        for (int q = 0; q < NP; ++q) tas[q] = g * KR + 2 * ((q + g * (CW / 8)) % NP);
-
-        bool ok = true;
-        int j = 0;
-        for (int task = blockIdx.x; task < p.M * p.S && ok; task += p.workers) {
-            const int sgm = task / p.M, m = task - sgm * p.M;
-            const int b = m / p.units;
-            const int dcta = (m - b * p.units) * CC;
-            const int d = dcta + w * CW + ch;
-            const bool ch_ok = d < p.dim;
-            const int cb = sgm * p.cps, ce = min(cb + p.cps, nch);
-            const int chain = m * CF::WARPS + w;
-
-            float2 A2[2];
-            {
-                const float4 a = ch_ok ? *reinterpret_cast<const float4*>(p.A + (size_t)d * N + 4 * g)
-                                       : make_float4(0.f, 0.f, 0.f, 0.f);
-                A2[0] = make_float2(a.x * kLog2e, a.y * kLog2e);
-                A2[1] = make_float2(a.z * kLog2e, a.w * kLog2e);
-            }
-            const float2 dskip2 = splat2((p.D && ch_ok) ? p.D[d] : 0.f);
-            const float2 bias2 = splat2((p.delta_bias && ch_ok) ? p.delta_bias[d] : 0.f);
-
-            float2 h0 = make_float2(0.f, 0.f), h1 = make_float2(0.f, 0.f);
-            float* hst = p.seg_state + ((size_t)chain * CW + ch) * N + 4 * g;
-            if (sgm > 0) {
-                if (!__all_sync(0xffffffffu, tm_flag_wait(p.seg_flag + chain, sgm))) {
-                    ok = false;
-                    if (lane == 0) raise_error(4u);
-                    break;
-                }
-                const float4 v = __ldcg(reinterpret_cast<const float4*>(hst));
-                h0 = make_float2(v.x, v.y);
-                h1 = make_float2(v.z, v.w);
-            } else if (p.h0 && ch_ok) {
-                const float4 v = *reinterpret_cast<const float4*>(p.h0 + ((size_t)b * p.dim + d) * N + 4 * g);
-                h0 = make_float2(v.x, v.y);
-                h1 = make_float2(v.z, v.w);
-            }
-
-            for (int c = cb; c < ce; ++c, ++j) {
-                const int slot = j & (P - 1), tb = j & 1;
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_full + 8u * slot, (uint32_t)((j / P) & 1)))) {
-                    ok = false;
-                    if (lane == 0) raise_error(1u);
-                    break;
-                }
-                const int t0 = c * K;
-                const unsigned char* sb = smem + slot * CF::SLOT;
-
-                // ---- per-(t, d) terms for this lane's step pairs
-                float2 uk[NP], gate[NP];
-                {
-                    float2 dpv[2 * NP];
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        const int ta = tas[q];
-                        const uint32_t oa = swz<CF::ROWB>(ta, w * CW + ch);
-                        const uint32_t ob = swz<CF::ROWB>(ta + 1, w * CW + ch);
-                        const float2 uv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + oa)),
-                                                      ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + ob)));
-                        const float2 xr = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + oa)),
-                                                      ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + ob)));
-                        float2 dl = add2(xr, bias2);
-                        if constexpr (kSoftplus) dl = relay_softplus2<true>(dl);
-                        if (t0 + K > L)
-                            dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + ta + 1 < L ? 1.f : 0.f));
-                        const float2 du = mul2(dl, uv);
-                        dpv[2 * q] = make_float2(dl.x, du.x);
-                        dpv[2 * q + 1] = make_float2(dl.y, du.y);
-                        uk[q] = uv;
-                        if constexpr (kGate) {
-                            const float2 zv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_Z + oa)),
-                                                          ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_Z + ob)));
-                            gate[q] = seg_silu2<true>(zv);
-                        } else {
-                            gate[q] = splat2(1.f);
-                        }
-                    }
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        dp[tas[q] * DPS + ch] = dpv[2 * q];
-                        dp[(tas[q] + 1) * DPS + ch] = dpv[2 * q + 1];
-                    }
-                }
-                __syncwarp();
-
-                // ---- this chunk's B and C are in TMEM buffer tb once its MMA completed
-                if (!__all_sync(0xffffffffu, mbar_wait(bar_tfull + 8u * tb, (uint32_t)((j >> 1) & 1)))) {
-                    ok = false;
-                    if (lane == 0) raise_error(2u);
-                    break;
-                }
-                tc_fence_after();
-                if (lane == 0) mbar_arrive(bar_empty + 8u * slot);
-
-                // ---- the recurrence, software-pipelined over the chunk's K steps:
-                // step t loads Delta and Delta u of step t+LA, evaluates exp(Delta A)
-                // and Delta B u of step t+EA, advances the state by step t and reads
-                // out C_t . h_t.  B and C come from TMEM in groups of 4 steps (32
-                // columns), each group requested one group ahead of its use.
-                constexpr int LA = 4, EA = 2, NG = K / 4;
-                const uint32_t tcol = tlane + (uint32_t)(tb * CF::TCOLS);
-                uint32_t gv[NG][32];
-                tmem_ld32(tcol, gv[0]);
-                tmem_wait(gv[0]);
-                if (NG > 1) tmem_ld32(tcol + 32, gv[1]);
-                float2 qv[K];
-                float2 dA[K][2], dB[K][2];
-                float2 s2v[K / 2];
-                auto bq = [&](int t, int i) { return __uint_as_float(gv[t >> 2][(t & 3) * 8 + i]); };
-                auto load_step = [&](int t) { qv[t] = dp[t * DPS + ch]; };
-                auto exp_step = [&](int t) {
-                    const float2 dl2 = splat2(qv[t].x), du2 = splat2(qv[t].y);
-                    const float2 e0 = mul2(dl2, A2[0]);
-                    const float2 e1 = mul2(dl2, A2[1]);
-                    dA[t][0] = make_float2(decay_exp2<true>(e0.x), decay_exp2<true>(e0.y));
-                    dA[t][1] = make_float2(decay_exp2<true>(e1.x), decay_exp2<true>(e1.y));
-                    dB[t][0] = mul2(du2, make_float2(bq(t, 0), bq(t, 1)));
-                    dB[t][1] = mul2(du2, make_float2(bq(t, 2), bq(t, 3)));
-                };
-#pragma unroll
-                for (int t = 0; t < LA; ++t) load_step(t);
-#pragma unroll
-                for (int t = 0; t < EA; ++t) exp_step(t);
-                float2 acc_prev = make_float2(0.f, 0.f);
-#pragma unroll
-                for (int t = 0; t < K; ++t) {
-                    if (t + EA < K && ((t + EA) & 3) == 0) {
-                        const int gr = (t + EA) >> 2;
-                        tmem_wait(gv[gr]);
-                        if (gr + 1 < NG) tmem_ld32(tcol + 32u * (uint32_t)(gr + 1), gv[gr + 1]);
-                    }
-                    if (t + LA < K) load_step(t + LA);
-                    if (t + EA < K) exp_step(t + EA);
-                    h0 = fma2(dA[t][0], h0, dB[t][0]);
-                    h1 = fma2(dA[t][1], h1, dB[t][1]);
-                    const float2 acc = fma2(make_float2(bq(t, 6), bq(t, 7)), h1,
-                                            mul2(make_float2(bq(t, 4), bq(t, 5)), h0));
-                    if (t & 1) s2v[t / 2] = make_float2(acc_prev.x + acc_prev.y, acc.x + acc.y);
-                    acc_prev = acc;
-                }
-                tc_fence_before();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_tempty + 8u * tb);
-
-                // ---- sum the R lanes of each channel for this lane's pairs
-                float2 yv[NP];
-                if constexpr (R == 1) {
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) yv[q] = s2v[tas[q] / 2];
-                } else {
-#pragma unroll
-                    for (int t = 0; t < K / 2; ++t) red[t * RS2 + lane] = s2v[t];
-                    __syncwarp();
-                    float2 pr[NP][R];
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        const float2* row = red + (tas[q] / 2) * RS2 + ch * R;
-#pragma unroll
-                        for (int gg = 0; gg < R; ++gg) pr[q][gg] = row[gg];
-                    }
-#pragma unroll
-                    for (int q = 0; q < NP; ++q) {
-                        float2 sum = pr[q][0];
-#pragma unroll
-                        for (int gg = 1; gg < R; ++gg) sum = add2(sum, pr[q][gg]);
-                        yv[q] = sum;
-                    }
-                }
-
-                // ---- D u and the gate into the CTA's output tile j % OB, once the
-                // store that last read it (chunk j - OB) has finished
-                const int o = j % OB;
-                if (j >= OB &&
-                    !__all_sync(0xffffffffu, mbar_wait(bar_oempty + 8u * o, (uint32_t)(((j / OB) - 1) & 1)))) {
-                    ok = false;
-                    if (lane == 0) raise_error(2u);
-                    break;
-                }
-                unsigned char* so = smem + CF::OUT + o * CF::OUTT;
-#pragma unroll
-                for (int q = 0; q < NP; ++q) {
-                    const float2 y = mul2(fma2(dskip2, uk[q], yv[q]), gate[q]);
-                    st_pair<T>(reinterpret_cast<T*>(so + swz<CF::ROWB>(tas[q], w * CW + ch)),
-                               reinterpret_cast<T*>(so + swz<CF::ROWB>(tas[q] + 1, w * CW + ch)), y);
-                }
-                fence_async_smem();
-                __syncwarp();
-                if (lane == 0) mbar_arrive(bar_ofull + 8u * o);
-            }
-            if (!ok) break;
-
-            // state leaving the segment
-            if (sgm + 1 < p.S) {
-                __stcg(reinterpret_cast<float4*>(hst), make_float4(h0.x, h0.y, h1.x, h1.y));
-                __threadfence();
-                __syncwarp();
-                if (lane == 0) tm_st_release(p.seg_flag + chain, sgm + 1);
-            } else if (p.last_state && ch_ok) {
-                *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) =
-                    make_float4(h0.x, h0.y, h1.x, h1.y);
-            }
-        }
-    }
-
-    // every warp ends here: the tensor memory is released exactly once
-    tc_fence_before();
-    __syncthreads();
-    if (warp == CF::W_LOAD) {
-        __syncwarp();
-        tc_fence_after();
-        tmem_dealloc(tmem, CF::TMEM_COLS);
-    }
-}
 
 // ===================================================================
 // Two states per lane: 8 consumer warps, two per TMEM lane quarter (both read
@@ -1000,7 +574,7 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                 __stcg(reinterpret_cast<float2*>(hst), h);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) tm_st_release(p.seg_flag + chain, sgm + 1);
+                if (lane == 0 && !withhold_handoff(chain, sgm)) tm_st_release(p.seg_flag + chain, sgm + 1);
             } else if (p.last_state && ch_ok) {
                 *reinterpret_cast<float2*>(p.last_state + ((size_t)b * p.dim + d) * N + 2 * g) = h;
             }
@@ -1518,7 +1092,7 @@ scan_ws_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant__
                 __stcg(reinterpret_cast<float4*>(hst), hv);
                 __threadfence();
                 __syncwarp();
-                if (lane == 0) tm_st_release(p.seg_flag + chain, sgm + 1);
+                if (lane == 0 && !withhold_handoff(chain, sgm)) tm_st_release(p.seg_flag + chain, sgm + 1);
             } else if (p.last_state && ch_ok) {
                 *reinterpret_cast<float4*>(p.last_state + ((size_t)b * p.dim + d) * N + 4 * g) = hv;
             }
@@ -1565,18 +1139,18 @@ __global__ void __launch_bounds__(256) tm_stage_kernel(const __nv_bfloat16* __re
     }
 }
 
+// The driver's tensor-map encoder (one process-wide entry point), looked up
+// once; the initialisation of a function-local static is thread-safe.
 PFN_cuTensorMapEncodeTiled_v12000 tm_encode_fn() {
-    static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
-    static bool tried = false;
-    if (!tried) {
-        tried = true;
+    static const PFN_cuTensorMapEncodeTiled_v12000 fn = [] {
         void* f = nullptr;
         cudaDriverEntryPointQueryResult q;
         if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) ==
                 cudaSuccess &&
             q == cudaDriverEntryPointSuccess)
-            fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
-    }
+            return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+        return static_cast<PFN_cuTensorMapEncodeTiled_v12000>(nullptr);
+    }();
     return fn;
 }
 
@@ -1598,13 +1172,15 @@ struct TmPlan {
     int units, M, S, cps, grid;
 };
 
-template <int N>
-TmPlan tm_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
-    using CF = TmCfg<N>;
+// Work split of one call: M chains (batch rows x channel groups of cc),
+// each cut into S segments of cps chunks of k steps; task i = s * M + m runs
+// on CTA i % grid.  With more chains than SMs, S is the most even split of
+// M * S tasks over the CTAs (segments of at least four chunks, at most 64).
+TmPlan tm_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms, int cc, int k) {
     TmPlan pl{};
-    pl.units = (int)((dim + CF::CC - 1) / CF::CC);
+    pl.units = (int)((dim + cc - 1) / cc);
     pl.M = (int)(batch * pl.units);
-    const int nch = (int)((seqlen + CF::K - 1) / CF::K);
+    const int nch = (int)((seqlen + k - 1) / k);
     if (pl.M <= sms) {
         pl.grid = pl.M;
         pl.S = 1;
@@ -1612,8 +1188,6 @@ TmPlan tm_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
         return pl;
     }
     pl.grid = sms;
-    // segments per chain: the most even split of M * S tasks over the CTAs,
-    // with segments of at least four chunks and at most 64 segments
     int bestS = 1;
     double best = 1e30;
     const int smax = std::max(1, std::min(64, nch / 4));
@@ -1632,98 +1206,27 @@ TmPlan tm_plan(int64_t batch, int64_t dim, int64_t seqlen, int sms) {
 }
 
 
-template <int N>
-cudaError_t launch_tmem_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
-    using CF = TmCfg<N>;
-    using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TmParams);
-    static const Kern kerns[4] = {scan_tmem_kernel<N, false, false>, scan_tmem_kernel<N, false, true>,
-                                  scan_tmem_kernel<N, true, false>, scan_tmem_kernel<N, true, true>};
-    const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
-    static int occ[4] = {0, 0, 0, 0};
-    if (occ[which] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        if (o != 1) return cudaErrorInvalidConfiguration;   // one CTA per SM: TMEM is never contended
-        occ[which] = o;
-    }
-    const TmPlan pl = tm_plan<N>(a.batch, a.dim, a.seqlen, sms);
-    const int64_t lpad = relay_lpad(a.seqlen);
-    unsigned char* w = static_cast<unsigned char*>(ws);
-    float* xop = reinterpret_cast<float*>(w);
-    const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
-    const int64_t chains = (int64_t)pl.M * CF::WARPS;
-    float* st = reinterpret_cast<float*>(w + x_bytes);
-    const int64_t st_bytes = (chains * CF::CW * N * 4 + 255) / 256 * 256;
-    int* flags = reinterpret_cast<int*>(w + x_bytes + st_bytes);
-    {
-        dim3 grid((unsigned)(lpad / 64), (unsigned)(a.batch * a.ngroups));
-        tm_stage_kernel<N><<<grid, 256, 0, s>>>(static_cast<const __nv_bfloat16*>(a.B),
-                                                static_cast<const __nv_bfloat16*>(a.C), xop, (int)a.seqlen, lpad,
-                                                flags, (int)chains);
-    }
-    const CUtensorMapSwizzle sw = CF::ROWB == 64 ? CU_TENSOR_MAP_SWIZZLE_64B : CU_TENSOR_MAP_SWIZZLE_128B;
-    CUtensorMap mu, md, mz, mo;
-    if (!tm_make_map(&mu, a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
-        !tm_make_map(&md, a.delta, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
-        !tm_make_map(&mz, a.z ? a.z : a.u, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw) ||
-        !tm_make_map(&mo, a.out, a.dim, a.seqlen, a.batch, CF::CC, CF::K, sw))
-        return cudaErrorInvalidValue;
-    TmParams tp{a.A, a.D, a.delta_bias, xop, a.last_state, st, flags, (int)a.dim, (int)a.seqlen, lpad,
-                pl.units, pl.M, pl.S, pl.cps, pl.grid, a.h0, (int)a.ngroups, (int)a.gch};
-    void* args[] = {&mu, &md, &mz, &mo, &tp};
-    // Segments wait on segments of other CTAs: every CTA must be resident,
-    // which the cooperative launch guarantees (one CTA per SM, grid <= SMs).
-    return cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kerns[which]), dim3(pl.grid),
-                                       dim3(CF::THREADS), args, CF::SMEM, s);
-}
-
 cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
     using CF = Tm2Cfg;
     using Kern = void (*)(CUtensorMap, CUtensorMap, CUtensorMap, CUtensorMap, TmParams);
     static const Kern kerns[4] = {scan_tmem2_kernel<false, false>, scan_tmem2_kernel<false, true>,
                                   scan_tmem2_kernel<true, false>, scan_tmem2_kernel<true, true>};
     const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
-    static int occ[4] = {0, 0, 0, 0};
-    if (occ[which] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        if (o != 1) return cudaErrorInvalidConfiguration;
-        occ[which] = o;
-    }
+    // shared-memory size set and one CTA per SM confirmed, once per device
+    static DeviceMemo memo[4];
+    int dev = 0, occ = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    cudaError_t err = cudaSuccess;
+    if (!memo[which].get(dev, [&](int& r) {
+            err = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kerns[which], CF::THREADS, CF::SMEM);
+            if (err == cudaSuccess && r != 1) err = cudaErrorInvalidConfiguration;   // TMEM never contended
+            return err == cudaSuccess;
+        }, &occ))
+        return err;
     // the work split depends only on the CTA's channel count and chunk length
-    TmPlan pl{};
-    {
-        pl.units = (int)((a.dim + CF::CC - 1) / CF::CC);
-        pl.M = (int)(a.batch * pl.units);
-        const int nch = (int)((a.seqlen + CF::K - 1) / CF::K);
-        if (pl.M <= sms) {
-            pl.grid = pl.M;
-            pl.S = 1;
-            pl.cps = nch;
-        } else {
-            pl.grid = sms;
-            int bestS = 1;
-            double best = 1e30;
-            const int smax = std::max(1, std::min(64, nch / 4));
-            for (int S = 1; S <= smax; ++S) {
-                const int cps = (nch + S - 1) / S;
-                const int s_eff = (nch + cps - 1) / cps;
-                const double cost = std::ceil(double(pl.M) * s_eff / pl.grid) * cps;
-                if (cost < best * 0.999) {
-                    best = cost;
-                    bestS = S;
-                }
-            }
-            pl.cps = (nch + bestS - 1) / bestS;
-            pl.S = (nch + pl.cps - 1) / pl.cps;
-        }
-    }
+    const TmPlan pl = tm_plan(a.batch, a.dim, a.seqlen, sms, CF::CC, CF::K);
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
@@ -1757,17 +1260,20 @@ cudaError_t launch_ws(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
     static const Kern kerns[4] = {scan_ws_kernel<false, false>, scan_ws_kernel<false, true>,
                                   scan_ws_kernel<true, false>, scan_ws_kernel<true, true>};
     const int which = (a.softplus ? 2 : 0) + (a.z ? 1 : 0);
-    static int occ[4] = {0, 0, 0, 0};
-    if (occ[which] == 0) {
-        cudaError_t e = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        int o = 0;
-        e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&o, kerns[which], CF::THREADS, CF::SMEM);
-        if (e != cudaSuccess) return e;
-        if (o != 1) return cudaErrorInvalidConfiguration;
-        occ[which] = o;
-    }
-    const TmPlan pl = tm_plan<16>(a.batch, a.dim, a.seqlen, sms);
+    // shared-memory size set and one CTA per SM confirmed, once per device
+    static DeviceMemo memo[4];
+    int dev = 0, occ = 0;
+    if (cudaError_t e = cudaGetDevice(&dev); e != cudaSuccess) return e;
+    cudaError_t err = cudaSuccess;
+    if (!memo[which].get(dev, [&](int& r) {
+            err = cudaFuncSetAttribute(kerns[which], cudaFuncAttributeMaxDynamicSharedMemorySize, CF::SMEM);
+            if (err == cudaSuccess)
+                err = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&r, kerns[which], CF::THREADS, CF::SMEM);
+            if (err == cudaSuccess && r != 1) err = cudaErrorInvalidConfiguration;   // TMEM never contended
+            return err == cudaSuccess;
+        }, &occ))
+        return err;
+    const TmPlan pl = tm_plan(a.batch, a.dim, a.seqlen, sms, CF::CC, CF::K);
     const int64_t lpad = relay_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
@@ -1820,8 +1326,13 @@ int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dst
 cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant) {
     if (dt != DType::BF16 || a.dstate != 16) return cudaErrorInvalidValue;
     if (variant == 3) return launch_ws(a, workspace, sms, s);
-    if (variant == 2) return launch_tmem2(a, workspace, sms, s);
-    return launch_tmem_t<16>(a, workspace, sms, s);
+    return launch_tmem2(a, workspace, sms, s);
+}
+
+int set_wait_test_tmem(int withhold, unsigned long long limit_ns) {
+    if (cudaMemcpyToSymbol(g_withhold_flag, &withhold, sizeof(withhold)) != cudaSuccess) return -1;
+    if (cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(limit_ns)) != cudaSuccess) return -1;
+    return 0;
 }
 
 int read_tmem_device_error(bool clear) {

@@ -58,6 +58,11 @@ ssm_status sm_count(int* out) {
     return SSM_OK;
 }
 
+// Kernel forced by ssm_force_scan_path (tests and benchmarks that compare the
+// kernels); the default, path 0, is the library's own choice.
+std::atomic<int> g_force_path{SSM_PATH_AUTO};
+std::atomic<int> g_force_layout{-1};
+
 // Pick a compiled scan layout.  Every channel walks the sequence in order,
 // so a CTA's work is CW channels x L steps and its warps share it.  The
 // score is the work of the busiest SM scheduler (warps are the unit a
@@ -66,11 +71,9 @@ ssm_status sm_count(int* out) {
 // few states per lane pay for the cross-lane y reduction.
 int plan_layout(int64_t batch, int64_t dim, int N, int sms) {
     const int count = ssm::scan_layout_count(N);
-    const char* env = std::getenv("SSM_SCAN_LAYOUT");
-    if (env) {
-        const int l = std::atoi(env);
-        if (l >= 0 && l < count) return l;
-    }
+    const int forced = g_force_layout.load(std::memory_order_relaxed);
+    if (g_force_path.load(std::memory_order_relaxed) == SSM_PATH_GENERIC && forced >= 0 && forced < count)
+        return forced;
     const double schedulers = 4.0 * sms;
     int best = 0;
     double best_t = 1e300;
@@ -124,7 +127,21 @@ const char* ssm_status_string(int status) {
     }
 }
 
-int ssm_version(void) { return 100; }
+int ssm_version(void) { return 101; }
+
+ssm_status ssm_debug_wait_test(int withhold_flag, int64_t wait_limit_ns) {
+    const unsigned long long ns = wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns : 1000000000ull;
+    const int w = withhold_flag ? 1 : 0;
+    if (ssm::set_wait_test_seg(w, ns) != 0 || ssm::set_wait_test_tmem(w, ns) != 0) return SSM_ERR_DEVICE;
+    return SSM_OK;
+}
+
+ssm_status ssm_force_scan_path(int path, int generic_layout) {
+    if (path < SSM_PATH_AUTO || path > SSM_PATH_GENERIC) return SSM_ERR_SHAPE;
+    g_force_layout.store(path == SSM_PATH_GENERIC ? generic_layout : -1, std::memory_order_relaxed);
+    g_force_path.store(path, std::memory_order_relaxed);
+    return SSM_OK;
+}
 
 const char* ssm_last_launch_error(void) {
     return t_last_launch == cudaSuccess ? "no launch error" : cudaGetErrorString(t_last_launch);
@@ -137,9 +154,7 @@ int64_t ssm_scan_workspace_bytes_grouped(int64_t batch, int64_t dim, int64_t seq
     if (batch <= 0 || seqlen <= 0 || !dstate_ok(dstate) || batch > 65535 || seqlen > (int64_t(1) << 40))
         return -1;
     if (ngroups <= 0 || dim % ngroups != 0 || too_many_elems(batch, seqlen, dim)) return -1;
-    int64_t need = std::max(ssm::relay_workspace_bytes(batch, seqlen, (int)dstate, ngroups),
-                            ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4,
-                                                     ngroups));
+    int64_t need = ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, dtype == SSM_BF16 ? 2 : 4, ngroups);
     if (dtype == SSM_BF16) need = std::max(need, ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate, ngroups));
     return need;
 }
@@ -233,36 +248,27 @@ ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A
     const ssm::DType dt = dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32;
     const cudaStream_t st = static_cast<cudaStream_t>(stream);
     // The tensor-memory scan (two states per lane) runs whenever its
-    // requirements hold (bf16, 16 states), else the segmented scan;
-    // SSM_SCAN_PATH=tmem2|tmem|seg|relay|generic forces one kernel (tests use it).
-    const char* force = std::getenv("SSM_SCAN_PATH");
+    // requirements hold (bf16, 16 states), else the segmented scan, else the
+    // generic kernel; ssm_force_scan_path picks one of them instead.
+    const int force = g_force_path.load(std::memory_order_relaxed);
     // (chains * 64 segments must stay a 32-bit task count)
     const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
                          batch * ((dim + 127) / 128 * dstate) * 64 < (int64_t(1) << 31);
-    if (force && std::strcmp(force, "relay") == 0) {
-        if (!fast_ok || workspace_bytes < ssm::relay_workspace_bytes(batch, seqlen, (int)dstate, ngroups))
-            return SSM_ERR_UNSUPPORTED;
-        return launch_status(ssm::launch_scan_relay(a, dt, workspace, st));
-    }
-    const bool want_generic = force && std::strcmp(force, "generic") == 0;
-    const bool want_seg = force && std::strcmp(force, "seg") == 0;
     const bool tmem_ok = fast_ok && ssm::tmem_supported(a, dt) &&
                          workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate, ngroups);
-    if (force && (std::strcmp(force, "tmem") == 0 || std::strcmp(force, "tmem2") == 0)) {
+    const bool seg_ok = fast_ok &&
+                        workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es, ngroups);
+    if (force == SSM_PATH_TMEM2 || force == SSM_PATH_WS) {
         if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
-        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, force[4] == '2' ? 2 : 4));
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, force == SSM_PATH_WS ? 3 : 2));
     }
-    if (force && std::strcmp(force, "ws") == 0) {
-        if (!tmem_ok) return SSM_ERR_UNSUPPORTED;
-        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 3));
-    }
-    if (!want_generic && !want_seg && tmem_ok)
-        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 2));
-    if (!want_generic && fast_ok &&
-        workspace_bytes >= ssm::seg_workspace_bytes(batch, dim, seqlen, (int)dstate, (int)es, ngroups)) {
+    if (force == SSM_PATH_SEG) {
+        if (!seg_ok) return SSM_ERR_UNSUPPORTED;
         return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
     }
-    if (want_seg) return SSM_ERR_UNSUPPORTED;
+    if (force == SSM_PATH_AUTO && tmem_ok)
+        return launch_status(ssm::launch_scan_tmem(a, dt, workspace, sms, st, 2));
+    if (force == SSM_PATH_AUTO && seg_ok) return launch_status(ssm::launch_scan_seg(a, dt, workspace, sms, st));
     ssm::ScanPlan plan{plan_layout(batch, dim, (int)dstate, sms)};
     return launch_status(ssm::launch_scan_fwd(a, dt, plan, st));
 }

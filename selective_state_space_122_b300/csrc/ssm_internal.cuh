@@ -66,12 +66,10 @@ struct ScanPlan {
     int layout;  // index into the compiled layouts for this d_state
 };
 
-// Fast path (scan_relay.cu): warp relay over TMA-staged chunks.  Needs a
-// float32 workspace for the staged B and C (relay_workspace_bytes).
+// TMA fast paths (scan_relay.cu): the staged-sequence padding (a multiple of
+// 64 steps) and whether a call's pointers and sizes suit the tensor maps.
 int64_t relay_lpad(int64_t seqlen);
-int64_t relay_workspace_bytes(int64_t batch, int64_t seqlen, int dstate, int64_t ngroups);
 bool relay_supported(const ScanArgs& a, DType dt);
-cudaError_t launch_scan_relay(const ScanArgs& a, DType dt, void* workspace, cudaStream_t s);
 // Segmented direct scan (scan_relay.cu): needs staged B/C plus the segment
 // hand-off state and flags (seg_workspace_bytes).
 int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes,
@@ -134,10 +132,15 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms
 // the staged one-hot MMA operands of B and C plus the segment hand-off state.
 bool tmem_supported(const ScanArgs& a, DType dt);
 int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int64_t ngroups);
-// variant 2: two states per lane (8 consumer warps); otherwise four.
+// variant 3: the warp-specialised kernel (four states per lane); otherwise
+// two states per lane (8 consumer warps).
 cudaError_t launch_scan_tmem(const ScanArgs& a, DType dt, void* workspace, int sms, cudaStream_t s, int variant);
 int read_tmem_device_error(bool clear);
 int read_device_error(bool clear);
+// The wait test hook (ssm_debug_wait_test) in the segmented and the
+// tensor-memory kernels' units: withhold flag and wait limit in ns; -1 on failure.
+int set_wait_test_seg(int withhold, unsigned long long limit_ns);
+int set_wait_test_tmem(int withhold, unsigned long long limit_ns);
 
 // Every host-side check of a scan call (ssm_api.cu): returns SSM_OK or the
 // ssm_status code the call would return, touching no device state.

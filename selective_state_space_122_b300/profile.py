@@ -1,7 +1,7 @@
 """Profiling drivers for the selective-scan library (run on a CUDA device).
 
     python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
-           [--N N] [--iters K] [--path tmem2|tmem|seg|relay|generic] [--ngroups G]
+           [--N N] [--iters K] [--path tmem2|ws|seg|generic] [--ngroups G]
     python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K] [--ngroups G]
     python -m selective_state_space_122_b300.profile conv [--batch B] [--dim D] [--L L] [--W W] [--iters K]
     python -m selective_state_space_122_b300.profile bwd [--batch B] [--dim D] [--L L] [--N N] [--iters K] [--ngroups G]
@@ -27,7 +27,7 @@ import sys
 import torch
 
 from . import build as libbuild
-from ._lib import device_error, scan_workspace_bytes, ssm_scan_fwd, ssm_state_update
+from ._lib import device_error, force_scan_path, scan_workspace_bytes, ssm_scan_fwd, ssm_state_update
 
 
 def _inputs(batch, dim, L, N, dev, seed=0, ngroups=1):
@@ -48,7 +48,7 @@ def _inputs(batch, dim, L, N, dev, seed=0, ngroups=1):
 
 def cmd_scan(a):
     if a.path:
-        os.environ["SSM_SCAN_PATH"] = a.path
+        force_scan_path(a.path)
     dev = torch.device("cuda", 0)
     u, dl, z, B, C, A, D, bias = _inputs(a.batch, a.dim, a.L, a.N, dev, ngroups=a.ngroups)
     out = torch.empty_like(u)
@@ -161,7 +161,7 @@ def main(argv=None):
     s.add_argument("--L", type=int, default=16384)
     s.add_argument("--N", type=int, default=16)
     s.add_argument("--iters", type=int, default=3)
-    s.add_argument("--path", default=None, choices=[None, "ws", "tmem2", "tmem", "relay", "seg", "generic"])
+    s.add_argument("--path", default=None, choices=[None, "tmem2", "ws", "seg", "generic"])
     s.add_argument("--ngroups", type=int, default=1)
     d = sub.add_parser("decode")
     d.add_argument("--batch", type=int, default=256)

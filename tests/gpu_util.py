@@ -14,7 +14,6 @@ Gaussians), where that rounding alone exceeds 2e-2 * rms(y).
 from __future__ import annotations
 
 import contextlib
-import os
 
 import numpy as np
 import torch
@@ -80,7 +79,7 @@ def check_state(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "last_
         assert rel <= STATE_REL, f"{what}: relative L2 error {rel:.3e} > 1e-3"
 
 
-# number of compiled generic-kernel layouts per d_state (selectable with SSM_SCAN_LAYOUT)
+# number of compiled generic-kernel layouts per d_state (selectable with ssm_force_scan_path)
 LAYOUTS = {16: 7, 8: 4, 4: 2}
 
 
@@ -96,33 +95,27 @@ def tmem_ok(N: int, dim: int, dtype: str) -> bool:
 
 
 def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
-    """Every way to run a scan of this shape: the tensor-memory, segmented and
-    relay paths (when they accept the shape) and each generic layout."""
-    fast = ["seg", "relay"] if relay_ok(dim, dtype) else []
+    """Every way to run a scan of this shape: the tensor-memory and segmented
+    paths (when they accept the shape) and each generic layout."""
+    fast = ["seg"] if relay_ok(dim, dtype) else []
     if tmem_ok(N, dim, dtype):
-        fast = ["ws", "tmem", "tmem2"] + fast
+        fast = ["tmem2", "ws"] + fast
     return fast + list(range(LAYOUTS[N]))
 
 
 @contextlib.contextmanager
 def scan_layout(layout):
-    """Force a path: None = the library's own choice, "tmem" / "tmem2" (four
-    or two states per lane) / "seg" / "relay" = that TMA kernel (an error if
-    it cannot take the shape), an int = that layout of the generic kernel."""
-    keys = ("SSM_SCAN_LAYOUT", "SSM_SCAN_PATH")
-    old = {k: os.environ.get(k) for k in keys}
-    for k in keys:
-        os.environ.pop(k, None)
-    if layout in ("relay", "seg", "tmem", "tmem2", "ws"):
-        os.environ["SSM_SCAN_PATH"] = layout
-    elif layout is not None:
-        os.environ["SSM_SCAN_PATH"] = "generic"
-        os.environ["SSM_SCAN_LAYOUT"] = str(layout)
+    """Force a path (ssm_force_scan_path): None = the library's own choice,
+    "tmem2" / "ws" / "seg" = that TMA kernel (an error if it cannot take the
+    shape), an int = that layout of the generic kernel."""
+    from selective_state_space_122_b300 import force_scan_path
+    if layout is None:
+        force_scan_path(None)
+    elif isinstance(layout, str):
+        force_scan_path(layout)
+    else:
+        force_scan_path("generic", layout)
     try:
         yield
     finally:
-        for k, v in old.items():
-            if v is None:
-                os.environ.pop(k, None)
-            else:
-                os.environ[k] = v
+        force_scan_path(None)

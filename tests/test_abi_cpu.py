@@ -190,6 +190,8 @@ def test_update_rejects_bad_arguments(lib, kw, code):
 def test_valid_call_without_device_reports_device_error(lib):
     assert call_scan(lib, scan_args()) == 8
     assert call_upd(lib, upd_args()) == 8
+    # the wait test hook writes device memory: without a device it reports so
+    assert lib.ssm_debug_wait_test(0, 0) == 8
 
 
 def test_binding_raises_without_cuda_tensors():
@@ -201,20 +203,18 @@ def test_binding_raises_without_cuda_tensors():
 
 
 def _ws_expected(batch, dim, seqlen, dstate, es, ngroups=1):
-    """The largest of the fast paths' needs, each part rounded up to 256 bytes:
-    B and C staged as float32 rows (sequence padded to 64 steps); B and C
-    staged in the activation type (es bytes) plus one float32 state per
-    (chain, channel, state) and one int flag per chain; and, for bf16 with 16
-    states, the tensor-memory path's one-hot operands (32 float32 per step)
-    plus its state and one flag per consumer warp (up to eight) of each
-    32-channel group.  Staged B/C (and operands) are per (batch row, B/C group)."""
+    """The larger of the fast paths' needs, each part rounded up to 256 bytes:
+    B and C staged in the activation type (es bytes, sequence padded to 64
+    steps) plus one float32 state per (chain, channel, state) and one int flag
+    per chain; and, for bf16 with 16 states, the tensor-memory paths' one-hot
+    operands (32 float32 per step) plus their state and one flag per consumer
+    warp (up to eight) of each 32-channel group.  Staged B/C (and operands)
+    are per (batch row, B/C group)."""
     up = lambda x: (x + 255) // 256 * 256
     lpad = (seqlen + 63) // 64 * 64
     cw = 32 // (dstate // 4)
     chains = batch * ((dim + cw - 1) // cw)
-    relay = batch * ngroups * lpad * 2 * dstate * 4
-    seg = up(batch * ngroups * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
-    need = max(relay, seg)
+    need = up(batch * ngroups * lpad * 2 * dstate * es) + up(chains * cw * dstate * 4) + up(chains * 4)
     if es == 2 and dstate == 16:
         groups = batch * ((dim + 31) // 32)
         need = max(need, up(batch * ngroups * lpad * 32 * 4) + up(groups * 32 * 16 * 4) + up(groups * 8 * 4))
@@ -380,3 +380,14 @@ def test_noalloc_checks_arguments_before_its_scratch(lib, kw, code):
     """Over-large sizes with a bad argument get the scan's own code for that
     argument, not SSM_ERR_SCRATCH: the argument checks come first."""
     assert _noalloc_call(lib, **kw) == code
+
+
+def test_force_scan_path_hook(lib):
+    """The kernel-selection hook: known paths are accepted (restoring the
+    default last), anything else is SSM_ERR_SHAPE; no device is touched."""
+    for path in (1, 2, 3, 4, 0):
+        assert lib.ssm_force_scan_path(path, -1) == 0
+    assert lib.ssm_force_scan_path(4, 2) == 0
+    assert lib.ssm_force_scan_path(5, -1) == 2
+    assert lib.ssm_force_scan_path(-1, -1) == 2
+    assert lib.ssm_force_scan_path(0, -1) == 0

@@ -24,9 +24,9 @@ def grouped_paths(N, dim, gch, dtype):
     whole blocks of 128 / N channels; the generic layouts take any size."""
     out = []
     for g in paths(N, dim, dtype):
-        if g in ("ws", "tmem", "tmem2") and gch % 32:
+        if g in ("ws", "tmem2") and gch % 32:
             continue
-        if g in ("seg", "relay") and gch % (128 // N):
+        if g == "seg" and gch % (128 // N):
             continue
         out.append(g)
     return out
@@ -73,7 +73,7 @@ def test_grouped_scan_every_path(bt, dim, L, N, dtype, G):
         check_state(host_f64(last), ref_last, dtype, f"grouped state, path {g}")
 
 
-@pytest.mark.parametrize("path", ["ws", "tmem2", "tmem", "seg", "relay"])
+@pytest.mark.parametrize("path", ["tmem2", "ws", "seg"])
 def test_fast_path_rejects_group_sizes_it_cannot_take(path):
     """Forcing a kernel onto groups that split its channel block is
     SSM_ERR_UNSUPPORTED, before anything is launched."""
@@ -84,7 +84,7 @@ def test_fast_path_rejects_group_sizes_it_cannot_take(path):
     assert e.value.code == 4
 
 
-@pytest.mark.parametrize("path", [None, "ws", "tmem2", "tmem", "seg"])
+@pytest.mark.parametrize("path", [None, "tmem2", "ws", "seg"])
 def test_grouped_long_multisegment(path):
     """Many segments per chain with 8 groups of 640 channels, checked on
     sampled channels of every group against the oracle of that group."""

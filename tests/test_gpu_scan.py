@@ -30,7 +30,7 @@ def layouts(N, dim=64, dtype=inputs.BF16):
 
 # ------------------------------------------------------------ the five workloads
 
-@pytest.mark.parametrize("g", [None, "seg", "relay"] + list(range(LAYOUTS[4])))
+@pytest.mark.parametrize("g", [None, "seg"] + list(range(LAYOUTS[4])))
 def test_tiny_f32_against_golden(g):
     inp = inputs.make_scan_inputs(inputs.TINY_F32, 0)
     with scan_layout(g):
@@ -47,7 +47,7 @@ def layer130m():
     return inp, oracle_of(inp)
 
 
-@pytest.mark.parametrize("g", [None, "ws", "tmem", "tmem2", "seg", "relay"] + list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("g", [None, "tmem2", "ws", "seg"] + list(range(LAYOUTS[16])))
 def test_layer130m_full(layer130m, g):
     inp, (ref, ref_last) = layer130m
     with scan_layout(g):
@@ -138,11 +138,11 @@ def test_ragged_shapes(bt, dim, L, N):
 @pytest.mark.parametrize("dtype", [inputs.F32, inputs.BF16])
 @pytest.mark.parametrize("bt,dim,L,N", [(1, 8, 1, 16), (2, 24, 77, 8), (3, 40, 65, 4), (1, 16, 7, 16),
                                          (2, 72, 200, 16), (1, 48, 9, 8), (2, 8, 1000, 16)])
-@pytest.mark.parametrize("path", ["ws", "tmem", "tmem2", "seg", "relay"])
+@pytest.mark.parametrize("path", ["tmem2", "ws", "seg"])
 def test_tma_paths_ragged(bt, dim, L, N, dtype, path):
     """The TMA paths on sequence ends that are not whole chunks, units whose
     last channels fall beyond dim, and sequences shorter than one chunk."""
-    if path in ("ws", "tmem", "tmem2") and not tmem_ok(N, dim, dtype):
+    if path in ("ws", "tmem2") and not tmem_ok(N, dim, dtype):
         pytest.skip("the tensor-memory path takes bf16 with 16 states only")
     inp = inputs.make_scan_inputs(inputs.ScanShape("tma-ragged", bt, dim, L, N, dtype), 7 * dim + L)
     ref, ref_last = oracle_of(inp)
@@ -152,7 +152,7 @@ def test_tma_paths_ragged(bt, dim, L, N, dtype, path):
     check_state(host_f64(last), ref_last, dtype)
 
 
-@pytest.mark.parametrize("path", ["ws", "tmem", "tmem2"])
+@pytest.mark.parametrize("path", ["tmem2", "ws"])
 @pytest.mark.parametrize("bt,dim,L", [(1, 5120, 4096), (1, 5120, 20000), (5, 1024, 777), (2, 4800, 3000)])
 def test_tmem_multisegment_schedule(bt, dim, L, path):
     """The tensor-memory path with more 32-channel groups than SMs: each group's
@@ -185,10 +185,10 @@ def test_seg_multisegment_schedule(bt, dim, L, N):
     check_state(host_f64(last[:, idx]), ref_last, inputs.BF16)
 
 
-@pytest.mark.parametrize("g", ["ws", "tmem", "tmem2", "seg", "relay"] + list(range(LAYOUTS[16])))
+@pytest.mark.parametrize("g", ["tmem2", "ws", "seg"] + list(range(LAYOUTS[16])))
 def test_writes_stay_in_bounds(g):
     """Outputs and the final state sit between guard words that must survive."""
-    dim = 48 if g in ("ws", "tmem", "tmem2", "seg", "relay") else 45     # the TMA paths need 16-byte rows
+    dim = 48 if g in ("ws", "tmem2", "seg") else 45     # the TMA paths need 16-byte rows
     shape = inputs.ScanShape("guard", 2, dim, 70, 16, inputs.BF16)
     inp = inputs.make_scan_inputs(shape, 30)
     n_out = 2 * 70 * dim
@@ -268,7 +268,7 @@ def test_small_delta_channels_long_sequence():
     assert worst_out <= 2e-2, f"per-channel output error above 2e-2 rms: {msg}"
 
 
-@pytest.mark.parametrize("g", [None, "ws", "tmem", "tmem2", "seg", "relay"])
+@pytest.mark.parametrize("g", [None, "tmem2", "ws", "seg"])
 def test_zero_timestep_limit_bf16_fast_paths(g):
     """Delta -> 0 on bf16 inputs (bias -1e4 under softplus), through the fast
     paths' own softplus: out = D u silu(z) to the bf16 bar, the state stays at
