@@ -37,11 +37,19 @@ from selective_state_space_122_b300 import inputs  # noqa: E402
 METRIC = "selective-scan elements (B·D·L·N)/s and achieved HBM GB/s vs roofline, 1 B300"
 SCAN = inputs.LONG_SEQ
 DECODE = inputs.DECODE_256
-# Transcendental work of the method per (b, t, d): N exp2 for exp(Delta A),
-# softplus = exp2 + log2, silu = exp2 + reciprocal.  The rates of ex2, lg2 and
-# rcp are measured on the GPU by libssmpeak.so before the timed region.
-def sfu_ops_per_td(n):
-    return {"ex2": n + 2, "lg2": 1, "rcp": 1}
+# Special-function work of the method per (b, t, d), in exp2-equivalents: N
+# exp2 for exp(Delta A), plus 4 for softplus (exp2 + log) and silu (exp2 +
+# reciprocal) -- the (N + 4) unit the roofline is quoted in, against the
+# exp2 rate measured on the GPU by libssmpeak.so before the timed region.
+def sfu_units_per_td(n):
+    return n + 4
+
+
+# What the benchmarked kernel actually issues per (b, t, d): N + 1 exp2
+# (decays and softplus, whose log1p is a polynomial on the FMA pipe) and one
+# tanh (silu(z) = (z/2)(1 + tanh(z/2))).
+def sfu_issued_per_td(n):
+    return {"ex2": n + 1, "tanh": 1}
 
 
 FALLBACK_PEAKS = {"hbm_gbs": 6400.0, "sm_max_mhz": 2032.0, "source": "fallback"}
@@ -53,9 +61,12 @@ def scan_elements(s=SCAN):
     return s.batch * s.dim * s.seqlen * s.dstate
 
 
-# Measured DRAM bytes of one full-size launch of the scan kernel (see the
-# "traffic" entry of the roofline object).
-SCAN_TRAFFIC_BYTES = 654.86e6 * 8
+# dram__bytes_read.sum + dram__bytes_write.sum of scan_tmem2_kernel as built
+# (polynomial softplus), from one ncu capture of the long-sequence workload cut
+# to L = 16384 (profiles/scan_tmem2_kernel_1x5120x16384.md), scaled by
+# 131072 / 16384: the traffic grows in proportion to L.
+SCAN_TRAFFIC_L16384 = 654.2e6
+SCAN_TRAFFIC_BYTES = SCAN_TRAFFIC_L16384 * 8
 
 
 def scan_bytes(s=SCAN, es=2):
@@ -66,15 +77,15 @@ def scan_bytes(s=SCAN, es=2):
             + s.dim * s.dstate * 4 + 2 * s.dim * 4 + s.batch * s.dim * s.dstate * 4)
 
 
-def scan_sfu_seconds(rates, s=SCAN):
-    """Time the special-function unit alone needs for one scan at the measured rates."""
+def scan_sfu_units(s=SCAN):
+    """SFU work of one scan in the roofline's unit: (N + 4) exp2-equivalents per (b, t, d)."""
+    return s.batch * s.seqlen * s.dim * sfu_units_per_td(s.dstate)
+
+
+def scan_sfu_issued_seconds(rates, s=SCAN):
+    """Time the SFU needs for the instructions the kernel issues, at the measured rates."""
     btd = s.batch * s.seqlen * s.dim
-    return sum(btd * k / rates[op] for op, k in sfu_ops_per_td(s.dstate).items())
-
-
-def scan_sfu_ex2_equiv(rates, s=SCAN):
-    """SFU work of one scan in ex2-equivalents: lg2 and rcp weighted by ex2_rate / their rate."""
-    return scan_sfu_seconds(rates, s) * rates["ex2"]
+    return sum(btd * k / rates[op] for op, k in sfu_issued_per_td(s.dstate).items())
 
 
 def decode_elements(s=DECODE):
@@ -100,7 +111,8 @@ def probe_units(device_index=0):
     lib.ssmpk_probe.restype = ctypes.c_double
     lib.ssmpk_sm_count.restype = ctypes.c_int
     out = {}
-    for name, kind, iters in (("ex2", 0, 20000), ("lg2", 1, 10000), ("rcp", 2, 10000), ("ffma", 3, 40000)):
+    for name, kind, iters in (("ex2", 0, 20000), ("lg2", 1, 10000), ("rcp", 2, 10000), ("ffma", 3, 40000),
+                              ("tanh", 4, 10000)):
         best = max(lib.ssmpk_probe(kind, iters, 4) for _ in range(3))
         out[name] = best
     out["sms"] = lib.ssmpk_sm_count()
@@ -379,6 +391,61 @@ def run_e2e(w, steps, device, pieces=16):
     return ms, h2d, d2h, same
 
 
+def time_side_kernels(w, device, iters=5):
+    """CUDA-event times, outside the timed step, of:
+    * the backward of the scan at the mid-size prefill shape (8 x 2048 x 2048,
+      N 16, bf16; every input's gradient);
+    * the causal conv1d + SiLU over the long-sequence activations (1 x 131072
+      x 5120, width 4, bf16);
+    * the decode step alone, each launch after a read of 512 MB that leaves
+      the L2 clean (in the step it runs after the scan, whose output lines are
+      still dirty in L2 and are written back during the decode).
+    Inputs: seeded, on the device."""
+    import torch
+    from selective_state_space_122_b300 import conv1d_fwd, ssm_scan_bwd, ssm_state_update
+    res = {}
+    ev = lambda: torch.cuda.Event(enable_timing=True)
+
+    def timed(fn, before=None):
+        ts = []
+        for i in range(iters + 2):
+            if before is not None:
+                before()
+            e0, e1 = ev(), ev()
+            e0.record()
+            fn()
+            e1.record()
+            torch.cuda.synchronize()
+            if i >= 2:
+                ts.append(e0.elapsed_time(e1))
+        return statistics.median(ts)
+
+    g = torch.Generator(device=device)
+    g.manual_seed(5)
+    bt, dim, L, N = 8, 2048, 2048, 16
+    u, dl, z, dout = (torch.randn(bt, L, dim, device=device, generator=g).bfloat16() for _ in range(4))
+    B, C = (torch.randn(bt, N, L, device=device, generator=g).bfloat16() for _ in range(2))
+    A = -torch.arange(1, N + 1, device=device, dtype=torch.float32).repeat(dim, 1).contiguous()
+    D = torch.ones(dim, device=device)
+    dt = torch.exp(torch.empty(dim, device=device).uniform_(np.log(1e-3), np.log(0.1), generator=g))
+    bias = dt + torch.log(-torch.expm1(-dt))
+    res["bwd_ms"] = timed(lambda: ssm_scan_bwd(u, dl, A, B, C, D, z, bias, True, dout))
+    del u, dl, z, dout, B, C
+    s = w["scan"]
+    wt = torch.randn(SCAN.dim, 4, device=device, generator=g) * 0.5
+    cb = torch.randn(SCAN.dim, device=device, generator=g) * 0.1
+    res["conv_ms"] = timed(lambda: conv1d_fwd(s["u"], wt, cb, True, out=w["scan_out"]))
+    flush = torch.empty(512 << 20, dtype=torch.uint8, device=device)
+    flush.zero_()
+    d = w["dec"]
+    res["decode_isolated_us"] = 1e3 * timed(
+        lambda: ssm_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"],
+                                 d["dt_bias"], True, out=w["dec_out"]),
+        before=lambda: flush.view(torch.int64).sum())
+    torch.cuda.synchronize()
+    return res
+
+
 def cpu_baseline_sample(si, target_s=12.0, max_channels=None):
     """Time the float64 oracle (as it stands) on a bounded channel sample of the
     long-sequence scan ``si``, all host cores.  Returns a dict for the JSON line."""
@@ -439,6 +506,8 @@ def bench_ours(args):
     total_ms = max_over_ranks(total_ms, world, device)
     clocks = clk.summary()
 
+    side = time_side_kernels(w, device)
+
     e2e = None
     if not args.no_e2e:
         e2e_ms, h2d, d2h, same = run_e2e(w, args.e2e_steps, device)
@@ -459,12 +528,14 @@ def bench_ours(args):
     elems = (scan_elements() + decode_elements()) * world
     scan_avg = statistics.mean(scan_ms)
     dec_avg = statistics.mean(dec_ms)
-    t_sfu = scan_sfu_seconds(units)
+    sfu_units = scan_sfu_units()
+    t_sfu = sfu_units / units["ex2"]
     t_hbm = scan_bytes() / (peaks["hbm_gbs"] * 1e9)
-    sfu_equiv = scan_sfu_ex2_equiv(units)
-    sfu_ach = sfu_equiv / (scan_avg * 1e-3)
+    sfu_ach = sfu_units / (scan_avg * 1e-3)
     hbm_ach = scan_bytes() / (scan_avg * 1e-3) / 1e9
     t_roof_ms = max(t_hbm, t_sfu) * 1e3
+    t_issued = scan_sfu_issued_seconds(units)
+    dec_iso = side["decode_isolated_us"]
     line = {
         "metric": METRIC,
         "value": elems / (ms_step * 1e-3),
@@ -488,26 +559,27 @@ def bench_ours(args):
         },
         "scan_ms": scan_avg,
         "decode_us": dec_avg * 1e3,
+        "bwd_ms": side["bwd_ms"],
+        "conv_ms": side["conv_ms"],
         "roofline": {
             "bound": "alu",
             "unit": "G ex2-equiv/s",
             "achieved": sfu_ach / 1e9,
             "peak": units["ex2"] / 1e9,
             "frac": sfu_ach / units["ex2"],
-            # dram__bytes_read.sum + dram__bytes_write.sum of scan_tmem2_kernel from one
-            # ncu capture of the same workload cut to L = 16384 (654.86 MB), scaled by
-            # 131072 / 16384 (traffic grows in proportion to L)
             "traffic": SCAN_TRAFFIC_BYTES,
-            "traffic_source": "ncu, scan_tmem2_kernel at L=16384 x 8",
+            "traffic_source": "ncu dram bytes of scan_tmem2_kernel (as built) at L=16384, x 8",
             "kernel": "ssm_scan_fwd: tm2_stage_kernel + scan_tmem2_kernel (long-sequence scan)",
-            "peak_source": ("measured on this GPU by libssmpeak.so: ex2 %.1f, lg2 %.1f, rcp %.1f G/s, "
-                            "packed FMA %.1f TFLOP/s; SFU work per (b,t,d): N+2 ex2, 1 lg2, 1 rcp, "
-                            "lg2/rcp weighted by ex2_rate/their rate"
-                            % (units["ex2"] / 1e9, units["lg2"] / 1e9, units["rcp"] / 1e9,
+            "work_unit": "(N + 4) exp2-equivalents per (b, t, d): N decays, softplus, silu",
+            "peak_source": ("measured on this GPU by libssmpeak.so: ex2 %.1f, lg2 %.1f, rcp %.1f, tanh %.1f G/s, "
+                            "packed FMA %.1f TFLOP/s"
+                            % (units["ex2"] / 1e9, units["lg2"] / 1e9, units["rcp"] / 1e9, units["tanh"] / 1e9,
                                2 * units["ffma"] / 1e12)),
-            "sfu_ex2_equiv_per_launch": sfu_equiv,
+            "sfu_units_per_launch": sfu_units,
+            "issued_sfu_per_td": sfu_issued_per_td(SCAN.dstate),
+            "frac_issued": t_issued / (scan_avg * 1e-3),
             "sfu_per_sm_per_clk": {k: units[k] / (sms * clocks_mhz_for_units * 1e6)
-                                   for k in ("ex2", "lg2", "rcp", "ffma")},
+                                   for k in ("ex2", "lg2", "rcp", "tanh", "ffma")},
             "hbm": {"achieved_gbs": hbm_ach, "peak_gbs": peaks["hbm_gbs"],
                     "frac": hbm_ach / peaks["hbm_gbs"], "bytes_per_launch": scan_bytes(),
                     "peak_source": peaks["source"]},
@@ -520,7 +592,16 @@ def bench_ours(args):
             "us_per_step": dec_avg * 1e3,
             "bytes_per_step": decode_bytes(),
             "achieved_gbs": decode_bytes() / (dec_avg * 1e-3) / 1e9,
-            "frac_hbm": decode_bytes() / (dec_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "frac_hbm_in_step": decode_bytes() / (dec_avg * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "isolated_us": dec_iso,
+            "frac_hbm": decode_bytes() / (dec_iso * 1e-6) / 1e9 / peaks["hbm_gbs"],
+            "note": ("frac_hbm: the step alone after a clean L2; in the step it follows the scan, whose "
+                     "dirty output lines in L2 are written back during it"),
+        },
+        "side_kernels": {
+            "bwd": {"workload": "backward 8x2048x2048 d_state 16 bf16 (every gradient)", "ms": side["bwd_ms"]},
+            "conv1d": {"workload": "causal conv1d + SiLU 1x131072x5120 width 4 bf16", "ms": side["conv_ms"],
+                       "achieved_gbs": 2 * SCAN.batch * SCAN.seqlen * SCAN.dim * 2 / (side["conv_ms"] * 1e-3) / 1e9},
         },
         "clocks": clocks,
         "gpu_launches": 3 * args.steps,

@@ -1,5 +1,5 @@
 // sfu_peak.cu -- throughput probes for the arithmetic units the selective
-// scan leans on: the special-function unit (ex2, lg2, rcp) and the float32
+// scan leans on: the special-function unit (ex2, lg2, rcp, tanh) and the float32
 // pipe (packed f32x2 FMA).  Built into its own library (libssmpeak.so),
 // separate from the scan library; the benchmark uses it to measure the
 // denominators of the scan's arithmetic roofline on the GPU it runs on.
@@ -40,10 +40,15 @@ __device__ __forceinline__ float rcpa(float x) {
     asm volatile("rcp.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
     return y;
 }
+__device__ __forceinline__ float tanha(float x) {
+    float y;
+    asm volatile("tanh.approx.f32 %0, %1;" : "=f"(y) : "f"(x));
+    return y;
+}
 
-// kind 0: ex2, 1: lg2, 2: rcp.  x_{i+1} = f(x_i) - c keeps x in (-1, 0]
-// for ex2 (2^x in (0.5, 1]), in [1, 2) for lg2 (log2 in [0, 1), + 1) and
-// in [1, 2] for rcp (1/x in [0.5, 1], + 1).
+// kind 0: ex2, 1: lg2, 2: rcp, 4: tanh.  x_{i+1} = f(x_i) - c keeps x in
+// (-1, 0] for ex2 (2^x in (0.5, 1]), in [1, 2) for lg2 (log2 in [0, 1), + 1),
+// in [1, 2] for rcp (1/x in [0.5, 1], + 1) and in (-0.75, 1.25) for tanh.
 template <int kKind>
 __global__ void __launch_bounds__(256) sfu_kernel(float* sink, int iters, float seed) {
     float v[kU];
@@ -54,6 +59,7 @@ __global__ void __launch_bounds__(256) sfu_kernel(float* sink, int iters, float 
         for (int i = 0; i < kU; ++i) {
             if constexpr (kKind == 0) v[i] = ex2a(v[i]) - 1.0f;
             else if constexpr (kKind == 1) v[i] = lg2a(v[i]) + 1.0f;
+            else if constexpr (kKind == 4) v[i] = tanha(v[i]) + 0.25f;
             else v[i] = rcpa(v[i]) + 1.0f;
         }
     }
@@ -97,7 +103,8 @@ __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, floa
 PK_API double ssmpk_probe_shape(int kind, int iters, int blocks_per_sm, int threads);
 
 // Runs one probe and returns its throughput in operations per second
-// (ex2 / lg2 / rcp results, or scalar FMAs for kind 3), timed with CUDA
+// (ex2 / lg2 / rcp / tanh results for kinds 0, 1, 2, 4, or scalar FMAs for
+// kind 3), timed with CUDA
 // events around a single launch of `blocks_per_sm` x SM-count blocks of 256
 // threads.  Returns a negative value on any CUDA error.  Synchronises the
 // device; a measurement tool, not part of the scan path.
@@ -105,7 +112,7 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1.0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1.0;
-    if (kind < 0 || kind > 3 || iters <= 0 || blocks_per_sm <= 0 || blocks_per_sm > 8) return -2.0;
+    if (kind < 0 || kind > 4 || iters <= 0 || blocks_per_sm <= 0 || blocks_per_sm > 8) return -2.0;
     float* sink = nullptr;
     if (cudaMalloc(&sink, 256 * sizeof(float)) != cudaSuccess) return -1.0;
     cudaEvent_t e0, e1;
@@ -117,6 +124,7 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
             case 0: sfu_kernel<0><<<grid, block>>>(sink, iters, 1e-7f); break;
             case 1: sfu_kernel<1><<<grid, block>>>(sink, iters, 1e-7f); break;
             case 2: sfu_kernel<2><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 4: sfu_kernel<4><<<grid, block>>>(sink, iters, 1e-7f); break;
             default: ffma2_kernel<<<grid, block>>>(sink, iters, 1e-7f); break;
         }
     };

@@ -21,10 +21,11 @@ def test_accounting_matches_the_workload():
     btd = 5120 * 131072
     # u, delta, z in + out, bf16; B, C; A, D, bias; final state
     assert bench.scan_bytes() == 8 * btd + 4 * 16 * 131072 + 5120 * 16 * 4 + 2 * 5120 * 4 + 5120 * 16 * 4
-    # SFU work: N + 2 ex2, one lg2, one rcp per (b, t, d), at per-op rates
-    rates = {"ex2": 2.0, "lg2": 1.0, "rcp": 0.5}
-    assert bench.scan_sfu_seconds(rates) == pytest.approx(btd * (18 / 2.0 + 1 / 1.0 + 1 / 0.5))
-    assert bench.scan_sfu_ex2_equiv(rates) == pytest.approx(btd * (18 + 2 + 4))
+    # SFU work in the roofline's unit: N + 4 exp2-equivalents per (b, t, d)
+    assert bench.scan_sfu_units() == btd * 20
+    # what the kernel issues: N + 1 exp2 and one tanh per (b, t, d), at per-op rates
+    rates = {"ex2": 2.0, "tanh": 0.5}
+    assert bench.scan_sfu_issued_seconds(rates) == pytest.approx(btd * (17 / 2.0 + 1 / 0.5))
     assert bench.decode_bytes() == (2 * 256 * 5120 * 16 * 4 + 4 * 256 * 5120 * 2 + 2 * 256 * 16 * 2
                                     + 5120 * 16 * 4 + 2 * 5120 * 4)
 
