@@ -65,7 +65,7 @@ def scan_elements(s=SCAN):
 # (polynomial softplus), from one ncu capture of the long-sequence workload cut
 # to L = 16384 (profiles/scan_tmem2_kernel_1x5120x16384.md), scaled by
 # 131072 / 16384: the traffic grows in proportion to L.
-SCAN_TRAFFIC_L16384 = 654.2e6
+SCAN_TRAFFIC_L16384 = 654.1e6
 SCAN_TRAFFIC_BYTES = SCAN_TRAFFIC_L16384 * 8
 
 

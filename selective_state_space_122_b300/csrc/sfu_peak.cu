@@ -69,6 +69,43 @@ __global__ void __launch_bounds__(256) sfu_kernel(float* sink, int iters, float 
     if (s == 12345.678f) sink[threadIdx.x & 255] = s;  // never true; keeps the chains live
 }
 
+// Co-issue of the SFU and the float32 pipe: each step is one ex2 (kind 5) or
+// one ex2 followed by K independent packed FMAs (kinds 6, 7: K = 1, 2), the
+// mix of a recurrence step.  The result is counted in ex2 per second: on a
+// GPU whose SFU and FMA pipes overlap perfectly, kinds 6 and 7 run at the
+// ex2 rate as long as the packed FMAs (two FMA-pipe cycles each) fit in the
+// SFU's cycles.
+template <int K>
+__global__ void __launch_bounds__(256) mix_kernel(float* sink, int iters, float seed) {
+    float v[kU];
+    unsigned long long p[kU][2];
+    const float2 q = make_float2(0.9999f, seed);
+    unsigned long long qq;
+    asm("mov.b64 %0, {%1, %2};" : "=l"(qq) : "f"(q.x), "f"(q.y));
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+        v[i] = -0.25f + seed * (threadIdx.x + i);
+        p[i][0] = p[i][1] = qq;
+    }
+    for (int it = 0; it < iters; ++it) {
+#pragma unroll
+        for (int i = 0; i < kU; ++i) {
+            v[i] = ex2a(v[i]) - 1.0f;
+#pragma unroll
+            for (int k = 0; k < K; ++k)
+                asm volatile("fma.rn.f32x2 %0, %0, %1, %1;" : "+l"(p[i][k]) : "l"(qq));
+        }
+    }
+    float s = 0.f;
+#pragma unroll
+    for (int i = 0; i < kU; ++i) {
+        float2 a;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(a.x), "=f"(a.y) : "l"(p[i][0] ^ p[i][1]));
+        s += v[i] + a.x;
+    }
+    if (s == 12345.678f) sink[threadIdx.x & 255] = s;
+}
+
 // Packed float32 FMA throughput: each step is one fma.rn.f32x2 (two FMAs).
 __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, float seed) {
     unsigned long long v[kU];
@@ -103,8 +140,8 @@ __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, floa
 PK_API double ssmpk_probe_shape(int kind, int iters, int blocks_per_sm, int threads);
 
 // Runs one probe and returns its throughput in operations per second
-// (ex2 / lg2 / rcp / tanh results for kinds 0, 1, 2, 4, or scalar FMAs for
-// kind 3), timed with CUDA
+// (ex2 / lg2 / rcp / tanh results for kinds 0, 1, 2, 4, scalar FMAs for
+// kind 3, ex2 results of the mixed steps for kinds 5, 6, 7), timed with CUDA
 // events around a single launch of `blocks_per_sm` x SM-count blocks of 256
 // threads.  Returns a negative value on any CUDA error.  Synchronises the
 // device; a measurement tool, not part of the scan path.
@@ -112,7 +149,7 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
     int dev = 0, sms = 0;
     if (cudaGetDevice(&dev) != cudaSuccess) return -1.0;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1.0;
-    if (kind < 0 || kind > 4 || iters <= 0 || blocks_per_sm <= 0 || blocks_per_sm > 8) return -2.0;
+    if (kind < 0 || kind > 7 || iters <= 0 || blocks_per_sm <= 0 || blocks_per_sm > 8) return -2.0;
     float* sink = nullptr;
     if (cudaMalloc(&sink, 256 * sizeof(float)) != cudaSuccess) return -1.0;
     cudaEvent_t e0, e1;
@@ -125,6 +162,9 @@ PK_API double ssmpk_probe(int kind, int iters, int blocks_per_sm) {
             case 1: sfu_kernel<1><<<grid, block>>>(sink, iters, 1e-7f); break;
             case 2: sfu_kernel<2><<<grid, block>>>(sink, iters, 1e-7f); break;
             case 4: sfu_kernel<4><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 5: mix_kernel<0><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 6: mix_kernel<1><<<grid, block>>>(sink, iters, 1e-7f); break;
+            case 7: mix_kernel<2><<<grid, block>>>(sink, iters, 1e-7f); break;
             default: ffma2_kernel<<<grid, block>>>(sink, iters, 1e-7f); break;
         }
     };

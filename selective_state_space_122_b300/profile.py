@@ -13,8 +13,10 @@ delta_bias = softplus^-1(dt), dt log-uniform in [1e-3, 0.1]) and prints the
 CUDA-event time of each call: the command behind the ncu captures of the scan
 kernels.  ``decode`` does the same for one ssm_state_update step.  --ngroups
 draws B and C per channel group (the grouped entry points).  ``units``
-prints the measured SFU (ex2) and packed-FMA throughput at 1, 2 and 8 warps
-per scheduler (libssmpeak.so).
+prints the measured SFU (ex2, tanh) and packed-FMA throughput at 1, 2 and 8
+warps per scheduler, and the ex2 rate when each ex2 is followed by 0, 1 or 2
+independent packed FMAs -- the SFU / FMA-pipe mix of a recurrence step
+(libssmpeak.so).
 """
 from __future__ import annotations
 
@@ -143,12 +145,20 @@ def cmd_units(a):
     lib.ssmpk_probe_shape.restype = ctypes.c_double
     lib.ssmpk_sm_count.restype = ctypes.c_int
     sms = lib.ssmpk_sm_count()
-    for name, kind, iters in (("ex2", 0, 20000), ("packed FMA", 3, 40000)):
+    for name, kind, iters in (("ex2", 0, 20000), ("packed FMA", 3, 40000), ("tanh", 4, 10000)):
         for bps, thr in ((1, 128), (2, 128), (4, 256)):
             r = max(lib.ssmpk_probe_shape(kind, iters, bps, thr) for _ in range(3))
             wps = bps * thr // 32 / 4
             print(f"{name:10s} {wps:3.0f} warp(s)/scheduler: {r / 1e9:9.1f} G/s "
                   f"= {r / (sms * a.clock_mhz * 1e6):6.2f} per clock per SM (at {a.clock_mhz:.0f} MHz)")
+    # co-issue: ex2 alone, then each ex2 followed by 1 or 2 independent packed FMAs
+    for name, kind in (("ex2 + 0 FFMA2", 5), ("ex2 + 1 FFMA2", 6), ("ex2 + 2 FFMA2", 7)):
+        for bps, thr in ((1, 128), (4, 256)):
+            r = max(lib.ssmpk_probe_shape(kind, 20000, bps, thr) for _ in range(3))
+            wps = bps * thr // 32 / 4
+            per = r / (sms * a.clock_mhz * 1e6)
+            print(f"{name:14s} {wps:3.0f} warp(s)/scheduler: {per:6.2f} ex2 per clock per SM "
+                  f"({128.0 / per:5.2f} cycles per warp-wide ex2 on a scheduler)")
     return 0
 
 
