@@ -270,7 +270,9 @@ SSM_API ssm_status ssm_state_update_grouped(float* state, const void* x, const v
  *   dD           [dim]                    f32     NULL = not computed (ignored without D)
  *   ddelta_bias  [dim]                    f32     NULL = not computed (ignored without a bias)
  *   workspace    at least ssm_scan_bwd_workspace_bytes(...) bytes, 16-byte
- *                aligned, owned by the caller: the state entering every chunk
+ *                aligned, owned by the caller: the states entering every
+ *                8-step chunk and the per-segment aggregates that carry the
+ *                state forward and the adjoint backward across segments
  *
  * All gradients are overwritten (the float32 ones are zeroed on `stream` and
  * accumulated with atomics, so their summation order, and the last bits, may
@@ -328,9 +330,14 @@ SSM_API ssm_status ssm_scan_bwd_from_state(const void* u, const void* delta, con
                                            int64_t workspace_bytes, void* stream);
 
 /*
- * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs:
- * batch * dim * ceil(seqlen / 8) * dstate * 4 bytes (the state entering
- * every 8-step chunk), at least 16; -1 for sizes or a dtype it would reject.
+ * ssm_scan_bwd_workspace_bytes -- workspace ssm_scan_bwd needs.  The
+ * sequence is cut into nch = ceil(seqlen / 8) chunks and those into
+ * S = min(64, max(1, ceil(nch / 32))) segments; with r(x) = x rounded up to a
+ * multiple of 256, the size is
+ *     r(batch * nch * dim * dstate * 4)   the local state entering every chunk
+ *   + r(batch * nch * dim * 4)            the sum of Delta before every chunk
+ *   + 3 * r(batch * S * dim * dstate * 4) per segment: decay product, state, adjoint
+ * bytes, at least 16; -1 for sizes or a dtype it would reject.
  */
 SSM_API int64_t ssm_scan_bwd_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int64_t dstate,
                                              int dtype);

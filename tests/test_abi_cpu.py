@@ -159,7 +159,10 @@ def test_scan_bwd_rejects_bad_arguments(lib, kw, code):
     assert lib.ssm_scan_bwd(a["u"], a["delta"], a["A"], a["B"], a["C"], a["D"], a["z"], a["bias"], 1, a["dout"],
                             a["du"], a["dd"], a["dA"], a["dB"], a["dC"], a["dD"], a["dz"], a["db"], a["batch"],
                             a["dim"], a["seqlen"], a["dstate"], a["dtype"], a["ws"], a["ws_bytes"], None) == code
-    assert lib.ssm_scan_bwd_workspace_bytes(2, 64, 128, 16, 1) == 2 * 64 * 16 * 16 * 4
+    for args in ((2, 64, 128, 16), (1, 37, 1100, 16), (8, 2048, 2048, 16), (1, 5120, 131072, 16),
+                 (3, 48, 1, 4)):
+        assert lib.ssm_scan_bwd_workspace_bytes(*args, 1) == _bwd_ws_expected(*args), args
+        assert lib.ssm_scan_bwd_workspace_bytes(*args, 0) == _bwd_ws_expected(*args), args
 
 
 def upd_args(**kw):
@@ -200,6 +203,16 @@ def test_binding_raises_without_cuda_tensors():
     B = torch.zeros(1, 4, 8)
     with pytest.raises(ValueError):
         _lib.ssm_scan_fwd(u, u, A, B, B)
+
+
+def _bwd_ws_expected(batch, dim, L, N):
+    """The backward's workspace as ssm_scan.h documents it: per-chunk local
+    states and Delta sums, three per-segment aggregates, each rounded up to
+    256 bytes."""
+    r = lambda x: (x + 255) // 256 * 256
+    nch = (L + 7) // 8
+    S = min(64, max(1, (nch + 31) // 32))
+    return max(16, r(batch * nch * dim * N * 4) + r(batch * nch * dim * 4) + 3 * r(batch * S * dim * N * 4))
 
 
 def _ws_expected(batch, dim, seqlen, dstate, es, ngroups=1):

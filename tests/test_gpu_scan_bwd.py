@@ -34,6 +34,14 @@ def _close(got, ref, rel, what, rounded=False):
     (3, 48, 129, 8, inputs.BF16, dict(random_a=True)),
     (1, 16, 1, 16, inputs.F32, {}),
     (2, 256, 2048, 16, inputs.BF16, {}),
+    # several segments per chain (the aggregates carry the state and the
+    # adjoint across them), ragged last segment and chunk, ragged channels
+    (2, 64, 1000, 16, inputs.BF16, {}),
+    (1, 96, 777, 8, inputs.F32, {}),
+    (2, 130, 600, 4, inputs.BF16, dict(random_a=True)),
+    # odd channel count: element-wise staging and stores
+    (1, 37, 1100, 16, inputs.BF16, {}),
+    (1, 45, 530, 16, inputs.F32, dict(with_z=False)),
 ])
 def test_scan_bwd_matches_adjoint_oracle(bt, dim, L, N, dtype, kw):
     inp = inputs.make_scan_inputs(inputs.ScanShape("bwd", bt, dim, L, N, dtype), 1200 + dim + L, **kw)
@@ -81,27 +89,43 @@ def test_scan_bwd_prefill_shape():
         _close(host_f64(g[k]), ref[k], 1e-4, k)
 
 
-@pytest.mark.parametrize("bt,dim,L,N,dtype,G", [
-    (2, 64, 300, 16, inputs.BF16, 1),
-    (1, 40, 100, 8, inputs.F32, 2),
-    (2, 96, 129, 4, inputs.F32, 1),
-    (2, 128, 77, 16, inputs.BF16, 4),
+@pytest.mark.parametrize("bt,dim,L,N,dtype,G,given", [
+    (2, 64, 300, 16, inputs.BF16, 1, "both"),
+    (1, 40, 100, 8, inputs.F32, 2, "both"),
+    (2, 96, 129, 4, inputs.F32, 1, "both"),
+    (2, 128, 77, 16, inputs.BF16, 4, "both"),
+    # several segments per chain
+    (2, 64, 1001, 16, inputs.BF16, 2, "both"),
+    # one of the two alone (the other is zero), dL/d initial_state requested,
+    # L not a multiple of the 8-step chunk
+    (2, 64, 301, 16, inputs.BF16, 1, "initial_state"),
+    (1, 48, 900, 8, inputs.F32, 2, "initial_state"),
+    (2, 64, 301, 16, inputs.BF16, 1, "dlast"),
+    (1, 48, 899, 8, inputs.F32, 2, "dlast"),
 ])
-def test_scan_bwd_from_state(bt, dim, L, N, dtype, G):
+def test_scan_bwd_from_state(bt, dim, L, N, dtype, G, given):
     """The backward of the scan from a given state whose final state enters the
     loss (ssm_scan_bwd_from_state) against the oracle, dL/d initial_state
-    included."""
+    included; with only one of initial_state and dlast given, the oracle takes
+    the missing one as zero."""
     inp = inputs.make_scan_inputs(inputs.ScanShape("bwd-h0", bt, dim, L, N, dtype), 1500 + dim + L, ngroups=G)
     r = np.random.Generator(np.random.PCG64(1600 + L))
     dout = inputs._activation(r, (bt, L, dim), dtype)
     h0 = (r.standard_normal((bt, dim, N)) * 0.5).astype(np.float32)
     dlast = r.standard_normal((bt, dim, N)).astype(np.float32)
+    if given == "initial_state":
+        dlast = None
+    elif given == "dlast":
+        h0 = None
     f = inp.as_f64()
     dout_f = inputs.bf16_bits_to_f64(dout) if dtype == inputs.BF16 else dout.astype(np.float64)
+    zero = np.zeros((bt, dim, N))
     ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"], f["delta_bias"],
-                          f["softplus"], dout_f, initial_state=h0.astype(np.float64), dlast=dlast.astype(np.float64))
+                          f["softplus"], dout_f, initial_state=zero if h0 is None else h0.astype(np.float64),
+                          dlast=zero if dlast is None else dlast.astype(np.float64))
     g = ssm_scan_bwd(dev(inp.u), dev(inp.delta), dev(inp.A), dev(inp.B), dev(inp.C), dev(inp.D), dev(inp.z),
-                     dev(inp.delta_bias), inp.softplus, dev(dout), initial_state=dev(h0), dlast=dev(dlast))
+                     dev(inp.delta_bias), inp.softplus, dev(dout),
+                     initial_state=None if h0 is None else dev(h0), dlast=None if dlast is None else dev(dlast))
     torch.cuda.synchronize()
     bf = dtype == inputs.BF16
     for k in ("du", "ddelta", "dz"):
