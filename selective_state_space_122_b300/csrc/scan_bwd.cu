@@ -94,7 +94,8 @@ struct BwCfg {
     static constexpr int O_P = O_SD + kK * CC * 8;         // float4 [K][threads]: dB or dC quads
     static constexpr int O_PAR = O_P + kK * kThreads * 16; // float2 [CC]: bias, D of each channel
     static constexpr int O_ACC = O_PAR + CC * 8;           // float2 [threads]: dD, dbias partial sums
-    static constexpr int SMEM3 = O_ACC + kThreads * 8;
+    static constexpr int O_SUM = O_ACC + kThreads * 8;     // float [2][N][K]: the chunk's dB, dC sums
+    static constexpr int SMEM3 = O_SUM + 2 * N * kK * 4;
     static_assert(STAGE % 16 == 0 && SMEM3 <= 227 * 1024, "shared memory of one CTA");
     static_assert(HP >= 1 && 2 * HP * KS == kK, "step pairs");
 };
@@ -110,6 +111,7 @@ struct BwdWs {
     int64_t cps;    // chunks per segment
     int64_t nseg;   // segments
     int vec;        // 16-byte asynchronous staging allowed (alignment and sizes)
+    int red4;       // dB, dC take 16-byte reductions (alignment, seqlen % 4 == 0)
 };
 
 // ---------------------------------------------------------------- helpers
@@ -118,6 +120,13 @@ __device__ __forceinline__ void cp_async16(uint32_t dst, const void* src, uint32
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16, %2;" ::"r"(dst), "l"(src), "r"(src_bytes)
                  : "memory");
 }
+// Four consecutive floats added to global memory in one reduction (16-byte
+// aligned address).
+__device__ __forceinline__ void red_add_v4(float* p, float4 v) {
+    asm volatile("red.global.add.v4.f32 [%0], {%1, %2, %3, %4};" ::"l"(p), "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w)
+                 : "memory");
+}
+
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 template <int n>
 __device__ __forceinline__ void cp_async_wait() {
@@ -182,67 +191,112 @@ __device__ __forceinline__ Geo make_geo(const BwdArgs& p, const BwdWs& w) {
 
 // Stage chunk ch (u, delta_raw, z, dout tiles and the B, C rows) into one
 // ring slot; positions past the sequence or the CTA's channels read as zero.
-// 16-byte asynchronous copies when the sizes and pointers allow it (one
-// commit group per chunk), plain loads otherwise.
+// With 16-byte asynchronous copies (vec: sizes and pointers allow them) each
+// thread owns fixed pieces of the slot, whose addresses at chunk 0 are set
+// up once (init) and advanced per chunk (one commit group per chunk); plain
+// loads otherwise.
 template <typename T, int N>
-__device__ __forceinline__ void stage_chunk(unsigned char* slot, const BwdArgs& p, const Geo& q, int64_t ch,
-                                            bool vec, int tid) {
+struct Stager {
+    using CF = BwCfg<T, N>;
+    static constexpr int CC = CF::CC;
+    static constexpr int EPP = 16 / CF::ES;         // elements per 16-byte piece
+    static constexpr int PR = CC / EPP;             // pieces per tile row
+    static constexpr int TP = kK * PR;              // pieces per (t, d) tile
+    static constexpr int BR = kK / EPP;             // pieces per B/C row
+    static constexpr int TOTAL = 4 * TP + 2 * N * BR;
+    static constexpr int MP = (TOTAL + kThreads - 1) / kThreads;
+    const char* src0[MP];   // the piece at chunk 0; null: always zero (no channel, no tensor)
+    uint32_t dst[MP];       // byte offset within the slot
+    int row[MP];            // step offset of the piece within its chunk; +256 for a B/C piece; -1: none
+    int64_t tstride;        // bytes of kK rows of a (t, d) tile
+
+    __device__ __forceinline__ void init(const BwdArgs& p, const Geo& q, int tid) {
+        const int64_t L = p.seqlen, dim = p.dim;
+        tstride = (int64_t)kK * dim * CF::ES;
+#pragma unroll
+        for (int m = 0; m < MP; ++m) {
+            const int i = tid + m * kThreads;
+            src0[m] = nullptr;
+            dst[m] = 0;
+            row[m] = -1;
+            if (i < 4 * TP) {
+                const int tsr = i / TP, r = i - tsr * TP, k = r / PR, col = r - k * PR;
+                const int dd = q.d0 + col * EPP;
+                const void* base = tsr == 0 ? p.u : tsr == 1 ? p.delta : tsr == 2 ? p.z : p.dout;
+                if (base && dd < q.dend)
+                    src0[m] = reinterpret_cast<const char*>(static_cast<const T*>(base) + (q.b * L + k) * dim + dd);
+                dst[m] = tsr * CF::TILE + (k * CC + col * EPP) * CF::ES;
+                row[m] = k;
+            } else if (i < TOTAL) {
+                const int j = i - 4 * TP, which = j / (N * BR), r = j - which * N * BR, n = r / BR,
+                          pc = r - n * BR;
+                const T* bc = static_cast<const T*>(which ? p.C : p.B);
+                src0[m] = reinterpret_cast<const char*>(bc + (q.blk * N + n) * L + pc * EPP);
+                dst[m] = 4 * CF::TILE + which * CF::BCT + (n * kK + pc * EPP) * CF::ES;
+                row[m] = 256 + pc * EPP;
+            }
+        }
+    }
+
+    __device__ __forceinline__ void issue(unsigned char* slot, const BwdArgs& p, int64_t ch) const {
+        const uint32_t base = smem_u32(slot);
+#pragma unroll
+        for (int m = 0; m < MP; ++m) {
+            if (row[m] < 0) continue;
+            const bool bc = row[m] >= 256;
+            const int64_t t = ch * kK + (row[m] & 255);
+            const bool ok = src0[m] != nullptr && t < p.seqlen;
+            const char* src = ok ? src0[m] + (bc ? ch * (kK * CF::ES) : ch * tstride) : static_cast<const char*>(p.u);
+            cp_async16(base + dst[m], src, ok ? 16u : 0u);
+        }
+        cp_async_commit();
+    }
+};
+
+template <typename T, int N>
+__device__ __forceinline__ void stage_scalar(unsigned char* slot, const BwdArgs& p, const Geo& q, int64_t ch,
+                                             int tid) {
     using CF = BwCfg<T, N>;
     constexpr int CC = CF::CC;
     const int64_t t0 = ch * kK, L = p.seqlen, dim = p.dim;
-    // tile tsr: u, delta_raw, z, dout (selected, not indexed: no local array)
-    const auto src4 = [&](int tsr) {
-        return static_cast<const T*>(tsr == 0 ? p.u : tsr == 1 ? p.delta : tsr == 2 ? p.z : p.dout);
-    };
-    const T* Bg = static_cast<const T*>(p.B);
-    const T* Cg = static_cast<const T*>(p.C);
+    T* tl = reinterpret_cast<T*>(slot);
+    constexpr int TOTAL = 4 * kK * CC + 2 * N * kK;
+    for (int i = tid; i < TOTAL; i += kThreads) {
+        float v = 0.f;
+        if (i < 4 * kK * CC) {
+            const int tsr = i / (kK * CC), r = i - tsr * kK * CC, k = r / CC, cc = r - k * CC;
+            const int64_t t = t0 + k, dd = q.d0 + cc;
+            const T* tp = static_cast<const T*>(tsr == 0 ? p.u : tsr == 1 ? p.delta : tsr == 2 ? p.z : p.dout);
+            if (tp && t < L && dd < q.dend) v = to_f32(tp[(q.b * L + t) * dim + dd]);
+        } else {
+            const int j = i - 4 * kK * CC, which = j / (N * kK), r = j - which * N * kK, n = r / kK,
+                      k = r - n * kK;
+            const int64_t t = t0 + k;
+            const T* bc = static_cast<const T*>(which ? p.C : p.B);
+            if (t < L) v = to_f32(bc[(q.blk * N + n) * L + t]);
+        }
+        tl[i] = from_f32<T>(v);
+    }
+}
+
+template <typename T, int N>
+__device__ __forceinline__ void stage_chunk(const Stager<T, N>& st, unsigned char* slot, const BwdArgs& p,
+                                            const Geo& q, int64_t ch, bool vec, int tid) {
+    if (vec) st.issue(slot, p, ch);
+    else stage_scalar<T, N>(slot, p, q, ch, tid);
+}
+
+// The same without held piece addresses (recomputed per chunk): for the
+// reverse pass, whose registers go to the chunk's states.
+template <typename T, int N>
+__device__ __forceinline__ void stage_chunk_direct(unsigned char* slot, const BwdArgs& p, const Geo& q, int64_t ch,
+                                                   bool vec, int tid) {
     if (vec) {
-        constexpr int EPP = 16 / CF::ES;           // elements per 16-byte piece
-        constexpr int PR = CC / EPP;               // pieces per tile row
-        constexpr int TP = kK * PR;                // pieces per (t, d) tile
-        constexpr int BR = kK / EPP;               // pieces per B/C row
-        constexpr int TOTAL = 4 * TP + 2 * N * BR;
-        const uint32_t base = smem_u32(slot);
-        for (int i = tid; i < TOTAL; i += kThreads) {
-            const void* src = p.u;
-            uint32_t dst;
-            bool ok;
-            if (i < 4 * TP) {
-                const int tsr = i / TP, r = i - tsr * TP, k = r / PR, col = r - k * PR;
-                const int64_t t = t0 + k, dd = q.d0 + col * EPP;
-                const T* tp = src4(tsr);
-                ok = tp != nullptr && t < L && dd < q.dend;
-                if (ok) src = tp + (q.b * L + t) * dim + dd;
-                dst = base + tsr * CF::TILE + (k * CC + col * EPP) * CF::ES;
-            } else {
-                const int j = i - 4 * TP, which = j / (N * BR), r = j - which * N * BR, n = r / BR,
-                          pc = r - n * BR;
-                const int64_t t = t0 + pc * EPP;
-                ok = t < L;
-                if (ok) src = (which ? Cg : Bg) + (q.blk * N + n) * L + t;
-                dst = base + 4 * CF::TILE + which * CF::BCT + (n * kK + pc * EPP) * CF::ES;
-            }
-            cp_async16(dst, src, ok ? 16u : 0u);
-        }
-        cp_async_commit();
+        Stager<T, N> st;
+        st.init(p, q, tid);
+        st.issue(slot, p, ch);
     } else {
-        T* tl = reinterpret_cast<T*>(slot);
-        constexpr int TOTAL = 4 * kK * CC + 2 * N * kK;
-        for (int i = tid; i < TOTAL; i += kThreads) {
-            float v = 0.f;
-            if (i < 4 * kK * CC) {
-                const int tsr = i / (kK * CC), r = i - tsr * kK * CC, k = r / CC, cc = r - k * CC;
-                const int64_t t = t0 + k, dd = q.d0 + cc;
-                const T* tp = src4(tsr);
-                if (tp && t < L && dd < q.dend) v = to_f32(tp[(q.b * L + t) * dim + dd]);
-            } else {
-                const int j = i - 4 * kK * CC, which = j / (N * kK), r = j - which * N * kK, n = r / kK,
-                          k = r - n * kK;
-                const int64_t t = t0 + k;
-                if (t < L) v = to_f32((which ? Cg : Bg)[(q.blk * N + n) * L + t]);
-            }
-            tl[i] = from_f32<T>(v);
-        }
+        stage_scalar<T, N>(slot, p, q, ch, tid);
     }
 }
 
@@ -308,7 +362,7 @@ __device__ __forceinline__ void chunk_terms(const unsigned char* slot, unsigned 
 // ------------------------------------------------------------ pass 1
 
 template <typename T, int N>
-__global__ void __launch_bounds__(kThreads, 6)
+__global__ void __launch_bounds__(kThreads, 5)
 bwd_local_kernel(const BwdArgs p, const BwdWs w) {
     using CF = BwCfg<T, N>;
     constexpr int R = CF::R, CPW = CF::CPW, CC = CF::CC;
@@ -333,6 +387,8 @@ bwd_local_kernel(const BwdArgs p, const BwdWs w) {
     const float4* s_B4 = reinterpret_cast<const float4*>(sm + CF::O_BC);
     const float4* s_C4 = s_B4 + kK * N / 4;
     const bool vec = w.vec != 0;
+    Stager<T, N> st;
+    if (vec) st.init(p, q, tid);
 
     float2 h0 = make_float2(0.f, 0.f), h1 = h0, L0 = h0, L1 = h0;
     float2 Q0 = make_float2(1.f, 1.f), Q1 = Q0;
@@ -340,7 +396,7 @@ bwd_local_kernel(const BwdArgs p, const BwdWs w) {
     const int64_t n_ch = q.c_end - q.c_begin;
 #pragma unroll 1
     for (int j = 0; j < kStages - 1; ++j)
-        if (j < n_ch) stage_chunk<T, N>(sm + j * CF::STAGE, p, q, q.c_begin + j, vec, tid);
+        if (j < n_ch) stage_chunk<T, N>(st, sm + j * CF::STAGE, p, q, q.c_begin + j, vec, tid);
         else if (vec) cp_async_commit();
 #pragma unroll 1
     for (int64_t i = 0; i < n_ch; ++i) {
@@ -349,7 +405,7 @@ bwd_local_kernel(const BwdArgs p, const BwdWs w) {
         __syncthreads();
         {
             const int64_t nx = i + kStages - 1;
-            if (nx < n_ch) stage_chunk<T, N>(sm + (nx % kStages) * CF::STAGE, p, q, q.c_begin + nx, vec, tid);
+            if (nx < n_ch) stage_chunk<T, N>(st, sm + (nx % kStages) * CF::STAGE, p, q, q.c_begin + nx, vec, tid);
             else if (vec) cp_async_commit();
         }
         chunk_terms<T, N, false>(sm + (i % kStages) * CF::STAGE, sm, p, q, c, bias, tid);
@@ -480,7 +536,7 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
     // staging order: the segment's chunks from the last one back
 #pragma unroll 1
     for (int j = 0; j < kStages - 1; ++j)
-        if (j < n_ch) stage_chunk<T, N>(sm + j * CF::STAGE, p, q, q.c_end - 1 - j, vec, tid);
+        if (j < n_ch) stage_chunk_direct<T, N>(sm + j * CF::STAGE, p, q, q.c_end - 1 - j, vec, tid);
         else if (vec) cp_async_commit();
 #pragma unroll 1
     for (int64_t i = 0; i < n_ch; ++i) {
@@ -490,7 +546,7 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
         __syncthreads();
         {
             const int64_t nx = i + kStages - 1;
-            if (nx < n_ch) stage_chunk<T, N>(sm + (nx % kStages) * CF::STAGE, p, q, q.c_end - 1 - nx, vec, tid);
+            if (nx < n_ch) stage_chunk_direct<T, N>(sm + (nx % kStages) * CF::STAGE, p, q, q.c_end - 1 - nx, vec, tid);
             else if (vec) cp_async_commit();
         }
         // the stored local state entering the chunk, the sum of Delta before
@@ -641,17 +697,16 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
             constexpr int LPW = 16 / R;                // lanes per warp holding one sum's quads
             const int si = tid / TPS, part = tid % TPS;
             const int k = si / (2 * R), rem = si % (2 * R), which = rem / R, gq = rem % R;
-            float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+            float2 a01 = make_float2(0.f, 0.f), a23 = a01;
 #pragma unroll
             for (int m = 0; m < 8; ++m) {
                 const int j = part + TPS * m;
                 const int wv = j / LPW, cw = which * LPW + j % LPW;
                 const float4 v = s_P[k * kThreads + wv * 32 + gq + R * cw];
-                acc.x += v.x;
-                acc.y += v.y;
-                acc.z += v.z;
-                acc.w += v.w;
+                a01 = add2(a01, make_float2(v.x, v.y));
+                a23 = add2(a23, make_float2(v.z, v.w));
             }
+            float4 acc = make_float4(a01.x, a01.y, a23.x, a23.y);
 #pragma unroll
             for (int o = 1; o < TPS; o <<= 1) {
                 acc.x += __shfl_xor_sync(0xffffffffu, acc.x, o);
@@ -659,12 +714,30 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
                 acc.z += __shfl_xor_sync(0xffffffffu, acc.z, o);
                 acc.w += __shfl_xor_sync(0xffffffffu, acc.w, o);
             }
-            const int64_t t = t0 + k;
-            if (t < L) {
-                float* dst = (which ? p.dC : p.dB) + (q.blk * N + 4 * gq) * L + t;
+            if (w.red4) {
+                // the sums as [which][n][k], then one 16-byte reduction per
+                // (which, state, four steps)
+                float* s_sum = reinterpret_cast<float*>(sm + CF::O_SUM);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    if (jj % TPS == part) atomicAdd(dst + jj * L, comp(acc, jj));
+                    if (jj % TPS == part) s_sum[(which * N + 4 * gq + jj) * kK + k] = comp(acc, jj);
+                __syncthreads();
+                constexpr int NQ = 2 * N * kK / 4;
+                for (int i2 = tid; i2 < NQ; i2 += kThreads) {
+                    const int wh = i2 / (2 * N), n = (i2 % (2 * N)) / 2, kq = i2 % 2;
+                    const int64_t t = t0 + 4 * kq;
+                    if (t < L)
+                        red_add_v4((wh ? p.dC : p.dB) + (q.blk * N + n) * L + t,
+                                   reinterpret_cast<const float4*>(s_sum)[i2]);
+                }
+            } else {
+                const int64_t t = t0 + k;
+                if (t < L) {
+                    float* dst = (which ? p.dC : p.dB) + (q.blk * N + 4 * gq) * L + t;
+#pragma unroll
+                    for (int jj = 0; jj < 4; ++jj)
+                        if (jj % TPS == part) atomicAdd(dst + jj * L, comp(acc, jj));
+                }
             }
         }
     }
@@ -772,6 +845,7 @@ cudaError_t launch_scan_bwd(const BwdArgs& a, DType dt, void* workspace, int sms
     // 16-byte staging: every staged row piece starts on a 16-byte boundary
     w.vec = al16(a.u) && al16(a.delta) && al16(a.z) && al16(a.dout) && al16(a.B) && al16(a.C) &&
             (a.dim * es) % 16 == 0 && (a.gch * es) % 16 == 0 && (a.seqlen * es) % 16 == 0;
+    w.red4 = al16(a.dB) && al16(a.dC) && a.seqlen % 4 == 0;
     const bool bf = dt == DType::BF16;
     switch (a.dstate) {
         case 4: return bf ? launch_bwd_t<__nv_bfloat16, 4>(a, w, s) : launch_bwd_t<float, 4>(a, w, s);
