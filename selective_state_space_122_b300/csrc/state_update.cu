@@ -16,16 +16,19 @@
 // its quad of the channel in L consecutive batch rows; lane g of a channel
 // computes that channel's per-(row, channel) terms -- softplus, Delta x, D x,
 // silu(z) -- for row g only, and the channel's lanes exchange them by
-// shuffle, so none of it is computed twice.  Per row: the states are updated
+// shuffle, so none of it is computed twice.  Row addresses advance by fixed
+// strides from the group's first row (the channel's B/C group is divided out
+// once per thread, not per row).  Per row: the states are updated
 // with one SFU exp2 each, C . h is summed over the channel's lanes by
 // shuffle, and the lane that owns the row writes the output.  A block covers
 // 32 * 4 / L channels x 2 L batch rows; each row of A is loaded once per
 // thread and reused over its rows.  State loads use the default cache
 // policy, state stores the streaming (evict-first) one.  Measured on a B300
 // (256 x 5120 x 16, CUDA events): 34.8 us with a clean L2 (5.1 TB/s for
-// 178.6 MB), 40.9 us when L2 first holds 126 MB of dirty lines, against
-// 38.9 / 43.0 us with default stores; streaming loads as well were slower
-// (45.0 / 49.2 us).
+// 178.6 MB), 38.9 us when L2 first holds dirty lines, against 38.9 / 43.0 us
+// with default stores; streaming loads as well were slower (45.0 / 49.2 us).
+// Five blocks of 256 threads per SM: more residency (fewer registers) ran
+// slower (41.0 us at six blocks, 61.4 us at eight).
 #include "ssm_internal.cuh"
 
 namespace ssm {
@@ -54,7 +57,7 @@ struct Quad<float> {
 // Block: kThreads lanes = 32 * 4 / L channels x L lanes (lane g of a channel
 // owns states 4g .. 4g+3), times kRowsY groups of L batch rows in y.
 template <typename T, int N, bool kFast, bool kVecBC>
-__global__ void __launch_bounds__(kThreads * kRowsY)
+__global__ void __launch_bounds__(kThreads * kRowsY, 5)
 state_update_kernel(UpdateArgs p) {
     static_assert(N % 4 == 0, "d_state must be a multiple of 4");
     constexpr int L = N / 4;                   // lanes (and rows) per channel
@@ -81,14 +84,21 @@ state_update_kernel(UpdateArgs p) {
         dlg = to_f32(static_cast<const T*>(p.dt)[bdg]) + bias;
         if (p.z) zg = to_f32(static_cast<const T*>(p.z)[bdg]);
     }
+    // row b0's state quad, B/C quad and output; the next row is dim * L
+    // quads, ngroups * N activations and dim outputs further (hoisted: no
+    // per-row division or 64-bit index products)
+    float4* st0 = reinterpret_cast<float4*>(p.state) + (b0 * p.dim + d) * L + g;
+    const int64_t st_row = p.dim * L;
+    const int64_t grp = d_ok ? (int64_t)((uint32_t)d / (uint32_t)p.gch) : 0;
+    const T* B0 = static_cast<const T*>(p.B) + (b0 * p.ngroups + grp) * N + 4 * g;
+    const T* C0 = static_cast<const T*>(p.C) + (b0 * p.ngroups + grp) * N + 4 * g;
+    const int64_t bc_row = p.ngroups * N;
+    T* out0 = static_cast<T*>(p.out) + b0 * p.dim + d;
+    const int nrow = d_ok ? (p.batch - b0 < L ? (int)(p.batch - b0) : L) : 0;   // valid rows of this group
     // the states of all L rows, loaded before any arithmetic (L loads in flight)
     float4 s[L];
 #pragma unroll
-    for (int r = 0; r < L; ++r) {
-        const int64_t br = b0 + r;
-        s[r] = (d_ok && br < p.batch) ? reinterpret_cast<const float4*>(p.state)[(br * p.dim + d) * L + g]
-                                      : make_float4(0.f, 0.f, 0.f, 0.f);
-    }
+    for (int r = 0; r < L; ++r) s[r] = r < nrow ? st0[r * st_row] : make_float4(0.f, 0.f, 0.f, 0.f);
     if (p.softplus) dlg = softplus_f<kFast>(dlg);
     const float dxg = dlg * xg;
     const float gate = p.z ? silu_f<kFast>(zg) : 1.f;
@@ -96,16 +106,14 @@ state_update_kernel(UpdateArgs p) {
 
 #pragma unroll
     for (int r = 0; r < L; ++r) {
-        const int64_t br = b0 + r;
-        const bool row_ok = d_ok && br < p.batch;
+        const bool row_ok = r < nrow;
         // row r's Delta and Delta x, from the lane that owns row r
         const float dl = __shfl_sync(0xffffffffu, dlg, base + r);
         const float dx = __shfl_sync(0xffffffffu, dxg, base + r);
         float4 bv = make_float4(0.f, 0.f, 0.f, 0.f), cv = bv;
         if (row_ok) {
-            const int64_t blk = br * p.ngroups + (int64_t)((uint32_t)d / (uint32_t)p.gch);
-            const T* Bp = static_cast<const T*>(p.B) + blk * N + 4 * g;
-            const T* Cp = static_cast<const T*>(p.C) + blk * N + 4 * g;
+            const T* Bp = B0 + r * bc_row;
+            const T* Cp = C0 + r * bc_row;
             if constexpr (kVecBC) {
                 bv = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Bp));
                 cv = Quad<T>::f(*reinterpret_cast<const typename Quad<T>::type*>(Cp));
@@ -125,9 +133,9 @@ state_update_kernel(UpdateArgs p) {
 #pragma unroll
         for (int o = 1; o < L; o <<= 1) y += __shfl_xor_sync(0xffffffffu, y, o);
         if (row_ok) {
-            __stcs(reinterpret_cast<float4*>(p.state) + (br * p.dim + d) * L + g, make_float4(h0.x, h0.y, h1.x, h1.y));
+            __stcs(st0 + r * st_row, make_float4(h0.x, h0.y, h1.x, h1.y));
             // the owner of row r has its D x and gate
-            if (g == r) static_cast<T*>(p.out)[br * p.dim + d] = from_f32<T>((y + dd * xg) * gate);
+            if (g == r) out0[r * p.dim] = from_f32<T>((y + dd * xg) * gate);
         }
     }
 }
