@@ -132,6 +132,135 @@ __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, floa
     if (s == 12345.678f) sink[threadIdx.x & 255] = s;
 }
 
+
+// The core of an in-warp time split of the scan, for measuring its cost: a
+// lane owns all 16 states of one channel over a sub-chunk of T steps (lane =
+// channel + 4 x sub-chunk, four channels and eight sub-chunks per warp, a
+// chunk of 8T steps).  Per chunk: (1) each lane runs its T steps from a zero
+// state, keeping the 16 T decays exp2(Delta A) in registers; (2) the
+// sub-chunks' (decay product, local state) pairs are combined by an
+// inclusive warp-shuffle scan (three levels), giving each lane the state
+// entering its sub-chunk from the chunk's carry; (3) each lane re-sweeps its
+// steps with the kept decays and sums C . h in-lane, one output per step.
+// Per-step Delta, Delta u, B and C come from shared memory as in a staged
+// kernel; no global memory is touched inside the loop, so the rate is the
+// design's compute-and-shared-memory ceiling.
+template <int T>
+__global__ void __launch_bounds__(128) tsplit_kernel(float* sink, int iters) {
+    constexpr int CH = 8 * T;   // steps per chunk
+    __shared__ float2 s_dd[CH][4];
+    __shared__ float4 s_b[CH][4], s_c[CH][4];
+    __shared__ float s_y[4][CH][4];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    for (int i = tid; i < CH * 4; i += 128) {
+        const int t = i / 4, q = i % 4;
+        s_dd[t][q] = make_float2(1e-3f + 1e-3f * ((t * 7 + q) % 97), 1e-2f * (((t * 5 + q) % 21) - 10));
+        s_b[t][q] = make_float4(0.1f * ((t + q) % 7) - 0.3f, 0.05f * ((t * 3 + q) % 9) - 0.2f, 0.1f, -0.1f);
+        s_c[t][q] = make_float4(0.2f, -0.1f * ((t + 2 * q) % 5), 0.05f * ((t + q) % 3), 0.3f);
+    }
+    __syncthreads();
+    const int ch = lane & 3, sub = lane >> 2;
+    float2 A[8], carry[8];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) {
+        A[p] = make_float2(-1.4427f * (2 * p + 1) * 0.1f, -1.4427f * (2 * p + 2) * 0.1f);
+        carry[p] = make_float2(0.f, 0.f);
+    }
+    const auto fma2 = [](float2 a, float2 b, float2 c) {
+        unsigned long long d, pa, pb, pc;
+        asm("mov.b64 %0, {%1, %2};" : "=l"(pa) : "f"(a.x), "f"(a.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(pb) : "f"(b.x), "f"(b.y));
+        asm("mov.b64 %0, {%1, %2};" : "=l"(pc) : "f"(c.x), "f"(c.y));
+        asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(pa), "l"(pb), "l"(pc));
+        float2 r;
+        asm("mov.b64 {%0, %1}, %2;" : "=f"(r.x), "=f"(r.y) : "l"(d));
+        return r;
+    };
+    const auto mul2 = [&](float2 a, float2 b) { return fma2(a, b, make_float2(0.f, 0.f)); };
+    for (int it = 0; it < iters; ++it) {
+        // (1) local sweep, decays kept
+        float2 a[T][8], h[8];
+        float sd = 0.f;
+#pragma unroll
+        for (int p = 0; p < 8; ++p) h[p] = make_float2(0.f, 0.f);
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const int t = sub * T + j;
+            const float2 dd = s_dd[t][ch];
+            sd += dd.x;
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 bq = s_b[t][q];
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int p = 2 * q + hlf;
+                    const float2 e = mul2(make_float2(dd.x, dd.x), A[p]);
+                    a[j][p] = make_float2(ex2a(e.x), ex2a(e.y));
+                    const float2 b2 = hlf ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+                    h[p] = fma2(a[j][p], h[p], mul2(make_float2(dd.y, dd.y), b2));
+                }
+            }
+        }
+        // (2) decay product of the sub-chunk, then the inclusive scan over
+        // the eight sub-chunks of each channel (lanes 4 apart)
+        float2 P[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const float2 e = mul2(make_float2(sd, sd), A[p]);
+            P[p] = make_float2(ex2a(e.x), ex2a(e.y));
+        }
+#pragma unroll
+        for (int off = 1; off < 8; off <<= 1) {
+#pragma unroll
+            for (int p = 0; p < 8; ++p) {
+                const float2 hp = make_float2(__shfl_up_sync(0xffffffffu, h[p].x, 4 * off),
+                                              __shfl_up_sync(0xffffffffu, h[p].y, 4 * off));
+                const float2 pp = make_float2(__shfl_up_sync(0xffffffffu, P[p].x, 4 * off),
+                                              __shfl_up_sync(0xffffffffu, P[p].y, 4 * off));
+                if (sub >= off) {
+                    h[p] = fma2(P[p], hp, h[p]);
+                    P[p] = mul2(P[p], pp);
+                }
+            }
+        }
+        // state entering this sub-chunk, from the chunk's carry; the carry
+        // of the next chunk from sub-chunk 7
+        float2 hin[8];
+#pragma unroll
+        for (int p = 0; p < 8; ++p) {
+            const float2 he = make_float2(__shfl_up_sync(0xffffffffu, h[p].x, 4), __shfl_up_sync(0xffffffffu, h[p].y, 4));
+            const float2 pe = make_float2(__shfl_up_sync(0xffffffffu, P[p].x, 4), __shfl_up_sync(0xffffffffu, P[p].y, 4));
+            hin[p] = sub == 0 ? carry[p] : fma2(pe, carry[p], he);
+            const float2 fin = fma2(P[p], carry[p], h[p]);
+            carry[p] = make_float2(__shfl_sync(0xffffffffu, fin.x, ch + 28), __shfl_sync(0xffffffffu, fin.y, ch + 28));
+        }
+        // (3) re-sweep with the kept decays; C . h in-lane
+#pragma unroll
+        for (int j = 0; j < T; ++j) {
+            const int t = sub * T + j;
+            const float2 dd = s_dd[t][ch];
+            float2 acc = make_float2(0.f, 0.f);
+#pragma unroll
+            for (int q = 0; q < 4; ++q) {
+                const float4 bq = s_b[t][q], cq = s_c[t][q];
+#pragma unroll
+                for (int hlf = 0; hlf < 2; ++hlf) {
+                    const int p = 2 * q + hlf;
+                    const float2 b2 = hlf ? make_float2(bq.z, bq.w) : make_float2(bq.x, bq.y);
+                    const float2 c2 = hlf ? make_float2(cq.z, cq.w) : make_float2(cq.x, cq.y);
+                    hin[p] = fma2(a[j][p], hin[p], mul2(make_float2(dd.y, dd.y), b2));
+                    acc = fma2(c2, hin[p], acc);
+                }
+            }
+            s_y[warp][t][ch] = acc.x + acc.y;
+        }
+    }
+    __syncthreads();
+    float s = s_y[warp][lane % CH][lane & 3];
+#pragma unroll
+    for (int p = 0; p < 8; ++p) s += carry[p].x + carry[p].y;
+    if (s == 12345.678f) sink[tid] = s;
+}
 }  // namespace
 
 // Same as ssmpk_probe but with an explicit block shape: `blocks_per_sm` x SM
@@ -198,4 +327,41 @@ PK_API int ssmpk_sm_count(void) {
     if (cudaGetDevice(&dev) != cudaSuccess) return -1;
     if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1;
     return sms;
+}
+
+// The in-warp time-split core (tsplit_kernel) with sub-chunks of T = 2 or 4
+// steps: returns scan elements (step x channel x state) per second over one
+// launch of 8 x SM-count blocks of 128 threads (residency set by the
+// kernel's registers), timed with CUDA events after a warm-up launch;
+// negative on error.  A measurement tool, not part of the scan path.
+PK_API double ssmpk_timesplit(int T, int iters) {
+    int dev = 0, sms = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) return -1.0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return -1.0;
+    if ((T != 2 && T != 4) || iters <= 0) return -2.0;
+    float* sink = nullptr;
+    if (cudaMalloc(&sink, 128 * sizeof(float)) != cudaSuccess) return -1.0;
+    cudaEvent_t e0, e1;
+    cudaEventCreate(&e0);
+    cudaEventCreate(&e1);
+    const dim3 grid(sms * 8), block(128);
+    auto launch = [&]() {
+        if (T == 2) tsplit_kernel<2><<<grid, block>>>(sink, iters);
+        else tsplit_kernel<4><<<grid, block>>>(sink, iters);
+    };
+    launch();
+    cudaEventRecord(e0);
+    launch();
+    cudaEventRecord(e1);
+    cudaEventSynchronize(e1);
+    float ms = 0.f;
+    const cudaError_t err = cudaEventElapsedTime(&ms, e0, e1);
+    const cudaError_t last = cudaGetLastError();
+    cudaEventDestroy(e0);
+    cudaEventDestroy(e1);
+    cudaFree(sink);
+    if (err != cudaSuccess || last != cudaSuccess || ms <= 0.f) return -1.0;
+    // per block and iteration: 4 warps x 4 channels x 8T steps x 16 states
+    const double per_block = double(iters) * 4 * 4 * 8 * T * 16;
+    return per_block * double(grid.x) / (ms * 1e-3);
 }

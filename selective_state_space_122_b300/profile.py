@@ -15,8 +15,10 @@ kernels.  ``decode`` does the same for one ssm_state_update step.  --ngroups
 draws B and C per channel group (the grouped entry points).  ``units``
 prints the measured SFU (ex2, tanh) and packed-FMA throughput at 1, 2 and 8
 warps per scheduler, and the ex2 rate when each ex2 is followed by 0, 1 or 2
-independent packed FMAs -- the SFU / FMA-pipe mix of a recurrence step
-(libssmpeak.so).
+independent packed FMAs -- the SFU / FMA-pipe mix of a recurrence step --
+and the rate of the in-warp time-split core (16 states per lane over short
+sub-chunks, warp-shuffle combine, re-sweep) with the long-sequence scan time
+it implies (libssmpeak.so).
 """
 from __future__ import annotations
 
@@ -159,6 +161,16 @@ def cmd_units(a):
             per = r / (sms * a.clock_mhz * 1e6)
             print(f"{name:14s} {wps:3.0f} warp(s)/scheduler: {per:6.2f} ex2 per clock per SM "
                   f"({128.0 / per:5.2f} cycles per warp-wide ex2 on a scheduler)")
+    # the in-warp time-split core (16 states per lane over T-step sub-chunks,
+    # shuffle combine, re-sweep) and what it implies for the long-sequence
+    # scan's 1 x 5120 x 131072 x 16 elements
+    lib.ssmpk_timesplit.argtypes = [ctypes.c_int, ctypes.c_int]
+    lib.ssmpk_timesplit.restype = ctypes.c_double
+    elems = 5120 * 131072 * 16
+    for T in (2, 4):
+        r = max(lib.ssmpk_timesplit(T, 2000) for _ in range(3))
+        print(f"time-split core T={T}: {r / 1e9:8.1f} G elements/s = {r / (sms * a.clock_mhz * 1e6):6.2f} "
+              f"per clock per SM; the long-sequence scan's elements alone: {elems / r * 1e3:6.3f} ms")
     return 0
 
 
