@@ -166,7 +166,8 @@ int64_t ssm_scan_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int
 int ssm_device_error(int clear) {
     const int a = ssm::read_device_error(clear != 0);
     const int b = ssm::read_tmem_device_error(clear != 0);
-    return (a < 0 || b < 0) ? -1 : (a | b);
+    const int c = ssm::read_update_device_error(clear != 0);
+    return (a < 0 || b < 0 || c < 0) ? -1 : (a | b | c);
 }
 
 }  // extern "C"
@@ -461,7 +462,7 @@ ssm_status ssm_state_update_grouped(float* state, const void* x, const void* dt,
                       dt_softplus ? 1 : 0};
     a.ngroups = ngroups;
     a.gch = dim / ngroups;
-    return launch_status(ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32,
+    return launch_status(ssm::launch_state_update(a, dtype == SSM_BF16 ? ssm::DType::BF16 : ssm::DType::F32, sms,
                                                   static_cast<cudaStream_t>(stream)));
 }
 

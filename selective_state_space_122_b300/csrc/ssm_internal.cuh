@@ -152,7 +152,9 @@ int check_scan_call(const void* u, const void* delta, const float* A, const void
 int scan_layout_count(int dstate);
 ScanLayoutInfo scan_layout_info(int dstate, int layout);
 cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s);
-cudaError_t launch_state_update(const UpdateArgs& a, DType dt, cudaStream_t s);
+cudaError_t launch_state_update(const UpdateArgs& a, DType dt, int sms, cudaStream_t s);
+// The decode unit's device error word (its bulk-copy pipeline's bounded waits).
+int read_update_device_error(bool clear);
 
 // ---------------------------------------------------------------- device side
 

@@ -24,7 +24,12 @@ def one_step_case(shape, seed, **kw):
 
 @pytest.mark.parametrize("dtype,N,bt,dim", [(inputs.BF16, 16, 256, 5120), (inputs.F32, 16, 3, 77),
                                              (inputs.BF16, 8, 5, 33), (inputs.F32, 4, 2, 9),
-                                             (inputs.BF16, 4, 1, 1)])
+                                             (inputs.BF16, 4, 1, 1),
+                                             # enough (row, 128-channel tile) pairs for the
+                                             # bulk-copy pipeline; ragged last tiles
+                                             (inputs.BF16, 16, 160, 200), (inputs.F32, 16, 300, 132),
+                                             (inputs.BF16, 8, 200, 264), (inputs.F32, 4, 400, 136),
+                                             (inputs.BF16, 4, 1000, 48)])
 def test_single_step_vs_oracle(dtype, N, bt, dim):
     shape = inputs.DecodeShape("step", bt, dim, N, dtype)
     d, x, dt, z, B, C = one_step_case(shape, 4)
@@ -123,3 +128,28 @@ def test_decode_writes_stay_in_bounds():
     torch.cuda.synchronize()
     assert bool((buf[:guard] == 77.0).all()) and bool((buf[guard + n:] == 77.0).all())
     assert bool((sbuf[:guard] == 5.0).all()) and bool((sbuf[guard + 3 * 50 * 16:] == 5.0).all())
+
+
+def test_decode_bulk_writes_stay_in_bounds():
+    """The bulk-copy pipeline (160 rows x two 128-channel tiles, the second
+    ragged) writes no state or output outside its tensors."""
+    bt, dim, N = 160, 200, 16
+    shape = inputs.DecodeShape("guard-bulk", bt, dim, N, inputs.BF16)
+    d, x, dt, z, B, C = one_step_case(shape, 9)
+    guard = 4096
+    n = bt * dim
+    buf = torch.full((n + 2 * guard,), 77.0, dtype=torch.bfloat16, device="cuda")
+    out = buf[guard:guard + n].view(bt, dim)
+    sbuf = torch.full((n * N + 2 * guard,), 5.0, dtype=torch.float32, device="cuda")
+    state = sbuf[guard:guard + n * N].view(bt, dim, N)
+    state.copy_(torch.from_numpy(d.state0))
+    ssm_state_update(state, dev(x), dev(dt), dev(d.A), dev(B), dev(C), dev(d.D), dev(z), dev(d.dt_bias),
+                     True, out=out)
+    torch.cuda.synchronize()
+    assert bool((buf[:guard] == 77.0).all()) and bool((buf[guard + n:] == 77.0).all())
+    assert bool((sbuf[:guard] == 5.0).all()) and bool((sbuf[guard + n * N:] == 5.0).all())
+    ref_state = d.state0.astype(np.float64)
+    ref = oracle.step(ref_state, f64(x, inputs.BF16), f64(dt, inputs.BF16), d.A, f64(B, inputs.BF16),
+                      f64(C, inputs.BF16), d.D, f64(z, inputs.BF16), d.dt_bias, True)
+    check_out(host_f64(out), ref, inputs.BF16)
+    check_state(host_f64(state), ref_state, inputs.BF16, "state")

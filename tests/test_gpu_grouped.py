@@ -123,7 +123,9 @@ def f64(a, dtype):
 
 
 @pytest.mark.parametrize("dtype,N,bt,dim,G", [(inputs.BF16, 16, 64, 5120, 8), (inputs.F32, 8, 3, 48, 3),
-                                               (inputs.BF16, 4, 5, 30, 10), (inputs.F32, 16, 2, 7, 7)])
+                                               (inputs.BF16, 4, 5, 30, 10), (inputs.F32, 16, 2, 7, 7),
+                                               # bulk-copy pipeline, groups crossing its tiles
+                                               (inputs.BF16, 16, 160, 200, 4), (inputs.F32, 8, 200, 192, 6)])
 def test_grouped_decode_step(dtype, N, bt, dim, G):
     d = inputs.make_decode_inputs(inputs.DecodeShape("grp-step", bt, dim, N, dtype), 2400 + dim)
     x, dt, z, B, C = d.token(ngroups=G)
