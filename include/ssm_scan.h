@@ -463,11 +463,14 @@ SSM_API ssm_status ssm_force_scan_path(int path, int generic_layout);
  *     after it (when the call is cut into segments: more 32-channel groups
  *     than SMs, or 128/N-channel groups than warps for the segmented kernel)
  *     waits until the limit and gives up (bit 4), and the warps that wait on
- *     it give up in turn.  Those calls' outputs are undefined.
+ *     it give up in turn; in the decode steps that take the bulk-copy
+ *     pipeline, block 0 never issues its first row's copies, so its consumers
+ *     wait that stage out and give up (bit 1).  Those calls' outputs (and the
+ *     decode step's state rows of block 0) are undefined.
  *   wait_limit_ns: the limit of every wait from now on (<= 0: the default).
- * ssm_debug_wait_test(0, 0) restores the defaults.  Writes two words of
- * device memory on the current device (a synchronous copy); call it only
- * while no scan runs.  Returns SSM_ERR_DEVICE if the copy fails.  Production
+ * ssm_debug_wait_test(0, 0) restores the defaults.  Writes a few words of
+ * device memory on the current device (synchronous copies); call it only
+ * while no scan or decode step runs.  Returns SSM_ERR_DEVICE if the copy fails.  Production
  * callers never need it.
  */
 SSM_API ssm_status ssm_debug_wait_test(int withhold_flag, int64_t wait_limit_ns);

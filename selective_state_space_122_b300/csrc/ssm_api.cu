@@ -132,7 +132,9 @@ int ssm_version(void) { return 101; }
 ssm_status ssm_debug_wait_test(int withhold_flag, int64_t wait_limit_ns) {
     const unsigned long long ns = wait_limit_ns > 0 ? (unsigned long long)wait_limit_ns : 1000000000ull;
     const int w = withhold_flag ? 1 : 0;
-    if (ssm::set_wait_test_seg(w, ns) != 0 || ssm::set_wait_test_tmem(w, ns) != 0) return SSM_ERR_DEVICE;
+    if (ssm::set_wait_test_seg(w, ns) != 0 || ssm::set_wait_test_tmem(w, ns) != 0 ||
+        ssm::set_wait_test_update(w, ns) != 0)
+        return SSM_ERR_DEVICE;
     return SSM_OK;
 }
 

@@ -153,8 +153,10 @@ int scan_layout_count(int dstate);
 ScanLayoutInfo scan_layout_info(int dstate, int layout);
 cudaError_t launch_scan_fwd(const ScanArgs& a, DType dt, const ScanPlan& plan, cudaStream_t s);
 cudaError_t launch_state_update(const UpdateArgs& a, DType dt, int sms, cudaStream_t s);
-// The decode unit's device error word (its bulk-copy pipeline's bounded waits).
+// The decode unit's device error word (its bulk-copy pipeline's bounded waits)
+// and its wait test hook (as set_wait_test_seg).
 int read_update_device_error(bool clear);
+int set_wait_test_update(int withhold, unsigned long long limit_ns);
 
 // ---------------------------------------------------------------- device side
 

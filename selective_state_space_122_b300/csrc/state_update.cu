@@ -218,6 +218,9 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(UpdateA
         const uint32_t tx = sbytes + (p.z ? 3 : 2) * tbytes + 2 * bcb;
         int64_t issued = 0;
         bool ok = true;
+        // the wait test hook: block 0 never issues its first row's copies, so
+        // its consumers wait that stage out and give up
+        const bool hold = withhold_handoff((int)blockIdx.x, 0);
         for (int64_t m = 0; m < nrows && ok; ++m) {
             const int st = (int)(m % kBulkStages);
             const uint32_t sb = base + st * CF::STAGE;
@@ -234,6 +237,10 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(UpdateA
                 bulk_store(p.state + (bp * p.dim + d0) * N, sb, sbytes);
                 bulk_commit();
                 bulk_wait_read<0>();
+            }
+            if (m == 0 && hold) {
+                issued = 1;
+                continue;
             }
             const int64_t b = rs + m * rsplit, off = b * p.dim + d0;
             const uint32_t fb = full0 + 8 * st;
@@ -406,6 +413,12 @@ cudaError_t launch_t(const UpdateArgs& a, int sms, cudaStream_t s) {
 cudaError_t launch_state_update(const UpdateArgs& a, DType dt, int sms, cudaStream_t s) {
     if (dt == DType::F32) return launch_t<float>(a, sms, s);
     return launch_t<__nv_bfloat16>(a, sms, s);
+}
+
+int set_wait_test_update(int withhold, unsigned long long limit_ns) {
+    if (cudaMemcpyToSymbol(g_withhold_flag, &withhold, sizeof(withhold)) != cudaSuccess) return -1;
+    if (cudaMemcpyToSymbol(g_wait_limit_ns, &limit_ns, sizeof(limit_ns)) != cudaSuccess) return -1;
+    return 0;
 }
 
 int read_update_device_error(bool clear) {
