@@ -156,13 +156,12 @@ SSM_API ssm_status ssm_scan_fwd_from_state(const void* u, const void* delta, con
 
 /*
  * ssm_scan_workspace_bytes -- bytes of workspace the fast paths of
- * ssm_scan_fwd need for these sizes: the largest of (a) B and C staged as
- * float32 rows, batch * round_up(seqlen, 64) * 2 * dstate * 4 bytes (relay
- * kernel); (b) B and C staged in the activation dtype (same count of
- * elements), the state handed between sequence segments of each chain
+ * ssm_scan_fwd need for these sizes: the larger of (a) B and C staged in the
+ * activation dtype as rows, batch * round_up(seqlen, 64) * 2 * dstate
+ * elements, the state handed between sequence segments of each chain
  * (chains * cw * dstate * 4 bytes, cw = 128 / dstate channels per chain,
  * chains = batch * ceil(dim / cw)) and one int flag per chain (segmented
- * kernel); and, for bf16 with dstate 16, (c) the tensor-memory kernels'
+ * kernel); and, for bf16 with dstate 16, (b) the tensor-memory kernels'
  * staged operand (batch * round_up(seqlen, 64) * 32 * 4 bytes), their
  * segment state (groups * 32 * 16 * 4 bytes, groups = batch * ceil(dim / 32))
  * and groups * 8 int flags; each part rounded up to 256 bytes.  Returns -1

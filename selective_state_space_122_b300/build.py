@@ -24,7 +24,7 @@ CSRC = os.path.join(PKG, "csrc")
 LIB = os.path.join(PKG, "libssmscan.so")
 PEAK_LIB = os.path.join(PKG, "libssmpeak.so")
 PEAK_SOURCES = ["sfu_peak.cu"]
-SOURCES = ["ssm_api.cu", "scan_fwd.cu", "scan_relay.cu", "scan_tmem.cu", "state_update.cu", "conv1d.cu", "scan_bwd.cu", "noalloc.cu"]
+SOURCES = ["ssm_api.cu", "scan_fwd.cu", "scan_seg.cu", "scan_tmem.cu", "state_update.cu", "conv1d.cu", "scan_bwd.cu", "noalloc.cu"]
 HEADERS = ["ssm_internal.cuh", "scan_common.cuh", "device_memo.h"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 COMPILE_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "-Xcompiler", "-fvisibility=hidden"]

@@ -79,20 +79,20 @@ __device__ __forceinline__ bool mbar_test(uint32_t bar, uint32_t parity) {
     return ok != 0;
 }
 
-#ifndef SSM_RELAY_SPIN
-#define SSM_RELAY_SPIN 0
+#ifndef SSM_WAIT_SPIN
+#define SSM_WAIT_SPIN 0
 #endif
 
 // Wait for the phase with the given parity to complete; false after ~1 s.
 __device__ __forceinline__ bool mbar_wait_slow(uint32_t bar, uint32_t parity) {
     const unsigned long long t0 = globaltimer();
-    while (!(SSM_RELAY_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)))
+    while (!(SSM_WAIT_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)))
         if (globaltimer() - t0 > wait_limit_ns()) return false;
     return true;
 }
 
 __device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity) {
-    if (SSM_RELAY_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
+    if (SSM_WAIT_SPIN ? mbar_test(bar, parity) : mbar_try(bar, parity)) return true;
     return mbar_wait_slow(bar, parity);
 }
 
@@ -185,7 +185,7 @@ __device__ __forceinline__ float2 softplus_poly2(float2 x) {
 }
 
 template <bool kFast>
-__device__ __forceinline__ float2 relay_softplus2(float2 x) {
+__device__ __forceinline__ float2 softplus2_path(float2 x) {
     if constexpr (kFast) return softplus_poly2(x);
     else return make_float2(softplus_acc(x.x), softplus_acc(x.y));
 }

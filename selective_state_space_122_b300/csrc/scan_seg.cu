@@ -1,4 +1,4 @@
-// scan_relay.cu -- the segmented selective scan (float32 activations, or
+// scan_seg.cu -- the segmented selective scan (float32 activations, or
 // d_state 4 / 8), the B/C staging kernel it shares with the tensor-memory
 // kernels' hosts, and the TMA capability checks of the fast paths.
 //
@@ -276,7 +276,7 @@ scan_seg_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constant_
 #pragma unroll
                 for (int q = 0; q < NP; ++q) {
                     float2 dl = add2(xr[q], bias2);
-                    if constexpr (kSoftplus) dl = relay_softplus2<kFast>(dl);
+                    if constexpr (kSoftplus) dl = softplus2_path<kFast>(dl);
                     if (tail) dl = mul2(dl, make_float2(t0 + tas[q] < L ? 1.f : 0.f, t0 + tas[q] + 1 < L ? 1.f : 0.f));
                     const float2 du = mul2(dl, uk[q]);
                     float2 gt = splat2(1.f);
@@ -602,7 +602,7 @@ cudaError_t launch_seg_t(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         }, &occ))
         return err;
     const SegPlan pl = seg_plan<N, CF::K>(a.batch, a.dim, a.seqlen, sms, occ);
-    const int64_t lpad = relay_lpad(a.seqlen);
+    const int64_t lpad = staged_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     T* bc = reinterpret_cast<T*>(w);
     const int64_t bc_bytes = (a.batch * a.ngroups * lpad * 2 * N * (int64_t)sizeof(T) + 255) / 256 * 256;
@@ -637,7 +637,7 @@ int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dsta
     const int cw = 32 / (dstate / 4);
     const int64_t units = (dim + cw - 1) / cw;
     const int64_t M = batch * units;
-    const int64_t bc_bytes = (batch * ngroups * relay_lpad(seqlen) * 2 * dstate * elem_bytes + 255) / 256 * 256;
+    const int64_t bc_bytes = (batch * ngroups * staged_lpad(seqlen) * 2 * dstate * elem_bytes + 255) / 256 * 256;
     const int64_t st_bytes = (M * cw * dstate * 4 + 255) / 256 * 256;
     return bc_bytes + st_bytes + (M * 4 + 255) / 256 * 256;
 }
@@ -659,9 +659,9 @@ cudaError_t launch_scan_seg(const ScanArgs& a, DType dt, void* ws, int sms, cuda
     return cudaErrorInvalidValue;
 }
 
-int64_t relay_lpad(int64_t seqlen) { return (seqlen + 63) / 64 * 64; }
+int64_t staged_lpad(int64_t seqlen) { return (seqlen + 63) / 64 * 64; }
 
-bool relay_supported(const ScanArgs& a, DType dt) {
+bool tma_rows_supported(const ScanArgs& a, DType dt) {
     const int64_t es = dt == DType::BF16 ? 2 : 4;
     auto al16 = [](const void* q) { return (reinterpret_cast<uintptr_t>(q) & 15u) == 0; };
     if (!al16(a.u) || !al16(a.delta) || !al16(a.out) || (a.z && !al16(a.z)) || !al16(a.A) ||

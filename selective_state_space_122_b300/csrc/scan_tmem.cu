@@ -458,7 +458,7 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                         const float2 xr = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + oa)),
                                                       ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + ob)));
                         float2 dl = add2(xr, bias2);
-                        if constexpr (kSoftplus) dl = relay_softplus2<true>(dl);
+                        if constexpr (kSoftplus) dl = softplus2_path<true>(dl);
                         if (t0 + K > L)
                             dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + ta + 1 < L ? 1.f : 0.f));
                         const float2 du = mul2(dl, uv);
@@ -1227,7 +1227,7 @@ cudaError_t launch_tmem2(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         return err;
     // the work split depends only on the CTA's channel count and chunk length
     const TmPlan pl = tm_plan(a.batch, a.dim, a.seqlen, sms, CF::CC, CF::K);
-    const int64_t lpad = relay_lpad(a.seqlen);
+    const int64_t lpad = staged_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
     const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
@@ -1274,7 +1274,7 @@ cudaError_t launch_ws(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
         }, &occ))
         return err;
     const TmPlan pl = tm_plan(a.batch, a.dim, a.seqlen, sms, CF::CC, CF::K);
-    const int64_t lpad = relay_lpad(a.seqlen);
+    const int64_t lpad = staged_lpad(a.seqlen);
     unsigned char* w = static_cast<unsigned char*>(ws);
     float* xop = reinterpret_cast<float*>(w);
     const int64_t x_bytes = (a.batch * a.ngroups * lpad * 32 * 4 + 255) / 256 * 256;
@@ -1305,7 +1305,7 @@ cudaError_t launch_ws(const ScanArgs& a, void* ws, int sms, cudaStream_t s) {
 
 bool tmem_supported(const ScanArgs& a, DType dt) {
     if (dt != DType::BF16 || a.dstate != 16) return false;
-    if (!relay_supported(a, dt)) return false;
+    if (!tma_rows_supported(a, dt)) return false;
     // B/C groups: every CTA's 32 channels lie in one group
     if (a.ngroups != 1 && a.gch % 32 != 0) return false;
     // the total task count (chains * 64 segments) stays a 32-bit int
@@ -1318,7 +1318,7 @@ int64_t tmem_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dst
     // (channel, state) of every 32-channel group, and one flag per consumer
     // warp of each group
     const int64_t groups = batch * ((dim + 31) / 32);
-    const int64_t x_bytes = (batch * ngroups * relay_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
+    const int64_t x_bytes = (batch * ngroups * staged_lpad(seqlen) * 32 * 4 + 255) / 256 * 256;
     const int64_t st_bytes = (groups * 32 * 16 * 4 + 255) / 256 * 256;
     return x_bytes + st_bytes + (groups * 8 * 4 + 255) / 256 * 256;
 }

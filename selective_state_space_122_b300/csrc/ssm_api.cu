@@ -255,7 +255,7 @@ ssm_status ssm_scan_fwd_grouped(const void* u, const void* delta, const float* A
     // generic kernel; ssm_force_scan_path picks one of them instead.
     const int force = g_force_path.load(std::memory_order_relaxed);
     // (chains * 64 segments must stay a 32-bit task count)
-    const bool fast_ok = workspace && ssm::relay_supported(a, dt) &&
+    const bool fast_ok = workspace && ssm::tma_rows_supported(a, dt) &&
                          batch * ((dim + 127) / 128 * dstate) * 64 < (int64_t(1) << 31);
     const bool tmem_ok = fast_ok && ssm::tmem_supported(a, dt) &&
                          workspace_bytes >= ssm::tmem_workspace_bytes(batch, dim, seqlen, (int)dstate, ngroups);

@@ -66,11 +66,11 @@ struct ScanPlan {
     int layout;  // index into the compiled layouts for this d_state
 };
 
-// TMA fast paths (scan_relay.cu): the staged-sequence padding (a multiple of
+// TMA fast paths (scan_seg.cu): the staged-sequence padding (a multiple of
 // 64 steps) and whether a call's pointers and sizes suit the tensor maps.
-int64_t relay_lpad(int64_t seqlen);
-bool relay_supported(const ScanArgs& a, DType dt);
-// Segmented direct scan (scan_relay.cu): needs staged B/C plus the segment
+int64_t staged_lpad(int64_t seqlen);
+bool tma_rows_supported(const ScanArgs& a, DType dt);
+// Segmented direct scan (scan_seg.cu): needs staged B/C plus the segment
 // hand-off state and flags (seg_workspace_bytes).
 int64_t seg_workspace_bytes(int64_t batch, int64_t dim, int64_t seqlen, int dstate, int elem_bytes,
                             int64_t ngroups);

@@ -83,21 +83,22 @@ def check_state(got: np.ndarray, ref: np.ndarray, dtype: str, what: str = "last_
 LAYOUTS = {16: 7, 8: 4, 4: 2}
 
 
-def relay_ok(dim: int, dtype: str) -> bool:
-    """Whether the relay (fast) path accepts this channel count: rows of
-    dim elements must be a multiple of 16 bytes for the TMA tensor maps."""
+def tma_rows_ok(dim: int, dtype: str) -> bool:
+    """Whether the TMA paths (segmented, tensor-memory) accept this channel
+    count: rows of dim elements must be a multiple of 16 bytes for the
+    tensor maps."""
     return (dim * (2 if dtype == inputs.BF16 else 4)) % 16 == 0
 
 
 def tmem_ok(N: int, dim: int, dtype: str) -> bool:
     """Whether the tensor-memory path takes the shape: bf16, 16 states, TMA rows."""
-    return N == 16 and dtype == inputs.BF16 and relay_ok(dim, dtype)
+    return N == 16 and dtype == inputs.BF16 and tma_rows_ok(dim, dtype)
 
 
 def paths(N: int, dim: int = 64, dtype: str = inputs.BF16):
     """Every way to run a scan of this shape: the tensor-memory and segmented
     paths (when they accept the shape) and each generic layout."""
-    fast = ["seg"] if relay_ok(dim, dtype) else []
+    fast = ["seg"] if tma_rows_ok(dim, dtype) else []
     if tmem_ok(N, dim, dtype):
         fast = ["tmem2", "ws"] + fast
     return fast + list(range(LAYOUTS[N]))

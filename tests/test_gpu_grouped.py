@@ -20,8 +20,8 @@ pytestmark = pytest.mark.gpu
 
 def grouped_paths(N, dim, gch, dtype):
     """The paths that take groups of gch channels: the tensor-memory kernels
-    need whole 32-channel blocks in a group, the segmented / relay kernels
-    whole blocks of 128 / N channels; the generic layouts take any size."""
+    need whole 32-channel blocks in a group, the segmented kernel whole
+    blocks of 128 / N channels; the generic layouts take any size."""
     out = []
     for g in paths(N, dim, dtype):
         if g in ("ws", "tmem2") and gch % 32:
@@ -53,7 +53,7 @@ def _oracle(inp, h0=None):
 @pytest.mark.parametrize("bt,dim,L,N,dtype,G", [
     (2, 128, 300, 16, inputs.BF16, 4),     # 32 channels per group: every path
     (2, 256, 200, 16, inputs.BF16, 2),
-    (2, 72, 130, 16, inputs.BF16, 9),      # 8 per group: segmented, relay, generic
+    (2, 72, 130, 16, inputs.BF16, 9),      # 8 per group: segmented, generic
     (2, 30, 77, 16, inputs.BF16, 10),      # 3 per group (odd): generic only
     (3, 64, 65, 8, inputs.F32, 4),         # 16 per group
     (2, 64, 50, 4, inputs.F32, 2),         # 32 per group
