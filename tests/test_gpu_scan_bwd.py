@@ -9,7 +9,7 @@ import torch
 
 import oracle
 from gpu_util import dev, host_f64
-from selective_state_space_122_b300 import inputs, ssm_scan_bwd
+from selective_state_space_122_b300 import inputs, ssm_scan_bwd, ssm_scan_fwd
 
 pytestmark = pytest.mark.gpu
 
@@ -132,3 +132,52 @@ def test_scan_bwd_from_state(bt, dim, L, N, dtype, G, given):
         _close(host_f64(g[k]), ref[k], 1e-4, k, rounded=bf)
     for k in ("dA", "dB", "dC", "dD", "ddelta_bias", "dinitial_state"):
         _close(host_f64(g[k]), ref[k], 1e-4, k)
+
+
+def test_scan_bwd_long_sequence_sampled_channels():
+    """The backward at the long-sequence size (1 x 5120 x 131072, d_state 16,
+    bf16): the chains cut into the maximum of 64 segments of 256 chunks.
+    Every per-channel gradient of 16 sampled channels -- du, ddelta, dz over
+    all 128K steps, dA, dD, ddelta_bias -- against the adjoint oracle run on
+    those channels alone.  dB and dC sum over every channel, so they are held
+    to the identity <dB, B> = <dC, C> = sum(dout * (out - D u silu(z))) (out
+    is linear in B and in C apart from the D u term), with out from the
+    forward scan and a bound on its bf16 rounding."""
+    shape = inputs.LONG_SEQ
+    inp = inputs.make_scan_inputs(shape, 31)
+    r = np.random.Generator(np.random.PCG64(32))
+    dout = inputs._activation(r, (shape.batch, shape.seqlen, shape.dim), shape.dtype)
+    t = dict(u=dev(inp.u), delta=dev(inp.delta), A=dev(inp.A), B=dev(inp.B), C=dev(inp.C), D=dev(inp.D),
+             z=dev(inp.z), bias=dev(inp.delta_bias))
+    do = dev(dout)
+    g = ssm_scan_bwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["bias"], inp.softplus, do)
+    torch.cuda.synchronize()
+    sel = np.array([0, 1, 31, 32, 33, 127, 128, 1000, 2047, 2560, 3333, 4095, 4096, 5087, 5118, 5119])
+    f = inp.channels(sel).as_f64()
+    dsel = inputs.bf16_bits_to_f64(np.ascontiguousarray(dout[:, :, sel]))
+    ref = oracle.scan_bwd(f["u"], f["delta"], f["A"], f["B"], f["C"], f["D"], f["z"], f["delta_bias"],
+                          f["softplus"], dsel)
+    idx = torch.as_tensor(sel, device=do.device)
+    for k in ("du", "ddelta", "dz"):
+        _close(host_f64(g[k][:, :, idx]), ref[k], 1e-4, k, rounded=True)
+    _close(host_f64(g["dA"][idx]), ref["dA"], 1e-4, "dA")
+    for k in ("dD", "ddelta_bias"):
+        _close(host_f64(g[k][idx]), ref[k], 1e-4, k)
+    for k in ("dB", "dC"):
+        assert bool(torch.isfinite(g[k]).all()), k
+    # the B/C identity against the forward scan's output
+    del g["du"], g["ddelta"], g["dz"]
+    out, _ = ssm_scan_fwd(t["u"], t["delta"], t["A"], t["B"], t["C"], t["D"], t["z"], t["bias"], inp.softplus)
+    torch.cuda.synchronize()
+    dof = do.double()
+    uu, zz = t["u"].double(), t["z"].double()
+    skip = t["D"].double() * uu * zz * torch.sigmoid(zz)
+    terms = dof * out.double()
+    rhs = float((terms - dof * skip).sum())
+    lhs_b = float((g["dB"].double() * t["B"].double()).sum())
+    lhs_c = float((g["dC"].double() * t["C"].double()).sum())
+    # out is rounded to bf16 (error <= 2^-8 |out|, roughly uniform): six
+    # standard deviations of the rounding's contribution to the sum
+    bound = 6.0 * 2.0 ** -8 / np.sqrt(3.0) * float(torch.sqrt((terms ** 2).sum())) + 1e-4 * abs(rhs)
+    assert abs(lhs_b - rhs) <= bound, (lhs_b, rhs, bound)
+    assert abs(lhs_c - rhs) <= bound, (lhs_c, rhs, bound)
