@@ -145,6 +145,10 @@ def test_grouped_decode_step(dtype, N, bt, dim, G):
     (2, 48, 77, 8, inputs.F32, 3),
     (1, 30, 65, 16, inputs.F32, 10),       # 3 channels per group
     (2, 256, 1024, 16, inputs.BF16, 2),
+    # several segments per chain, groups narrower than the 64- and 128-channel
+    # blocks of d_state 8 and 4
+    (1, 96, 2000, 8, inputs.BF16, 3),
+    (1, 200, 1500, 4, inputs.F32, 5),
 ])
 def test_grouped_bwd(bt, dim, L, N, dtype, G):
     inp = inputs.make_scan_inputs(inputs.ScanShape("grp-bwd", bt, dim, L, N, dtype), 2500 + dim + L, ngroups=G)
