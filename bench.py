@@ -585,6 +585,10 @@ def bench_ours(args):
                     "peak_source": peaks["source"]},
             "t_sfu_ms": t_sfu * 1e3,
             "t_hbm_ms": t_hbm * 1e3,
+            # diagnostic: the float32 pipe's share, 4 FMA-pipe operations per
+            # element (Delta A, Delta u B, the state FMA, C . h) at the
+            # measured packed-FMA rate
+            "t_fma_ms": 4 * scan_elements() / units["ffma"] * 1e3,
             "t_roof_ms": t_roof_ms,
             "frac_of_roofline_time": t_roof_ms / scan_avg,
         },
