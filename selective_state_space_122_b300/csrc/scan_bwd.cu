@@ -88,14 +88,14 @@ struct BwCfg {
     static constexpr int O_TD = kStages * STAGE;           // float4 [K][CC]: Delta, Delta u, dy, u
     static constexpr int O_BC = O_TD + kK * CC * 16;       // float [2][K][N]: B, C
     static constexpr int SMEM1 = O_BC + 2 * kK * N * 4;
-    static constexpr int O_EZ = SMEM1;                     // float2 [K][CC]: dz factor, softplus'
-    static constexpr int O_YP = O_EZ + kK * CC * 8;        // float [K][CC][R]: readout partials
+    static constexpr int O_YP = SMEM1;                     // float [K][CC][R]: readout partials
     static constexpr int O_SD = O_YP + kK * CC * R * 4;    // float2 [K][CC]: sum lambda B, sum A w
     static constexpr int O_P = O_SD + kK * CC * 8;         // float4 [K][threads]: dB or dC quads
     static constexpr int O_PAR = O_P + kK * kThreads * 16; // float2 [CC]: bias, D of each channel
     static constexpr int O_ACC = O_PAR + CC * 8;           // float2 [threads]: dD, dbias partial sums
-    static constexpr int O_SUM = O_ACC + kThreads * 8;     // float [2][N][K]: the chunk's dB, dC sums
-    static constexpr int SMEM3 = O_SUM + 2 * N * kK * 4;
+    static constexpr int SUMROW = kK + 4;                  // padded row (48 bytes): fewer bank conflicts
+    static constexpr int O_SUM = O_ACC + kThreads * 8;     // float [2][N][SUMROW]: the chunk's dB, dC sums
+    static constexpr int SMEM3 = O_SUM + 2 * N * SUMROW * 4;
     static_assert(STAGE % 16 == 0 && SMEM3 <= 227 * 1024, "shared memory of one CTA");
     static_assert(HP >= 1 && 2 * HP * KS == kK, "step pairs");
 };
@@ -300,14 +300,23 @@ __device__ __forceinline__ void stage_chunk_direct(unsigned char* slot, const Bw
     }
 }
 
+// A thread's per-(t, d) factors the output pass needs, kept in registers
+// across the chunk (item j: step tid / CC + j * KS).
+template <int NI>
+struct EpiKeep {
+    float fz[NI], sg[NI];   // dout silu'(z), softplus'(x)
+};
+
 // The per-(t, d) terms of one staged chunk: Delta (zero past the sequence
 // and the CTA's channels, so such steps leave the recurrence unchanged),
 // Delta u, dy, u into s_td; B and C as float32 into s_BC; with kMain also the
-// dz factor dout silu'(z) and softplus'(x) into s_ez.  bias: delta_bias of
+// dz factor dout silu'(z) and softplus'(x) into *keep.  bias: delta_bias of
 // this thread's channel.
+
 template <typename T, int N, bool kMain>
 __device__ __forceinline__ void chunk_terms(const unsigned char* slot, unsigned char* sm, const BwdArgs& p,
-                                            const Geo& q, int64_t ch, float bias, int tid) {
+                                            const Geo& q, int64_t ch, float bias, int tid,
+                                            EpiKeep<2 * BwCfg<T, N>::HP>* keep = nullptr) {
     using CF = BwCfg<T, N>;
     constexpr int CC = CF::CC;
     constexpr bool kFast = !std::is_same<T, float>::value;
@@ -316,7 +325,6 @@ __device__ __forceinline__ void chunk_terms(const unsigned char* slot, unsigned 
     const T* tz = reinterpret_cast<const T*>(slot + 2 * CF::TILE);
     const T* to = reinterpret_cast<const T*>(slot + 3 * CF::TILE);
     float4* s_td = reinterpret_cast<float4*>(sm + CF::O_TD);
-    float2* s_ez = reinterpret_cast<float2*>(sm + CF::O_EZ);
     const int c = tid % CC;
     const bool cok = q.d0 + c < q.dend;
 #pragma unroll
@@ -346,16 +354,16 @@ __device__ __forceinline__ void chunk_terms(const unsigned char* slot, unsigned 
         s_td[o0] = make_float4(dl.x, du.x, dy.x, u2.x);
         s_td[o1] = make_float4(dl.y, du.y, dy.y, u2.y);
         if constexpr (kMain) {
-            s_ez[o0] = make_float2(fz.x, sg.x);
-            s_ez[o1] = make_float2(fz.y, sg.y);
+            keep->fz[j] = fz.x, keep->sg[j] = sg.x;
+            keep->fz[j + CF::HP] = fz.y, keep->sg[j + CF::HP] = sg.y;
         }
     }
     // B and C rows [N][K] -> float32 [K][N]
     const T* tb = reinterpret_cast<const T*>(slot + 4 * CF::TILE);
     float* s_bc = reinterpret_cast<float*>(sm + CF::O_BC);
-    for (int i = tid; i < 2 * N * kK; i += kThreads) {
-        const int which = i / (N * kK), r = i - which * N * kK, n = r / kK, k = r - n * kK;
-        s_bc[which * kK * N + k * N + n] = to_f32(tb[i]);
+    for (int i = tid; i < 2 * N * kK; i += kThreads) {   // i: destination order [which][k][n]
+        const int which = i / (N * kK), r = i - which * N * kK, k = r / N, n = r - k * N;
+        s_bc[i] = to_f32(tb[which * N * kK + n * kK + k]);
     }
 }
 
@@ -558,7 +566,8 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
             cmc = w.cum[(q.b * w.nch + c) * dim + d];
             hs = *reinterpret_cast<const float4*>(w.aggH + seg_o);
         }
-        chunk_terms<T, N, true>(sm + (i % kStages) * CF::STAGE, sm, p, q, c, s_par[ct].x, tid);
+        EpiKeep<2 * CF::HP> keep;
+        chunk_terms<T, N, true>(sm + (i % kStages) * CF::STAGE, sm, p, q, c, s_par[ct].x, tid, &keep);
         __syncthreads();
         // the true state entering the chunk: local state + exp(A sum Delta) H_s
         const float2 cm2 = splat2(cmc);
@@ -652,7 +661,6 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
         __syncthreads();
         // per-(t, d) outputs of the chunk
         {
-            const float2* s_ez = reinterpret_cast<const float2*>(sm + CF::O_EZ);
             const float2* s_sd2 = reinterpret_cast<const float2*>(sm + CF::O_SD);
             const float Dd = s_par[ct].y;
             float accD = 0.f, accb = 0.f;
@@ -662,7 +670,8 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
                 const int64_t t = t0 + k;
                 const int o = k * CC + ct;
                 const float4 ta = s_td[o];
-                const float2 ez = s_ez[o], sd = s_sd2[o];
+                const float2 sd = s_sd2[o];
+                const float dlj = ta.x, dyj = ta.z, uj = ta.w;
                 float y = 0.f;
                 if constexpr (R == 4) {
                     const float4 v = reinterpret_cast<const float4*>(s_yp)[o];
@@ -673,18 +682,18 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
                 } else {
                     y = s_yp[o];
                 }
-                y = fmaf(Dd, ta.w, y);
-                const float du = fmaf(Dd, ta.z, ta.x * sd.x);
-                float dd = fmaf(ta.w, sd.x, kLn2 * sd.y);
-                if (p.softplus) dd *= ez.y;
+                y = fmaf(Dd, uj, y);
+                const float du = fmaf(Dd, dyj, dlj * sd.x);
+                float dd = fmaf(uj, sd.x, kLn2 * sd.y);
+                if (p.softplus) dd *= keep.sg[j];
                 const bool ok = tok_c && t < L;
-                accD = fmaf(ta.z, ta.w, accD);
+                accD = fmaf(dyj, uj, accD);
                 accb += ok ? dd : 0.f;
                 if (ok) {
                     const int64_t gi = (q.b * L + t) * dim + dt;
                     static_cast<T*>(p.du)[gi] = from_f32<T>(du);
                     static_cast<T*>(p.ddelta)[gi] = from_f32<T>(dd);
-                    if (p.z && p.dz) static_cast<T*>(p.dz)[gi] = from_f32<T>(ez.x * y);
+                    if (p.z && p.dz) static_cast<T*>(p.dz)[gi] = from_f32<T>(keep.fz[j] * y);
                 }
             }
             const float2 a = s_acc[tid];
@@ -720,7 +729,7 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
                 float* s_sum = reinterpret_cast<float*>(sm + CF::O_SUM);
 #pragma unroll
                 for (int jj = 0; jj < 4; ++jj)
-                    if (jj % TPS == part) s_sum[(which * N + 4 * gq + jj) * kK + k] = comp(acc, jj);
+                    if (jj % TPS == part) s_sum[(which * N + 4 * gq + jj) * CF::SUMROW + k] = comp(acc, jj);
                 __syncthreads();
                 constexpr int NQ = 2 * N * kK / 4;
                 for (int i2 = tid; i2 < NQ; i2 += kThreads) {
@@ -728,7 +737,7 @@ bwd_main_kernel(const BwdArgs p, const BwdWs w) {
                     const int64_t t = t0 + 4 * kq;
                     if (t < L)
                         red_add_v4((wh ? p.dC : p.dB) + (q.blk * N + n) * L + t,
-                                   reinterpret_cast<const float4*>(s_sum)[i2]);
+                                   reinterpret_cast<const float4*>(s_sum + (wh * N + n) * CF::SUMROW)[kq]);
                 }
             } else {
                 const int64_t t = t0 + k;
