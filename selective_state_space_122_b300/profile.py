@@ -3,6 +3,7 @@
     python -m selective_state_space_122_b300.profile scan [--batch B] [--dim D] [--L L]
            [--N N] [--iters K] [--path tmem2|ws|seg|generic] [--ngroups G]
     python -m selective_state_space_122_b300.profile decode [--batch B] [--dim D] [--N N] [--iters K] [--ngroups G]
+           [--graph STEPS]
     python -m selective_state_space_122_b300.profile conv [--batch B] [--dim D] [--L L] [--W W] [--iters K]
     python -m selective_state_space_122_b300.profile bwd [--batch B] [--dim D] [--L L] [--N N] [--iters K] [--ngroups G]
     python -m selective_state_space_122_b300.profile units
@@ -11,7 +12,9 @@
 pages' workloads (u, delta_raw, z, B, C ~ N(0, 1); A = -(1..N); D = 1;
 delta_bias = softplus^-1(dt), dt log-uniform in [1e-3, 0.1]) and prints the
 CUDA-event time of each call: the command behind the ncu captures of the scan
-kernels.  ``decode`` does the same for one ssm_state_update step.  --ngroups
+kernels.  ``decode`` does the same for one ssm_state_update step; with
+``--graph STEPS`` it also times STEPS back-to-back steps issued eagerly against
+the same steps captured once into a CUDA graph and replayed (per step).  --ngroups
 draws B and C per channel group (the grouped entry points).  ``units``
 prints the measured SFU (ex2, tanh) and packed-FMA throughput at 1, 2 and 8
 warps per scheduler, and the ex2 rate when each ex2 is followed by 0, 1 or 2
@@ -96,6 +99,34 @@ def cmd_decode(a):
         ms = e0.elapsed_time(e1)
         print(f"decode {a.batch}x{a.dim} N{a.N} G{a.ngroups} iter {i}: {ms * 1e3:.1f} us "
               f"({nbytes / (ms * 1e-3) / 1e9:.0f} GB/s)", flush=True)
+    if a.graph:
+        def steps():
+            for _ in range(a.graph):
+                ssm_state_update(st, x, dt, A, B, C, D, z, bias, True, out=out)
+
+        def per_step(fn):
+            best = float("inf")
+            for _ in range(5):
+                e0.record()
+                fn()
+                e1.record()
+                torch.cuda.synchronize()
+                best = min(best, e0.elapsed_time(e1) / a.graph)
+            return best
+
+        eager = per_step(steps)
+        side = torch.cuda.Stream()
+        side.wait_stream(torch.cuda.current_stream())
+        with torch.cuda.stream(side):
+            steps()
+        torch.cuda.current_stream().wait_stream(side)
+        torch.cuda.synchronize()
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            steps()
+        graph = per_step(g.replay)
+        print(f"decode {a.batch}x{a.dim} N{a.N}: {a.graph} steps, eager {eager * 1e3:.2f} us/step, "
+              f"CUDA graph replay {graph * 1e3:.2f} us/step", flush=True)
     return 0
 
 
@@ -191,6 +222,7 @@ def main(argv=None):
     d.add_argument("--N", type=int, default=16)
     d.add_argument("--iters", type=int, default=5)
     d.add_argument("--ngroups", type=int, default=1)
+    d.add_argument("--graph", type=int, default=0, help="also time this many steps eagerly and as a CUDA graph")
     bw = sub.add_parser("bwd")
     bw.add_argument("--batch", type=int, default=8)
     bw.add_argument("--dim", type=int, default=2048)
