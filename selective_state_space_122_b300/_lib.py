@@ -7,6 +7,7 @@ device is present the calls raise.
 """
 from __future__ import annotations
 
+import contextlib
 import ctypes
 import os
 from typing import Optional, Tuple
@@ -135,15 +136,24 @@ def _dtype_code(t: torch.Tensor) -> int:
 def _ptr(t: Optional[torch.Tensor], dtype=None, device=None) -> Optional[int]:
     if t is None:
         return None
-    if not t.is_cuda:
+    idx = t.get_device()          # -1 off the GPU; an int compare, cheaper than torch.device objects
+    if idx < 0:
         raise ValueError("every tensor must be on a CUDA device")
-    if device is not None and t.device != device:
+    if device is not None and idx != device.index:
         raise ValueError("every tensor must be on the same CUDA device")
     if not t.is_contiguous():
         raise ValueError("every tensor must be contiguous")
     if dtype is not None and t.dtype != dtype:
         raise TypeError(f"expected {dtype}, got {t.dtype}")
     return t.data_ptr()
+
+
+def _on(device: torch.device):
+    """The device context of a call: switch only when the tensors live on a
+    device other than the current one (the switch costs more than the check)."""
+    if device.index is None or device.index == torch.cuda.current_device():
+        return contextlib.nullcontext()
+    return torch.cuda.device(device)
 
 
 def _stream(device: torch.device) -> int:
@@ -213,7 +223,7 @@ def ssm_scan_fwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
     ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
     if initial_state is not None and tuple(initial_state.shape) != (bt, dim, N):
         raise ValueError(f"initial_state must be {(bt, dim, N)}, got {tuple(initial_state.shape)}")
-    with torch.cuda.device(dev):
+    with _on(dev):
         if G != 1:
             code = lib.ssm_scan_fwd_grouped(
                 _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
@@ -277,7 +287,7 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
             if t is not None and tuple(t.shape) != (bt, dim, N):
                 raise ValueError(f"ssm_scan_bwd: {name} must be {(bt, dim, N)}, got {tuple(t.shape)}")
         g["dinitial_state"] = torch.empty(bt, dim, N, **f32)
-        with torch.cuda.device(dev):
+        with _on(dev):
             code = lib.ssm_scan_bwd_from_state(
                 _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
                 _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev),
@@ -289,7 +299,7 @@ def ssm_scan_bwd(u: torch.Tensor, delta: torch.Tensor, A: torch.Tensor, B: torch
                 bt, dim, L, N, G, _dtype_code(u), _ptr(workspace, None, dev), ws_bytes, _stream(dev))
         _check("ssm_scan_bwd_from_state", code)
         return g
-    with torch.cuda.device(dev):
+    with _on(dev):
         code = lib.ssm_scan_bwd_grouped(
             _ptr(u, dt, dev), _ptr(delta, dt, dev), _ptr(A, torch.float32, dev), _ptr(B, dt, dev),
             _ptr(C, dt, dev), _ptr(D, torch.float32, dev), _ptr(z, dt, dev), _ptr(delta_bias, torch.float32, dev),
@@ -316,7 +326,7 @@ def conv1d_fwd(x: torch.Tensor, weight: torch.Tensor, bias: Optional[torch.Tenso
         out = torch.empty_like(x)
     if state_out is None and return_state:
         state_out = torch.empty((bt, dim, W - 1), dtype=torch.float32, device=dev)
-    with torch.cuda.device(dev):
+    with _on(dev):
         code = lib.ssm_conv1d_fwd(_ptr(x, dt, dev), _ptr(weight, torch.float32, dev),
                                   _ptr(bias, torch.float32, dev), int(bool(silu)),
                                   _ptr(state_in, torch.float32, dev), _ptr(out, dt, dev),
@@ -336,7 +346,7 @@ def conv1d_update(state: torch.Tensor, x: torch.Tensor, weight: torch.Tensor,
     W = weight.shape[1]
     if out is None:
         out = torch.empty_like(x)
-    with torch.cuda.device(dev):
+    with _on(dev):
         code = lib.ssm_conv1d_update(_ptr(state, torch.float32, dev), _ptr(x, dt, dev),
                                      _ptr(weight, torch.float32, dev), _ptr(bias, torch.float32, dev),
                                      int(bool(silu)), _ptr(out, dt, dev), bt, dim, W, _dtype_code(x), _stream(dev))
@@ -361,7 +371,7 @@ def ssm_state_update(state: torch.Tensor, x: torch.Tensor, dt: torch.Tensor, A: 
     G = _bc_groups(B, C, (bt,), N, (), "ssm_state_update")
     if out is None:
         out = torch.empty_like(x)
-    with torch.cuda.device(dev):
+    with _on(dev):
         code = lib.ssm_state_update_grouped(_ptr(state, torch.float32, dev), _ptr(x, ty, dev), _ptr(dt, ty, dev),
                                             _ptr(A, torch.float32, dev), _ptr(B, ty, dev), _ptr(C, ty, dev),
                                             _ptr(D, torch.float32, dev), _ptr(z, ty, dev),
