@@ -29,7 +29,7 @@ namespace ssm {
 
 namespace {
 
-constexpr int kConvTile = 64;      // steps per thread
+constexpr int kConvTile = 128;     // steps per thread (64: 0.479 ms on 1 x 131072 x 5120, 128: 0.442 ms)
 constexpr int kConvThreads = 128;
 
 template <typename T>
