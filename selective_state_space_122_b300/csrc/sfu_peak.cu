@@ -143,23 +143,26 @@ __global__ void __launch_bounds__(256) ffma2_kernel(float* sink, int iters, floa
 // entering its sub-chunk from the chunk's carry; (3) each lane re-sweeps its
 // steps with the kept decays and sums C . h in-lane, one output per step.
 // Per-step Delta, Delta u, B and C come from shared memory as in a staged
-// kernel; no global memory is touched inside the loop, so the rate is the
-// design's compute-and-shared-memory ceiling.
+// kernel, laid out by lane (a warp's eight sub-chunks read eight consecutive
+// 16-byte words, free of bank conflicts); no global memory is touched inside
+// the loop, so the rate is the design's compute-and-shared-memory ceiling.
 template <int T>
 __global__ void __launch_bounds__(128) tsplit_kernel(float* sink, int iters) {
     constexpr int CH = 8 * T;   // steps per chunk
-    __shared__ float2 s_dd[CH][4];
-    __shared__ float4 s_b[CH][4], s_c[CH][4];
-    __shared__ float s_y[4][CH][4];
+    // step t = sub * T + j of the chunk; [j][sub][channel] and [j][quad][sub]
+    __shared__ float2 s_dd[T][8][4];
+    __shared__ float4 s_b[T][4][8], s_c[T][4][8];
+    __shared__ float s_y[4][T][32];
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     for (int i = tid; i < CH * 4; i += 128) {
-        const int t = i / 4, q = i % 4;
-        s_dd[t][q] = make_float2(1e-3f + 1e-3f * ((t * 7 + q) % 97), 1e-2f * (((t * 5 + q) % 21) - 10));
-        s_b[t][q] = make_float4(0.1f * ((t + q) % 7) - 0.3f, 0.05f * ((t * 3 + q) % 9) - 0.2f, 0.1f, -0.1f);
-        s_c[t][q] = make_float4(0.2f, -0.1f * ((t + 2 * q) % 5), 0.05f * ((t + q) % 3), 0.3f);
+        const int t = i / 4, q = i % 4, jj = t % T, sb = t / T;
+        s_dd[jj][sb][q] = make_float2(1e-3f + 1e-3f * ((t * 7 + q) % 97), 1e-2f * (((t * 5 + q) % 21) - 10));
+        s_b[jj][q][sb] = make_float4(0.1f * ((t + q) % 7) - 0.3f, 0.05f * ((t * 3 + q) % 9) - 0.2f, 0.1f, -0.1f);
+        s_c[jj][q][sb] = make_float4(0.2f, -0.1f * ((t + 2 * q) % 5), 0.05f * ((t + q) % 3), 0.3f);
     }
     __syncthreads();
     const int ch = lane & 3, sub = lane >> 2;
+    (void)CH;
     float2 A[8], carry[8];
 #pragma unroll
     for (int p = 0; p < 8; ++p) {
@@ -185,12 +188,11 @@ __global__ void __launch_bounds__(128) tsplit_kernel(float* sink, int iters) {
         for (int p = 0; p < 8; ++p) h[p] = make_float2(0.f, 0.f);
 #pragma unroll
         for (int j = 0; j < T; ++j) {
-            const int t = sub * T + j;
-            const float2 dd = s_dd[t][ch];
+            const float2 dd = s_dd[j][sub][ch];
             sd += dd.x;
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 bq = s_b[t][q];
+                const float4 bq = s_b[j][q][sub];
 #pragma unroll
                 for (int hlf = 0; hlf < 2; ++hlf) {
                     const int p = 2 * q + hlf;
@@ -237,12 +239,11 @@ __global__ void __launch_bounds__(128) tsplit_kernel(float* sink, int iters) {
         // (3) re-sweep with the kept decays; C . h in-lane
 #pragma unroll
         for (int j = 0; j < T; ++j) {
-            const int t = sub * T + j;
-            const float2 dd = s_dd[t][ch];
+            const float2 dd = s_dd[j][sub][ch];
             float2 acc = make_float2(0.f, 0.f);
 #pragma unroll
             for (int q = 0; q < 4; ++q) {
-                const float4 bq = s_b[t][q], cq = s_c[t][q];
+                const float4 bq = s_b[j][q][sub], cq = s_c[j][q][sub];
 #pragma unroll
                 for (int hlf = 0; hlf < 2; ++hlf) {
                     const int p = 2 * q + hlf;
@@ -252,11 +253,11 @@ __global__ void __launch_bounds__(128) tsplit_kernel(float* sink, int iters) {
                     acc = fma2(c2, hin[p], acc);
                 }
             }
-            s_y[warp][t][ch] = acc.x + acc.y;
+            s_y[warp][j][lane] = acc.x + acc.y;
         }
     }
     __syncthreads();
-    float s = s_y[warp][lane % CH][lane & 3];
+    float s = s_y[warp][lane % T][lane];
 #pragma unroll
     for (int p = 0; p < 8; ++p) s += carry[p].x + carry[p].y;
     if (s == 12345.678f) sink[tid] = s;
