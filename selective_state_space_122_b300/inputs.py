@@ -17,7 +17,11 @@ Recipe (one numpy ``Generator(PCG64(seed))`` per workload):
 * delta_bias = softplus^-1(dt) with dt log-uniform in [1e-3, 0.1] per
   channel: the "targeted range" initialisation of the Delta projection bias
   named in the state-spaces/mamba docs ("Troubleshoot initialization issues");
-* decode state0 ~ N(0, 0.1) (standard deviation 0.1), fp32.
+* decode state0 ~ N(0, 0.1) (standard deviation 0.1), fp32;
+* activations too large to draw on the host (more than 2^31 elements) are
+  counter-based instead: uniform on [-1, 1) from an integer hash of the
+  element index (below), built on the device in slices and recomputed on the
+  host for the channels the oracle checks.
 
 Layouts follow the (batch, length, dim) convention of the Mamba block:
 u, delta, z, out are (batch, L, D) channel-contiguous; B and C are
@@ -204,3 +208,80 @@ def make_decode_inputs(shape: DecodeShape, seed: int) -> DecodeInputs:
     state0 = _normal(rng, (shape.batch, shape.dim, shape.dstate), sigma=0.1)
     return DecodeInputs(shape, state0, a_s4d_real(shape.dim, shape.dstate),
                         np.ones(shape.dim, np.float32), bias, rng)
+
+
+# ------------------------------------------------------------------
+# Counter-based draws, for activations too large to draw on the host.
+#
+# Value i of stream s under seed k is a pure function of (k, s, i): the
+# 64-bit element index i (row-major over (batch, L, D)) is hashed with
+# C. Wellons' "lowbias32" integer hash ("Prospecting for Hash Functions",
+# 2018), and the top 24 bits of the hash give a uniform value on [-1, 1)
+# with 2^-23 spacing, exact in float32.  The same code runs on numpy int64
+# arrays (the oracle's sampled channels) and on torch int64 tensors (the
+# full tensors, built on the device in slices), and gives bit-identical
+# values on both: every step is an integer operation whose intermediate
+# results stay below 2^49, then one exact conversion and scaling in float32.
+
+_M32 = 0xFFFFFFFF
+
+
+def _mul32(x, c: int):
+    """(x * c) mod 2^32 for integers 0 <= x < 2^32, with c split in 16-bit
+    halves so that no product exceeds 2^49 (no signed 64-bit overflow)."""
+    lo, hi = c & 0xFFFF, c >> 16
+    return (x * lo + (((x * hi) & 0xFFFF) << 16)) & _M32
+
+
+def _lowbias32(x):
+    x = x ^ (x >> 16)
+    x = _mul32(x, 0x7FEB352D)
+    x = x ^ (x >> 15)
+    x = _mul32(x, 0x846CA68B)
+    return x ^ (x >> 16)
+
+
+def counter_bits(index, stream: int, seed: int):
+    """32-bit hash of (seed, stream, index) for a non-negative int64 index
+    array or tensor (either library)."""
+    key = int(_lowbias32(((seed & _M32) * 0x9E3779B9 + stream) & _M32))
+    return _lowbias32((index & _M32) ^ _lowbias32((index >> 32) ^ key))
+
+
+def counter_uniform_np(index: np.ndarray, stream: int, seed: int) -> np.ndarray:
+    """Uniform [-1, 1) float32 values for an int64 index array."""
+    h = counter_bits(np.asarray(index, dtype=np.int64), stream, seed)
+    return (h >> 8).astype(np.float32) * np.float32(2.0 ** -23) - np.float32(1.0)
+
+
+def counter_uniform_torch(index, stream: int, seed: int):
+    """The same values for an int64 torch tensor (on any device)."""
+    import torch
+    h = counter_bits(index, stream, seed)
+    return (h >> 8).to(torch.float32) * (2.0 ** -23) - 1.0
+
+
+def counter_activation_channels(batch: int, seqlen: int, dim: int, sel, stream: int, seed: int,
+                                dtype: str) -> np.ndarray:
+    """Channels ``sel`` of the (batch, seqlen, dim) counter-drawn activation
+    (bf16 bits or float32), shaped (batch, seqlen, len(sel))."""
+    sel = np.asarray(sel, dtype=np.int64)
+    rows = np.arange(batch * seqlen, dtype=np.int64).reshape(batch, seqlen, 1)
+    v = counter_uniform_np(rows * dim + sel.reshape(1, 1, -1), stream, seed)
+    return round_to_bf16_bits(v) if dtype == BF16 else v
+
+
+def counter_activation_device(batch: int, seqlen: int, dim: int, stream: int, seed: int, dtype: str,
+                              device, rows_per_slice: int = 8192):
+    """The whole (batch, seqlen, dim) counter-drawn activation as a torch
+    tensor on ``device`` (bfloat16 or float32), built slice by slice."""
+    import torch
+    tdt = torch.bfloat16 if dtype == BF16 else torch.float32
+    out = torch.empty((batch, seqlen, dim), dtype=tdt, device=device)
+    col = torch.arange(dim, dtype=torch.int64, device=device).reshape(1, -1)
+    for b in range(batch):
+        for t0 in range(0, seqlen, rows_per_slice):
+            t1 = min(seqlen, t0 + rows_per_slice)
+            rows = torch.arange(b * seqlen + t0, b * seqlen + t1, dtype=torch.int64, device=device).reshape(-1, 1)
+            out[b, t0:t1] = counter_uniform_torch(rows * dim + col, stream, seed).to(tdt)
+    return out

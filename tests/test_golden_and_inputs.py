@@ -70,3 +70,51 @@ def test_grouped_draws_keep_the_one_group_stream():
     d = inputs.make_decode_inputs(inputs.DecodeShape("g", 3, 8, 4, inputs.F32), 9)
     x, dt, z, B, C = d.token(ngroups=2)
     assert B.shape == (3, 2, 4) and C.shape == (3, 2, 4) and x.shape == (3, 8)
+
+
+def _lowbias32_int(x: int) -> int:
+    # the hash written out on Python integers, arbitrary precision, masked
+    x ^= x >> 16
+    x = (x * 0x7FEB352D) & 0xFFFFFFFF
+    x ^= x >> 15
+    x = (x * 0x846CA68B) & 0xFFFFFFFF
+    return x ^ (x >> 16)
+
+
+def test_counter_draws_match_the_hash_on_both_libraries():
+    """The counter-based draws (activations larger than the host can draw)
+    equal the lowbias32 hash written out on Python integers, for indices
+    below and beyond 2^31 and 2^32, bit for bit on numpy and on torch, and
+    torch's bf16 conversion of them equals the host rounding."""
+    idx = np.array([0, 1, 2, 2**31 - 1, 2**31, 2**32 - 1, 2**32, 2**33 + 5, 3 * 131072 * 8192 - 1,
+                    12345678901], dtype=np.int64)
+    for seed, stream in [(7, 1), (0, 0), (123456789, 3)]:
+        key = _lowbias32_int(((seed & 0xFFFFFFFF) * 0x9E3779B9 + stream) & 0xFFFFFFFF)
+        ref = [_lowbias32_int((int(i) & 0xFFFFFFFF) ^ _lowbias32_int((int(i) >> 32) ^ key)) for i in idx]
+        assert [int(v) for v in inputs.counter_bits(idx, stream, seed)] == ref
+        assert [int(v) for v in inputs.counter_bits(torch.from_numpy(idx), stream, seed)] == ref
+        a = inputs.counter_uniform_np(idx, stream, seed)
+        b = inputs.counter_uniform_torch(torch.from_numpy(idx), stream, seed).numpy()
+        assert np.array_equal(a.view(np.uint32), b.view(np.uint32))
+        assert np.array_equal(a, np.array([(h >> 8) * 2.0 ** -23 - 1.0 for h in ref], dtype=np.float32))
+        tb = torch.from_numpy(a).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+        assert np.array_equal(inputs.round_to_bf16_bits(a), tb)
+
+
+def test_counter_draws_are_uniform_and_distinct_per_stream():
+    x = inputs.counter_uniform_np(np.arange(1 << 20, dtype=np.int64), 1, 7)
+    assert -1.0 <= float(x.min()) and float(x.max()) < 1.0
+    assert abs(float(x.mean())) < 5e-3 and abs(float(x.std()) - 1 / np.sqrt(3.0)) < 5e-3
+    y = inputs.counter_uniform_np(np.arange(1 << 20, dtype=np.int64), 2, 7)
+    assert abs(float(np.corrcoef(x, y)[0, 1])) < 5e-3
+
+
+def test_counter_activation_device_equals_host_channels():
+    """The slice-by-slice tensor build (run here on the CPU) holds exactly the
+    values the host computes for sampled channels, slices of odd length."""
+    for dt in (inputs.BF16, inputs.F32):
+        d = inputs.counter_activation_device(2, 100, 40, 2, 9, dt, "cpu", rows_per_slice=33)
+        sel = [0, 5, 39]
+        h = inputs.counter_activation_channels(2, 100, 40, sel, 2, 9, dt)
+        got = d[:, :, sel].view(torch.int16).numpy().view(np.uint16) if dt == inputs.BF16 else d[:, :, sel].numpy()
+        assert np.array_equal(got, h)
