@@ -35,7 +35,8 @@
 // workspace with a bounded release/acquire flag wait; the launch is
 // cooperative, so every CTA a segment may wait on is resident.  A loader
 // warp issues the TMA loads of the u, delta_raw and z tiles (64-byte rows,
-// hardware-swizzled so that column reads are free of bank conflicts) and of
+// hardware-swizzled: with the consumers' row order, column reads are free of
+// bank conflicts) and of
 // the chunk's staged X operand, an MMA warp the one-hot product into one of
 // two TMEM buffers, a store warp the TMA stores of the output tiles; the
 // compute warps of the two kernels are described with each.
@@ -239,7 +240,7 @@ struct Tm2Cfg {
     static constexpr int OUTT = tm_al(TILE, 1024);
     static constexpr int W_BASE = OUT + OB * OUTT;
     static constexpr int DPS = K + 4;           // float2 stride of a channel's dp row (conflict-free 16-byte stores)
-    static constexpr int RS2 = 33;              // float2 stride of a reduction row
+    static constexpr int RS2 = 49;              // float2 stride of a reduction row (= 1 mod 16)
     static constexpr int W_RED = tm_al(CW * DPS * 8, 128);
     static constexpr int W_BYTES = W_RED + tm_al((K / 2) * RS2 * 8, 128);
     static constexpr int BAR = W_BASE + WARPS * W_BYTES;
@@ -397,6 +398,13 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
         float2* dp = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES);
         float2* red = reinterpret_cast<float2*>(smem + CF::W_BASE + w * CF::W_BYTES + CF::W_RED);
         const uint32_t tlane = tmem + ((uint32_t)(32 * (w & 3)) << 16);
+        // a lane's slot in a reduction row: lanes 16-31 four slots further on,
+        // so that the channel sums read back (channels c and c + 2 of a half
+        // warp) fall in different banks
+        const int rpos = lane + ((lane >> 4) << 2);
+        // per-(t, d) items: lanes 16-31 take their odd step first, so that the
+        // eight rows of every tile access differ mod 8 (distinct banks)
+        const bool sw = lane >= 16;
         int ipv[NI];   // step pair of each item
 #pragma unroll
         for (int i = 0; i < NI; ++i) ipv[i] = (lane + 32 * i) / CW;
@@ -451,8 +459,9 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
 #pragma unroll
                     for (int i = 0; i < NI; ++i) {
                         const int ta = 2 * ipv[i];
-                        const uint32_t oa = swz<CF::ROWB>(ta, w * CW + ich);
-                        const uint32_t ob = swz<CF::ROWB>(ta + 1, w * CW + ich);
+                        const int tf = ta + (sw ? 1 : 0), ts = ta + (sw ? 0 : 1);
+                        const uint32_t oa = swz<CF::ROWB>(tf, w * CW + ich);
+                        const uint32_t ob = swz<CF::ROWB>(ts, w * CW + ich);
                         const float2 uv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + oa)),
                                                       ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_U + ob)));
                         const float2 xr = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_D + oa)),
@@ -460,10 +469,10 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                         float2 dl = add2(xr, bias2);
                         if constexpr (kSoftplus) dl = softplus2_path<true>(dl);
                         if (t0 + K > L)
-                            dl = mul2(dl, make_float2(t0 + ta < L ? 1.f : 0.f, t0 + ta + 1 < L ? 1.f : 0.f));
+                            dl = mul2(dl, make_float2(t0 + tf < L ? 1.f : 0.f, t0 + ts < L ? 1.f : 0.f));
                         const float2 du = mul2(dl, uv);
-                        dpv[2 * i] = make_float2(dl.x, du.x);
-                        dpv[2 * i + 1] = make_float2(dl.y, du.y);
+                        dpv[2 * i] = sw ? make_float2(dl.y, du.y) : make_float2(dl.x, du.x);
+                        dpv[2 * i + 1] = sw ? make_float2(dl.x, du.x) : make_float2(dl.y, du.y);
                         uk[i] = uv;
                         if constexpr (kGate) {
                             const float2 zv = make_float2(ld_elem(reinterpret_cast<const T*>(sb + CF::SLOT_Z + oa)),
@@ -521,16 +530,18 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                     }
                 };
                 auto finish_item = [&](int q) {
-                    const float2* row = red + ipv[q] * RS2 + ich * R;
+                    const float2* row = red + ipv[q] * RS2 + ich * R + (ich >= 2 ? 4 : 0);
                     float2 pr[R];
 #pragma unroll
                     for (int gg = 0; gg < R; ++gg) pr[gg] = row[gg];
                     const float2 a0 = add2(pr[0], pr[1]), a1 = add2(pr[2], pr[3]);
                     const float2 a2 = add2(pr[4], pr[5]), a3 = add2(pr[6], pr[7]);
-                    const float2 yv = add2(add2(a0, a1), add2(a2, a3));
+                    const float2 ys = add2(add2(a0, a1), add2(a2, a3));
+                    const float2 yv = sw ? make_float2(ys.y, ys.x) : ys;
                     const float2 y = mul2(fma2(dskip2, uk[q], yv), gate[q]);
-                    st_pair<T>(reinterpret_cast<T*>(so + swz<CF::ROWB>(2 * ipv[q], w * CW + ich)),
-                               reinterpret_cast<T*>(so + swz<CF::ROWB>(2 * ipv[q] + 1, w * CW + ich)), y);
+                    const int ta = 2 * ipv[q];
+                    st_pair<T>(reinterpret_cast<T*>(so + swz<CF::ROWB>(ta + (sw ? 1 : 0), w * CW + ich)),
+                               reinterpret_cast<T*>(so + swz<CF::ROWB>(ta + (sw ? 0 : 1), w * CW + ich)), y);
                 };
                 auto exp_step = [&](int t) {
                     const float2 e = mul2(splat2(qv[t].x), A2);
@@ -554,7 +565,7 @@ scan_tmem2_kernel(const __grid_constant__ CUtensorMap tm_u, const __grid_constan
                     h = fma2(dA[t], h, dB[t]);
                     const float2 cy = mul2(make_float2(bc(t, 2), bc(t, 3)), h);
                     const float sy = cy.x + cy.y;
-                    if (t & 1) red[(t / 2) * RS2 + lane] = make_float2(s_prev, sy);
+                    if (t & 1) red[(t / 2) * RS2 + rpos] = make_float2(s_prev, sy);
                     s_prev = sy;
                     if ((t % 16) == 15 && t / 16 < NI) {
                         __syncwarp();
