@@ -62,10 +62,11 @@ def scan_elements(s=SCAN):
 
 
 # dram__bytes_read.sum + dram__bytes_write.sum of scan_tmem2_kernel as built
-# (polynomial softplus), from one ncu capture of the long-sequence workload cut
-# to L = 16384 (profiles/scan_tmem2_kernel_1x5120x16384.md), scaled by
-# 131072 / 16384: the traffic grows in proportion to L.
-SCAN_TRAFFIC_L16384 = 654.1e6
+# (conflict-free shared-memory layouts), from one ncu capture of the
+# long-sequence workload cut to L = 16384
+# (profiles/scan_tmem2_kernel_1x5120x16384.md), scaled by 131072 / 16384: the
+# traffic grows in proportion to L.
+SCAN_TRAFFIC_L16384 = 654.7e6
 SCAN_TRAFFIC_BYTES = SCAN_TRAFFIC_L16384 * 8
 
 
@@ -399,16 +400,18 @@ def time_side_kernels(w, device, iters=5):
       x 5120, width 4, bf16);
     * the decode step alone, each launch after a read of 512 MB that leaves
       the L2 clean (in the step it runs after the scan, whose output lines are
-      still dirty in L2 and are written back during the decode).
+      still dirty in L2 and are written back during the decode); the mean of
+      40 launches, since one ~30 us launch is only a few ticks of the event
+      timer (2.05 us on this hardware).
     Inputs: seeded, on the device."""
     import torch
     from selective_state_space_122_b300 import conv1d_fwd, ssm_scan_bwd, ssm_state_update
     res = {}
     ev = lambda: torch.cuda.Event(enable_timing=True)
 
-    def timed(fn, before=None):
+    def timed(fn, before=None, n=iters, reduce=statistics.median):
         ts = []
-        for i in range(iters + 2):
+        for i in range(n + 2):
             if before is not None:
                 before()
             e0, e1 = ev(), ev()
@@ -418,7 +421,7 @@ def time_side_kernels(w, device, iters=5):
             torch.cuda.synchronize()
             if i >= 2:
                 ts.append(e0.elapsed_time(e1))
-        return statistics.median(ts)
+        return reduce(ts)
 
     g = torch.Generator(device=device)
     g.manual_seed(5)
@@ -441,7 +444,7 @@ def time_side_kernels(w, device, iters=5):
     res["decode_isolated_us"] = 1e3 * timed(
         lambda: ssm_state_update(d["state"], d["x"], d["dt"], d["A"], d["B"], d["C"], d["D"], d["z"],
                                  d["dt_bias"], True, out=w["dec_out"]),
-        before=lambda: flush.view(torch.int64).sum())
+        before=lambda: flush.view(torch.int64).sum(), n=40, reduce=statistics.mean)
     torch.cuda.synchronize()
     return res
 
