@@ -187,6 +187,14 @@ __device__ __forceinline__ void bulk_store(void* dst, uint32_t src, uint32_t byt
                  : "memory");
 }
 
+// Four consecutive elements (8 or 16 bytes, aligned) of B or C as floats.
+__device__ __forceinline__ float4 ld_quad(const float* q) { return *reinterpret_cast<const float4*>(q); }
+__device__ __forceinline__ float4 ld_quad(const __nv_bfloat16* q) {
+    const uint2 v = *reinterpret_cast<const uint2*>(q);
+    return make_float4(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u), __uint_as_float(v.y << 16),
+                       __uint_as_float(v.y & 0xFFFF0000u));
+}
+
 template <typename T, int N, bool kFast>
 __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(UpdateArgs p, int rsplit, int ntile) {
     using CF = BulkCfg<T, N>;
@@ -314,10 +322,8 @@ __global__ void __launch_bounds__(kBulkThreads) state_update_bulk_kernel(UpdateA
             float dl = to_f32(tdt[c]) + bias[j];
             if (p.softplus) dl = softplus_f<kFast>(dl);
             const float gate = p.z ? silu_f<kFast>(to_f32(tz[c])) : 1.f;
-            const T* bq = tb + grp[j] * N + 4 * g;
-            const T* cq = tc + grp[j] * N + 4 * g;
-            const float4 bv = make_float4(to_f32(bq[0]), to_f32(bq[1]), to_f32(bq[2]), to_f32(bq[3]));
-            const float4 cv = make_float4(to_f32(cq[0]), to_f32(cq[1]), to_f32(cq[2]), to_f32(cq[3]));
+            const float4 bv = ld_quad(tb + grp[j] * N + 4 * g);
+            const float4 cv = ld_quad(tc + grp[j] * N + 4 * g);
             const float4 h = sst[q];
             const float2 dl2 = splat2(dl), dx2 = splat2(dl * xv);
             const float2 e0 = mul2(dl2, make_float2(a4[j].x, a4[j].y)), e1 = mul2(dl2, make_float2(a4[j].z, a4[j].w));
